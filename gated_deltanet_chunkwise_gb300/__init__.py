@@ -1,0 +1,23 @@
+"""Gated DeltaNet chunkwise forward pass and decode step for GB300 (sm_103a).
+
+The compute lives in a native library (``_lib/libgdn_gb300.so``) built from
+``csrc/`` by ``build.build()``; ``abi`` is a thin ctypes binding with the same
+entry-point names as ``include/gdn.h``. There is no CPU fallback: touching an
+entry point without the built library raises.
+
+``inputs`` (seeded synthetic data) is importable without the native library.
+"""
+from __future__ import annotations
+
+_ABI_NAMES = (
+    "gdn_chunk_fwd", "gdn_chunk_fwd_f32", "gdn_chunk_fwd_ex",
+    "gdn_recurrent_step", "gdn_status_string", "GdnError", "library_path",
+    "library", "kernel_counters",
+)
+
+
+def __getattr__(name):
+    if name in _ABI_NAMES:
+        from . import abi
+        return getattr(abi, name)
+    raise AttributeError(name)
