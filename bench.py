@@ -1,0 +1,498 @@
+#!/usr/bin/env python3
+"""Benchmark of the Gated DeltaNet chunkwise forward pass on GB300.
+
+Default workload (the headline): gdn_chunk_fwd on B=4, H=16, T=2048,
+dk=dv=128, C=64, bf16 q/k/v, fp32 gates and state, zero initial state.
+One step = one call of the whole forward path (every kernel the library
+launches for it). Prints ONE JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload w1|w2|w3|w4]
+
+Timing: inputs resident in HBM, the L2 (129 MB) is flushed by a 256 MiB
+memset before every timed step, each step is bracketed by CUDA events on the
+launching stream; ms_per_step is the mean. Under torchrun every rank runs the
+same workload on its own GPU (independent problems, weak scaling, no
+collective on the data path) and the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import torch
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "GDN chunk-fwd tokens/s + % of GB300 tensor/HBM roofline, 1 GPU"
+FLUSH_BYTES = 256 << 20
+
+# Algorithmic work per token-head of the chunked forward pass:
+#   flops  = 2 C (3 dk + 2 dv) + 6 dk dv   (K K^T, Q K^T, T.K, T.V, P.U;
+#            W S^T, U^T Kbar, Q S^T)
+#   bytes  = 2 (2 dk + dv) in + 2 dv out + 8 (g, beta)   [bf16]
+# plus 4 dk dv per (sequence, head) for each of h0 / hT when present.
+
+
+def chunk_flops(tok_heads, dk, dv, C=64):
+    return tok_heads * (2 * C * (3 * dk + 2 * dv) + 6 * dk * dv)
+
+
+def chunk_bytes(tok_heads, dk, dv, n_states, elem=2):
+    return tok_heads * (elem * (2 * dk + dv) + elem * dv + 8) + \
+        n_states * 4 * dk * dv
+
+
+WORKLOADS = {
+    "w1": dict(kind="chunk", B=4, H=16, T=2048, dk=128, dv=128, h0=False,
+               desc="gdn_chunk_fwd B=4 H=16 T=2048 dk=dv=128 C=64 bf16, h0=0"),
+    "w2": dict(kind="chunk", B=1, H=16, T=65536, dk=128, dv=128, h0=False,
+               desc="gdn_chunk_fwd B=1 H=16 T=65536 dk=dv=128 C=64 bf16 "
+                    "(sequence-parallel split)"),
+    "w3": dict(kind="chunk", B=32, H=16, T=0, dk=128, dv=128, h0=True,
+               lengths=(256, 8192),
+               desc="gdn_chunk_fwd packed 32 seqs len U{256..8192} H=16 "
+                    "dk=dv=128 C=64 bf16, h0~0.1N(0,1), hT returned"),
+    "w4": dict(kind="decode", N=512, H=32, dk=128, dv=128,
+               desc="gdn_recurrent_step N=512 H=32 dk=dv=128 bf16 token, "
+                    "fp32 state in place"),
+}
+
+# DRAM traffic per launch of the dominant kernel from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and the
+# hash of the kernel source it was taken on; a changed kernel reports null.
+MEASURED_TRAFFIC = {}
+
+
+def _kernel_source_hash(kind):
+    csrc = ROOT / "gated_deltanet_chunkwise_gb300" / "csrc"
+    files = ["decode.cu"] if kind == "decode" else sorted(
+        p.name for p in csrc.glob("chunk_*.cu"))
+    h = hashlib.sha256()
+    for f in files:
+        h.update((csrc / f).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def _peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = Path(os.environ.get("TMPDIR", "/tmp")) / \
+            f"gdn_clocks_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev),
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in self.path.read_text().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        try:
+            self.path.unlink()
+        except OSError:
+            pass
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows
+                          for i, x in enumerate(r) if x.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": reasons}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _init_dist(ws, use_cuda):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if use_cuda else "gloo")
+        return dist
+    return None
+
+
+def reduce_max(dist, value, device):
+    """Max of a float over ranks (identity without a process group)."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(dist, value, device):
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def _barrier(dist, device):
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+
+
+# ---------------------------------------------------------------------------
+def _make_inputs(w, seed=0):
+    from gated_deltanet_chunkwise_gb300 import inputs
+    if w["kind"] == "decode":
+        return inputs.decode_inputs(w["N"], w["H"], w["dk"], w["dv"],
+                                    dtype="bf16", seed=seed)
+    return inputs.chunk_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
+                               dtype="bf16", seed=seed, h0=w["h0"],
+                               length_range=w.get("lengths"))
+
+
+def _units(w, d):
+    """(tokens, token-heads, sequences) of one step."""
+    if w["kind"] == "decode":
+        return w["N"], w["N"] * w["H"], w["N"]
+    tokens = d["q"].shape[0] * d["q"].shape[1]
+    nseq = w["B"]
+    return tokens, tokens * w["H"], nseq
+
+
+def run_ours(args, w, device, dist, rank, ws):
+    import gated_deltanet_chunkwise_gb300 as gdn
+    from gated_deltanet_chunkwise_gb300 import build
+    build.build()
+    d_host = _make_inputs(w, seed=rank)
+    tokens, tok_heads, nseq = _units(w, d_host)
+    dk, dv, H = w["dk"], w["dv"], w["H"]
+    d = {k: (None if v is None else v.to(device)) for k, v in d_host.items()}
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    if w["kind"] == "decode":
+        out = torch.empty_like(d["v"])
+        state0 = d["state"].clone()
+
+        def step():
+            gdn.gdn_recurrent_step(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                   d["state"], out=out)
+        n_states = 0
+    else:
+        out = torch.empty_like(d["v"])
+        N = nseq
+        hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=device)
+        want_hT = w["h0"]
+
+        def step():
+            gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                              d["h0"], d["cu_seqlens"], out=out,
+                              hT=hT if want_hT else None,
+                              output_final_state=want_hT)
+        n_states = N * H * ((1 if w["h0"] else 0) + (1 if want_hT else 0))
+
+    # warm-up (also sizes the default step count: ~2 s of timed work)
+    for _ in range(max(args.warmup, 1)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(3):
+        flush.zero_()
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    probe_ms = e0.elapsed_time(e1) / 3
+    steps = args.steps if args.steps else int(min(20000, max(20, math.ceil(2000.0 / max(probe_ms, 1e-3)))))
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    sampler = ClockSampler(device.index or 0)
+    sampler.start()
+    time.sleep(0.2)
+    _barrier(dist, device)
+    launches0 = gdn.kernel_counters()
+    t_wall = time.perf_counter()
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    _barrier(dist, device)
+    wall = time.perf_counter() - t_wall
+    launches = gdn.kernel_counters() - launches0
+    clocks = sampler.stop()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = sum(per) / len(per)
+    ms = reduce_max(dist, ms_local, device)
+    units_all = reduce_sum(dist, tokens if w["kind"] != "decode" else tokens, device)
+
+    # ---- end to end through the public API with host buffers ----
+    pinned = {k: (None if v is None else v.pin_memory())
+              for k, v in d_host.items()}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values()
+              if v is not None)
+    d2h = out_host.numel() * out_host.element_size()
+    hT_host = None
+    if w["kind"] == "chunk" and w["h0"]:
+        hT_host = torch.empty(hT.shape, dtype=torch.float32).pin_memory()
+        d2h += hT_host.numel() * 4
+    if w["kind"] == "decode":
+        # the updated state is the step's result as well
+        d2h += pinned["state"].numel() * 4
+    e2e_steps = max(5, min(steps, 50))
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps + 2):
+        flush.zero_()
+        if i >= 2:
+            es[i - 2].record(stream)
+        for k_, v_ in pinned.items():
+            if v_ is not None:
+                d[k_].copy_(v_, non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+        if hT_host is not None:
+            hT_host.copy_(hT, non_blocking=True)
+        if w["kind"] == "decode":
+            pinned["state"].copy_(d["state"], non_blocking=True)
+        if i >= 2:
+            ee[i - 2].record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = reduce_max(dist, sum(s.elapsed_time(e) for s, e in zip(es, ee)) / e2e_steps, device)
+
+    hbm_gbs, bf16_tflops, peak_kind = _peaks()
+    if w["kind"] == "decode":
+        alg_bytes = tok_heads * (8 * dk * dv + 2 * (2 * dk + 2 * dv) + 8)
+        achieved = alg_bytes / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1),
+                "peak": hbm_gbs, "unit": "GB/s",
+                "frac": round(achieved / hbm_gbs, 4),
+                "peak_source": f"{peak_kind} hbm_gbs",
+                "algorithmic_bytes_per_launch": alg_bytes}
+        value = units_all / (ms * 1e-3) * (tok_heads / tokens)  # heads/s
+        unit = "token-heads/s"
+        e2e_val = units_all / (e2e_ms * 1e-3) * (tok_heads / tokens)
+    else:
+        flops = chunk_flops(tok_heads, dk, dv)
+        nbytes = chunk_bytes(tok_heads, dk, dv, n_states)
+        achieved = flops / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2),
+                "peak": bf16_tflops, "unit": "TFLOP/s",
+                "frac": round(achieved / bf16_tflops, 4),
+                "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                "algorithmic_flops_per_launch": flops,
+                "hbm_achieved_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                "hbm_frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm_gbs, 4),
+                "algorithmic_bytes_per_launch": nbytes}
+        value = units_all / (ms * 1e-3)
+        unit = "tokens/s"
+        e2e_val = units_all / (e2e_ms * 1e-3)
+    key = f"{args.workload}:{_kernel_source_hash(w['kind'])}"
+    roof["traffic"] = MEASURED_TRAFFIC.get(key)
+    roof["dominant_kernel_launches_per_step"] = launches / steps
+    if w["kind"] == "decode":
+        d["state"].copy_(state0)
+
+    line = {
+        "metric": METRIC if w["kind"] == "chunk" else
+        "GDN decode-step token-heads/s + % of GB300 HBM roofline, 1 GPU",
+        "value": value, "unit": unit, "n_gpus": ws, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), "
+                "g=-softplus(N(0,1)), beta=sigmoid(N(0,1)))",
+        "config": {"workload": w["desc"],
+                   "l2": "flushed by a 256 MiB memset before every timed step",
+                   "timing": "CUDA events per step on the launching stream"},
+        "roofline": roof,
+        "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    return line, d_host
+
+
+def cpu_baseline(w, d_host, budget_s=20.0):
+    """The oracle as it stands, on the host cores, on a bounded sample."""
+    import oracle
+    cores = oracle.max_threads()
+    if w["kind"] == "decode":
+        n = w["N"]
+        t0 = time.perf_counter()
+        oracle.recurrent_step(d_host["q"][:n], d_host["k"][:n],
+                              d_host["v"][:n], d_host["g"][:n],
+                              d_host["beta"][:n], d_host["state"][:n])
+        dt = time.perf_counter() - t0
+        return {"value": n * w["H"] / dt, "unit": "token-heads/s",
+                "cores": cores, "kind": "oracle",
+                "sample": f"full workload ({n} sequences x {w['H']} heads, one token)",
+                "seconds": round(dt, 3)}
+    # dense: whole sequences (all heads); packed: the first sequences
+    if d_host["cu_seqlens"] is None:
+        nb = d_host["q"].shape[0]
+        take = nb
+        sl = lambda x: x[:take]
+        t0 = time.perf_counter()
+        oracle.forward(sl(d_host["q"]), sl(d_host["k"]), sl(d_host["v"]),
+                       sl(d_host["g"]), sl(d_host["beta"]),
+                       None if d_host["h0"] is None else d_host["h0"][:take])
+        dt = time.perf_counter() - t0
+        tokens = take * d_host["q"].shape[1]
+        sample = f"{take} of {nb} sequences x all {w['H']} heads"
+    else:
+        cu = d_host["cu_seqlens"].numpy()
+        take = min(len(cu) - 1, 4)
+        end = int(cu[take])
+        t0 = time.perf_counter()
+        oracle.forward(d_host["q"][:, :end], d_host["k"][:, :end],
+                       d_host["v"][:, :end], d_host["g"][:, :end],
+                       d_host["beta"][:, :end], d_host["h0"][:take],
+                       cu_seqlens=cu[:take + 1])
+        dt = time.perf_counter() - t0
+        tokens = end
+        sample = f"first {take} of {len(cu) - 1} packed sequences ({end} tokens) x all {w['H']} heads"
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": cores,
+            "kind": "oracle", "sample": sample, "seconds": round(dt, 3)}
+
+
+def run_reference(args, w):
+    """The oracle arm: each step is the fp64 CPU oracle on a bounded sample
+    of the same workload (one sequence of the dense batch, all heads)."""
+    import oracle
+    from gated_deltanet_chunkwise_gb300 import inputs
+    if w["kind"] == "decode":
+        d = inputs.decode_inputs(64, w["H"], w["dk"], w["dv"], seed=0)
+
+        def step():
+            oracle.recurrent_step(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                  d["state"])
+        units, unit, sample = 64 * w["H"], "token-heads/s", \
+            f"64 of {w['N']} sequences x {w['H']} heads, one token"
+    else:
+        T = w["T"] if w["T"] else 4096
+        T = min(T, 4096)
+        d = inputs.chunk_inputs(1, w["H"], T, w["dk"], w["dv"], dtype="bf16",
+                                seed=0, h0=w["h0"])
+
+        def step():
+            oracle.forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+        units, unit, sample = T, "tokens/s", \
+            f"one sequence of {T} tokens x all {w['H']} heads"
+    for _ in range(args.warmup):
+        step()
+    times = []
+    for _ in range(args.steps or 5):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    value = units / sec
+    cores = oracle.max_threads()
+    return {
+        "impl": "reference", "metric": METRIC if w["kind"] == "chunk" else
+        "GDN decode-step token-heads/s + % of GB300 HBM roofline, 1 GPU",
+        "value": value, "unit": unit, "n_gpus": 1, "steps": len(times),
+        "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded, same recipe)",
+        "config": {"workload": w["desc"]},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps (0 = enough for ~2 s of timed work)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="w1")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+    w = WORKLOADS[args.workload]
+    ws, rank, local = _dist()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, w)), flush=True)
+        return 0
+
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device; the library has no CPU "
+                          "fallback"}), flush=True)
+        return 2
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = _init_dist(ws, True)
+    line, d_host = run_ours(args, w, device, dist, rank, ws)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, d_host)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,211 @@
+"""Thin ctypes binding of ``include/gdn.h`` (argument marshalling only).
+
+Each function takes CUDA torch tensors, checks dtypes/shapes/contiguity,
+passes raw device pointers and the current torch stream to the native entry
+point of the same name, and raises ``GdnError`` on a negative status. Output
+tensors are allocated with torch when not supplied (torch is the memory and
+stream provider; every step of the computation runs in the library's
+kernels). There is no CPU fallback: without the built library, or with a
+non-CUDA tensor, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+from . import build as _build
+
+GDN_OK = 0
+GDN_GATE_BEFORE_PREDICT = 0
+GDN_GATE_AFTER_PREDICT = 1
+GDN_DTYPE_BF16 = 0
+GDN_DTYPE_F32 = 1
+GDN_PATH_AUTO = 0
+GDN_PATH_SIMT = 1
+GDN_PATH_TCGEN05 = 2
+
+_lib = None
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {gdn_status_string(status)} ({status})")
+
+
+def library_path() -> Path:
+    return _build.LIB
+
+
+def library():
+    """The loaded ``libgdn_gb300.so`` (ctypes.CDLL) with typed entry points."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not path.exists():
+        raise RuntimeError(
+            f"native library {path} is missing: run "
+            "`python -c 'import __graft_entry__ as g; g.build()'` first "
+            "(there is no fallback implementation)")
+    lib = ctypes.CDLL(str(path))
+    vp, fp, ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+    i = ctypes.c_int
+    chunk_args = [vp, vp, vp, fp, fp, fp, vp, fp, ip, i, i, i, i, i, i, vp]
+    lib.gdn_chunk_fwd.argtypes = chunk_args
+    lib.gdn_chunk_fwd.restype = i
+    lib.gdn_chunk_fwd_f32.argtypes = chunk_args
+    lib.gdn_chunk_fwd_f32.restype = i
+    lib.gdn_chunk_fwd_ex.argtypes = chunk_args[:-1] + [i, i, i, i, vp]
+    lib.gdn_chunk_fwd_ex.restype = i
+    lib.gdn_recurrent_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, i, i, i,
+                                       vp]
+    lib.gdn_recurrent_step.restype = i
+    lib.gdn_device_status.argtypes = [vp]
+    lib.gdn_device_status.restype = i
+    lib.gdn_status_string.argtypes = [i]
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_version.restype = i
+    lib.gdn_kernel_launches.restype = ctypes.c_ulonglong
+    _lib = lib
+    return lib
+
+
+def gdn_status_string(status: int) -> str:
+    return library().gdn_status_string(int(status)).decode()
+
+
+def kernel_counters() -> int:
+    """Kernels enqueued by the library so far in this process."""
+    return int(library().gdn_kernel_launches())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, name, dtype, device):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU fallback)")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _chunk_call(fn_name, q, k, v, g, beta, h0, cu_seqlens, out, hT,
+                output_final_state, C, stream, io_dtype, extra=()):
+    dev = q.device
+    _need(q, "q", io_dtype, None)
+    _need(k, "k", io_dtype, dev)
+    _need(v, "v", io_dtype, dev)
+    _need(g, "g", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    Bt, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (Bt, T, H):
+        raise ValueError("q/k/v shapes disagree")
+    if g.shape != (Bt, T, H) or beta.shape != (Bt, T, H):
+        raise ValueError("g/beta must be [B, T, H]")
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        if Bt != 1:
+            raise ValueError("packed sequences are passed as [1, T, H, ...]")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = Bt
+    if h0 is not None:
+        _need(h0, "h0", torch.float32, dev)
+        if h0.shape != (N, H, dk, dv):
+            raise ValueError(f"h0 must be [{N}, {H}, {dk}, {dv}]")
+    if out is None:
+        out = torch.empty_like(v)
+    else:
+        _need(out, "out", io_dtype, dev)
+    if hT is None and output_final_state:
+        hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    elif hT is not None:
+        _need(hT, "hT", torch.float32, dev)
+    with torch.cuda.device(dev):
+        rc = getattr(library(), fn_name)(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+            _ptr(out), _ptr(hT), _ptr(cu_seqlens), N, H, T, dk, dv, C,
+            *extra, _stream(stream))
+    if rc != GDN_OK:
+        raise GdnError(rc, fn_name)
+    return out, hT
+
+
+def gdn_chunk_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, out=None,
+                  hT=None, output_final_state=True, C=64, stream=None):
+    """bf16 chunkwise forward; returns (out bf16 like v, hT fp32 or None)."""
+    return _chunk_call("gdn_chunk_fwd", q, k, v, g, beta, h0, cu_seqlens, out,
+                       hT, output_final_state, C, stream, torch.bfloat16)
+
+
+def gdn_chunk_fwd_f32(q, k, v, g, beta, h0=None, cu_seqlens=None, *, out=None,
+                      hT=None, output_final_state=True, C=64, stream=None):
+    """fp32 chunkwise forward; returns (out fp32, hT fp32 or None)."""
+    return _chunk_call("gdn_chunk_fwd_f32", q, k, v, g, beta, h0, cu_seqlens,
+                       out, hT, output_final_state, C, stream, torch.float32)
+
+
+def gdn_chunk_fwd_ex(q, k, v, g, beta, h0=None, cu_seqlens=None, *, out=None,
+                     hT=None, output_final_state=True, C=64,
+                     variant=GDN_GATE_BEFORE_PREDICT, path=GDN_PATH_AUTO,
+                     sp_parts=0, stream=None):
+    """Chunkwise forward with explicit gate placement, kernel family and
+    sequence-parallel split; q/k/v dtype (bf16 or fp32) selects the dtype."""
+    dtype = {torch.bfloat16: GDN_DTYPE_BF16, torch.float32: GDN_DTYPE_F32}.get(
+        q.dtype)
+    if dtype is None:
+        raise ValueError("q/k/v must be bf16 or fp32")
+    return _chunk_call("gdn_chunk_fwd_ex", q, k, v, g, beta, h0, cu_seqlens,
+                       out, hT, output_final_state, C, stream, q.dtype,
+                       extra=(dtype, int(variant), int(path), int(sp_parts)))
+
+
+def gdn_recurrent_step(q, k, v, g, beta, state, *, out=None, stream=None):
+    """One decode token per (sequence, head); ``state`` is updated in place.
+    q, k [N, H, dk] bf16, v [N, H, dv] bf16, g/beta [N, H] fp32, state
+    [N, H, dk, dv] fp32. Returns out [N, H, dv] bf16."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, None)
+    _need(k, "k", torch.bfloat16, dev)
+    _need(v, "v", torch.bfloat16, dev)
+    _need(g, "g", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    _need(state, "state", torch.float32, dev)
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if state.shape != (N, H, dk, dv):
+        raise ValueError("state must be [N, H, dk, dv]")
+    if out is None:
+        out = torch.empty_like(v)
+    else:
+        _need(out, "out", torch.bfloat16, dev)
+    with torch.cuda.device(dev):
+        rc = library().gdn_recurrent_step(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+            _ptr(out), N, H, dk, dv, _stream(stream))
+    if rc != GDN_OK:
+        raise GdnError(rc, "gdn_recurrent_step")
+    return out
+
+
+def gdn_device_status(stream=None) -> int:
+    """Synchronises ``stream`` and returns/clears the kernels' status word."""
+    return int(library().gdn_device_status(_stream(stream)))

@@ -1,0 +1,331 @@
+// Chunkwise Gated DeltaNet forward pass in fp32 CUDA-core arithmetic.
+//
+// Serves fp32 inputs (tensor cores at TF32 would not hold a 1e-3 bound after
+// the triangular solve) and any bf16 request the tensor-core path does not
+// take. One CTA owns (sequence, head, a DVT-row tile of the d_v x d_k state)
+// and walks the sequence's chunks in order; per chunk it performs
+//   (a) the gated UT/WY transform: A = strict_lower(diag(beta)(K K^T) (.) D'),
+//       then W = (I + A)^{-1} diag(beta e^{G'}) K and U0 = (I + A)^{-1}
+//       diag(beta) V by forward substitution, one column per thread
+//       ("UT transform" page of the illustrated DeltaNet walk-through: the
+//       unit-lower-triangular system solved by structure, no inverse);
+//   (b) U = U0 - W S^T and S <- gamma S + U^T Kbar with Kbar = diag(e^{G_L-G})K
+//       (its chunkwise state-passing paragraph, gated with the Gamma/gamma
+//       prefixes of its GLA section);
+//   (c) O = diag(e^G) Q S^T + ((Q K^T) (.) D (.) M_incl) U (its chunkwise
+//       output paragraph; the diagonal is kept because the read follows the
+//       write).
+// D_rj = exp(G_r - G_j) with G the chunk-local cumulative log gate; D' uses
+// G_{r-1} instead of G_r for GDN_GATE_AFTER_PREDICT. All exponents are <= 0.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kDVT = 32;  // state rows per CTA
+
+template <int DK, int C>
+struct SimtSmem {
+  static constexpr int KP = DK + 1;        // padded K/Q row
+  static constexpr int XW = DK + kDVT;     // solve width: W | U
+  static constexpr int XP = XW + 1;
+  static constexpr int CP = C + 1;
+  static constexpr int kFloats = C * KP * 2 + C * XP + C * CP * 2 +
+                                 kDVT * KP + C * kDVT + 5 * C;
+  static constexpr size_t kBytes = sizeof(float) * kFloats;
+};
+
+template <typename InT, int DK, int C, int VARIANT>
+__global__ void __launch_bounds__(kThreads)
+    chunk_simt_kernel(const ChunkParams p) {
+  using L = SimtSmem<DK, C>;
+  extern __shared__ float smem[];
+  float* sK = smem;                 // [C][KP]
+  float* sQ = sK + C * L::KP;       // [C][KP]
+  float* sX = sQ + C * L::KP;       // [C][XP]  W | U0 -> U
+  float* sA = sX + C * L::XP;       // [C][CP]  strict-lower system matrix
+  float* sP = sA + C * L::CP;       // [C][CP]  gated causal scores
+  float* sS = sP + C * L::CP;       // [DVT][KP] state rows (fp32)
+  float* sV = sS + kDVT * L::KP;    // [C][DVT] V tile, then history read
+  float* sG = sV + C * kDVT;        // [C] cumulative log gate
+  float* sGp = sG + C;              // [C] prediction exponent base
+  float* sB = sGp + C;              // [C] beta
+  float* sRaw = sB + C;             // [C] raw g
+  float* sDec = sRaw + C;           // [C] exp(G_last - G_r)
+
+  const int tid = threadIdx.x;
+  const int H = p.H, dv = p.dv;
+  const int h = blockIdx.y;
+  const int n = blockIdx.z / p.part_count;
+  const int part = p.part_begin + blockIdx.z % p.part_count;
+  const int row0 = blockIdx.x * kDVT;
+
+  // Role of this CTA.
+  const bool value_rows = row0 < dv;
+  const bool split_tail = (p.mode == kModeSplit) && part > 0;
+  if (!value_rows && !(split_tail && row0 < dv + DK)) return;
+  const bool scale_rows = !value_rows;              // rows of M
+  const bool emit = (p.mode == kModeOutput) || part == 0;
+
+  long long bos, eos;
+  if (!sequence_range(p, n, bos, eos)) return;
+  const int nch = (int)((eos - bos + C - 1) / C);
+  int c_begin, c_end;
+  part_range(nch, p.parts, part, c_begin, c_end);
+
+  const InT* q = static_cast<const InT*>(p.q);
+  const InT* k = static_cast<const InT*>(p.k);
+  const InT* v = static_cast<const InT*>(p.v);
+  InT* out = static_cast<InT*>(p.out);
+  const size_t nh = (size_t)n * H + h;
+
+  // ---- initial state rows ----
+  for (int idx = tid; idx < kDVT * DK; idx += kThreads) {
+    const int i = idx / kDVT, c = idx % kDVT;  // c fastest: coalesced h0 read
+    float s = 0.f;
+    if (scale_rows) {
+      s = (i == row0 - dv + c) ? 1.f : 0.f;
+    } else if (split_tail) {
+      s = 0.f;
+    } else if (part > 0) {
+      s = p.ws_start[((nh * p.parts + part) * dv + row0 + c) * DK + i];
+    } else if (p.h0) {
+      s = p.h0[(nh * DK + i) * dv + row0 + c];
+    }
+    sS[c * L::KP + i] = s;
+  }
+
+  for (int ch = c_begin; ch < c_end; ++ch) {
+    const long long t0 = bos + (long long)ch * C;
+    const int len = (int)min((long long)C, eos - t0);
+    __syncthreads();  // previous chunk done with the tiles
+
+    // ---- load K, Q (zero past the sequence end), V tile, g, beta ----
+    for (int idx = tid; idx < C * DK; idx += kThreads) {
+      const int r = idx / DK, i = idx % DK;
+      float kv = 0.f, qv = 0.f;
+      if (r < len) {
+        const size_t row = (size_t)(t0 + r) * H + h;
+        kv = to_f32(k[row * DK + i]);
+        qv = to_f32(q[row * DK + i]);
+      }
+      sK[r * L::KP + i] = kv;
+      sQ[r * L::KP + i] = qv;
+    }
+    for (int idx = tid; idx < C * kDVT; idx += kThreads) {
+      const int r = idx / kDVT, c = idx % kDVT;
+      float vv = 0.f;
+      if (r < len && value_rows) {
+        const size_t row = (size_t)(t0 + r) * H + h;
+        vv = to_f32(v[row * dv + row0 + c]);
+      }
+      sV[r * kDVT + c] = vv;
+    }
+    if (tid < C) {
+      float gg = 0.f, bb = 0.f;
+      if (tid < len) {
+        const size_t row = (size_t)(t0 + tid) * H + h;
+        gg = p.g[row];
+        bb = p.beta[row];
+      }
+      sRaw[tid] = gg;
+      sB[tid] = bb;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float acc = 0.f;
+      for (int r = 0; r < C; ++r) {
+        acc += sRaw[r];
+        sG[r] = acc;
+        sGp[r] = VARIANT == GDN_GATE_BEFORE_PREDICT ? acc : acc - sRaw[r];
+      }
+    }
+    __syncthreads();
+    const float Glast = sG[C - 1];
+    if (tid < C) sDec[tid] = expf(Glast - sG[tid]);
+
+    // ---- system matrix A and gated scores P ----
+    for (int idx = tid; idx < C * C; idx += kThreads) {
+      const int r = idx / C, j = idx % C;
+      float a = 0.f, pp = 0.f;
+      if (j <= r) {
+        float kk = 0.f, qk = 0.f;
+#pragma unroll 8
+        for (int i = 0; i < DK; ++i) {
+          const float kj = sK[j * L::KP + i];
+          kk = fmaf(sK[r * L::KP + i], kj, kk);
+          qk = fmaf(sQ[r * L::KP + i], kj, qk);
+        }
+        pp = expf(sG[r] - sG[j]) * qk;
+        if (j < r) a = sB[r] * expf(sGp[r] - sG[j]) * kk;
+      }
+      sA[r * L::CP + j] = a;
+      sP[r * L::CP + j] = pp;
+    }
+    __syncthreads();
+
+    // ---- forward substitution: (I + A) X = [diag(beta e^G') K | diag(beta) V]
+    if (tid < L::XW) {
+      const int col = tid;
+      for (int r = 0; r < C; ++r) {
+        float x = col < DK ? sB[r] * expf(sGp[r]) * sK[r * L::KP + col]
+                           : sB[r] * sV[r * kDVT + (col - DK)];
+        for (int j = 0; j < r; ++j)
+          x = fmaf(-sA[r * L::CP + j], sX[j * L::XP + col], x);
+        sX[r * L::XP + col] = x;
+      }
+    }
+    __syncthreads();
+
+    // ---- U = U0 - W S^T ; history read e^{G} Q S^T (into sV) ----
+    for (int idx = tid; idx < C * kDVT; idx += kThreads) {
+      const int r = idx / kDVT, c = idx % kDVT;
+      float ws = 0.f, qs = 0.f;
+#pragma unroll 8
+      for (int i = 0; i < DK; ++i) {
+        const float s = sS[c * L::KP + i];
+        ws = fmaf(sX[r * L::XP + i], s, ws);
+        qs = fmaf(sQ[r * L::KP + i], s, qs);
+      }
+      sX[r * L::XP + DK + c] -= ws;
+      sV[r * kDVT + c] = expf(sG[r]) * qs;
+    }
+    __syncthreads();
+
+    // ---- output rows (read after the write: j <= r) ----
+    if (emit) {
+      for (int idx = tid; idx < C * kDVT; idx += kThreads) {
+        const int r = idx / kDVT, c = idx % kDVT;
+        if (r < len) {
+          float o = sV[r * kDVT + c];
+          for (int j = 0; j <= r; ++j)
+            o = fmaf(sP[r * L::CP + j], sX[j * L::XP + DK + c], o);
+          const size_t row = (size_t)(t0 + r) * H + h;
+          out[row * dv + row0 + c] = from_f32<InT>(o);
+        }
+      }
+    }
+    // ---- state: S <- gamma S + U^T Kbar ----
+    const float gam = expf(Glast);
+    for (int idx = tid; idx < kDVT * DK; idx += kThreads) {
+      const int c = idx / DK, i = idx % DK;
+      float acc = 0.f;
+#pragma unroll 8
+      for (int r = 0; r < C; ++r)
+        acc = fmaf(sX[r * L::XP + DK + c] * sDec[r], sK[r * L::KP + i], acc);
+      sS[c * L::KP + i] = fmaf(gam, sS[c * L::KP + i], acc);
+    }
+  }
+  __syncthreads();
+
+  // ---- final state ----
+  if (p.mode == kModeSplit) {
+    if (part == 0) {
+      if (p.parts > 1)
+        for (int idx = tid; idx < kDVT * DK; idx += kThreads) {
+          const int c = idx / DK, i = idx % DK;
+          p.ws_start[((nh * p.parts + 1) * dv + row0 + c) * DK + i] =
+              sS[c * L::KP + i];
+        }
+    } else {
+      for (int idx = tid; idx < kDVT * DK; idx += kThreads) {
+        const int c = idx / DK, i = idx % DK;
+        p.ws_end[((nh * p.parts + part) * (dv + DK) + row0 + c) * DK + i] =
+            sS[c * L::KP + i];
+      }
+    }
+  } else if (p.hT && part == p.parts - 1) {
+    for (int idx = tid; idx < kDVT * DK; idx += kThreads) {
+      const int i = idx / kDVT, c = idx % kDVT;
+      p.hT[(nh * DK + i) * dv + row0 + c] = sS[c * L::KP + i];
+    }
+  }
+}
+
+// Serial correction chain over sub-sequences (the CP=4 chain of the sequence
+// parallelism note): S_start(p + 1) = dS_end(p) + S_start(p) M_end(p) for
+// p = 1 .. parts - 2; S_start(1) was written by part 0 of the split pass.
+template <int DK>
+__global__ void __launch_bounds__(kThreads) sp_chain_kernel(const ChunkParams p) {
+  __shared__ float sS[kDVT][DK + 1];
+  const int tid = threadIdx.x;
+  const int h = blockIdx.y, n = blockIdx.z;
+  const int row0 = blockIdx.x * kDVT;
+  const int dv = p.dv;
+  const size_t nh = (size_t)n * p.H + h;
+  if (p.cu_seqlens) {
+    long long bos, eos;
+    if (!sequence_range(p, n, bos, eos)) return;
+  }
+  for (int idx = tid; idx < kDVT * DK; idx += kThreads) {
+    const int c = idx / DK, i = idx % DK;
+    sS[c][i] = p.ws_start[((nh * p.parts + 1) * dv + row0 + c) * DK + i];
+  }
+  for (int part = 1; part + 1 < p.parts; ++part) {
+    __syncthreads();
+    const float* end = p.ws_end + (nh * p.parts + part) * (size_t)(dv + DK) * DK;
+    const float* M = end + (size_t)dv * DK;
+    float acc[kDVT * DK / kThreads];
+#pragma unroll
+    for (int e = 0; e < kDVT * DK / kThreads; ++e) {
+      const int idx = tid + e * kThreads;
+      const int c = idx / DK, j = idx % DK;
+      float s = end[(size_t)(row0 + c) * DK + j];
+      for (int i = 0; i < DK; ++i) s = fmaf(sS[c][i], M[(size_t)i * DK + j], s);
+      acc[e] = s;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < kDVT * DK / kThreads; ++e) {
+      const int idx = tid + e * kThreads;
+      const int c = idx / DK, j = idx % DK;
+      sS[c][j] = acc[e];
+      p.ws_start[((nh * p.parts + part + 1) * dv + row0 + c) * DK + j] = acc[e];
+    }
+  }
+}
+
+template <typename InT, int DK, int VARIANT>
+cudaError_t launch_typed(const ChunkParams& p, cudaStream_t stream) {
+  constexpr int C = 64;
+  auto kern = chunk_simt_kernel<InT, DK, C, VARIANT>;
+  const size_t bytes = SimtSmem<DK, C>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  const int rows = p.mode == kModeSplit ? p.dv + DK : p.dv;
+  dim3 grid(rows / kDVT, p.H, p.N * p.part_count);
+  kern<<<grid, kThreads, bytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename InT>
+cudaError_t launch_dk(const ChunkParams& p, cudaStream_t stream) {
+  const bool after = p.variant == GDN_GATE_AFTER_PREDICT;
+  if (p.dk == 64)
+    return after ? launch_typed<InT, 64, GDN_GATE_AFTER_PREDICT>(p, stream)
+                 : launch_typed<InT, 64, GDN_GATE_BEFORE_PREDICT>(p, stream);
+  return after ? launch_typed<InT, 128, GDN_GATE_AFTER_PREDICT>(p, stream)
+               : launch_typed<InT, 128, GDN_GATE_BEFORE_PREDICT>(p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_simt(const ChunkParams& p, bool bf16,
+                              cudaStream_t stream) {
+  return bf16 ? launch_dk<__nv_bfloat16>(p, stream)
+              : launch_dk<float>(p, stream);
+}
+
+cudaError_t launch_sp_chain(const ChunkParams& p, cudaStream_t stream) {
+  if (p.parts < 3) return cudaSuccess;
+  dim3 grid(p.dv / kDVT, p.H, p.N);
+  if (p.dk == 64)
+    sp_chain_kernel<64><<<grid, kThreads, 0, stream>>>(p);
+  else
+    sp_chain_kernel<128><<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

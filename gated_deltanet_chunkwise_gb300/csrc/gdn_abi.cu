@@ -1,0 +1,243 @@
+// C-ABI entry points: host-side argument checks, workspace, kernel choice.
+// Every check runs before anything is enqueued; a failing check returns a
+// negative gdn_status_t and leaves the stream untouched.
+#include <atomic>
+#include <mutex>
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+// Status word written by kernels (first error wins), one per device.
+__device__ int g_device_status;
+
+std::atomic<unsigned long long> g_launches{0};
+
+cudaError_t counted(cudaError_t e, int launches) {
+  if (e == cudaSuccess) g_launches.fetch_add(launches);
+  return e;
+}
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices];
+std::mutex g_status_mutex;
+
+int current_status_ptr(int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return GDN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_status_mutex);
+  if (!g_status_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess)
+      return GDN_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<int*>(ptr);
+  }
+  *out = g_status_ptr[dev];
+  return GDN_OK;
+}
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+bool head_dim_ok(int d) { return d == 64 || d == 128; }
+
+int check_chunk_args(const void* q, const void* k, const void* v,
+                     const float* g, const float* beta, const float* h0,
+                     const void* out, const float* hT,
+                     const int32_t* cu_seqlens, int B, int H, int T, int dk,
+                     int dv, int C, int dtype, int variant, int path,
+                     int sp_parts) {
+  if (B < 0 || H <= 0 || T < 0) return GDN_ERR_INVALID_ARG;
+  if (dtype != GDN_DTYPE_BF16 && dtype != GDN_DTYPE_F32)
+    return GDN_ERR_INVALID_ARG;
+  if (variant != GDN_GATE_BEFORE_PREDICT && variant != GDN_GATE_AFTER_PREDICT)
+    return GDN_ERR_INVALID_ARG;
+  if (path < GDN_PATH_AUTO || path > GDN_PATH_TCGEN05)
+    return GDN_ERR_INVALID_ARG;
+  if (sp_parts < 0 || sp_parts > 4096) return GDN_ERR_INVALID_ARG;
+  if (cu_seqlens && B == 0) return GDN_ERR_INVALID_ARG;
+  const long long tokens = cu_seqlens ? (long long)T : (long long)B * T;
+  if (tokens > 0 || (cu_seqlens && B > 0)) {
+    if (!q || !k || !v || !g || !beta || !out) return GDN_ERR_INVALID_ARG;
+  }
+  if (!head_dim_ok(dk) || !head_dim_ok(dv) || C != 64)
+    return GDN_ERR_UNSUPPORTED;
+  if (path == GDN_PATH_TCGEN05 && dtype != GDN_DTYPE_BF16)
+    return GDN_ERR_UNSUPPORTED;
+  // Size limits: token-head rows index with 64-bit math, but grid.z holds
+  // sequences x parts and the tensor maps hold 32-bit extents.
+  if ((long long)tokens * H > (1ll << 40)) return GDN_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q, k, v, g, beta, h0, out, hT, cu_seqlens};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+  // out must not alias an input.
+  if (out && (out == q || out == k || out == v)) return GDN_ERR_INVALID_ARG;
+  return GDN_OK;
+}
+
+int choose_parts(int requested, int N, int H, int T, int dv, int C,
+                 bool packed) {
+  if (requested > 0) return requested;
+  if (packed) return 1;
+  // Automatic split: only long sequences, and only until the state-row CTAs
+  // cover the SMs about twice.
+  const int nch = (T + C - 1) / C;
+  int sms = 148;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
+            cudaSuccess && v > 0)
+      sms = v;
+  }
+  const long long ctas = (long long)N * H * (dv / 32);
+  if (nch < 64 || ctas >= 2ll * sms) return 1;
+  int parts = (int)((2ll * sms + ctas - 1) / ctas);
+  parts = parts < 2 ? 2 : parts;
+  const int max_parts = nch / 16;  // keep >= 16 chunks per sub-sequence
+  if (parts > max_parts) parts = max_parts;
+  return parts < 1 ? 1 : parts;
+}
+
+int run_chunk(const void* q, const void* k, const void* v, const float* g,
+              const float* beta, const float* h0, void* out, float* hT,
+              const int32_t* cu_seqlens, int B, int H, int T, int dk, int dv,
+              int C, int dtype, int variant, int path, int sp_parts,
+              cudaStream_t stream) {
+  int rc = check_chunk_args(q, k, v, g, beta, h0, out, hT, cu_seqlens, B, H,
+                            T, dk, dv, C, dtype, variant, path, sp_parts);
+  if (rc != GDN_OK) return rc;
+  if (B == 0 || H == 0) return GDN_OK;
+  int* status = nullptr;
+  if ((rc = current_status_ptr(&status)) != GDN_OK) return rc;
+
+  ChunkParams p{};
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0;
+  p.out = out; p.hT = hT; p.cu_seqlens = cu_seqlens;
+  p.N = B; p.H = H; p.T = T; p.dk = dk; p.dv = dv; p.C = C;
+  p.variant = variant;
+  p.status = status;
+  const bool bf16 = dtype == GDN_DTYPE_BF16;
+  const int parts = choose_parts(sp_parts, B, H, T, dv, C, cu_seqlens != nullptr);
+  p.parts = parts;
+
+  if (parts == 1) {
+    p.part_begin = 0; p.part_count = 1; p.mode = kModeOutput;
+    return counted(launch_chunk_simt(p, bf16, stream), 1) == cudaSuccess
+               ? GDN_OK
+               : GDN_ERR_CUDA;
+  }
+
+  // Sequence-parallel: split pass, correction chain, corrected output pass.
+  const size_t nhp = (size_t)B * H * parts;
+  const size_t end_bytes = nhp * (size_t)(dv + dk) * dk * sizeof(float);
+  const size_t start_bytes = nhp * (size_t)dv * dk * sizeof(float);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, end_bytes + start_bytes, stream) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  p.ws_end = static_cast<float*>(ws);
+  p.ws_start = reinterpret_cast<float*>(static_cast<char*>(ws) + end_bytes);
+  cudaError_t e;
+  p.mode = kModeSplit; p.part_begin = 0; p.part_count = parts - 1;
+  e = counted(launch_chunk_simt(p, bf16, stream), 1);
+  if (e == cudaSuccess && parts > 2) e = counted(launch_sp_chain(p, stream), 1);
+  if (e == cudaSuccess) {
+    p.mode = kModeOutput; p.part_begin = 1; p.part_count = parts - 1;
+    e = counted(launch_chunk_simt(p, bf16, stream), 1);
+  }
+  cudaError_t f = cudaFreeAsync(ws, stream);
+  return (e == cudaSuccess && f == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" {
+
+int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                  const float* beta, const float* h0, void* out, float* hT,
+                  const int32_t* cu_seqlens, int B, int H, int T, int dk,
+                  int dv, int C, gdn_stream_t stream) {
+  return gdn::run_chunk(q, k, v, g, beta, h0, out, hT, cu_seqlens, B, H, T,
+                        dk, dv, C, GDN_DTYPE_BF16, GDN_GATE_BEFORE_PREDICT,
+                        GDN_PATH_AUTO, 0, stream);
+}
+
+int gdn_chunk_fwd_f32(const float* q, const float* k, const float* v,
+                      const float* g, const float* beta, const float* h0,
+                      float* out, float* hT, const int32_t* cu_seqlens, int B,
+                      int H, int T, int dk, int dv, int C,
+                      gdn_stream_t stream) {
+  return gdn::run_chunk(q, k, v, g, beta, h0, out, hT, cu_seqlens, B, H, T,
+                        dk, dv, C, GDN_DTYPE_F32, GDN_GATE_BEFORE_PREDICT,
+                        GDN_PATH_AUTO, 0, stream);
+}
+
+int gdn_chunk_fwd_ex(const void* q, const void* k, const void* v,
+                     const float* g, const float* beta, const float* h0,
+                     void* out, float* hT, const int32_t* cu_seqlens, int B,
+                     int H, int T, int dk, int dv, int C, int dtype,
+                     int variant, int path, int sp_parts,
+                     gdn_stream_t stream) {
+  return gdn::run_chunk(q, k, v, g, beta, h0, out, hT, cu_seqlens, B, H, T,
+                        dk, dv, C, dtype, variant, path, sp_parts, stream);
+}
+
+int gdn_recurrent_step(const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, float* state,
+                       void* out, int N, int H, int dk, int dv,
+                       gdn_stream_t stream) {
+  if (N < 0 || H <= 0) return GDN_ERR_INVALID_ARG;
+  if (!gdn::head_dim_ok(dk) || !gdn::head_dim_ok(dv))
+    return GDN_ERR_UNSUPPORTED;
+  if (N == 0) return GDN_OK;
+  if (!q || !k || !v || !g || !beta || !state || !out)
+    return GDN_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, g, beta, state, out};
+  for (const void* p : ptrs)
+    if (!gdn::aligned16(p)) return GDN_ERR_MISALIGNED;
+  if ((long long)N * H > 0x7fffffffll) return GDN_ERR_UNSUPPORTED;
+  if (out == q || out == k || out == v) return GDN_ERR_INVALID_ARG;
+  gdn::DecodeParams p{};
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.state = state;
+  p.out = out; p.N = N; p.H = H; p.dk = dk; p.dv = dv;
+  p.variant = GDN_GATE_BEFORE_PREDICT;
+  return gdn::counted(gdn::launch_decode(p, stream), 1) == cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_CUDA;
+}
+
+int gdn_device_status(gdn_stream_t stream) {
+  int* status = nullptr;
+  int rc = gdn::current_status_ptr(&status);
+  if (rc != GDN_OK) return rc;
+  int value = 0;
+  if (cudaMemcpyAsync(&value, status, sizeof(int), cudaMemcpyDeviceToHost,
+                      stream) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return GDN_ERR_CUDA;
+  return value;
+}
+
+const char* gdn_status_string(int status) {
+  switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_MISALIGNED: return "GDN_ERR_MISALIGNED";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+    default: return "GDN_UNKNOWN_STATUS";
+  }
+}
+
+int gdn_version(void) { return 100; }
+
+unsigned long long gdn_kernel_launches(void) { return gdn::g_launches.load(); }
+
+}  // extern "C"

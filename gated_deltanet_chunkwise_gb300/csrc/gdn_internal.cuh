@@ -1,0 +1,118 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// One chunked forward request after host validation.
+//
+// Sequence-parallel passes (parts > 1) split each sequence's chunks into
+// `parts` contiguous sub-sequences. `mode` selects what a launch does:
+//   kModeOutput : state rows start from h0 / zero (part 0) or from
+//                 ws_start (part p >= 1); outputs are written; the last part
+//                 writes hT.
+//   kModeSplit  : part 0 runs the true recurrence from h0 and writes both its
+//                 outputs and its end state (the start of part 1, into
+//                 ws_start); parts p >= 1 run from a zero state (rows
+//                 [0, dv): the incremental state) and from the identity
+//                 (rows [dv, dv + dk): the scaling matrix) and write both end
+//                 values into ws_end.
+// Workspace layouts (math orientation, row-major, dk columns):
+//   ws_end   [N, H, parts, dv + dk, dk]
+//   ws_start [N, H, parts, dv, dk]   (entry p holds the true start of part p)
+enum { kModeOutput = 0, kModeSplit = 1 };
+
+struct ChunkParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  const float* h0;
+  void* out;
+  float* hT;
+  const int32_t* cu_seqlens;
+  int N, H, T, dk, dv, C;
+  int variant;     // GDN_GATE_BEFORE_PREDICT / GDN_GATE_AFTER_PREDICT
+  int parts;       // sequence-parallel split (>= 1)
+  int part_begin;  // first part covered by this launch
+  int part_count;  // parts covered by this launch (grid.z = N * part_count)
+  int mode;
+  float* ws_end;
+  float* ws_start;
+  int* status;     // device status word (first error wins)
+};
+
+struct DecodeParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  float* state;
+  void* out;
+  int N, H, dk, dv;
+  int variant;
+};
+
+// Launchers (return a cudaError_t from the launch itself).
+cudaError_t launch_chunk_simt(const ChunkParams& p, bool bf16,
+                              cudaStream_t stream);
+cudaError_t launch_sp_chain(const ChunkParams& p, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+
+// Device-side helpers --------------------------------------------------------
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) {
+  return x;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ void record_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Token range [bos, eos) of sequence n; false (and a recorded error) when the
+// packing is inconsistent.
+__device__ __forceinline__ bool sequence_range(const ChunkParams& p, int n,
+                                               long long& bos,
+                                               long long& eos) {
+  if (p.cu_seqlens) {
+    const int b = p.cu_seqlens[n], e = p.cu_seqlens[n + 1];
+    if (b < 0 || e < b || e > p.T) {
+      record_status(p.status, GDN_ERR_INVALID_ARG);
+      return false;
+    }
+    bos = b;
+    eos = e;
+  } else {
+    bos = (long long)n * p.T;
+    eos = bos + p.T;
+  }
+  return true;
+}
+
+// Chunk range [c_begin, c_end) of part `part` of a sequence with nch chunks.
+__device__ __forceinline__ void part_range(int nch, int parts, int part,
+                                           int& c_begin, int& c_end) {
+  const int per = (nch + parts - 1) / parts;
+  c_begin = min(nch, part * per);
+  c_end = min(nch, c_begin + per);
+}
+
+}  // namespace gdn

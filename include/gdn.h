@@ -1,0 +1,167 @@
+/*
+ * gdn.h -- C ABI of the GB300 Gated DeltaNet library (libgdn_gb300.so).
+ *
+ * The method. For every sequence and head, with a d_v x d_k state S, scalar
+ * gates alpha_t = exp(g_t) in (0, 1] and write strengths beta_t:
+ *
+ *     S~_t = alpha_t S_{t-1}                       (forget first)
+ *     u_t  = beta_t (v_t - S~_t k_t)               (error of the prediction)
+ *     S_t  = S~_t + u_t k_t^T                      (delta-rule write)
+ *     o_t  = S_t q_t                               (read after the write)
+ *
+ * This is the Gated DeltaNet update as the illustrated DeltaNet walk-through
+ * (stay-hungry-time.github.io/deltanet) states it in its GDN paragraph (worked
+ * example 3 -> 2.4 -> 3.7), with the read after the write and the diagonal
+ * included as in its DeltaNet output paragraphs. alpha = 1 gives plain
+ * DeltaNet. GDN_GATE_AFTER_PREDICT selects the other placement, u_t =
+ * beta_t (v_t - S_{t-1} k_t), S_t = alpha_t S_{t-1} + u_t k_t^T, the form of
+ * the lqnn.cn "GPU parallelisation of Gated DeltaNet" page, section 1.2.
+ *
+ * The library evaluates it chunkwise (chunks of C tokens): a gated UT/WY
+ * transform per chunk (the walk-through's "UT transform" and "WY
+ * representation" pages), the serial state recurrence across chunks and the
+ * chunk output (its chunkwise DeltaNet state/output paragraphs), and for long
+ * sequences the incremental-state / scaling-matrix correction of "How to
+ * Implement Sequence Parallelism in DeltaNet" (papercache.org, A2). Results
+ * equal the token recurrence up to floating-point rounding.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, row-major
+ *     and contiguous, and must not alias each other (except where stated).
+ *   - States are stored transposed: h0, hT and state are [N, H, dk, dv] fp32
+ *     and element (i, j) of a head's dk x dv block is S[j][i].
+ *   - Work is enqueued on `stream` (NULL = legacy default stream) and runs
+ *     asynchronously; no entry point synchronises the host. Argument checks
+ *     run on the host first: a failing check returns a negative status and
+ *     enqueues nothing.
+ *   - Workspace, when a path needs it, is taken with cudaMallocAsync on
+ *     `stream` and released with cudaFreeAsync on the same stream.
+ *   - Thread safety: entry points may be called concurrently from several
+ *     host threads on different streams.
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* gdn_stream_t;
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = -1,  /* null pointer, bad size, bad packing */
+  GDN_ERR_UNSUPPORTED = -2,  /* valid request this build does not serve */
+  GDN_ERR_MISALIGNED = -3,   /* pointer not 16-byte aligned */
+  GDN_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed */
+  GDN_ERR_TIMEOUT = -5       /* a bounded device wait gave up */
+} gdn_status_t;
+
+/* Gate placement (see the top of this file). */
+#define GDN_GATE_BEFORE_PREDICT 0 /* default */
+#define GDN_GATE_AFTER_PREDICT 1
+
+/* Element type of q, k, v and out for gdn_chunk_fwd_ex. */
+#define GDN_DTYPE_BF16 0
+#define GDN_DTYPE_F32 1
+
+/* Kernel family for gdn_chunk_fwd_ex (GDN_PATH_AUTO picks the fastest one
+ * that serves the request). */
+#define GDN_PATH_AUTO 0
+#define GDN_PATH_SIMT 1   /* fp32 CUDA-core arithmetic; any supported shape */
+#define GDN_PATH_TCGEN05 2 /* bf16 tcgen05/TMEM tensor-core path */
+
+/*
+ * gdn_chunk_fwd -- chunkwise forward pass, bf16 q/k/v/out.
+ *
+ *   q, k        bf16 [B, T, H, dk]; k (and usually q) L2-normalised per row
+ *   v           bf16 [B, T, H, dv]
+ *   g           fp32 [B, T, H], log alpha (<= 0)
+ *   beta        fp32 [B, T, H]
+ *   h0          fp32 [N, H, dk, dv] initial states, or NULL for zero states
+ *   out         bf16 [B, T, H, dv] (written)
+ *   hT          fp32 [N, H, dk, dv] final states (written), or NULL
+ *   cu_seqlens  NULL for a dense batch (N = B sequences of T tokens), or a
+ *               DEVICE int32 [B + 1] array of packed sequence offsets: then
+ *               the tensors are [1, T, H, ...], B = N is the number of
+ *               sequences, cu_seqlens[0] = 0, non-decreasing, and
+ *               cu_seqlens[B] = T. Chunks never cross a sequence boundary;
+ *               each sequence starts from its own h0 (or zero) state. The
+ *               host never reads this array; a kernel that finds an
+ *               inconsistent entry skips that sequence and records
+ *               GDN_ERR_INVALID_ARG, returned by gdn_device_status.
+ *   B, H, T     sizes; T may be any value >= 0 (no multiple of C needed)
+ *   dk, dv      64 or 128 each
+ *   C           chunk size; 64
+ * Returns GDN_OK or a negative gdn_status_t.
+ */
+int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                  const float* beta, const float* h0, void* out, float* hT,
+                  const int32_t* cu_seqlens, int B, int H, int T, int dk,
+                  int dv, int C, gdn_stream_t stream);
+
+/* gdn_chunk_fwd_f32 -- the same with fp32 q, k, v and out (fp32 CUDA-core
+ * arithmetic throughout). */
+int gdn_chunk_fwd_f32(const float* q, const float* k, const float* v,
+                      const float* g, const float* beta, const float* h0,
+                      float* out, float* hT, const int32_t* cu_seqlens, int B,
+                      int H, int T, int dk, int dv, int C,
+                      gdn_stream_t stream);
+
+/*
+ * gdn_chunk_fwd_ex -- gdn_chunk_fwd with explicit options.
+ *   dtype      GDN_DTYPE_BF16 or GDN_DTYPE_F32 (q, k, v, out)
+ *   variant    GDN_GATE_BEFORE_PREDICT or GDN_GATE_AFTER_PREDICT
+ *   path       GDN_PATH_* (GDN_PATH_TCGEN05 requires bf16)
+ *   sp_parts   sequence-parallel split: 0 = automatic, 1 = never split,
+ *              P >= 2 = split every sequence into P sub-sequences of whole
+ *              chunks (incremental state from zero + scaling matrix, then the
+ *              serial correction chain and the fused corrected output)
+ * Other arguments as gdn_chunk_fwd.
+ */
+int gdn_chunk_fwd_ex(const void* q, const void* k, const void* v,
+                     const float* g, const float* beta, const float* h0,
+                     void* out, float* hT, const int32_t* cu_seqlens, int B,
+                     int H, int T, int dk, int dv, int C, int dtype,
+                     int variant, int path, int sp_parts,
+                     gdn_stream_t stream);
+
+/*
+ * gdn_recurrent_step -- one decode token per (sequence, head), state updated
+ * in place (the token recurrence above applied once).
+ *   q, k   bf16 [N, H, dk]      v, out  bf16 [N, H, dv]
+ *   g      fp32 [N, H] (log alpha)       beta  fp32 [N, H]
+ *   state  fp32 [N, H, dk, dv], read and overwritten
+ *   dk, dv 64 or 128 each
+ * The state is streamed from HBM once and written once (16-byte vectors).
+ */
+int gdn_recurrent_step(const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, float* state,
+                       void* out, int N, int H, int dk, int dv,
+                       gdn_stream_t stream);
+
+/* gdn_device_status -- waits for `stream`, then returns and clears the
+ * status recorded by kernels on the current device (GDN_OK, or the first
+ * GDN_ERR_INVALID_ARG / GDN_ERR_TIMEOUT recorded since the last call). */
+int gdn_device_status(gdn_stream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* gdn_status_string(int status);
+
+/* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
+int gdn_version(void);
+
+/* Number of kernels this library has enqueued in this process so far (all
+ * devices, all streams). Lets a caller count the launches inside a timed
+ * region. */
+unsigned long long gdn_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_GB300_H */

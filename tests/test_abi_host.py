@@ -1,0 +1,126 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load on a machine without a GPU, export every function that
+``include/gdn.h`` declares, and reject bad arguments on the host with the
+documented status, before touching CUDA. Fault injection happens here, on the
+host: bad sizes, null and misaligned pointers, unsupported head sizes and
+chunk sizes, aliasing output.
+"""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+HEADER = ROOT / "include" / "gdn.h"
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA = 0, -1, -2, -3, -4
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(gdn_\w+)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("gdn_chunk_fwd", "gdn_chunk_fwd_f32", "gdn_chunk_fwd_ex",
+                     "gdn_recurrent_step", "gdn_status_string"):
+        assert required in names
+
+
+def test_library_loads_and_exports_every_declared_symbol(lib):
+    so = lib.library()
+    for name in declared_functions():
+        assert hasattr(so, name), f"{name} declared in gdn.h but not exported"
+
+
+def test_status_strings(lib):
+    assert lib.gdn_status_string(OK) == "GDN_OK"
+    assert lib.gdn_status_string(MISALIGNED) == "GDN_ERR_MISALIGNED"
+    assert lib.gdn_status_string(12345) == "GDN_UNKNOWN_STATUS"
+
+
+# Fake device addresses: never dereferenced because every call below fails a
+# host check first.
+A = 0x7F0000000000  # 16-byte aligned
+ODD = A + 4
+
+
+def chunk(so, q=A, k=A + 0x1000, v=A + 0x2000, g=A + 0x3000, beta=A + 0x4000,
+          h0=None, out=A + 0x5000, hT=None, cu=None, B=1, H=1, T=64, dk=64,
+          dv=64, C=64, **ex):
+    if ex:
+        return so.gdn_chunk_fwd_ex(q, k, v, g, beta, h0, out, hT, cu, B, H, T,
+                                   dk, dv, C, ex.get("dtype", 0),
+                                   ex.get("variant", 0), ex.get("path", 0),
+                                   ex.get("sp_parts", 0), None)
+    return so.gdn_chunk_fwd(q, k, v, g, beta, h0, out, hT, cu, B, H, T, dk, dv,
+                            C, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), INVALID),
+    (dict(out=None), INVALID),
+    (dict(g=None), INVALID),
+    (dict(B=-1), INVALID),
+    (dict(H=0), INVALID),
+    (dict(T=-5), INVALID),
+    (dict(dk=96), UNSUPPORTED),
+    (dict(dv=32), UNSUPPORTED),
+    (dict(C=32), UNSUPPORTED),
+    (dict(C=128), UNSUPPORTED),
+    (dict(q=ODD), MISALIGNED),
+    (dict(beta=ODD), MISALIGNED),
+    (dict(h0=ODD), MISALIGNED),
+    (dict(hT=ODD), MISALIGNED),
+    (dict(cu=ODD, B=2), MISALIGNED),
+    (dict(out=A), INVALID),              # out aliases q
+    (dict(cu=A + 0x6000, B=0), INVALID),  # packed batch needs >= 1 sequence
+    (dict(variant=7), INVALID),
+    (dict(path=9), INVALID),
+    (dict(dtype=5), INVALID),
+    (dict(sp_parts=-1), INVALID),
+    (dict(dtype=1, path=2), UNSUPPORTED),  # tensor-core path is bf16 only
+])
+def test_chunk_fwd_rejects_on_host(lib, kw, expect):
+    assert chunk(lib.library(), **kw) == expect
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert chunk(lib.library(), B=0) == OK
+    # T = 0 with dense batches: nothing to do, but arguments still checked
+    assert chunk(lib.library(), T=0, dk=96) == UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(N=-1), INVALID), (dict(H=0), INVALID), (dict(dk=80), UNSUPPORTED),
+    (dict(state=None), INVALID), (dict(q=ODD), MISALIGNED),
+    (dict(out=A), INVALID),
+])
+def test_recurrent_step_rejects_on_host(lib, kw, expect):
+    a = dict(q=A, k=A + 0x100, v=A + 0x200, g=A + 0x300, beta=A + 0x400,
+             state=A + 0x500, out=A + 0x600, N=2, H=2, dk=64, dv=64)
+    a.update(kw)
+    so = lib.library()
+    rc = so.gdn_recurrent_step(a["q"], a["k"], a["v"], a["g"], a["beta"],
+                               a["state"], a["out"], a["N"], a["H"], a["dk"],
+                               a["dv"], None)
+    assert rc == expect
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(1, 4, 1, 64, dtype=torch.bfloat16)
+    gb = torch.zeros(1, 4, 1)
+    with pytest.raises(ValueError, match="CUDA"):
+        lib.gdn_chunk_fwd(x, x, x, gb, gb)
+
+
+def test_launch_counter_is_monotone(lib):
+    a = lib.kernel_counters()
+    chunk(lib.library(), B=0)
+    assert lib.kernel_counters() == a

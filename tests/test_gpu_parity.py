@@ -1,0 +1,175 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Acceptance (per output tensor and per final state):
+    max|X_gpu - X_ref| / max|X_ref| <= 1e-3 for fp32 inputs, <= 2e-2 for bf16.
+Both sides read identical seeded inputs (bf16 values upcast exactly).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_chunkwise_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-3, "bf16": 2e-2}
+
+
+def rel_err(x, ref):
+    x = x.detach().cpu().double().numpy() if hasattr(x, "detach") else x
+    denom = np.max(np.abs(ref))
+    assert np.all(np.isfinite(x)), "non-finite values in the GPU result"
+    return float(np.max(np.abs(x - ref)) / max(denom, 1e-30))
+
+
+def to_dev(d, dev):
+    return {k: (None if v is None else v.to(dev)) for k, v in d.items()}
+
+
+def run_gpu(lib, d, dev, dtype, variant=0, path=0, sp_parts=0, poison=True):
+    x = to_dev(d, dev)
+    out = torch.empty_like(x["v"])
+    N = x["h0"].shape[0] if x["h0"] is not None else (
+        x["cu_seqlens"].numel() - 1 if x["cu_seqlens"] is not None
+        else x["q"].shape[0])
+    H, dk, dv = x["q"].shape[2], x["q"].shape[3], x["v"].shape[3]
+    hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    if poison:  # unwritten elements would surface as NaN
+        out.fill_(float("nan"))
+        hT.fill_(float("nan"))
+    lib.gdn_chunk_fwd_ex(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"],
+                         x["cu_seqlens"], out=out, hT=hT, variant=variant,
+                         path=path, sp_parts=sp_parts)
+    torch.cuda.synchronize()
+    assert lib.gdn_device_status() == 0
+    return out, hT
+
+
+def check(lib, dev, d, dtype, variant=0, path=0, sp_parts=0):
+    o_ref, h_ref = oracle.forward(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                  d["h0"], d["cu_seqlens"], variant=variant)
+    out, hT = run_gpu(lib, d, dev, dtype, variant, path, sp_parts)
+    eo, eh = rel_err(out, o_ref), rel_err(hT, h_ref)
+    assert eo <= TOL[dtype], f"output rel err {eo:.3e}"
+    assert eh <= TOL[dtype], f"final-state rel err {eh:.3e}"
+    return eo, eh
+
+
+# ---- workload 0: B=1, H=1, T=256, dk=dv=64, fp32, gated and alpha = 1 ----
+@pytest.mark.parametrize("gated", [True, False])
+def test_small_fp32_gated_and_deltanet(lib, cuda_device, gated):
+    d = inputs.chunk_inputs(1, 1, 256, 64, 64, dtype="f32", seed=0,
+                            gated=gated)
+    check(lib, cuda_device, d, "f32")
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64), (128, 128)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ragged_multi_chunk_shapes(lib, cuda_device, dk, dv, dtype):
+    # several chunks plus a ragged tail, nonzero initial states
+    d = inputs.chunk_inputs(2, 3, 64 * 3 + 17, dk, dv, dtype=dtype, seed=1,
+                            h0=True)
+    check(lib, cuda_device, d, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gate_after_prediction_variant(lib, cuda_device, dtype):
+    d = inputs.chunk_inputs(2, 2, 150, 64, 64, dtype=dtype, seed=2, h0=True)
+    check(lib, cuda_device, d, dtype, variant=1)
+
+
+@pytest.mark.parametrize("T", [1, 5, 63, 64, 65])
+def test_short_and_boundary_lengths(lib, cuda_device, T):
+    d = inputs.chunk_inputs(1, 2, T, 128, 128, dtype="f32", seed=3, h0=True)
+    check(lib, cuda_device, d, "f32")
+
+
+@pytest.mark.parametrize("parts", [2, 3, 5])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_sequence_parallel_split_matches_oracle(lib, cuda_device, parts,
+                                                dtype):
+    d = inputs.chunk_inputs(2, 2, 64 * 9 + 40, 64, 128, dtype=dtype, seed=4,
+                            h0=True)
+    check(lib, cuda_device, d, dtype, sp_parts=parts)
+
+
+def test_sequence_parallel_more_parts_than_chunks(lib, cuda_device):
+    d = inputs.chunk_inputs(1, 2, 64 * 2 + 3, 64, 64, dtype="f32", seed=5,
+                            h0=True)
+    check(lib, cuda_device, d, "f32", sp_parts=6)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_packed_sequences_with_empty_and_short(lib, cuda_device, dtype):
+    lengths = [70, 0, 1, 64, 200, 3]
+    d = inputs.chunk_inputs(len(lengths), 2, 0, 128, 64, dtype=dtype, seed=6,
+                            h0=True, lengths=lengths)
+    check(lib, cuda_device, d, dtype)
+
+
+def test_packed_sequences_sequence_parallel(lib, cuda_device):
+    lengths = [300, 5, 640]
+    d = inputs.chunk_inputs(len(lengths), 2, 0, 64, 64, dtype="f32", seed=7,
+                            h0=True, lengths=lengths)
+    check(lib, cuda_device, d, "f32", sp_parts=3)
+
+
+def test_resume_through_final_state(lib, cuda_device):
+    d = inputs.chunk_inputs(2, 2, 300, 128, 128, dtype="f32", seed=8, h0=True)
+    x = to_dev(d, cuda_device)
+    o_all, h_all = lib.gdn_chunk_fwd_f32(x["q"], x["k"], x["v"], x["g"],
+                                         x["beta"], x["h0"])
+    t = 131
+    part = lambda a, s: a[:, s].contiguous()
+    o1, h1 = lib.gdn_chunk_fwd_f32(*(part(x[n], slice(0, t)) for n in
+                                     ("q", "k", "v", "g", "beta")), x["h0"])
+    o2, h2 = lib.gdn_chunk_fwd_f32(*(part(x[n], slice(t, None)) for n in
+                                     ("q", "k", "v", "g", "beta")), h1)
+    torch.cuda.synchronize()
+    o_cat = torch.cat([o1, o2], 1)
+    ref = o_all.double().cpu().numpy()
+    assert rel_err(o_cat, ref) <= 1e-4
+    assert rel_err(h2, h_all.double().cpu().numpy()) <= 1e-4
+
+
+def test_invalid_packing_is_reported_on_device(lib, cuda_device):
+    d = inputs.chunk_inputs(2, 1, 0, 64, 64, dtype="f32", seed=9,
+                            lengths=[10, 20])
+    x = to_dev(d, cuda_device)
+    cu = torch.tensor([0, 25, 20], dtype=torch.int32, device=cuda_device)
+    lib.gdn_device_status()  # clear
+    lib.gdn_chunk_fwd_f32(x["q"], x["k"], x["v"], x["g"], x["beta"], None,
+                          cu)
+    assert lib.gdn_device_status() == -1
+    assert lib.gdn_device_status() == 0  # cleared by the read
+
+
+# ---- decode step ----
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 64), (64, 128), (128, 128)])
+def test_recurrent_step_small(lib, cuda_device, dk, dv):
+    d = inputs.decode_inputs(7, 3, dk, dv, seed=10)
+    o_ref, s_ref = oracle.recurrent_step(d["q"], d["k"], d["v"], d["g"],
+                                         d["beta"], d["state"])
+    x = to_dev(d, cuda_device)
+    out = lib.gdn_recurrent_step(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                 x["state"])
+    torch.cuda.synchronize()
+    assert rel_err(out, o_ref) <= TOL["bf16"]
+    assert rel_err(x["state"], s_ref) <= 1e-5  # fp32 state, bf16 token
+
+
+def test_recurrent_step_matches_chunk_path_single_token(lib, cuda_device):
+    d = inputs.decode_inputs(4, 2, 128, 128, seed=11)
+    x = to_dev(d, cuda_device)
+    h0 = x["state"].clone()
+    o_c, h_c = lib.gdn_chunk_fwd(x["q"][:, None].contiguous(),
+                                 x["k"][:, None].contiguous(),
+                                 x["v"][:, None].contiguous(),
+                                 x["g"][:, None].contiguous(),
+                                 x["beta"][:, None].contiguous(), h0)
+    o_d = lib.gdn_recurrent_step(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                 x["state"])
+    torch.cuda.synchronize()
+    assert rel_err(x["state"], h_c.double().cpu().numpy()) <= 1e-4
+    assert rel_err(o_d, o_c[:, 0].double().cpu().numpy()) <= 2e-2
