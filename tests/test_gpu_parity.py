@@ -46,9 +46,16 @@ def run_gpu(lib, d, dev, dtype, variant=0, path=0, sp_parts=0, poison=True):
     return out, hT
 
 
+def oracle_variant(abi_variant):
+    """The ABI numbers gate placements 0 = decay first, 1 = decay after the
+    prediction; the oracle names them G1 and G0."""
+    return oracle.G1 if abi_variant == 0 else oracle.G0
+
+
 def check(lib, dev, d, dtype, variant=0, path=0, sp_parts=0):
     o_ref, h_ref = oracle.forward(d["q"], d["k"], d["v"], d["g"], d["beta"],
-                                  d["h0"], d["cu_seqlens"], variant=variant)
+                                  d["h0"], d["cu_seqlens"],
+                                  variant=oracle_variant(variant))
     out, hT = run_gpu(lib, d, dev, dtype, variant, path, sp_parts)
     eo, eh = rel_err(out, o_ref), rel_err(hT, h_ref)
     assert eo <= TOL[dtype], f"output rel err {eo:.3e}"
