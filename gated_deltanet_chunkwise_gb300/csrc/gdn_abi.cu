@@ -153,6 +153,23 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
 }
 
 }  // namespace
+
+int validate_chunk_args(const void* q, const void* k, const void* v,
+                        const float* g, const float* beta, const float* h0,
+                        const void* out, const float* hT,
+                        const int32_t* cu_seqlens, int B, int H, int T,
+                        int dk, int dv, int C, int dtype, int variant,
+                        int path, int sp_parts) {
+  return check_chunk_args(q, k, v, g, beta, h0, out, hT, cu_seqlens, B, H, T,
+                          dk, dv, C, dtype, variant, path, sp_parts);
+}
+
+int device_status_ptr(int** out) { return current_status_ptr(out); }
+
+cudaError_t count_launches(cudaError_t e, int launches) {
+  return counted(e, launches);
+}
+
 }  // namespace gdn
 
 extern "C" {

@@ -66,6 +66,16 @@ cudaError_t launch_chunk_simt(const ChunkParams& p, bool bf16,
 cudaError_t launch_sp_chain(const ChunkParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 
+// Host helpers owned by gdn_abi.cu.
+int validate_chunk_args(const void* q, const void* k, const void* v,
+                        const float* g, const float* beta, const float* h0,
+                        const void* out, const float* hT,
+                        const int32_t* cu_seqlens, int B, int H, int T,
+                        int dk, int dv, int C, int dtype, int variant,
+                        int path, int sp_parts);
+int device_status_ptr(int** out);
+cudaError_t count_launches(cudaError_t e, int launches);
+
 // Device-side helpers --------------------------------------------------------
 
 __device__ __forceinline__ float to_f32(float x) { return x; }

@@ -144,6 +144,45 @@ int gdn_recurrent_step(const void* q, const void* k, const void* v,
                        void* out, int N, int H, int dk, int dv,
                        gdn_stream_t stream);
 
+/*
+ * gdn_chunk_fwd_sp_noalloc -- the sequence-parallel forward pass of
+ * gdn_chunk_fwd_ex (path GDN_PATH_SIMT, sp_parts >= 2) for callers that may
+ * not allocate device memory while they enqueue work (for example a plugin
+ * of an inference engine whose memory plan is fixed in advance, or a serving
+ * loop under a fixed memory budget). The pages describe no such variant; it
+ * exists for this library's callers only.
+ *
+ * Instead of cudaMallocAsync it uses one fixed scratch array in device memory
+ * owned by the library: GDN_NOALLOC_SCRATCH_BYTES per device, held by every
+ * device that loads the library until the process exits. It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current and caches it; make
+ *     that first call before any stream capture on that device.
+ *   - Size limit: the request needs gdn_noalloc_scratch_bytes(B, H, dk, dv,
+ *     sp_parts) bytes; a request above GDN_NOALLOC_SCRATCH_BYTES returns
+ *     GDN_ERR_UNSUPPORTED and enqueues nothing. sp_parts < 2 returns
+ *     GDN_ERR_INVALID_ARG.
+ *   - Sharing: all calls on a device use the same array, which keeps the last
+ *     call's contents (every entry a call reads is written earlier in that
+ *     call). Calls that overlap on the GPU (different streams, or host
+ *     threads without ordering) race on it; the caller must serialise them.
+ * Arguments and results are those of gdn_chunk_fwd_ex (dtype, variant,
+ * sp_parts); other status codes as there.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)
+int gdn_chunk_fwd_sp_noalloc(const void* q, const void* k, const void* v,
+                             const float* g, const float* beta,
+                             const float* h0, void* out, float* hT,
+                             const int32_t* cu_seqlens, int B, int H, int T,
+                             int dk, int dv, int C, int dtype, int variant,
+                             int sp_parts, gdn_stream_t stream);
+
+/* Scratch bytes gdn_chunk_fwd_sp_noalloc needs for these sizes (0 when
+ * sp_parts < 2 or a size is not positive). */
+unsigned long long gdn_noalloc_scratch_bytes(int B, int H, int dk, int dv,
+                                             int sp_parts);
+
 /* gdn_device_status -- waits for `stream`, then returns and clears the
  * status recorded by kernels on the current device (GDN_OK, or the first
  * GDN_ERR_INVALID_ARG / GDN_ERR_TIMEOUT recorded since the last call). */
