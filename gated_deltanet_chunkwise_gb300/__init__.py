@@ -12,7 +12,7 @@ from __future__ import annotations
 _ABI_NAMES = (
     "gdn_chunk_fwd", "gdn_chunk_fwd_f32", "gdn_chunk_fwd_ex",
     "gdn_recurrent_step", "gdn_status_string", "GdnError", "library_path",
-    "library", "kernel_counters", "gdn_device_status",
+    "library", "kernel_counters", "gdn_device_status", "gdn_selftest_mma",
 )
 
 

@@ -121,14 +121,20 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
   p.variant = variant;
   p.status = status;
   const bool bf16 = dtype == GDN_DTYPE_BF16;
+  const long long tokens = cu_seqlens ? (long long)T : (long long)B * T;
+  const bool tc_ok = bf16 && chunk_tc_supported(dk, dv, tokens);
+  if (path == GDN_PATH_TCGEN05 && !tc_ok) return GDN_ERR_UNSUPPORTED;
+  const bool use_tc = tc_ok && path != GDN_PATH_SIMT;
+  auto launch = [&](const ChunkParams& q) {
+    return use_tc ? launch_chunk_tc(q, stream)
+                  : launch_chunk_simt(q, bf16, stream);
+  };
   const int parts = choose_parts(sp_parts, B, H, T, dv, C, cu_seqlens != nullptr);
   p.parts = parts;
 
   if (parts == 1) {
     p.part_begin = 0; p.part_count = 1; p.mode = kModeOutput;
-    return counted(launch_chunk_simt(p, bf16, stream), 1) == cudaSuccess
-               ? GDN_OK
-               : GDN_ERR_CUDA;
+    return counted(launch(p), 1) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
   }
 
   // Sequence-parallel: split pass, correction chain, corrected output pass.
@@ -142,11 +148,11 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
   p.ws_start = reinterpret_cast<float*>(static_cast<char*>(ws) + end_bytes);
   cudaError_t e;
   p.mode = kModeSplit; p.part_begin = 0; p.part_count = parts - 1;
-  e = counted(launch_chunk_simt(p, bf16, stream), 1);
+  e = counted(launch(p), 1);
   if (e == cudaSuccess && parts > 2) e = counted(launch_sp_chain(p, stream), 1);
   if (e == cudaSuccess) {
     p.mode = kModeOutput; p.part_begin = 1; p.part_count = parts - 1;
-    e = counted(launch_chunk_simt(p, bf16, stream), 1);
+    e = counted(launch(p), 1);
   }
   cudaError_t f = cudaFreeAsync(ws, stream);
   return (e == cudaSuccess && f == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;

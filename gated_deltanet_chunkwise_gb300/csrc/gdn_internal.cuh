@@ -64,6 +64,9 @@ struct DecodeParams {
 cudaError_t launch_chunk_simt(const ChunkParams& p, bool bf16,
                               cudaStream_t stream);
 cudaError_t launch_sp_chain(const ChunkParams& p, cudaStream_t stream);
+// Tensor-core (tcgen05) chunk kernel: bf16, dk = 128, dv in {64, 128}.
+bool chunk_tc_supported(int dk, int dv, long long tokens);
+cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 
 // Host helpers owned by gdn_abi.cu.

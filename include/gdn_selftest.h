@@ -1,0 +1,39 @@
+/*
+ * gdn_selftest.h -- self-test entry points of libgdn_gb300.so.
+ *
+ * Not part of the method: these exist so that a test suite can check, on the
+ * device, the building blocks the tensor-core kernels rely on (shared-memory
+ * tile layouts, tcgen05 descriptors, TMEM read-back) against a reference
+ * product computed elsewhere.
+ */
+#ifndef GDN_GB300_SELFTEST_H
+#define GDN_GB300_SELFTEST_H
+
+#include "gdn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * gdn_selftest_mma -- D = A * B (times 2 when `twice`) on one CTA with
+ * tcgen05.mma kind::f16 (M = 128, N = 64), using the shared-memory layouts of
+ * the chunk kernel.
+ *   A  bf16 [128, K] row-major (device)    B  bf16 [K, 64] row-major (device)
+ *   D  fp32 [128, 64] row-major (device, written)
+ *   K  64 or 128
+ *   a_mn       store A M-major (else K-major) before the MMA
+ *   b_mn       store B N-major (else K-major)
+ *   b_stacked  K-major B placed in the first 64 rows of a 128-row tile
+ *   twice      issue the MMA sequence twice with accumulation
+ * Returns GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_TIMEOUT (the completion wait
+ * gave up) or GDN_ERR_CUDA. Synchronises `stream`.
+ */
+int gdn_selftest_mma(const void* A, const void* B, float* D, int K, int a_mn,
+                     int b_mn, int b_stacked, int twice, gdn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_GB300_SELFTEST_H */

@@ -180,3 +180,41 @@ def test_recurrent_step_matches_chunk_path_single_token(lib, cuda_device):
     torch.cuda.synchronize()
     assert rel_err(x["state"], h_c.double().cpu().numpy()) <= 1e-4
     assert rel_err(o_d, o_c[:, 0].double().cpu().numpy()) <= 2e-2
+
+
+# ---- tensor-core (tcgen05) path, forced ----
+TC = 2
+
+
+@pytest.mark.parametrize("dv", [64, 128])
+@pytest.mark.parametrize("variant", [0, 1])
+def test_tensor_core_path(lib, cuda_device, dv, variant):
+    d = inputs.chunk_inputs(2, 3, 64 * 4 + 29, 128, dv, dtype="bf16", seed=12,
+                            h0=True)
+    check(lib, cuda_device, d, "bf16", variant=variant, path=TC)
+
+
+def test_tensor_core_alpha_one_single_chunk(lib, cuda_device):
+    d = inputs.chunk_inputs(1, 2, 64, 128, 128, dtype="bf16", seed=13,
+                            gated=False)
+    check(lib, cuda_device, d, "bf16", path=TC)
+
+
+@pytest.mark.parametrize("T", [1, 17, 63, 65, 128])
+def test_tensor_core_short_lengths(lib, cuda_device, T):
+    d = inputs.chunk_inputs(2, 2, T, 128, 128, dtype="bf16", seed=14, h0=True)
+    check(lib, cuda_device, d, "bf16", path=TC)
+
+
+@pytest.mark.parametrize("parts", [2, 3, 5])
+def test_tensor_core_sequence_parallel(lib, cuda_device, parts):
+    d = inputs.chunk_inputs(1, 2, 64 * 9 + 40, 128, 128, dtype="bf16", seed=15,
+                            h0=True)
+    check(lib, cuda_device, d, "bf16", path=TC, sp_parts=parts)
+
+
+def test_tensor_core_packed(lib, cuda_device):
+    lengths = [70, 0, 1, 64, 200, 3, 129]
+    d = inputs.chunk_inputs(len(lengths), 2, 0, 128, 128, dtype="bf16",
+                            seed=16, h0=True, lengths=lengths)
+    check(lib, cuda_device, d, "bf16", path=TC)

@@ -1,0 +1,35 @@
+"""Building blocks of the tensor-core kernel, checked on the device.
+
+gdn_selftest_mma lays out A [128, K] and B [K, 64] in shared memory exactly as
+the chunk kernel does (128-byte swizzle; K-major or M/N-major; a K-major B in
+the first rows of a 128-row stacked tile), runs the tcgen05 MMA sequence with
+the kernel's instruction descriptors and reads D back from TMEM. The
+reference is the fp32 product of the same bf16 values.
+"""
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+# (K, a_mn, b_mn, b_stacked): the operand forms of the chunk kernel's MMAs
+CASES = [
+    (128, False, False, True),   # [K;Q] K^T            (K-major A, K-major B)
+    (128, False, True, False),   # [K;Q^] S^T           (K-major A, N-major B)
+    (64, False, True, False),    # [T;0] R, [0;P] U     (K-major A, N-major B)
+    (64, True, True, False),     # Kbar^T U             (M-major A, N-major B)
+    (128, False, False, False),  # dense K-major B
+]
+
+
+@pytest.mark.parametrize("K,a_mn,b_mn,b_stacked", CASES)
+@pytest.mark.parametrize("twice", [False, True])
+def test_mma_layouts(lib, cuda_device, K, a_mn, b_mn, b_stacked, twice):
+    g = torch.Generator(device="cpu").manual_seed(K * 7 + a_mn * 3 + b_mn)
+    A = torch.randn(128, K, generator=g).to(torch.bfloat16)
+    B = torch.randn(K, 64, generator=g).to(torch.bfloat16)
+    ref = (A.double() @ B.double()) * (2 if twice else 1)
+    D = lib.gdn_selftest_mma(A.to(cuda_device), B.to(cuda_device), a_mn=a_mn,
+                             b_mn=b_mn, b_stacked=b_stacked, twice=twice)
+    torch.cuda.synchronize()
+    err = (D.double().cpu() - ref).abs().max().item()
+    assert err <= 1e-3 * ref.abs().max().item(), f"max abs err {err}"
