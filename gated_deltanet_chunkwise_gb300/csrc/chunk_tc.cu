@@ -63,11 +63,15 @@ constexpr uint32_t OFF_U = OFF_R + 8192;
 constexpr int AP = 68;  // fp32 row pitch of the solve buffers
 constexpr uint32_t OFF_AT = OFF_U + 8192;
 constexpr uint32_t OFF_TF = OFF_AT + 64 * AP * 4;
-constexpr int VEC_G = 0, VEC_ALPHA = 64, VEC_EG = 128, VEC_EGP = 192,
-              VEC_BETA = 256, VEC_DEC = 320, VEC_GAMMA = 384, VEC_FLOATS = 388;
+// Per-stage gate vectors written by the producer warp: cumulative log gate G,
+// alpha = e^g, e^G, e^{G'} beta (the prediction scale times beta), beta,
+// e^{G_L - G}, e^{-G}, gamma = e^{G_L}, and whether e^{G_r} e^{-G_j} stays in
+// the normal fp32 range for the whole chunk.
+constexpr int VEC_G = 0, VEC_ALPHA = 64, VEC_EG = 128, VEC_EGPB = 192,
+              VEC_BETA = 256, VEC_DEC = 320, VEC_IEG = 384, VEC_GAMMA = 448,
+              VEC_SAFE = 449, VEC_FLOATS = 452;
 constexpr uint32_t OFF_VEC = OFF_TF + 64 * AP * 4;
-constexpr uint32_t OFF_GB = OFF_VEC + 2 * VEC_FLOATS * 4;
-constexpr uint32_t OFF_BAR = OFF_GB + 2 * 128 * 4;
+constexpr uint32_t OFF_BAR = OFF_VEC + 2 * VEC_FLOATS * 4;
 
 enum {
   B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_MMA0, B_D0FREE, B_PREP, B_SREADY,
@@ -138,14 +142,18 @@ __device__ __forceinline__ void store_row_bf16(uint8_t* tile, int r,
   }
 }
 
-// Scale the 64 bf16 values of row r / column block cb of a swizzled tile.
+// Scale the 64 bf16 values of row r of a swizzled 128-byte-row tile (all
+// loads are issued before any store, so src may equal dst).
 __device__ __forceinline__ void scale_row_half(const uint8_t* src, uint8_t* dst,
                                                int r, float s) {
+  uint4 u[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    u[c] = *reinterpret_cast<const uint4*>(src + sw128(r, c));
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
-    uint4 u = *reinterpret_cast<const uint4*>(src + sw128(r, c));
     float f[8];
-    unpack_bf16x8(u, f);
+    unpack_bf16x8(u[c], f);
     uint4 w;
     w.x = pack_bf16x2(f[0] * s, f[1] * s);
     w.y = pack_bf16x2(f[2] * s, f[3] * s);
@@ -155,97 +163,131 @@ __device__ __forceinline__ void scale_row_half(const uint8_t* src, uint8_t* dst,
   }
 }
 
+__device__ __forceinline__ void load_vec64(const float* src, float (&x)[64]) {
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const float4 v = reinterpret_cast<const float4*>(src)[c];
+    x[4 * c] = v.x; x[4 * c + 1] = v.y; x[4 * c + 2] = v.z; x[4 * c + 3] = v.w;
+  }
+}
+
 // ---------------------------------------------------------------------------
-// (I + A)^{-1} for the strictly lower 64 x 64 A, stored transposed in At
-// (At[j][r] = A_rj, zero for r <= j). Result in Tf (lower triangle, unit
-// diagonal; entries above the diagonal are not meaningful except inside the
-// 32 x 32 diagonal blocks, whose upper parts stay zero). Blocked: the 16 x 16
-// diagonal blocks by forward substitution, then T_10 = -T_11 A_10 T_00 at
-// 16 and at 32. Products use the zero part of At (r < j) as scratch.
-// All 128 prep threads take part.
-__device__ __forceinline__ void solve_unit_lower(float* At, float* Tf,
+// Small tensor-core products for the triangular solve: mma.sync m16n8k8 with
+// tf32 inputs and fp32 accumulation, fragments loaded from row-major fp32
+// tiles of pitch AP (conflict-free for the A fragment since AP = 4 mod 32).
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+struct FragA { uint32_t a[4]; };
+struct FragB { uint32_t b[2]; };
+
+// 16 x 8 tile of a row-major matrix at (r0, c0).
+__device__ __forceinline__ FragA load_frag_a(const float* X, int r0, int c0,
+                                             int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  FragA f;
+  f.a[0] = to_tf32(X[(r0 + g) * AP + c0 + t]);
+  f.a[1] = to_tf32(X[(r0 + g + 8) * AP + c0 + t]);
+  f.a[2] = to_tf32(X[(r0 + g) * AP + c0 + t + 4]);
+  f.a[3] = to_tf32(X[(r0 + g + 8) * AP + c0 + t + 4]);
+  return f;
+}
+
+// 8 x 8 tile (k rows, n columns) of a row-major matrix at (k0, n0).
+__device__ __forceinline__ FragB load_frag_b(const float* X, int k0, int n0,
+                                             int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  FragB f;
+  f.b[0] = to_tf32(X[(k0 + t) * AP + n0 + g]);
+  f.b[1] = to_tf32(X[(k0 + t + 4) * AP + n0 + g]);
+  return f;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const FragA& a,
+                                         const FragB& b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a.a[0]), "r"(a.a[1]), "r"(a.a[2]), "r"(a.a[3]), "r"(b.b[0]),
+        "r"(b.b[1]));
+}
+
+// Store s * C (16 x 8 accumulator tile) at (r0, c0) of a row-major matrix.
+__device__ __forceinline__ void store_frag_c(float* X, int r0, int c0,
+                                             const float (&c)[4], float s,
+                                             int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  *reinterpret_cast<float2*>(X + (r0 + g) * AP + c0 + 2 * t) =
+      make_float2(s * c[0], s * c[1]);
+  *reinterpret_cast<float2*>(X + (r0 + g + 8) * AP + c0 + 2 * t) =
+      make_float2(s * c[2], s * c[3]);
+}
+
+// D(16 x 16 at (dr, dc)) = s * X(16 x K at (xr, xc)) Y(K x 16 at (yr, yc)).
+template <int K>
+__device__ __forceinline__ void mm16x16(float* D, int dr, int dc, const float* X,
+                                        int xr, int xc, const float* Y, int yr,
+                                        int yc, float s, int lane) {
+  float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < K; k += 8) {
+    const FragA a = load_frag_a(X, xr, xc + k, lane);
+    mma_tf32(c0, a, load_frag_b(Y, yr + k, yc, lane));
+    mma_tf32(c1, a, load_frag_b(Y, yr + k, yc + 8, lane));
+  }
+  store_frag_c(D, dr, dc, c0, s, lane);
+  store_frag_c(D, dr, dc + 8, c1, s, lane);
+}
+
+// (I + A)^{-1} for the strictly lower 64 x 64 A (row-major in Am, entries on
+// and above the diagonal zero). Result in Tf: lower triangle with unit
+// diagonal; the blocks above the 16 x 16 diagonal blocks that the products
+// read stay zero. Blocked in powers of two: the four 16 x 16 diagonal blocks
+// by substitution, then T_10 = -T_11 A_10 T_00 at 16 and at 32, the products
+// on the tensor cores (tf32). Scratch lives in the unused upper triangle of
+// Am. All 128 prep threads take part.
+__device__ __forceinline__ void solve_unit_lower(float* Am, float* Tf,
                                                  int tid) {
   const int warp = tid >> 5, lane = tid & 31;
-  // 1. diagonal 16 x 16 blocks, one per warp, one column per lane
+  // 1. diagonal 16 x 16 blocks: one per warp, lane l < 16 owns column l,
+  //    x_m = delta_ml - sum_{j<m} A_mj x_j
   if (lane < 16) {
     const int b = 16 * warp;
     float xs[16];
 #pragma unroll
-    for (int m = 0; m < 16; ++m) xs[m] = (m == lane) ? 1.f : 0.f;
+    for (int m = 0; m < 16; ++m) {
+      const float* arow = Am + (b + m) * AP + b;
+      float acc = (m == lane) ? 1.f : 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float xj = xs[j];
-      const float* arow = At + (b + j) * AP + b;  // A_{b+m, b+j}
-#pragma unroll
-      for (int m = j + 1; m < 16; ++m) xs[m] = fmaf(-arow[m], xj, xs[m]);
+      for (int j = 0; j < m; ++j) acc = fmaf(-arow[j], xs[j], acc);
+      xs[m] = acc;
     }
 #pragma unroll
     for (int m = 0; m < 16; ++m) Tf[(b + m) * AP + b + lane] = xs[m];
   }
   named_bar(1, 128);
-  // 2. merge pairs of 16-blocks: (0,1) by warps 0-1, (2,3) by warps 2-3
-  {
-    const int pair = warp >> 1;
-    const int kb = 32 * pair, rb = kb + 16;
-    const int pp = tid & 63, c = pp & 15, rg = pp >> 4;
-    float tcol[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) tcol[k] = Tf[(kb + k) * AP + kb + c];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r = rg * 4 + q;
-      float acc = 0.f;
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        acc = fmaf(At[(kb + k) * AP + rb + r], tcol[k], acc);
-      At[(kb + 16 + r) * AP + kb + c] = acc;  // X = A_10 T_00 (scratch)
-    }
-    named_bar(5 + pair, 64);
-    float xcol[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) xcol[k] = At[(kb + 16 + k) * AP + kb + c];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r = rg * 4 + q;
-      float acc = 0.f;
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        acc = fmaf(Tf[(rb + r) * AP + rb + k], xcol[k], acc);
-      Tf[(rb + r) * AP + kb + c] = -acc;
-    }
+  // 2. 16 -> 32: warp p in {0, 1} merges diagonal blocks (2p, 2p+1)
+  if (warp < 2) {
+    const int kb = 32 * warp;
+    // X = A_10 T_00 into the unused block (kb.., kb+16..) of Am
+    mm16x16<16>(Am, kb, kb + 16, Am, kb + 16, kb, Tf, kb, kb, 1.f, lane);
+    __syncwarp();
+    // T_10 = -T_11 X
+    mm16x16<16>(Tf, kb + 16, kb, Tf, kb + 16, kb + 16, Am, kb, kb + 16, -1.f,
+                lane);
   }
   named_bar(1, 128);
-  // 3. merge the two 32-blocks
+  // 3. 32 -> 64: X = A_21 T_11 (32 x 32, into Am rows 0-31, cols 32-63),
+  //    then T_21 = -T_22 X; warp w owns rows 16 (w >> 1), columns 16 (w & 1)
   {
-    const int c = tid & 31, rg = tid >> 5;
-    float tcol[32];
-#pragma unroll
-    for (int k = 0; k < 32; ++k) tcol[k] = Tf[k * AP + c];
-    float xv[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int r = rg * 8 + q;
-      float acc = 0.f;
-#pragma unroll
-      for (int k = 0; k < 32; ++k)
-        acc = fmaf(At[k * AP + 32 + r], tcol[k], acc);
-      xv[q] = acc;
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) At[(32 + rg * 8 + q) * AP + c] = xv[q];
+    const int mr = 16 * (warp >> 1), nc = 16 * (warp & 1);
+    mm16x16<32>(Am, mr, 32 + nc, Am, 32 + mr, 0, Tf, 0, nc, 1.f, lane);
     named_bar(1, 128);
-    float xcol[32];
-#pragma unroll
-    for (int k = 0; k < 32; ++k) xcol[k] = At[(32 + k) * AP + c];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int r = rg * 8 + q;
-      float acc = 0.f;
-#pragma unroll
-      for (int k = 0; k < 32; ++k)
-        acc = fmaf(Tf[(32 + r) * AP + 32 + k], xcol[k], acc);
-      Tf[(32 + r) * AP + c] = -acc;
-    }
+    mm16x16<32>(Tf, 32 + mr, nc, Tf, 32 + mr, 32, Am, 0, 32 + nc, -1.f, lane);
   }
   named_bar(1, 128);
 }
@@ -334,16 +376,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(st + ST_Q + ST_CB, &tmq, full, 64, h, tok);
         tma_load_3d(st + ST_V, &tmv, full, value_rows ? row0 : 0, h, tok);
       }
-      float* gb = reinterpret_cast<float*>(sm + OFF_GB) + s * 128;
-      for (int r = lane; r < C; r += 32) {
-        float gg = 0.f, bb = 0.f;
-        if (r < len) {
-          const size_t row = (size_t)(t0 + r) * H + h;
-          gg = p.g[row];
-          bb = p.beta[row];
+      // gate vectors of this chunk (tokens past the end: g = 0, beta = 0)
+      {
+        const unsigned fm = 0xffffffffu;
+        float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+        const size_t rbase = (size_t)t0 * H + h;
+        if (lane < len) {
+          g0 = p.g[rbase + (size_t)lane * H];
+          b0 = p.beta[rbase + (size_t)lane * H];
         }
-        gb[r] = gg;
-        gb[64 + r] = bb;
+        if (lane + 32 < len) {
+          g1 = p.g[rbase + (size_t)(lane + 32) * H];
+          b1 = p.beta[rbase + (size_t)(lane + 32) * H];
+        }
+        float s0 = g0, s1 = g1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float u0 = __shfl_up_sync(fm, s0, o);
+          const float u1 = __shfl_up_sync(fm, s1, o);
+          if (lane >= o) {
+            s0 += u0;
+            s1 += u1;
+          }
+        }
+        s1 += __shfl_sync(fm, s0, 31);
+        const float Gl = __shfl_sync(fm, s1, 31);
+        const float p0 = VARIANT == GDN_GATE_BEFORE_PREDICT ? s0 : s0 - g0;
+        const float p1 = VARIANT == GDN_GATE_BEFORE_PREDICT ? s1 : s1 - g1;
+        const bool in_range =
+            __all_sync(fm, s0 >= -87.f && s0 <= 87.f && s1 >= -87.f && s1 <= 87.f);
+        float* vec = reinterpret_cast<float*>(sm + OFF_VEC) + s * VEC_FLOATS;
+        vec[VEC_G + lane] = s0;
+        vec[VEC_G + 32 + lane] = s1;
+        vec[VEC_ALPHA + lane] = expf(g0);
+        vec[VEC_ALPHA + 32 + lane] = expf(g1);
+        vec[VEC_EG + lane] = expf(s0);
+        vec[VEC_EG + 32 + lane] = expf(s1);
+        vec[VEC_EGPB + lane] = expf(p0) * b0;
+        vec[VEC_EGPB + 32 + lane] = expf(p1) * b1;
+        vec[VEC_BETA + lane] = b0;
+        vec[VEC_BETA + 32 + lane] = b1;
+        vec[VEC_DEC + lane] = expf(Gl - s0);
+        vec[VEC_DEC + 32 + lane] = expf(Gl - s1);
+        vec[VEC_IEG + lane] = expf(-s0);
+        vec[VEC_IEG + 32 + lane] = expf(-s1);
+        if (lane == 0) {
+          vec[VEC_GAMMA] = expf(Gl);
+          vec[VEC_SAFE] = in_range ? 1.f : 0.f;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(full);
@@ -434,86 +514,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lanes = (uint32_t)(32 * warp) << 16;
     for (int j = 0; j < nloc; ++j) {
       const int s = j & 1;
-      float* vec = reinterpret_cast<float*>(sm + OFF_VEC) + s * VEC_FLOATS;
-      const float* gb = reinterpret_cast<const float*>(sm + OFF_GB) + s * 128;
+      const float* vec =
+          reinterpret_cast<const float*>(sm + OFF_VEC) + s * VEC_FLOATS;
       uint8_t* st = sm + OFF_STAGE + s * STAGE_BYTES;
       uint8_t* tp = sm + OFF_TP + s * TP_BYTES;
-      // the stage's TMA data and gates (full) and the K K^T / Q K^T product
+      // the stage's TMA data and gate vectors (full), and K K^T / Q K^T
       bool ok = mbar_wait(&bars[B_FULL0 + s], (j >> 1) & 1, abort_flag) &&
                 mbar_wait(&bars[B_MMA0], j & 1, abort_flag);
       if (!bar_and(1, 128, ok)) break;
       tc_fence_after();
-      if (warp == 0) {
-        // chunk-local gate prefixes (inclusive scan of g over 64 tokens)
-        const unsigned full = 0xffffffffu;
-        const float g0 = gb[lane], g1 = gb[lane + 32];
-        float s0 = g0, s1 = g1;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float t0 = __shfl_up_sync(full, s0, o);
-          const float t1 = __shfl_up_sync(full, s1, o);
-          if (lane >= o) {
-            s0 += t0;
-            s1 += t1;
-          }
-        }
-        s1 += __shfl_sync(full, s0, 31);
-        const float Gl = __shfl_sync(full, s1, 31);
-        vec[VEC_G + lane] = s0;
-        vec[VEC_G + 32 + lane] = s1;
-        vec[VEC_ALPHA + lane] = expf(g0);
-        vec[VEC_ALPHA + 32 + lane] = expf(g1);
-        vec[VEC_EG + lane] = expf(s0);
-        vec[VEC_EG + 32 + lane] = expf(s1);
-        const float p0 = VARIANT == GDN_GATE_BEFORE_PREDICT ? s0 : s0 - g0;
-        const float p1 = VARIANT == GDN_GATE_BEFORE_PREDICT ? s1 : s1 - g1;
-        vec[VEC_EGP + lane] = expf(p0);
-        vec[VEC_EGP + 32 + lane] = expf(p1);
-        vec[VEC_BETA + lane] = gb[64 + lane];
-        vec[VEC_BETA + 32 + lane] = gb[96 + lane];
-        vec[VEC_DEC + lane] = expf(Gl - s0);
-        vec[VEC_DEC + 32 + lane] = expf(Gl - s1);
-        if (lane == 0) vec[VEC_GAMMA] = expf(Gl);
-      }
       float x[64];
       tmem_ld64(tmem + TM_D0 + lanes, x);
       tc_fence_before();
       mbar_arrive(&bars[B_D0FREE]);
       ok = j < 2 || mbar_wait(&bars[B_TPFREE0 + s], ((j >> 1) - 1) & 1,
                               abort_flag);
-      if (!bar_and(1, 128, ok)) break;  // also publishes vec
-      const float* alpha = vec + VEC_ALPHA;
+      if (!bar_and(1, 128, ok)) break;
+      const bool safe = vec[VEC_SAFE] != 0.f;
+      // w = e^{-G} (factored decays) or alpha (running products)
+      float w[64];
+      load_vec64(vec + (safe ? VEC_IEG : VEC_ALPHA), w);
       if (tid < 64) {
-        // row r of A: beta_r exp(G'_r - G_j) k_r.k_j for j < r
+        // row r of A (row-major): beta_r exp(G'_r - G_j) k_r.k_j for j < r
         const int r = tid;
-        const float br = vec[VEC_BETA + r];
-        float d = 1.f;
+        if (safe) {
+          const float er = vec[VEC_EGPB + r];
 #pragma unroll
-        for (int jj = 63; jj >= 0; --jj) {
-          float a = 0.f;
-          if (jj < r) {
-            if (VARIANT == GDN_GATE_BEFORE_PREDICT) {
-              d *= alpha[jj + 1];
-              a = br * d * x[jj];
-            } else {
-              a = br * d * x[jj];
-              d *= alpha[jj];
+          for (int jj = 0; jj < 64; ++jj) x[jj] = jj < r ? er * w[jj] * x[jj] : 0.f;
+        } else {
+          const float br = vec[VEC_BETA + r];
+          float d = 1.f;
+          x[63] = 0.f;
+#pragma unroll
+          for (int jj = 62; jj >= 0; --jj) {
+            float a = 0.f;
+            if (jj < r) {
+              if (VARIANT == GDN_GATE_BEFORE_PREDICT) {
+                d *= w[jj + 1];
+                a = br * d * x[jj];
+              } else {
+                a = br * d * x[jj];
+                d *= w[jj];
+              }
             }
+            x[jj] = a;
           }
-          At[jj * AP + r] = a;
         }
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4)
+          *reinterpret_cast<float4*>(At + r * AP + 4 * c4) =
+              make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
       } else {
         // row r of P: exp(G_r - G_j) q_r.k_j for j <= r
         const int r = tid - 64;
-        float d = 1.f;
+        if (safe) {
+          const float er = vec[VEC_EG + r];
 #pragma unroll
-        for (int jj = 63; jj >= 0; --jj) {
-          float pv = 0.f;
-          if (jj <= r) {
-            pv = d * x[jj];
-            d *= alpha[jj];
+          for (int jj = 0; jj < 64; ++jj) x[jj] = jj <= r ? er * w[jj] * x[jj] : 0.f;
+        } else {
+          float d = 1.f;
+#pragma unroll
+          for (int jj = 63; jj >= 0; --jj) {
+            float pv = 0.f;
+            if (jj <= r) {
+              pv = d * x[jj];
+              d *= w[jj];
+            }
+            x[jj] = pv;
           }
-          x[jj] = pv;
         }
         store_row_bf16(tp + TP_P, r, x);
       }
@@ -528,21 +596,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         // T -> bf16 rows 0-63 of [T;0]
         const int r = tid >> 1, hh = tid & 1;
+        float f[32];
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 t4 =
+              *reinterpret_cast<const float4*>(Tf + r * AP + hh * 32 + 4 * c4);
+          f[4 * c4] = t4.x; f[4 * c4 + 1] = t4.y;
+          f[4 * c4 + 2] = t4.z; f[4 * c4 + 3] = t4.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = hh * 32 + e;
+          f[e] = col < r ? f[e] : (col == r ? 1.f : 0.f);
+        }
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          const int cc = hh * 4 + q4;
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int col = cc * 8 + e;
-            f[e] = col < r ? Tf[r * AP + col] : (col == r ? 1.f : 0.f);
-          }
-          uint4 w;
-          w.x = pack_bf16x2(f[0], f[1]);
-          w.y = pack_bf16x2(f[2], f[3]);
-          w.z = pack_bf16x2(f[4], f[5]);
-          w.w = pack_bf16x2(f[6], f[7]);
-          *reinterpret_cast<uint4*>(tp + TP_T + sw128(r, cc)) = w;
+          uint4 u;
+          u.x = pack_bf16x2(f[8 * q4 + 0], f[8 * q4 + 1]);
+          u.y = pack_bf16x2(f[8 * q4 + 2], f[8 * q4 + 3]);
+          u.z = pack_bf16x2(f[8 * q4 + 4], f[8 * q4 + 5]);
+          u.w = pack_bf16x2(f[8 * q4 + 6], f[8 * q4 + 7]);
+          *reinterpret_cast<uint4*>(tp + TP_T + sw128(r, hh * 4 + q4)) = u;
         }
       }
       ok = j == 0 || mbar_wait(&bars[B_KBFREE], (j - 1) & 1, abort_flag);
@@ -609,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           float ks[64];
           tmem_ld64(tmem + TM_D1 + 64 * b + lanes, ks);
-          const float e = vec[VEC_EGP + r], be = vec[VEC_BETA + r];
+          const float ebe = vec[VEC_EGPB + r], be = vec[VEC_BETA + r];
           const uint8_t* vt = sm + OFF_STAGE + s * STAGE_BYTES + ST_V;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -622,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int e8 = 0; e8 < 8; ++e8)
-              ks[8 * c + e8] = be * fmaf(-e, ks[8 * c + e8], f[e8]);
+              ks[8 * c + e8] = fmaf(-ebe, ks[8 * c + e8], be * f[e8]);
           }
           store_row_bf16(sm + OFF_R, r, ks);
           fence_proxy_async();

@@ -178,8 +178,10 @@ def test_recurrent_step_matches_chunk_path_single_token(lib, cuda_device):
     o_d = lib.gdn_recurrent_step(x["q"], x["k"], x["v"], x["g"], x["beta"],
                                  x["state"])
     torch.cuda.synchronize()
-    assert rel_err(x["state"], h_c.double().cpu().numpy()) <= 1e-4
-    assert rel_err(o_d, o_c[:, 0].double().cpu().numpy()) <= 2e-2
+    # the bf16 chunk path multiplies by a bf16 copy of the state, so the two
+    # agree to the bf16 parity bound, not to fp32 rounding
+    assert rel_err(x["state"], h_c.double().cpu().numpy()) <= TOL["bf16"]
+    assert rel_err(o_d, o_c[:, 0].double().cpu().numpy()) <= TOL["bf16"]
 
 
 # ---- tensor-core (tcgen05) path, forced ----
@@ -217,4 +219,24 @@ def test_tensor_core_packed(lib, cuda_device):
     lengths = [70, 0, 1, 64, 200, 3, 129]
     d = inputs.chunk_inputs(len(lengths), 2, 0, 128, 128, dtype="bf16",
                             seed=16, h0=True, lengths=lengths)
+    check(lib, cuda_device, d, "bf16", path=TC)
+
+
+@pytest.mark.parametrize("path", [1, TC])
+def test_strong_gates_chunk_decay_beyond_fp32_range(lib, cuda_device, path):
+    """Log-gates ~6x stronger than the workload's, so a chunk's total decay
+    exceeds e^-87: the tensor-core kernel must switch from factored decays
+    e^{G_r} e^{-G_j} to running products without overflow."""
+    d = inputs.chunk_inputs(2, 2, 64 * 3 + 11, 128, 128, dtype="bf16",
+                            seed=17, h0=True)
+    d["g"] = d["g"] * 6.0
+    check(lib, cuda_device, d, "bf16", path=path)
+
+
+def test_mixed_gate_strength_across_chunks(lib, cuda_device):
+    """Weak gates in one chunk, strong in the next: per-chunk path choice."""
+    d = inputs.chunk_inputs(1, 2, 64 * 4, 128, 64, dtype="bf16", seed=18,
+                            h0=True)
+    d["g"][:, 64:128] *= 8.0
+    d["g"][:, 192:] *= 5.0
     check(lib, cuda_device, d, "bf16", path=TC)
