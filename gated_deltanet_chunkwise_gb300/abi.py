@@ -69,7 +69,7 @@ def library():
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_version.restype = i
     lib.gdn_kernel_launches.restype = ctypes.c_ulonglong
-    lib.gdn_selftest_mma.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+    lib.gdn_selftest_mma.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp]
     lib.gdn_selftest_mma.restype = i
     _lib = lib
     return lib
@@ -211,16 +211,16 @@ def gdn_recurrent_step(q, k, v, g, beta, state, *, out=None, stream=None):
 def gdn_selftest_mma(A, B, *, a_mn=False, b_mn=False, b_stacked=False,
                      twice=False, stream=None):
     """D = A @ B (x2 when ``twice``) through one tcgen05 MMA sequence with the
-    chunk kernel's shared-memory layouts. A bf16 [128, K], B bf16 [K, 64]."""
+    chunk kernel's shared-memory layouts. A bf16 [128, K], B bf16 [K, N]."""
     dev = A.device
     _need(A, "A", torch.bfloat16, None)
     _need(B, "B", torch.bfloat16, dev)
-    K = A.shape[1]
-    if A.shape != (128, K) or B.shape != (K, 64):
-        raise ValueError("A must be [128, K] and B [K, 64]")
-    D = torch.empty((128, 64), dtype=torch.float32, device=dev)
+    K, N = A.shape[1], B.shape[1]
+    if A.shape != (128, K) or B.shape != (K, N):
+        raise ValueError("A must be [128, K] and B [K, N]")
+    D = torch.empty((128, N), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
-        rc = library().gdn_selftest_mma(_ptr(A), _ptr(B), _ptr(D), K,
+        rc = library().gdn_selftest_mma(_ptr(A), _ptr(B), _ptr(D), K, N,
                                         int(a_mn), int(b_mn), int(b_stacked),
                                         int(twice), _stream(stream))
     if rc != GDN_OK:

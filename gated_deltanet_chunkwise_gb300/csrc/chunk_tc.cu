@@ -4,29 +4,30 @@
 // walks the sequence's chunks (C = 64, d_k = 128) in order. The state is kept
 // transposed, S^T (d_k x 64), in fp32 registers of the "chain" warpgroup (one
 // d_k row per thread) and mirrored as bf16 in shared memory for the MMAs.
-// Per chunk (illustrated DeltaNet walk-through: UT transform, chunkwise state
-// passing and output; scalar gate prefixes of its GLA section):
+// Per chunk (illustrated DeltaNet walk-through: UT transform, WY
+// representation, chunkwise state passing and output; scalar gate prefixes
+// of its GLA section), with D_rj = exp(G_r - G_j), G the chunk-local
+// cumulative log gate, and G' = G (decay first) or G_{r-1} (decay after the
+// prediction):
 //
-//   MMA0  [K;Q] K^T           -> K K^T (rows 0-63), Q K^T (rows 64-127)
-//   prep  A = strict_lower(diag(beta) K K^T (.) D'),  T = (I + A)^{-1}
-//         P = (Q K^T) (.) D (.) M_incl,  Q^ = diag(e^G) Q,  Kbar = diag(e^{G_L-G}) K
-//   MMA1  [K;Q^] S^T          -> K S^T, Q^ S^T  (history read)
-//   chain R = diag(beta) (V - diag(e^{G'}) K S^T)
-//   MMA2  [T;0] R             -> U = T R  (= U0 - W S^T of the WY form)
-//   MMA3  Kbar^T U            -> Delta;  S^T <- gamma S^T + Delta
-//   MMA4  [0;P] U  (accumulated onto the history read) -> O = Q^ S^T + P U
+//   prep   MMA0  [K;Q] K^T -> K K^T, Q K^T
+//          A = strict_lower(diag(beta) K K^T (.) D'),  T = (I + A)^{-1}
+//          P = (Q K^T) (.) D (.) M_incl,  Q^ = diag(e^G) Q,
+//          K' = diag(beta e^{G'}) K,  V' = diag(beta) V,  Kbar = diag(e^{G_L-G}) K
+//          MMA   [T;T] K' -> W (twice);   [T;0] V' -> U0 into the chunk's
+//                accumulator; -W replaces K in the stage tile: [-W;Q^]
+//   chain  MMA1  accumulator += [-W;Q^] S^T -> U = U0 - W S^T, Q^ S^T
+//          MMA2  Kbar^T U -> Delta;  S^T <- gamma S^T + Delta
+//          MMA3  accumulator += [0;P] U -> O = Q^ S^T + P U
 //
-// Folding W into U = T diag(beta)(V - diag(e^{G'}) K S^T) is the same algebra
-// as U = U0 - W S^T with U0 = T diag(beta) V, W = T diag(beta e^{G'}) K; it
-// removes the W product and its store. D_rj = exp(G_r - G_j) with G the
-// chunk-local cumulative log gate, D' and G' take G_{r-1} for
-// GDN_GATE_AFTER_PREDICT. Decays are formed as running products of alpha, so
-// no exponent is ever positive.
+// so the serial chain per chunk is two MMA round trips and two short
+// register phases; everything else overlaps it.
 //
-// Warp roles (320 threads): warps 0-3 prep, 4-7 chain, 8 TMA producer, 9 MMA
-// issuer. Operand tiles are bf16 with the 128-byte swizzle; K/Q/V arrive by
-// TMA in a two-stage ring. Every wait is bounded; a CTA that gives up records
-// GDN_ERR_TIMEOUT, drains its MMAs, frees its TMEM and exits.
+// Warp roles (320 threads): warps 0-3 prep, 4-7 chain, 8 TMA producer (also
+// the chunk's gate vectors), 9 MMA issuer (an event loop that gives the chain's
+// MMAs priority). Operand tiles are bf16 with the 128-byte swizzle; K/Q/V
+// arrive by TMA in a two-stage ring. Every wait is bounded; a CTA that gives
+// up records GDN_ERR_TIMEOUT, drains its MMAs, frees its TMEM and exits.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -45,57 +46,59 @@ constexpr int DVT = 64;
 constexpr int kThreads = 320;
 
 // Stage: [K;Q] stacked K-major tile (two 16 KB column blocks of 64 columns;
-// rows 0-63 K, rows 64-127 Q) followed by the V tile (64 x 64).
+// rows 0-63 K (later -W), rows 64-127 Q (later Q^)), then the V tile (later V').
 constexpr uint32_t ST_K = 0;
 constexpr uint32_t ST_Q = 8192;
 constexpr uint32_t ST_CB = 16384;
 constexpr uint32_t ST_V = 32768;
 constexpr uint32_t STAGE_BYTES = 40960;
-// T | 0 | P buffer: [T;0] and [0;P] are both 128-row K-major tiles.
-constexpr uint32_t TP_T = 0, TP_Z = 8192, TP_P = 16384, TP_BYTES = 24576;
+// T buffer: T, a copy of T, zeros, P (even chunks), zeros, P (odd chunks);
+// [T;T], [T;0], [0;P0] and [0;P1] are 128-row K-major tiles.
+constexpr uint32_t TB_T = 0, TB_T2 = 8192, TB_Z = 16384, TB_P0 = 24576,
+                   TB_Z2 = 32768, TB_P1 = 40960, TB_BYTES = 49152;
 
 constexpr uint32_t OFF_STAGE = 0;
-constexpr uint32_t OFF_TP = 2 * STAGE_BYTES;
-constexpr uint32_t OFF_KBAR = OFF_TP + 2 * TP_BYTES;
-constexpr uint32_t OFF_S = OFF_KBAR + 16384;
-constexpr uint32_t OFF_R = OFF_S + 16384;
-constexpr uint32_t OFF_U = OFF_R + 8192;
-constexpr int AP = 68;  // fp32 row pitch of the solve buffers
-constexpr uint32_t OFF_AT = OFF_U + 8192;
-constexpr uint32_t OFF_TF = OFF_AT + 64 * AP * 4;
+constexpr uint32_t OFF_TB = 2 * STAGE_BYTES;               // 81920
+constexpr uint32_t OFF_KBAR = OFF_TB + TB_BYTES;           // 2 x 16 KB
+constexpr uint32_t OFF_KP = OFF_KBAR + 2 * 16384;          // K'
+constexpr uint32_t OFF_S = OFF_KP + 16384;
+constexpr uint32_t OFF_U = OFF_S + 16384;
+constexpr int AP = 68;  // fp32 row pitch of the solve buffer
+constexpr uint32_t OFF_AT = OFF_U + 8192;                  // A, then T (fp32)
 // Per-stage gate vectors written by the producer warp: cumulative log gate G,
-// alpha = e^g, e^G, e^{G'} beta (the prediction scale times beta), beta,
-// e^{G_L - G}, e^{-G}, gamma = e^{G_L}, and whether e^{G_r} e^{-G_j} stays in
-// the normal fp32 range for the whole chunk.
+// alpha = e^g, e^G, beta e^{G'}, beta, e^{G_L - G}, e^{-G}, gamma = e^{G_L},
+// and whether e^{G_r} e^{-G_j} stays in the normal fp32 range.
 constexpr int VEC_G = 0, VEC_ALPHA = 64, VEC_EG = 128, VEC_EGPB = 192,
               VEC_BETA = 256, VEC_DEC = 320, VEC_IEG = 384, VEC_GAMMA = 448,
               VEC_SAFE = 449, VEC_FLOATS = 452;
-constexpr uint32_t OFF_VEC = OFF_TF + 64 * AP * 4;
+constexpr uint32_t OFF_VEC = OFF_AT + 64 * AP * 4;
 constexpr uint32_t OFF_BAR = OFF_VEC + 2 * VEC_FLOATS * 4;
 
 enum {
-  B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_MMA0, B_D0FREE, B_PREP, B_SREADY,
-  B_D1FULL0, B_D1FULL1, B_RREADY, B_UFULL, B_UREADY, B_D2FULL, B_D3FULL0,
-  B_D3FULL1, B_D1FREE0, B_D1FREE1, B_TPFREE0, B_TPFREE1, B_KBFREE, B_DRAIN,
-  NBARS
+  B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_MMA0, B_D0FREE, B_PREPT, B_WDONE,
+  B_PREPD0, B_PREPD1, B_SREADY, B_D1FULL0, B_D1FULL1, B_UREADY, B_D2FULL,
+  B_D3FULL0, B_D3FULL1, B_D1FREE0, B_D1FREE1, B_TPFREE0, B_TPFREE1,
+  B_KBFREE0, B_KBFREE1, B_DRAIN, NBARS
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // TMEM columns (fp32 accumulators, 128 lanes each).
-constexpr uint32_t TM_D0 = 0, TM_D1 = 64, TM_DTR = 192, TM_D2 = 256;
+constexpr uint32_t TM_D0 = 0, TM_D1 = 64, TM_DW = 192, TM_D2 = 320;
 constexpr uint32_t TMEM_COLS = 512;
 
 constexpr uint32_t ID_KK = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_KMN = idesc_bf16(128, 64, false, true);
+constexpr uint32_t ID_KMN128 = idesc_bf16(128, 128, false, true);
 constexpr uint32_t ID_MNMN = idesc_bf16(128, 64, true, true);
 
 __device__ __forceinline__ uint32_t bar_count(int b) {
   switch (b) {
     case B_FULL0: case B_FULL1: return 2;
-    case B_D0FREE: case B_PREP: case B_SREADY: return 128;
-    case B_RREADY: case B_UREADY: case B_D1FREE0: case B_D1FREE1: return 64;
+    case B_D0FREE: case B_PREPT: case B_PREPD0: case B_PREPD1: case B_SREADY:
+      return 128;
+    case B_UREADY: case B_D1FREE0: case B_D1FREE1: return 64;
     default: return 1;
   }
 }
@@ -243,51 +246,54 @@ __device__ __forceinline__ void mm16x16(float* D, int dr, int dc, const float* X
   store_frag_c(D, dr, dc + 8, c1, s, lane);
 }
 
-// (I + A)^{-1} for the strictly lower 64 x 64 A (row-major in Am, entries on
-// and above the diagonal zero). Result in Tf: lower triangle with unit
-// diagonal; the blocks above the 16 x 16 diagonal blocks that the products
-// read stay zero. Blocked in powers of two: the four 16 x 16 diagonal blocks
-// by substitution, then T_10 = -T_11 A_10 T_00 at 16 and at 32, the products
-// on the tensor cores (tf32). Scratch lives in the unused upper triangle of
-// Am. All 128 prep threads take part.
-__device__ __forceinline__ void solve_unit_lower(float* Am, float* Tf,
-                                                 int tid) {
+// (I + A)^{-1} for the strictly lower 64 x 64 A, in place: on entry AT holds
+// A row-major (zeros on and above the diagonal), on exit its lower triangle
+// holds T with a unit diagonal, and its 16 x 16 blocks above the diagonal
+// blocks are zero except the upper-right 32 x 32 block, which is scratch.
+// Blocked in powers of two: the four 16 x 16 diagonal blocks by substitution,
+// then T_10 = -T_11 A_10 T_00 at 16 and at 32 with the products on the tensor
+// cores (tf32). All 128 prep threads take part.
+__device__ __forceinline__ void solve_unit_lower(float* AT, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
   // 1. diagonal 16 x 16 blocks: one per warp, lane l < 16 owns column l,
   //    x_m = delta_ml - sum_{j<m} A_mj x_j
-  if (lane < 16) {
+  {
     const int b = 16 * warp;
     float xs[16];
+    if (lane < 16) {
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float* arow = Am + (b + m) * AP + b;
-      float acc = (m == lane) ? 1.f : 0.f;
+      for (int m = 0; m < 16; ++m) {
+        const float* arow = AT + (b + m) * AP + b;
+        float acc = (m == lane) ? 1.f : 0.f;
 #pragma unroll
-      for (int j = 0; j < m; ++j) acc = fmaf(-arow[j], xs[j], acc);
-      xs[m] = acc;
+        for (int j = 0; j < m; ++j) acc = fmaf(-arow[j], xs[j], acc);
+        xs[m] = acc;
+      }
     }
+    __syncwarp();  // the whole block is read before it is overwritten
+    if (lane < 16) {
 #pragma unroll
-    for (int m = 0; m < 16; ++m) Tf[(b + m) * AP + b + lane] = xs[m];
+      for (int m = 0; m < 16; ++m) AT[(b + m) * AP + b + lane] = xs[m];
+    }
   }
   named_bar(1, 128);
-  // 2. 16 -> 32: warp p in {0, 1} merges diagonal blocks (2p, 2p+1)
+  // 2. 16 -> 32: warp p in {0, 1} merges diagonal blocks (2p, 2p+1); the
+  //    product X = A_10 T_00 goes to rows 16p.., columns 32+16p.. (scratch)
   if (warp < 2) {
-    const int kb = 32 * warp;
-    // X = A_10 T_00 into the unused block (kb.., kb+16..) of Am
-    mm16x16<16>(Am, kb, kb + 16, Am, kb + 16, kb, Tf, kb, kb, 1.f, lane);
+    const int kb = 32 * warp, xr = 16 * warp, xc = 32 + 16 * warp;
+    mm16x16<16>(AT, xr, xc, AT, kb + 16, kb, AT, kb, kb, 1.f, lane);
     __syncwarp();
-    // T_10 = -T_11 X
-    mm16x16<16>(Tf, kb + 16, kb, Tf, kb + 16, kb + 16, Am, kb, kb + 16, -1.f,
+    mm16x16<16>(AT, kb + 16, kb, AT, kb + 16, kb + 16, AT, xr, xc, -1.f,
                 lane);
   }
   named_bar(1, 128);
-  // 3. 32 -> 64: X = A_21 T_11 (32 x 32, into Am rows 0-31, cols 32-63),
-  //    then T_21 = -T_22 X; warp w owns rows 16 (w >> 1), columns 16 (w & 1)
+  // 3. 32 -> 64: X = A_21 T_11 into rows 0-31, columns 32-63, then
+  //    T_21 = -T_22 X; warp w owns rows 16 (w >> 1), columns 16 (w & 1)
   {
     const int mr = 16 * (warp >> 1), nc = 16 * (warp & 1);
-    mm16x16<32>(Am, mr, 32 + nc, Am, 32 + mr, 0, Tf, 0, nc, 1.f, lane);
+    mm16x16<32>(AT, mr, 32 + nc, AT, 32 + mr, 0, AT, 0, nc, 1.f, lane);
     named_bar(1, 128);
-    mm16x16<32>(Tf, 32 + mr, nc, Tf, 32 + mr, 32, Am, 0, 32 + nc, -1.f, lane);
+    mm16x16<32>(AT, 32 + mr, nc, AT, 32 + mr, 32, AT, 0, 32 + nc, -1.f, lane);
   }
   named_bar(1, 128);
 }
@@ -331,14 +337,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (tid < 128) {
-    // zero blocks of both T|0|P buffers and the whole fp32 T buffer
-    uint4 z = make_uint4(0, 0, 0, 0);
-    for (int i = tid; i < 2 * 512; i += 128) {
-      const int b = i >> 9, e = i & 511;
-      *reinterpret_cast<uint4*>(sm + OFF_TP + b * TP_BYTES + TP_Z + e * 16) = z;
+    // the two zero blocks of the T buffer
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < 1024; i += 128) {
+      const uint32_t off = (i < 512 ? TB_Z : TB_Z2) + (uint32_t)(i & 511) * 16;
+      *reinterpret_cast<uint4*>(sm + OFF_TB + off) = z;
     }
-    for (int i = tid; i < 64 * AP / 4; i += 128)
-      reinterpret_cast<uint4*>(sm + OFF_TF)[i] = z;
   }
   if (warp == 9) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 8) {
-    // ================= TMA producer =================
+    // ================= TMA producer + gate vectors =================
     int issued = 0;
     for (int i = 0; i < nloc; ++i) {
       const int s = i & 1;
@@ -376,8 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(st + ST_Q + ST_CB, &tmq, full, 64, h, tok);
         tma_load_3d(st + ST_V, &tmv, full, value_rows ? row0 : 0, h, tok);
       }
-      // gate vectors of this chunk (tokens past the end: g = 0, beta = 0)
       {
+        // gate vectors (tokens past the end: g = 0, beta = 0)
         const unsigned fm = 0xffffffffu;
         float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
         const size_t rbase = (size_t)t0 * H + h;
@@ -403,8 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float Gl = __shfl_sync(fm, s1, 31);
         const float p0 = VARIANT == GDN_GATE_BEFORE_PREDICT ? s0 : s0 - g0;
         const float p1 = VARIANT == GDN_GATE_BEFORE_PREDICT ? s1 : s1 - g1;
-        const bool in_range =
-            __all_sync(fm, s0 >= -87.f && s0 <= 87.f && s1 >= -87.f && s1 <= 87.f);
+        const bool in_range = __all_sync(
+            fm, s0 >= -87.f && s0 <= 87.f && s1 >= -87.f && s1 <= 87.f);
         float* vec = reinterpret_cast<float*>(sm + OFF_VEC) + s * VEC_FLOATS;
         vec[VEC_G + lane] = s0;
         vec[VEC_G + 32 + lane] = s1;
@@ -434,74 +438,96 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = max(0, issued - 2); i < issued; ++i)
         wait_ignoring_abort(&bars[B_FULL0 + (i & 1)], (i >> 1) & 1);
   } else if (warp == 9) {
-    // ================= MMA issuer =================
+    // ================= MMA issuer (event loop) =================
     if (lane == 0 && nloc > 0) {
+      const uint32_t tb = base + OFF_TB;
       auto stage = [&](int i) { return base + OFF_STAGE + (i & 1) * STAGE_BYTES; };
-      auto mma0 = [&](int i) {
-        const uint32_t st = stage(i);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t a = sdesc(st + (k >> 2) * ST_CB + (k & 3) * 32, 16, 1024);
-          mma_bf16(tmem + TM_D0, a, a, ID_KK, k > 0);
-        }
-      };
-      bool ok = mbar_wait(&bars[B_FULL0], 0, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        mma0(0);
-        mma_commit(&bars[B_MMA0]);
-      }
-      for (int i = 0; ok && i < nloc; ++i) {
-        const int b = i & 1;
-        if (i + 1 < nloc) {
-          ok = mbar_wait(&bars[B_FULL0 + ((i + 1) & 1)], ((i + 1) >> 1) & 1,
-                         abort_flag) &&
-               mbar_wait(&bars[B_D0FREE], i & 1, abort_flag);
-          if (!ok) break;
+      int j0 = 0;   // next MMA0 (K K^T, Q K^T)
+      int jw = 0;   // next W / U0 products
+      int i1 = 0;   // next MMA1 (chain: accumulator += [-W;Q^] S^T)
+      int i2 = 0;   // next MMA2 + MMA3
+      uint64_t t_idle = 0;
+      while (i2 < nloc) {
+        const int b1 = i1 & 1, b2 = i2 & 1;
+        if (i2 < i1 && mbar_test(&bars[B_UREADY], i2 & 1)) {
           tc_fence_after();
-          mma0(i + 1);
-          mma_commit(&bars[B_MMA0]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tmem + TM_D2,
+                     sdesc(base + OFF_KBAR + b2 * 16384 + k * 2048, 8192, 1024),
+                     sdesc(base + OFF_U + k * 2048, 8192, 1024), ID_MNMN, k > 0);
+          mma_commit(&bars[B_D2FULL]);
+          mma_commit(&bars[B_KBFREE0 + b2]);
+          const uint32_t zp = tb + (b2 ? TB_Z2 : TB_Z);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tmem + TM_D1 + 64 * b2, sdesc(zp + k * 32, 16, 1024),
+                     sdesc(base + OFF_U + k * 2048, 8192, 1024), ID_KMN, 1);
+          mma_commit(&bars[B_D3FULL0 + b2]);
+          mma_commit(&bars[B_TPFREE0 + b2]);
+          ++i2;
+          t_idle = 0;
+          continue;
         }
-        ok = mbar_wait(&bars[B_SREADY], i & 1, abort_flag) &&
-             mbar_wait(&bars[B_PREP], i & 1, abort_flag) &&
-             (i < 2 || mbar_wait(&bars[B_D1FREE0 + b], ((i >> 1) - 1) & 1,
-                                 abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t st = stage(i);
-        const uint32_t d1 = tmem + TM_D1 + 64 * b;
+        if (i1 < jw && mbar_test(&bars[B_SREADY], i1 & 1) &&
+            mbar_test(&bars[B_PREPD0 + b1], (i1 >> 1) & 1)) {
+          tc_fence_after();
+          const uint32_t st = stage(i1);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_bf16(d1, sdesc(st + (k >> 2) * ST_CB + (k & 3) * 32, 16, 1024),
-                   sdesc(base + OFF_S + k * 2048, 8192, 1024), ID_KMN, k > 0);
-        mma_commit(&bars[B_D1FULL0 + b]);
-
-        ok = mbar_wait(&bars[B_RREADY], i & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t tp = base + OFF_TP + b * TP_BYTES;
+          for (int k = 0; k < 8; ++k)
+            mma_bf16(tmem + TM_D1 + 64 * b1,
+                     sdesc(st + (k >> 2) * ST_CB + (k & 3) * 32, 16, 1024),
+                     sdesc(base + OFF_S + k * 2048, 8192, 1024), ID_KMN, 1);
+          mma_commit(&bars[B_D1FULL0 + b1]);
+          mma_commit(&bars[B_EMPTY0 + b1]);
+          ++i1;
+          t_idle = 0;
+          continue;
+        }
+        if (jw < j0 && mbar_test(&bars[B_PREPT], jw & 1) &&
+            (jw < 2 ||
+             mbar_test(&bars[B_D1FREE0 + (jw & 1)], ((jw >> 1) - 1) & 1))) {
+          tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_DTR, sdesc(tp + TP_T + k * 32, 16, 1024),
-                   sdesc(base + OFF_R + k * 2048, 8192, 1024), ID_KMN, k > 0);
-        mma_commit(&bars[B_UFULL]);
-        mma_commit(&bars[B_EMPTY0 + b]);
-
-        ok = mbar_wait(&bars[B_UREADY], i & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
+          for (int k = 0; k < 4; ++k)  // W (twice) = [T;T] K'
+            mma_bf16(tmem + TM_DW, sdesc(tb + TB_T + k * 32, 16, 1024),
+                     sdesc(base + OFF_KP + k * 2048, 8192, 1024), ID_KMN128,
+                     k > 0);
+          const uint32_t st = stage(jw);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_D2, sdesc(base + OFF_KBAR + k * 2048, 8192, 1024),
-                   sdesc(base + OFF_U + k * 2048, 8192, 1024), ID_MNMN, k > 0);
-        mma_commit(&bars[B_D2FULL]);
-        mma_commit(&bars[B_KBFREE]);
+          for (int k = 0; k < 4; ++k)  // U0 = [T;0] V' starts the accumulator
+            mma_bf16(tmem + TM_D1 + 64 * (jw & 1),
+                     sdesc(tb + TB_T2 + k * 32, 16, 1024),
+                     sdesc(st + ST_V + k * 2048, 8192, 1024), ID_KMN, k > 0);
+          mma_commit(&bars[B_WDONE]);
+          ++jw;
+          t_idle = 0;
+          continue;
+        }
+        if (j0 < nloc &&
+            mbar_test(&bars[B_FULL0 + (j0 & 1)], (j0 >> 1) & 1) &&
+            (j0 == 0 || mbar_test(&bars[B_D0FREE], (j0 - 1) & 1))) {
+          tc_fence_after();
+          const uint32_t st = stage(j0);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(d1, sdesc(tp + TP_Z + k * 32, 16, 1024),
-                   sdesc(base + OFF_U + k * 2048, 8192, 1024), ID_KMN, 1);
-        mma_commit(&bars[B_D3FULL0 + b]);
-        mma_commit(&bars[B_TPFREE0 + b]);
+          for (int k = 0; k < 8; ++k) {
+            const uint64_t a = sdesc(st + (k >> 2) * ST_CB + (k & 3) * 32, 16, 1024);
+            mma_bf16(tmem + TM_D0, a, a, ID_KK, k > 0);
+          }
+          mma_commit(&bars[B_MMA0]);
+          ++j0;
+          t_idle = 0;
+          continue;
+        }
+        // nothing ready: bounded idle
+        if (*abort_flag) break;
+        const uint64_t now = globaltimer_ns();
+        if (t_idle == 0) {
+          t_idle = now;
+        } else if (now - t_idle > kWaitLimitNs) {
+          *abort_flag = 1;
+          break;
+        }
       }
       // every MMA issued must finish before TMEM is released
       mma_commit(&bars[B_DRAIN]);
@@ -509,16 +535,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 4) {
     // ================= prep warpgroup =================
-    float* At = reinterpret_cast<float*>(sm + OFF_AT);
-    float* Tf = reinterpret_cast<float*>(sm + OFF_TF);
+    float* AT = reinterpret_cast<float*>(sm + OFF_AT);
+    uint8_t* tbuf = sm + OFF_TB;
     const uint32_t lanes = (uint32_t)(32 * warp) << 16;
     for (int j = 0; j < nloc; ++j) {
       const int s = j & 1;
       const float* vec =
           reinterpret_cast<const float*>(sm + OFF_VEC) + s * VEC_FLOATS;
       uint8_t* st = sm + OFF_STAGE + s * STAGE_BYTES;
-      uint8_t* tp = sm + OFF_TP + s * TP_BYTES;
-      // the stage's TMA data and gate vectors (full), and K K^T / Q K^T
+      // stage data and gate vectors (full), K K^T and Q K^T (MMA0)
       bool ok = mbar_wait(&bars[B_FULL0 + s], (j >> 1) & 1, abort_flag) &&
                 mbar_wait(&bars[B_MMA0], j & 1, abort_flag);
       if (!bar_and(1, 128, ok)) break;
@@ -527,15 +552,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld64(tmem + TM_D0 + lanes, x);
       tc_fence_before();
       mbar_arrive(&bars[B_D0FREE]);
-      ok = j < 2 || mbar_wait(&bars[B_TPFREE0 + s], ((j >> 1) - 1) & 1,
-                              abort_flag);
+      // P (for MMA3 of chunk j-2) and Kbar (MMA2 of chunk j-2) buffers free
+      ok = j < 2 ||
+           (mbar_wait(&bars[B_TPFREE0 + s], ((j >> 1) - 1) & 1, abort_flag) &&
+            mbar_wait(&bars[B_KBFREE0 + s], ((j >> 1) - 1) & 1, abort_flag));
       if (!bar_and(1, 128, ok)) break;
       const bool safe = vec[VEC_SAFE] != 0.f;
       // w = e^{-G} (factored decays) or alpha (running products)
       float w[64];
       load_vec64(vec + (safe ? VEC_IEG : VEC_ALPHA), w);
       if (tid < 64) {
-        // row r of A (row-major): beta_r exp(G'_r - G_j) k_r.k_j for j < r
+        // row r of A: beta_r exp(G'_r - G_j) k_r.k_j for j < r
         const int r = tid;
         if (safe) {
           const float er = vec[VEC_EGPB + r];
@@ -562,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int c4 = 0; c4 < 16; ++c4)
-          *reinterpret_cast<float4*>(At + r * AP + 4 * c4) =
+          *reinterpret_cast<float4*>(AT + r * AP + 4 * c4) =
               make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
       } else {
         // row r of P: exp(G_r - G_j) q_r.k_j for j <= r
@@ -583,24 +610,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             x[jj] = pv;
           }
         }
-        store_row_bf16(tp + TP_P, r, x);
+        store_row_bf16(tbuf + (s ? TB_P1 : TB_P0), r, x);
       }
       {
-        // Q^ = diag(e^G) Q in place (MMA0 is done with Q)
+        // row r = tid / 2, column block cb = tid % 2 of the stage:
+        // Q^ = e^{G_r} q_r in place, K' = beta_r e^{G'_r} k_r and
+        // Kbar = e^{G_L - G_r} k_r into their buffers, V' = beta_r v_r in place
         const int r = tid >> 1, cb = tid & 1;
         uint8_t* q = st + ST_Q + cb * ST_CB;
         scale_row_half(q, q, r, vec[VEC_EG + r]);
+        const uint8_t* k = st + ST_K + cb * ST_CB;
+        scale_row_half(k, sm + OFF_KP + cb * 8192, r, vec[VEC_EGPB + r]);
+        scale_row_half(k, sm + OFF_KBAR + s * 16384 + cb * 8192, r,
+                       vec[VEC_DEC + r]);
+        if (cb == 0) {
+          uint8_t* v = st + ST_V;
+          scale_row_half(v, v, r, scale_rows ? 0.f : vec[VEC_BETA + r]);
+        }
       }
       named_bar(1, 128);
-      solve_unit_lower(At, Tf, tid);
+      solve_unit_lower(AT, tid);
       {
-        // T -> bf16 rows 0-63 of [T;0]
+        // T -> bf16 into both copies (rows 0-63 of [T;T] and of [T;0])
         const int r = tid >> 1, hh = tid & 1;
         float f[32];
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 t4 =
-              *reinterpret_cast<const float4*>(Tf + r * AP + hh * 32 + 4 * c4);
+              *reinterpret_cast<const float4*>(AT + r * AP + hh * 32 + 4 * c4);
           f[4 * c4] = t4.x; f[4 * c4 + 1] = t4.y;
           f[4 * c4 + 2] = t4.z; f[4 * c4 + 3] = t4.w;
         }
@@ -616,19 +653,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           u.y = pack_bf16x2(f[8 * q4 + 2], f[8 * q4 + 3]);
           u.z = pack_bf16x2(f[8 * q4 + 4], f[8 * q4 + 5]);
           u.w = pack_bf16x2(f[8 * q4 + 6], f[8 * q4 + 7]);
-          *reinterpret_cast<uint4*>(tp + TP_T + sw128(r, hh * 4 + q4)) = u;
+          *reinterpret_cast<uint4*>(tbuf + TB_T + sw128(r, hh * 4 + q4)) = u;
+          *reinterpret_cast<uint4*>(tbuf + TB_T2 + sw128(r, hh * 4 + q4)) = u;
         }
       }
-      ok = j == 0 || mbar_wait(&bars[B_KBFREE], (j - 1) & 1, abort_flag);
-      if (!bar_and(1, 128, ok)) break;
-      {
-        // Kbar = diag(e^{G_L - G}) K
-        const int r = tid >> 1, cb = tid & 1;
-        scale_row_half(st + ST_K + cb * ST_CB, sm + OFF_KBAR + cb * 8192, r,
-                       vec[VEC_DEC + r]);
-      }
       fence_proxy_async();
-      mbar_arrive(&bars[B_PREP]);
+      mbar_arrive(&bars[B_PREPT]);
+      // -W replaces K in the stage: warps 0-1 columns 0-63 (lanes 0-63),
+      // warps 2-3 columns 64-127 (lanes 64-127 hold the second copy of W)
+      ok = mbar_wait(&bars[B_WDONE], j & 1, abort_flag);
+      if (!bar_and(1, 128, ok)) break;
+      tc_fence_after();
+      {
+        const int cb = warp >> 1, r = tid & 63;
+        float wv[64];
+        tmem_ld64(tmem + TM_DW + lanes + 64 * cb, wv);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) wv[c] = -wv[c];
+        store_row_bf16(st + ST_K + cb * ST_CB, r, wv);
+      }
+      tc_fence_before();
+      fence_proxy_async();
+      mbar_arrive(&bars[B_PREPD0 + s]);
     }
   } else {
     // ================= chain warpgroup =================
@@ -660,63 +706,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 64; ++c) S[c] = 0.f;
     }
     store_row_bf16(s_tile, ct, S);
+    bool ok = true;
+    float gam = 1.f;
+    // gamma of chunk 0 (read before S_READY lets the stage be recycled)
+    if (nloc > 0) {
+      ok = mbar_wait(&bars[B_FULL0], 0, abort_flag);
+      gam = reinterpret_cast<const float*>(sm + OFF_VEC)[VEC_GAMMA];
+    }
     fence_proxy_async();
     mbar_arrive(&bars[B_SREADY]);
-    bool ok = true;
     for (int i = 0; i < nloc; ++i) {
-      const int s = i & 1, b = i & 1;
-      ok = ok && mbar_wait(&bars[B_PREP], i & 1, abort_flag);
-      if (!bar_and(2, 128, ok)) {
-        ok = false;
-        break;
-      }
-      const float* vec = reinterpret_cast<const float*>(sm + OFF_VEC) + s * VEC_FLOATS;
-      const float gam = vec[VEC_GAMMA];
+      const int b = i & 1;
       const long long t0 = bos + (long long)(c_begin + i) * C;
       const int len = (int)min((long long)C, eos - t0);
       if (cw < 2) {
+        // U = U0 - W S^T (rows 0-63 of the accumulator) -> bf16 U tile
         const int r = ct;
-        bool ok1 = mbar_wait(&bars[B_FULL0 + s], (i >> 1) & 1, abort_flag) &&
-                   mbar_wait(&bars[B_D1FULL0 + b], (i >> 1) & 1, abort_flag);
+        bool ok1 = ok && mbar_wait(&bars[B_D1FULL0 + b], (i >> 1) & 1, abort_flag);
         ok1 = bar_and(3, 64, ok1);
         if (ok1) {
           tc_fence_after();
-          float ks[64];
-          tmem_ld64(tmem + TM_D1 + 64 * b + lanes, ks);
-          const float ebe = vec[VEC_EGPB + r], be = vec[VEC_BETA + r];
-          const uint8_t* vt = sm + OFF_STAGE + s * STAGE_BYTES + ST_V;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            float f[8];
-            if (scale_rows) {
-#pragma unroll
-              for (int e8 = 0; e8 < 8; ++e8) f[e8] = 0.f;
-            } else {
-              unpack_bf16x8(*reinterpret_cast<const uint4*>(vt + sw128(r, c)), f);
-            }
-#pragma unroll
-            for (int e8 = 0; e8 < 8; ++e8)
-              ks[8 * c + e8] = fmaf(-ebe, ks[8 * c + e8], be * f[e8]);
-          }
-          store_row_bf16(sm + OFF_R, r, ks);
+          float u[64];
+          tmem_ld64(tmem + TM_D1 + 64 * b + lanes, u);
+          store_row_bf16(sm + OFF_U, r, u);
           fence_proxy_async();
           tc_fence_before();
-          mbar_arrive(&bars[B_RREADY]);
-          bool ok2 = mbar_wait(&bars[B_UFULL], i & 1, abort_flag);
-          ok2 = bar_and(3, 64, ok2);
-          if (ok2) {
-            tc_fence_after();
-            float u[64];
-            tmem_ld64(tmem + TM_DTR + lanes, u);
-            store_row_bf16(sm + OFF_U, r, u);
-            fence_proxy_async();
-            tc_fence_before();
-            mbar_arrive(&bars[B_UREADY]);
-          }
-          ok = ok2;
-        } else {
-          ok = false;
+          mbar_arrive(&bars[B_UREADY]);
         }
+        ok = ok1;
       }
       bool ok3 = ok && mbar_wait(&bars[B_D2FULL], i & 1, abort_flag);
       if (!bar_and(2, 128, ok3)) {
@@ -731,12 +748,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 64; ++c) S[c] = fmaf(gam, S[c], dl[c]);
       }
       store_row_bf16(s_tile, ct, S);
+      if (i + 1 < nloc) {
+        ok = mbar_wait(&bars[B_FULL0 + (b ^ 1)], ((i + 1) >> 1) & 1, abort_flag);
+        gam = reinterpret_cast<const float*>(sm + OFF_VEC)[(b ^ 1) * VEC_FLOATS +
+                                                           VEC_GAMMA];
+      }
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&bars[B_SREADY]);
       if (cw >= 2) {
         const int r = ct - 64;
-        bool ok4 = mbar_wait(&bars[B_D3FULL0 + b], (i >> 1) & 1, abort_flag);
+        bool ok4 = ok && mbar_wait(&bars[B_D3FULL0 + b], (i >> 1) & 1, abort_flag);
         ok4 = bar_and(4, 64, ok4);
         if (ok4) {
           tc_fence_after();
@@ -748,19 +770,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ((size_t)(t0 + r) * H + h) * dv + row0);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-              uint4 w;
-              w.x = pack_bf16x2(o[8 * c + 0], o[8 * c + 1]);
-              w.y = pack_bf16x2(o[8 * c + 2], o[8 * c + 3]);
-              w.z = pack_bf16x2(o[8 * c + 4], o[8 * c + 5]);
-              w.w = pack_bf16x2(o[8 * c + 6], o[8 * c + 7]);
-              dst[c] = w;
+              uint4 wq;
+              wq.x = pack_bf16x2(o[8 * c + 0], o[8 * c + 1]);
+              wq.y = pack_bf16x2(o[8 * c + 2], o[8 * c + 3]);
+              wq.z = pack_bf16x2(o[8 * c + 4], o[8 * c + 5]);
+              wq.w = pack_bf16x2(o[8 * c + 6], o[8 * c + 7]);
+              dst[c] = wq;
             }
           }
           tc_fence_before();
           mbar_arrive(&bars[B_D1FREE0 + b]);
-        } else {
-          ok = false;
         }
+        ok = ok && ok4;
+      }
+      if (!bar_and(2, 128, ok)) {
+        ok = false;
+        break;
       }
     }
     if (ok && !*abort_flag) {
@@ -797,10 +822,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------
 // Self-test: D = A * B (x2 when twice) with the layouts above, one CTA.
+// N = 64 or 128 (an N-major B of 128 columns is two 64-column blocks).
 __global__ void __launch_bounds__(128)
     selftest_mma_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B,
-                        float* D, int K, int a_mn, int b_mn, int b_stacked,
-                        int twice, int* status) {
+                        float* D, int K, int N, int a_mn, int b_mn,
+                        int b_stacked, int twice, int* status) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -810,7 +836,7 @@ __global__ void __launch_bounds__(128)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + 65548);
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp == 0) {
-    tmem_alloc(slot, 64);
+    tmem_alloc(slot, 128);
     tmem_relinquish();
   }
   if (tid == 0) {
@@ -828,11 +854,11 @@ __global__ void __launch_bounds__(128)
              : (uint32_t)((k >> 6) * 16384) + sw128(m, (k & 63) >> 3) + (k & 7) * 2;
     *reinterpret_cast<__nv_bfloat16*>(sm + off) = A[idx];
   }
-  const uint32_t bstride = b_stacked ? 16384u : 8192u;
-  for (int idx = tid; idx < K * 64; idx += 128) {
-    const int k = idx / 64, nn = idx % 64;
+  const uint32_t bstride = b_stacked ? 16384u : (uint32_t)N * 128u;
+  for (int idx = tid; idx < K * N; idx += 128) {
+    const int k = idx / N, nn = idx % N;
     const uint32_t off =
-        b_mn ? sw128(k, nn >> 3) + (nn & 7) * 2
+        b_mn ? (uint32_t)((nn >> 6) * (K * 128)) + sw128(k, (nn & 63) >> 3) + (nn & 7) * 2
              : (uint32_t)(k >> 6) * bstride + sw128(nn, (k & 63) >> 3) + (k & 7) * 2;
     *reinterpret_cast<__nv_bfloat16*>(sm + 32768 + off) = B[idx];
   }
@@ -842,14 +868,14 @@ __global__ void __launch_bounds__(128)
   tc_fence_after();
   const uint32_t tmem = *slot;
   if (tid == 0) {
-    const uint32_t id = idesc_bf16(128, 64, a_mn != 0, b_mn != 0);
+    const uint32_t id = idesc_bf16(128, N, a_mn != 0, b_mn != 0);
     for (int pass = 0; pass <= (twice ? 1 : 0); ++pass)
       for (int s = 0; s < K / 16; ++s) {
         const uint64_t a =
             a_mn ? sdesc(base + s * 2048, K * 128, 1024)
                  : sdesc(base + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
         const uint64_t b =
-            b_mn ? sdesc(base + 32768 + s * 2048, 8192, 1024)
+            b_mn ? sdesc(base + 32768 + s * 2048, K * 128, 1024)
                  : sdesc(base + 32768 + (s >> 2) * bstride + (s & 3) * 32, 16, 1024);
         mma_bf16(tmem, a, b, id, (pass > 0 || s > 0) ? 1u : 0u);
       }
@@ -858,10 +884,12 @@ __global__ void __launch_bounds__(128)
   const bool ok = __syncthreads_and(mbar_wait(bar, 0, abort_flag)) != 0;
   tc_fence_after();
   if (ok) {
-    float d[64];
-    tmem_ld64(tmem + ((uint32_t)(32 * warp) << 16), d);
+    for (int c0 = 0; c0 < N; c0 += 64) {
+      float d[64];
+      tmem_ld64(tmem + ((uint32_t)(32 * warp) << 16) + c0, d);
 #pragma unroll
-    for (int c = 0; c < 64; ++c) D[tid * 64 + c] = d[c];
+      for (int c = 0; c < 64; ++c) D[tid * N + c0 + c] = d[c];
+    }
   } else if (tid == 0) {
     record_status(status, GDN_ERR_TIMEOUT);
   }
@@ -870,7 +898,7 @@ __global__ void __launch_bounds__(128)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 64);
+    tmem_dealloc(tmem, 128);
   }
 }
 
@@ -945,10 +973,12 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream) {
 }  // namespace gdn
 
 extern "C" int gdn_selftest_mma(const void* A, const void* B, float* D, int K,
-                                int a_mn, int b_mn, int b_stacked, int twice,
-                                gdn_stream_t stream) {
+                                int N, int a_mn, int b_mn, int b_stacked,
+                                int twice, gdn_stream_t stream) {
   using namespace gdn;
-  if (!A || !B || !D || (K != 64 && K != 128)) return GDN_ERR_INVALID_ARG;
+  if (!A || !B || !D || (K != 64 && K != 128) || (N != 64 && N != 128))
+    return GDN_ERR_INVALID_ARG;
+  if (b_stacked && N != 64) return GDN_ERR_INVALID_ARG;
   if (b_stacked && b_mn) return GDN_ERR_INVALID_ARG;
   int* status = nullptr;
   int rc = device_status_ptr(&status);
@@ -960,8 +990,8 @@ extern "C" int gdn_selftest_mma(const void* A, const void* B, float* D, int K,
     return GDN_ERR_CUDA;
   selftest_mma_kernel<<<1, 128, bytes, stream>>>(
       static_cast<const __nv_bfloat16*>(A),
-      static_cast<const __nv_bfloat16*>(B), D, K, a_mn, b_mn, b_stacked, twice,
-      status);
+      static_cast<const __nv_bfloat16*>(B), D, K, N, a_mn, b_mn, b_stacked,
+      twice, status);
   if (count_launches(cudaGetLastError(), 1) != cudaSuccess) return GDN_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return GDN_ERR_CUDA;
   return gdn_device_status(stream);

@@ -17,11 +17,11 @@ extern "C" {
 
 /*
  * gdn_selftest_mma -- D = A * B (times 2 when `twice`) on one CTA with
- * tcgen05.mma kind::f16 (M = 128, N = 64), using the shared-memory layouts of
- * the chunk kernel.
- *   A  bf16 [128, K] row-major (device)    B  bf16 [K, 64] row-major (device)
- *   D  fp32 [128, 64] row-major (device, written)
- *   K  64 or 128
+ * tcgen05.mma kind::f16 (M = 128), using the shared-memory layouts of the
+ * chunk kernel.
+ *   A  bf16 [128, K] row-major (device)    B  bf16 [K, N] row-major (device)
+ *   D  fp32 [128, N] row-major (device, written)
+ *   K  64 or 128;  N  64 or 128 (b_stacked requires N = 64)
  *   a_mn       store A M-major (else K-major) before the MMA
  *   b_mn       store B N-major (else K-major)
  *   b_stacked  K-major B placed in the first 64 rows of a 128-row tile
@@ -29,8 +29,9 @@ extern "C" {
  * Returns GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_TIMEOUT (the completion wait
  * gave up) or GDN_ERR_CUDA. Synchronises `stream`.
  */
-int gdn_selftest_mma(const void* A, const void* B, float* D, int K, int a_mn,
-                     int b_mn, int b_stacked, int twice, gdn_stream_t stream);
+int gdn_selftest_mma(const void* A, const void* B, float* D, int K, int N,
+                     int a_mn, int b_mn, int b_stacked, int twice,
+                     gdn_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -11,22 +11,23 @@ import torch
 
 pytestmark = pytest.mark.gpu
 
-# (K, a_mn, b_mn, b_stacked): the operand forms of the chunk kernel's MMAs
+# (K, N, a_mn, b_mn, b_stacked): the operand forms of the chunk kernel's MMAs
 CASES = [
-    (128, False, False, True),   # [K;Q] K^T            (K-major A, K-major B)
-    (128, False, True, False),   # [K;Q^] S^T           (K-major A, N-major B)
-    (64, False, True, False),    # [T;0] R, [0;P] U     (K-major A, N-major B)
-    (64, True, True, False),     # Kbar^T U             (M-major A, N-major B)
-    (128, False, False, False),  # dense K-major B
+    (128, 64, False, False, True),   # [K;Q] K^T         (K-major A, K-major B)
+    (128, 64, False, True, False),   # [-W;Q^] S^T       (K-major A, N-major B)
+    (64, 64, False, True, False),    # [T;0] V', [0;P] U (K-major A, N-major B)
+    (64, 128, False, True, False),   # [T;T] K'          (N-major B, 2 blocks)
+    (64, 64, True, True, False),     # Kbar^T U          (M-major A, N-major B)
+    (128, 64, False, False, False),  # dense K-major B
 ]
 
 
-@pytest.mark.parametrize("K,a_mn,b_mn,b_stacked", CASES)
+@pytest.mark.parametrize("K,N,a_mn,b_mn,b_stacked", CASES)
 @pytest.mark.parametrize("twice", [False, True])
-def test_mma_layouts(lib, cuda_device, K, a_mn, b_mn, b_stacked, twice):
-    g = torch.Generator(device="cpu").manual_seed(K * 7 + a_mn * 3 + b_mn)
+def test_mma_layouts(lib, cuda_device, K, N, a_mn, b_mn, b_stacked, twice):
+    g = torch.Generator(device="cpu").manual_seed(K * 7 + N + a_mn * 3 + b_mn)
     A = torch.randn(128, K, generator=g).to(torch.bfloat16)
-    B = torch.randn(K, 64, generator=g).to(torch.bfloat16)
+    B = torch.randn(K, N, generator=g).to(torch.bfloat16)
     ref = (A.double() @ B.double()) * (2 if twice else 1)
     D = lib.gdn_selftest_mma(A.to(cuda_device), B.to(cuda_device), a_mn=a_mn,
                              b_mn=b_mn, b_stacked=b_stacked, twice=twice)
