@@ -7,27 +7,29 @@
 // Per chunk (illustrated DeltaNet walk-through: UT transform, WY
 // representation, chunkwise state passing and output; scalar gate prefixes
 // of its GLA section), with D_rj = exp(G_r - G_j), G the chunk-local
-// cumulative log gate, and G' = G (decay first) or G_{r-1} (decay after the
-// prediction):
+// cumulative log gate, G' = G (decay first) or G_{r-1} (decay after the
+// prediction), and every gate factor folded into an operand that is written
+// anyway (all such factors lie in (0, 1]):
 //
 //   prep   MMA0  [K;Q] K^T -> K K^T, Q K^T
-//          A = strict_lower(diag(beta) K K^T (.) D'),  T = (I + A)^{-1}
-//          P = (Q K^T) (.) D (.) M_incl,  Q^ = diag(e^G) Q,
-//          K' = diag(beta e^{G'}) K,  V' = diag(beta) V,  Kbar = diag(e^{G_L-G}) K
-//          MMA   [T;T] K' -> W (twice);   [T;0] V' -> U0 into the chunk's
-//                accumulator; -W replaces K in the stage tile: [-W;Q^]
-//   chain  MMA1  accumulator += [-W;Q^] S^T -> U = U0 - W S^T, Q^ S^T
-//          MMA2  Kbar^T U -> Delta;  S^T <- gamma S^T + Delta
-//          MMA3  accumulator += [0;P] U -> O = Q^ S^T + P U
+//          A = strict_lower(diag(beta) K K^T (.) D'),  T = (I + A)^{-1},
+//          P = (Q K^T) (.) D (.) M_incl,
+//          T_W = T diag(beta e^{G'}),  T_U = T diag(beta)
+//          MMA   [T_W;T_W] K -> W (twice);  [0;T_U] V -> U0 starts the
+//                chunk's accumulator (rows 64-127);  -W is stored after Q
+//   chain  MMA1  accumulator += [Q;-W] S^T -> H = Q S^T (rows 0-63),
+//                U = U0 - W S^T (rows 64-127)
+//          MMA2  K^T (diag(e^{G_L - G}) U) -> Delta;  S^T <- gamma S^T + Delta
+//          MMA3  [P;0] U -> P U;   O = diag(e^G) H + P U at read-out
 //
-// so the serial chain per chunk is two MMA round trips and two short
-// register phases; everything else overlaps it.
+// The serial chain per chunk is two MMA round trips and two short register
+// phases; everything else overlaps it.
 //
-// Warp roles (320 threads): warps 0-3 prep, 4-7 chain, 8 TMA producer (also
-// the chunk's gate vectors), 9 MMA issuer (an event loop that gives the chain's
-// MMAs priority). Operand tiles are bf16 with the 128-byte swizzle; K/Q/V
-// arrive by TMA in a two-stage ring. Every wait is bounded; a CTA that gives
-// up records GDN_ERR_TIMEOUT, drains its MMAs, frees its TMEM and exits.
+// Warp roles (352 threads): warps 0-3 prep, 4-7 chain, 8 TMA producer (also
+// the chunk's gate vectors), 9 issues the chain's MMAs, 10 the prep's MMAs.
+// Operand tiles are bf16 with the 128-byte swizzle; K/Q/V arrive by TMA in a
+// two-stage ring. Every wait is bounded; a CTA that gives up records
+// GDN_ERR_TIMEOUT, drains its MMAs, frees its TMEM and exits.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -43,28 +45,32 @@ using namespace tc;
 constexpr int C = 64;
 constexpr int DK = 128;
 constexpr int DVT = 64;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 
-// Stage: [K;Q] stacked K-major tile (two 16 KB column blocks of 64 columns;
-// rows 0-63 K (later -W), rows 64-127 Q (later Q^)), then the V tile (later V').
+// Stage: per 64-column block of d_k, three 64-row groups K | Q | -W (the
+// first two by TMA, -W by the prep); [K;Q] and [Q;-W] are 128-row K-major
+// tiles and K alone is the N-major operand of the W and Delta products. The
+// V tile (64 x 64) follows the two column blocks.
 constexpr uint32_t ST_K = 0;
 constexpr uint32_t ST_Q = 8192;
-constexpr uint32_t ST_CB = 16384;
-constexpr uint32_t ST_V = 32768;
-constexpr uint32_t STAGE_BYTES = 40960;
-// T buffer: T, a copy of T, zeros, P (even chunks), zeros, P (odd chunks);
-// [T;T], [T;0], [0;P0] and [0;P1] are 128-row K-major tiles.
-constexpr uint32_t TB_T = 0, TB_T2 = 8192, TB_Z = 16384, TB_P0 = 24576,
-                   TB_Z2 = 32768, TB_P1 = 40960, TB_BYTES = 49152;
+constexpr uint32_t ST_W = 16384;
+constexpr uint32_t ST_CB = 24576;
+constexpr uint32_t ST_V = 49152;
+constexpr uint32_t STAGE_BYTES = 57344;
+constexpr uint32_t STAGE_TMA_BYTES = 40960;
+// T buffer: T_W twice, P (even chunks), zeros, T_U, P (odd chunks), zeros;
+// [T_W;T_W], [P0;0], [0;T_U] and [P1;0] are 128-row K-major tiles.
+constexpr uint32_t TB_TW = 0, TB_TW2 = 8192, TB_P0 = 16384, TB_Z = 24576,
+                   TB_TU = 32768, TB_P1 = 40960, TB_Z2 = 49152,
+                   TB_BYTES = 57344;
 
 constexpr uint32_t OFF_STAGE = 0;
-constexpr uint32_t OFF_TB = 2 * STAGE_BYTES;               // 81920
-constexpr uint32_t OFF_KBAR = OFF_TB + TB_BYTES;           // 2 x 16 KB
-constexpr uint32_t OFF_KP = OFF_KBAR + 2 * 16384;          // K'
-constexpr uint32_t OFF_S = OFF_KP + 16384;
-constexpr uint32_t OFF_U = OFF_S + 16384;
+constexpr uint32_t OFF_TB = 2 * STAGE_BYTES;               // 114688
+constexpr uint32_t OFF_S = OFF_TB + TB_BYTES;              // S^T, bf16
+constexpr uint32_t OFF_U = OFF_S + 16384;                  // U, bf16
+constexpr uint32_t OFF_UD = OFF_U + 8192;                  // diag(e^{G_L-G}) U
 constexpr int AP = 68;  // fp32 row pitch of the solve buffer
-constexpr uint32_t OFF_AT = OFF_U + 8192;                  // A, then T (fp32)
+constexpr uint32_t OFF_AT = OFF_UD + 8192;                 // A, then T (fp32)
 // Per-stage gate vectors written by the producer warp: cumulative log gate G,
 // alpha = e^g, e^G, beta e^{G'}, beta, e^{G_L - G}, e^{-G}, gamma = e^{G_L},
 // and whether e^{G_r} e^{-G_j} stays in the normal fp32 range.
@@ -78,14 +84,15 @@ enum {
   B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_MMA0, B_D0FREE, B_PREPT, B_WDONE,
   B_PREPD0, B_PREPD1, B_SREADY, B_D1FULL0, B_D1FULL1, B_UREADY, B_D2FULL,
   B_D3FULL0, B_D3FULL1, B_D1FREE0, B_D1FREE1, B_TPFREE0, B_TPFREE1,
-  B_KBFREE0, B_KBFREE1, B_DRAIN, NBARS
+  B_DRAIN_C, B_DRAIN_P, NBARS
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // TMEM columns (fp32 accumulators, 128 lanes each).
-constexpr uint32_t TM_D0 = 0, TM_D1 = 64, TM_DW = 192, TM_D2 = 320;
+constexpr uint32_t TM_D0 = 0, TM_D1 = 64, TM_DW = 192, TM_D2 = 320,
+                   TM_D3 = 384;
 constexpr uint32_t TMEM_COLS = 512;
 
 constexpr uint32_t ID_KK = idesc_bf16(128, 64, false, false);
@@ -142,27 +149,6 @@ __device__ __forceinline__ void store_row_bf16(uint8_t* tile, int r,
     w.z = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]);
     w.w = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
     *reinterpret_cast<uint4*>(tile + sw128(r, c)) = w;
-  }
-}
-
-// Scale the 64 bf16 values of row r of a swizzled 128-byte-row tile (all
-// loads are issued before any store, so src may equal dst).
-__device__ __forceinline__ void scale_row_half(const uint8_t* src, uint8_t* dst,
-                                               int r, float s) {
-  uint4 u[8];
-#pragma unroll
-  for (int c = 0; c < 8; ++c)
-    u[c] = *reinterpret_cast<const uint4*>(src + sw128(r, c));
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    float f[8];
-    unpack_bf16x8(u[c], f);
-    uint4 w;
-    w.x = pack_bf16x2(f[0] * s, f[1] * s);
-    w.y = pack_bf16x2(f[2] * s, f[3] * s);
-    w.z = pack_bf16x2(f[4] * s, f[5] * s);
-    w.w = pack_bf16x2(f[6] * s, f[7] * s);
-    *reinterpret_cast<uint4*>(dst + sw128(r, c)) = w;
   }
 }
 
@@ -358,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  auto stage = [&](int i) { return base + OFF_STAGE + (i & 1) * STAGE_BYTES; };
 
   if (warp == 8) {
     // ================= TMA producer + gate vectors =================
@@ -372,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* st = sm + OFF_STAGE + s * STAGE_BYTES;
       uint64_t* full = &bars[B_FULL0 + s];
       if (lane == 0) {
-        mbar_arrive_expect_tx(full, STAGE_BYTES);
+        mbar_arrive_expect_tx(full, STAGE_TMA_BYTES);
         const int tok = (int)t0;
         tma_load_3d(st + ST_K, &tmk, full, 0, h, tok);
         tma_load_3d(st + ST_K + ST_CB, &tmk, full, 64, h, tok);
@@ -437,101 +424,89 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0)
       for (int i = max(0, issued - 2); i < issued; ++i)
         wait_ignoring_abort(&bars[B_FULL0 + (i & 1)], (i >> 1) & 1);
-  } else if (warp == 9) {
-    // ================= MMA issuer (event loop) =================
+  } else if (warp == 10) {
+    // ================= prep MMAs: K K^T / Q K^T, W and U0 =================
     if (lane == 0 && nloc > 0) {
       const uint32_t tb = base + OFF_TB;
-      auto stage = [&](int i) { return base + OFF_STAGE + (i & 1) * STAGE_BYTES; };
-      int j0 = 0;   // next MMA0 (K K^T, Q K^T)
-      int jw = 0;   // next W / U0 products
-      int i1 = 0;   // next MMA1 (chain: accumulator += [-W;Q^] S^T)
-      int i2 = 0;   // next MMA2 + MMA3
-      uint64_t t_idle = 0;
-      while (i2 < nloc) {
-        const int b1 = i1 & 1, b2 = i2 & 1;
-        if (i2 < i1 && mbar_test(&bars[B_UREADY], i2 & 1)) {
-          tc_fence_after();
+      auto mma0 = [&](int j) {
+        const uint32_t st = stage(j);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + TM_D2,
-                     sdesc(base + OFF_KBAR + b2 * 16384 + k * 2048, 8192, 1024),
-                     sdesc(base + OFF_U + k * 2048, 8192, 1024), ID_MNMN, k > 0);
-          mma_commit(&bars[B_D2FULL]);
-          mma_commit(&bars[B_KBFREE0 + b2]);
-          const uint32_t zp = tb + (b2 ? TB_Z2 : TB_Z);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + TM_D1 + 64 * b2, sdesc(zp + k * 32, 16, 1024),
-                     sdesc(base + OFF_U + k * 2048, 8192, 1024), ID_KMN, 1);
-          mma_commit(&bars[B_D3FULL0 + b2]);
-          mma_commit(&bars[B_TPFREE0 + b2]);
-          ++i2;
-          t_idle = 0;
-          continue;
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t a =
+              sdesc(st + ST_K + (k >> 2) * ST_CB + (k & 3) * 32, 16, 1024);
+          mma_bf16(tmem + TM_D0, a, a, ID_KK, k > 0);
         }
-        if (i1 < jw && mbar_test(&bars[B_SREADY], i1 & 1) &&
-            mbar_test(&bars[B_PREPD0 + b1], (i1 >> 1) & 1)) {
-          tc_fence_after();
-          const uint32_t st = stage(i1);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_bf16(tmem + TM_D1 + 64 * b1,
-                     sdesc(st + (k >> 2) * ST_CB + (k & 3) * 32, 16, 1024),
-                     sdesc(base + OFF_S + k * 2048, 8192, 1024), ID_KMN, 1);
-          mma_commit(&bars[B_D1FULL0 + b1]);
-          mma_commit(&bars[B_EMPTY0 + b1]);
-          ++i1;
-          t_idle = 0;
-          continue;
-        }
-        if (jw < j0 && mbar_test(&bars[B_PREPT], jw & 1) &&
-            (jw < 2 ||
-             mbar_test(&bars[B_D1FREE0 + (jw & 1)], ((jw >> 1) - 1) & 1))) {
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < 4; ++k)  // W (twice) = [T;T] K'
-            mma_bf16(tmem + TM_DW, sdesc(tb + TB_T + k * 32, 16, 1024),
-                     sdesc(base + OFF_KP + k * 2048, 8192, 1024), ID_KMN128,
-                     k > 0);
-          const uint32_t st = stage(jw);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)  // U0 = [T;0] V' starts the accumulator
-            mma_bf16(tmem + TM_D1 + 64 * (jw & 1),
-                     sdesc(tb + TB_T2 + k * 32, 16, 1024),
-                     sdesc(st + ST_V + k * 2048, 8192, 1024), ID_KMN, k > 0);
-          mma_commit(&bars[B_WDONE]);
-          ++jw;
-          t_idle = 0;
-          continue;
-        }
-        if (j0 < nloc &&
-            mbar_test(&bars[B_FULL0 + (j0 & 1)], (j0 >> 1) & 1) &&
-            (j0 == 0 || mbar_test(&bars[B_D0FREE], (j0 - 1) & 1))) {
-          tc_fence_after();
-          const uint32_t st = stage(j0);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t a = sdesc(st + (k >> 2) * ST_CB + (k & 3) * 32, 16, 1024);
-            mma_bf16(tmem + TM_D0, a, a, ID_KK, k > 0);
-          }
-          mma_commit(&bars[B_MMA0]);
-          ++j0;
-          t_idle = 0;
-          continue;
-        }
-        // nothing ready: bounded idle
-        if (*abort_flag) break;
-        const uint64_t now = globaltimer_ns();
-        if (t_idle == 0) {
-          t_idle = now;
-        } else if (now - t_idle > kWaitLimitNs) {
-          *abort_flag = 1;
-          break;
-        }
+        mma_commit(&bars[B_MMA0]);
+      };
+      bool ok = mbar_wait(&bars[B_FULL0], 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        mma0(0);
       }
-      // every MMA issued must finish before TMEM is released
-      mma_commit(&bars[B_DRAIN]);
-      wait_ignoring_abort(&bars[B_DRAIN], 0);
+      for (int j = 0; ok && j < nloc; ++j) {
+        if (j + 1 < nloc) {
+          ok = mbar_wait(&bars[B_D0FREE], j & 1, abort_flag) &&
+               mbar_wait(&bars[B_FULL0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1,
+                         abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          mma0(j + 1);
+        }
+        ok = mbar_wait(&bars[B_PREPT], j & 1, abort_flag) &&
+             (j < 2 || mbar_wait(&bars[B_D1FREE0 + (j & 1)],
+                                 ((j >> 1) - 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t st = stage(j);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // W (twice) = [T_W;T_W] K
+          mma_bf16(tmem + TM_DW, sdesc(tb + TB_TW + k * 32, 16, 1024),
+                   sdesc(st + ST_K + k * 2048, ST_CB, 1024), ID_KMN128, k > 0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // U0 = [0;T_U] V starts the accumulator
+          mma_bf16(tmem + TM_D1 + 64 * (j & 1), sdesc(tb + TB_Z + k * 32, 16, 1024),
+                   sdesc(st + ST_V + k * 2048, 8192, 1024), ID_KMN, k > 0);
+        mma_commit(&bars[B_WDONE]);
+      }
+      mma_commit(&bars[B_DRAIN_P]);
+      wait_ignoring_abort(&bars[B_DRAIN_P], 0);
+    }
+  } else if (warp == 9) {
+    // ================= chain MMAs =================
+    if (lane == 0 && nloc > 0) {
+      const uint32_t tb = base + OFF_TB;
+      for (int i = 0; i < nloc; ++i) {
+        const int b = i & 1;
+        bool ok = mbar_wait(&bars[B_SREADY], i & 1, abort_flag) &&
+                  mbar_wait(&bars[B_PREPD0 + b], (i >> 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t st = stage(i);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)  // += [Q;-W] S^T
+          mma_bf16(tmem + TM_D1 + 64 * b,
+                   sdesc(st + ST_Q + (k >> 2) * ST_CB + (k & 3) * 32, 16, 1024),
+                   sdesc(base + OFF_S + k * 2048, 8192, 1024), ID_KMN, 1);
+        mma_commit(&bars[B_D1FULL0 + b]);
+        ok = mbar_wait(&bars[B_UREADY], i & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // Delta = K^T diag(e^{G_L-G}) U
+          mma_bf16(tmem + TM_D2, sdesc(st + ST_K + k * 2048, ST_CB, 1024),
+                   sdesc(base + OFF_UD + k * 2048, 8192, 1024), ID_MNMN, k > 0);
+        mma_commit(&bars[B_D2FULL]);
+        mma_commit(&bars[B_EMPTY0 + b]);
+        const uint32_t pz = tb + (b ? TB_P1 : TB_P0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // P U
+          mma_bf16(tmem + TM_D3 + 64 * b, sdesc(pz + k * 32, 16, 1024),
+                   sdesc(base + OFF_U + k * 2048, 8192, 1024), ID_KMN, k > 0);
+        mma_commit(&bars[B_D3FULL0 + b]);
+        mma_commit(&bars[B_TPFREE0 + b]);
+      }
+      mma_commit(&bars[B_DRAIN_C]);
+      wait_ignoring_abort(&bars[B_DRAIN_C], 0);
     }
   } else if (warp < 4) {
     // ================= prep warpgroup =================
@@ -552,10 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld64(tmem + TM_D0 + lanes, x);
       tc_fence_before();
       mbar_arrive(&bars[B_D0FREE]);
-      // P (for MMA3 of chunk j-2) and Kbar (MMA2 of chunk j-2) buffers free
+      // P buffer of chunk j-2 consumed
       ok = j < 2 ||
-           (mbar_wait(&bars[B_TPFREE0 + s], ((j >> 1) - 1) & 1, abort_flag) &&
-            mbar_wait(&bars[B_KBFREE0 + s], ((j >> 1) - 1) & 1, abort_flag));
+           mbar_wait(&bars[B_TPFREE0 + s], ((j >> 1) - 1) & 1, abort_flag);
       if (!bar_and(1, 128, ok)) break;
       const bool safe = vec[VEC_SAFE] != 0.f;
       // w = e^{-G} (factored decays) or alpha (running products)
@@ -612,34 +586,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         store_row_bf16(tbuf + (s ? TB_P1 : TB_P0), r, x);
       }
-      {
-        // row r = tid / 2, column block cb = tid % 2 of the stage:
-        // Q^ = e^{G_r} q_r in place, K' = beta_r e^{G'_r} k_r and
-        // Kbar = e^{G_L - G_r} k_r into their buffers, V' = beta_r v_r in place
-        const int r = tid >> 1, cb = tid & 1;
-        uint8_t* q = st + ST_Q + cb * ST_CB;
-        scale_row_half(q, q, r, vec[VEC_EG + r]);
-        const uint8_t* k = st + ST_K + cb * ST_CB;
-        scale_row_half(k, sm + OFF_KP + cb * 8192, r, vec[VEC_EGPB + r]);
-        scale_row_half(k, sm + OFF_KBAR + s * 16384 + cb * 8192, r,
-                       vec[VEC_DEC + r]);
-        if (cb == 0) {
-          uint8_t* v = st + ST_V;
-          scale_row_half(v, v, r, scale_rows ? 0.f : vec[VEC_BETA + r]);
-        }
-      }
       named_bar(1, 128);
       solve_unit_lower(AT, tid);
       {
-        // T -> bf16 into both copies (rows 0-63 of [T;T] and of [T;0])
+        // T_W = T diag(beta e^{G'}) (two copies), T_U = T diag(beta)
         const int r = tid >> 1, hh = tid & 1;
-        float f[32];
+        float f[32], fw[32], fu[32];
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 t4 =
               *reinterpret_cast<const float4*>(AT + r * AP + hh * 32 + 4 * c4);
+          const float4 w4 = *reinterpret_cast<const float4*>(
+              vec + VEC_EGPB + hh * 32 + 4 * c4);
+          // rows of the scaling matrix see V = 0, so U0 = 0 for them
+          const float4 u4 = scale_rows
+                                ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                : *reinterpret_cast<const float4*>(
+                                      vec + VEC_BETA + hh * 32 + 4 * c4);
           f[4 * c4] = t4.x; f[4 * c4 + 1] = t4.y;
           f[4 * c4 + 2] = t4.z; f[4 * c4 + 3] = t4.w;
+          fw[4 * c4] = w4.x; fw[4 * c4 + 1] = w4.y;
+          fw[4 * c4 + 2] = w4.z; fw[4 * c4 + 3] = w4.w;
+          fu[4 * c4] = u4.x; fu[4 * c4 + 1] = u4.y;
+          fu[4 * c4 + 2] = u4.z; fu[4 * c4 + 3] = u4.w;
         }
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
@@ -648,18 +617,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 u;
-          u.x = pack_bf16x2(f[8 * q4 + 0], f[8 * q4 + 1]);
-          u.y = pack_bf16x2(f[8 * q4 + 2], f[8 * q4 + 3]);
-          u.z = pack_bf16x2(f[8 * q4 + 4], f[8 * q4 + 5]);
-          u.w = pack_bf16x2(f[8 * q4 + 6], f[8 * q4 + 7]);
-          *reinterpret_cast<uint4*>(tbuf + TB_T + sw128(r, hh * 4 + q4)) = u;
-          *reinterpret_cast<uint4*>(tbuf + TB_T2 + sw128(r, hh * 4 + q4)) = u;
+          uint4 a, c;
+          a.x = pack_bf16x2(f[8 * q4 + 0] * fw[8 * q4 + 0], f[8 * q4 + 1] * fw[8 * q4 + 1]);
+          a.y = pack_bf16x2(f[8 * q4 + 2] * fw[8 * q4 + 2], f[8 * q4 + 3] * fw[8 * q4 + 3]);
+          a.z = pack_bf16x2(f[8 * q4 + 4] * fw[8 * q4 + 4], f[8 * q4 + 5] * fw[8 * q4 + 5]);
+          a.w = pack_bf16x2(f[8 * q4 + 6] * fw[8 * q4 + 6], f[8 * q4 + 7] * fw[8 * q4 + 7]);
+          c.x = pack_bf16x2(f[8 * q4 + 0] * fu[8 * q4 + 0], f[8 * q4 + 1] * fu[8 * q4 + 1]);
+          c.y = pack_bf16x2(f[8 * q4 + 2] * fu[8 * q4 + 2], f[8 * q4 + 3] * fu[8 * q4 + 3]);
+          c.z = pack_bf16x2(f[8 * q4 + 4] * fu[8 * q4 + 4], f[8 * q4 + 5] * fu[8 * q4 + 5]);
+          c.w = pack_bf16x2(f[8 * q4 + 6] * fu[8 * q4 + 6], f[8 * q4 + 7] * fu[8 * q4 + 7]);
+          const uint32_t off = sw128(r, hh * 4 + q4);
+          *reinterpret_cast<uint4*>(tbuf + TB_TW + off) = a;
+          *reinterpret_cast<uint4*>(tbuf + TB_TW2 + off) = a;
+          *reinterpret_cast<uint4*>(tbuf + TB_TU + off) = c;
         }
       }
       fence_proxy_async();
       mbar_arrive(&bars[B_PREPT]);
-      // -W replaces K in the stage: warps 0-1 columns 0-63 (lanes 0-63),
+      // -W after Q in the stage: warps 0-1 columns 0-63 (lanes 0-63),
       // warps 2-3 columns 64-127 (lanes 64-127 hold the second copy of W)
       ok = mbar_wait(&bars[B_WDONE], j & 1, abort_flag);
       if (!bar_and(1, 128, ok)) break;
@@ -670,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld64(tmem + TM_DW + lanes + 64 * cb, wv);
 #pragma unroll
         for (int c = 0; c < 64; ++c) wv[c] = -wv[c];
-        store_row_bf16(st + ST_K + cb * ST_CB, r, wv);
+        store_row_bf16(st + ST_W + cb * ST_CB, r, wv);
       }
       tc_fence_before();
       fence_proxy_async();
@@ -678,6 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ================= chain warpgroup =================
+    // warps 4-5: output rows (lanes 0-63), warps 6-7: U rows (lanes 64-127),
+    // all four: state rows (lane = d_k index)
     const int ct = tid - 128, cw = warp - 4;
     const uint32_t lanes = (uint32_t)(32 * cw) << 16;
     uint8_t* s_tile = sm + OFF_S;
@@ -707,28 +684,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     store_row_bf16(s_tile, ct, S);
     bool ok = true;
-    float gam = 1.f;
-    // gamma of chunk 0 (read before S_READY lets the stage be recycled)
+    // per-chunk scalars read while the chunk's stage is certainly resident:
+    // gamma (all), e^{G_r} of the output row (warps 4-5)
+    float gam = 1.f, eg = 1.f;
     if (nloc > 0) {
       ok = mbar_wait(&bars[B_FULL0], 0, abort_flag);
-      gam = reinterpret_cast<const float*>(sm + OFF_VEC)[VEC_GAMMA];
+      const float* vec = reinterpret_cast<const float*>(sm + OFF_VEC);
+      gam = vec[VEC_GAMMA];
+      eg = vec[VEC_EG + (ct & 63)];
     }
     fence_proxy_async();
     mbar_arrive(&bars[B_SREADY]);
     for (int i = 0; i < nloc; ++i) {
-      const int b = i & 1;
+      const int b = i & 1, s = i & 1;
       const long long t0 = bos + (long long)(c_begin + i) * C;
       const int len = (int)min((long long)C, eos - t0);
-      if (cw < 2) {
-        // U = U0 - W S^T (rows 0-63 of the accumulator) -> bf16 U tile
-        const int r = ct;
+      if (cw >= 2) {
+        // U = U0 - W S^T (rows 64-127 of the accumulator)
+        const int r = ct - 64;
         bool ok1 = ok && mbar_wait(&bars[B_D1FULL0 + b], (i >> 1) & 1, abort_flag);
         ok1 = bar_and(3, 64, ok1);
         if (ok1) {
           tc_fence_after();
+          const float dec = reinterpret_cast<const float*>(sm + OFF_VEC)[
+              s * VEC_FLOATS + VEC_DEC + r];
           float u[64];
           tmem_ld64(tmem + TM_D1 + 64 * b + lanes, u);
           store_row_bf16(sm + OFF_U, r, u);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) u[c] *= dec;
+          store_row_bf16(sm + OFF_UD, r, u);
           fence_proxy_async();
           tc_fence_before();
           mbar_arrive(&bars[B_UREADY]);
@@ -748,34 +733,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 64; ++c) S[c] = fmaf(gam, S[c], dl[c]);
       }
       store_row_bf16(s_tile, ct, S);
+      const float eg_now = eg;
       if (i + 1 < nloc) {
         ok = mbar_wait(&bars[B_FULL0 + (b ^ 1)], ((i + 1) >> 1) & 1, abort_flag);
-        gam = reinterpret_cast<const float*>(sm + OFF_VEC)[(b ^ 1) * VEC_FLOATS +
-                                                           VEC_GAMMA];
+        const float* vec =
+            reinterpret_cast<const float*>(sm + OFF_VEC) + (b ^ 1) * VEC_FLOATS;
+        gam = vec[VEC_GAMMA];
+        eg = vec[VEC_EG + (ct & 63)];
       }
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&bars[B_SREADY]);
-      if (cw >= 2) {
-        const int r = ct - 64;
+      if (cw < 2) {
+        // O = e^{G_r} H + P U
+        const int r = ct;
         bool ok4 = ok && mbar_wait(&bars[B_D3FULL0 + b], (i >> 1) & 1, abort_flag);
         ok4 = bar_and(4, 64, ok4);
         if (ok4) {
           tc_fence_after();
-          float o[64];
-          tmem_ld64(tmem + TM_D1 + 64 * b + lanes, o);
-          if (emit && r < len) {
-            uint4* dst = reinterpret_cast<uint4*>(
-                static_cast<__nv_bfloat16*>(p.out) +
-                ((size_t)(t0 + r) * H + h) * dv + row0);
+          const bool store = emit && r < len;
+          uint4* dst = reinterpret_cast<uint4*>(
+              static_cast<__nv_bfloat16*>(p.out) +
+              ((size_t)(t0 + (store ? r : 0)) * H + h) * dv + row0);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              uint4 wq;
-              wq.x = pack_bf16x2(o[8 * c + 0], o[8 * c + 1]);
-              wq.y = pack_bf16x2(o[8 * c + 2], o[8 * c + 3]);
-              wq.z = pack_bf16x2(o[8 * c + 4], o[8 * c + 5]);
-              wq.w = pack_bf16x2(o[8 * c + 6], o[8 * c + 7]);
-              dst[c] = wq;
+          for (int half = 0; half < 2; ++half) {
+            float o[32], pu[32];
+            tmem_ld32(tmem + TM_D1 + 64 * b + lanes + 32 * half, o);
+            tmem_ld32(tmem + TM_D3 + 64 * b + lanes + 32 * half, pu);
+            tmem_ld_wait();
+            if (store) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                uint4 wq;
+                wq.x = pack_bf16x2(fmaf(eg_now, o[8 * c + 0], pu[8 * c + 0]),
+                                   fmaf(eg_now, o[8 * c + 1], pu[8 * c + 1]));
+                wq.y = pack_bf16x2(fmaf(eg_now, o[8 * c + 2], pu[8 * c + 2]),
+                                   fmaf(eg_now, o[8 * c + 3], pu[8 * c + 3]));
+                wq.z = pack_bf16x2(fmaf(eg_now, o[8 * c + 4], pu[8 * c + 4]),
+                                   fmaf(eg_now, o[8 * c + 5], pu[8 * c + 5]));
+                wq.w = pack_bf16x2(fmaf(eg_now, o[8 * c + 6], pu[8 * c + 6]),
+                                   fmaf(eg_now, o[8 * c + 7], pu[8 * c + 7]));
+                dst[4 * half + c] = wq;
+              }
             }
           }
           tc_fence_before();
