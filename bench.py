@@ -70,7 +70,14 @@ WORKLOADS = {
 # DRAM traffic per launch of the dominant kernel from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and the
 # hash of the kernel source it was taken on; a changed kernel reports null.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {
+    # chunk_tc_kernel, W1, one launch (ncu --set full, profiles/chunk_tc_kernel_w1.md)
+    "w1:ef603e955bba204e": 101860864 + 12745728,
+    # decode_kernel captured at N=128 (481.3 MB), scaled x4 to N=512
+    # (traffic is proportional to the sequences processed;
+    # profiles/decode_kernel_w4.md)
+    "w4:74a5715498108110": 4 * (271674112 + 209667840),
+}
 
 
 def _kernel_source_hash(kind):
