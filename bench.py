@@ -71,11 +71,10 @@ WORKLOADS = {
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and the
 # hash of the kernel source it was taken on; a changed kernel reports null.
 MEASURED_TRAFFIC = {
-    # chunk_tc_kernel, W1, one launch (ncu --set full, profiles/chunk_tc_kernel_w1.md)
+    # chunk_tc_kernel, W1, one launch (ncu --set full)
     "w1:ef603e955bba204e": 101860864 + 12745728,
-    # decode_kernel captured at N=128 (481.3 MB), scaled x4 to N=512
-    # (traffic is proportional to the sequences processed;
-    # profiles/decode_kernel_w4.md)
+    # decode_kernel captured with --sequences 128 (481.3 MB) and scaled x4 to
+    # N=512: its traffic is proportional to the sequences processed
     "w4:74a5715498108110": 4 * (271674112 + 209667840),
 }
 
@@ -473,9 +472,15 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="w1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sequences", type=int, default=0,
+                    help="override the number of sequences of the workload "
+                         "(smaller cases for profiler captures)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
-    w = WORKLOADS[args.workload]
+    w = dict(WORKLOADS[args.workload])
+    if args.sequences > 0:
+        w["N" if w["kind"] == "decode" else "B"] = args.sequences
+        w["desc"] += f" [sequences overridden: {args.sequences}]"
     ws, rank, local = _dist()
 
     if args.impl == "reference":
