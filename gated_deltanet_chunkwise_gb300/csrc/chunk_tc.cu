@@ -1,35 +1,35 @@
 // Chunkwise Gated DeltaNet forward pass on the sm_103a tensor cores.
 //
-// One CTA owns (sequence, head, a 64-row tile of the state's d_v rows) and
-// walks the sequence's chunks (C = 64, d_k = 128) in order. The state is kept
-// transposed, S^T (d_k x 64), in fp32 registers of the "chain" warpgroup (one
-// d_k row per thread) and mirrored as bf16 in shared memory for the MMAs.
-// Per chunk (illustrated DeltaNet walk-through: UT transform, WY
-// representation, chunkwise state passing and output; scalar gate prefixes
-// of its GLA section), with D_rj = exp(G_r - G_j), G the chunk-local
-// cumulative log gate, G' = G (decay first) or G_{r-1} (decay after the
-// prediction), and every gate factor folded into an operand that is written
-// anyway (all such factors lie in (0, 1]):
+// Two kernels, in stream order (illustrated DeltaNet walk-through: UT
+// transform, WY representation, chunkwise state passing and output; scalar
+// gate prefixes of its GLA section). D_rj = exp(G_r - G_j) with G the
+// chunk-local cumulative log gate, G' = G (decay first) or G_{r-1} (decay
+// after the prediction); every gate factor lies in (0, 1] and is folded into
+// an operand that is written anyway.
 //
-//   prep   MMA0  [K;Q] K^T -> K K^T, Q K^T
-//          A = strict_lower(diag(beta) K K^T (.) D'),  T = (I + A)^{-1},
-//          P = (Q K^T) (.) D (.) M_incl,
-//          T_W = T diag(beta e^{G'}),  T_U = T diag(beta)
-//          MMA   [T_W;T_W] K -> W (twice);  [0;T_U] V -> U0 starts the
-//                chunk's accumulator (rows 64-127);  -W is stored after Q
-//   chain  MMA1  accumulator += [Q;-W] S^T -> H = Q S^T (rows 0-63),
-//                U = U0 - W S^T (rows 64-127)
-//          MMA2  K^T (diag(e^{G_L - G}) U) -> Delta;  S^T <- gamma S^T + Delta
-//          MMA3  [P;0] U -> P U;   O = diag(e^G) H + P U at read-out
+// ut_prep_kernel — fully parallel over (chunk, head), four CTAs per SM:
+//     K K^T on tcgen05,  A = strict_lower(diag(beta) K K^T (.) D'),
+//     T = (I + A)^{-1} (blocked substitution + m16n8k8 tf32 merges),
+//     T_W = T diag(beta e^{G'}),  T_U = T diag(beta)  -> HBM/L2 (bf16).
 //
+// chunk_tc_kernel — one CTA per (sequence, head, 64 state rows) walking the
+// chunks in order; the state S^T (d_k x 64) lives in fp32 registers of the
+// chain warpgroup and as bf16 in shared memory for the MMAs. Per chunk:
+//   side   [K;Q] K^T -> Q K^T -> P = (Q K^T) (.) D (.) M_incl   (bf16)
+//          [T_W;.] K -> W, stored as -W after Q;  [0;T_U] V -> U0 starts the
+//          chunk's accumulator (rows 64-127)
+//   chain  += [Q;-W] S^T -> H = Q S^T (rows 0-63), U = U0 - W S^T (64-127)
+//          K^T diag(e^{G_L - G}) U -> Delta;   S^T <- gamma S^T + Delta
+//          [P;.] U -> P U;   O = diag(e^G) H + P U at read-out
 // The serial chain per chunk is two MMA round trips and two short register
-// phases; everything else overlaps it.
+// phases; the side work overlaps it.
 //
-// Warp roles (352 threads): warps 0-3 prep, 4-7 chain, 8 TMA producer (also
-// the chunk's gate vectors), 9 issues the chain's MMAs, 10 the prep's MMAs.
-// Operand tiles are bf16 with the 128-byte swizzle; K/Q/V arrive by TMA in a
-// two-stage ring. Every wait is bounded; a CTA that gives up records
-// GDN_ERR_TIMEOUT, drains its MMAs, frees its TMEM and exits.
+// Warp roles of chunk_tc_kernel (352 threads): warps 0-3 side work (P rows,
+// -W), 4-7 chain, 8 TMA producer (also the chunk's gate vectors), 9 issues the
+// chain's MMAs, 10 the side MMAs. Operand tiles are bf16 with the 128-byte
+// swizzle; K/Q/V/T_W/T_U arrive by TMA in a two-stage ring. Every wait is
+// bounded; a CTA that gives up records GDN_ERR_TIMEOUT, drains its MMAs,
+// frees its TMEM and exits.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -45,72 +45,93 @@ using namespace tc;
 constexpr int C = 64;
 constexpr int DK = 128;
 constexpr int DVT = 64;
-constexpr int kThreads = 352;
-
-// Stage: per 64-column block of d_k, three 64-row groups K | Q | -W (the
-// first two by TMA, -W by the prep); [K;Q] and [Q;-W] are 128-row K-major
-// tiles and K alone is the N-major operand of the W and Delta products. The
-// V tile (64 x 64) follows the two column blocks.
-constexpr uint32_t ST_K = 0;
-constexpr uint32_t ST_Q = 8192;
-constexpr uint32_t ST_W = 16384;
-constexpr uint32_t ST_CB = 24576;
-constexpr uint32_t ST_V = 49152;
-constexpr uint32_t STAGE_BYTES = 57344;
-constexpr uint32_t STAGE_TMA_BYTES = 40960;
-// T buffer: T_W twice, P (even chunks), zeros, T_U, P (odd chunks), zeros;
-// [T_W;T_W], [P0;0], [0;T_U] and [P1;0] are 128-row K-major tiles.
-constexpr uint32_t TB_TW = 0, TB_TW2 = 8192, TB_P0 = 16384, TB_Z = 24576,
-                   TB_TU = 32768, TB_P1 = 40960, TB_Z2 = 49152,
-                   TB_BYTES = 57344;
-
-constexpr uint32_t OFF_STAGE = 0;
-constexpr uint32_t OFF_TB = 2 * STAGE_BYTES;               // 114688
-constexpr uint32_t OFF_S = OFF_TB + TB_BYTES;              // S^T, bf16
-constexpr uint32_t OFF_U = OFF_S + 16384;                  // U, bf16
-constexpr uint32_t OFF_UD = OFF_U + 8192;                  // diag(e^{G_L-G}) U
 constexpr int AP = 68;  // fp32 row pitch of the solve buffer
-constexpr uint32_t OFF_AT = OFF_UD + 8192;                 // A, then T (fp32)
-// Per-stage gate vectors written by the producer warp: cumulative log gate G,
+
+// Gate vectors of one chunk (written by one warp): cumulative log gate G,
 // alpha = e^g, e^G, beta e^{G'}, beta, e^{G_L - G}, e^{-G}, gamma = e^{G_L},
 // and whether e^{G_r} e^{-G_j} stays in the normal fp32 range.
 constexpr int VEC_G = 0, VEC_ALPHA = 64, VEC_EG = 128, VEC_EGPB = 192,
               VEC_BETA = 256, VEC_DEC = 320, VEC_IEG = 384, VEC_GAMMA = 448,
               VEC_SAFE = 449, VEC_FLOATS = 452;
-constexpr uint32_t OFF_VEC = OFF_AT + 64 * AP * 4;
-constexpr uint32_t OFF_BAR = OFF_VEC + 2 * VEC_FLOATS * 4;
 
-enum {
-  B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_MMA0, B_D0FREE, B_PREPT, B_WDONE,
-  B_PREPD0, B_PREPD1, B_SREADY, B_D1FULL0, B_D1FULL1, B_UREADY, B_D2FULL,
-  B_D3FULL0, B_D3FULL1, B_D1FREE0, B_D1FREE1, B_TPFREE0, B_TPFREE1,
-  B_DRAIN_C, B_DRAIN_P, NBARS
-};
-constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;
-constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-// TMEM columns (fp32 accumulators, 128 lanes each).
-constexpr uint32_t TM_D0 = 0, TM_D1 = 64, TM_DW = 192, TM_D2 = 320,
-                   TM_D3 = 384;
-constexpr uint32_t TMEM_COLS = 512;
 
-constexpr uint32_t ID_KK = idesc_bf16(128, 64, false, false);
-constexpr uint32_t ID_KMN = idesc_bf16(128, 64, false, true);
-constexpr uint32_t ID_KMN128 = idesc_bf16(128, 128, false, true);
-constexpr uint32_t ID_MNMN = idesc_bf16(128, 64, true, true);
-
-__device__ __forceinline__ uint32_t bar_count(int b) {
-  switch (b) {
-    case B_FULL0: case B_FULL1: return 2;
-    case B_D0FREE: case B_PREPT: case B_PREPD0: case B_PREPD1: case B_SREADY:
-      return 128;
-    case B_UREADY: case B_D1FREE0: case B_D1FREE1: return 64;
-    default: return 1;
+// Gate vectors of the chunk whose first token row (token * H + head) is
+// rbase; tokens at or past len get g = 0 and beta = 0. One whole warp.
+template <int VARIANT>
+__device__ __forceinline__ void gate_vectors(const float* g, const float* beta,
+                                             size_t rbase, int H, int len,
+                                             float* vec, int lane) {
+  const unsigned fm = 0xffffffffu;
+  float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+  if (lane < len) {
+    g0 = g[rbase + (size_t)lane * H];
+    b0 = beta[rbase + (size_t)lane * H];
+  }
+  if (lane + 32 < len) {
+    g1 = g[rbase + (size_t)(lane + 32) * H];
+    b1 = beta[rbase + (size_t)(lane + 32) * H];
+  }
+  float s0 = g0, s1 = g1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float u0 = __shfl_up_sync(fm, s0, o);
+    const float u1 = __shfl_up_sync(fm, s1, o);
+    if (lane >= o) {
+      s0 += u0;
+      s1 += u1;
+    }
+  }
+  s1 += __shfl_sync(fm, s0, 31);
+  const float Gl = __shfl_sync(fm, s1, 31);
+  const float p0 = VARIANT == GDN_GATE_BEFORE_PREDICT ? s0 : s0 - g0;
+  const float p1 = VARIANT == GDN_GATE_BEFORE_PREDICT ? s1 : s1 - g1;
+  const bool in_range =
+      __all_sync(fm, s0 >= -87.f && s0 <= 87.f && s1 >= -87.f && s1 <= 87.f);
+  vec[VEC_G + lane] = s0;
+  vec[VEC_G + 32 + lane] = s1;
+  vec[VEC_ALPHA + lane] = expf(g0);
+  vec[VEC_ALPHA + 32 + lane] = expf(g1);
+  vec[VEC_EG + lane] = expf(s0);
+  vec[VEC_EG + 32 + lane] = expf(s1);
+  vec[VEC_EGPB + lane] = expf(p0) * b0;
+  vec[VEC_EGPB + 32 + lane] = expf(p1) * b1;
+  vec[VEC_BETA + lane] = b0;
+  vec[VEC_BETA + 32 + lane] = b1;
+  vec[VEC_DEC + lane] = expf(Gl - s0);
+  vec[VEC_DEC + 32 + lane] = expf(Gl - s1);
+  vec[VEC_IEG + lane] = expf(-s0);
+  vec[VEC_IEG + 32 + lane] = expf(-s1);
+  if (lane == 0) {
+    vec[VEC_GAMMA] = expf(Gl);
+    vec[VEC_SAFE] = in_range ? 1.f : 0.f;
   }
 }
 
+// Chunk `c` of the whole call -> (sequence n, chunk index within n).
+__device__ __forceinline__ void locate_chunk(const ChunkParams& p, int c,
+                                             int nch_dense, int& n, int& lc) {
+  if (!p.chunk_off) {
+    n = c / nch_dense;
+    lc = c - n * nch_dense;
+    return;
+  }
+  int lo = 0, hi = p.N;  // chunk_off[lo] <= c < chunk_off[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.chunk_off[mid] <= c) lo = mid; else hi = mid;
+  }
+  n = lo;
+  lc = c - p.chunk_off[lo];
+}
+
+__device__ __forceinline__ int chunk_base(const ChunkParams& p, int n,
+                                          int nch_dense) {
+  return p.chunk_off ? p.chunk_off[n] : n * nch_dense;
+}
+
 // AND of `v` over the threads of named barrier `id` (also a barrier).
+
 __device__ __forceinline__ bool bar_and(int id, int count, bool v) {
   uint32_t r;
   asm volatile(
@@ -284,11 +305,329 @@ __device__ __forceinline__ void solve_unit_lower(float* AT, int tid) {
   named_bar(1, 128);
 }
 
+
+// ---------------------------------------------------------------------------
+// ut_prep_kernel: T_W = T diag(beta e^{G'}) and T_U = T diag(beta) for every
+// (chunk, head), T = (I + A)^{-1}. 160 threads: warps 0-3 compute, warp 4
+// loads K tiles by TMA and writes the gate vectors (two-stage ring).
+constexpr int kPrepThreads = 160;
+constexpr uint32_t PR_STAGE = 16384;  // K: two dense 64-column blocks
+constexpr uint32_t PR_OFF_AT = 2 * PR_STAGE;
+constexpr uint32_t PR_OFF_VEC = PR_OFF_AT + 64 * AP * 4;
+constexpr uint32_t PR_OFF_BAR = PR_OFF_VEC + 2 * VEC_FLOATS * 4;
+enum { PB_FULL0, PB_FULL1, PB_EMPTY0, PB_EMPTY1, PB_MMA, PB_DRAIN, PB_N };
+constexpr uint32_t PR_OFF_MISC = PR_OFF_BAR + PB_N * 8;
+constexpr uint32_t PR_SMEM_BYTES = PR_OFF_MISC + 16 + 1024;
+constexpr uint32_t ID_PREP = idesc_bf16(128, 64, false, false);
+
+template <int VARIANT>
+__global__ void __launch_bounds__(kPrepThreads, 4)
+    ut_prep_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tmk,
+                   int nch_dense, int total_chunks_bound) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PR_OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PR_OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + PR_OFF_MISC + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = p.H;
+  // an invalid packing (already recorded as GDN_ERR_INVALID_ARG) can count
+  // more chunks than the workspace holds: never write past it
+  const int total_chunks =
+      p.chunk_off ? min(p.chunk_off[p.N], total_chunks_bound) : total_chunks_bound;
+  const int items = total_chunks * H;
+
+  if (tid == 0) {
+    mbar_init(&bars[PB_FULL0], 2);
+    mbar_init(&bars[PB_FULL1], 2);
+    mbar_init(&bars[PB_EMPTY0], 1);
+    mbar_init(&bars[PB_EMPTY1], 1);
+    mbar_init(&bars[PB_MMA], 1);
+    mbar_init(&bars[PB_DRAIN], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(tmem_slot, 64);
+    tmem_relinquish();
+    if (lane == 0) prefetch_tmap(&tmk);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    int li = 0;
+    for (int it = blockIdx.x; it < items; it += gridDim.x, ++li) {
+      const int s = li & 1;
+      if (li >= 2 && !mbar_wait(&bars[PB_EMPTY0 + s], ((li >> 1) - 1) & 1,
+                                abort_flag))
+        break;
+      const int c = it / H, h = it - (it / H) * H;
+      int n, lc;
+      locate_chunk(p, c, nch_dense, n, lc);
+      long long bos, eos;
+      if (!sequence_range(p, n, bos, eos)) bos = eos = 0;
+      const long long t0 = bos + (long long)lc * C;
+      const int len = (int)max(0ll, min((long long)C, eos - t0));
+      uint64_t* full = &bars[PB_FULL0 + s];
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full, PR_STAGE);
+        uint8_t* st = sm + s * PR_STAGE;
+        tma_load_3d(st, &tmk, full, 0, h, (int)t0);
+        tma_load_3d(st + 8192, &tmk, full, 64, h, (int)t0);
+      }
+      gate_vectors<VARIANT>(p.g, p.beta, (size_t)t0 * H + h, H, len,
+                            reinterpret_cast<float*>(sm + PR_OFF_VEC) + s * VEC_FLOATS,
+                            lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full);
+    }
+    if (lane == 0 && li > 0)
+      for (int i = max(0, li - 2); i < li; ++i)
+        wait_ignoring_abort(&bars[PB_FULL0 + (i & 1)], (i >> 1) & 1);
+  } else {
+    float* AT = reinterpret_cast<float*>(sm + PR_OFF_AT);
+    int li = 0;
+    for (int it = blockIdx.x; it < items; it += gridDim.x, ++li) {
+      const int s = li & 1;
+      const float* vec =
+          reinterpret_cast<const float*>(sm + PR_OFF_VEC) + s * VEC_FLOATS;
+      bool ok = mbar_wait(&bars[PB_FULL0 + s], (li >> 1) & 1, abort_flag);
+      if (!bar_and(1, 128, ok)) break;
+      if (tid == 0) {
+        // K K^T (rows 0-63 of a 128-row MMA; rows 64-127 are discarded)
+        tc_fence_after();
+        const uint32_t st = base + s * PR_STAGE;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t a = sdesc(st + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
+          mma_bf16(tmem, a, a, ID_PREP, k > 0);
+        }
+        mma_commit(&bars[PB_MMA]);
+      }
+      ok = mbar_wait(&bars[PB_MMA], li & 1, abort_flag);
+      if (!bar_and(1, 128, ok)) break;
+      tc_fence_after();
+      if (warp < 2) {
+        // row r of A: beta_r exp(G'_r - G_j) k_r.k_j for j < r, in two
+        // 32-column halves (high half first so the fallback's running decay
+        // product runs from the diagonal down)
+        const int r = tid;
+        const bool safe = vec[VEC_SAFE] != 0.f;
+        const float er = vec[VEC_EGPB + r];
+        const float br = vec[VEC_BETA + r];
+        const float* alpha = vec + VEC_ALPHA;
+        float d = 1.f;
+#pragma unroll
+        for (int hf = 1; hf >= 0; --hf) {
+          float x[32];
+          tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * hf, x);
+          tmem_ld_wait();
+          if (safe) {
+            const float4* w4 = reinterpret_cast<const float4*>(vec + VEC_IEG + 32 * hf);
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 w = w4[c4];
+              const int j = 32 * hf + 4 * c4;
+              x[4 * c4] = j < r ? er * w.x * x[4 * c4] : 0.f;
+              x[4 * c4 + 1] = j + 1 < r ? er * w.y * x[4 * c4 + 1] : 0.f;
+              x[4 * c4 + 2] = j + 2 < r ? er * w.z * x[4 * c4 + 2] : 0.f;
+              x[4 * c4 + 3] = j + 3 < r ? er * w.w * x[4 * c4 + 3] : 0.f;
+            }
+          } else {
+            // D'_rj = prod of alpha over (j, r] (decay first) or [j, r)
+#pragma unroll
+            for (int e = 31; e >= 0; --e) {
+              const int jj = 32 * hf + e;
+              float a = 0.f;
+              if (jj < r) {
+                if (VARIANT == GDN_GATE_BEFORE_PREDICT) {
+                  d *= alpha[jj + 1];
+                  a = br * d * x[e];
+                } else {
+                  a = br * d * x[e];
+                  d *= alpha[jj];
+                }
+              }
+              x[e] = a;
+            }
+          }
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4)
+            *reinterpret_cast<float4*>(AT + r * AP + 32 * hf + 4 * c4) =
+                make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
+        }
+        tc_fence_before();
+      }
+      named_bar(1, 128);
+      solve_unit_lower(AT, tid);
+      {
+        // T_W and T_U rows to global memory: thread (r, half) writes 32
+        // columns of each (64 bytes, four 16-byte stores)
+        const int r = tid >> 1, hh = tid & 1;
+        const int c = it / H, h = it - (it / H) * H;
+        const size_t tile = ((size_t)c * H + h) * 64 * 64;
+        __nv_bfloat16* tw = static_cast<__nv_bfloat16*>(p.tw) + tile + r * 64 + hh * 32;
+        __nv_bfloat16* tu = static_cast<__nv_bfloat16*>(p.tu) + tile + r * 64 + hh * 32;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float f[8], fw[8], fu[8];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int c0 = hh * 32 + 8 * q4 + 4 * h2;
+            const float4 t4 = *reinterpret_cast<const float4*>(AT + r * AP + c0);
+            const float4 w4 = *reinterpret_cast<const float4*>(vec + VEC_EGPB + c0);
+            const float4 u4 = *reinterpret_cast<const float4*>(vec + VEC_BETA + c0);
+            f[4 * h2] = t4.x; f[4 * h2 + 1] = t4.y; f[4 * h2 + 2] = t4.z; f[4 * h2 + 3] = t4.w;
+            fw[4 * h2] = w4.x; fw[4 * h2 + 1] = w4.y; fw[4 * h2 + 2] = w4.z; fw[4 * h2 + 3] = w4.w;
+            fu[4 * h2] = u4.x; fu[4 * h2 + 1] = u4.y; fu[4 * h2 + 2] = u4.z; fu[4 * h2 + 3] = u4.w;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int col = hh * 32 + 8 * q4 + e;
+            f[e] = col < r ? f[e] : (col == r ? 1.f : 0.f);
+          }
+          uint4 a, u;
+          a.x = pack_bf16x2(f[0] * fw[0], f[1] * fw[1]);
+          a.y = pack_bf16x2(f[2] * fw[2], f[3] * fw[3]);
+          a.z = pack_bf16x2(f[4] * fw[4], f[5] * fw[5]);
+          a.w = pack_bf16x2(f[6] * fw[6], f[7] * fw[7]);
+          u.x = pack_bf16x2(f[0] * fu[0], f[1] * fu[1]);
+          u.y = pack_bf16x2(f[2] * fu[2], f[3] * fu[3]);
+          u.z = pack_bf16x2(f[4] * fu[4], f[5] * fu[5]);
+          u.w = pack_bf16x2(f[6] * fu[6], f[7] * fu[7]);
+          reinterpret_cast<uint4*>(tw)[q4] = a;
+          reinterpret_cast<uint4*>(tu)[q4] = u;
+        }
+      }
+      named_bar(1, 128);  // stage, vec and A/T buffer free for the next item
+      if (tid == 0) mbar_arrive(&bars[PB_EMPTY0 + s]);
+    }
+    if (tid == 0) {
+      mma_commit(&bars[PB_DRAIN]);
+      wait_ignoring_abort(&bars[PB_DRAIN], 0);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+  if (tid == 0 && *abort_flag) record_status(p.status, GDN_ERR_TIMEOUT);
+}
+
+// Exclusive prefix of per-sequence chunk counts: chunk_off[n] = sum_{m<n}
+// ceil(len_m / C), chunk_off[N] = total. One CTA.
+__global__ void __launch_bounds__(1024)
+    chunk_offsets_kernel(const int32_t* cu_seqlens, int N, int T,
+                         int32_t* chunk_off, int* status) {
+  __shared__ int carry;
+  __shared__ int warp_sums[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < N; base += blockDim.x) {
+    const int n = base + tid;
+    int v = 0;
+    if (n < N) {
+      const int b = cu_seqlens[n], e = cu_seqlens[n + 1];
+      if (b < 0 || e < b || e > T) {
+        record_status(status, GDN_ERR_INVALID_ARG);
+      } else {
+        v = (e - b + C - 1) / C;
+      }
+    }
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sums[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int incl = x + (warp > 0 ? warp_sums[warp - 1] : 0);
+    if (n < N) chunk_off[n] = carry + incl - v;
+    __syncthreads();
+    if (tid == (int)blockDim.x - 1) carry += incl;
+    __syncthreads();
+  }
+  if (tid == 0) chunk_off[N] = carry;
+}
+
+
+// ---------------------------------------------------------------------------
+// chunk_tc_kernel: the serial chain (see the top of this file).
+constexpr int kThreads = 352;
+// Stage: per 64-column block of d_k, three 64-row groups K | Q | -W (K, Q by
+// TMA, -W by the side warps): [K;Q] and [Q;-W] are 128-row K-major tiles and
+// K alone is the N-major operand of the W and Delta products. Then V, a zero
+// block, T_U ([0;T_U] is a 128-row tile), P and T_W (by TMA; [P;T_W] and
+// [T_W;...] are 128-row tiles whose second half only feeds discarded rows).
+constexpr uint32_t ST_K = 0, ST_Q = 8192, ST_W = 16384, ST_CB = 24576;
+constexpr uint32_t ST_V = 49152, ST_Z = 57344, ST_TU = 65536, ST_P = 73728,
+                   ST_TW = 81920;
+constexpr uint32_t STAGE_BYTES = 90112;
+constexpr uint32_t STAGE_TMA_BYTES = 57344;  // K, Q, V, T_W, T_U
+
+constexpr uint32_t OFF_STAGE = 0;
+constexpr uint32_t OFF_S = 2 * STAGE_BYTES;   // S^T, bf16 (N-major B)
+constexpr uint32_t OFF_U = OFF_S + 16384;     // U, bf16
+constexpr uint32_t OFF_UD = OFF_U + 8192;     // diag(e^{G_L-G}) U, bf16
+constexpr uint32_t OFF_VEC = OFF_UD + 8192;
+constexpr uint32_t OFF_BAR = OFF_VEC + 2 * VEC_FLOATS * 4;
+
+enum {
+  B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_MMA0, B_D0FREE, B_WDONE, B_DWFREE,
+  B_SIDE0, B_SIDE1, B_SREADY, B_D1FULL0, B_D1FULL1, B_UDREADY, B_UREADY,
+  B_D2FULL, B_D3FULL0, B_D3FULL1, B_D1FREE0, B_D1FREE1, B_DRAIN_C, B_DRAIN_S,
+  NBARS
+};
+constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+// TMEM columns (fp32 accumulators, 128 lanes each).
+constexpr uint32_t TM_D0 = 0, TM_DW = 64, TM_D1 = 192, TM_D2 = 320,
+                   TM_D3 = 384;
+constexpr uint32_t TMEM_COLS = 512;
+
+constexpr uint32_t ID_KK = idesc_bf16(128, 64, false, false);
+constexpr uint32_t ID_KMN = idesc_bf16(128, 64, false, true);
+constexpr uint32_t ID_KMN128 = idesc_bf16(128, 128, false, true);
+constexpr uint32_t ID_MNMN = idesc_bf16(128, 64, true, true);
+
+__device__ __forceinline__ uint32_t bar_count(int b) {
+  switch (b) {
+    case B_FULL0: case B_FULL1: return 2;
+    case B_SIDE0: case B_SIDE1: case B_SREADY: return 128;
+    case B_D0FREE: case B_DWFREE: case B_UDREADY: case B_UREADY:
+    case B_D1FREE0: case B_D1FREE1: return 64;
+    default: return 1;
+  }
+}
+
 template <int VARIANT>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk,
-                    const __grid_constant__ CUtensorMap tmv) {
+                    const __grid_constant__ CUtensorMap tmv,
+                    const __grid_constant__ CUtensorMap tmtw,
+                    const __grid_constant__ CUtensorMap tmtu, int nch_dense) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -323,11 +662,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (tid < 128) {
-    // the two zero blocks of the T buffer
+    // zero blocks of both stages; V tiles too for rows of the scaling matrix
     const uint4 z = make_uint4(0, 0, 0, 0);
     for (int i = tid; i < 1024; i += 128) {
-      const uint32_t off = (i < 512 ? TB_Z : TB_Z2) + (uint32_t)(i & 511) * 16;
-      *reinterpret_cast<uint4*>(sm + OFF_TB + off) = z;
+      const uint32_t st = (i >> 9) * STAGE_BYTES;
+      *reinterpret_cast<uint4*>(sm + st + ST_Z + (i & 511) * 16) = z;
+      if (scale_rows) *reinterpret_cast<uint4*>(sm + st + ST_V + (i & 511) * 16) = z;
     }
   }
   if (warp == 9) {
@@ -338,6 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmq);
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
+    prefetch_tmap(&tmtw);
+    prefetch_tmap(&tmtu);
   }
   fence_proxy_async();
   tc_fence_before();
@@ -345,6 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   auto stage = [&](int i) { return base + OFF_STAGE + (i & 1) * STAGE_BYTES; };
+  const int cbase = nloc > 0 ? chunk_base(p, n, nch_dense) + c_begin : 0;
 
   if (warp == 8) {
     // ================= TMA producer + gate vectors =================
@@ -359,63 +702,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* st = sm + OFF_STAGE + s * STAGE_BYTES;
       uint64_t* full = &bars[B_FULL0 + s];
       if (lane == 0) {
-        mbar_arrive_expect_tx(full, STAGE_TMA_BYTES);
+        mbar_arrive_expect_tx(full, STAGE_TMA_BYTES - (scale_rows ? 8192u : 0u));
         const int tok = (int)t0;
+        const int tz = (cbase + i) * H + h;
         tma_load_3d(st + ST_K, &tmk, full, 0, h, tok);
         tma_load_3d(st + ST_K + ST_CB, &tmk, full, 64, h, tok);
         tma_load_3d(st + ST_Q, &tmq, full, 0, h, tok);
         tma_load_3d(st + ST_Q + ST_CB, &tmq, full, 64, h, tok);
-        tma_load_3d(st + ST_V, &tmv, full, value_rows ? row0 : 0, h, tok);
+        if (!scale_rows) tma_load_3d(st + ST_V, &tmv, full, row0, h, tok);
+        tma_load_3d(st + ST_TW, &tmtw, full, 0, 0, tz);
+        tma_load_3d(st + ST_TU, &tmtu, full, 0, 0, tz);
       }
-      {
-        // gate vectors (tokens past the end: g = 0, beta = 0)
-        const unsigned fm = 0xffffffffu;
-        float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-        const size_t rbase = (size_t)t0 * H + h;
-        if (lane < len) {
-          g0 = p.g[rbase + (size_t)lane * H];
-          b0 = p.beta[rbase + (size_t)lane * H];
-        }
-        if (lane + 32 < len) {
-          g1 = p.g[rbase + (size_t)(lane + 32) * H];
-          b1 = p.beta[rbase + (size_t)(lane + 32) * H];
-        }
-        float s0 = g0, s1 = g1;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float u0 = __shfl_up_sync(fm, s0, o);
-          const float u1 = __shfl_up_sync(fm, s1, o);
-          if (lane >= o) {
-            s0 += u0;
-            s1 += u1;
-          }
-        }
-        s1 += __shfl_sync(fm, s0, 31);
-        const float Gl = __shfl_sync(fm, s1, 31);
-        const float p0 = VARIANT == GDN_GATE_BEFORE_PREDICT ? s0 : s0 - g0;
-        const float p1 = VARIANT == GDN_GATE_BEFORE_PREDICT ? s1 : s1 - g1;
-        const bool in_range = __all_sync(
-            fm, s0 >= -87.f && s0 <= 87.f && s1 >= -87.f && s1 <= 87.f);
-        float* vec = reinterpret_cast<float*>(sm + OFF_VEC) + s * VEC_FLOATS;
-        vec[VEC_G + lane] = s0;
-        vec[VEC_G + 32 + lane] = s1;
-        vec[VEC_ALPHA + lane] = expf(g0);
-        vec[VEC_ALPHA + 32 + lane] = expf(g1);
-        vec[VEC_EG + lane] = expf(s0);
-        vec[VEC_EG + 32 + lane] = expf(s1);
-        vec[VEC_EGPB + lane] = expf(p0) * b0;
-        vec[VEC_EGPB + 32 + lane] = expf(p1) * b1;
-        vec[VEC_BETA + lane] = b0;
-        vec[VEC_BETA + 32 + lane] = b1;
-        vec[VEC_DEC + lane] = expf(Gl - s0);
-        vec[VEC_DEC + 32 + lane] = expf(Gl - s1);
-        vec[VEC_IEG + lane] = expf(-s0);
-        vec[VEC_IEG + 32 + lane] = expf(-s1);
-        if (lane == 0) {
-          vec[VEC_GAMMA] = expf(Gl);
-          vec[VEC_SAFE] = in_range ? 1.f : 0.f;
-        }
-      }
+      gate_vectors<VARIANT>(p.g, p.beta, (size_t)t0 * H + h, H, len,
+                            reinterpret_cast<float*>(sm + OFF_VEC) + s * VEC_FLOATS,
+                            lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(full);
       issued = i + 1;
@@ -425,60 +725,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = max(0, issued - 2); i < issued; ++i)
         wait_ignoring_abort(&bars[B_FULL0 + (i & 1)], (i >> 1) & 1);
   } else if (warp == 10) {
-    // ================= prep MMAs: K K^T / Q K^T, W and U0 =================
+    // ================= side MMAs: Q K^T, W, U0 =================
     if (lane == 0 && nloc > 0) {
-      const uint32_t tb = base + OFF_TB;
-      auto mma0 = [&](int j) {
+      for (int j = 0; j < nloc; ++j) {
+        const int s = j & 1;
+        bool ok = mbar_wait(&bars[B_FULL0 + s], (j >> 1) & 1, abort_flag) &&
+                  (j == 0 || mbar_wait(&bars[B_D0FREE], (j - 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
         const uint32_t st = stage(j);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 8; ++k) {  // [K;Q] K^T (rows 64-127: Q K^T)
           const uint64_t a =
               sdesc(st + ST_K + (k >> 2) * ST_CB + (k & 3) * 32, 16, 1024);
           mma_bf16(tmem + TM_D0, a, a, ID_KK, k > 0);
         }
         mma_commit(&bars[B_MMA0]);
-      };
-      bool ok = mbar_wait(&bars[B_FULL0], 0, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        mma0(0);
-      }
-      for (int j = 0; ok && j < nloc; ++j) {
-        if (j + 1 < nloc) {
-          ok = mbar_wait(&bars[B_D0FREE], j & 1, abort_flag) &&
-               mbar_wait(&bars[B_FULL0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1,
-                         abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          mma0(j + 1);
-        }
-        ok = mbar_wait(&bars[B_PREPT], j & 1, abort_flag) &&
-             (j < 2 || mbar_wait(&bars[B_D1FREE0 + (j & 1)],
-                                 ((j >> 1) - 1) & 1, abort_flag));
+        ok = (j == 0 || mbar_wait(&bars[B_DWFREE], (j - 1) & 1, abort_flag)) &&
+             (j < 2 || mbar_wait(&bars[B_D1FREE0 + s], ((j >> 1) - 1) & 1,
+                                 abort_flag));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t st = stage(j);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)  // W (twice) = [T_W;T_W] K
-          mma_bf16(tmem + TM_DW, sdesc(tb + TB_TW + k * 32, 16, 1024),
+        for (int k = 0; k < 4; ++k)  // W = [T_W;.] K (rows 0-63)
+          mma_bf16(tmem + TM_DW, sdesc(st + ST_TW + k * 32, 16, 1024),
                    sdesc(st + ST_K + k * 2048, ST_CB, 1024), ID_KMN128, k > 0);
 #pragma unroll
         for (int k = 0; k < 4; ++k)  // U0 = [0;T_U] V starts the accumulator
-          mma_bf16(tmem + TM_D1 + 64 * (j & 1), sdesc(tb + TB_Z + k * 32, 16, 1024),
+          mma_bf16(tmem + TM_D1 + 64 * s, sdesc(st + ST_Z + k * 32, 16, 1024),
                    sdesc(st + ST_V + k * 2048, 8192, 1024), ID_KMN, k > 0);
         mma_commit(&bars[B_WDONE]);
       }
-      mma_commit(&bars[B_DRAIN_P]);
-      wait_ignoring_abort(&bars[B_DRAIN_P], 0);
+      mma_commit(&bars[B_DRAIN_S]);
+      wait_ignoring_abort(&bars[B_DRAIN_S], 0);
     }
   } else if (warp == 9) {
     // ================= chain MMAs =================
     if (lane == 0 && nloc > 0) {
-      const uint32_t tb = base + OFF_TB;
       for (int i = 0; i < nloc; ++i) {
         const int b = i & 1;
         bool ok = mbar_wait(&bars[B_SREADY], i & 1, abort_flag) &&
-                  mbar_wait(&bars[B_PREPD0 + b], (i >> 1) & 1, abort_flag);
+                  mbar_wait(&bars[B_SIDE0 + b], (i >> 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
         const uint32_t st = stage(i);
@@ -488,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    sdesc(st + ST_Q + (k >> 2) * ST_CB + (k & 3) * 32, 16, 1024),
                    sdesc(base + OFF_S + k * 2048, 8192, 1024), ID_KMN, 1);
         mma_commit(&bars[B_D1FULL0 + b]);
-        ok = mbar_wait(&bars[B_UREADY], i & 1, abort_flag);
+        ok = mbar_wait(&bars[B_UDREADY], i & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -496,160 +783,84 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16(tmem + TM_D2, sdesc(st + ST_K + k * 2048, ST_CB, 1024),
                    sdesc(base + OFF_UD + k * 2048, 8192, 1024), ID_MNMN, k > 0);
         mma_commit(&bars[B_D2FULL]);
-        mma_commit(&bars[B_EMPTY0 + b]);
-        const uint32_t pz = tb + (b ? TB_P1 : TB_P0);
+        ok = mbar_wait(&bars[B_UREADY], i & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 4; ++k)  // P U
-          mma_bf16(tmem + TM_D3 + 64 * b, sdesc(pz + k * 32, 16, 1024),
+        for (int k = 0; k < 4; ++k)  // P U (rows 0-63)
+          mma_bf16(tmem + TM_D3 + 64 * b, sdesc(st + ST_P + k * 32, 16, 1024),
                    sdesc(base + OFF_U + k * 2048, 8192, 1024), ID_KMN, k > 0);
         mma_commit(&bars[B_D3FULL0 + b]);
-        mma_commit(&bars[B_TPFREE0 + b]);
+        mma_commit(&bars[B_EMPTY0 + b]);
       }
       mma_commit(&bars[B_DRAIN_C]);
       wait_ignoring_abort(&bars[B_DRAIN_C], 0);
     }
   } else if (warp < 4) {
-    // ================= prep warpgroup =================
-    float* AT = reinterpret_cast<float*>(sm + OFF_AT);
-    uint8_t* tbuf = sm + OFF_TB;
-    const uint32_t lanes = (uint32_t)(32 * warp) << 16;
+    // ================= side warps: P rows, -W =================
     for (int j = 0; j < nloc; ++j) {
       const int s = j & 1;
+      uint8_t* st = sm + OFF_STAGE + s * STAGE_BYTES;
       const float* vec =
           reinterpret_cast<const float*>(sm + OFF_VEC) + s * VEC_FLOATS;
-      uint8_t* st = sm + OFF_STAGE + s * STAGE_BYTES;
-      // stage data and gate vectors (full), K K^T and Q K^T (MMA0)
-      bool ok = mbar_wait(&bars[B_FULL0 + s], (j >> 1) & 1, abort_flag) &&
-                mbar_wait(&bars[B_MMA0], j & 1, abort_flag);
-      if (!bar_and(1, 128, ok)) break;
-      tc_fence_after();
-      float x[64];
-      tmem_ld64(tmem + TM_D0 + lanes, x);
-      tc_fence_before();
-      mbar_arrive(&bars[B_D0FREE]);
-      // P buffer of chunk j-2 consumed
-      ok = j < 2 ||
-           mbar_wait(&bars[B_TPFREE0 + s], ((j >> 1) - 1) & 1, abort_flag);
-      if (!bar_and(1, 128, ok)) break;
-      const bool safe = vec[VEC_SAFE] != 0.f;
-      // w = e^{-G} (factored decays) or alpha (running products)
-      float w[64];
-      load_vec64(vec + (safe ? VEC_IEG : VEC_ALPHA), w);
-      if (tid < 64) {
-        // row r of A: beta_r exp(G'_r - G_j) k_r.k_j for j < r
-        const int r = tid;
-        if (safe) {
-          const float er = vec[VEC_EGPB + r];
+      bool ok;
+      if (warp >= 2) {
+        // row r of P: exp(G_r - G_j) q_r.k_j for j <= r (lanes 64-127 of D0)
+        const int r = tid - 64;
+        ok = mbar_wait(&bars[B_FULL0 + s], (j >> 1) & 1, abort_flag) &&
+             mbar_wait(&bars[B_MMA0], j & 1, abort_flag);
+        ok = bar_and(5, 64, ok);
+        if (ok) {
+          tc_fence_after();
+          float x[64], w[64];
+          tmem_ld64(tmem + TM_D0 + ((uint32_t)(32 * warp) << 16), x);
+          tc_fence_before();
+          mbar_arrive(&bars[B_D0FREE]);
+          const bool safe = vec[VEC_SAFE] != 0.f;
+          load_vec64(vec + (safe ? VEC_IEG : VEC_ALPHA), w);
+          if (safe) {
+            const float er = vec[VEC_EG + r];
 #pragma unroll
-          for (int jj = 0; jj < 64; ++jj) x[jj] = jj < r ? er * w[jj] * x[jj] : 0.f;
-        } else {
-          const float br = vec[VEC_BETA + r];
-          float d = 1.f;
-          x[63] = 0.f;
+            for (int jj = 0; jj < 64; ++jj) x[jj] = jj <= r ? er * w[jj] * x[jj] : 0.f;
+          } else {
+            float d = 1.f;
 #pragma unroll
-          for (int jj = 62; jj >= 0; --jj) {
-            float a = 0.f;
-            if (jj < r) {
-              if (VARIANT == GDN_GATE_BEFORE_PREDICT) {
-                d *= w[jj + 1];
-                a = br * d * x[jj];
-              } else {
-                a = br * d * x[jj];
+            for (int jj = 63; jj >= 0; --jj) {
+              float pv = 0.f;
+              if (jj <= r) {
+                pv = d * x[jj];
                 d *= w[jj];
               }
+              x[jj] = pv;
             }
-            x[jj] = a;
           }
+          store_row_bf16(st + ST_P, r, x);
+          fence_proxy_async();
         }
-#pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4)
-          *reinterpret_cast<float4*>(AT + r * AP + 4 * c4) =
-              make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
       } else {
-        // row r of P: exp(G_r - G_j) q_r.k_j for j <= r
-        const int r = tid - 64;
-        if (safe) {
-          const float er = vec[VEC_EG + r];
+        // -W rows after Q: lanes 0-63 of the W accumulator, 128 columns
+        const int r = tid;
+        ok = mbar_wait(&bars[B_WDONE], j & 1, abort_flag);
+        ok = bar_and(6, 64, ok);
+        if (ok) {
+          tc_fence_after();
+          float w0[64], w1[64];
+          tmem_ld64(tmem + TM_DW + ((uint32_t)(32 * warp) << 16), w0);
+          tmem_ld64(tmem + TM_DW + ((uint32_t)(32 * warp) << 16) + 64, w1);
+          tc_fence_before();
+          mbar_arrive(&bars[B_DWFREE]);
 #pragma unroll
-          for (int jj = 0; jj < 64; ++jj) x[jj] = jj <= r ? er * w[jj] * x[jj] : 0.f;
-        } else {
-          float d = 1.f;
-#pragma unroll
-          for (int jj = 63; jj >= 0; --jj) {
-            float pv = 0.f;
-            if (jj <= r) {
-              pv = d * x[jj];
-              d *= w[jj];
-            }
-            x[jj] = pv;
+          for (int c = 0; c < 64; ++c) {
+            w0[c] = -w0[c];
+            w1[c] = -w1[c];
           }
-        }
-        store_row_bf16(tbuf + (s ? TB_P1 : TB_P0), r, x);
-      }
-      named_bar(1, 128);
-      solve_unit_lower(AT, tid);
-      {
-        // T_W = T diag(beta e^{G'}) (two copies), T_U = T diag(beta)
-        const int r = tid >> 1, hh = tid & 1;
-        float f[32], fw[32], fu[32];
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 t4 =
-              *reinterpret_cast<const float4*>(AT + r * AP + hh * 32 + 4 * c4);
-          const float4 w4 = *reinterpret_cast<const float4*>(
-              vec + VEC_EGPB + hh * 32 + 4 * c4);
-          // rows of the scaling matrix see V = 0, so U0 = 0 for them
-          const float4 u4 = scale_rows
-                                ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                : *reinterpret_cast<const float4*>(
-                                      vec + VEC_BETA + hh * 32 + 4 * c4);
-          f[4 * c4] = t4.x; f[4 * c4 + 1] = t4.y;
-          f[4 * c4 + 2] = t4.z; f[4 * c4 + 3] = t4.w;
-          fw[4 * c4] = w4.x; fw[4 * c4 + 1] = w4.y;
-          fw[4 * c4 + 2] = w4.z; fw[4 * c4 + 3] = w4.w;
-          fu[4 * c4] = u4.x; fu[4 * c4 + 1] = u4.y;
-          fu[4 * c4 + 2] = u4.z; fu[4 * c4 + 3] = u4.w;
-        }
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = hh * 32 + e;
-          f[e] = col < r ? f[e] : (col == r ? 1.f : 0.f);
-        }
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 a, c;
-          a.x = pack_bf16x2(f[8 * q4 + 0] * fw[8 * q4 + 0], f[8 * q4 + 1] * fw[8 * q4 + 1]);
-          a.y = pack_bf16x2(f[8 * q4 + 2] * fw[8 * q4 + 2], f[8 * q4 + 3] * fw[8 * q4 + 3]);
-          a.z = pack_bf16x2(f[8 * q4 + 4] * fw[8 * q4 + 4], f[8 * q4 + 5] * fw[8 * q4 + 5]);
-          a.w = pack_bf16x2(f[8 * q4 + 6] * fw[8 * q4 + 6], f[8 * q4 + 7] * fw[8 * q4 + 7]);
-          c.x = pack_bf16x2(f[8 * q4 + 0] * fu[8 * q4 + 0], f[8 * q4 + 1] * fu[8 * q4 + 1]);
-          c.y = pack_bf16x2(f[8 * q4 + 2] * fu[8 * q4 + 2], f[8 * q4 + 3] * fu[8 * q4 + 3]);
-          c.z = pack_bf16x2(f[8 * q4 + 4] * fu[8 * q4 + 4], f[8 * q4 + 5] * fu[8 * q4 + 5]);
-          c.w = pack_bf16x2(f[8 * q4 + 6] * fu[8 * q4 + 6], f[8 * q4 + 7] * fu[8 * q4 + 7]);
-          const uint32_t off = sw128(r, hh * 4 + q4);
-          *reinterpret_cast<uint4*>(tbuf + TB_TW + off) = a;
-          *reinterpret_cast<uint4*>(tbuf + TB_TW2 + off) = a;
-          *reinterpret_cast<uint4*>(tbuf + TB_TU + off) = c;
+          store_row_bf16(st + ST_W, r, w0);
+          store_row_bf16(st + ST_W + ST_CB, r, w1);
+          fence_proxy_async();
         }
       }
-      fence_proxy_async();
-      mbar_arrive(&bars[B_PREPT]);
-      // -W after Q in the stage: warps 0-1 columns 0-63 (lanes 0-63),
-      // warps 2-3 columns 64-127 (lanes 64-127 hold the second copy of W)
-      ok = mbar_wait(&bars[B_WDONE], j & 1, abort_flag);
+      mbar_arrive(&bars[B_SIDE0 + s]);
       if (!bar_and(1, 128, ok)) break;
-      tc_fence_after();
-      {
-        const int cb = warp >> 1, r = tid & 63;
-        float wv[64];
-        tmem_ld64(tmem + TM_DW + lanes + 64 * cb, wv);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) wv[c] = -wv[c];
-        store_row_bf16(st + ST_W + cb * ST_CB, r, wv);
-      }
-      tc_fence_before();
-      fence_proxy_async();
-      mbar_arrive(&bars[B_PREPD0 + s]);
     }
   } else {
     // ================= chain warpgroup =================
@@ -683,22 +894,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 64; ++c) S[c] = 0.f;
     }
     store_row_bf16(s_tile, ct, S);
-    bool ok = true;
-    // per-chunk scalars read while the chunk's stage is certainly resident:
-    // gamma (all), e^{G_r} of the output row (warps 4-5)
-    float gam = 1.f, eg = 1.f;
-    if (nloc > 0) {
-      ok = mbar_wait(&bars[B_FULL0], 0, abort_flag);
-      const float* vec = reinterpret_cast<const float*>(sm + OFF_VEC);
-      gam = vec[VEC_GAMMA];
-      eg = vec[VEC_EG + (ct & 63)];
-    }
     fence_proxy_async();
     mbar_arrive(&bars[B_SREADY]);
+    bool ok = true;
     for (int i = 0; i < nloc; ++i) {
       const int b = i & 1, s = i & 1;
       const long long t0 = bos + (long long)(c_begin + i) * C;
       const int len = (int)min((long long)C, eos - t0);
+      // this chunk's scalars, read while its stage is certainly resident
+      ok = ok && mbar_wait(&bars[B_FULL0 + s], (i >> 1) & 1, abort_flag);
+      const float* vec =
+          reinterpret_cast<const float*>(sm + OFF_VEC) + s * VEC_FLOATS;
+      const float gam = vec[VEC_GAMMA];
+      const float rowf = vec[(cw < 2 ? VEC_EG : VEC_DEC) + (ct & 63)];
       if (cw >= 2) {
         // U = U0 - W S^T (rows 64-127 of the accumulator)
         const int r = ct - 64;
@@ -706,14 +914,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok1 = bar_and(3, 64, ok1);
         if (ok1) {
           tc_fence_after();
-          const float dec = reinterpret_cast<const float*>(sm + OFF_VEC)[
-              s * VEC_FLOATS + VEC_DEC + r];
-          float u[64];
+          float u[64], ud[64];
           tmem_ld64(tmem + TM_D1 + 64 * b + lanes, u);
-          store_row_bf16(sm + OFF_U, r, u);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) u[c] *= dec;
-          store_row_bf16(sm + OFF_UD, r, u);
+          for (int c = 0; c < 64; ++c) ud[c] = u[c] * rowf;
+          store_row_bf16(sm + OFF_UD, r, ud);
+          fence_proxy_async();
+          mbar_arrive(&bars[B_UDREADY]);
+          store_row_bf16(sm + OFF_U, r, u);
           fence_proxy_async();
           tc_fence_before();
           mbar_arrive(&bars[B_UREADY]);
@@ -733,14 +941,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 64; ++c) S[c] = fmaf(gam, S[c], dl[c]);
       }
       store_row_bf16(s_tile, ct, S);
-      const float eg_now = eg;
-      if (i + 1 < nloc) {
-        ok = mbar_wait(&bars[B_FULL0 + (b ^ 1)], ((i + 1) >> 1) & 1, abort_flag);
-        const float* vec =
-            reinterpret_cast<const float*>(sm + OFF_VEC) + (b ^ 1) * VEC_FLOATS;
-        gam = vec[VEC_GAMMA];
-        eg = vec[VEC_EG + (ct & 63)];
-      }
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&bars[B_SREADY]);
@@ -765,14 +965,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
                 uint4 wq;
-                wq.x = pack_bf16x2(fmaf(eg_now, o[8 * c + 0], pu[8 * c + 0]),
-                                   fmaf(eg_now, o[8 * c + 1], pu[8 * c + 1]));
-                wq.y = pack_bf16x2(fmaf(eg_now, o[8 * c + 2], pu[8 * c + 2]),
-                                   fmaf(eg_now, o[8 * c + 3], pu[8 * c + 3]));
-                wq.z = pack_bf16x2(fmaf(eg_now, o[8 * c + 4], pu[8 * c + 4]),
-                                   fmaf(eg_now, o[8 * c + 5], pu[8 * c + 5]));
-                wq.w = pack_bf16x2(fmaf(eg_now, o[8 * c + 6], pu[8 * c + 6]),
-                                   fmaf(eg_now, o[8 * c + 7], pu[8 * c + 7]));
+                wq.x = pack_bf16x2(fmaf(rowf, o[8 * c + 0], pu[8 * c + 0]),
+                                   fmaf(rowf, o[8 * c + 1], pu[8 * c + 1]));
+                wq.y = pack_bf16x2(fmaf(rowf, o[8 * c + 2], pu[8 * c + 2]),
+                                   fmaf(rowf, o[8 * c + 3], pu[8 * c + 3]));
+                wq.z = pack_bf16x2(fmaf(rowf, o[8 * c + 4], pu[8 * c + 4]),
+                                   fmaf(rowf, o[8 * c + 5], pu[8 * c + 5]));
+                wq.w = pack_bf16x2(fmaf(rowf, o[8 * c + 6], pu[8 * c + 6]),
+                                   fmaf(rowf, o[8 * c + 7], pu[8 * c + 7]));
                 dst[4 * half + c] = wq;
               }
             }
@@ -818,6 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 0 && *abort_flag) record_status(p.status, GDN_ERR_TIMEOUT);
 }
+
 
 // ---------------------------------------------------------------------------
 // Self-test: D = A * B (x2 when twice) with the layouts above, one CTA.
@@ -901,6 +1102,7 @@ __global__ void __launch_bounds__(128)
   }
 }
 
+
 // ---------------------------------------------------------------------------
 // Host side
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -919,15 +1121,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return g_encode;
 }
 
-// 3-D map over a [tokens, H, d] bf16 tensor, box = 64 features x 1 head x
-// 64 tokens, 128-byte swizzle.
-bool make_map(CUtensorMap* map, const void* ptr, int d, int H,
-              long long tokens) {
+// 3-D bf16 map, dims (d0, d1, d2) with d0 contiguous, box (64, b1, b2),
+// 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* ptr, long long d0, long long d1,
+              long long d2, uint32_t b1, uint32_t b2) {
   auto enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)tokens};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
-  cuuint32_t box[3] = {64, 1, 64};
+  cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+  cuuint64_t strides[2] = {(cuuint64_t)d0 * 2, (cuuint64_t)d0 * d1 * 2};
+  cuuint32_t box[3] = {64, b1, b2};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr),
              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -935,18 +1137,18 @@ bool make_map(CUtensorMap* map, const void* ptr, int d, int H,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int VARIANT>
-cudaError_t launch_variant(const ChunkParams& p, const CUtensorMap& mq,
-                           const CUtensorMap& mk, const CUtensorMap& mv,
-                           cudaStream_t stream) {
-  auto kern = chunk_tc_kernel<VARIANT>;
-  cudaError_t e = cudaFuncSetAttribute(
-      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  const int rows = p.mode == kModeSplit ? p.dv + DK : p.dv;
-  dim3 grid(rows / DVT, p.H, p.N * p.part_count);
-  kern<<<grid, kThreads, SMEM_BYTES, stream>>>(p, mq, mk, mv);
-  return cudaGetLastError();
+long long call_tokens(const ChunkParams& p) {
+  return p.cu_seqlens ? (long long)p.T : (long long)p.N * p.T;
+}
+
+int sm_count() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
+          cudaSuccess &&
+      v > 0)
+    return v;
+  return 148;
 }
 
 }  // namespace
@@ -956,17 +1158,87 @@ bool chunk_tc_supported(int dk, int dv, long long tokens) {
          tokens < (1ll << 31) - 64;
 }
 
-cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream) {
-  const long long tokens =
-      p.cu_seqlens ? (long long)p.T : (long long)p.N * p.T;
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.q, p.dk, p.H, tokens) ||
-      !make_map(&mk, p.k, p.dk, p.H, tokens) ||
-      !make_map(&mv, p.v, p.dv, p.H, tokens))
+int chunk_tc_nch_dense(const ChunkParams& p) { return (p.T + C - 1) / C; }
+
+long long chunk_tc_chunks_bound(const ChunkParams& p) {
+  // packed: sum of ceil(len / C) <= T / C + N
+  return p.cu_seqlens ? (long long)(p.T + C - 1) / C + p.N
+                      : (long long)p.N * chunk_tc_nch_dense(p);
+}
+
+size_t chunk_tc_workspace_bytes(const ChunkParams& p) {
+  const size_t tiles = (size_t)chunk_tc_chunks_bound(p) * p.H;
+  size_t bytes = 2 * tiles * 64 * 64 * 2;  // T_W and T_U, bf16
+  if (p.cu_seqlens) bytes += ((size_t)p.N + 1) * sizeof(int32_t) + 256;
+  return bytes;
+}
+
+void chunk_tc_bind_workspace(ChunkParams& p, void* ws) {
+  const size_t tiles = (size_t)chunk_tc_chunks_bound(p) * p.H;
+  char* c = static_cast<char*>(ws);
+  p.tw = c;
+  p.tu = c + tiles * 64 * 64 * 2;
+  p.chunk_off = p.cu_seqlens
+                    ? reinterpret_cast<int32_t*>(c + 2 * tiles * 64 * 64 * 2)
+                    : nullptr;
+}
+
+// Chunk offsets (packed calls) and the UT preparation of every chunk.
+cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
+                           int* launches) {
+  *launches = 0;
+  if (p.cu_seqlens) {
+    chunk_offsets_kernel<<<1, 1024, 0, stream>>>(
+        p.cu_seqlens, p.N, p.T, const_cast<int32_t*>(p.chunk_off), p.status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ++*launches;
+  }
+  CUtensorMap mk;
+  if (!make_map(&mk, p.k, p.dk, p.H, call_tokens(p), 1, 64))
     return cudaErrorInvalidValue;
+  const long long bound = chunk_tc_chunks_bound(p);
+  const long long items = bound * p.H;
+  const int grid = (int)std::min<long long>(items, 4ll * sm_count());
+  const int nchd = chunk_tc_nch_dense(p);
+  auto launch = [&](auto kern) {
+    cudaError_t e = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PR_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kPrepThreads, PR_SMEM_BYTES, stream>>>(p, mk, nchd, (int)bound);
+    return cudaGetLastError();
+  };
+  cudaError_t e = p.variant == GDN_GATE_AFTER_PREDICT
+                      ? launch(ut_prep_kernel<GDN_GATE_AFTER_PREDICT>)
+                      : launch(ut_prep_kernel<GDN_GATE_BEFORE_PREDICT>);
+  if (e == cudaSuccess) ++*launches;
+  return e;
+}
+
+// One pass of the chain kernel (after launch_ut_prep on the same stream).
+cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream) {
+  const long long tokens = call_tokens(p);
+  const long long tiles = chunk_tc_chunks_bound(p) * p.H;
+  CUtensorMap mq, mk, mv, mtw, mtu;
+  if (!make_map(&mq, p.q, p.dk, p.H, tokens, 1, 64) ||
+      !make_map(&mk, p.k, p.dk, p.H, tokens, 1, 64) ||
+      !make_map(&mv, p.v, p.dv, p.H, tokens, 1, 64) ||
+      !make_map(&mtw, p.tw, 64, 64, tiles, 64, 1) ||
+      !make_map(&mtu, p.tu, 64, 64, tiles, 64, 1))
+    return cudaErrorInvalidValue;
+  const int nchd = chunk_tc_nch_dense(p);
+  auto launch = [&](auto kern) {
+    cudaError_t e = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int rows = p.mode == kModeSplit ? p.dv + DK : p.dv;
+    dim3 grid(rows / DVT, p.H, p.N * p.part_count);
+    kern<<<grid, kThreads, SMEM_BYTES, stream>>>(p, mq, mk, mv, mtw, mtu, nchd);
+    return cudaGetLastError();
+  };
   return p.variant == GDN_GATE_AFTER_PREDICT
-             ? launch_variant<GDN_GATE_AFTER_PREDICT>(p, mq, mk, mv, stream)
-             : launch_variant<GDN_GATE_BEFORE_PREDICT>(p, mq, mk, mv, stream);
+             ? launch(chunk_tc_kernel<GDN_GATE_AFTER_PREDICT>)
+             : launch(chunk_tc_kernel<GDN_GATE_BEFORE_PREDICT>);
 }
 
 }  // namespace gdn
@@ -978,7 +1250,6 @@ extern "C" int gdn_selftest_mma(const void* A, const void* B, float* D, int K,
   if (!A || !B || !D || (K != 64 && K != 128) || (N != 64 && N != 128))
     return GDN_ERR_INVALID_ARG;
   if (b_stacked && N != 64) return GDN_ERR_INVALID_ARG;
-  if (b_stacked && b_mn) return GDN_ERR_INVALID_ARG;
   int* status = nullptr;
   int rc = device_status_ptr(&status);
   if (rc != GDN_OK) return rc;

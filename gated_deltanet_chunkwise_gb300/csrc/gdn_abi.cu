@@ -102,6 +102,38 @@ int choose_parts(int requested, int N, int H, int T, int dv, int C,
   return parts < 1 ? 1 : parts;
 }
 
+// Sequence-parallel split for the tensor-core path: one CTA per SM, so a
+// pass costs (waves of resident CTAs) x (chunks per sub-sequence); pick the
+// split count P that minimises split pass + corrected output pass.
+int choose_parts_tc(int requested, int N, int H, int T, int dv, int C,
+                    bool packed) {
+  if (requested > 0) return requested;
+  if (packed) return 1;
+  int sms = 148, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
+            cudaSuccess && v > 0)
+      sms = v;
+  }
+  const long long nch = (T + C - 1) / C;
+  const long long nh = (long long)N * H, tv = dv / 64, tk = 2;
+  auto waves = [&](long long ctas) { return (ctas + sms - 1) / sms; };
+  long long best = waves(nh * tv) * nch;
+  int best_p = 1;
+  for (int P = 2; P <= 64 && P <= nch; ++P) {
+    const long long per = (nch + P - 1) / P;
+    const long long split = nh * (tv + (long long)(P - 2) * (tv + tk));
+    const long long outp = nh * (P - 1) * tv;
+    const long long cost = (waves(split) + waves(outp)) * per;
+    if (cost < best) {
+      best = cost;
+      best_p = P;
+    }
+  }
+  return best_p;
+}
+
 int run_chunk(const void* q, const void* k, const void* v, const float* g,
               const float* beta, const float* h0, void* out, float* hT,
               const int32_t* cu_seqlens, int B, int H, int T, int dk, int dv,
@@ -129,32 +161,52 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
     return use_tc ? launch_chunk_tc(q, stream)
                   : launch_chunk_simt(q, bf16, stream);
   };
-  const int parts = choose_parts(sp_parts, B, H, T, dv, C, cu_seqlens != nullptr);
+  const int parts =
+      use_tc ? choose_parts_tc(sp_parts, B, H, T, dv, C, cu_seqlens != nullptr)
+             : choose_parts(sp_parts, B, H, T, dv, C, cu_seqlens != nullptr);
   p.parts = parts;
 
-  if (parts == 1) {
-    p.part_begin = 0; p.part_count = 1; p.mode = kModeOutput;
-    return counted(launch(p), 1) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
-  }
-
-  // Sequence-parallel: split pass, correction chain, corrected output pass.
+  // Workspace: UT factors (tensor-core path) and sequence-parallel states.
   const size_t nhp = (size_t)B * H * parts;
-  const size_t end_bytes = nhp * (size_t)(dv + dk) * dk * sizeof(float);
-  const size_t start_bytes = nhp * (size_t)dv * dk * sizeof(float);
+  const size_t end_bytes =
+      parts > 1 ? nhp * (size_t)(dv + dk) * dk * sizeof(float) : 0;
+  const size_t start_bytes =
+      parts > 1 ? nhp * (size_t)dv * dk * sizeof(float) : 0;
+  const size_t tc_bytes = use_tc ? chunk_tc_workspace_bytes(p) : 0;
+  const size_t total = end_bytes + start_bytes + tc_bytes;
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, end_bytes + start_bytes, stream) != cudaSuccess)
+  if (total > 0 && cudaMallocAsync(&ws, total, stream) != cudaSuccess)
     return GDN_ERR_CUDA;
-  p.ws_end = static_cast<float*>(ws);
-  p.ws_start = reinterpret_cast<float*>(static_cast<char*>(ws) + end_bytes);
-  cudaError_t e;
-  p.mode = kModeSplit; p.part_begin = 0; p.part_count = parts - 1;
-  e = counted(launch(p), 1);
-  if (e == cudaSuccess && parts > 2) e = counted(launch_sp_chain(p, stream), 1);
-  if (e == cudaSuccess) {
-    p.mode = kModeOutput; p.part_begin = 1; p.part_count = parts - 1;
-    e = counted(launch(p), 1);
+  char* wsc = static_cast<char*>(ws);
+  if (parts > 1) {
+    p.ws_end = reinterpret_cast<float*>(wsc);
+    p.ws_start = reinterpret_cast<float*>(wsc + end_bytes);
   }
-  cudaError_t f = cudaFreeAsync(ws, stream);
+  if (use_tc) chunk_tc_bind_workspace(p, wsc + end_bytes + start_bytes);
+
+  cudaError_t e = cudaSuccess;
+  if (use_tc) {
+    int n_prep = 0;
+    e = launch_ut_prep(p, stream, &n_prep);
+    counted(e, n_prep);
+  }
+  if (e == cudaSuccess) {
+    if (parts == 1) {
+      p.part_begin = 0; p.part_count = 1; p.mode = kModeOutput;
+      e = counted(launch(p), 1);
+    } else {
+      // split pass, correction chain, corrected output pass
+      p.mode = kModeSplit; p.part_begin = 0; p.part_count = parts - 1;
+      e = counted(launch(p), 1);
+      if (e == cudaSuccess && parts > 2)
+        e = counted(launch_sp_chain(p, stream), 1);
+      if (e == cudaSuccess) {
+        p.mode = kModeOutput; p.part_begin = 1; p.part_count = parts - 1;
+        e = counted(launch(p), 1);
+      }
+    }
+  }
+  cudaError_t f = ws ? cudaFreeAsync(ws, stream) : cudaSuccess;
   return (e == cudaSuccess && f == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
 }
 

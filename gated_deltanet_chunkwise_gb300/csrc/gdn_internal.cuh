@@ -46,6 +46,10 @@ struct ChunkParams {
   float* ws_end;
   float* ws_start;
   int* status;     // device status word (first error wins)
+  // tensor-core path: per-chunk UT factors and (packed calls) chunk offsets
+  const int32_t* chunk_off;  // [N + 1] first chunk of each sequence
+  void* tw;                  // [chunks, H, 64, 64] bf16, T diag(beta e^{G'})
+  void* tu;                  // [chunks, H, 64, 64] bf16, T diag(beta)
 };
 
 struct DecodeParams {
@@ -64,8 +68,14 @@ struct DecodeParams {
 cudaError_t launch_chunk_simt(const ChunkParams& p, bool bf16,
                               cudaStream_t stream);
 cudaError_t launch_sp_chain(const ChunkParams& p, cudaStream_t stream);
-// Tensor-core (tcgen05) chunk kernel: bf16, dk = 128, dv in {64, 128}.
+// Tensor-core (tcgen05) path: bf16, dk = 128, dv in {64, 128}. A call takes
+// chunk_tc_workspace_bytes of workspace (bound with chunk_tc_bind_workspace),
+// runs launch_ut_prep once, then launch_chunk_tc for each pass.
 bool chunk_tc_supported(int dk, int dv, long long tokens);
+size_t chunk_tc_workspace_bytes(const ChunkParams& p);
+void chunk_tc_bind_workspace(ChunkParams& p, void* ws);
+cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
+                           int* launches);
 cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 
