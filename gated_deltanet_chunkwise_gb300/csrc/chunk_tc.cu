@@ -7,29 +7,34 @@
 // after the prediction); every gate factor lies in (0, 1] and is folded into
 // an operand that is written anyway.
 //
-// ut_prep_kernel — fully parallel over (chunk, head), four CTAs per SM:
-//     K K^T on tcgen05,  A = strict_lower(diag(beta) K K^T (.) D'),
-//     T = (I + A)^{-1} (blocked substitution + m16n8k8 tf32 merges),
-//     T_W = T diag(beta e^{G'}),  T_U = T diag(beta)  -> HBM/L2 (bf16).
+// ut_prep_kernel — everything that does not depend on the running state,
+// fully parallel over (chunk, head), four CTAs per SM:
+//     [K;Q] K^T on tcgen05  ->  A = strict_lower(diag(beta) K K^T (.) D')
+//                               P = (Q K^T) (.) D (.) M_incl
+//     T = (I + A)^{-1} (blocked substitution + m16n8k8 tf32 merges)
+//     T_W = T diag(beta e^{G'}),  T_U = T diag(beta)
+//     W = T_W K on tcgen05
+//   and writes -W, P, T_U (bf16) and the chunk's decay vectors (fp32) for
+//   the chain kernel.
 //
 // chunk_tc_kernel — one CTA per (sequence, head, 64 state rows) walking the
 // chunks in order; the state S^T (d_k x 64) lives in fp32 registers of the
-// chain warpgroup and as bf16 in shared memory for the MMAs. Per chunk:
-//   side   [K;Q] K^T -> Q K^T -> P = (Q K^T) (.) D (.) M_incl   (bf16)
-//          [T_W;.] K -> W, stored as -W after Q;  [0;T_U] V -> U0 starts the
-//          chunk's accumulator (rows 64-127)
+// chain warps and as bf16 in shared memory for the MMAs. Per chunk:
+//   side   [0;T_U] V -> U0 starts the chunk's accumulator (rows 64-127)
 //   chain  += [Q;-W] S^T -> H = Q S^T (rows 0-63), U = U0 - W S^T (64-127)
 //          K^T diag(e^{G_L - G}) U -> Delta;   S^T <- gamma S^T + Delta
 //          [P;.] U -> P U;   O = diag(e^G) H + P U at read-out
 // The serial chain per chunk is two MMA round trips and two short register
-// phases; the side work overlaps it.
+// phases; everything else arrives by TMA.
 //
-// Warp roles of chunk_tc_kernel (352 threads): warps 0-3 side work (P rows,
-// -W), 4-7 chain, 8 TMA producer (also the chunk's gate vectors), 9 issues the
-// chain's MMAs, 10 the side MMAs. Operand tiles are bf16 with the 128-byte
-// swizzle; K/Q/V/T_W/T_U arrive by TMA in a two-stage ring. Every wait is
-// bounded; a CTA that gives up records GDN_ERR_TIMEOUT, drains its MMAs,
-// frees its TMEM and exits.
+// Warp roles of chunk_tc_kernel (320 threads): warps 0-7 the chain (state
+// rows; warps with lane quarter 2-3 also U rows, 0-1 output rows; each warp
+// takes 32 of the 64 columns; one of their threads issues the chain's own
+// MMAs right after the named barrier that completes their operands), 8 TMA
+// producer, 9 the off-chain MMAs (U0, P U). Operand tiles are bf16 with the
+// 128-byte swizzle and arrive in a two-stage ring; whole output tiles leave
+// by TMA store. Every wait is bounded; a CTA that gives up records
+// GDN_ERR_TIMEOUT, drains its MMAs, frees its TMEM and exits.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -42,6 +47,7 @@ namespace gdn {
 namespace {
 using namespace tc;
 
+
 constexpr int C = 64;
 constexpr int DK = 128;
 constexpr int DVT = 64;
@@ -53,15 +59,20 @@ constexpr int AP = 68;  // fp32 row pitch of the solve buffer
 constexpr int VEC_G = 0, VEC_ALPHA = 64, VEC_EG = 128, VEC_EGPB = 192,
               VEC_BETA = 256, VEC_DEC = 320, VEC_IEG = 384, VEC_GAMMA = 448,
               VEC_SAFE = 449, VEC_FLOATS = 452;
+// The part of them the chain kernel reads, per (chunk, head) in the
+// workspace: e^G, e^{G_L - G}, gamma (padded to a multiple of 16 bytes).
+constexpr int CV_EG = 0, CV_DEC = 64, CV_GAMMA = 128, CV_FLOATS = 132;
+constexpr uint32_t CV_BYTES = CV_FLOATS * 4;
 
 
 
 // Gate vectors of the chunk whose first token row (token * H + head) is
-// rbase; tokens at or past len get g = 0 and beta = 0. One whole warp.
+// rbase; tokens at or past len get g = 0 and beta = 0. One whole warp; the
+// chain kernel's part also goes to cv (global memory).
 template <int VARIANT>
 __device__ __forceinline__ void gate_vectors(const float* g, const float* beta,
                                              size_t rbase, int H, int len,
-                                             float* vec, int lane) {
+                                             float* vec, float* cv, int lane) {
   const unsigned fm = 0xffffffffu;
   float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
   if (lane < len) {
@@ -92,20 +103,28 @@ __device__ __forceinline__ void gate_vectors(const float* g, const float* beta,
   vec[VEC_G + 32 + lane] = s1;
   vec[VEC_ALPHA + lane] = expf(g0);
   vec[VEC_ALPHA + 32 + lane] = expf(g1);
-  vec[VEC_EG + lane] = expf(s0);
-  vec[VEC_EG + 32 + lane] = expf(s1);
   vec[VEC_EGPB + lane] = expf(p0) * b0;
   vec[VEC_EGPB + 32 + lane] = expf(p1) * b1;
   vec[VEC_BETA + lane] = b0;
   vec[VEC_BETA + 32 + lane] = b1;
-  vec[VEC_DEC + lane] = expf(Gl - s0);
-  vec[VEC_DEC + 32 + lane] = expf(Gl - s1);
+  const float e0 = expf(s0), e1 = expf(s1);
+  const float d0 = expf(Gl - s0), d1 = expf(Gl - s1);
+  const float gam = expf(Gl);
+  vec[VEC_EG + lane] = e0;
+  vec[VEC_EG + 32 + lane] = e1;
+  vec[VEC_DEC + lane] = d0;
+  vec[VEC_DEC + 32 + lane] = d1;
   vec[VEC_IEG + lane] = expf(-s0);
   vec[VEC_IEG + 32 + lane] = expf(-s1);
   if (lane == 0) {
-    vec[VEC_GAMMA] = expf(Gl);
+    vec[VEC_GAMMA] = gam;
     vec[VEC_SAFE] = in_range ? 1.f : 0.f;
   }
+  cv[CV_EG + lane] = e0;
+  cv[CV_EG + 32 + lane] = e1;
+  cv[CV_DEC + lane] = d0;
+  cv[CV_DEC + 32 + lane] = d1;
+  if (lane < 4) cv[CV_GAMMA + lane] = lane == 0 ? gam : 0.f;
 }
 
 // Chunk `c` of the whole call -> (sequence n, chunk index within n).
@@ -157,28 +176,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
   tmem_ld32(taddr, lo);
   tmem_ld32(taddr + 32, hi);
   tmem_ld_wait();
-}
-
-// Write a 64-value fp32 row as bf16 into row r of a 128-byte-row swizzled tile.
-__device__ __forceinline__ void store_row_bf16(uint8_t* tile, int r,
-                                               const float (&x)[64]) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint4 w;
-    w.x = pack_bf16x2(x[8 * c + 0], x[8 * c + 1]);
-    w.y = pack_bf16x2(x[8 * c + 2], x[8 * c + 3]);
-    w.z = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]);
-    w.w = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
-    *reinterpret_cast<uint4*>(tile + sw128(r, c)) = w;
-  }
-}
-
-__device__ __forceinline__ void load_vec64(const float* src, float (&x)[64]) {
-#pragma unroll
-  for (int c = 0; c < 16; ++c) {
-    const float4 v = reinterpret_cast<const float4*>(src)[c];
-    x[4 * c] = v.x; x[4 * c + 1] = v.y; x[4 * c + 2] = v.z; x[4 * c + 3] = v.w;
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -270,10 +267,16 @@ __device__ __forceinline__ void solve_unit_lower(float* AT, int tid) {
     if (lane < 16) {
 #pragma unroll
       for (int m = 0; m < 16; ++m) {
-        const float* arow = AT + (b + m) * AP + b;
+        const float4* arow = reinterpret_cast<const float4*>(AT + (b + m) * AP + b);
         float acc = (m == lane) ? 1.f : 0.f;
 #pragma unroll
-        for (int j = 0; j < m; ++j) acc = fmaf(-arow[j], xs[j], acc);
+        for (int q = 0; q < (m + 3) / 4; ++q) {
+          const float4 a = arow[q];  // one broadcast load for four terms
+          if (4 * q < m) acc = fmaf(-a.x, xs[4 * q], acc);
+          if (4 * q + 1 < m) acc = fmaf(-a.y, xs[4 * q + 1], acc);
+          if (4 * q + 2 < m) acc = fmaf(-a.z, xs[4 * q + 2], acc);
+          if (4 * q + 3 < m) acc = fmaf(-a.w, xs[4 * q + 3], acc);
+        }
         xs[m] = acc;
       }
     }
@@ -306,24 +309,76 @@ __device__ __forceinline__ void solve_unit_lower(float* AT, int tid) {
 }
 
 
+
+// Write 32 fp32 values as bf16 into 16-byte chunks 4 hf .. 4 hf + 3 of row r
+// of a 128-byte-row swizzled tile.
+__device__ __forceinline__ void store_half_bf16(uint8_t* tile, int r, int hf,
+                                                const float (&x)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 w;
+    w.x = pack_bf16x2(x[8 * c + 0], x[8 * c + 1]);
+    w.y = pack_bf16x2(x[8 * c + 2], x[8 * c + 3]);
+    w.z = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]);
+    w.w = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
+    *reinterpret_cast<uint4*>(tile + sw128(r, 4 * hf + c)) = w;
+  }
+}
+
+// As store_half_bf16, scaled by s.
+__device__ __forceinline__ void store_half_bf16_scaled(uint8_t* tile, int r,
+                                                       int hf,
+                                                       const float (&x)[32],
+                                                       float s) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 w;
+    w.x = pack_bf16x2(s * x[8 * c + 0], s * x[8 * c + 1]);
+    w.y = pack_bf16x2(s * x[8 * c + 2], s * x[8 * c + 3]);
+    w.z = pack_bf16x2(s * x[8 * c + 4], s * x[8 * c + 5]);
+    w.w = pack_bf16x2(s * x[8 * c + 6], s * x[8 * c + 7]);
+    *reinterpret_cast<uint4*>(tile + sw128(r, 4 * hf + c)) = w;
+  }
+}
+
+// Per-(chunk, head) operands the preparation writes for the chain kernel,
+// each the exact image of a 1024-byte-aligned shared-memory tile (64 rows of
+// 128 bytes, 128-byte swizzle) so that both sides move them with plain bulk
+// copies: -W as two 64-column blocks, P, T_U.
+constexpr uint32_t TILE_BYTES = 8192;
+constexpr uint32_t WS_W_BYTES = 2 * TILE_BYTES;
+constexpr uint32_t WS_P_BYTES = TILE_BYTES;
+constexpr uint32_t WS_TU_BYTES = TILE_BYTES;
+
 // ---------------------------------------------------------------------------
-// ut_prep_kernel: T_W = T diag(beta e^{G'}) and T_U = T diag(beta) for every
-// (chunk, head), T = (I + A)^{-1}. 160 threads: warps 0-3 compute, warp 4
-// loads K tiles by TMA and writes the gate vectors (two-stage ring).
+// ut_prep_kernel: the state-independent part of every (chunk, head).
+// 160 threads: warps 0-3 compute, warp 4 loads the K and Q tiles by TMA and
+// writes the gate vectors. One stage; four CTAs per SM hide the latencies.
 constexpr int kPrepThreads = 160;
-constexpr uint32_t PR_STAGE = 16384;  // K: two dense 64-column blocks
-constexpr uint32_t PR_OFF_AT = 2 * PR_STAGE;
+// Stage: K0 | Q0 | K1 | Q1 (8 KB each, 64-column blocks of d_k): [K_c;Q_c]
+// is a 128-row K-major tile and K (two blocks, 16 KB apart) the N-major B
+// operand of W = T_W K. Once a block's last reader is done it holds an output
+// image on its way to the workspace: P in Q0, T_U in Q1, -W in K0 and K1.
+constexpr uint32_t PR_STAGE = 32768;
+// fp32 A / T (row pitch AP); after T is read out the same bytes hold the
+// 128-row bf16 tile [T_W; T_W].
+constexpr uint32_t PR_OFF_AT = PR_STAGE;
 constexpr uint32_t PR_OFF_VEC = PR_OFF_AT + 64 * AP * 4;
 constexpr uint32_t PR_OFF_BAR = PR_OFF_VEC + 2 * VEC_FLOATS * 4;
-enum { PB_FULL0, PB_FULL1, PB_EMPTY0, PB_EMPTY1, PB_MMA, PB_DRAIN, PB_N };
+enum { PB_FULL, PB_EMPTY, PB_MMA, PB_MMAW, PB_DRAIN, PB_N };
 constexpr uint32_t PR_OFF_MISC = PR_OFF_BAR + PB_N * 8;
 constexpr uint32_t PR_SMEM_BYTES = PR_OFF_MISC + 16 + 1024;
+constexpr uint32_t PR_TMEM_COLS = 128;
 constexpr uint32_t ID_PREP = idesc_bf16(128, 64, false, false);
+constexpr uint32_t ID_PREP_W = idesc_bf16(128, 128, false, true);
+static_assert(64 * AP * 4 >= 16384, "[T_W; T_W] must fit the solve buffer");
+static_assert(PR_OFF_BAR % 8 == 0, "mbarrier alignment");
 
 template <int VARIANT>
 __global__ void __launch_bounds__(kPrepThreads, 4)
     ut_prep_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tmk,
-                   int nch_dense, int total_chunks_bound) {
+                   const __grid_constant__ CUtensorMap tmq, int nch_dense,
+                   int total_chunks_bound) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -331,6 +386,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PR_OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PR_OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + PR_OFF_MISC + 4);
+  float* vecs = reinterpret_cast<float*>(sm + PR_OFF_VEC);  // two buffers
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H;
   // an invalid packing (already recorded as GDN_ERR_INVALID_ARG) can count
@@ -340,19 +396,21 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   const int items = total_chunks * H;
 
   if (tid == 0) {
-    mbar_init(&bars[PB_FULL0], 2);
-    mbar_init(&bars[PB_FULL1], 2);
-    mbar_init(&bars[PB_EMPTY0], 1);
-    mbar_init(&bars[PB_EMPTY1], 1);
+    mbar_init(&bars[PB_FULL], 1);
+    mbar_init(&bars[PB_EMPTY], 1);
     mbar_init(&bars[PB_MMA], 1);
+    mbar_init(&bars[PB_MMAW], 1);
     mbar_init(&bars[PB_DRAIN], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 4) {
-    tmem_alloc(tmem_slot, 64);
+    tmem_alloc(tmem_slot, PR_TMEM_COLS);
     tmem_relinquish();
-    if (lane == 0) prefetch_tmap(&tmk);
+    if (lane == 0) {
+      prefetch_tmap(&tmk);
+      prefetch_tmap(&tmq);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -360,12 +418,11 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 4) {
+    // ================= TMA producer + gate vectors =================
+    // The gate vectors of item li go to buffer li & 1 (free since item li - 2
+    // finished) before the wait for the stage, so they overlap item li - 1.
     int li = 0;
     for (int it = blockIdx.x; it < items; it += gridDim.x, ++li) {
-      const int s = li & 1;
-      if (li >= 2 && !mbar_wait(&bars[PB_EMPTY0 + s], ((li >> 1) - 1) & 1,
-                                abort_flag))
-        break;
       const int c = it / H, h = it - (it / H) * H;
       int n, lc;
       locate_chunk(p, c, nch_dense, n, lc);
@@ -373,38 +430,50 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       if (!sequence_range(p, n, bos, eos)) bos = eos = 0;
       const long long t0 = bos + (long long)lc * C;
       const int len = (int)max(0ll, min((long long)C, eos - t0));
-      uint64_t* full = &bars[PB_FULL0 + s];
-      if (lane == 0) {
-        mbar_arrive_expect_tx(full, PR_STAGE);
-        uint8_t* st = sm + s * PR_STAGE;
-        tma_load_3d(st, &tmk, full, 0, h, (int)t0);
-        tma_load_3d(st + 8192, &tmk, full, 64, h, (int)t0);
-      }
       gate_vectors<VARIANT>(p.g, p.beta, (size_t)t0 * H + h, H, len,
-                            reinterpret_cast<float*>(sm + PR_OFF_VEC) + s * VEC_FLOATS,
-                            lane);
+                            vecs + (li & 1) * VEC_FLOATS,
+                            p.cv + (size_t)it * CV_FLOATS, lane);
       __syncwarp();
-      if (lane == 0) mbar_arrive(full);
+      if (li >= 1 && !mbar_wait(&bars[PB_EMPTY], (li - 1) & 1, abort_flag)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[PB_FULL], PR_STAGE);
+        tma_load_3d(sm, &tmk, &bars[PB_FULL], 0, h, (int)t0);
+        tma_load_3d(sm + 8192, &tmq, &bars[PB_FULL], 0, h, (int)t0);
+        tma_load_3d(sm + 16384, &tmk, &bars[PB_FULL], 64, h, (int)t0);
+        tma_load_3d(sm + 24576, &tmq, &bars[PB_FULL], 64, h, (int)t0);
+        // the CTA's next item into L2 while this one is processed
+        const int nx = it + gridDim.x;
+        if (nx < items) {
+          const int c2 = nx / H, h2 = nx - (nx / H) * H;
+          int n2, lc2;
+          locate_chunk(p, c2, nch_dense, n2, lc2);
+          long long b2, e2;
+          if (sequence_range(p, n2, b2, e2)) {
+            const int tok2 = (int)(b2 + (long long)lc2 * C);
+            prefetch_l2_3d(&tmk, 0, h2, tok2);
+            prefetch_l2_3d(&tmk, 64, h2, tok2);
+            prefetch_l2_3d(&tmq, 0, h2, tok2);
+            prefetch_l2_3d(&tmq, 64, h2, tok2);
+          }
+        }
+      }
     }
-    if (lane == 0 && li > 0)
-      for (int i = max(0, li - 2); i < li; ++i)
-        wait_ignoring_abort(&bars[PB_FULL0 + (i & 1)], (i >> 1) & 1);
+    // never leave with a TMA copy still landing in shared memory
+    if (lane == 0 && li > 0) wait_ignoring_abort(&bars[PB_FULL], (li - 1) & 1);
   } else {
+    // ================= compute warps =================
     float* AT = reinterpret_cast<float*>(sm + PR_OFF_AT);
     int li = 0;
     for (int it = blockIdx.x; it < items; it += gridDim.x, ++li) {
-      const int s = li & 1;
-      const float* vec =
-          reinterpret_cast<const float*>(sm + PR_OFF_VEC) + s * VEC_FLOATS;
-      bool ok = mbar_wait(&bars[PB_FULL0 + s], (li >> 1) & 1, abort_flag);
+      bool ok = mbar_wait(&bars[PB_FULL], li & 1, abort_flag);
       if (!bar_and(1, 128, ok)) break;
+      const float* vec = vecs + (li & 1) * VEC_FLOATS;
       if (tid == 0) {
-        // K K^T (rows 0-63 of a 128-row MMA; rows 64-127 are discarded)
+        // [K;Q] K^T: rows 0-63 K K^T, rows 64-127 Q K^T
         tc_fence_after();
-        const uint32_t st = base + s * PR_STAGE;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint64_t a = sdesc(st + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024);
+          const uint64_t a = sdesc(base + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
           mma_bf16(tmem, a, a, ID_PREP, k > 0);
         }
         mma_commit(&bars[PB_MMA]);
@@ -412,6 +481,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       ok = mbar_wait(&bars[PB_MMA], li & 1, abort_flag);
       if (!bar_and(1, 128, ok)) break;
       tc_fence_after();
+      const size_t tile = (size_t)it;  // it = chunk * H + head
       if (warp < 2) {
         // row r of A: beta_r exp(G'_r - G_j) k_r.k_j for j < r, in two
         // 32-column halves (high half first so the fallback's running decay
@@ -461,62 +531,140 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
             *reinterpret_cast<float4*>(AT + r * AP + 32 * hf + 4 * c4) =
                 make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
         }
-        tc_fence_before();
+      } else {
+        // row r of P: exp(G_r - G_j) q_r.k_j for j <= r (lanes 64-127), to
+        // the workspace as bf16
+        const int r = tid - 64;
+        const bool safe = vec[VEC_SAFE] != 0.f;
+        const float er = vec[VEC_EG + r];
+        const float* alpha = vec + VEC_ALPHA;
+        uint8_t* ptile = sm + 8192;  // Q0: read by the K K^T MMA only
+        float d = 1.f;
+#pragma unroll
+        for (int hf = 1; hf >= 0; --hf) {
+          float x[32];
+          tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * hf, x);
+          tmem_ld_wait();
+          if (safe) {
+            const float4* w4 = reinterpret_cast<const float4*>(vec + VEC_IEG + 32 * hf);
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 w = w4[c4];
+              const int j = 32 * hf + 4 * c4;
+              x[4 * c4] = j <= r ? w.x * x[4 * c4] : 0.f;
+              x[4 * c4 + 1] = j + 1 <= r ? w.y * x[4 * c4 + 1] : 0.f;
+              x[4 * c4 + 2] = j + 2 <= r ? w.z * x[4 * c4 + 2] : 0.f;
+              x[4 * c4 + 3] = j + 3 <= r ? w.w * x[4 * c4 + 3] : 0.f;
+            }
+            store_half_bf16_scaled(ptile, r, hf, x, er);
+          } else {
+            // D_rj = prod of alpha over (j, r]
+#pragma unroll
+            for (int e = 31; e >= 0; --e) {
+              const int jj = 32 * hf + e;
+              float pv = 0.f;
+              if (jj <= r) {
+                pv = d * x[e];
+                d *= alpha[jj];
+              }
+              x[e] = pv;
+            }
+            store_half_bf16(ptile, r, hf, x);
+          }
+        }
       }
+      fence_proxy_async();
+      tc_fence_before();
       named_bar(1, 128);
       solve_unit_lower(AT, tid);
       {
-        // T_W and T_U rows to global memory: thread (r, half) writes 32
-        // columns of each (64 bytes, four 16-byte stores)
-        const int r = tid >> 1, hh = tid & 1;
-        const int c = it / H, h = it - (it / H) * H;
-        const size_t tile = ((size_t)c * H + h) * 64 * 64;
-        __nv_bfloat16* tw = static_cast<__nv_bfloat16*>(p.tw) + tile + r * 64 + hh * 32;
-        __nv_bfloat16* tu = static_cast<__nv_bfloat16*>(p.tu) + tile + r * 64 + hh * 32;
+        // T_W rows into the [T_W; T_W] operand tile (over the solve buffer,
+        // so every thread reads its part of T first), T_U rows into Q1.
+        // Thread (r, hh) handles columns 32 hh .. 32 hh + 31.
+        const int r = tid & 63, hh = tid >> 6;
+        float t[32];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float f[8], fw[8], fu[8];
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int c0 = hh * 32 + 8 * q4 + 4 * h2;
-            const float4 t4 = *reinterpret_cast<const float4*>(AT + r * AP + c0);
-            const float4 w4 = *reinterpret_cast<const float4*>(vec + VEC_EGPB + c0);
-            const float4 u4 = *reinterpret_cast<const float4*>(vec + VEC_BETA + c0);
-            f[4 * h2] = t4.x; f[4 * h2 + 1] = t4.y; f[4 * h2 + 2] = t4.z; f[4 * h2 + 3] = t4.w;
-            fw[4 * h2] = w4.x; fw[4 * h2 + 1] = w4.y; fw[4 * h2 + 2] = w4.z; fw[4 * h2 + 3] = w4.w;
-            fu[4 * h2] = u4.x; fu[4 * h2 + 1] = u4.y; fu[4 * h2 + 2] = u4.z; fu[4 * h2 + 3] = u4.w;
-          }
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int col = hh * 32 + 8 * q4 + e;
-            f[e] = col < r ? f[e] : (col == r ? 1.f : 0.f);
-          }
-          uint4 a, u;
-          a.x = pack_bf16x2(f[0] * fw[0], f[1] * fw[1]);
-          a.y = pack_bf16x2(f[2] * fw[2], f[3] * fw[3]);
-          a.z = pack_bf16x2(f[4] * fw[4], f[5] * fw[5]);
-          a.w = pack_bf16x2(f[6] * fw[6], f[7] * fw[7]);
-          u.x = pack_bf16x2(f[0] * fu[0], f[1] * fu[1]);
-          u.y = pack_bf16x2(f[2] * fu[2], f[3] * fu[3]);
-          u.z = pack_bf16x2(f[4] * fu[4], f[5] * fu[5]);
-          u.w = pack_bf16x2(f[6] * fu[6], f[7] * fu[7]);
-          reinterpret_cast<uint4*>(tw)[q4] = a;
-          reinterpret_cast<uint4*>(tu)[q4] = u;
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 v = *reinterpret_cast<const float4*>(AT + r * AP + 32 * hh + 4 * c4);
+          t[4 * c4] = v.x; t[4 * c4 + 1] = v.y; t[4 * c4 + 2] = v.z; t[4 * c4 + 3] = v.w;
         }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = 32 * hh + e;
+          t[e] = col < r ? t[e] : (col == r ? 1.f : 0.f);
+        }
+        named_bar(1, 128);  // T fully read before the tile overwrites it
+        float tw[32], tu[32];
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 w4 = *reinterpret_cast<const float4*>(vec + VEC_EGPB + 32 * hh + 4 * c4);
+          const float4 u4 = *reinterpret_cast<const float4*>(vec + VEC_BETA + 32 * hh + 4 * c4);
+          tw[4 * c4] = t[4 * c4] * w4.x; tw[4 * c4 + 1] = t[4 * c4 + 1] * w4.y;
+          tw[4 * c4 + 2] = t[4 * c4 + 2] * w4.z; tw[4 * c4 + 3] = t[4 * c4 + 3] * w4.w;
+          tu[4 * c4] = t[4 * c4] * u4.x; tu[4 * c4 + 1] = t[4 * c4 + 1] * u4.y;
+          tu[4 * c4 + 2] = t[4 * c4 + 2] * u4.z; tu[4 * c4 + 3] = t[4 * c4 + 3] * u4.w;
+        }
+        uint8_t* tile_tw = sm + PR_OFF_AT;
+        store_half_bf16(tile_tw, r, hh, tw);
+        store_half_bf16(tile_tw, 64 + r, hh, tw);
+        store_half_bf16(sm + 24576, r, hh, tu);
+        fence_proxy_async();
       }
-      named_bar(1, 128);  // stage, vec and A/T buffer free for the next item
-      if (tid == 0) mbar_arrive(&bars[PB_EMPTY0 + s]);
+      named_bar(1, 128);
+      if (tid == 0) {
+        bulk_store(static_cast<uint8_t*>(p.pm) + tile * WS_P_BYTES, sm + 8192,
+                   TILE_BYTES);
+        bulk_store(static_cast<uint8_t*>(p.tu) + tile * WS_TU_BYTES, sm + 24576,
+                   TILE_BYTES);
+        bulk_commit();
+        // [T_W; T_W] K: both halves of the accumulator hold W
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_bf16(tmem, sdesc(base + PR_OFF_AT + k * 32, 16, 1024),
+                   sdesc(base + k * 2048, 16384, 1024), ID_PREP_W, k > 0);
+        mma_commit(&bars[PB_MMAW]);
+      }
+      ok = mbar_wait(&bars[PB_MMAW], li & 1, abort_flag);
+      if (!bar_and(1, 128, ok)) break;
+      tc_fence_after();
+      {
+        // -W images: warps 0-1 columns 0-63 (lanes 0-63) into K0, warps 2-3
+        // columns 64-127 (lanes 64-127, the copy) into K1; the W product has
+        // completed, so K is no longer read
+        const int r = tid & 63, cb = warp >> 1;
+        uint8_t* wtile = sm + cb * 16384;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float x[32];
+          tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 64 * cb + 32 * hf, x);
+          tmem_ld_wait();
+          store_half_bf16_scaled(wtile, r, hf, x, -1.f);
+        }
+        fence_proxy_async();
+      }
+      tc_fence_before();
+      named_bar(1, 128);  // vec, TMEM and the A/T buffer free again
+      if (tid == 0) {
+        uint8_t* wdst = static_cast<uint8_t*>(p.wneg) + tile * WS_W_BYTES;
+        bulk_store(wdst, sm, TILE_BYTES);
+        bulk_store(wdst + TILE_BYTES, sm + 16384, TILE_BYTES);
+        bulk_commit();
+        bulk_wait_read();  // the stage is free once the copies have read it
+        mbar_arrive(&bars[PB_EMPTY]);
+      }
     }
     if (tid == 0) {
       mma_commit(&bars[PB_DRAIN]);
       wait_ignoring_abort(&bars[PB_DRAIN], 0);
+      bulk_wait_all();
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 4) {
     tc_fence_after();
-    tmem_dealloc(tmem, 64);
+    tmem_dealloc(tmem, PR_TMEM_COLS);
   }
   if (tid == 0 && *abort_flag) record_status(p.status, GDN_ERR_TIMEOUT);
 }
@@ -570,53 +718,52 @@ __global__ void __launch_bounds__(1024)
 }
 
 
+
 // ---------------------------------------------------------------------------
 // chunk_tc_kernel: the serial chain (see the top of this file).
-constexpr int kThreads = 352;
-// Stage: per 64-column block of d_k, three 64-row groups K | Q | -W (K, Q by
-// TMA, -W by the side warps): [K;Q] and [Q;-W] are 128-row K-major tiles and
-// K alone is the N-major operand of the W and Delta products. Then V, a zero
-// block, T_U ([0;T_U] is a 128-row tile), P and T_W (by TMA; [P;T_W] and
-// [T_W;...] are 128-row tiles whose second half only feeds discarded rows).
+constexpr int kThreads = 320;
+constexpr int kChainThreads = 256;
+constexpr int kIssuer = 64;  // chain thread that issues the chain's MMAs
+// Stage: per 64-column block of d_k, three 64-row groups K | Q | -W: [Q;-W]
+// is a 128-row K-major tile and K alone the M-major operand of the Delta
+// product. Then V, a zero block and T_U ([0;T_U] is a 128-row tile), P
+// ([P;...] feeds only discarded rows beyond 64) and the decay vectors.
 constexpr uint32_t ST_K = 0, ST_Q = 8192, ST_W = 16384, ST_CB = 24576;
 constexpr uint32_t ST_V = 49152, ST_Z = 57344, ST_TU = 65536, ST_P = 73728,
-                   ST_TW = 81920;
-constexpr uint32_t STAGE_BYTES = 90112;
-constexpr uint32_t STAGE_TMA_BYTES = 57344;  // K, Q, V, T_W, T_U
+                   ST_CV = 81920;
+constexpr uint32_t STAGE_BYTES = 82944;
+constexpr uint32_t STAGE_TMA_BYTES = 73728 + CV_BYTES;  // K, Q, -W, V, T_U, P, cv
 
 constexpr uint32_t OFF_STAGE = 0;
 constexpr uint32_t OFF_S = 2 * STAGE_BYTES;   // S^T, bf16 (N-major B)
 constexpr uint32_t OFF_U = OFF_S + 16384;     // U, bf16
 constexpr uint32_t OFF_UD = OFF_U + 8192;     // diag(e^{G_L-G}) U, bf16
-constexpr uint32_t OFF_VEC = OFF_UD + 8192;
-constexpr uint32_t OFF_BAR = OFF_VEC + 2 * VEC_FLOATS * 4;
+constexpr uint32_t OFF_O = OFF_UD + 8192;     // output tile on its way out
+constexpr uint32_t OFF_BAR = OFF_O + 8192;
+static_assert(ST_CV + CV_BYTES <= STAGE_BYTES && STAGE_BYTES % 1024 == 0,
+              "stage layout");
 
 enum {
-  B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_MMA0, B_D0FREE, B_WDONE, B_DWFREE,
-  B_SIDE0, B_SIDE1, B_SREADY, B_D1FULL0, B_D1FULL1, B_UDREADY, B_UREADY,
-  B_D2FULL, B_D3FULL0, B_D3FULL1, B_D1FREE0, B_D1FREE1, B_DRAIN_C, B_DRAIN_S,
-  NBARS
+  B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SIDE0, B_SIDE1, B_D1FULL0,
+  B_D1FULL1, B_UREADY, B_D2FULL, B_D3FULL0, B_D3FULL1, B_D1FREE0, B_D1FREE1,
+  B_DRAIN_C, B_DRAIN_S, NBARS
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // TMEM columns (fp32 accumulators, 128 lanes each).
-constexpr uint32_t TM_D0 = 0, TM_DW = 64, TM_D1 = 192, TM_D2 = 320,
-                   TM_D3 = 384;
+constexpr uint32_t TM_D1 = 0, TM_D3 = 128, TM_D2 = 256;  // D1, D3 two buffers
 constexpr uint32_t TMEM_COLS = 512;
 
-constexpr uint32_t ID_KK = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_KMN = idesc_bf16(128, 64, false, true);
-constexpr uint32_t ID_KMN128 = idesc_bf16(128, 128, false, true);
 constexpr uint32_t ID_MNMN = idesc_bf16(128, 64, true, true);
 
 __device__ __forceinline__ uint32_t bar_count(int b) {
   switch (b) {
-    case B_FULL0: case B_FULL1: return 2;
-    case B_SIDE0: case B_SIDE1: case B_SREADY: return 128;
-    case B_D0FREE: case B_DWFREE: case B_UDREADY: case B_UREADY:
-    case B_D1FREE0: case B_D1FREE1: return 64;
+    // the issuer's and the side warp's MMA commits, one arrive per chain warp
+    case B_EMPTY0: case B_EMPTY1: return 2 + kChainThreads / 32;
+    case B_UREADY: case B_D1FREE0: case B_D1FREE1: return kChainThreads / 2;
     default: return 1;
   }
 }
@@ -626,8 +773,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv,
-                    const __grid_constant__ CUtensorMap tmtw,
-                    const __grid_constant__ CUtensorMap tmtu, int nch_dense) {
+                    const __grid_constant__ CUtensorMap tmo, int nch_dense,
+                    int tiles) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -661,10 +808,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (tid < 128) {
+  if (tid < kChainThreads) {
     // zero blocks of both stages; V tiles too for rows of the scaling matrix
     const uint4 z = make_uint4(0, 0, 0, 0);
-    for (int i = tid; i < 1024; i += 128) {
+    for (int i = tid; i < 1024; i += kChainThreads) {
       const uint32_t st = (i >> 9) * STAGE_BYTES;
       *reinterpret_cast<uint4*>(sm + st + ST_Z + (i & 511) * 16) = z;
       if (scale_rows) *reinterpret_cast<uint4*>(sm + st + ST_V + (i & 511) * 16) = z;
@@ -678,8 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmq);
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
-    prefetch_tmap(&tmtw);
-    prefetch_tmap(&tmtu);
+    prefetch_tmap(&tmo);
   }
   fence_proxy_async();
   tc_fence_before();
@@ -690,323 +836,292 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cbase = nloc > 0 ? chunk_base(p, n, nch_dense) + c_begin : 0;
 
   if (warp == 8) {
-    // ================= TMA producer + gate vectors =================
-    int issued = 0;
-    for (int i = 0; i < nloc; ++i) {
-      const int s = i & 1;
-      if (i >= 2 && !mbar_wait(&bars[B_EMPTY0 + s], ((i >> 1) - 1) & 1,
-                               abort_flag))
-        break;
-      const long long t0 = bos + (long long)(c_begin + i) * C;
-      const int len = (int)min((long long)C, eos - t0);
-      uint8_t* st = sm + OFF_STAGE + s * STAGE_BYTES;
-      uint64_t* full = &bars[B_FULL0 + s];
-      if (lane == 0) {
+    // ================= TMA producer =================
+    // K, Q, V by tensor map; -W, P, T_U and the decay vectors are images in
+    // the workspace (plain bulk copies; the tile index is clamped because
+    // those copies have no bounds check and an invalid packing, already
+    // recorded, could otherwise send them past the workspace). Chunk i + 2 is
+    // prefetched into L2 when chunk i is loaded.
+    if (lane == 0) {
+      const uint8_t* wimg = static_cast<const uint8_t*>(p.wneg);
+      const uint8_t* pimg = static_cast<const uint8_t*>(p.pm);
+      const uint8_t* uimg = static_cast<const uint8_t*>(p.tu);
+      auto prefetch = [&](int i) {
+        const int tok = (int)(bos + (long long)(c_begin + i) * C);
+        const size_t tz = (size_t)min((cbase + i) * H + h, tiles - 1);
+        prefetch_l2_3d(&tmk, 0, h, tok);
+        prefetch_l2_3d(&tmk, 64, h, tok);
+        prefetch_l2_3d(&tmq, 0, h, tok);
+        prefetch_l2_3d(&tmq, 64, h, tok);
+        if (!scale_rows) prefetch_l2_3d(&tmv, row0, h, tok);
+        prefetch_l2(wimg + tz * WS_W_BYTES, WS_W_BYTES);
+        prefetch_l2(pimg + tz * WS_P_BYTES, WS_P_BYTES);
+        prefetch_l2(uimg + tz * WS_TU_BYTES, WS_TU_BYTES);
+        prefetch_l2(p.cv + tz * CV_FLOATS, CV_BYTES);
+      };
+      if (nloc > 0) prefetch(0);
+      if (nloc > 1) prefetch(1);
+      int issued = 0;
+      for (int i = 0; i < nloc; ++i) {
+        const int s = i & 1;
+        if (i >= 2 && !mbar_wait(&bars[B_EMPTY0 + s], ((i >> 1) - 1) & 1,
+                                 abort_flag))
+          break;
+        const int tok = (int)(bos + (long long)(c_begin + i) * C);
+        const size_t tz = (size_t)min((cbase + i) * H + h, tiles - 1);
+        uint8_t* st = sm + OFF_STAGE + s * STAGE_BYTES;
+        uint64_t* full = &bars[B_FULL0 + s];
         mbar_arrive_expect_tx(full, STAGE_TMA_BYTES - (scale_rows ? 8192u : 0u));
-        const int tok = (int)t0;
-        const int tz = (cbase + i) * H + h;
-        tma_load_3d(st + ST_K, &tmk, full, 0, h, tok);
-        tma_load_3d(st + ST_K + ST_CB, &tmk, full, 64, h, tok);
         tma_load_3d(st + ST_Q, &tmq, full, 0, h, tok);
         tma_load_3d(st + ST_Q + ST_CB, &tmq, full, 64, h, tok);
+        bulk_load(st + ST_W, wimg + tz * WS_W_BYTES, TILE_BYTES, full);
+        bulk_load(st + ST_W + ST_CB, wimg + tz * WS_W_BYTES + TILE_BYTES,
+                  TILE_BYTES, full);
         if (!scale_rows) tma_load_3d(st + ST_V, &tmv, full, row0, h, tok);
-        tma_load_3d(st + ST_TW, &tmtw, full, 0, 0, tz);
-        tma_load_3d(st + ST_TU, &tmtu, full, 0, 0, tz);
+        bulk_load(st + ST_TU, uimg + tz * WS_TU_BYTES, TILE_BYTES, full);
+        bulk_load(st + ST_CV, p.cv + tz * CV_FLOATS, CV_BYTES, full);
+        tma_load_3d(st + ST_K, &tmk, full, 0, h, tok);
+        tma_load_3d(st + ST_K + ST_CB, &tmk, full, 64, h, tok);
+        bulk_load(st + ST_P, pimg + tz * WS_P_BYTES, TILE_BYTES, full);
+        if (i + 2 < nloc) prefetch(i + 2);
+        issued = i + 1;
       }
-      gate_vectors<VARIANT>(p.g, p.beta, (size_t)t0 * H + h, H, len,
-                            reinterpret_cast<float*>(sm + OFF_VEC) + s * VEC_FLOATS,
-                            lane);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(full);
-      issued = i + 1;
-    }
-    // never leave with a TMA copy still landing in shared memory
-    if (lane == 0)
+      // never leave with a TMA copy still landing in shared memory
       for (int i = max(0, issued - 2); i < issued; ++i)
         wait_ignoring_abort(&bars[B_FULL0 + (i & 1)], (i >> 1) & 1);
-  } else if (warp == 10) {
-    // ================= side MMAs: Q K^T, W, U0 =================
+    }
+  } else if (warp == 9) {
+    // ================= side MMAs: U0 = [0;T_U] V and P U =================
     if (lane == 0 && nloc > 0) {
-      for (int j = 0; j < nloc; ++j) {
+      auto issue_u0 = [&](int j) {
         const int s = j & 1;
-        bool ok = mbar_wait(&bars[B_FULL0 + s], (j >> 1) & 1, abort_flag) &&
-                  (j == 0 || mbar_wait(&bars[B_D0FREE], (j - 1) & 1, abort_flag));
-        if (!ok) break;
+        const bool ok =
+            mbar_wait(&bars[B_FULL0 + s], (j >> 1) & 1, abort_flag) &&
+            (j < 2 || mbar_wait(&bars[B_D1FREE0 + s], ((j >> 1) - 1) & 1,
+                                abort_flag));
+        if (!ok) return false;
         tc_fence_after();
         const uint32_t st = stage(j);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {  // [K;Q] K^T (rows 64-127: Q K^T)
-          const uint64_t a =
-              sdesc(st + ST_K + (k >> 2) * ST_CB + (k & 3) * 32, 16, 1024);
-          mma_bf16(tmem + TM_D0, a, a, ID_KK, k > 0);
-        }
-        mma_commit(&bars[B_MMA0]);
-        ok = (j == 0 || mbar_wait(&bars[B_DWFREE], (j - 1) & 1, abort_flag)) &&
-             (j < 2 || mbar_wait(&bars[B_D1FREE0 + s], ((j >> 1) - 1) & 1,
-                                 abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 4; ++k)  // W = [T_W;.] K (rows 0-63)
-          mma_bf16(tmem + TM_DW, sdesc(st + ST_TW + k * 32, 16, 1024),
-                   sdesc(st + ST_K + k * 2048, ST_CB, 1024), ID_KMN128, k > 0);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)  // U0 = [0;T_U] V starts the accumulator
+        for (int k = 0; k < 4; ++k)
           mma_bf16(tmem + TM_D1 + 64 * s, sdesc(st + ST_Z + k * 32, 16, 1024),
                    sdesc(st + ST_V + k * 2048, 8192, 1024), ID_KMN, k > 0);
-        mma_commit(&bars[B_WDONE]);
-      }
-      mma_commit(&bars[B_DRAIN_S]);
-      wait_ignoring_abort(&bars[B_DRAIN_S], 0);
-    }
-  } else if (warp == 9) {
-    // ================= chain MMAs =================
-    if (lane == 0 && nloc > 0) {
-      for (int i = 0; i < nloc; ++i) {
-        const int b = i & 1;
-        bool ok = mbar_wait(&bars[B_SREADY], i & 1, abort_flag) &&
-                  mbar_wait(&bars[B_SIDE0 + b], (i >> 1) & 1, abort_flag);
-        if (!ok) break;
+        mma_commit(&bars[B_SIDE0 + s]);
+        return true;
+      };
+      bool ok = issue_u0(0);
+      for (int j = 0; ok && j < nloc; ++j) {
+        const int b = j & 1;
+        if (!mbar_wait(&bars[B_UREADY], j & 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t st = stage(i);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)  // += [Q;-W] S^T
-          mma_bf16(tmem + TM_D1 + 64 * b,
-                   sdesc(st + ST_Q + (k >> 2) * ST_CB + (k & 3) * 32, 16, 1024),
-                   sdesc(base + OFF_S + k * 2048, 8192, 1024), ID_KMN, 1);
-        mma_commit(&bars[B_D1FULL0 + b]);
-        ok = mbar_wait(&bars[B_UDREADY], i & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 4; ++k)  // Delta = K^T diag(e^{G_L-G}) U
-          mma_bf16(tmem + TM_D2, sdesc(st + ST_K + k * 2048, ST_CB, 1024),
-                   sdesc(base + OFF_UD + k * 2048, 8192, 1024), ID_MNMN, k > 0);
-        mma_commit(&bars[B_D2FULL]);
-        ok = mbar_wait(&bars[B_UREADY], i & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
+        const uint32_t st = stage(j);
 #pragma unroll
         for (int k = 0; k < 4; ++k)  // P U (rows 0-63)
           mma_bf16(tmem + TM_D3 + 64 * b, sdesc(st + ST_P + k * 32, 16, 1024),
                    sdesc(base + OFF_U + k * 2048, 8192, 1024), ID_KMN, k > 0);
         mma_commit(&bars[B_D3FULL0 + b]);
         mma_commit(&bars[B_EMPTY0 + b]);
+        if (j + 1 < nloc) ok = issue_u0(j + 1);
       }
-      mma_commit(&bars[B_DRAIN_C]);
-      wait_ignoring_abort(&bars[B_DRAIN_C], 0);
-    }
-  } else if (warp < 4) {
-    // ================= side warps: P rows, -W =================
-    for (int j = 0; j < nloc; ++j) {
-      const int s = j & 1;
-      uint8_t* st = sm + OFF_STAGE + s * STAGE_BYTES;
-      const float* vec =
-          reinterpret_cast<const float*>(sm + OFF_VEC) + s * VEC_FLOATS;
-      bool ok;
-      if (warp >= 2) {
-        // row r of P: exp(G_r - G_j) q_r.k_j for j <= r (lanes 64-127 of D0)
-        const int r = tid - 64;
-        ok = mbar_wait(&bars[B_FULL0 + s], (j >> 1) & 1, abort_flag) &&
-             mbar_wait(&bars[B_MMA0], j & 1, abort_flag);
-        ok = bar_and(5, 64, ok);
-        if (ok) {
-          tc_fence_after();
-          float x[64], w[64];
-          tmem_ld64(tmem + TM_D0 + ((uint32_t)(32 * warp) << 16), x);
-          tc_fence_before();
-          mbar_arrive(&bars[B_D0FREE]);
-          const bool safe = vec[VEC_SAFE] != 0.f;
-          load_vec64(vec + (safe ? VEC_IEG : VEC_ALPHA), w);
-          if (safe) {
-            const float er = vec[VEC_EG + r];
-#pragma unroll
-            for (int jj = 0; jj < 64; ++jj) x[jj] = jj <= r ? er * w[jj] * x[jj] : 0.f;
-          } else {
-            float d = 1.f;
-#pragma unroll
-            for (int jj = 63; jj >= 0; --jj) {
-              float pv = 0.f;
-              if (jj <= r) {
-                pv = d * x[jj];
-                d *= w[jj];
-              }
-              x[jj] = pv;
-            }
-          }
-          store_row_bf16(st + ST_P, r, x);
-          fence_proxy_async();
-        }
-      } else {
-        // -W rows after Q: lanes 0-63 of the W accumulator, 128 columns
-        const int r = tid;
-        ok = mbar_wait(&bars[B_WDONE], j & 1, abort_flag);
-        ok = bar_and(6, 64, ok);
-        if (ok) {
-          tc_fence_after();
-          float w0[64], w1[64];
-          tmem_ld64(tmem + TM_DW + ((uint32_t)(32 * warp) << 16), w0);
-          tmem_ld64(tmem + TM_DW + ((uint32_t)(32 * warp) << 16) + 64, w1);
-          tc_fence_before();
-          mbar_arrive(&bars[B_DWFREE]);
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            w0[c] = -w0[c];
-            w1[c] = -w1[c];
-          }
-          store_row_bf16(st + ST_W, r, w0);
-          store_row_bf16(st + ST_W + ST_CB, r, w1);
-          fence_proxy_async();
-        }
-      }
-      mbar_arrive(&bars[B_SIDE0 + s]);
-      if (!bar_and(1, 128, ok)) break;
+      mma_commit(&bars[B_DRAIN_S]);
+      wait_ignoring_abort(&bars[B_DRAIN_S], 0);
     }
   } else {
-    // ================= chain warpgroup =================
-    // warps 4-5: output rows (lanes 0-63), warps 6-7: U rows (lanes 64-127),
-    // all four: state rows (lane = d_k index)
-    const int ct = tid - 128, cw = warp - 4;
-    const uint32_t lanes = (uint32_t)(32 * cw) << 16;
+    // ================= chain warps 0-7 =================
+    // lane quarter qw = warp & 3 (TMEM lanes 32 qw ..), column half hf:
+    // state rows ct = 32 qw + lane (d_k index), columns 32 hf .. 32 hf + 31;
+    // qw >= 2 also U rows ct - 64, qw < 2 output rows ct. Thread kIssuer (a
+    // U-row thread) issues the chain's own MMAs right after the barrier that
+    // completes their operands.
+    const int qw = warp & 3, hf = warp >> 2;
+    const int ct = 32 * qw + lane;
+    const uint32_t lanes = (uint32_t)(32 * qw) << 16;
+    const uint32_t cols = 32 * hf;
+    const bool u_rows = qw >= 2;
+    const bool issuer = tid == kIssuer;
     uint8_t* s_tile = sm + OFF_S;
-    float S[64];
+    float S[32];
     if (scale_rows) {
-      const int a0 = row0 - dv;
+      const int a0 = row0 - dv + 32 * hf;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) S[c] = (ct == a0 + c) ? 1.f : 0.f;
+      for (int c = 0; c < 32; ++c) S[c] = (ct == a0 + c) ? 1.f : 0.f;
     } else if (split_tail) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) S[c] = 0.f;
+      for (int c = 0; c < 32; ++c) S[c] = 0.f;
     } else if (part > 0) {
-      const float* src = p.ws_start + ((nh * p.parts + part) * dv + row0) * DK + ct;
+      const float* src =
+          p.ws_start + ((nh * p.parts + part) * dv + row0 + cols) * DK + ct;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) S[c] = src[(size_t)c * DK];
+      for (int c = 0; c < 32; ++c) S[c] = src[(size_t)c * DK];
     } else if (p.h0) {
-      const float4* src =
-          reinterpret_cast<const float4*>(p.h0 + (nh * DK + ct) * dv + row0);
+      const float4* src = reinterpret_cast<const float4*>(
+          p.h0 + (nh * DK + ct) * dv + row0 + cols);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
+      for (int c = 0; c < 8; ++c) {
         const float4 v4 = src[c];
         S[4 * c] = v4.x; S[4 * c + 1] = v4.y; S[4 * c + 2] = v4.z; S[4 * c + 3] = v4.w;
       }
     } else {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) S[c] = 0.f;
+      for (int c = 0; c < 32; ++c) S[c] = 0.f;
     }
-    store_row_bf16(s_tile, ct, S);
+    store_half_bf16(s_tile, ct, hf, S);
     fence_proxy_async();
-    mbar_arrive(&bars[B_SREADY]);
+    named_bar(2, kChainThreads);
+    // [Q;-W] S^T accumulated onto U0: H = Q S^T (rows 0-63), U (64-127)
+    auto issue_mma1 = [&](int i) {
+      const int b = i & 1;
+      if (!mbar_wait(&bars[B_SIDE0 + b], (i >> 1) & 1, abort_flag)) return false;
+      tc_fence_after();
+      const uint32_t st = stage(i);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        mma_bf16(tmem + TM_D1 + 64 * b,
+                 sdesc(st + ST_Q + (k >> 2) * ST_CB + (k & 3) * 32, 16, 1024),
+                 sdesc(base + OFF_S + k * 2048, 8192, 1024), ID_KMN, 1);
+      mma_commit(&bars[B_D1FULL0 + b]);
+      return true;
+    };
     bool ok = true;
+    if (issuer && nloc > 0) ok = issue_mma1(0);
     for (int i = 0; i < nloc; ++i) {
-      const int b = i & 1, s = i & 1;
+      const int b = i & 1;
       const long long t0 = bos + (long long)(c_begin + i) * C;
       const int len = (int)min((long long)C, eos - t0);
-      // this chunk's scalars, read while its stage is certainly resident
-      ok = ok && mbar_wait(&bars[B_FULL0 + s], (i >> 1) & 1, abort_flag);
-      const float* vec =
-          reinterpret_cast<const float*>(sm + OFF_VEC) + s * VEC_FLOATS;
-      const float gam = vec[VEC_GAMMA];
-      const float rowf = vec[(cw < 2 ? VEC_EG : VEC_DEC) + (ct & 63)];
-      if (cw >= 2) {
+      // this chunk's scalars; the stage is recycled only after every chain
+      // warp has said it is done with them (and the chunk's MMAs completed)
+      ok = ok && mbar_wait(&bars[B_FULL0 + b], (i >> 1) & 1, abort_flag);
+      const float* cv =
+          reinterpret_cast<const float*>(sm + OFF_STAGE + b * STAGE_BYTES + ST_CV);
+      const float gam = cv[CV_GAMMA];
+      const float rowf = cv[(u_rows ? CV_DEC : CV_EG) + (ct & 63)];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_EMPTY0 + b]);
+      if (u_rows) {
         // U = U0 - W S^T (rows 64-127 of the accumulator)
         const int r = ct - 64;
         bool ok1 = ok && mbar_wait(&bars[B_D1FULL0 + b], (i >> 1) & 1, abort_flag);
-        ok1 = bar_and(3, 64, ok1);
+        // the U tile is free once the previous chunk's P U has completed
+        ok1 = ok1 && (i == 0 || mbar_wait(&bars[B_D3FULL0 + (b ^ 1)],
+                                          ((i - 1) >> 1) & 1, abort_flag));
+        ok1 = bar_and(3, kChainThreads / 2, ok1);
         if (ok1) {
           tc_fence_after();
-          float u[64], ud[64];
-          tmem_ld64(tmem + TM_D1 + 64 * b + lanes, u);
+          float u[32], ud[32];
+          tmem_ld32(tmem + TM_D1 + 64 * b + lanes + cols, u);
+          tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 64; ++c) ud[c] = u[c] * rowf;
-          store_row_bf16(sm + OFF_UD, r, ud);
-          fence_proxy_async();
-          mbar_arrive(&bars[B_UDREADY]);
-          store_row_bf16(sm + OFF_U, r, u);
+          for (int c = 0; c < 32; ++c) ud[c] = u[c] * rowf;
+          store_half_bf16(sm + OFF_UD, r, hf, ud);
+          store_half_bf16(sm + OFF_U, r, hf, u);
           fence_proxy_async();
           tc_fence_before();
-          mbar_arrive(&bars[B_UREADY]);
         }
+        ok1 = bar_and(3, kChainThreads / 2, ok1);
+        if (ok1 && issuer) {
+          // Delta = K^T diag(e^{G_L-G}) U
+          tc_fence_after();
+          const uint32_t st = stage(i);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tmem + TM_D2, sdesc(st + ST_K + k * 2048, ST_CB, 1024),
+                     sdesc(base + OFF_UD + k * 2048, 8192, 1024), ID_MNMN, k > 0);
+          mma_commit(&bars[B_D2FULL]);
+          mma_commit(&bars[B_EMPTY0 + b]);
+        }
+        if (ok1) mbar_arrive(&bars[B_UREADY]);
         ok = ok1;
       }
       bool ok3 = ok && mbar_wait(&bars[B_D2FULL], i & 1, abort_flag);
-      if (!bar_and(2, 128, ok3)) {
+      if (!bar_and(2, kChainThreads, ok3)) {
         ok = false;
         break;
       }
       tc_fence_after();
       {
-        float dl[64];
-        tmem_ld64(tmem + TM_D2 + lanes, dl);
+        float dl[32];
+        tmem_ld32(tmem + TM_D2 + lanes + cols, dl);
+        tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 64; ++c) S[c] = fmaf(gam, S[c], dl[c]);
+        for (int c = 0; c < 32; ++c) S[c] = fmaf(gam, S[c], dl[c]);
       }
-      store_row_bf16(s_tile, ct, S);
+      store_half_bf16(s_tile, ct, hf, S);
       fence_proxy_async();
       tc_fence_before();
-      mbar_arrive(&bars[B_SREADY]);
-      if (cw < 2) {
-        // O = e^{G_r} H + P U
+      named_bar(2, kChainThreads);
+      if (issuer && i + 1 < nloc) ok = issue_mma1(i + 1);
+      if (!u_rows) {
+        // O = e^{G_r} H + P U, through a shared-memory tile and a TMA store
+        // for a whole chunk, direct stores for a partial one
         const int r = ct;
         bool ok4 = ok && mbar_wait(&bars[B_D3FULL0 + b], (i >> 1) & 1, abort_flag);
-        ok4 = bar_and(4, 64, ok4);
+        if (tid == 0) bulk_wait_read();  // previous output tile read out
+        ok4 = bar_and(4, kChainThreads / 2, ok4);
         if (ok4) {
           tc_fence_after();
-          const bool store = emit && r < len;
-          uint4* dst = reinterpret_cast<uint4*>(
-              static_cast<__nv_bfloat16*>(p.out) +
-              ((size_t)(t0 + (store ? r : 0)) * H + h) * dv + row0);
+          float o[32], pu[32];
+          tmem_ld32(tmem + TM_D1 + 64 * b + lanes + cols, o);
+          tmem_ld32(tmem + TM_D3 + 64 * b + lanes + cols, pu);
+          tmem_ld_wait();
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float o[32], pu[32];
-            tmem_ld32(tmem + TM_D1 + 64 * b + lanes + 32 * half, o);
-            tmem_ld32(tmem + TM_D3 + 64 * b + lanes + 32 * half, pu);
-            tmem_ld_wait();
-            if (store) {
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                uint4 wq;
-                wq.x = pack_bf16x2(fmaf(rowf, o[8 * c + 0], pu[8 * c + 0]),
-                                   fmaf(rowf, o[8 * c + 1], pu[8 * c + 1]));
-                wq.y = pack_bf16x2(fmaf(rowf, o[8 * c + 2], pu[8 * c + 2]),
-                                   fmaf(rowf, o[8 * c + 3], pu[8 * c + 3]));
-                wq.z = pack_bf16x2(fmaf(rowf, o[8 * c + 4], pu[8 * c + 4]),
-                                   fmaf(rowf, o[8 * c + 5], pu[8 * c + 5]));
-                wq.w = pack_bf16x2(fmaf(rowf, o[8 * c + 6], pu[8 * c + 6]),
-                                   fmaf(rowf, o[8 * c + 7], pu[8 * c + 7]));
-                dst[4 * half + c] = wq;
-              }
-            }
-          }
+          for (int c = 0; c < 32; ++c) o[c] = fmaf(rowf, o[c], pu[c]);
           tc_fence_before();
           mbar_arrive(&bars[B_D1FREE0 + b]);
+          if (emit && len == C) {
+            store_half_bf16(sm + OFF_O, r, hf, o);
+            fence_proxy_async();
+          } else if (emit && r < len) {
+            uint4* dst = reinterpret_cast<uint4*>(
+                static_cast<__nv_bfloat16*>(p.out) +
+                ((size_t)(t0 + r) * H + h) * dv + row0 + cols);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint4 wq;
+              wq.x = pack_bf16x2(o[8 * c + 0], o[8 * c + 1]);
+              wq.y = pack_bf16x2(o[8 * c + 2], o[8 * c + 3]);
+              wq.z = pack_bf16x2(o[8 * c + 4], o[8 * c + 5]);
+              wq.w = pack_bf16x2(o[8 * c + 6], o[8 * c + 7]);
+              dst[c] = wq;
+            }
+          }
+        }
+        if (emit && len == C) {
+          named_bar(4, kChainThreads / 2);
+          if (tid == 0 && ok4) {
+            tma_store_3d(&tmo, sm + OFF_O, row0, h, (int)t0);
+            bulk_commit();
+          }
         }
         ok = ok && ok4;
       }
-      if (!bar_and(2, 128, ok)) {
-        ok = false;
-        break;
-      }
     }
+    ok = bar_and(2, kChainThreads, ok);
+    if (tid == 0) bulk_wait_all();
     if (ok && !*abort_flag) {
       if (p.mode == kModeSplit) {
         if (part == 0) {
           if (p.parts > 1) {
-            float* dst = p.ws_start + ((nh * p.parts + 1) * dv + row0) * DK + ct;
+            float* dst =
+                p.ws_start + ((nh * p.parts + 1) * dv + row0 + cols) * DK + ct;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) dst[(size_t)c * DK] = S[c];
+            for (int c = 0; c < 32; ++c) dst[(size_t)c * DK] = S[c];
           }
         } else {
-          float* dst =
-              p.ws_end + ((nh * p.parts + part) * (dv + DK) + row0) * DK + ct;
+          float* dst = p.ws_end +
+                       ((nh * p.parts + part) * (dv + DK) + row0 + cols) * DK + ct;
 #pragma unroll
-          for (int c = 0; c < 64; ++c) dst[(size_t)c * DK] = S[c];
+          for (int c = 0; c < 32; ++c) dst[(size_t)c * DK] = S[c];
         }
       } else if (p.hT && part == p.parts - 1) {
-        float4* dst = reinterpret_cast<float4*>(p.hT + (nh * DK + ct) * dv + row0);
+        float4* dst = reinterpret_cast<float4*>(p.hT + (nh * DK + ct) * dv + row0 + cols);
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
+        for (int c = 0; c < 8; ++c)
           dst[c] = make_float4(S[4 * c], S[4 * c + 1], S[4 * c + 2], S[4 * c + 3]);
       }
+    }
+    if (issuer) {
+      mma_commit(&bars[B_DRAIN_C]);
+      wait_ignoring_abort(&bars[B_DRAIN_C], 0);
     }
   }
 
@@ -1153,9 +1268,11 @@ int sm_count() {
 
 }  // namespace
 
-bool chunk_tc_supported(int dk, int dv, long long tokens) {
+bool chunk_tc_supported(int dk, int dv, long long tokens, int N, int H) {
+  // chunk-tile indices (chunk * H + head) and token rows stay in int
   return dk == DK && (dv == 64 || dv == 128) && tokens > 0 &&
-         tokens < (1ll << 31) - 64;
+         tokens < (1ll << 31) - 64 &&
+         (tokens / C + N + 1) * (long long)H < (1ll << 31);
 }
 
 int chunk_tc_nch_dense(const ChunkParams& p) { return (p.T + C - 1) / C; }
@@ -1168,7 +1285,7 @@ long long chunk_tc_chunks_bound(const ChunkParams& p) {
 
 size_t chunk_tc_workspace_bytes(const ChunkParams& p) {
   const size_t tiles = (size_t)chunk_tc_chunks_bound(p) * p.H;
-  size_t bytes = 2 * tiles * 64 * 64 * 2;  // T_W and T_U, bf16
+  size_t bytes = tiles * (WS_W_BYTES + WS_P_BYTES + WS_TU_BYTES + CV_BYTES);
   if (p.cu_seqlens) bytes += ((size_t)p.N + 1) * sizeof(int32_t) + 256;
   return bytes;
 }
@@ -1176,14 +1293,18 @@ size_t chunk_tc_workspace_bytes(const ChunkParams& p) {
 void chunk_tc_bind_workspace(ChunkParams& p, void* ws) {
   const size_t tiles = (size_t)chunk_tc_chunks_bound(p) * p.H;
   char* c = static_cast<char*>(ws);
-  p.tw = c;
-  p.tu = c + tiles * 64 * 64 * 2;
-  p.chunk_off = p.cu_seqlens
-                    ? reinterpret_cast<int32_t*>(c + 2 * tiles * 64 * 64 * 2)
-                    : nullptr;
+  p.wneg = c;
+  c += tiles * WS_W_BYTES;
+  p.pm = c;
+  c += tiles * WS_P_BYTES;
+  p.tu = c;
+  c += tiles * WS_TU_BYTES;
+  p.cv = reinterpret_cast<float*>(c);
+  c += tiles * CV_BYTES;
+  p.chunk_off = p.cu_seqlens ? reinterpret_cast<int32_t*>(c) : nullptr;
 }
 
-// Chunk offsets (packed calls) and the UT preparation of every chunk.
+// Chunk offsets (packed calls) and the preparation of every chunk.
 cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
                            int* launches) {
   *launches = 0;
@@ -1194,8 +1315,9 @@ cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
     if (e != cudaSuccess) return e;
     ++*launches;
   }
-  CUtensorMap mk;
-  if (!make_map(&mk, p.k, p.dk, p.H, call_tokens(p), 1, 64))
+  CUtensorMap mk, mq;
+  if (!make_map(&mk, p.k, p.dk, p.H, call_tokens(p), 1, 64) ||
+      !make_map(&mq, p.q, p.dk, p.H, call_tokens(p), 1, 64))
     return cudaErrorInvalidValue;
   const long long bound = chunk_tc_chunks_bound(p);
   const long long items = bound * p.H;
@@ -1205,7 +1327,8 @@ cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
     cudaError_t e = cudaFuncSetAttribute(
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PR_SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kPrepThreads, PR_SMEM_BYTES, stream>>>(p, mk, nchd, (int)bound);
+    kern<<<grid, kPrepThreads, PR_SMEM_BYTES, stream>>>(p, mk, mq, nchd,
+                                                         (int)bound);
     return cudaGetLastError();
   };
   cudaError_t e = p.variant == GDN_GATE_AFTER_PREDICT
@@ -1219,12 +1342,11 @@ cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
 cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream) {
   const long long tokens = call_tokens(p);
   const long long tiles = chunk_tc_chunks_bound(p) * p.H;
-  CUtensorMap mq, mk, mv, mtw, mtu;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map(&mq, p.q, p.dk, p.H, tokens, 1, 64) ||
       !make_map(&mk, p.k, p.dk, p.H, tokens, 1, 64) ||
       !make_map(&mv, p.v, p.dv, p.H, tokens, 1, 64) ||
-      !make_map(&mtw, p.tw, 64, 64, tiles, 64, 1) ||
-      !make_map(&mtu, p.tu, 64, 64, tiles, 64, 1))
+      !make_map(&mo, p.out, p.dv, p.H, tokens, 1, 64))
     return cudaErrorInvalidValue;
   const int nchd = chunk_tc_nch_dense(p);
   auto launch = [&](auto kern) {
@@ -1233,7 +1355,8 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const int rows = p.mode == kModeSplit ? p.dv + DK : p.dv;
     dim3 grid(rows / DVT, p.H, p.N * p.part_count);
-    kern<<<grid, kThreads, SMEM_BYTES, stream>>>(p, mq, mk, mv, mtw, mtu, nchd);
+    kern<<<grid, kThreads, SMEM_BYTES, stream>>>(p, mq, mk, mv, mo, nchd,
+                                                 (int)tiles);
     return cudaGetLastError();
   };
   return p.variant == GDN_GATE_AFTER_PREDICT
@@ -1266,3 +1389,4 @@ extern "C" int gdn_selftest_mma(const void* A, const void* B, float* D, int K,
   if (cudaStreamSynchronize(stream) != cudaSuccess) return GDN_ERR_CUDA;
   return gdn_device_status(stream);
 }
+

@@ -154,7 +154,7 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
   p.status = status;
   const bool bf16 = dtype == GDN_DTYPE_BF16;
   const long long tokens = cu_seqlens ? (long long)T : (long long)B * T;
-  const bool tc_ok = bf16 && chunk_tc_supported(dk, dv, tokens);
+  const bool tc_ok = bf16 && chunk_tc_supported(dk, dv, tokens, B, H);
   if (path == GDN_PATH_TCGEN05 && !tc_ok) return GDN_ERR_UNSUPPORTED;
   const bool use_tc = tc_ok && path != GDN_PATH_SIMT;
   auto launch = [&](const ChunkParams& q) {

@@ -46,10 +46,13 @@ struct ChunkParams {
   float* ws_end;
   float* ws_start;
   int* status;     // device status word (first error wins)
-  // tensor-core path: per-chunk UT factors and (packed calls) chunk offsets
+  // tensor-core path: per-(chunk, head) operands written by the preparation
+  // kernel (index chunk * H + head) and, for packed calls, chunk offsets
   const int32_t* chunk_off;  // [N + 1] first chunk of each sequence
-  void* tw;                  // [chunks, H, 64, 64] bf16, T diag(beta e^{G'})
+  void* wneg;                // [chunks, H, 64, dk] bf16, -W = -T_W K
+  void* pm;                  // [chunks, H, 64, 64] bf16, (Q K^T) (.) D (.) M
   void* tu;                  // [chunks, H, 64, 64] bf16, T diag(beta)
+  float* cv;                 // [chunks, H, 132] fp32, e^G, e^{G_L-G}, gamma
 };
 
 struct DecodeParams {
@@ -71,7 +74,7 @@ cudaError_t launch_sp_chain(const ChunkParams& p, cudaStream_t stream);
 // Tensor-core (tcgen05) path: bf16, dk = 128, dv in {64, 128}. A call takes
 // chunk_tc_workspace_bytes of workspace (bound with chunk_tc_bind_workspace),
 // runs launch_ut_prep once, then launch_chunk_tc for each pass.
-bool chunk_tc_supported(int dk, int dv, long long tokens);
+bool chunk_tc_supported(int dk, int dv, long long tokens, int N, int H);
 size_t chunk_tc_workspace_bytes(const ChunkParams& p);
 void chunk_tc_bind_workspace(ChunkParams& p, void* ws);
 cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
