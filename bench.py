@@ -47,6 +47,18 @@ def chunk_flops(tok_heads, dk, dv, C=64):
     return tok_heads * (2 * C * (3 * dk + 2 * dv) + 6 * dk * dv)
 
 
+# Algorithmic flops of the chunk path split by kernel (per token-head):
+# the preparation forms K K^T, Q K^T and W = T_W K (2 C dk each); the chain
+# forms U0 = T_U V and P U (2 C dv each) and Q S^T, W S^T, K^T U (2 dk dv
+# each). The two add up to chunk_flops.
+def prep_flops(tok_heads, dk, dv, C=64):
+    return tok_heads * 6 * C * dk
+
+
+def chain_flops(tok_heads, dk, dv, C=64):
+    return tok_heads * (4 * C * dv + 6 * dk * dv)
+
+
 def chunk_bytes(tok_heads, dk, dv, n_states, elem=2):
     return tok_heads * (elem * (2 * dk + dv) + elem * dv + 8) + \
         n_states * 4 * dk * dv
@@ -71,11 +83,11 @@ WORKLOADS = {
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and the
 # hash of the kernel source it was taken on; a changed kernel reports null.
 MEASURED_TRAFFIC = {
-    # chunk_tc_kernel, W1, one launch (ncu --set full)
-    "w1:ef603e955bba204e": 101860864 + 12745728,
-    # decode_kernel captured with --sequences 128 (481.3 MB) and scaled x4 to
-    # N=512: its traffic is proportional to the sequences processed
-    "w4:74a5715498108110": 4 * (271674112 + 209667840),
+    # chunk_tc_kernel, W1, one launch (ncu --set full, caches flushed)
+    "w1:63877aff79eb014b": 168908032 + 23252992,
+    # decode_kernel captured with --sequences 128 and scaled x4 to N=512:
+    # its traffic is proportional to the sequences processed
+    "w4:83c7aa23b4500b6b": 4 * (271642880 + 210279936),
 }
 
 
@@ -277,6 +289,19 @@ def run_ours(args, w, device, dist, rank, ws):
     wall = time.perf_counter() - t_wall
     launches = gdn.kernel_counters() - launches0
     clocks = sampler.stop()
+    # Per-kernel durations: a second pass over the same number of steps with
+    # the library's CUDA events around every launch (the events between
+    # kernels cost a few microseconds per step, so the step time above is
+    # taken without them).
+    kstep_n = min(steps, 2000)
+    gdn.gdn_timing_enable(True)
+    for i in range(kstep_n):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    kern = {k: (n * steps / kstep_n, t * steps / kstep_n)
+            for k, (n, t) in gdn.kernel_timings().items()}
+    gdn.gdn_timing_enable(False)
     per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_local = sum(per) / len(per)
     ms = reduce_max(dist, ms_local, device)
@@ -320,33 +345,58 @@ def run_ours(args, w, device, dist, rank, ws):
     hbm_gbs, bf16_tflops, peak_kind = _peaks()
     if w["kind"] == "decode":
         alg_bytes = tok_heads * (8 * dk * dv + 2 * (2 * dk + 2 * dv) + 8)
-        achieved = alg_bytes / (ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1),
+        n_dec, ms_dec = kern.get("decode_kernel", (0, 0.0))
+        dec_ms = ms_dec / n_dec if n_dec else ms
+        achieved = alg_bytes / (dec_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": "decode_kernel",
+                "achieved": round(achieved, 1),
                 "peak": hbm_gbs, "unit": "GB/s",
                 "frac": round(achieved / hbm_gbs, 4),
                 "peak_source": f"{peak_kind} hbm_gbs",
-                "algorithmic_bytes_per_launch": alg_bytes}
+                "algorithmic_bytes_per_launch": alg_bytes,
+                "launches_per_step": n_dec / steps,
+                "ms_per_launch": dec_ms}
         value = units_all / (ms * 1e-3) * (tok_heads / tokens)  # heads/s
         unit = "token-heads/s"
         e2e_val = units_all / (e2e_ms * 1e-3) * (tok_heads / tokens)
     else:
-        flops = chunk_flops(tok_heads, dk, dv)
-        nbytes = chunk_bytes(tok_heads, dk, dv, n_states)
-        achieved = flops / (ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 2),
+        # roofline of the dominant kernel (the chain), from the library's own
+        # CUDA events around each of its launches in the timed region
+        n_chain, ms_chain = kern.get("chunk_tc_kernel", (0, 0.0))
+        chain_step_ms = ms_chain / steps if n_chain else ms
+        flops = chain_flops(tok_heads, dk, dv)
+        achieved = flops / (chain_step_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": "chunk_tc_kernel",
+                "achieved": round(achieved, 2),
                 "peak": bf16_tflops, "unit": "TFLOP/s",
                 "frac": round(achieved / bf16_tflops, 4),
                 "peak_source": f"{peak_kind} bf16_tflops (burst)",
-                "algorithmic_flops_per_launch": flops,
-                "hbm_achieved_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
-                "hbm_frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm_gbs, 4),
-                "algorithmic_bytes_per_launch": nbytes}
+                "algorithmic_flops_per_launch": flops * steps // max(n_chain, 1),
+                "launches_per_step": n_chain / steps,
+                "ms_per_launch": ms_chain / max(n_chain, 1)}
+        n_prep, ms_prep = kern.get("ut_prep_kernel", (0, 0.0))
+        if n_prep:
+            pf = prep_flops(tok_heads, dk, dv)
+            pa = pf / (ms_prep / steps * 1e-3) / 1e12
+            roof["other_kernels"] = {"ut_prep_kernel": {
+                "bound": "tensor", "achieved": round(pa, 2),
+                "frac": round(pa / bf16_tflops, 4), "unit": "TFLOP/s",
+                "algorithmic_flops_per_launch": pf * steps // n_prep,
+                "ms_per_launch": ms_prep / n_prep}}
+        tf = chunk_flops(tok_heads, dk, dv)
+        nbytes = chunk_bytes(tok_heads, dk, dv, n_states)
+        roof["whole_step"] = {
+            "tflops": round(tf / (ms * 1e-3) / 1e12, 2),
+            "frac": round(tf / (ms * 1e-3) / 1e12 / bf16_tflops, 4),
+            "algorithmic_flops": tf, "algorithmic_bytes": nbytes,
+            "hbm_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
         value = units_all / (ms * 1e-3)
         unit = "tokens/s"
         e2e_val = units_all / (e2e_ms * 1e-3)
     key = f"{args.workload}:{_kernel_source_hash(w['kind'])}"
     roof["traffic"] = MEASURED_TRAFFIC.get(key)
-    roof["dominant_kernel_launches_per_step"] = launches / steps
+    roof["kernel_ms_per_step"] = {k: round(v[1] / steps, 5)
+                                  for k, v in kern.items()}
     if w["kind"] == "decode":
         d["state"].copy_(state0)
 
@@ -360,7 +410,10 @@ def run_ours(args, w, device, dist, rank, ws):
                 "g=-softplus(N(0,1)), beta=sigmoid(N(0,1)))",
         "config": {"workload": w["desc"],
                    "l2": "flushed by a 256 MiB memset before every timed step",
-                   "timing": "CUDA events per step on the launching stream"},
+                   "timing": "CUDA events per step on the launching stream; "
+                             "per-kernel durations from the library's events "
+                             "around each launch in a second pass of the same "
+                             "steps"},
         "roofline": roof,
         "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,

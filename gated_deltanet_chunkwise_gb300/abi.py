@@ -25,6 +25,22 @@ GDN_DTYPE_F32 = 1
 GDN_PATH_AUTO = 0
 GDN_PATH_SIMT = 1
 GDN_PATH_TCGEN05 = 2
+# kernel families for per-kernel timing (gdn_kernel_t)
+GDN_KERNEL_CHUNK_PREP = 0
+GDN_KERNEL_CHUNK_CHAIN = 1
+GDN_KERNEL_CHUNK_SIMT = 2
+GDN_KERNEL_SP_CHAIN = 3
+GDN_KERNEL_DECODE = 4
+GDN_KERNEL_CHUNK_OFFSETS = 5
+GDN_KERNEL_COUNT = 6
+KERNEL_NAMES = {
+    GDN_KERNEL_CHUNK_PREP: "ut_prep_kernel",
+    GDN_KERNEL_CHUNK_CHAIN: "chunk_tc_kernel",
+    GDN_KERNEL_CHUNK_SIMT: "chunk_simt_kernel",
+    GDN_KERNEL_SP_CHAIN: "sp_chain_kernel",
+    GDN_KERNEL_DECODE: "decode_kernel",
+    GDN_KERNEL_CHUNK_OFFSETS: "chunk_offsets_kernel",
+}
 
 _lib = None
 
@@ -71,6 +87,11 @@ def library():
     lib.gdn_kernel_launches.restype = ctypes.c_ulonglong
     lib.gdn_selftest_mma.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp]
     lib.gdn_selftest_mma.restype = i
+    lib.gdn_timing_enable.argtypes = [i]
+    lib.gdn_timing_enable.restype = i
+    lib.gdn_timing_read.argtypes = [i, ctypes.POINTER(ctypes.c_ulonglong),
+                                    ctypes.POINTER(ctypes.c_double)]
+    lib.gdn_timing_read.restype = i
     _lib = lib
     return lib
 
@@ -231,3 +252,32 @@ def gdn_selftest_mma(A, B, *, a_mn=False, b_mn=False, b_stacked=False,
 def gdn_device_status(stream=None) -> int:
     """Synchronises ``stream`` and returns/clears the kernels' status word."""
     return int(library().gdn_device_status(_stream(stream)))
+
+
+def gdn_timing_enable(on: bool) -> None:
+    """Per-kernel device timing on/off (resets the accumulated totals)."""
+    rc = library().gdn_timing_enable(1 if on else 0)
+    if rc != GDN_OK:
+        raise GdnError(rc, "gdn_timing_enable")
+
+
+def gdn_timing_read(kernel: int):
+    """(launches, total_ms) of one kernel family since timing was enabled;
+    waits for the recorded events."""
+    n = ctypes.c_ulonglong(0)
+    ms = ctypes.c_double(0.0)
+    rc = library().gdn_timing_read(int(kernel), ctypes.byref(n),
+                                   ctypes.byref(ms))
+    if rc != GDN_OK:
+        raise GdnError(rc, "gdn_timing_read")
+    return int(n.value), float(ms.value)
+
+
+def kernel_timings():
+    """{kernel name: (launches, total_ms)} for every family timed so far."""
+    out = {}
+    for k in range(GDN_KERNEL_COUNT):
+        n, ms = gdn_timing_read(k)
+        if n:
+            out[KERNEL_NAMES[k]] = (n, ms)
+    return out

@@ -296,8 +296,11 @@ cudaError_t launch_typed(const ChunkParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int rows = p.mode == kModeSplit ? p.dv + DK : p.dv;
   dim3 grid(rows / kDVT, p.H, p.N * p.part_count);
+  const int t = timing_start(GDN_KERNEL_CHUNK_SIMT, stream);
   kern<<<grid, kThreads, bytes, stream>>>(p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  timing_stop(t, stream, e);
+  return e;
 }
 
 template <typename InT>
@@ -321,11 +324,14 @@ cudaError_t launch_chunk_simt(const ChunkParams& p, bool bf16,
 cudaError_t launch_sp_chain(const ChunkParams& p, cudaStream_t stream) {
   if (p.parts < 3) return cudaSuccess;
   dim3 grid(p.dv / kDVT, p.H, p.N);
+  const int t = timing_start(GDN_KERNEL_SP_CHAIN, stream);
   if (p.dk == 64)
     sp_chain_kernel<64><<<grid, kThreads, 0, stream>>>(p);
   else
     sp_chain_kernel<128><<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  timing_stop(t, stream, e);
+  return e;
 }
 
 }  // namespace gdn

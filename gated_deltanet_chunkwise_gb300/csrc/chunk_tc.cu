@@ -902,26 +902,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) return false;
         tc_fence_after();
         const uint32_t st = stage(j);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_bf16(tmem + TM_D1 + 64 * s, sdesc(st + ST_Z + k * 32, 16, 1024),
-                   sdesc(st + ST_V + k * 2048, 8192, 1024), ID_KMN, k > 0);
+        mma_bf16_run<4>(tmem + TM_D1 + 64 * s, sdesc(st + ST_Z, 16, 1024), 32,
+                        sdesc(st + ST_V, 8192, 1024), 2048, ID_KMN, false);
         mma_commit(&bars[B_SIDE0 + s]);
         return true;
       };
+      // U0 of chunk j + 1 enters the tensor pipe as soon as chunk j's first
+      // chain product has completed, i.e. while the chain warps form U; P U
+      // of chunk j follows once U is in shared memory.
       bool ok = issue_u0(0);
       for (int j = 0; ok && j < nloc; ++j) {
         const int b = j & 1;
+        if (j + 1 < nloc) {
+          ok = mbar_wait(&bars[B_D1FULL0 + b], (j >> 1) & 1, abort_flag) &&
+               issue_u0(j + 1);
+          if (!ok) break;
+        }
         if (!mbar_wait(&bars[B_UREADY], j & 1, abort_flag)) break;
         tc_fence_after();
         const uint32_t st = stage(j);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)  // P U (rows 0-63)
-          mma_bf16(tmem + TM_D3 + 64 * b, sdesc(st + ST_P + k * 32, 16, 1024),
-                   sdesc(base + OFF_U + k * 2048, 8192, 1024), ID_KMN, k > 0);
+        mma_bf16_run<4>(tmem + TM_D3 + 64 * b, sdesc(st + ST_P, 16, 1024), 32,
+                        sdesc(base + OFF_U, 8192, 1024), 2048, ID_KMN, false);
         mma_commit(&bars[B_D3FULL0 + b]);
         mma_commit(&bars[B_EMPTY0 + b]);
-        if (j + 1 < nloc) ok = issue_u0(j + 1);
       }
       mma_commit(&bars[B_DRAIN_S]);
       wait_ignoring_abort(&bars[B_DRAIN_S], 0);
@@ -974,11 +977,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&bars[B_SIDE0 + b], (i >> 1) & 1, abort_flag)) return false;
       tc_fence_after();
       const uint32_t st = stage(i);
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        mma_bf16(tmem + TM_D1 + 64 * b,
-                 sdesc(st + ST_Q + (k >> 2) * ST_CB + (k & 3) * 32, 16, 1024),
-                 sdesc(base + OFF_S + k * 2048, 8192, 1024), ID_KMN, 1);
+      const uint64_t sb = sdesc(base + OFF_S, 8192, 1024);
+      mma_bf16_run<4>(tmem + TM_D1 + 64 * b, sdesc(st + ST_Q, 16, 1024), 32, sb,
+                      2048, ID_KMN, true);
+      mma_bf16_run<4>(tmem + TM_D1 + 64 * b, sdesc(st + ST_Q + ST_CB, 16, 1024),
+                      32, sb + (8192 >> 4), 2048, ID_KMN, true);
       mma_commit(&bars[B_D1FULL0 + b]);
       return true;
     };
@@ -1022,10 +1025,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Delta = K^T diag(e^{G_L-G}) U
           tc_fence_after();
           const uint32_t st = stage(i);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + TM_D2, sdesc(st + ST_K + k * 2048, ST_CB, 1024),
-                     sdesc(base + OFF_UD + k * 2048, 8192, 1024), ID_MNMN, k > 0);
+          mma_bf16_run<4>(tmem + TM_D2, sdesc(st + ST_K, ST_CB, 1024), 2048,
+                          sdesc(base + OFF_UD, 8192, 1024), 2048, ID_MNMN, false);
           mma_commit(&bars[B_D2FULL]);
           mma_commit(&bars[B_EMPTY0 + b]);
         }
@@ -1309,9 +1310,11 @@ cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
                            int* launches) {
   *launches = 0;
   if (p.cu_seqlens) {
+    const int t = timing_start(GDN_KERNEL_CHUNK_OFFSETS, stream);
     chunk_offsets_kernel<<<1, 1024, 0, stream>>>(
         p.cu_seqlens, p.N, p.T, const_cast<int32_t*>(p.chunk_off), p.status);
     cudaError_t e = cudaGetLastError();
+    timing_stop(t, stream, e);
     if (e != cudaSuccess) return e;
     ++*launches;
   }
@@ -1327,9 +1330,12 @@ cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
     cudaError_t e = cudaFuncSetAttribute(
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PR_SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    const int t = timing_start(GDN_KERNEL_CHUNK_PREP, stream);
     kern<<<grid, kPrepThreads, PR_SMEM_BYTES, stream>>>(p, mk, mq, nchd,
                                                          (int)bound);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    timing_stop(t, stream, e);
+    return e;
   };
   cudaError_t e = p.variant == GDN_GATE_AFTER_PREDICT
                       ? launch(ut_prep_kernel<GDN_GATE_AFTER_PREDICT>)
@@ -1355,9 +1361,12 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const int rows = p.mode == kModeSplit ? p.dv + DK : p.dv;
     dim3 grid(rows / DVT, p.H, p.N * p.part_count);
+    const int t = timing_start(GDN_KERNEL_CHUNK_CHAIN, stream);
     kern<<<grid, kThreads, SMEM_BYTES, stream>>>(p, mq, mk, mv, mo, nchd,
                                                  (int)tiles);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    timing_stop(t, stream, e);
+    return e;
   };
   return p.variant == GDN_GATE_AFTER_PREDICT
              ? launch(chunk_tc_kernel<GDN_GATE_AFTER_PREDICT>)

@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(kThreads)
 template <typename InT, int VARIANT>
 cudaError_t launch_shape(const DecodeParams& p, cudaStream_t stream) {
   const unsigned grid = (unsigned)((size_t)p.N * p.H);
+  const int t = timing_start(GDN_KERNEL_DECODE, stream);
   if (p.dk == 128 && p.dv == 128)
     decode_kernel<InT, 128, 128, VARIANT><<<grid, kThreads, 0, stream>>>(p);
   else if (p.dk == 128 && p.dv == 64)
@@ -124,7 +125,9 @@ cudaError_t launch_shape(const DecodeParams& p, cudaStream_t stream) {
     decode_kernel<InT, 64, 128, VARIANT><<<grid, kThreads, 0, stream>>>(p);
   else
     decode_kernel<InT, 64, 64, VARIANT><<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  timing_stop(t, stream, e);
+  return e;
 }
 
 }  // namespace

@@ -3,6 +3,7 @@
 // negative gdn_status_t and leaves the stream untouched.
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "gdn_internal.cuh"
 
@@ -228,6 +229,71 @@ cudaError_t count_launches(cudaError_t e, int launches) {
   return counted(e, launches);
 }
 
+// ---- per-kernel timing ------------------------------------------------------
+namespace {
+struct TimingRecord {
+  int kernel;
+  int device;
+  cudaEvent_t start, stop;
+  bool closed;
+};
+std::mutex g_timing_mutex;
+bool g_timing_on = false;
+std::vector<TimingRecord> g_timing_pending;
+std::vector<cudaEvent_t> g_event_pool[kMaxDevices];
+unsigned g_timing_generation = 0;  // bumped whenever pending is cleared
+double g_timing_ms[GDN_KERNEL_COUNT];
+unsigned long long g_timing_launches[GDN_KERNEL_COUNT];
+
+// Caller holds g_timing_mutex.
+cudaEvent_t take_event(int dev) {
+  std::vector<cudaEvent_t>& pool = g_event_pool[dev];
+  if (!pool.empty()) {
+    cudaEvent_t e = pool.back();
+    pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+void give_back(const TimingRecord& r) {
+  g_event_pool[r.device].push_back(r.start);
+  g_event_pool[r.device].push_back(r.stop);
+}
+}  // namespace
+
+int timing_start(int kernel, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_timing_mutex);
+  if (!g_timing_on) return -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return -1;
+  TimingRecord r{kernel, dev, take_event(dev), take_event(dev), false};
+  if (!r.start || !r.stop || cudaEventRecord(r.start, stream) != cudaSuccess) {
+    if (r.start) g_event_pool[dev].push_back(r.start);
+    if (r.stop) g_event_pool[dev].push_back(r.stop);
+    return -1;
+  }
+  g_timing_pending.push_back(r);
+  return (int)((g_timing_generation & 0x7f) << 24) |
+         ((int)g_timing_pending.size() - 1);
+}
+
+void timing_stop(int token, cudaStream_t stream, cudaError_t launch_result) {
+  if (token < 0) return;
+  std::lock_guard<std::mutex> lock(g_timing_mutex);
+  const int index = token & 0xffffff;
+  if ((unsigned)(token >> 24) != (g_timing_generation & 0x7f) ||
+      index >= (int)g_timing_pending.size())
+    return;  // discarded meanwhile
+  TimingRecord& r = g_timing_pending[index];
+  if (launch_result == cudaSuccess &&
+      cudaEventRecord(r.stop, stream) == cudaSuccess)
+    r.closed = true;
+}
+
 }  // namespace gdn
 
 extern "C" {
@@ -314,5 +380,49 @@ const char* gdn_status_string(int status) {
 int gdn_version(void) { return 100; }
 
 unsigned long long gdn_kernel_launches(void) { return gdn::g_launches.load(); }
+
+int gdn_timing_enable(int on) {
+  using namespace gdn;
+  std::lock_guard<std::mutex> lock(g_timing_mutex);
+  int rc = GDN_OK;
+  for (const TimingRecord& r : g_timing_pending) {
+    if (r.closed && cudaEventSynchronize(r.stop) != cudaSuccess) rc = GDN_ERR_CUDA;
+    give_back(r);
+  }
+  g_timing_pending.clear();
+  ++g_timing_generation;
+  for (int k = 0; k < GDN_KERNEL_COUNT; ++k) {
+    g_timing_ms[k] = 0.0;
+    g_timing_launches[k] = 0;
+  }
+  g_timing_on = on != 0;
+  return rc;
+}
+
+int gdn_timing_read(int kernel, unsigned long long* launches,
+                    double* total_ms) {
+  using namespace gdn;
+  if (kernel < 0 || kernel >= GDN_KERNEL_COUNT) return GDN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_timing_mutex);
+  int rc = GDN_OK;
+  for (const TimingRecord& r : g_timing_pending) {
+    float ms = 0.f;
+    if (r.closed) {
+      if (cudaEventSynchronize(r.stop) == cudaSuccess &&
+          cudaEventElapsedTime(&ms, r.start, r.stop) == cudaSuccess) {
+        g_timing_ms[r.kernel] += ms;
+        g_timing_launches[r.kernel] += 1;
+      } else {
+        rc = GDN_ERR_CUDA;
+      }
+    }
+    give_back(r);
+  }
+  g_timing_pending.clear();
+  ++g_timing_generation;
+  if (launches) *launches = g_timing_launches[kernel];
+  if (total_ms) *total_ms = g_timing_ms[kernel];
+  return rc;
+}
 
 }  // extern "C"

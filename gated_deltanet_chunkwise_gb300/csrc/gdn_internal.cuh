@@ -91,6 +91,12 @@ int validate_chunk_args(const void* q, const void* k, const void* v,
                         int path, int sp_parts);
 int device_status_ptr(int** out);
 cudaError_t count_launches(cudaError_t e, int launches);
+// Per-kernel timing (gdn_timing_enable): timing_start records the opening
+// event of a launch of `kernel` on `stream` and returns a token (-1 while
+// timing is off); timing_stop records the closing event, or drops the
+// record when the launch itself failed.
+int timing_start(int kernel, cudaStream_t stream);
+void timing_stop(int token, cudaStream_t stream, cudaError_t launch_result);
 
 // Device-side helpers --------------------------------------------------------
 

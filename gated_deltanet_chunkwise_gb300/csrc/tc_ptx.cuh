@@ -213,6 +213,25 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc,
       : "memory");
 }
 
+// NK MMAs over consecutive K steps of one accumulator: the descriptors'
+// start addresses advance by a_step / b_step bytes per step (the address
+// field holds bytes / 16 in its low bits, so the sum stays in that field for
+// shared-memory offsets below 256 KB); only the first step may start fresh.
+template <int NK>
+__device__ __forceinline__ void mma_bf16_run(uint32_t d_tmem, uint64_t a,
+                                             uint32_t a_step, uint64_t b,
+                                             uint32_t b_step, uint32_t idesc,
+                                             bool accumulate) {
+  mma_bf16(d_tmem, a, b, idesc, accumulate ? 1u : 0u);
+#pragma unroll
+  for (int k = 1; k < NK; ++k)
+    asm volatile(
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem),
+        "l"(a + (uint64_t)((k * a_step) >> 4)),
+        "l"(b + (uint64_t)((k * b_step) >> 4)), "r"(idesc)
+        : "memory");
+}
+
 // Arrive on `bar` once every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(

@@ -199,6 +199,35 @@ int gdn_version(void);
  * region. */
 unsigned long long gdn_kernel_launches(void);
 
+/* Kernel families, for per-kernel timing (no paper counterpart: a
+ * measurement aid). */
+typedef enum {
+  GDN_KERNEL_CHUNK_PREP = 0,    /* tensor-core path: state-independent part
+                                   of every (chunk, head) */
+  GDN_KERNEL_CHUNK_CHAIN = 1,   /* tensor-core path: chunk-to-chunk state
+                                   chain and outputs */
+  GDN_KERNEL_CHUNK_SIMT = 2,    /* fp32-arithmetic chunk kernel */
+  GDN_KERNEL_SP_CHAIN = 3,      /* sequence-parallel start-state chain */
+  GDN_KERNEL_DECODE = 4,        /* single-token recurrent step */
+  GDN_KERNEL_CHUNK_OFFSETS = 5, /* chunk offsets of packed sequences */
+  GDN_KERNEL_COUNT = 6
+} gdn_kernel_t;
+
+/* gdn_timing_enable -- per-kernel device timing on (nonzero) or off (0).
+ * While on, every kernel the library enqueues is bracketed by two CUDA
+ * events recorded on its stream (no synchronisation is added). Switching
+ * discards all accumulated and pending timings. Returns GDN_OK or
+ * GDN_ERR_CUDA. Events belong to the device current at launch time. */
+int gdn_timing_enable(int on);
+
+/* gdn_timing_read -- waits for the events recorded so far, folds their
+ * elapsed times into per-kernel totals and writes, for `kernel` (a
+ * gdn_kernel_t), the number of timed launches and their summed device time
+ * in milliseconds since timing was last enabled. Either pointer may be NULL.
+ * Returns GDN_OK, GDN_ERR_INVALID_ARG (unknown kernel) or GDN_ERR_CUDA. */
+int gdn_timing_read(int kernel, unsigned long long* launches,
+                    double* total_ms);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,22 +14,28 @@ import pytest
 
 ROOT = Path(__file__).resolve().parents[1]
 HEADER = ROOT / "include" / "gdn.h"
+HEADERS = sorted((ROOT / "include").glob("*.h"))
 
 OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA = 0, -1, -2, -3, -4
 
 
-def declared_functions():
-    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(gdn_\w+)\s*\(",
-                       text, flags=re.M)
-    return sorted(set(names))
+def declared_functions(headers=None):
+    names = set()
+    for h in headers or HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", h.read_text(), flags=re.S)
+        names.update(re.findall(
+            r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(gdn_\w+)\s*\(",
+            text, flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
-    names = declared_functions()
+    names = declared_functions([HEADER])
     for required in ("gdn_chunk_fwd", "gdn_chunk_fwd_f32", "gdn_chunk_fwd_ex",
-                     "gdn_recurrent_step", "gdn_status_string"):
+                     "gdn_recurrent_step", "gdn_status_string",
+                     "gdn_timing_enable", "gdn_timing_read"):
         assert required in names
+    assert "gdn_selftest_mma" in declared_functions()
 
 
 def test_library_loads_and_exports_every_declared_symbol(lib):
@@ -124,3 +130,19 @@ def test_launch_counter_is_monotone(lib):
     a = lib.kernel_counters()
     chunk(lib.library(), B=0)
     assert lib.kernel_counters() == a
+
+
+def test_timing_switch_and_read_on_host(lib):
+    """Per-kernel timing: switching and reading need no GPU while nothing
+    has been timed; an unknown kernel family is rejected."""
+    so = lib.library()
+    n = ctypes.c_ulonglong(7)
+    ms = ctypes.c_double(7.0)
+    assert so.gdn_timing_enable(1) == OK
+    for k in range(lib.GDN_KERNEL_COUNT):
+        assert so.gdn_timing_read(k, ctypes.byref(n), ctypes.byref(ms)) == OK
+        assert n.value == 0 and ms.value == 0.0
+    assert so.gdn_timing_read(lib.GDN_KERNEL_COUNT, None, None) == INVALID
+    assert so.gdn_timing_read(-1, None, None) == INVALID
+    assert so.gdn_timing_enable(0) == OK
+    assert lib.kernel_timings() == {}

@@ -240,3 +240,20 @@ def test_mixed_gate_strength_across_chunks(lib, cuda_device):
     d["g"][:, 64:128] *= 8.0
     d["g"][:, 192:] *= 5.0
     check(lib, cuda_device, d, "bf16", path=TC)
+
+
+@pytest.mark.gpu
+def test_kernel_timing_counts_the_launches(lib, cuda_device):
+    """Per-kernel timing sees exactly the launches of each path."""
+    d = inputs.chunk_inputs(2, 4, 200, 128, 128, dtype="bf16", seed=5)
+    lib.gdn_timing_enable(True)
+    try:
+        run_gpu(lib, d, cuda_device, "bf16", path=2, sp_parts=1)
+        run_gpu(lib, d, cuda_device, "bf16", path=1, sp_parts=1)
+        t = lib.kernel_timings()
+    finally:
+        lib.gdn_timing_enable(False)
+    assert t["ut_prep_kernel"][0] == 1
+    assert t["chunk_tc_kernel"][0] == 1
+    assert t["chunk_simt_kernel"][0] == 1
+    assert all(ms > 0 for _, ms in t.values())
