@@ -394,6 +394,11 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   const int total_chunks =
       p.chunk_off ? min(p.chunk_off[p.N], total_chunks_bound) : total_chunks_bound;
   const int items = total_chunks * H;
+  // the chain kernel behind this one may be scheduled once every CTA of this
+  // grid has passed here (so all of them hold their SMs already and none can
+  // be starved by it); it takes SMs as they free up and waits for this grid
+  // to complete before touching its output
+  griddep_launch_dependents();
 
   if (tid == 0) {
     mbar_init(&bars[PB_FULL], 1);
@@ -833,6 +838,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   auto stage = [&](int i) { return base + OFF_STAGE + (i & 1) * STAGE_BYTES; };
+  // set-up above overlaps the tail of the preceding kernel; nothing it
+  // writes (workspace, chunk offsets, split states, outputs) is touched
+  // before this point
+  griddep_wait();
   const int cbase = nloc > 0 ? chunk_base(p, n, nch_dense) + c_begin : 0;
 
   if (warp == 8) {
@@ -1362,9 +1371,20 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream) {
     const int rows = p.mode == kModeSplit ? p.dv + DK : p.dv;
     dim3 grid(rows / DVT, p.H, p.N * p.part_count);
     const int t = timing_start(GDN_KERNEL_CHUNK_CHAIN, stream);
-    kern<<<grid, kThreads, SMEM_BYTES, stream>>>(p, mq, mk, mv, mo, nchd,
-                                                 (int)tiles);
-    e = cudaGetLastError();
+    // programmatic stream serialisation: the launch may begin while the
+    // preceding kernel drains; the kernel waits for it in griddep_wait
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p, mq, mk, mv, mo, nchd, (int)tiles);
+    if (e == cudaSuccess) e = cudaGetLastError();
     timing_stop(t, stream, e);
     return e;
   };

@@ -93,6 +93,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// Wait until the grid this one was launched behind (programmatic stream
+// serialisation) has completed and its memory operations are visible; a
+// no-op for an ordinary launch.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allow the grid launched behind this one to be scheduled (its blocks still
+// wait in griddep_wait for this grid's completion).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- proxy fences / named barriers -----------------------------------------
 // Generic-proxy shared-memory writes that the tensor core (async proxy) reads.
 __device__ __forceinline__ void fence_proxy_async() {
