@@ -27,11 +27,12 @@
 // The serial chain per chunk is two MMA round trips and two short register
 // phases; everything else arrives by TMA.
 //
-// Warp roles of chunk_tc_kernel (320 threads): warps 0-7 the chain (state
+// Warp roles of chunk_tc_kernel (352 threads): warps 0-7 the chain (state
 // rows; warps with lane quarter 2-3 also U rows, 0-1 output rows; each warp
-// takes 32 of the 64 columns; one of their threads issues the chain's own
-// MMAs right after the named barrier that completes their operands), 8 TMA
-// producer, 9 the off-chain MMAs (U0, P U). Operand tiles are bf16 with the
+// takes 32 of the 64 columns; one U-row thread issues the Delta product right
+// after the barrier that completes its operand), 8 TMA producer, 9 P U, 10
+// U0 and [Q;-W] S^T (woken when the state is in shared memory). Operand
+// tiles are bf16 with the
 // 128-byte swizzle and arrive in a two-stage ring; whole output tiles leave
 // by TMA store. Every wait is bounded; a CTA that gives up records
 // GDN_ERR_TIMEOUT, drains its MMAs, frees its TMEM and exits.
@@ -726,9 +727,11 @@ __global__ void __launch_bounds__(1024)
 
 // ---------------------------------------------------------------------------
 // chunk_tc_kernel: the serial chain (see the top of this file).
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kChainThreads = 256;
-constexpr int kIssuer = 64;  // chain thread that issues the chain's MMAs
+// The chain thread that issues the Delta product right after the barrier
+// that completes diag(e^{G_L-G}) U (a U-row thread: it waits there anyway).
+constexpr int kIssuerU = 64;
 // Stage: per 64-column block of d_k, three 64-row groups K | Q | -W: [Q;-W]
 // is a 128-row K-major tile and K alone the M-major operand of the Delta
 // product. Then V, a zero block and T_U ([0;T_U] is a 128-row tile), P
@@ -749,9 +752,9 @@ static_assert(ST_CV + CV_BYTES <= STAGE_BYTES && STAGE_BYTES % 1024 == 0,
               "stage layout");
 
 enum {
-  B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SIDE0, B_SIDE1, B_D1FULL0,
-  B_D1FULL1, B_UREADY, B_D2FULL, B_D3FULL0, B_D3FULL1, B_D1FREE0, B_D1FREE1,
-  B_DRAIN_C, B_DRAIN_S, NBARS
+  B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SREADY, B_D1FULL0, B_D1FULL1,
+  B_UREADY, B_D2FULL, B_D3FULL0, B_D3FULL1, B_D3FREE0, B_D3FREE1, B_DRAIN_C,
+  B_DRAIN_S, NBARS
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -766,9 +769,12 @@ constexpr uint32_t ID_MNMN = idesc_bf16(128, 64, true, true);
 
 __device__ __forceinline__ uint32_t bar_count(int b) {
   switch (b) {
-    // the issuer's and the side warp's MMA commits, one arrive per chain warp
+    // the U issuer's and the P U warp's MMA commits (the state issuer's
+    // products have completed before the U issuer's), one per chain warp
     case B_EMPTY0: case B_EMPTY1: return 2 + kChainThreads / 32;
-    case B_UREADY: case B_D1FREE0: case B_D1FREE1: return kChainThreads / 2;
+    case B_SREADY: return kChainThreads;
+    case B_UREADY: case B_D3FREE0: case B_D3FREE1: return kChainThreads / 2;
+    case B_DRAIN_C: return 2;  // the state issuer warp and the U issuer
     default: return 1;
   }
 }
@@ -899,35 +905,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = max(0, issued - 2); i < issued; ++i)
         wait_ignoring_abort(&bars[B_FULL0 + (i & 1)], (i >> 1) & 1);
     }
-  } else if (warp == 9) {
-    // ================= side MMAs: U0 = [0;T_U] V and P U =================
+  } else if (warp == 10) {
+    // ================= U0 and [Q;-W] S^T =================
     if (lane == 0 && nloc > 0) {
+      // All from one thread so that they execute in issue order: U0 =
+      // [0;T_U] V starts a chunk's accumulator, [Q;-W] S^T is added once the
+      // state is in shared memory, and the next chunk's U0 follows right
+      // behind it when its stage has landed (it then runs while U is formed;
+      // otherwise it is issued just before that chunk's [Q;-W] S^T). The accumulator of chunk i + 1 was last read (H and U of chunk
+      // i - 1) before the chain warps signalled the state of chunk i - 1,
+      // which this thread has waited for.
+      int u0_next = 0;  // first chunk whose U0 is not issued yet
       auto issue_u0 = [&](int j) {
         const int s = j & 1;
-        const bool ok =
-            mbar_wait(&bars[B_FULL0 + s], (j >> 1) & 1, abort_flag) &&
-            (j < 2 || mbar_wait(&bars[B_D1FREE0 + s], ((j >> 1) - 1) & 1,
-                                abort_flag));
-        if (!ok) return false;
+        if (!mbar_wait(&bars[B_FULL0 + s], (j >> 1) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t st = stage(j);
         mma_bf16_run<4>(tmem + TM_D1 + 64 * s, sdesc(st + ST_Z, 16, 1024), 32,
                         sdesc(st + ST_V, 8192, 1024), 2048, ID_KMN, false);
-        mma_commit(&bars[B_SIDE0 + s]);
+        u0_next = j + 1;
         return true;
       };
-      // U0 of chunk j + 1 enters the tensor pipe as soon as chunk j's first
-      // chain product has completed, i.e. while the chain warps form U; P U
-      // of chunk j follows once U is in shared memory.
-      bool ok = issue_u0(0);
-      for (int j = 0; ok && j < nloc; ++j) {
+      auto issue_mma1 = [&](int i) {
+        const int b = i & 1;
+        if (u0_next <= i && !issue_u0(i)) return false;
+        tc_fence_after();
+        const uint32_t st = stage(i);
+        const uint64_t sb = sdesc(base + OFF_S, 8192, 1024);
+        mma_bf16_run<4>(tmem + TM_D1 + 64 * b, sdesc(st + ST_Q, 16, 1024), 32, sb,
+                        2048, ID_KMN, true);
+        mma_bf16_run<4>(tmem + TM_D1 + 64 * b, sdesc(st + ST_Q + ST_CB, 16, 1024),
+                        32, sb + (8192 >> 4), 2048, ID_KMN, true);
+        mma_commit(&bars[B_D1FULL0 + b]);
+        const int j = i + 1;
+        if (j < nloc && mbar_test(&bars[B_FULL0 + (j & 1)], (j >> 1) & 1))
+          return issue_u0(j);
+        return true;
+      };
+      bool ok = true;
+      for (int i = 0; ok && i < nloc; ++i) {
+        if (!mbar_wait(&bars[B_SREADY], i & 1, abort_flag)) break;
+        ok = issue_mma1(i);
+      }
+      mma_commit(&bars[B_DRAIN_C]);
+      wait_ignoring_abort(&bars[B_DRAIN_C], 0);
+    }
+  } else if (warp == 9) {
+    // ================= P U, off the chain =================
+    if (lane == 0 && nloc > 0) {
+      for (int j = 0; j < nloc; ++j) {
         const int b = j & 1;
-        if (j + 1 < nloc) {
-          ok = mbar_wait(&bars[B_D1FULL0 + b], (j >> 1) & 1, abort_flag) &&
-               issue_u0(j + 1);
-          if (!ok) break;
-        }
         if (!mbar_wait(&bars[B_UREADY], j & 1, abort_flag)) break;
+        // P U of chunk j - 2 has been read out of this accumulator
+        if (j >= 2 &&
+            !mbar_wait(&bars[B_D3FREE0 + b], ((j >> 1) - 1) & 1, abort_flag))
+          break;
         tc_fence_after();
         const uint32_t st = stage(j);
         mma_bf16_run<4>(tmem + TM_D3 + 64 * b, sdesc(st + ST_P, 16, 1024), 32,
@@ -942,15 +974,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= chain warps 0-7 =================
     // lane quarter qw = warp & 3 (TMEM lanes 32 qw ..), column half hf:
     // state rows ct = 32 qw + lane (d_k index), columns 32 hf .. 32 hf + 31;
-    // qw >= 2 also U rows ct - 64, qw < 2 output rows ct. Thread kIssuer (a
-    // U-row thread) issues the chain's own MMAs right after the barrier that
+    // qw >= 2 also U rows ct - 64, qw < 2 output rows ct. Threads kIssuerS
+    // and kIssuerU issue the chain's own MMAs right after the barrier that
     // completes their operands.
     const int qw = warp & 3, hf = warp >> 2;
     const int ct = 32 * qw + lane;
     const uint32_t lanes = (uint32_t)(32 * qw) << 16;
     const uint32_t cols = 32 * hf;
     const bool u_rows = qw >= 2;
-    const bool issuer = tid == kIssuer;
+    const bool issuer_u = tid == kIssuerU;
     uint8_t* s_tile = sm + OFF_S;
     float S[32];
     if (scale_rows) {
@@ -979,23 +1011,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     store_half_bf16(s_tile, ct, hf, S);
     fence_proxy_async();
-    named_bar(2, kChainThreads);
+    mbar_arrive(&bars[B_SREADY]);
     // [Q;-W] S^T accumulated onto U0: H = Q S^T (rows 0-63), U (64-127)
-    auto issue_mma1 = [&](int i) {
-      const int b = i & 1;
-      if (!mbar_wait(&bars[B_SIDE0 + b], (i >> 1) & 1, abort_flag)) return false;
-      tc_fence_after();
-      const uint32_t st = stage(i);
-      const uint64_t sb = sdesc(base + OFF_S, 8192, 1024);
-      mma_bf16_run<4>(tmem + TM_D1 + 64 * b, sdesc(st + ST_Q, 16, 1024), 32, sb,
-                      2048, ID_KMN, true);
-      mma_bf16_run<4>(tmem + TM_D1 + 64 * b, sdesc(st + ST_Q + ST_CB, 16, 1024),
-                      32, sb + (8192 >> 4), 2048, ID_KMN, true);
-      mma_commit(&bars[B_D1FULL0 + b]);
-      return true;
-    };
     bool ok = true;
-    if (issuer && nloc > 0) ok = issue_mma1(0);
     for (int i = 0; i < nloc; ++i) {
       const int b = i & 1;
       const long long t0 = bos + (long long)(c_begin + i) * C;
@@ -1009,6 +1027,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float rowf = cv[(u_rows ? CV_DEC : CV_EG) + (ct & 63)];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_EMPTY0 + b]);
+      float hq[32];  // H = Q S^T of this chunk (output rows)
+      if (!u_rows) {
+        // read H as soon as it is complete: the accumulator is reused by the
+        // U0 product of the chunk after next, issued after this chunk's state
+        // barrier
+        bool okh = ok && mbar_wait(&bars[B_D1FULL0 + b], (i >> 1) & 1, abort_flag);
+        okh = bar_and(4, kChainThreads / 2, okh);
+        if (okh) {
+          tc_fence_after();
+          tmem_ld32(tmem + TM_D1 + 64 * b + lanes + cols, hq);
+          tmem_ld_wait();
+          tc_fence_before();
+        }
+        ok = okh;
+      }
       if (u_rows) {
         // U = U0 - W S^T (rows 64-127 of the accumulator)
         const int r = ct - 64;
@@ -1017,20 +1050,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok1 = ok1 && (i == 0 || mbar_wait(&bars[B_D3FULL0 + (b ^ 1)],
                                           ((i - 1) >> 1) & 1, abort_flag));
         ok1 = bar_and(3, kChainThreads / 2, ok1);
+        float u[32];
         if (ok1) {
           tc_fence_after();
-          float u[32], ud[32];
+          float ud[32];
           tmem_ld32(tmem + TM_D1 + 64 * b + lanes + cols, u);
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 32; ++c) ud[c] = u[c] * rowf;
           store_half_bf16(sm + OFF_UD, r, hf, ud);
-          store_half_bf16(sm + OFF_U, r, hf, u);
           fence_proxy_async();
-          tc_fence_before();
         }
-        ok1 = bar_and(3, kChainThreads / 2, ok1);
-        if (ok1 && issuer) {
+        ok1 = bar_and(3, kChainThreads / 2, ok1);  // diag(e^{G_L-G}) U complete
+        if (ok1 && issuer_u) {
           // Delta = K^T diag(e^{G_L-G}) U
           tc_fence_after();
           const uint32_t st = stage(i);
@@ -1039,7 +1071,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&bars[B_D2FULL]);
           mma_commit(&bars[B_EMPTY0 + b]);
         }
-        if (ok1) mbar_arrive(&bars[B_UREADY]);
+        if (ok1) {
+          // U itself only feeds P U, off the chain
+          store_half_bf16(sm + OFF_U, r, hf, u);
+          fence_proxy_async();
+          tc_fence_before();
+          mbar_arrive(&bars[B_UREADY]);
+        }
         ok = ok1;
       }
       bool ok3 = ok && mbar_wait(&bars[B_D2FULL], i & 1, abort_flag);
@@ -1058,8 +1096,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       store_half_bf16(s_tile, ct, hf, S);
       fence_proxy_async();
       tc_fence_before();
-      named_bar(2, kChainThreads);
-      if (issuer && i + 1 < nloc) ok = issue_mma1(i + 1);
+      mbar_arrive(&bars[B_SREADY]);
       if (!u_rows) {
         // O = e^{G_r} H + P U, through a shared-memory tile and a TMA store
         // for a whole chunk, direct stores for a partial one
@@ -1069,14 +1106,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok4 = bar_and(4, kChainThreads / 2, ok4);
         if (ok4) {
           tc_fence_after();
-          float o[32], pu[32];
-          tmem_ld32(tmem + TM_D1 + 64 * b + lanes + cols, o);
-          tmem_ld32(tmem + TM_D3 + 64 * b + lanes + cols, pu);
+          float o[32];
+          tmem_ld32(tmem + TM_D3 + 64 * b + lanes + cols, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = fmaf(rowf, o[c], pu[c]);
+          for (int c = 0; c < 32; ++c) o[c] = fmaf(rowf, hq[c], o[c]);
           tc_fence_before();
-          mbar_arrive(&bars[B_D1FREE0 + b]);
+          mbar_arrive(&bars[B_D3FREE0 + b]);
           if (emit && len == C) {
             store_half_bf16(sm + OFF_O, r, hf, o);
             fence_proxy_async();
@@ -1129,7 +1165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst[c] = make_float4(S[4 * c], S[4 * c + 1], S[4 * c + 2], S[4 * c + 3]);
       }
     }
-    if (issuer) {
+    if (issuer_u) {
       mma_commit(&bars[B_DRAIN_C]);
       wait_ignoring_abort(&bars[B_DRAIN_C], 0);
     }
