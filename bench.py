@@ -9,8 +9,10 @@ launches for it). Prints ONE JSON line on rank 0.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload w1|w2|w3|w4]
 
-Timing: inputs resident in HBM, the L2 (129 MB) is flushed by a 256 MiB
-memset before every timed step, each step is bracketed by CUDA events on the
+Timing: inputs resident in HBM, the L2 (129 MB) is flushed before every
+timed step by a 256 MiB memset followed by a read of another 256 MiB buffer
+(so the memset's dirty lines are written back before the step, not during
+it), each step is bracketed by CUDA events on the
 launching stream; ms_per_step is the mean. Under torchrun every rank runs the
 same workload on its own GPU (independent problems, weak scaling, no
 collective on the data path) and the max over ranks is reported.
@@ -234,7 +236,12 @@ def run_ours(args, w, device, dist, rank, ws):
     dk, dv, H = w["dk"], w["dv"], w["H"]
     d = {k: (None if v is None else v.to(device)) for k, v in d_host.items()}
     stream = torch.cuda.current_stream(device)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush_r = torch.zeros(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def l2_flush():
+        flush_w.zero_()  # write a buffer larger than L2
+        flush_r.max()    # then read one: L2 holds clean foreign lines only
 
     if w["kind"] == "decode":
         out = torch.empty_like(d["v"])
@@ -259,13 +266,13 @@ def run_ours(args, w, device, dist, rank, ws):
 
     # warm-up (also sizes the default step count: ~2 s of timed work)
     for _ in range(max(args.warmup, 1)):
-        flush.zero_()
+        l2_flush()
         step()
     torch.cuda.synchronize(device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(3):
-        flush.zero_()
+        l2_flush()
         step()
     e1.record(stream)
     torch.cuda.synchronize(device)
@@ -281,7 +288,7 @@ def run_ours(args, w, device, dist, rank, ws):
     launches0 = gdn.kernel_counters()
     t_wall = time.perf_counter()
     for i in range(steps):
-        flush.zero_()
+        l2_flush()
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -296,7 +303,7 @@ def run_ours(args, w, device, dist, rank, ws):
     kstep_n = min(steps, 2000)
     gdn.gdn_timing_enable(True)
     for i in range(kstep_n):
-        flush.zero_()
+        l2_flush()
         step()
     torch.cuda.synchronize(device)
     kern = {k: (n * steps / kstep_n, t * steps / kstep_n)
@@ -325,7 +332,7 @@ def run_ours(args, w, device, dist, rank, ws):
     es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
     ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
     for i in range(e2e_steps + 2):
-        flush.zero_()
+        l2_flush()
         if i >= 2:
             es[i - 2].record(stream)
         for k_, v_ in pinned.items():
@@ -409,7 +416,9 @@ def run_ours(args, w, device, dist, rank, ws):
         "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), "
                 "g=-softplus(N(0,1)), beta=sigmoid(N(0,1)))",
         "config": {"workload": w["desc"],
-                   "l2": "flushed by a 256 MiB memset before every timed step",
+                   "l2": "flushed before every timed step: 256 MiB memset, then a "
+                         "256 MiB read (write-back of the memset outside the "
+                         "timed events)",
                    "timing": "CUDA events per step on the launching stream; "
                              "per-kernel durations from the library's events "
                              "around each launch in a second pass of the same "

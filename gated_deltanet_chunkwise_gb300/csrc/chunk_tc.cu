@@ -354,19 +354,26 @@ constexpr uint32_t WS_TU_BYTES = TILE_BYTES;
 // ---------------------------------------------------------------------------
 // ut_prep_kernel: the state-independent part of every (chunk, head).
 // 160 threads: warps 0-3 compute, warp 4 loads the K and Q tiles by TMA and
-// writes the gate vectors. One stage; four CTAs per SM hide the latencies.
+// writes the gate vectors. kPrepStages stages, kPrepCtas CTAs per SM.
 constexpr int kPrepThreads = 160;
+constexpr int kPrepStages = 1;
+constexpr int kPrepCtas = 4;
+constexpr int kPrepVecs = kPrepStages + 1;  // gate-vector buffers
 // Stage: K0 | Q0 | K1 | Q1 (8 KB each, 64-column blocks of d_k): [K_c;Q_c]
 // is a 128-row K-major tile and K (two blocks, 16 KB apart) the N-major B
-// operand of W = T_W K. Once a block's last reader is done it holds an output
-// image on its way to the workspace: P in Q0, T_U in Q1, -W in K0 and K1.
+// operand of W = T_W K. Once Q's last reader is done its blocks hold output
+// images on their way to the workspace: P in Q0, T_U in Q1; -W goes out of
+// the solve buffer, so the stage is released right after the W product.
 constexpr uint32_t PR_STAGE = 32768;
 // fp32 A / T (row pitch AP); after T is read out the same bytes hold the
-// 128-row bf16 tile [T_W; T_W].
-constexpr uint32_t PR_OFF_AT = PR_STAGE;
+// 128-row bf16 tile [T_W; T_W], and after the W product the -W images.
+constexpr uint32_t PR_OFF_AT = kPrepStages * PR_STAGE;
 constexpr uint32_t PR_OFF_VEC = PR_OFF_AT + 64 * AP * 4;
-constexpr uint32_t PR_OFF_BAR = PR_OFF_VEC + 2 * VEC_FLOATS * 4;
-enum { PB_FULL, PB_EMPTY, PB_MMA, PB_MMAW, PB_DRAIN, PB_N };
+constexpr uint32_t PR_OFF_BAR = PR_OFF_VEC + kPrepVecs * VEC_FLOATS * 4;
+enum {
+  PB_FULL = 0, PB_EMPTY = PB_FULL + kPrepStages,
+  PB_MMA = PB_EMPTY + kPrepStages, PB_MMAW, PB_DRAIN, PB_N
+};
 constexpr uint32_t PR_OFF_MISC = PR_OFF_BAR + PB_N * 8;
 constexpr uint32_t PR_SMEM_BYTES = PR_OFF_MISC + 16 + 1024;
 constexpr uint32_t PR_TMEM_COLS = 128;
@@ -376,7 +383,7 @@ static_assert(64 * AP * 4 >= 16384, "[T_W; T_W] must fit the solve buffer");
 static_assert(PR_OFF_BAR % 8 == 0, "mbarrier alignment");
 
 template <int VARIANT>
-__global__ void __launch_bounds__(kPrepThreads, 4)
+__global__ void __launch_bounds__(kPrepThreads, kPrepCtas)
     ut_prep_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmq, int nch_dense,
                    int total_chunks_bound) {
@@ -387,7 +394,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PR_OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PR_OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + PR_OFF_MISC + 4);
-  float* vecs = reinterpret_cast<float*>(sm + PR_OFF_VEC);  // two buffers
+  float* vecs = reinterpret_cast<float*>(sm + PR_OFF_VEC);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H;
   // an invalid packing (already recorded as GDN_ERR_INVALID_ARG) can count
@@ -402,8 +409,10 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
   griddep_launch_dependents();
 
   if (tid == 0) {
-    mbar_init(&bars[PB_FULL], 1);
-    mbar_init(&bars[PB_EMPTY], 1);
+    for (int st = 0; st < kPrepStages; ++st) {
+      mbar_init(&bars[PB_FULL + st], 1);
+      mbar_init(&bars[PB_EMPTY + st], 1);
+    }
     mbar_init(&bars[PB_MMA], 1);
     mbar_init(&bars[PB_MMAW], 1);
     mbar_init(&bars[PB_DRAIN], 1);
@@ -425,8 +434,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
 
   if (warp == 4) {
     // ================= TMA producer + gate vectors =================
-    // The gate vectors of item li go to buffer li & 1 (free since item li - 2
-    // finished) before the wait for the stage, so they overlap item li - 1.
+    // The gate vectors of item li go to buffer li % kPrepVecs (its previous
+    // user finished before the stage wait of the previous iteration) ahead of
+    // the wait for the stage, so they overlap the items in flight.
     int li = 0;
     for (int it = blockIdx.x; it < items; it += gridDim.x, ++li) {
       const int c = it / H, h = it - (it / H) * H;
@@ -437,16 +447,21 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       const long long t0 = bos + (long long)lc * C;
       const int len = (int)max(0ll, min((long long)C, eos - t0));
       gate_vectors<VARIANT>(p.g, p.beta, (size_t)t0 * H + h, H, len,
-                            vecs + (li & 1) * VEC_FLOATS,
+                            vecs + (li % kPrepVecs) * VEC_FLOATS,
                             p.cv + (size_t)it * CV_FLOATS, lane);
       __syncwarp();
-      if (li >= 1 && !mbar_wait(&bars[PB_EMPTY], (li - 1) & 1, abort_flag)) break;
+      const int s = li % kPrepStages;
+      if (li >= kPrepStages &&
+          !mbar_wait(&bars[PB_EMPTY + s], (li / kPrepStages - 1) & 1, abort_flag))
+        break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[PB_FULL], PR_STAGE);
-        tma_load_3d(sm, &tmk, &bars[PB_FULL], 0, h, (int)t0);
-        tma_load_3d(sm + 8192, &tmq, &bars[PB_FULL], 0, h, (int)t0);
-        tma_load_3d(sm + 16384, &tmk, &bars[PB_FULL], 64, h, (int)t0);
-        tma_load_3d(sm + 24576, &tmq, &bars[PB_FULL], 64, h, (int)t0);
+        uint64_t* full = &bars[PB_FULL + s];
+        uint8_t* st = sm + s * PR_STAGE;
+        mbar_arrive_expect_tx(full, PR_STAGE);
+        tma_load_3d(st, &tmk, full, 0, h, (int)t0);
+        tma_load_3d(st + 8192, &tmq, full, 0, h, (int)t0);
+        tma_load_3d(st + 16384, &tmk, full, 64, h, (int)t0);
+        tma_load_3d(st + 24576, &tmq, full, 64, h, (int)t0);
         // the CTA's next item into L2 while this one is processed
         const int nx = it + gridDim.x;
         if (nx < items) {
@@ -465,26 +480,33 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       }
     }
     // never leave with a TMA copy still landing in shared memory
-    if (lane == 0 && li > 0) wait_ignoring_abort(&bars[PB_FULL], (li - 1) & 1);
+    if (lane == 0)
+      for (int j = max(0, li - kPrepStages); j < li; ++j)
+        wait_ignoring_abort(&bars[PB_FULL + j % kPrepStages],
+                            (j / kPrepStages) & 1);
   } else {
     // ================= compute warps =================
     float* AT = reinterpret_cast<float*>(sm + PR_OFF_AT);
     int li = 0;
     for (int it = blockIdx.x; it < items; it += gridDim.x, ++li) {
-      bool ok = mbar_wait(&bars[PB_FULL], li & 1, abort_flag);
+      const int s = li % kPrepStages;
+      uint8_t* st = sm + s * PR_STAGE;            // this item's stage
+      const uint32_t stb = base + s * PR_STAGE;   // (shared-window address)
+      bool ok = mbar_wait(&bars[PB_FULL + s], (li / kPrepStages) & 1, abort_flag);
       if (!bar_and(1, 128, ok)) break;
-      const float* vec = vecs + (li & 1) * VEC_FLOATS;
+      const float* vec = vecs + (li % kPrepVecs) * VEC_FLOATS;
       if (tid == 0) {
         // [K;Q] K^T: rows 0-63 K K^T, rows 64-127 Q K^T
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint64_t a = sdesc(base + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+          const uint64_t a = sdesc(stb + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
           mma_bf16(tmem, a, a, ID_PREP, k > 0);
         }
         mma_commit(&bars[PB_MMA]);
       }
       ok = mbar_wait(&bars[PB_MMA], li & 1, abort_flag);
+      if (tid == 0) bulk_wait_read();  // previous -W copy out of the buffer
       if (!bar_and(1, 128, ok)) break;
       tc_fence_after();
       const size_t tile = (size_t)it;  // it = chunk * H + head
@@ -544,7 +566,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
         const bool safe = vec[VEC_SAFE] != 0.f;
         const float er = vec[VEC_EG + r];
         const float* alpha = vec + VEC_ALPHA;
-        uint8_t* ptile = sm + 8192;  // Q0: read by the K K^T MMA only
+        uint8_t* ptile = st + 8192;  // Q0: read by the K K^T MMA only
         float d = 1.f;
 #pragma unroll
         for (int hf = 1; hf >= 0; --hf) {
@@ -613,14 +635,14 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
         uint8_t* tile_tw = sm + PR_OFF_AT;
         store_half_bf16(tile_tw, r, hh, tw);
         store_half_bf16(tile_tw, 64 + r, hh, tw);
-        store_half_bf16(sm + 24576, r, hh, tu);
+        store_half_bf16(st + 24576, r, hh, tu);
         fence_proxy_async();
       }
       named_bar(1, 128);
       if (tid == 0) {
-        bulk_store(static_cast<uint8_t*>(p.pm) + tile * WS_P_BYTES, sm + 8192,
+        bulk_store(static_cast<uint8_t*>(p.pm) + tile * WS_P_BYTES, st + 8192,
                    TILE_BYTES);
-        bulk_store(static_cast<uint8_t*>(p.tu) + tile * WS_TU_BYTES, sm + 24576,
+        bulk_store(static_cast<uint8_t*>(p.tu) + tile * WS_TU_BYTES, st + 24576,
                    TILE_BYTES);
         bulk_commit();
         // [T_W; T_W] K: both halves of the accumulator hold W
@@ -628,18 +650,24 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_bf16(tmem, sdesc(base + PR_OFF_AT + k * 32, 16, 1024),
-                   sdesc(base + k * 2048, 16384, 1024), ID_PREP_W, k > 0);
+                   sdesc(stb + k * 2048, 16384, 1024), ID_PREP_W, k > 0);
         mma_commit(&bars[PB_MMAW]);
       }
       ok = mbar_wait(&bars[PB_MMAW], li & 1, abort_flag);
       if (!bar_and(1, 128, ok)) break;
+      if (tid == 0) {
+        // the W product has read K and the P / T_U copies have read Q: the
+        // stage is free for the next item while -W is read out
+        bulk_wait_read();
+        mbar_arrive(&bars[PB_EMPTY + s]);
+      }
       tc_fence_after();
       {
-        // -W images: warps 0-1 columns 0-63 (lanes 0-63) into K0, warps 2-3
-        // columns 64-127 (lanes 64-127, the copy) into K1; the W product has
-        // completed, so K is no longer read
+        // -W images into the solve buffer, whose [T_W; T_W] tile the W
+        // product has read: warps 0-1 columns 0-63 (lanes 0-63), warps 2-3
+        // columns 64-127 (lanes 64-127, the copy)
         const int r = tid & 63, cb = warp >> 1;
-        uint8_t* wtile = sm + cb * 16384;
+        uint8_t* wtile = sm + PR_OFF_AT + cb * TILE_BYTES;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float x[32];
@@ -650,14 +678,11 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
         fence_proxy_async();
       }
       tc_fence_before();
-      named_bar(1, 128);  // vec, TMEM and the A/T buffer free again
+      named_bar(1, 128);  // vec and TMEM free again; -W complete
       if (tid == 0) {
-        uint8_t* wdst = static_cast<uint8_t*>(p.wneg) + tile * WS_W_BYTES;
-        bulk_store(wdst, sm, TILE_BYTES);
-        bulk_store(wdst + TILE_BYTES, sm + 16384, TILE_BYTES);
+        bulk_store(static_cast<uint8_t*>(p.wneg) + tile * WS_W_BYTES,
+                   sm + PR_OFF_AT, WS_W_BYTES);
         bulk_commit();
-        bulk_wait_read();  // the stage is free once the copies have read it
-        mbar_arrive(&bars[PB_EMPTY]);
       }
     }
     if (tid == 0) {
@@ -740,7 +765,10 @@ constexpr uint32_t ST_K = 0, ST_Q = 8192, ST_W = 16384, ST_CB = 24576;
 constexpr uint32_t ST_V = 49152, ST_Z = 57344, ST_TU = 65536, ST_P = 73728,
                    ST_CV = 81920;
 constexpr uint32_t STAGE_BYTES = 82944;
-constexpr uint32_t STAGE_TMA_BYTES = 73728 + CV_BYTES;  // K, Q, -W, V, T_U, P, cv
+// A stage arrives in two parts: what U0 and the chain warps' scalars need
+// (V, T_U, decay vectors) first, then Q, -W, K and P.
+constexpr uint32_t STAGE_A_BYTES = 16384 + CV_BYTES;  // V, T_U, cv
+constexpr uint32_t STAGE_B_BYTES = 57344;             // Q, -W, K, P
 
 constexpr uint32_t OFF_STAGE = 0;
 constexpr uint32_t OFF_S = 2 * STAGE_BYTES;   // S^T, bf16 (N-major B)
@@ -752,7 +780,8 @@ static_assert(ST_CV + CV_BYTES <= STAGE_BYTES && STAGE_BYTES % 1024 == 0,
               "stage layout");
 
 enum {
-  B_FULL0, B_FULL1, B_EMPTY0, B_EMPTY1, B_SREADY, B_D1FULL0, B_D1FULL1,
+  B_FULLA0, B_FULLA1, B_FULLB0, B_FULLB1, B_EMPTY0, B_EMPTY1, B_SREADY,
+  B_D1FULL0, B_D1FULL1,
   B_UREADY, B_D2FULL, B_D3FULL0, B_D3FULL1, B_D3FREE0, B_D3FREE1, B_DRAIN_C,
   B_DRAIN_S, NBARS
 };
@@ -885,50 +914,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tok = (int)(bos + (long long)(c_begin + i) * C);
         const size_t tz = (size_t)min((cbase + i) * H + h, tiles - 1);
         uint8_t* st = sm + OFF_STAGE + s * STAGE_BYTES;
-        uint64_t* full = &bars[B_FULL0 + s];
-        mbar_arrive_expect_tx(full, STAGE_TMA_BYTES - (scale_rows ? 8192u : 0u));
-        tma_load_3d(st + ST_Q, &tmq, full, 0, h, tok);
-        tma_load_3d(st + ST_Q + ST_CB, &tmq, full, 64, h, tok);
-        bulk_load(st + ST_W, wimg + tz * WS_W_BYTES, TILE_BYTES, full);
+        uint64_t* fa = &bars[B_FULLA0 + s];
+        uint64_t* fb = &bars[B_FULLB0 + s];
+        mbar_arrive_expect_tx(fa, STAGE_A_BYTES - (scale_rows ? 8192u : 0u));
+        if (!scale_rows) tma_load_3d(st + ST_V, &tmv, fa, row0, h, tok);
+        bulk_load(st + ST_TU, uimg + tz * WS_TU_BYTES, TILE_BYTES, fa);
+        bulk_load(st + ST_CV, p.cv + tz * CV_FLOATS, CV_BYTES, fa);
+        mbar_arrive_expect_tx(fb, STAGE_B_BYTES);
+        tma_load_3d(st + ST_Q, &tmq, fb, 0, h, tok);
+        tma_load_3d(st + ST_Q + ST_CB, &tmq, fb, 64, h, tok);
+        bulk_load(st + ST_W, wimg + tz * WS_W_BYTES, TILE_BYTES, fb);
         bulk_load(st + ST_W + ST_CB, wimg + tz * WS_W_BYTES + TILE_BYTES,
-                  TILE_BYTES, full);
-        if (!scale_rows) tma_load_3d(st + ST_V, &tmv, full, row0, h, tok);
-        bulk_load(st + ST_TU, uimg + tz * WS_TU_BYTES, TILE_BYTES, full);
-        bulk_load(st + ST_CV, p.cv + tz * CV_FLOATS, CV_BYTES, full);
-        tma_load_3d(st + ST_K, &tmk, full, 0, h, tok);
-        tma_load_3d(st + ST_K + ST_CB, &tmk, full, 64, h, tok);
-        bulk_load(st + ST_P, pimg + tz * WS_P_BYTES, TILE_BYTES, full);
+                  TILE_BYTES, fb);
+        tma_load_3d(st + ST_K, &tmk, fb, 0, h, tok);
+        tma_load_3d(st + ST_K + ST_CB, &tmk, fb, 64, h, tok);
+        bulk_load(st + ST_P, pimg + tz * WS_P_BYTES, TILE_BYTES, fb);
         if (i + 2 < nloc) prefetch(i + 2);
         issued = i + 1;
       }
       // never leave with a TMA copy still landing in shared memory
-      for (int i = max(0, issued - 2); i < issued; ++i)
-        wait_ignoring_abort(&bars[B_FULL0 + (i & 1)], (i >> 1) & 1);
+      for (int i = max(0, issued - 2); i < issued; ++i) {
+        wait_ignoring_abort(&bars[B_FULLA0 + (i & 1)], (i >> 1) & 1);
+        wait_ignoring_abort(&bars[B_FULLB0 + (i & 1)], (i >> 1) & 1);
+      }
     }
   } else if (warp == 10) {
     // ================= U0 and [Q;-W] S^T =================
     if (lane == 0 && nloc > 0) {
       // All from one thread so that they execute in issue order: U0 =
-      // [0;T_U] V starts a chunk's accumulator, [Q;-W] S^T is added once the
-      // state is in shared memory, and the next chunk's U0 follows right
-      // behind it when its stage has landed (it then runs while U is formed;
-      // otherwise it is issued just before that chunk's [Q;-W] S^T). The accumulator of chunk i + 1 was last read (H and U of chunk
-      // i - 1) before the chain warps signalled the state of chunk i - 1,
-      // which this thread has waited for.
-      int u0_next = 0;  // first chunk whose U0 is not issued yet
+      // [0;T_U] V starts a chunk's accumulator and [Q;-W] S^T is added once
+      // the state is in shared memory. The next chunk's U0 goes in as soon
+      // as this chunk's Delta product has completed, so that it runs while
+      // the chain warps update the state. The accumulator of chunk i + 1 was
+      // last read (H and U of chunk i - 1) before the chain warps signalled
+      // the state of chunk i - 1, which this thread has waited for.
       auto issue_u0 = [&](int j) {
         const int s = j & 1;
-        if (!mbar_wait(&bars[B_FULL0 + s], (j >> 1) & 1, abort_flag)) return false;
+        if (!mbar_wait(&bars[B_FULLA0 + s], (j >> 1) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t st = stage(j);
         mma_bf16_run<4>(tmem + TM_D1 + 64 * s, sdesc(st + ST_Z, 16, 1024), 32,
                         sdesc(st + ST_V, 8192, 1024), 2048, ID_KMN, false);
-        u0_next = j + 1;
         return true;
       };
-      auto issue_mma1 = [&](int i) {
+      bool ok = issue_u0(0);
+      for (int i = 0; ok && i < nloc; ++i) {
         const int b = i & 1;
-        if (u0_next <= i && !issue_u0(i)) return false;
+        if (!mbar_wait(&bars[B_SREADY], i & 1, abort_flag) ||
+            !mbar_wait(&bars[B_FULLB0 + b], (i >> 1) & 1, abort_flag))
+          break;
         tc_fence_after();
         const uint32_t st = stage(i);
         const uint64_t sb = sdesc(base + OFF_S, 8192, 1024);
@@ -937,15 +971,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_bf16_run<4>(tmem + TM_D1 + 64 * b, sdesc(st + ST_Q + ST_CB, 16, 1024),
                         32, sb + (8192 >> 4), 2048, ID_KMN, true);
         mma_commit(&bars[B_D1FULL0 + b]);
-        const int j = i + 1;
-        if (j < nloc && mbar_test(&bars[B_FULL0 + (j & 1)], (j >> 1) & 1))
-          return issue_u0(j);
-        return true;
-      };
-      bool ok = true;
-      for (int i = 0; ok && i < nloc; ++i) {
-        if (!mbar_wait(&bars[B_SREADY], i & 1, abort_flag)) break;
-        ok = issue_mma1(i);
+        if (i + 1 < nloc)
+          ok = mbar_wait(&bars[B_D2FULL], i & 1, abort_flag) && issue_u0(i + 1);
       }
       mma_commit(&bars[B_DRAIN_C]);
       wait_ignoring_abort(&bars[B_DRAIN_C], 0);
@@ -955,7 +982,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && nloc > 0) {
       for (int j = 0; j < nloc; ++j) {
         const int b = j & 1;
-        if (!mbar_wait(&bars[B_UREADY], j & 1, abort_flag)) break;
+        if (!mbar_wait(&bars[B_UREADY], j & 1, abort_flag) ||
+            !mbar_wait(&bars[B_FULLB0 + b], (j >> 1) & 1, abort_flag))
+          break;
         // P U of chunk j - 2 has been read out of this accumulator
         if (j >= 2 &&
             !mbar_wait(&bars[B_D3FREE0 + b], ((j >> 1) - 1) & 1, abort_flag))
@@ -1020,7 +1049,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int len = (int)min((long long)C, eos - t0);
       // this chunk's scalars; the stage is recycled only after every chain
       // warp has said it is done with them (and the chunk's MMAs completed)
-      ok = ok && mbar_wait(&bars[B_FULL0 + b], (i >> 1) & 1, abort_flag);
+      ok = ok && mbar_wait(&bars[B_FULLA0 + b], (i >> 1) & 1, abort_flag);
       const float* cv =
           reinterpret_cast<const float*>(sm + OFF_STAGE + b * STAGE_BYTES + ST_CV);
       const float gam = cv[CV_GAMMA];
@@ -1062,7 +1091,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async();
         }
         ok1 = bar_and(3, kChainThreads / 2, ok1);  // diag(e^{G_L-G}) U complete
-        if (ok1 && issuer_u) {
+        if (ok1 && issuer_u &&
+            mbar_wait(&bars[B_FULLB0 + b], (i >> 1) & 1, abort_flag)) {
           // Delta = K^T diag(e^{G_L-G}) U
           tc_fence_after();
           const uint32_t st = stage(i);
@@ -1369,7 +1399,7 @@ cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
     return cudaErrorInvalidValue;
   const long long bound = chunk_tc_chunks_bound(p);
   const long long items = bound * p.H;
-  const int grid = (int)std::min<long long>(items, 4ll * sm_count());
+  const int grid = (int)std::min<long long>(items, (long long)kPrepCtas * sm_count());
   const int nchd = chunk_tc_nch_dense(p);
   auto launch = [&](auto kern) {
     cudaError_t e = cudaFuncSetAttribute(
