@@ -27,15 +27,16 @@
 // The serial chain per chunk is two MMA round trips and two short register
 // phases; everything else arrives by TMA.
 //
-// Warp roles of chunk_tc_kernel (352 threads): warps 0-7 the chain (state
-// rows; warps with lane quarter 2-3 also U rows, 0-1 output rows; each warp
-// takes 32 of the 64 columns; one U-row thread issues the Delta product right
-// after the barrier that completes its operand), 8 TMA producer, 9 P U, 10
-// U0 and [Q;-W] S^T (woken when the state is in shared memory). Operand
-// tiles are bf16 with the
-// 128-byte swizzle and arrive in a two-stage ring; whole output tiles leave
-// by TMA store. Every wait is bounded; a CTA that gives up records
-// GDN_ERR_TIMEOUT, drains its MMAs, frees its TMEM and exits.
+// Warp roles of chunk_tc_kernel (kChainWarps + 3 warps; with 8 chain warps
+// 352 threads): the chain warps hold the state rows (those with lane quarter
+// 2-3 also U rows, 0-1 output rows; each takes 32 of the 64 columns; one
+// U-row thread issues the Delta product right after the barrier that
+// completes its operand), then the TMA producer, the P U warp and the U0 /
+// [Q;-W] S^T warp (woken when the state is in shared memory). Operand tiles
+// are bf16 with the 128-byte swizzle and arrive in a two-stage ring, each
+// stage in two parts; whole output tiles leave by TMA store. Every wait is
+// bounded; a CTA that gives up records GDN_ERR_TIMEOUT, drains its MMAs,
+// frees its TMEM and exits.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -323,6 +324,22 @@ __device__ __forceinline__ void store_half_bf16(uint8_t* tile, int r, int hf,
     w.z = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]);
     w.w = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
     *reinterpret_cast<uint4*>(tile + sw128(r, 4 * hf + c)) = w;
+  }
+}
+
+// kN fp32 values as bf16 into 16-byte chunks c0 .. c0 + kN / 8 - 1 of row r
+// of a 128-byte-row swizzled tile.
+template <int kN>
+__device__ __forceinline__ void store_cols_bf16(uint8_t* tile, int r, int c0,
+                                                const float (&x)[kN]) {
+#pragma unroll
+  for (int c = 0; c < kN / 8; ++c) {
+    uint4 w;
+    w.x = pack_bf16x2(x[8 * c + 0], x[8 * c + 1]);
+    w.y = pack_bf16x2(x[8 * c + 2], x[8 * c + 3]);
+    w.z = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]);
+    w.w = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
+    *reinterpret_cast<uint4*>(tile + sw128(r, c0 + c)) = w;
   }
 }
 
@@ -752,8 +769,15 @@ __global__ void __launch_bounds__(1024)
 
 // ---------------------------------------------------------------------------
 // chunk_tc_kernel: the serial chain (see the top of this file).
-constexpr int kThreads = 352;
-constexpr int kChainThreads = 256;
+// Chain warps: lane quarter warp & 3, column group warp >> 2 of the CTA's 64
+// state columns (kCW columns each); then the producer, the P U warp and the
+// U0 / [Q;-W] S^T warp.
+constexpr int kChainWarps = 8;
+constexpr int kChainThreads = 32 * kChainWarps;
+constexpr int kCW = 64 / (kChainWarps / 4);
+constexpr int kWarpProducer = kChainWarps, kWarpPU = kChainWarps + 1,
+              kWarpMMA = kChainWarps + 2;
+constexpr int kThreads = 32 * (kChainWarps + 3);
 // The chain thread that issues the Delta product right after the barrier
 // that completes diag(e^{G_L-G}) U (a U-row thread: it waits there anyway).
 constexpr int kIssuerU = 64;
@@ -857,11 +881,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (scale_rows) *reinterpret_cast<uint4*>(sm + st + ST_V + (i & 511) * 16) = z;
     }
   }
-  if (warp == 9) {
+  if (warp == kWarpPU) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == kWarpProducer && lane == 0) {
     prefetch_tmap(&tmq);
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
@@ -879,7 +903,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_wait();
   const int cbase = nloc > 0 ? chunk_base(p, n, nch_dense) + c_begin : 0;
 
-  if (warp == 8) {
+  if (warp == kWarpProducer) {
     // ================= TMA producer =================
     // K, Q, V by tensor map; -W, P, T_U and the decay vectors are images in
     // the workspace (plain bulk copies; the tile index is clamped because
@@ -938,7 +962,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_ignoring_abort(&bars[B_FULLB0 + (i & 1)], (i >> 1) & 1);
       }
     }
-  } else if (warp == 10) {
+  } else if (warp == kWarpMMA) {
     // ================= U0 and [Q;-W] S^T =================
     if (lane == 0 && nloc > 0) {
       // All from one thread so that they execute in issue order: U0 =
@@ -977,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars[B_DRAIN_C]);
       wait_ignoring_abort(&bars[B_DRAIN_C], 0);
     }
-  } else if (warp == 9) {
+  } else if (warp == kWarpPU) {
     // ================= P U, off the chain =================
     if (lane == 0 && nloc > 0) {
       for (int j = 0; j < nloc; ++j) {
@@ -1000,45 +1024,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_ignoring_abort(&bars[B_DRAIN_S], 0);
     }
   } else {
-    // ================= chain warps 0-7 =================
-    // lane quarter qw = warp & 3 (TMEM lanes 32 qw ..), column half hf:
-    // state rows ct = 32 qw + lane (d_k index), columns 32 hf .. 32 hf + 31;
-    // qw >= 2 also U rows ct - 64, qw < 2 output rows ct. Threads kIssuerS
-    // and kIssuerU issue the chain's own MMAs right after the barrier that
-    // completes their operands.
-    const int qw = warp & 3, hf = warp >> 2;
+    // ================= chain warps =================
+    // lane quarter qw = warp & 3 (TMEM lanes 32 qw ..), column group cg:
+    // state rows ct = 32 qw + lane (d_k index), columns cols .. cols + kCW - 1;
+    // qw >= 2 also U rows ct - 64, qw < 2 output rows ct. Thread kIssuerU
+    // issues the Delta product right after the barrier that completes its
+    // operand.
+    const int qw = warp & 3, cg = warp >> 2;
     const int ct = 32 * qw + lane;
     const uint32_t lanes = (uint32_t)(32 * qw) << 16;
-    const uint32_t cols = 32 * hf;
+    const uint32_t cols = kCW * cg;
+    const int chunk0 = cols / 8;  // first 16-byte chunk of the columns
     const bool u_rows = qw >= 2;
     const bool issuer_u = tid == kIssuerU;
     uint8_t* s_tile = sm + OFF_S;
-    float S[32];
+    float S[kCW];
     if (scale_rows) {
-      const int a0 = row0 - dv + 32 * hf;
+      const int a0 = row0 - dv + (int)cols;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) S[c] = (ct == a0 + c) ? 1.f : 0.f;
+      for (int c = 0; c < kCW; ++c) S[c] = (ct == a0 + c) ? 1.f : 0.f;
     } else if (split_tail) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) S[c] = 0.f;
+      for (int c = 0; c < kCW; ++c) S[c] = 0.f;
     } else if (part > 0) {
       const float* src =
           p.ws_start + ((nh * p.parts + part) * dv + row0 + cols) * DK + ct;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) S[c] = src[(size_t)c * DK];
+      for (int c = 0; c < kCW; ++c) S[c] = src[(size_t)c * DK];
     } else if (p.h0) {
       const float4* src = reinterpret_cast<const float4*>(
           p.h0 + (nh * DK + ct) * dv + row0 + cols);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < kCW / 4; ++c) {
         const float4 v4 = src[c];
         S[4 * c] = v4.x; S[4 * c + 1] = v4.y; S[4 * c + 2] = v4.z; S[4 * c + 3] = v4.w;
       }
     } else {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) S[c] = 0.f;
+      for (int c = 0; c < kCW; ++c) S[c] = 0.f;
     }
-    store_half_bf16(s_tile, ct, hf, S);
+    store_cols_bf16<kCW>(s_tile, ct, chunk0, S);
     fence_proxy_async();
     mbar_arrive(&bars[B_SREADY]);
     // [Q;-W] S^T accumulated onto U0: H = Q S^T (rows 0-63), U (64-127)
@@ -1056,7 +1081,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float rowf = cv[(u_rows ? CV_DEC : CV_EG) + (ct & 63)];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_EMPTY0 + b]);
-      float hq[32];  // H = Q S^T of this chunk (output rows)
+      float hq[kCW];  // H = Q S^T of this chunk (output rows)
       if (!u_rows) {
         // read H as soon as it is complete: the accumulator is reused by the
         // U0 product of the chunk after next, issued after this chunk's state
@@ -1065,7 +1090,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         okh = bar_and(4, kChainThreads / 2, okh);
         if (okh) {
           tc_fence_after();
-          tmem_ld32(tmem + TM_D1 + 64 * b + lanes + cols, hq);
+          tmem_ldn<kCW>(tmem + TM_D1 + 64 * b + lanes + cols, hq);
           tmem_ld_wait();
           tc_fence_before();
         }
@@ -1079,15 +1104,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok1 = ok1 && (i == 0 || mbar_wait(&bars[B_D3FULL0 + (b ^ 1)],
                                           ((i - 1) >> 1) & 1, abort_flag));
         ok1 = bar_and(3, kChainThreads / 2, ok1);
-        float u[32];
+        float u[kCW];
         if (ok1) {
           tc_fence_after();
-          float ud[32];
-          tmem_ld32(tmem + TM_D1 + 64 * b + lanes + cols, u);
+          float ud[kCW];
+          tmem_ldn<kCW>(tmem + TM_D1 + 64 * b + lanes + cols, u);
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) ud[c] = u[c] * rowf;
-          store_half_bf16(sm + OFF_UD, r, hf, ud);
+          for (int c = 0; c < kCW; ++c) ud[c] = u[c] * rowf;
+          store_cols_bf16<kCW>(sm + OFF_UD, r, chunk0, ud);
           fence_proxy_async();
         }
         ok1 = bar_and(3, kChainThreads / 2, ok1);  // diag(e^{G_L-G}) U complete
@@ -1103,7 +1128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok1) {
           // U itself only feeds P U, off the chain
-          store_half_bf16(sm + OFF_U, r, hf, u);
+          store_cols_bf16<kCW>(sm + OFF_U, r, chunk0, u);
           fence_proxy_async();
           tc_fence_before();
           mbar_arrive(&bars[B_UREADY]);
@@ -1117,13 +1142,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       {
-        float dl[32];
-        tmem_ld32(tmem + TM_D2 + lanes + cols, dl);
+        float dl[kCW];
+        tmem_ldn<kCW>(tmem + TM_D2 + lanes + cols, dl);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) S[c] = fmaf(gam, S[c], dl[c]);
+        for (int c = 0; c < kCW; ++c) S[c] = fmaf(gam, S[c], dl[c]);
       }
-      store_half_bf16(s_tile, ct, hf, S);
+      store_cols_bf16<kCW>(s_tile, ct, chunk0, S);
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&bars[B_SREADY]);
@@ -1136,22 +1161,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok4 = bar_and(4, kChainThreads / 2, ok4);
         if (ok4) {
           tc_fence_after();
-          float o[32];
-          tmem_ld32(tmem + TM_D3 + 64 * b + lanes + cols, o);
+          float o[kCW];
+          tmem_ldn<kCW>(tmem + TM_D3 + 64 * b + lanes + cols, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = fmaf(rowf, hq[c], o[c]);
+          for (int c = 0; c < kCW; ++c) o[c] = fmaf(rowf, hq[c], o[c]);
           tc_fence_before();
           mbar_arrive(&bars[B_D3FREE0 + b]);
           if (emit && len == C) {
-            store_half_bf16(sm + OFF_O, r, hf, o);
+            store_cols_bf16<kCW>(sm + OFF_O, r, chunk0, o);
             fence_proxy_async();
           } else if (emit && r < len) {
             uint4* dst = reinterpret_cast<uint4*>(
                 static_cast<__nv_bfloat16*>(p.out) +
                 ((size_t)(t0 + r) * H + h) * dv + row0 + cols);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < kCW / 8; ++c) {
               uint4 wq;
               wq.x = pack_bf16x2(o[8 * c + 0], o[8 * c + 1]);
               wq.y = pack_bf16x2(o[8 * c + 2], o[8 * c + 3]);
@@ -1180,18 +1205,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* dst =
                 p.ws_start + ((nh * p.parts + 1) * dv + row0 + cols) * DK + ct;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) dst[(size_t)c * DK] = S[c];
+            for (int c = 0; c < kCW; ++c) dst[(size_t)c * DK] = S[c];
           }
         } else {
           float* dst = p.ws_end +
                        ((nh * p.parts + part) * (dv + DK) + row0 + cols) * DK + ct;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) dst[(size_t)c * DK] = S[c];
+          for (int c = 0; c < kCW; ++c) dst[(size_t)c * DK] = S[c];
         }
       } else if (p.hT && part == p.parts - 1) {
         float4* dst = reinterpret_cast<float4*>(p.hT + (nh * DK + ct) * dv + row0 + cols);
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
+        for (int c = 0; c < kCW / 4; ++c)
           dst[c] = make_float4(S[4 * c], S[4 * c + 1], S[4 * c + 2], S[4 * c + 3]);
       }
     }
@@ -1203,7 +1228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpPU) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }

@@ -14,6 +14,11 @@ Two parts:
   WY/UT chunk form, the sequence-parallel correction, the Householder product
   sum). They exist only to pin ``forward`` from independent directions in the
   CPU tests; the GPU is never compared with them.
+* ``oracle.sublayer`` -- the steps either side of the recurrence in fp64
+  (L2 normalisation of q and k, the sigmoid / softplus gate activations, the
+  RMS normalisation and sigmoid gate of the output) and ``fused_forward``,
+  which wraps ``forward`` with them; pinned in
+  ``tests/test_oracle_sublayer_pins.py``.
 
 Pins (all in ``tests/test_oracle_pins.py``): worked numbers of the illustrated
 DeltaNet page (delta-rule 1.5/2.25/2.625, the 2-D example, prediction/error,
