@@ -76,6 +76,10 @@ WORKLOADS = {
                lengths=(256, 8192),
                desc="gdn_chunk_fwd packed 32 seqs len U{256..8192} H=16 "
                     "dk=dv=128 C=64 bf16, h0~0.1N(0,1), hT returned"),
+    "w1f": dict(kind="fused", B=4, H=16, T=2048, dk=128, dv=128, h0=False,
+                desc="gdn_chunk_fwd_fused B=4 H=16 T=2048 dk=dv=128 C=64 bf16: "
+                     "raw q/k (L2 norm in the kernels), gate and step logits, "
+                     "output RMSNorm (weight [dv]) and sigmoid gate, h0=0"),
     "w4": dict(kind="decode", N=512, H=32, dk=128, dv=128,
                desc="gdn_recurrent_step N=512 H=32 dk=dv=128 bf16 token, "
                     "fp32 state in place"),
@@ -213,6 +217,9 @@ def _make_inputs(w, seed=0):
     if w["kind"] == "decode":
         return inputs.decode_inputs(w["N"], w["H"], w["dk"], w["dv"],
                                     dtype="bf16", seed=seed)
+    if w["kind"] == "fused":
+        return inputs.fused_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
+                                   seed=seed, h0=w["h0"])
     return inputs.chunk_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
                                dtype="bf16", seed=seed, h0=w["h0"],
                                length_range=w.get("lengths"))
@@ -258,6 +265,13 @@ def run_ours(args, w, device, dist, rank, ws):
         want_hT = w["h0"]
 
         def step():
+            if w["kind"] == "fused":
+                gdn.gdn_chunk_fwd_fused(
+                    d["q"], d["k"], d["v"], d["a"], d["b"], d["h0"],
+                    d["cu_seqlens"], norm_weight=d["norm_weight"],
+                    gate=d["gate"], out=out, hT=hT if want_hT else None,
+                    output_final_state=want_hT)
+                return
             gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
                               d["h0"], d["cu_seqlens"], out=out,
                               hT=hT if want_hT else None,
@@ -322,7 +336,7 @@ def run_ours(args, w, device, dist, rank, ws):
               if v is not None)
     d2h = out_host.numel() * out_host.element_size()
     hT_host = None
-    if w["kind"] == "chunk" and w["h0"]:
+    if w["kind"] != "decode" and w["h0"]:
         hT_host = torch.empty(hT.shape, dtype=torch.float32).pin_memory()
         d2h += hT_host.numel() * 4
     if w["kind"] == "decode":
@@ -408,7 +422,7 @@ def run_ours(args, w, device, dist, rank, ws):
         d["state"].copy_(state0)
 
     line = {
-        "metric": METRIC if w["kind"] == "chunk" else
+        "metric": METRIC if w["kind"] != "decode" else
         "GDN decode-step token-heads/s + % of GB300 HBM roofline, 1 GPU",
         "value": value, "unit": unit, "n_gpus": ws, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -448,6 +462,19 @@ def cpu_baseline(w, d_host, budget_s=20.0):
         return {"value": n * w["H"] / dt, "unit": "token-heads/s",
                 "cores": cores, "kind": "oracle",
                 "sample": f"full workload ({n} sequences x {w['H']} heads, one token)",
+                "seconds": round(dt, 3)}
+    if w["kind"] == "fused":
+        from oracle import sublayer
+        t0 = time.perf_counter()
+        sublayer.fused_forward(d_host["q"], d_host["k"], d_host["v"],
+                               d_host["a"], d_host["b"], d_host["h0"],
+                               weight=d_host["norm_weight"],
+                               gate=d_host["gate"])
+        dt = time.perf_counter() - t0
+        tokens = d_host["q"].shape[0] * d_host["q"].shape[1]
+        return {"value": tokens / dt, "unit": "tokens/s", "cores": cores,
+                "kind": "oracle",
+                "sample": f"full workload, oracle with the steps either side",
                 "seconds": round(dt, 3)}
     # dense: whole sequences (all heads); packed: the first sequences
     if d_host["cu_seqlens"] is None:

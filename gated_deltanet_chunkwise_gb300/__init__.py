@@ -11,7 +11,8 @@ from __future__ import annotations
 
 _ABI_NAMES = (
     "gdn_chunk_fwd", "gdn_chunk_fwd_f32", "gdn_chunk_fwd_ex",
-    "gdn_recurrent_step", "gdn_status_string", "GdnError", "library_path",
+    "gdn_recurrent_step", "gdn_chunk_fwd_fused", "gdn_status_string",
+    "GdnError", "library_path",
     "library", "kernel_counters", "gdn_device_status", "gdn_selftest_mma",
     "gdn_timing_enable", "gdn_timing_read", "kernel_timings",
     "GDN_KERNEL_CHUNK_PREP", "GDN_KERNEL_CHUNK_CHAIN", "GDN_KERNEL_CHUNK_SIMT",

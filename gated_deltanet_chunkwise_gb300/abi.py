@@ -87,6 +87,10 @@ def library():
     lib.gdn_kernel_launches.restype = ctypes.c_ulonglong
     lib.gdn_selftest_mma.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp]
     lib.gdn_selftest_mma.restype = i
+    lib.gdn_chunk_fwd_fused.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, ip,
+                                        fp, vp, ctypes.c_float, i, i, i, i,
+                                        i, i, vp]
+    lib.gdn_chunk_fwd_fused.restype = i
     lib.gdn_timing_enable.argtypes = [i]
     lib.gdn_timing_enable.restype = i
     lib.gdn_timing_read.argtypes = [i, ctypes.POINTER(ctypes.c_ulonglong),
@@ -131,6 +135,16 @@ def _need(t, name, dtype, device):
 
 def _chunk_call(fn_name, q, k, v, g, beta, h0, cu_seqlens, out, hT,
                 output_final_state, C, stream, io_dtype, extra=()):
+    fn = getattr(library(), fn_name)
+    if extra:
+        f0 = fn
+        fn = (lambda *a: f0(*a[:-1], *extra, a[-1]))
+    return _chunk_call_fn(fn, fn_name, q, k, v, g, beta, h0, cu_seqlens, out,
+                          hT, output_final_state, C, stream, io_dtype)
+
+
+def _chunk_call_fn(fn, fn_name, q, k, v, g, beta, h0, cu_seqlens, out, hT,
+                   output_final_state, C, stream, io_dtype):
     dev = q.device
     _need(q, "q", io_dtype, None)
     _need(k, "k", io_dtype, dev)
@@ -163,10 +177,9 @@ def _chunk_call(fn_name, q, k, v, g, beta, h0, cu_seqlens, out, hT,
     elif hT is not None:
         _need(hT, "hT", torch.float32, dev)
     with torch.cuda.device(dev):
-        rc = getattr(library(), fn_name)(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
-            _ptr(out), _ptr(hT), _ptr(cu_seqlens), N, H, T, dk, dv, C,
-            *extra, _stream(stream))
+        rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                _ptr(out), _ptr(hT), _ptr(cu_seqlens), N, H, T, dk, dv, C,
+                _stream(stream))
     if rc != GDN_OK:
         raise GdnError(rc, fn_name)
     return out, hT
@@ -199,6 +212,40 @@ def gdn_chunk_fwd_ex(q, k, v, g, beta, h0=None, cu_seqlens=None, *, out=None,
     return _chunk_call("gdn_chunk_fwd_ex", q, k, v, g, beta, h0, cu_seqlens,
                        out, hT, output_final_state, C, stream, q.dtype,
                        extra=(dtype, int(variant), int(path), int(sp_parts)))
+
+
+def gdn_chunk_fwd_fused(q, k, v, a, b, h0=None, cu_seqlens=None, *,
+                        norm_weight=None, gate=None, eps=1e-6, out=None,
+                        hT=None, output_final_state=True, C=64, stream=None):
+    """The forward pass with the steps either side fused: raw q, k (L2-
+    normalised in the kernels), gate logits a (log alpha = -softplus(a)) and
+    step logits b (beta = sigmoid(b)); output RMS-normalised over d_v and
+    scaled by ``norm_weight`` [dv] fp32 when given, then gated by
+    sigmoid(``gate``) (bf16, like v) when given. Returns (out bf16, hT)."""
+    dev = q.device
+    if norm_weight is not None:
+        _need(norm_weight, "norm_weight", torch.float32, dev)
+        if norm_weight.shape != (v.shape[-1],):
+            raise ValueError("norm_weight must be [dv]")
+    if gate is not None:
+        _need(gate, "gate", torch.bfloat16, dev)
+        if gate.shape != v.shape:
+            raise ValueError("gate must have the shape of v")
+    extra_ptrs = (_ptr(norm_weight), _ptr(gate), ctypes.c_float(float(eps)))
+
+    class _Fn:  # argument order of gdn_chunk_fwd_fused
+        def __init__(self, f):
+            self.f = f
+
+        def __call__(self, q_, k_, v_, a_, b_, h0_, out_, hT_, cu_, N, H, T,
+                     dk, dv, C_, stream_):
+            return self.f(q_, k_, v_, a_, b_, h0_, out_, hT_, cu_,
+                          *extra_ptrs, N, H, T, dk, dv, C_, stream_)
+
+    lib = library()
+    return _chunk_call_fn(_Fn(lib.gdn_chunk_fwd_fused), "gdn_chunk_fwd_fused",
+                          q, k, v, a, b, h0, cu_seqlens, out, hT,
+                          output_final_state, C, stream, torch.bfloat16)
 
 
 def gdn_recurrent_step(q, k, v, g, beta, state, *, out=None, stream=None):

@@ -57,10 +57,11 @@ constexpr int AP = 68;  // fp32 row pitch of the solve buffer
 
 // Gate vectors of one chunk (written by one warp): cumulative log gate G,
 // alpha = e^g, e^G, beta e^{G'}, beta, e^{G_L - G}, e^{-G}, gamma = e^{G_L},
-// and whether e^{G_r} e^{-G_j} stays in the normal fp32 range.
+// and whether e^{G_r} e^{-G_j} stays in the normal fp32 range; then the
+// inverse lengths of the chunk's k and q rows (1 when they come normalised).
 constexpr int VEC_G = 0, VEC_ALPHA = 64, VEC_EG = 128, VEC_EGPB = 192,
               VEC_BETA = 256, VEC_DEC = 320, VEC_IEG = 384, VEC_GAMMA = 448,
-              VEC_SAFE = 449, VEC_FLOATS = 452;
+              VEC_SAFE = 449, VEC_SK = 452, VEC_SQ = 516, VEC_FLOATS = 580;
 // The part of them the chain kernel reads, per (chunk, head) in the
 // workspace: e^G, e^{G_L - G}, gamma (padded to a multiple of 16 bytes).
 constexpr int CV_EG = 0, CV_DEC = 64, CV_GAMMA = 128, CV_FLOATS = 132;
@@ -68,22 +69,40 @@ constexpr uint32_t CV_BYTES = CV_FLOATS * 4;
 
 
 
+// log alpha = -softplus(a) and beta = sigmoid(b) from the logits.
+__device__ __forceinline__ float neg_softplus(float a) {
+  return -(fmaxf(a, 0.f) + log1pf(expf(-fabsf(a))));
+}
+__device__ __forceinline__ float sigmoid_f(float b) {
+  return 1.f / (1.f + expf(-b));
+}
+
 // Gate vectors of the chunk whose first token row (token * H + head) is
-// rbase; tokens at or past len get g = 0 and beta = 0. One whole warp; the
-// chain kernel's part also goes to cv (global memory).
+// rbase; tokens at or past len get g = 0 and beta = 0. One whole warp. With
+// `logits` the inputs are a and b of log alpha = -softplus(a), beta =
+// sigmoid(b).
 template <int VARIANT>
 __device__ __forceinline__ void gate_vectors(const float* g, const float* beta,
                                              size_t rbase, int H, int len,
-                                             float* vec, float* cv, int lane) {
+                                             float* vec, bool logits,
+                                             int lane) {
   const unsigned fm = 0xffffffffu;
   float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
   if (lane < len) {
     g0 = g[rbase + (size_t)lane * H];
     b0 = beta[rbase + (size_t)lane * H];
+    if (logits) {
+      g0 = neg_softplus(g0);
+      b0 = sigmoid_f(b0);
+    }
   }
   if (lane + 32 < len) {
     g1 = g[rbase + (size_t)(lane + 32) * H];
     b1 = beta[rbase + (size_t)(lane + 32) * H];
+    if (logits) {
+      g1 = neg_softplus(g1);
+      b1 = sigmoid_f(b1);
+    }
   }
   float s0 = g0, s1 = g1;
 #pragma unroll
@@ -122,11 +141,6 @@ __device__ __forceinline__ void gate_vectors(const float* g, const float* beta,
     vec[VEC_GAMMA] = gam;
     vec[VEC_SAFE] = in_range ? 1.f : 0.f;
   }
-  cv[CV_EG + lane] = e0;
-  cv[CV_EG + 32 + lane] = e1;
-  cv[CV_DEC + lane] = d0;
-  cv[CV_DEC + 32 + lane] = d1;
-  if (lane < 4) cv[CV_GAMMA + lane] = lane == 0 ? gam : 0.f;
 }
 
 // Chunk `c` of the whole call -> (sequence n, chunk index within n).
@@ -465,7 +479,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtas)
       const int len = (int)max(0ll, min((long long)C, eos - t0));
       gate_vectors<VARIANT>(p.g, p.beta, (size_t)t0 * H + h, H, len,
                             vecs + (li % kPrepVecs) * VEC_FLOATS,
-                            p.cv + (size_t)it * CV_FLOATS, lane);
+                            p.prologue != 0, lane);
       __syncwarp();
       const int s = li % kPrepStages;
       if (li >= kPrepStages &&
@@ -511,7 +525,7 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtas)
       const uint32_t stb = base + s * PR_STAGE;   // (shared-window address)
       bool ok = mbar_wait(&bars[PB_FULL + s], (li / kPrepStages) & 1, abort_flag);
       if (!bar_and(1, 128, ok)) break;
-      const float* vec = vecs + (li % kPrepVecs) * VEC_FLOATS;
+      float* vec = vecs + (li % kPrepVecs) * VEC_FLOATS;
       if (tid == 0) {
         // [K;Q] K^T: rows 0-63 K K^T, rows 64-127 Q K^T
         tc_fence_after();
@@ -521,6 +535,51 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtas)
           mma_bf16(tmem, a, a, ID_PREP, k > 0);
         }
         mma_commit(&bars[PB_MMA]);
+      }
+      {
+        // Inverse lengths of the raw k and q rows (when the prologue is on):
+        // thread t < 64 takes row t of K, t >= 64 row t - 64 of Q, both
+        // 64-column blocks of the swizzled tile. They are folded into the
+        // factors the rows and columns are scaled with anyway: 1/|k| into
+        // beta e^{G'} (rows of A, columns of T_W), e^{-G} (columns of A and
+        // P) and e^{G_L - G} (the chain's diag(e^{G_L-G}) U); 1/|q| into e^G
+        // (rows of P and of the chain's output).
+        const int r = tid & 63;
+        float inv = 1.f;
+        if (p.prologue) {
+          const uint8_t* tl = st + (tid < 64 ? 0 : 8192);
+          float ss = 0.f;
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              float f[8];
+              unpack_bf16x8(*reinterpret_cast<const uint4*>(tl + cb * 16384 + sw128(r, c)), f);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+            }
+          }
+          inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+        }
+        vec[(tid < 64 ? VEC_SK : VEC_SQ) + r] = inv;
+        if (p.prologue) {
+          if (tid < 64) {
+            vec[VEC_EGPB + r] *= inv;
+            vec[VEC_IEG + r] *= inv;
+            vec[VEC_DEC + r] *= inv;
+          } else {
+            vec[VEC_EG + r] *= inv;
+          }
+        }
+        named_bar(1, 128);
+        // the chain kernel's decay vectors (after the fold)
+        float* cv = p.cv + (size_t)it * CV_FLOATS;
+        if (tid < 64) {
+          cv[CV_EG + tid] = vec[VEC_EG + tid];
+          cv[CV_DEC + tid] = vec[VEC_DEC + tid];
+        } else if (tid < 68) {
+          cv[CV_GAMMA + tid - 64] = tid == 64 ? vec[VEC_GAMMA] : 0.f;
+        }
       }
       ok = mbar_wait(&bars[PB_MMA], li & 1, abort_flag);
       if (tid == 0) bulk_wait_read();  // previous -W copy out of the buffer
@@ -534,8 +593,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtas)
         const int r = tid;
         const bool safe = vec[VEC_SAFE] != 0.f;
         const float er = vec[VEC_EGPB + r];
-        const float br = vec[VEC_BETA + r];
+        const float br = vec[VEC_BETA + r] * vec[VEC_SK + r];
         const float* alpha = vec + VEC_ALPHA;
+        const float* sk = vec + VEC_SK;
         float d = 1.f;
 #pragma unroll
         for (int hf = 1; hf >= 0; --hf) {
@@ -562,9 +622,9 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtas)
               if (jj < r) {
                 if (VARIANT == GDN_GATE_BEFORE_PREDICT) {
                   d *= alpha[jj + 1];
-                  a = br * d * x[e];
+                  a = br * d * sk[jj] * x[e];
                 } else {
-                  a = br * d * x[e];
+                  a = br * d * sk[jj] * x[e];
                   d *= alpha[jj];
                 }
               }
@@ -604,17 +664,18 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtas)
             store_half_bf16_scaled(ptile, r, hf, x, er);
           } else {
             // D_rj = prod of alpha over (j, r]
+            const float* sk = vec + VEC_SK;
 #pragma unroll
             for (int e = 31; e >= 0; --e) {
               const int jj = 32 * hf + e;
               float pv = 0.f;
               if (jj <= r) {
-                pv = d * x[e];
+                pv = d * sk[jj] * x[e];
                 d *= alpha[jj];
               }
               x[e] = pv;
             }
-            store_half_bf16(ptile, r, hf, x);
+            store_half_bf16_scaled(ptile, r, hf, x, vec[VEC_SQ + r]);
           }
         }
       }
@@ -788,7 +849,8 @@ constexpr int kIssuerU = 64;
 constexpr uint32_t ST_K = 0, ST_Q = 8192, ST_W = 16384, ST_CB = 24576;
 constexpr uint32_t ST_V = 49152, ST_Z = 57344, ST_TU = 65536, ST_P = 73728,
                    ST_CV = 81920;
-constexpr uint32_t STAGE_BYTES = 82944;
+constexpr uint32_t ST_G = 82944;  // output gate tile (fused epilogue only)
+constexpr uint32_t STAGE_BYTES = 91136;
 // A stage arrives in two parts: what U0 and the chain warps' scalars need
 // (V, T_U, decay vectors) first, then Q, -W, K and P.
 constexpr uint32_t STAGE_A_BYTES = 16384 + CV_BYTES;  // V, T_U, cv
@@ -799,7 +861,13 @@ constexpr uint32_t OFF_S = 2 * STAGE_BYTES;   // S^T, bf16 (N-major B)
 constexpr uint32_t OFF_U = OFF_S + 16384;     // U, bf16
 constexpr uint32_t OFF_UD = OFF_U + 8192;     // diag(e^{G_L-G}) U, bf16
 constexpr uint32_t OFF_O = OFF_UD + 8192;     // output tile on its way out
-constexpr uint32_t OFF_BAR = OFF_O + 8192;
+// fused epilogue: norm weights of the CTA's 64 columns, per-row partial sums
+// of squares of the column groups, and the partner CTA's row sums (two
+// chunk-parity slots written by the partner)
+constexpr uint32_t OFF_EPW = OFF_O + 8192;
+constexpr uint32_t OFF_EPRED = OFF_EPW + 64 * 4;
+constexpr uint32_t OFF_EPX = OFF_EPRED + (kChainWarps / 4) * 64 * 4;
+constexpr uint32_t OFF_BAR = OFF_EPX + 2 * 64 * 4;
 static_assert(ST_CV + CV_BYTES <= STAGE_BYTES && STAGE_BYTES % 1024 == 0,
               "stage layout");
 
@@ -807,7 +875,7 @@ enum {
   B_FULLA0, B_FULLA1, B_FULLB0, B_FULLB1, B_EMPTY0, B_EMPTY1, B_SREADY,
   B_D1FULL0, B_D1FULL1,
   B_UREADY, B_D2FULL, B_D3FULL0, B_D3FULL1, B_D3FREE0, B_D3FREE1, B_DRAIN_C,
-  B_DRAIN_S, NBARS
+  B_DRAIN_S, B_XS0, B_XS1, NBARS
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -828,6 +896,7 @@ __device__ __forceinline__ uint32_t bar_count(int b) {
     case B_SREADY: return kChainThreads;
     case B_UREADY: case B_D3FREE0: case B_D3FREE1: return kChainThreads / 2;
     case B_DRAIN_C: return 2;  // the state issuer warp and the U issuer
+    // the partner's 64 row sums, counted in bytes (armed once per use)
     default: return 1;
   }
 }
@@ -837,7 +906,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv,
-                    const __grid_constant__ CUtensorMap tmo, int nch_dense,
+                    const __grid_constant__ CUtensorMap tmo,
+                    const __grid_constant__ CUtensorMap tmg, int nch_dense,
                     int tiles) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -858,6 +928,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!value_rows && !(split_tail && row0 < dv + DK)) return;
   const bool scale_rows = !value_rows;
   const bool emit = (p.mode == kModeOutput) || part == 0;
+  // fused epilogue on this CTA's outputs; with d_v = 128 the two CTAs of a
+  // (sequence, head, part) form a cluster and exchange the per-row sums of
+  // squares of their halves of each output row
+  const bool epi = p.epilogue && emit;
+  const bool clustered = p.epilogue && dv == 128;
+  const bool has_gate = epi && p.gate_z != nullptr;
   long long bos, eos;
   if (!sequence_range(p, n, bos, eos)) return;
   const int nch = (int)((eos - bos + C - 1) / C);
@@ -890,6 +966,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
     prefetch_tmap(&tmo);
+    if (has_gate) prefetch_tmap(&tmg);
   }
   fence_proxy_async();
   tc_fence_before();
@@ -902,6 +979,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // before this point
   griddep_wait();
   const int cbase = nloc > 0 ? chunk_base(p, n, nch_dense) + c_begin : 0;
+  if (epi && tid < 64) {
+    reinterpret_cast<float*>(sm + OFF_EPW)[tid] =
+        p.norm_w ? p.norm_w[row0 + tid] : 1.f;
+  }
+  // slots of the first two chunks armed for the partner's 64 row sums, and
+  // the partner's barriers initialised, before anything is sent
+  if (clustered && tid == 0) {
+    mbar_arrive_expect_tx(&bars[B_XS0], 64 * 4);
+    mbar_arrive_expect_tx(&bars[B_XS1], 64 * 4);
+  }
+  if (clustered) cluster_sync();
 
   if (warp == kWarpProducer) {
     // ================= TMA producer =================
@@ -944,7 +1032,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!scale_rows) tma_load_3d(st + ST_V, &tmv, fa, row0, h, tok);
         bulk_load(st + ST_TU, uimg + tz * WS_TU_BYTES, TILE_BYTES, fa);
         bulk_load(st + ST_CV, p.cv + tz * CV_FLOATS, CV_BYTES, fa);
-        mbar_arrive_expect_tx(fb, STAGE_B_BYTES);
+        mbar_arrive_expect_tx(fb, STAGE_B_BYTES + (has_gate ? 8192u : 0u));
+        if (has_gate) tma_load_3d(st + ST_G, &tmg, fb, row0, h, tok);
         tma_load_3d(st + ST_Q, &tmq, fb, 0, h, tok);
         tma_load_3d(st + ST_Q + ST_CB, &tmq, fb, 64, h, tok);
         bulk_load(st + ST_W, wimg + tz * WS_W_BYTES, TILE_BYTES, fb);
@@ -1067,6 +1156,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async();
     mbar_arrive(&bars[B_SREADY]);
     // [Q;-W] S^T accumulated onto U0: H = Q S^T (rows 0-63), U (64-127)
+    // Fused epilogue on one chunk's output rows (o: this thread's kCW
+    // columns of row r): o <- o / sqrt(mean(o^2) + eps) * w, then *
+    // sigmoid(gate). Returns false, the same on every output thread, when a
+    // wait for the partner CTA gave up.
+    const float* ep_w = reinterpret_cast<const float*>(sm + OFF_EPW);
+    float* ep_red = reinterpret_cast<float*>(sm + OFF_EPRED);
+    float* ep_x = reinterpret_cast<float*>(sm + OFF_EPX);
+    const uint32_t partner = clustered ? (cluster_ctarank() ^ 1u) : 0u;
+    auto epilogue_rows = [&](float (&o)[kCW], const uint4 (&gzv)[kCW / 8],
+                             int r, int cgi, int i, int b) {
+      bool okp = true;
+      if (p.norm_w) {
+        float ss = 0.f;
+#pragma unroll
+        for (int c = 0; c < kCW; ++c) ss = fmaf(o[c], o[c], ss);
+        ep_red[cgi * 64 + r] = ss;
+        named_bar(4, kChainThreads / 2);
+        float tot = 0.f;
+#pragma unroll
+        for (int g = 0; g < kChainWarps / 4; ++g) tot += ep_red[g * 64 + r];
+        if (clustered) {
+          // Send this half-row sum to the partner (its slot b counts the
+          // bytes), then take the partner's from ours. Slot b is not
+          // rewritten before it is read here: the partner sends chunk i + 2
+          // only after it has received this CTA's chunk i + 1, sent after
+          // this read.
+          if (cgi == 0)
+            st_async_f32(map_to_cta(ep_x + b * 64 + r, partner), tot,
+                         map_to_cta(&bars[B_XS0 + b], partner));
+          okp = mbar_wait_cluster(&bars[B_XS0 + b], (i >> 1) & 1, abort_flag);
+          if (okp) tot += ep_x[b * 64 + r];
+          okp = bar_and(4, kChainThreads / 2, okp);  // every row read its slot
+          // arm slot b for chunk i + 2
+          if (okp && tid == 0 && i + 2 < nloc)
+            mbar_arrive_expect_tx(&bars[B_XS0 + b], 64 * 4);
+        }
+        const float sc = rsqrtf(tot * (1.f / (float)dv) + p.eps);
+#pragma unroll
+        for (int c = 0; c < kCW; ++c) o[c] *= sc * ep_w[cols + c];
+      }
+      if (has_gate) {
+#pragma unroll
+        for (int c8 = 0; c8 < kCW / 8; ++c8) {
+          float f[8];
+          unpack_bf16x8(gzv[c8], f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[8 * c8 + e] *= sigmoid_approx(f[e]);
+        }
+      }
+      return okp;
+    };
     bool ok = true;
     for (int i = 0; i < nloc; ++i) {
       const int b = i & 1;
@@ -1079,6 +1219,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           reinterpret_cast<const float*>(sm + OFF_STAGE + b * STAGE_BYTES + ST_CV);
       const float gam = cv[CV_GAMMA];
       const float rowf = cv[(u_rows ? CV_DEC : CV_EG) + (ct & 63)];
+      // the output row's gate logits, copied out before the stage is freed
+      uint4 gz[kCW / 8];
+      if (has_gate && !u_rows) {
+        ok = ok && mbar_wait(&bars[B_FULLB0 + b], (i >> 1) & 1, abort_flag);
+        const uint8_t* gt = sm + OFF_STAGE + b * STAGE_BYTES + ST_G;
+#pragma unroll
+        for (int c = 0; c < kCW / 8; ++c)
+          gz[c] = *reinterpret_cast<const uint4*>(gt + sw128(ct, chunk0 + c));
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_EMPTY0 + b]);
       float hq[kCW];  // H = Q S^T of this chunk (output rows)
@@ -1168,6 +1317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kCW; ++c) o[c] = fmaf(rowf, hq[c], o[c]);
           tc_fence_before();
           mbar_arrive(&bars[B_D3FREE0 + b]);
+          if (epi) ok4 = epilogue_rows(o, gz, r, cg, i, b);
           if (emit && len == C) {
             store_cols_bf16<kCW>(sm + OFF_O, r, chunk0, o);
             fence_proxy_async();
@@ -1228,6 +1378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // no CTA leaves while its partner may still write into its shared memory
+  if (clustered) cluster_sync();
   if (warp == kWarpPU) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -1448,12 +1600,16 @@ cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
 cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream) {
   const long long tokens = call_tokens(p);
   const long long tiles = chunk_tc_chunks_bound(p) * p.H;
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv, mo, mg;
   if (!make_map(&mq, p.q, p.dk, p.H, tokens, 1, 64) ||
       !make_map(&mk, p.k, p.dk, p.H, tokens, 1, 64) ||
       !make_map(&mv, p.v, p.dv, p.H, tokens, 1, 64) ||
-      !make_map(&mo, p.out, p.dv, p.H, tokens, 1, 64))
+      !make_map(&mo, p.out, p.dv, p.H, tokens, 1, 64) ||
+      !make_map(&mg, p.gate_z ? p.gate_z : p.out, p.dv, p.H, tokens, 1, 64))
     return cudaErrorInvalidValue;
+  // the fused epilogue pairs the two CTAs of each (sequence, head, part)
+  // when d_v = 128 (grid.x is then 2 or 4)
+  const bool clustered = p.epilogue && p.dv == 128;
   const int nchd = chunk_tc_nch_dense(p);
   auto launch = [&](auto kern) {
     cudaError_t e = cudaFuncSetAttribute(
@@ -1469,12 +1625,16 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = clustered ? 2 : 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, p, mq, mk, mv, mo, nchd, (int)tiles);
+    cfg.numAttrs = clustered ? 2 : 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p, mq, mk, mv, mo, mg, nchd, (int)tiles);
     if (e == cudaSuccess) e = cudaGetLastError();
     timing_stop(t, stream, e);
     return e;

@@ -135,14 +135,32 @@ int choose_parts_tc(int requested, int N, int H, int T, int dv, int C,
   return best_p;
 }
 
+// The steps either side of the recurrence (gdn_chunk_fwd_fused).
+struct Sublayer {
+  bool on = false;
+  const float* norm_w = nullptr;
+  const void* gate = nullptr;
+  float eps = 0.f;
+};
+
 int run_chunk(const void* q, const void* k, const void* v, const float* g,
               const float* beta, const float* h0, void* out, float* hT,
               const int32_t* cu_seqlens, int B, int H, int T, int dk, int dv,
               int C, int dtype, int variant, int path, int sp_parts,
-              cudaStream_t stream) {
+              cudaStream_t stream, const Sublayer& sub = Sublayer{}) {
   int rc = check_chunk_args(q, k, v, g, beta, h0, out, hT, cu_seqlens, B, H,
                             T, dk, dv, C, dtype, variant, path, sp_parts);
   if (rc != GDN_OK) return rc;
+  if (sub.on) {
+    if (!(sub.eps >= 0.f) || sub.eps > 3.0e38f) return GDN_ERR_INVALID_ARG;
+    // the tensor-core path's shapes only
+    if (dtype != GDN_DTYPE_BF16 || dk != 128 || (dv != 64 && dv != 128))
+      return GDN_ERR_UNSUPPORTED;
+    if ((sub.norm_w && !aligned16(sub.norm_w)) ||
+        (sub.gate && !aligned16(sub.gate)))
+      return GDN_ERR_MISALIGNED;
+    if (sub.gate && sub.gate == out) return GDN_ERR_INVALID_ARG;
+  }
   if (B == 0 || H == 0) return GDN_OK;
   int* status = nullptr;
   if ((rc = current_status_ptr(&status)) != GDN_OK) return rc;
@@ -156,8 +174,15 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
   const bool bf16 = dtype == GDN_DTYPE_BF16;
   const long long tokens = cu_seqlens ? (long long)T : (long long)B * T;
   const bool tc_ok = bf16 && chunk_tc_supported(dk, dv, tokens, B, H);
-  if (path == GDN_PATH_TCGEN05 && !tc_ok) return GDN_ERR_UNSUPPORTED;
+  if ((path == GDN_PATH_TCGEN05 || sub.on) && !tc_ok) return GDN_ERR_UNSUPPORTED;
   const bool use_tc = tc_ok && path != GDN_PATH_SIMT;
+  if (sub.on) {
+    p.prologue = 1;
+    p.epilogue = (sub.norm_w || sub.gate) ? 1 : 0;
+    p.norm_w = sub.norm_w;
+    p.gate_z = sub.gate;
+    p.eps = sub.eps;
+  }
   auto launch = [&](const ChunkParams& q) {
     return use_tc ? launch_chunk_tc(q, stream)
                   : launch_chunk_simt(q, bf16, stream);
@@ -325,6 +350,22 @@ int gdn_chunk_fwd_ex(const void* q, const void* k, const void* v,
                      gdn_stream_t stream) {
   return gdn::run_chunk(q, k, v, g, beta, h0, out, hT, cu_seqlens, B, H, T,
                         dk, dv, C, dtype, variant, path, sp_parts, stream);
+}
+
+int gdn_chunk_fwd_fused(const void* q, const void* k, const void* v,
+                        const float* a, const float* b, const float* h0,
+                        void* out, float* hT, const int32_t* cu_seqlens,
+                        const float* norm_weight, const void* gate, float eps,
+                        int B, int H, int T, int dk, int dv, int C,
+                        gdn_stream_t stream) {
+  gdn::Sublayer sub;
+  sub.on = true;
+  sub.norm_w = norm_weight;
+  sub.gate = gate;
+  sub.eps = eps;
+  return gdn::run_chunk(q, k, v, a, b, h0, out, hT, cu_seqlens, B, H, T, dk,
+                        dv, C, GDN_DTYPE_BF16, GDN_GATE_BEFORE_PREDICT,
+                        GDN_PATH_TCGEN05, 0, stream, sub);
 }
 
 int gdn_recurrent_step(const void* q, const void* k, const void* v,

@@ -53,6 +53,17 @@ struct ChunkParams {
   void* pm;                  // [chunks, H, 64, 64] bf16, (Q K^T) (.) D (.) M
   void* tu;                  // [chunks, H, 64, 64] bf16, T diag(beta)
   float* cv;                 // [chunks, H, 132] fp32, e^G, e^{G_L-G}, gamma
+  // steps either side of the recurrence (gdn_chunk_fwd_fused; tensor-core
+  // path only): with `prologue` set, q and k are raw (normalised in the
+  // kernels), g holds the gate logits a (g = -softplus(a)) and beta the step
+  // logits b (beta = sigmoid(b)); with `epilogue` set, each output row is
+  // RMS-normalised over d_v (times norm_w when given) and gated by
+  // sigmoid(gate_z) when given
+  int prologue;
+  int epilogue;
+  const float* norm_w;       // [dv] fp32 or null
+  const void* gate_z;        // like out (bf16) or null
+  float eps;
 };
 
 struct DecodeParams {

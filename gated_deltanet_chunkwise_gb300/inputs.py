@@ -102,3 +102,41 @@ def decode_inputs(N, H, dk, dv, *, dtype="bf16", seed=0):
         "beta": torch.from_numpy(beta),
         "state": torch.from_numpy(state),
     }
+
+
+def fused_inputs(B, H, T, dk, dv, *, seed=0, h0=False, lengths=None,
+                 weight=True, gate=True):
+    """Raw inputs of gdn_chunk_fwd_fused: q and k NOT normalised (each row
+    an N(0, 1) vector times a length drawn from U[0.25, 4)), v ~ N(0, 1),
+    gate logits a and step logits b ~ N(0, 1) (fp32), h0 ~ 0.1 N(0, 1), the
+    output norm weight 1 + 0.1 N(0, 1) (fp32 [dv]) and the output gate
+    logits ~ N(0, 1) (bf16, like v). Draw order: lengths, q, q lengths, k,
+    k lengths, v, a, b, h0, weight, gate."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if lengths is not None:
+        lengths = [int(x) for x in lengths]
+        N = len(lengths)
+        cu = np.zeros(N + 1, dtype=np.int32)
+        cu[1:] = np.cumsum(lengths)
+        Bt, Tt = 1, int(cu[-1])
+    else:
+        N, Bt, Tt, cu = B, B, T, None
+    q = _normal(rng, (Bt, Tt, H, dk))
+    q *= rng.uniform(0.25, 4.0, (Bt, Tt, H, 1)).astype(np.float32)
+    k = _normal(rng, (Bt, Tt, H, dk))
+    k *= rng.uniform(0.25, 4.0, (Bt, Tt, H, 1)).astype(np.float32)
+    v = _normal(rng, (Bt, Tt, H, dv))
+    a = _normal(rng, (Bt, Tt, H))
+    b = _normal(rng, (Bt, Tt, H))
+    h = (0.1 * _normal(rng, (N, H, dk, dv))).astype(np.float32) if h0 else None
+    w = (1.0 + 0.1 * _normal(rng, (dv,))).astype(np.float32) if weight else None
+    z = _normal(rng, (Bt, Tt, H, dv)) if gate else None
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x))
+    bf = lambda x: t(x).to(torch.bfloat16)
+    return {
+        "q": bf(q), "k": bf(k), "v": bf(v), "a": t(a), "b": t(b),
+        "h0": None if h is None else t(h),
+        "cu_seqlens": None if cu is None else t(cu),
+        "norm_weight": None if w is None else t(w),
+        "gate": None if z is None else bf(z),
+    }

@@ -131,6 +131,33 @@ int gdn_chunk_fwd_ex(const void* q, const void* k, const void* v,
                      gdn_stream_t stream);
 
 /*
+ * gdn_chunk_fwd_fused -- the forward pass with the steps either side of the
+ * recurrence done in the same kernels (illustrated DeltaNet page, the
+ * architecture table and its L2 Norm / RMSNorm paragraphs; its GDN section
+ * for the output gate):
+ *   in:  q <- q / |q|, k <- k / |k| per (token, head) over d_k (a zero vector
+ *        stays zero); log alpha g = -softplus(a); beta = sigmoid(b)
+ *   out: o <- o / sqrt(mean_{d_v}(o^2) + eps) * norm_weight, per (token,
+ *        head), when norm_weight is given; then o <- o * sigmoid(gate)
+ *        elementwise when gate is given
+ *   q, k        bf16 [B, T, H, dk], raw (not normalised)
+ *   a, b        fp32 [B, T, H] gate and step logits
+ *   norm_weight fp32 [dv] (device) or NULL: no output normalisation
+ *   gate        bf16 [B, T, H, dv] (device) or NULL: no output gate
+ *   eps         >= 0, added to the mean of squares
+ * Other arguments as gdn_chunk_fwd (decay before the prediction, automatic
+ * sequence-parallel split). Served by the bf16 tensor-core path only:
+ * dk = 128 and dv in {64, 128}; other shapes return GDN_ERR_UNSUPPORTED.
+ * The pages print no interface; this one is the library's.
+ */
+int gdn_chunk_fwd_fused(const void* q, const void* k, const void* v,
+                        const float* a, const float* b, const float* h0,
+                        void* out, float* hT, const int32_t* cu_seqlens,
+                        const float* norm_weight, const void* gate, float eps,
+                        int B, int H, int T, int dk, int dv, int C,
+                        gdn_stream_t stream);
+
+/*
  * gdn_recurrent_step -- one decode token per (sequence, head), state updated
  * in place (the token recurrence above applied once).
  *   q, k   bf16 [N, H, dk]      v, out  bf16 [N, H, dv]

@@ -12,7 +12,9 @@ parameterisation of the workloads (alpha = exp(-softplus(x))).
 Readings (the pages leave these open): a zero q or k vector stays zero (its
 length is 0, nothing to divide); the RMSNorm epsilon is added to the mean of
 squares; the output gate multiplies after the weight, out = RMSNorm(o) * w *
-sigmoid(z), z an input of the same shape as o.
+sigmoid(z), z an input of the same shape as o; the normalisation is applied
+when a weight is given (a unit weight is passed as ones) and the gate when
+gate logits are given, so either step can be left out.
 """
 from __future__ import annotations
 
@@ -64,8 +66,9 @@ def prologue(q_raw, k_raw, a, b):
 
 
 def epilogue(o, weight=None, gate=None, eps=1e-6):
-    """RMSNorm(o) * weight, then * sigmoid(gate) when a gate is given."""
-    y = rms_norm(o, weight, eps)
+    """RMSNorm(o) * weight when a weight is given, then * sigmoid(gate) when
+    gate logits are given."""
+    y = _f64(o) if weight is None else rms_norm(o, weight, eps)
     return y if gate is None else y * sigmoid(gate)
 
 

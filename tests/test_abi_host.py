@@ -146,3 +146,30 @@ def test_timing_switch_and_read_on_host(lib):
     assert so.gdn_timing_read(-1, None, None) == INVALID
     assert so.gdn_timing_enable(0) == OK
     assert lib.kernel_timings() == {}
+
+
+def fused(so, q=A, k=A + 0x1000, v=A + 0x2000, a=A + 0x3000, b=A + 0x4000,
+          h0=None, out=A + 0x5000, hT=None, cu=None, w=A + 0x7000,
+          gate=A + 0x8000, eps=1e-6, B=1, H=1, T=64, dk=128, dv=128, C=64):
+    return so.gdn_chunk_fwd_fused(q, k, v, a, b, h0, out, hT, cu, w, gate,
+                                  ctypes.c_float(eps), B, H, T, dk, dv, C,
+                                  None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), INVALID),
+    (dict(eps=-1.0), INVALID),
+    (dict(eps=float("nan")), INVALID),
+    (dict(dk=64), UNSUPPORTED),          # the tensor-core path's shapes only
+    (dict(dv=32), UNSUPPORTED),
+    (dict(w=ODD), MISALIGNED),
+    (dict(gate=ODD), MISALIGNED),
+    (dict(gate=A + 0x5000), INVALID),    # gate aliases out
+    (dict(C=32), UNSUPPORTED),
+])
+def test_fused_rejects_on_host(lib, kw, expect):
+    assert fused(lib.library(), **kw) == expect
+
+
+def test_fused_empty_batch_is_a_no_op(lib):
+    assert fused(lib.library(), B=0) == OK

@@ -74,15 +74,22 @@ def _raw(B, H, T, d, seed):
 
 def test_fused_forward_invariants():
     q, k, v, a, b = _raw(1, 2, 40, 16, 1)
-    out, hT = sublayer.fused_forward(q, k, v, a, b, eps=0.0)
+    ones = np.ones(16)
+    out, hT = sublayer.fused_forward(q, k, v, a, b, weight=ones, eps=0.0)
     # the recurrence sees unit q, k: scaling the raw vectors changes nothing
-    out2, hT2 = sublayer.fused_forward(3.0 * q, 0.25 * k, v, a, b, eps=0.0)
+    out2, hT2 = sublayer.fused_forward(3.0 * q, 0.25 * k, v, a, b, weight=ones,
+                                       eps=0.0)
     assert np.allclose(out, out2) and np.allclose(hT, hT2)
-    # output RMS is 1 per (token, head) without weight and gate
+    # output RMS is 1 per (token, head) with a unit weight and no gate
     assert np.allclose(np.mean(out ** 2, axis=-1), 1.0)
     # the gate multiplies elementwise; an all-zero gate logit halves the output
-    out3, _ = sublayer.fused_forward(q, k, v, a, b, gate=np.zeros_like(v), eps=0.0)
+    out3, _ = sublayer.fused_forward(q, k, v, a, b, weight=ones,
+                                     gate=np.zeros_like(v), eps=0.0)
     assert np.allclose(out3, 0.5 * out)
+    # without weight and gate the read-out is passed through unchanged
+    o_plain, _ = sublayer.fused_forward(q, k, v, a, b)
+    assert np.allclose(o_plain * np.sqrt(np.mean(o_plain ** 2, axis=-1,
+                                                  keepdims=True)) ** -1, out)
     # the recurrence between the two is the oracle's, on the activated inputs
     o_ref, h_ref = oracle.forward(q / np.linalg.norm(q, axis=-1, keepdims=True),
                                   k / np.linalg.norm(k, axis=-1, keepdims=True),
