@@ -277,9 +277,10 @@ def gdn_recurrent_step(q, k, v, g, beta, state, *, out=None, stream=None):
 
 
 def gdn_selftest_mma(A, B, *, a_mn=False, b_mn=False, b_stacked=False,
-                     twice=False, stream=None):
+                     twice=False, a_tmem=False, stream=None):
     """D = A @ B (x2 when ``twice``) through one tcgen05 MMA sequence with the
-    chunk kernel's shared-memory layouts. A bf16 [128, K], B bf16 [K, N]."""
+    chunk kernel's shared-memory layouts. A bf16 [128, K], B bf16 [K, N];
+    ``a_tmem`` places A in TMEM instead of shared memory."""
     dev = A.device
     _need(A, "A", torch.bfloat16, None)
     _need(B, "B", torch.bfloat16, dev)
@@ -289,7 +290,8 @@ def gdn_selftest_mma(A, B, *, a_mn=False, b_mn=False, b_stacked=False,
     D = torch.empty((128, N), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
         rc = library().gdn_selftest_mma(_ptr(A), _ptr(B), _ptr(D), K, N,
-                                        int(a_mn), int(b_mn), int(b_stacked),
+                                        2 if a_tmem else int(a_mn),
+                                        int(b_mn), int(b_stacked),
                                         int(twice), _stream(stream))
     if rc != GDN_OK:
         raise GdnError(rc, "gdn_selftest_mma")

@@ -892,9 +892,10 @@ __device__ __forceinline__ uint32_t bar_count(int b) {
   switch (b) {
     // the U issuer's and the P U warp's MMA commits (the state issuer's
     // products have completed before the U issuer's), one per chain warp
+    // (each chain warp arrives once, after its lanes' writes and fences)
     case B_EMPTY0: case B_EMPTY1: return 2 + kChainThreads / 32;
-    case B_SREADY: return kChainThreads;
-    case B_UREADY: case B_D3FREE0: case B_D3FREE1: return kChainThreads / 2;
+    case B_SREADY: return kChainThreads / 32;
+    case B_UREADY: case B_D3FREE0: case B_D3FREE1: return kChainThreads / 64;
     case B_DRAIN_C: return 2;  // the state issuer warp and the U issuer
     // the partner's 64 row sums, counted in bytes (armed once per use)
     default: return 1;
@@ -1154,7 +1155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     store_cols_bf16<kCW>(s_tile, ct, chunk0, S);
     fence_proxy_async();
-    mbar_arrive(&bars[B_SREADY]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[B_SREADY]);
     // [Q;-W] S^T accumulated onto U0: H = Q S^T (rows 0-63), U (64-127)
     // Fused epilogue on one chunk's output rows (o: this thread's kCW
     // columns of row r): o <- o / sqrt(mean(o^2) + eps) * w, then *
@@ -1280,7 +1282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           store_cols_bf16<kCW>(sm + OFF_U, r, chunk0, u);
           fence_proxy_async();
           tc_fence_before();
-          mbar_arrive(&bars[B_UREADY]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[B_UREADY]);
         }
         ok = ok1;
       }
@@ -1300,7 +1303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       store_cols_bf16<kCW>(s_tile, ct, chunk0, S);
       fence_proxy_async();
       tc_fence_before();
-      mbar_arrive(&bars[B_SREADY]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_SREADY]);
       if (!u_rows) {
         // O = e^{G_r} H + P U, through a shared-memory tile and a TMA store
         // for a whole chunk, direct stores for a partial one
@@ -1316,7 +1320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kCW; ++c) o[c] = fmaf(rowf, hq[c], o[c]);
           tc_fence_before();
-          mbar_arrive(&bars[B_D3FREE0 + b]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[B_D3FREE0 + b]);
           if (epi) ok4 = epilogue_rows(o, gz, r, cg, i, b);
           if (emit && len == C) {
             store_cols_bf16<kCW>(sm + OFF_O, r, chunk0, o);
@@ -1391,6 +1396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // Self-test: D = A * B (x2 when twice) with the layouts above, one CTA.
 // N = 64 or 128 (an N-major B of 128 columns is two 64-column blocks).
+// a_mn: 0 A K-major in shared memory, 1 M-major, 2 A in TMEM (bf16 pairs in
+// columns 128 .. 128 + K / 2, written with tcgen05.st).
 __global__ void __launch_bounds__(128)
     selftest_mma_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B,
                         float* D, int K, int N, int a_mn, int b_mn,
@@ -1404,7 +1411,7 @@ __global__ void __launch_bounds__(128)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + 65548);
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp == 0) {
-    tmem_alloc(slot, 128);
+    tmem_alloc(slot, 256);
     tmem_relinquish();
   }
   if (tid == 0) {
@@ -1415,7 +1422,7 @@ __global__ void __launch_bounds__(128)
   for (int i = tid; i < 65536 / 16; i += 128)
     reinterpret_cast<uint4*>(sm)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
-  for (int idx = tid; idx < 128 * K; idx += 128) {
+  for (int idx = tid; a_mn != 2 && idx < 128 * K; idx += 128) {
     const int m = idx / K, k = idx % K;
     const uint32_t off =
         a_mn ? (uint32_t)((m >> 6) * (K * 128)) + sw128(k, (m & 63) >> 3) + (m & 7) * 2
@@ -1435,8 +1442,23 @@ __global__ void __launch_bounds__(128)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot;
+  if (a_mn == 2) {
+    // row tid of A into this thread's lane (warp w owns lanes 32 w ..)
+    for (int c0 = 0; c0 < K / 2; c0 += 32) {
+      uint32_t u[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        u[j] = pack_bf16x2(__bfloat162float(A[tid * K + 2 * (c0 + j)]),
+                           __bfloat162float(A[tid * K + 2 * (c0 + j) + 1]));
+      tmem_st32(tmem + ((uint32_t)(32 * warp) << 16) + 128 + c0, u);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
   if (tid == 0) {
-    const uint32_t id = idesc_bf16(128, N, a_mn != 0, b_mn != 0);
+    const uint32_t id = idesc_bf16(128, N, a_mn == 1, b_mn != 0);
     for (int pass = 0; pass <= (twice ? 1 : 0); ++pass)
       for (int s = 0; s < K / 16; ++s) {
         const uint64_t a =
@@ -1445,7 +1467,10 @@ __global__ void __launch_bounds__(128)
         const uint64_t b =
             b_mn ? sdesc(base + 32768 + s * 2048, K * 128, 1024)
                  : sdesc(base + 32768 + (s >> 2) * bstride + (s & 3) * 32, 16, 1024);
-        mma_bf16(tmem, a, b, id, (pass > 0 || s > 0) ? 1u : 0u);
+        if (a_mn == 2)
+          mma_bf16_ta(tmem, tmem + 128 + 8 * s, b, id, (pass > 0 || s > 0) ? 1u : 0u);
+        else
+          mma_bf16(tmem, a, b, id, (pass > 0 || s > 0) ? 1u : 0u);
       }
     mma_commit(bar);
   }
@@ -1466,7 +1491,7 @@ __global__ void __launch_bounds__(128)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 256);
   }
 }
 
@@ -1653,6 +1678,7 @@ extern "C" int gdn_selftest_mma(const void* A, const void* B, float* D, int K,
   if (!A || !B || !D || (K != 64 && K != 128) || (N != 64 && N != 128))
     return GDN_ERR_INVALID_ARG;
   if (b_stacked && N != 64) return GDN_ERR_INVALID_ARG;
+  if (a_mn < 0 || a_mn > 2) return GDN_ERR_INVALID_ARG;
   int* status = nullptr;
   int rc = device_status_ptr(&status);
   if (rc != GDN_OK) return rc;

@@ -327,6 +327,35 @@ __device__ __forceinline__ void mma_bf16_run(uint32_t d_tmem, uint64_t a,
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem], bf16 inputs, fp32 accumulation. A holds
+// its rows in TMEM lanes, two bf16 elements per 32-bit column (element 2j in
+// the low half of column j), so a K step of 16 spans 8 columns.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem,
+                                            uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// As mma_bf16_run with A in TMEM: NK consecutive K steps.
+template <int NK>
+__device__ __forceinline__ void mma_bf16_ta_run(uint32_t d_tmem, uint32_t a_tmem,
+                                                uint64_t b, uint32_t b_step,
+                                                uint32_t idesc, bool accumulate) {
+  mma_bf16_ta(d_tmem, a_tmem, b, idesc, accumulate ? 1u : 0u);
+#pragma unroll
+  for (int k = 1; k < NK; ++k)
+    asm volatile(
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
+        "r"(a_tmem + 8u * k), "l"(b + (uint64_t)((k * b_step) >> 4)), "r"(idesc)
+        : "memory");
+}
+
 // Arrive on `bar` once every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -371,6 +400,34 @@ template <int N>
 __device__ __forceinline__ void tmem_ldn(uint32_t taddr, float (&r)[N]) {
   static_assert(N == 16 || N == 32, "16 or 32 columns");
   if constexpr (N == 16) tmem_ld16(taddr, r); else tmem_ld32(taddr, r);
+}
+
+// Store 16 / 32 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&u)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+      ::"r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]),
+      "r"(u[5]), "r"(u[6]), "r"(u[7]), "r"(u[8]), "r"(u[9]), "r"(u[10]),
+      "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&u)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, "
+      "%31, %32};"
+      ::"r"(taddr), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]),
+      "r"(u[5]), "r"(u[6]), "r"(u[7]), "r"(u[8]), "r"(u[9]), "r"(u[10]),
+      "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15]), "r"(u[16]),
+      "r"(u[17]), "r"(u[18]), "r"(u[19]), "r"(u[20]), "r"(u[21]), "r"(u[22]),
+      "r"(u[23]), "r"(u[24]), "r"(u[25]), "r"(u[26]), "r"(u[27]), "r"(u[28]),
+      "r"(u[29]), "r"(u[30]), "r"(u[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {

@@ -22,7 +22,10 @@ extern "C" {
  *   A  bf16 [128, K] row-major (device)    B  bf16 [K, N] row-major (device)
  *   D  fp32 [128, N] row-major (device, written)
  *   K  64 or 128;  N  64 or 128 (b_stacked requires N = 64)
- *   a_mn       store A M-major (else K-major) before the MMA
+ *   a_mn       0: A K-major in shared memory; 1: A M-major in shared memory;
+ *              2: A in TMEM (row m in lane m, bf16 pairs per 32-bit column,
+ *              written with tcgen05.st), the form of the chain's S and U
+ *              operands
  *   b_mn       store B N-major (else K-major)
  *   b_stacked  K-major B placed in the first 64 rows of a 128-row tile
  *   twice      issue the MMA sequence twice with accumulation
