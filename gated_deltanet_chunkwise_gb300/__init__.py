@@ -17,7 +17,9 @@ _ABI_NAMES = (
     "gdn_timing_enable", "gdn_timing_read", "kernel_timings",
     "GDN_KERNEL_CHUNK_PREP", "GDN_KERNEL_CHUNK_CHAIN", "GDN_KERNEL_CHUNK_SIMT",
     "GDN_KERNEL_SP_CHAIN", "GDN_KERNEL_DECODE", "GDN_KERNEL_CHUNK_OFFSETS",
-    "GDN_KERNEL_COUNT", "KERNEL_NAMES",
+    "GDN_KERNEL_CHUNK_CHAIN_WHOLE", "GDN_KERNEL_COUNT", "KERNEL_NAMES",
+    "GDN_PATH_AUTO", "GDN_PATH_SIMT", "GDN_PATH_TCGEN05",
+    "GDN_PATH_TCGEN05_SPLIT", "GDN_PATH_TCGEN05_WHOLE",
 )
 
 

@@ -25,6 +25,8 @@ GDN_DTYPE_F32 = 1
 GDN_PATH_AUTO = 0
 GDN_PATH_SIMT = 1
 GDN_PATH_TCGEN05 = 2
+GDN_PATH_TCGEN05_SPLIT = 3
+GDN_PATH_TCGEN05_WHOLE = 4
 # kernel families for per-kernel timing (gdn_kernel_t)
 GDN_KERNEL_CHUNK_PREP = 0
 GDN_KERNEL_CHUNK_CHAIN = 1
@@ -32,7 +34,8 @@ GDN_KERNEL_CHUNK_SIMT = 2
 GDN_KERNEL_SP_CHAIN = 3
 GDN_KERNEL_DECODE = 4
 GDN_KERNEL_CHUNK_OFFSETS = 5
-GDN_KERNEL_COUNT = 6
+GDN_KERNEL_CHUNK_CHAIN_WHOLE = 6
+GDN_KERNEL_COUNT = 7
 KERNEL_NAMES = {
     GDN_KERNEL_CHUNK_PREP: "ut_prep_kernel",
     GDN_KERNEL_CHUNK_CHAIN: "chunk_tc_kernel",
@@ -40,6 +43,7 @@ KERNEL_NAMES = {
     GDN_KERNEL_SP_CHAIN: "sp_chain_kernel",
     GDN_KERNEL_DECODE: "decode_kernel",
     GDN_KERNEL_CHUNK_OFFSETS: "chunk_offsets_kernel",
+    GDN_KERNEL_CHUNK_CHAIN_WHOLE: "chain_tx_kernel",
 }
 
 _lib = None
@@ -89,7 +93,7 @@ def library():
     lib.gdn_selftest_mma.restype = i
     lib.gdn_chunk_fwd_fused.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, ip,
                                         fp, vp, ctypes.c_float, i, i, i, i,
-                                        i, i, vp]
+                                        i, i, i, vp]
     lib.gdn_chunk_fwd_fused.restype = i
     lib.gdn_timing_enable.argtypes = [i]
     lib.gdn_timing_enable.restype = i
@@ -216,7 +220,8 @@ def gdn_chunk_fwd_ex(q, k, v, g, beta, h0=None, cu_seqlens=None, *, out=None,
 
 def gdn_chunk_fwd_fused(q, k, v, a, b, h0=None, cu_seqlens=None, *,
                         norm_weight=None, gate=None, eps=1e-6, out=None,
-                        hT=None, output_final_state=True, C=64, stream=None):
+                        hT=None, output_final_state=True, C=64,
+                        path=GDN_PATH_AUTO, stream=None):
     """The forward pass with the steps either side fused: raw q, k (L2-
     normalised in the kernels), gate logits a (log alpha = -softplus(a)) and
     step logits b (beta = sigmoid(b)); output RMS-normalised over d_v and
@@ -240,7 +245,8 @@ def gdn_chunk_fwd_fused(q, k, v, a, b, h0=None, cu_seqlens=None, *,
         def __call__(self, q_, k_, v_, a_, b_, h0_, out_, hT_, cu_, N, H, T,
                      dk, dv, C_, stream_):
             return self.f(q_, k_, v_, a_, b_, h0_, out_, hT_, cu_,
-                          *extra_ptrs, N, H, T, dk, dv, C_, stream_)
+                          *extra_ptrs, N, H, T, dk, dv, C_, int(path),
+                          stream_)
 
     lib = library()
     return _chunk_call_fn(_Fn(lib.gdn_chunk_fwd_fused), "gdn_chunk_fwd_fused",

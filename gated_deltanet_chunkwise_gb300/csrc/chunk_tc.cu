@@ -1394,6 +1394,654 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 
 // ---------------------------------------------------------------------------
+// chain_tx_kernel: the serial chain with the state rows in TMEM lanes, one
+// CTA per (sequence, head, part) and 128 state rows (the d_v value rows,
+// padded with zero rows when d_v = 64; in a split pass a second CTA takes
+// the 128 rows of the scaling matrix). With S (rows x d_k) and U^T (rows x tokens) in TMEM lanes both
+// are A operands straight from TMEM, so the chain has no shared-memory
+// round trip:
+//   side   V^T T_U^T -> U0^T starts the chunk's accumulator (cols 0-63; the
+//          output warps zeroed cols 64-127 when they read the accumulator
+//          out)
+//   chain  += S [-W;Q]^T -> U^T = U0^T - S W^T (cols 0-63),
+//                           H^T = S Q^T (cols 64-127)
+//          U^T -> bf16 pairs in TMEM;  U^T K_d -> Delta^T;
+//          S <- gamma S + Delta^T -> bf16 pairs in TMEM
+//   side   U^T P^T -> cols 0-63 (U^T has been converted)
+//   out    O^T = H^T diag(e^G) + U^T P^T
+// with K_d = diag(e^{G_L-G}) K scaled in place in shared memory by the chain
+// warps while the [-W;Q] product runs.
+//
+// Warps: 0-7 chain (lane quarter warp & 3, d_k half warp >> 2: 64 fp32 state
+// columns each), 8-11 output (one row of O^T per thread), 12 TMA producer,
+// 13 issuer of the chain's products ([-W;Q_g], Delta^T), 14 issuer of the
+// side products (U0^T, P), which it slots into the tensor pipe's idle spells
+// of the chain (the conversion of U^T, the state update).
+constexpr int kTxChainThreads = 256;
+constexpr int kTxOutThreads = 128;
+constexpr int kTxWarpProducer = 12, kTxWarpMMA = 13, kTxWarpSide = 14;
+constexpr int kTxThreads = 15 * 32;
+constexpr int TXR = 128;  // state rows per CTA
+// Stage: per 64-column block of d_k a 128-row K-major tile [-W; Q]; K
+// (N-major B of the Delta^T product; two 64-column blocks); V (M-major A of
+// U0^T; two 64-column blocks); T_U (K-major B); P; the decay vectors.
+constexpr uint32_t TX_W = 0, TX_Q = 8192, TX_WQ_CB = 16384;
+constexpr uint32_t TX_K = 32768, TX_V = 49152, TX_TU = 65536, TX_P = 73728,
+                   TX_CV = 81920;
+constexpr uint32_t TX_STAGE = 82944;
+// A stage arrives and is released in three groups, each as soon as its last
+// reader is done: V, T_U (U0^T); -W, Q ([-W;Q] product); K, P and the decay
+// vectors (Delta^T and P products, chain and output warps).
+constexpr uint32_t TX_A_BYTES = 16384 + TILE_BYTES;             // V, T_U
+constexpr uint32_t TX_B_BYTES = 2 * 16384;                      // -W, Q
+constexpr uint32_t TX_C_BYTES = 16384 + TILE_BYTES + CV_BYTES;  // K, P, cv
+// After the two stages: two output tiles (64 tokens x 128 values, two
+// 64-column blocks each; the fused gate is loaded into them), the output
+// warps' partial sums of squares and per-token scales.
+constexpr uint32_t TXO_OUT = 2 * TX_STAGE;
+constexpr uint32_t TXO_RED = TXO_OUT + 2 * 16384;
+constexpr uint32_t TXO_RS = TXO_RED + 4 * 64 * 4;
+constexpr uint32_t TXO_BAR = TXO_RS + 64 * 4;
+enum {
+  TB_FULLA0, TB_FULLA1, TB_FULLB0, TB_FULLB1, TB_FULLC0, TB_FULLC1,
+  TB_EMPTYA0, TB_EMPTYA1, TB_EMPTYB0, TB_EMPTYB1, TB_EMPTYC0, TB_EMPTYC1,
+  TB_SREADY, TB_D1FULL0, TB_D1FULL1, TB_UREADY,
+  TB_D2FULL, TB_OFULL0, TB_OFULL1, TB_D1FREE0, TB_D1FREE1, TB_GATE0,
+  TB_GATE1, TB_U0DONE0, TB_U0DONE1, TB_DRAIN, TB_DRAIN2, TB_COUNT
+};
+constexpr uint32_t TXO_MISC = TXO_BAR + TB_COUNT * 8;
+constexpr uint32_t TX_SMEM = TXO_MISC + 16 + 1024;
+static_assert(TX_CV + CV_BYTES <= TX_STAGE && TX_STAGE % 1024 == 0,
+              "transposed stage layout");
+static_assert(TX_SMEM <= 232448, "shared memory budget");
+// TMEM columns: two accumulators [U^T -> U^T P^T | H^T] (128 each),
+// Delta^T (128), S and U^T as bf16 pairs (64, 32).
+constexpr uint32_t TX_D1 = 0, TX_D2 = 256, TX_SB = 384, TX_UB = 448;
+constexpr uint32_t ID_TX_U0 = idesc_bf16(128, 64, true, false);
+constexpr uint32_t ID_TX_N128 = idesc_bf16(128, 128, false, false);
+constexpr uint32_t ID_TX_D = idesc_bf16(128, 128, false, true);
+constexpr uint32_t ID_TX_N64 = idesc_bf16(128, 64, false, false);
+
+__device__ __forceinline__ uint32_t tx_bar_count(int b) {
+  switch (b) {
+    case TB_D1FREE0: case TB_D1FREE1: return kTxOutThreads / 32;
+    // both issuers' commits (Delta^T reads K_d, P U reads P), one per chain
+    // warp (gamma, K_d) and one per output warp (e^G)
+    case TB_EMPTYC0: case TB_EMPTYC1:
+      return 2 + (kTxChainThreads + kTxOutThreads) / 32;
+    case TB_SREADY: case TB_UREADY: return kTxChainThreads / 32;
+    default: return 1;
+  }
+}
+
+// Byte offset of element (token t, column c) of a 64-token x 128-column
+// bf16 tile stored as two 64-column blocks with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t tx_tile_off(int t, int c) {
+  return (uint32_t)((c >> 6) * 8192) + sw128(t, (c & 63) >> 3) + (c & 7) * 2;
+}
+
+// Scale the 64 rows of a bf16 tile pair (two 8 KB 64-column blocks `blk`
+// bytes apart) by f[row], in place; the 256 chain threads, thread c of them.
+// All loads go out before the first store (the stores could alias them).
+__device__ __forceinline__ void tx_scale_rows(uint8_t* tile, uint32_t blk,
+                                              const float* f, int c) {
+  uint4 x[4];
+  float s[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e = c + k * kTxChainThreads, t = (e >> 3) & 63;
+    x[k] = *reinterpret_cast<const uint4*>(tile + (e >> 9) * blk + t * 128 +
+                                           (e & 7) * 16);
+    s[k] = f[t];
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e = c + k * kTxChainThreads, t = (e >> 3) & 63;
+    float v[8];
+    unpack_bf16x8(x[k], v);
+    uint4 w;
+    w.x = pack_bf16x2(v[0] * s[k], v[1] * s[k]);
+    w.y = pack_bf16x2(v[2] * s[k], v[3] * s[k]);
+    w.z = pack_bf16x2(v[4] * s[k], v[5] * s[k]);
+    w.w = pack_bf16x2(v[6] * s[k], v[7] * s[k]);
+    *reinterpret_cast<uint4*>(tile + (e >> 9) * blk + t * 128 + (e & 7) * 16) = w;
+  }
+}
+
+__global__ void __launch_bounds__(kTxThreads, 1)
+    chain_tx_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tmq,
+                    const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv,
+                    const __grid_constant__ CUtensorMap tmo,
+                    const __grid_constant__ CUtensorMap tmg, int nch_dense,
+                    int tiles) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + TXO_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + TXO_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + TXO_MISC + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = p.H, dv = p.dv;
+  const int h = blockIdx.y;
+  const int n = blockIdx.z / p.part_count;
+  const int part = p.part_begin + blockIdx.z % p.part_count;
+  const int row0 = blockIdx.x * TXR;
+  const bool value_rows = row0 < dv;
+  const bool split_tail = (p.mode == kModeSplit) && part > 0;
+  if (!value_rows && !(split_tail && row0 < dv + DK)) return;
+  const bool scale_rows = !value_rows;
+  const bool emit = value_rows && ((p.mode == kModeOutput) || part == 0);
+  const bool epi = p.epilogue && emit;
+  const bool has_gate = epi && p.gate_z != nullptr;
+  long long bos, eos;
+  if (!sequence_range(p, n, bos, eos)) return;
+  const int nch = (int)((eos - bos + C - 1) / C);
+  int c_begin, c_end;
+  part_range(nch, p.parts, part, c_begin, c_end);
+  const int nloc = c_end - c_begin;
+  const size_t nh = (size_t)n * H + h;
+
+  // ---- set-up ----
+  if (tid == 0) {
+    for (int b = 0; b < TB_COUNT; ++b) mbar_init(&bars[b], tx_bar_count(b));
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (tid < kTxChainThreads) {
+    // V of both stages for rows of the scaling matrix (the second 64-column
+    // block only when d_v = 64)
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    const int v0 = scale_rows ? 0 : dv * 8;
+    for (int i = tid; i < 2048; i += kTxChainThreads)
+      if ((i & 1023) >= v0)
+        *reinterpret_cast<uint4*>(sm + (i >> 10) * TX_STAGE + TX_V + (i & 1023) * 16) = z;
+  }
+  if (warp == kTxWarpMMA) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == kTxWarpProducer && lane == 0) {
+    prefetch_tmap(&tmq);
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+    prefetch_tmap(&tmo);
+    if (has_gate) prefetch_tmap(&tmg);
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto stage = [&](int i) { return base + (i & 1) * TX_STAGE; };
+  // set-up above overlaps the tail of the preceding kernel
+  griddep_wait();
+  const int cbase = nloc > 0 ? chunk_base(p, n, nch_dense) + c_begin : 0;
+
+  if (warp == kTxWarpProducer) {
+    // ================= TMA producer =================
+    // Q, K, V by tensor map; -W, P, T_U and the decay vectors are images in
+    // the workspace (bulk copies; the tile index is clamped because those
+    // copies have no bounds check). Chunk i + 2 is prefetched into L2 when
+    // chunk i is loaded.
+    if (lane == 0) {
+      const uint8_t* wimg = static_cast<const uint8_t*>(p.wneg);
+      const uint8_t* pimg = static_cast<const uint8_t*>(p.pm);
+      const uint8_t* uimg = static_cast<const uint8_t*>(p.tu);
+      auto prefetch = [&](int i) {
+        const int tok = (int)(bos + (long long)(c_begin + i) * C);
+        const size_t tz = (size_t)min((cbase + i) * H + h, tiles - 1);
+        prefetch_l2_3d(&tmk, 0, h, tok);
+        prefetch_l2_3d(&tmk, 64, h, tok);
+        if (emit) {
+          prefetch_l2_3d(&tmq, 0, h, tok);
+          prefetch_l2_3d(&tmq, 64, h, tok);
+        }
+        if (!scale_rows) prefetch_l2_3d(&tmv, 0, h, tok);
+        if (!scale_rows && dv > 64) prefetch_l2_3d(&tmv, 64, h, tok);
+        prefetch_l2(wimg + tz * WS_W_BYTES, WS_W_BYTES);
+        prefetch_l2(pimg + tz * WS_P_BYTES, WS_P_BYTES);
+        prefetch_l2(uimg + tz * WS_TU_BYTES, WS_TU_BYTES);
+        prefetch_l2(p.cv + tz * CV_FLOATS, CV_BYTES);
+      };
+      if (nloc > 0) prefetch(0);
+      if (nloc > 1) prefetch(1);
+      int issued = 0, part_groups = 0;  // chunks fully issued; groups of the next
+      for (int i = 0; i < nloc; ++i) {
+        const int s = i & 1;
+        const uint32_t ph = ((i >> 1) - 1) & 1;  // release of chunk i - 2
+        const int tok = (int)(bos + (long long)(c_begin + i) * C);
+        const size_t tz = (size_t)min((cbase + i) * H + h, tiles - 1);
+        uint8_t* st = sm + s * TX_STAGE;
+        if (i >= 2 && !mbar_wait(&bars[TB_EMPTYA0 + s], ph, abort_flag)) break;
+        uint64_t* fa = &bars[TB_FULLA0 + s];
+        mbar_arrive_expect_tx(fa, TX_A_BYTES - (scale_rows ? 16384u : 128u * (128 - dv)));
+        if (!scale_rows) tma_load_3d(st + TX_V, &tmv, fa, 0, h, tok);
+        if (!scale_rows && dv > 64) tma_load_3d(st + TX_V + 8192, &tmv, fa, 64, h, tok);
+        bulk_load(st + TX_TU, uimg + tz * WS_TU_BYTES, TILE_BYTES, fa);
+        if (i >= 2 && !mbar_wait(&bars[TB_EMPTYB0 + s], ph, abort_flag)) {
+          part_groups = 1;  // group A of chunk i is in flight
+          break;
+        }
+        uint64_t* fb = &bars[TB_FULLB0 + s];
+        mbar_arrive_expect_tx(fb, TX_B_BYTES);
+        bulk_load(st + TX_W, wimg + tz * WS_W_BYTES, TILE_BYTES, fb);
+        bulk_load(st + TX_W + TX_WQ_CB, wimg + tz * WS_W_BYTES + TILE_BYTES,
+                  TILE_BYTES, fb);
+        tma_load_3d(st + TX_Q, &tmq, fb, 0, h, tok);
+        tma_load_3d(st + TX_Q + TX_WQ_CB, &tmq, fb, 64, h, tok);
+        if (i >= 2 && !mbar_wait(&bars[TB_EMPTYC0 + s], ph, abort_flag)) {
+          part_groups = 2;  // groups A and B of chunk i are in flight
+          break;
+        }
+        uint64_t* fc = &bars[TB_FULLC0 + s];
+        mbar_arrive_expect_tx(fc, TX_C_BYTES);
+        tma_load_3d(st + TX_K, &tmk, fc, 0, h, tok);
+        tma_load_3d(st + TX_K + 8192, &tmk, fc, 64, h, tok);
+        bulk_load(st + TX_P, pimg + tz * WS_P_BYTES, TILE_BYTES, fc);
+        bulk_load(st + TX_CV, p.cv + tz * CV_FLOATS, CV_BYTES, fc);
+        if (i + 2 < nloc) prefetch(i + 2);
+        issued = i + 1;
+      }
+      // never leave with a copy still landing in shared memory: the groups
+      // of the last two chunks issued (a chunk cut short by an abort has
+      // only its first groups in flight)
+      const int full = issued;
+      for (int i = max(0, full - 2); i < full; ++i) {
+        wait_ignoring_abort(&bars[TB_FULLA0 + (i & 1)], (i >> 1) & 1);
+        wait_ignoring_abort(&bars[TB_FULLB0 + (i & 1)], (i >> 1) & 1);
+        wait_ignoring_abort(&bars[TB_FULLC0 + (i & 1)], (i >> 1) & 1);
+      }
+      if (part_groups >= 1)
+        wait_ignoring_abort(&bars[TB_FULLA0 + (full & 1)], (full >> 1) & 1);
+      if (part_groups >= 2)
+        wait_ignoring_abort(&bars[TB_FULLB0 + (full & 1)], (full >> 1) & 1);
+    }
+  } else if (warp == kTxWarpMMA) {
+    // ================= chain products =================
+    // [-W;Q] of chunk i once the state is in TMEM (and U0^T of chunk i has
+    // completed), Delta^T once U^T and K_d are; polled, so that each goes
+    // in the moment its barrier completes.
+    if (lane == 0 && nloc > 0) {
+      for (int i = 0; i < nloc; ++i) {
+        const int b = i & 1;
+        if (!mbar_spin(&bars[TB_SREADY], i & 1, abort_flag) ||
+            !mbar_spin(&bars[TB_FULLB0 + b], (i >> 1) & 1, abort_flag) ||
+            !mbar_spin(&bars[TB_U0DONE0 + b], (i >> 1) & 1, abort_flag))
+          break;
+        tc_fence_after();
+        const uint32_t st = stage(i);
+        const uint32_t d1 = tmem + TX_D1 + 128 * b;
+        // += S [-W; Q]^T, one 64-column block of d_k at a time
+        mma_bf16_ta_run<4>(d1, tmem + TX_SB, sdesc(st + TX_W, 16, 1024), 32,
+                           ID_TX_N128, true);
+        mma_bf16_ta_run<4>(d1, tmem + TX_SB + 32,
+                           sdesc(st + TX_W + TX_WQ_CB, 16, 1024), 32,
+                           ID_TX_N128, true);
+        mma_commit(&bars[TB_D1FULL0 + b]);
+        mma_commit(&bars[TB_EMPTYB0 + b]);
+        if (!mbar_spin(&bars[TB_UREADY], i & 1, abort_flag) ||
+            !mbar_spin(&bars[TB_FULLC0 + b], (i >> 1) & 1, abort_flag))
+          break;
+        tc_fence_after();
+        // Delta^T = U^T K_d
+        mma_bf16_ta_run<4>(tmem + TX_D2, tmem + TX_UB,
+                           sdesc(st + TX_K, 8192, 1024), 2048, ID_TX_D, false);
+        mma_commit(&bars[TB_D2FULL]);
+        mma_commit(&bars[TB_EMPTYC0 + b]);
+      }
+      mma_commit(&bars[TB_DRAIN]);
+      wait_ignoring_abort(&bars[TB_DRAIN], 0);
+    }
+  } else if (warp == kTxWarpSide) {
+    // ================= side products =================
+    // U0^T of chunk i + 1 into the other accumulator once chunk i's [-W;Q]
+    // product has completed (it then runs while U^T is converted) and the
+    // output warps have read chunk i - 1 out of it (and zeroed its H^T); U^T P^T of chunk i over
+    // the converted U^T once chunk i's Delta^T has completed (it runs during
+    // the state update). A commit covers only this thread's products, so
+    // the chain warps check P U (chunk i - 1) before they overwrite U^T.
+    if (lane == 0 && nloc > 0) {
+      auto u0 = [&](int j) {
+        const int s = j & 1;
+        if (!mbar_wait(&bars[TB_FULLA0 + s], (j >> 1) & 1, abort_flag))
+          return false;
+        // (the output warps free each accumulator once before chunk 0)
+        if (emit && !mbar_wait(&bars[TB_D1FREE0 + s], (j >> 1) & 1, abort_flag))
+          return false;
+        tc_fence_after();
+        const uint32_t st = stage(j);
+        mma_bf16_run<4>(tmem + TX_D1 + 128 * s, sdesc(st + TX_V, 8192, 1024),
+                        2048, sdesc(st + TX_TU, 16, 1024), 32, ID_TX_U0, false);
+        mma_commit(&bars[TB_U0DONE0 + s]);
+        mma_commit(&bars[TB_EMPTYA0 + s]);
+        return true;
+      };
+      bool ok = u0(0);
+      for (int i = 0; ok && i < nloc; ++i) {
+        const int b = i & 1;
+        if (i + 1 < nloc) {
+          ok = mbar_wait(&bars[TB_D1FULL0 + b], (i >> 1) & 1, abort_flag) &&
+               u0(i + 1);
+          if (!ok) break;
+        }
+        if (emit) {
+          if (!mbar_wait(&bars[TB_D2FULL], i & 1, abort_flag) ||
+              !mbar_wait(&bars[TB_FULLC0 + b], (i >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // U^T P^T over U^T
+          mma_bf16_ta_run<4>(tmem + TX_D1 + 128 * b, tmem + TX_UB,
+                             sdesc(stage(i) + TX_P, 16, 1024), 32, ID_TX_N64,
+                             false);
+          mma_commit(&bars[TB_OFULL0 + b]);
+        }
+        mma_commit(&bars[TB_EMPTYC0 + b]);
+      }
+      mma_commit(&bars[TB_DRAIN2]);
+      wait_ignoring_abort(&bars[TB_DRAIN2], 0);
+    }
+  } else if (warp < kTxChainThreads / 32) {
+    // ================= chain warps =================
+    // row r = 32 (warp & 3) + lane of S (TMEM lane r), d_k columns
+    // 64 ch .. 64 ch + 63 with ch = warp >> 2 (fp32, in registers)
+    const int ch = warp >> 2;
+    const int r = 32 * (warp & 3) + lane;
+    const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
+    float S[64];
+    // value rows r >= d_v (d_v = 64) stay zero: no input, no output
+    const bool live = scale_rows || r < dv;
+    if (scale_rows) {
+#pragma unroll
+      for (int c = 0; c < 64; ++c) S[c] = (r == 64 * ch + c) ? 1.f : 0.f;
+    } else if (split_tail || !live) {
+#pragma unroll
+      for (int c = 0; c < 64; ++c) S[c] = 0.f;
+    } else if (part > 0) {
+      const float4* src = reinterpret_cast<const float4*>(
+          p.ws_start + ((nh * p.parts + part) * dv + r) * DK + 64 * ch);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float4 v4 = src[c];
+        S[4 * c] = v4.x; S[4 * c + 1] = v4.y; S[4 * c + 2] = v4.z; S[4 * c + 3] = v4.w;
+      }
+    } else if (p.h0) {
+      const float* src = p.h0 + (nh * DK + 64 * ch) * dv + r;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) S[c] = src[(size_t)c * dv];
+    } else {
+#pragma unroll
+      for (int c = 0; c < 64; ++c) S[c] = 0.f;
+    }
+    // S as bf16 pairs: the A operand of the next [-W;Q_g] product
+    auto put_s = [&]() {
+      uint32_t w[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) w[c] = pack_bf16x2(S[2 * c], S[2 * c + 1]);
+      tmem_st32(tmem + TX_SB + lanes + 32 * ch, w);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[TB_SREADY]);
+    };
+    bool ok = true;
+    put_s();
+    for (int i = 0; ok && i < nloc; ++i) {
+      const int b = i & 1;
+      ok = __all_sync(0xffffffffu,
+                      ok && mbar_wait(&bars[TB_FULLC0 + b], (i >> 1) & 1, abort_flag));
+      if (!ok) break;
+      const float gam =
+          reinterpret_cast<const float*>(sm + b * TX_STAGE + TX_CV)[CV_GAMMA];
+      // K -> K_d in place while the [-W;Q] product runs (the stage is
+      // released only after the products that read K_d have completed)
+      tx_scale_rows(sm + b * TX_STAGE + TX_K, 8192,
+                    reinterpret_cast<const float*>(sm + b * TX_STAGE + TX_CV) + CV_DEC,
+                    tid);
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[TB_EMPTYC0 + b]);
+      // U^T (fp32, accumulator columns 32 ch ..: tokens) -> bf16 pairs, over
+      // chunk i - 1's, which P U has read
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&bars[TB_D1FULL0 + b], (i >> 1) & 1, abort_flag) &&
+                          (!emit || i == 0 ||
+                           mbar_wait(&bars[TB_OFULL0 + (b ^ 1)], ((i - 1) >> 1) & 1,
+                                     abort_flag)));
+      if (!ok) break;
+      tc_fence_after();
+      {
+        float u[32];
+        tmem_ldn<32>(tmem + TX_D1 + 128 * b + lanes + 32 * ch, u);
+        tmem_ld_wait();
+        uint32_t w[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) w[c] = pack_bf16x2(u[2 * c], u[2 * c + 1]);
+        tmem_st16(tmem + TX_UB + lanes + 16 * ch, w);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[TB_UREADY]);
+
+      // S <- gamma S + Delta^T
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars[TB_D2FULL], i & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      {
+        float d[32];
+        tmem_ldn<32>(tmem + TX_D2 + lanes + 64 * ch, d);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) S[c] = fmaf(gam, S[c], d[c]);
+        tmem_ldn<32>(tmem + TX_D2 + lanes + 64 * ch + 32, d);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) S[32 + c] = fmaf(gam, S[32 + c], d[c]);
+      }
+      put_s();
+    }
+    if (ok && live && !*abort_flag) {
+      if (p.mode == kModeSplit) {
+        float* dst = nullptr;
+        if (part == 0) {
+          if (p.parts > 1) dst = p.ws_start + ((nh * p.parts + 1) * dv + r) * DK;
+        } else {
+          dst = p.ws_end +
+                ((nh * p.parts + part) * (dv + DK) + (scale_rows ? dv : 0) + r) * DK;
+        }
+        if (dst) {
+          float4* d4 = reinterpret_cast<float4*>(dst + 64 * ch);
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            d4[c] = make_float4(S[4 * c], S[4 * c + 1], S[4 * c + 2], S[4 * c + 3]);
+        }
+      } else if (p.hT && part == p.parts - 1) {
+        float* dst = p.hT + (nh * DK + 64 * ch) * dv + r;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) dst[(size_t)c * dv] = S[c];
+      }
+    }
+  } else {
+    // ================= output =================
+    // Thread o of 128 (warp 8 + (warp & 3), TMEM lane quarter warp & 3) owns
+    // row r of O^T, i.e. output column r of the chunk's 64 tokens.
+    const int o = tid - kTxChainThreads;
+    const int r = 32 * (warp & 3) + lane;
+    const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
+    const float wr = (epi && p.norm_w && r < dv) ? p.norm_w[r] : 1.f;
+    float* red = reinterpret_cast<float*>(sm + TXO_RED);
+    float* rs = reinterpret_cast<float*>(sm + TXO_RS);
+    auto gate_load = [&](int j) {  // gate tile of chunk j into output tile j & 1
+      const int tok = (int)(bos + (long long)(c_begin + j) * C);
+      uint8_t* ob = sm + TXO_OUT + (j & 1) * 16384;
+      uint64_t* gb = &bars[TB_GATE0 + (j & 1)];
+      mbar_arrive_expect_tx(gb, 128u * dv);
+      tma_load_3d(ob, &tmg, gb, 0, h, tok);
+      if (dv > 64) tma_load_3d(ob + 8192, &tmg, gb, 64, h, tok);
+    };
+    bool ok = true;
+    if (emit) {
+      // H^T columns of both accumulators start at zero ([-W;Q] accumulates
+      // onto them); each is then free for its first U0^T
+      uint32_t z[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) z[c] = 0u;
+#pragma unroll
+      for (int bb = 0; bb < 2; ++bb) {
+        tmem_st32(tmem + TX_D1 + 128 * bb + 64 + lanes, z);
+        tmem_st32(tmem + TX_D1 + 128 * bb + 96 + lanes, z);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[TB_D1FREE0]);
+        mbar_arrive(&bars[TB_D1FREE1]);
+      }
+    }
+    if (has_gate && o == 0 && nloc > 0) gate_load(0);
+    for (int i = 0; ok && i < nloc; ++i) {
+      const int b = i & 1;
+      if (!emit) {
+        // nothing to read out: only release the chunk's last stage group
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&bars[TB_FULLC0 + b], (i >> 1) & 1, abort_flag));
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[TB_EMPTYC0 + b]);
+        continue;
+      }
+      const long long t0 = bos + (long long)(c_begin + i) * C;
+      const int len = (int)min((long long)C, eos - t0);
+      // (all output threads decide alike: they meet at named barriers)
+      ok = bar_and(5, kTxOutThreads,
+                   mbar_wait(&bars[TB_FULLC0 + b], (i >> 1) & 1, abort_flag) &&
+                       mbar_wait(&bars[TB_OFULL0 + b], (i >> 1) & 1, abort_flag));
+      if (!ok) break;
+      tc_fence_after();
+      // O^T = H^T diag(e^G) + U^T P^T, 32 tokens at a time
+      const float* eg =
+          reinterpret_cast<const float*>(sm + b * TX_STAGE + TX_CV) + CV_EG;
+      float y[64];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float hv[32];
+        tmem_ldn<32>(tmem + TX_D1 + 128 * b + 64 + 32 * hh + lanes, hv);
+        tmem_ldn<32>(tmem + TX_D1 + 128 * b + 32 * hh + lanes,
+                     *reinterpret_cast<float(*)[32]>(&y[32 * hh]));
+        tmem_ld_wait();
+#pragma unroll
+        for (int t4 = 0; t4 < 8; ++t4) {
+          const float4 e4 = reinterpret_cast<const float4*>(eg + 32 * hh)[t4];
+          float* yy = y + 32 * hh + 4 * t4;
+          yy[0] = fmaf(e4.x, hv[4 * t4], yy[0]);
+          yy[1] = fmaf(e4.y, hv[4 * t4 + 1], yy[1]);
+          yy[2] = fmaf(e4.z, hv[4 * t4 + 2], yy[2]);
+          yy[3] = fmaf(e4.w, hv[4 * t4 + 3], yy[3]);
+        }
+      }
+      {
+        // H^T back to zero for the accumulator's next chunk
+        uint32_t z[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) z[c] = 0u;
+        tmem_st32(tmem + TX_D1 + 128 * b + 64 + lanes, z);
+        tmem_st32(tmem + TX_D1 + 128 * b + 96 + lanes, z);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[TB_D1FREE0 + b]);
+        mbar_arrive(&bars[TB_EMPTYC0 + b]);  // e^G has been read
+      }
+      if (epi && p.norm_w) {
+        // sum over the 128 rows of O^T (a token's d_v values) of y^2: a
+        // transposing butterfly leaves lane l the warp's sums of tokens
+        // tb(l) and tb(l) + 1, then the four warps add up in shared memory
+        float x[64];
+#pragma unroll
+        for (int t = 0; t < 64; ++t) x[t] = y[t] * y[t];
+#pragma unroll
+        for (int w = 32, m = 16; m >= 1; w >>= 1, m >>= 1) {
+          const bool up = (lane & m) != 0;
+#pragma unroll
+          for (int j = 0; j < w; ++j) {
+            const float give = up ? x[j] : x[j + w];
+            const float keep = up ? x[j + w] : x[j];
+            x[j] = keep + __shfl_xor_sync(0xffffffffu, give, m);
+          }
+        }
+        const int tb = ((lane & 16) ? 32 : 0) + ((lane & 8) ? 16 : 0) +
+                       ((lane & 4) ? 8 : 0) + ((lane & 2) ? 4 : 0) +
+                       ((lane & 1) ? 2 : 0);
+        red[(warp & 3) * 64 + tb] = x[0];
+        red[(warp & 3) * 64 + tb + 1] = x[1];
+        named_bar(5, kTxOutThreads);
+        if (o < 64)
+          rs[o] = rsqrtf((red[o] + red[64 + o] + red[128 + o] + red[192 + o]) *
+                             (1.f / (float)dv) + p.eps);
+        named_bar(5, kTxOutThreads);
+#pragma unroll
+        for (int t = 0; t < 64; ++t) y[t] *= rs[t] * wr;
+      }
+      uint8_t* ob = sm + TXO_OUT + b * 16384;
+      if (has_gate) {
+        ok = bar_and(5, kTxOutThreads,
+                     mbar_wait(&bars[TB_GATE0 + b], (i >> 1) & 1, abort_flag));
+        if (!ok) break;
+#pragma unroll
+        for (int t = 0; t < 64; ++t)
+          y[t] *= sigmoid_approx(__bfloat162float(
+              *reinterpret_cast<const __nv_bfloat16*>(ob + tx_tile_off(t, r))));
+      }
+      // (the tile's previous store, chunk i - 2, was read out before the
+      // barrier at the top of this iteration)
+      if (len == C) {
+        // through the tile (column r of its rows) and one TMA store
+#pragma unroll
+        for (int t = 0; t < 64; ++t)
+          *reinterpret_cast<__nv_bfloat16*>(ob + tx_tile_off(t, r)) =
+              __float2bfloat16_rn(y[t]);
+        fence_proxy_async();
+        named_bar(5, kTxOutThreads);
+        if (o == 0) {
+          tma_store_3d(&tmo, ob, 0, h, (int)t0);
+          if (dv > 64) tma_store_3d(&tmo, ob + 8192, 64, h, (int)t0);
+          bulk_commit();
+        }
+      } else if (r < dv) {
+        // a partial chunk (the end of a sequence): directly, column r
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
+                             ((size_t)t0 * H + h) * dv + r;
+#pragma unroll
+        for (int t = 0; t < 64; ++t)
+          if (t < len) dst[(size_t)t * H * dv] = __float2bfloat16_rn(y[t]);
+      }
+      // the other tile's store (chunk i - 1) read out before the next
+      // iteration writes into it; then the gate of chunk i + 1 into it
+      if (o == 0) bulk_wait_read_1();
+      if (has_gate && o == 0 && i + 1 < nloc) gate_load(i + 1);
+    }
+    if (o == 0) bulk_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kTxWarpMMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+  if (tid == 0 && *abort_flag) record_status(p.status, GDN_ERR_TIMEOUT);
+}
+
+
+// ---------------------------------------------------------------------------
 // Self-test: D = A * B (x2 when twice) with the layouts above, one CTA.
 // N = 64 or 128 (an N-major B of 128 columns is two 64-column blocks).
 // a_mn: 0 A K-major in shared memory, 1 M-major, 2 A in TMEM (bf16 pairs in
@@ -1632,10 +2280,35 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream) {
       !make_map(&mo, p.out, p.dv, p.H, tokens, 1, 64) ||
       !make_map(&mg, p.gate_z ? p.gate_z : p.out, p.dv, p.H, tokens, 1, 64))
     return cudaErrorInvalidValue;
+  const int nchd = chunk_tc_nch_dense(p);
+  if (p.chain_rows == TXR) {
+    // one CTA per 128 state rows: the value rows, and in a split pass the
+    // rows of the scaling matrix
+    cudaError_t e = cudaFuncSetAttribute(
+        chain_tx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (int)TX_SMEM);
+    if (e != cudaSuccess) return e;
+    const int blocks = p.mode == kModeSplit ? 2 : 1;
+    const int t = timing_start(GDN_KERNEL_CHUNK_CHAIN_WHOLE, stream);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(blocks, p.H, p.N * p.part_count);
+    cfg.blockDim = dim3(kTxThreads);
+    cfg.dynamicSmemBytes = TX_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, chain_tx_kernel, p, mq, mk, mv, mo, mg, nchd,
+                           (int)tiles);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    timing_stop(t, stream, e);
+    return e;
+  }
   // the fused epilogue pairs the two CTAs of each (sequence, head, part)
   // when d_v = 128 (grid.x is then 2 or 4)
   const bool clustered = p.epilogue && p.dv == 128;
-  const int nchd = chunk_tc_nch_dense(p);
   auto launch = [&](auto kern) {
     cudaError_t e = cudaFuncSetAttribute(
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);

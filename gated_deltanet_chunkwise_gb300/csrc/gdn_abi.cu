@@ -56,7 +56,7 @@ int check_chunk_args(const void* q, const void* k, const void* v,
     return GDN_ERR_INVALID_ARG;
   if (variant != GDN_GATE_BEFORE_PREDICT && variant != GDN_GATE_AFTER_PREDICT)
     return GDN_ERR_INVALID_ARG;
-  if (path < GDN_PATH_AUTO || path > GDN_PATH_TCGEN05)
+  if (path < GDN_PATH_AUTO || path > GDN_PATH_TCGEN05_WHOLE)
     return GDN_ERR_INVALID_ARG;
   if (sp_parts < 0 || sp_parts > 4096) return GDN_ERR_INVALID_ARG;
   if (cu_seqlens && B == 0) return GDN_ERR_INVALID_ARG;
@@ -66,7 +66,7 @@ int check_chunk_args(const void* q, const void* k, const void* v,
   }
   if (!head_dim_ok(dk) || !head_dim_ok(dv) || C != 64)
     return GDN_ERR_UNSUPPORTED;
-  if (path == GDN_PATH_TCGEN05 && dtype != GDN_DTYPE_BF16)
+  if (path >= GDN_PATH_TCGEN05 && dtype != GDN_DTYPE_BF16)
     return GDN_ERR_UNSUPPORTED;
   // Size limits: token-head rows index with 64-bit math, but grid.z holds
   // sequences x parts and the tensor maps hold 32-bit extents.
@@ -103,25 +103,26 @@ int choose_parts(int requested, int N, int H, int T, int dv, int C,
   return parts < 1 ? 1 : parts;
 }
 
-// Sequence-parallel split for the tensor-core path: one CTA per SM, so a
-// pass costs (waves of resident CTAs) x (chunks per sub-sequence); pick the
-// split count P that minimises split pass + corrected output pass.
-int choose_parts_tc(int requested, int N, int H, int T, int dv, int C,
-                    bool packed) {
-  if (requested > 0) return requested;
-  if (packed) return 1;
-  int sms = 148, dev = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess) {
-    int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
-            cudaSuccess && v > 0)
-      sms = v;
-  }
+// Chain kernel and sequence-parallel split for the tensor-core path. One
+// chain CTA per SM, so a pass costs (waves of resident CTAs) x (chunks per
+// sub-sequence); `rows` state rows per CTA (64: the split chain kernel, 128:
+// the whole-state one), so a (sequence, head) takes ceil(dv / rows) CTAs and
+// a split pass ceil(dk / rows) more for the scaling matrix. Picks the split
+// count P that minimises split pass + corrected output pass and returns
+// that cost.
+long long parts_cost_tc(int requested, int N, int H, int T, int dv, int C,
+                        bool packed, int rows, int sms, int* parts_out) {
   const long long nch = (T + C - 1) / C;
-  const long long nh = (long long)N * H, tv = dv / 64, tk = 2;
+  const long long nh = (long long)N * H, tv = (dv + rows - 1) / rows,
+                  tk = (128 + rows - 1) / rows;
   auto waves = [&](long long ctas) { return (ctas + sms - 1) / sms; };
-  long long best = waves(nh * tv) * nch;
+  // packed calls: one pass over the longest possible sequence
+  long long best = waves(nh * tv) * (packed ? (long long)T / C + 1 : nch);
   int best_p = 1;
+  if (requested > 0 || packed) {
+    *parts_out = requested > 0 ? requested : 1;
+    return best;
+  }
   for (int P = 2; P <= 64 && P <= nch; ++P) {
     const long long per = (nch + P - 1) / P;
     const long long split = nh * (tv + (long long)(P - 2) * (tv + tk));
@@ -132,7 +133,30 @@ int choose_parts_tc(int requested, int N, int H, int T, int dv, int C,
       best_p = P;
     }
   }
-  return best_p;
+  *parts_out = best_p;
+  return best;
+}
+
+// rows per chain CTA and the split for the tensor-core path (`path` may fix
+// the chain kernel)
+void choose_chain_tc(int path, int requested, int N, int H, int T, int dv,
+                     int C, bool packed, int* rows, int* parts) {
+  int sms = 148, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
+            cudaSuccess && v > 0)
+      sms = v;
+  }
+  int p64 = 1, p128 = 1;
+  const long long c64 = parts_cost_tc(requested, N, H, T, dv, C, packed, 64,
+                                      sms, &p64);
+  const long long c128 = parts_cost_tc(requested, N, H, T, dv, C, packed, 128,
+                                       sms, &p128);
+  const bool whole = path == GDN_PATH_TCGEN05_WHOLE ||
+                     (path != GDN_PATH_TCGEN05_SPLIT && c128 < c64);
+  *rows = whole ? 128 : 64;
+  *parts = whole ? p128 : p64;
 }
 
 // The steps either side of the recurrence (gdn_chunk_fwd_fused).
@@ -174,7 +198,7 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
   const bool bf16 = dtype == GDN_DTYPE_BF16;
   const long long tokens = cu_seqlens ? (long long)T : (long long)B * T;
   const bool tc_ok = bf16 && chunk_tc_supported(dk, dv, tokens, B, H);
-  if ((path == GDN_PATH_TCGEN05 || sub.on) && !tc_ok) return GDN_ERR_UNSUPPORTED;
+  if ((path >= GDN_PATH_TCGEN05 || sub.on) && !tc_ok) return GDN_ERR_UNSUPPORTED;
   const bool use_tc = tc_ok && path != GDN_PATH_SIMT;
   if (sub.on) {
     p.prologue = 1;
@@ -187,9 +211,12 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
     return use_tc ? launch_chunk_tc(q, stream)
                   : launch_chunk_simt(q, bf16, stream);
   };
-  const int parts =
-      use_tc ? choose_parts_tc(sp_parts, B, H, T, dv, C, cu_seqlens != nullptr)
-             : choose_parts(sp_parts, B, H, T, dv, C, cu_seqlens != nullptr);
+  int parts = 1;
+  if (use_tc)
+    choose_chain_tc(path, sp_parts, B, H, T, dv, C, cu_seqlens != nullptr,
+                    &p.chain_rows, &parts);
+  else
+    parts = choose_parts(sp_parts, B, H, T, dv, C, cu_seqlens != nullptr);
   p.parts = parts;
 
   // Workspace: UT factors (tensor-core path) and sequence-parallel states.
@@ -356,8 +383,11 @@ int gdn_chunk_fwd_fused(const void* q, const void* k, const void* v,
                         const float* a, const float* b, const float* h0,
                         void* out, float* hT, const int32_t* cu_seqlens,
                         const float* norm_weight, const void* gate, float eps,
-                        int B, int H, int T, int dk, int dv, int C,
+                        int B, int H, int T, int dk, int dv, int C, int path,
                         gdn_stream_t stream) {
+  if (path < GDN_PATH_AUTO || path > GDN_PATH_TCGEN05_WHOLE)
+    return GDN_ERR_INVALID_ARG;
+  if (path == GDN_PATH_SIMT) return GDN_ERR_UNSUPPORTED;
   gdn::Sublayer sub;
   sub.on = true;
   sub.norm_w = norm_weight;
@@ -365,7 +395,8 @@ int gdn_chunk_fwd_fused(const void* q, const void* k, const void* v,
   sub.eps = eps;
   return gdn::run_chunk(q, k, v, a, b, h0, out, hT, cu_seqlens, B, H, T, dk,
                         dv, C, GDN_DTYPE_BF16, GDN_GATE_BEFORE_PREDICT,
-                        GDN_PATH_TCGEN05, 0, stream, sub);
+                        path == GDN_PATH_AUTO ? GDN_PATH_TCGEN05 : path, 0,
+                        stream, sub);
 }
 
 int gdn_recurrent_step(const void* q, const void* k, const void* v,

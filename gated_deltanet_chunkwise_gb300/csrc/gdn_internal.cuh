@@ -59,6 +59,7 @@ struct ChunkParams {
   // logits b (beta = sigmoid(b)); with `epilogue` set, each output row is
   // RMS-normalised over d_v (times norm_w when given) and gated by
   // sigmoid(gate_z) when given
+  int chain_rows;  // state rows per chain CTA: 64 (chunk_tc_kernel) or 128
   int prologue;
   int epilogue;
   const float* norm_w;       // [dv] fp32 or null

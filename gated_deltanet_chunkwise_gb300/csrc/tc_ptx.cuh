@@ -93,6 +93,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// As mbar_wait, polling with the non-blocking test instead of a suspending
+// try_wait: for a single thread on the critical path that must react to the
+// phase at once.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity,
+                                          volatile int* abort_flag) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test(bar, parity)) return true;
+    if ((it & 255) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // ---- fast activation ----------------------------------------------------------
 // sigmoid(z) = (1 + tanh(z / 2)) / 2 with the hardware tanh approximation
 // (one instruction; about 2^-11 relative error, below bf16 rounding).
@@ -242,6 +261,10 @@ __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 // This thread's bulk stores have finished reading shared memory.
+// Wait until at most the most recent bulk group is still reading its source.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }

@@ -74,6 +74,12 @@ typedef enum {
 #define GDN_PATH_AUTO 0
 #define GDN_PATH_SIMT 1   /* fp32 CUDA-core arithmetic; any supported shape */
 #define GDN_PATH_TCGEN05 2 /* bf16 tcgen05/TMEM tensor-core path */
+/* The tensor-core path with its chain kernel fixed (GDN_PATH_TCGEN05 picks
+ * the one that needs fewer waves of CTAs, the split one on a tie): */
+#define GDN_PATH_TCGEN05_SPLIT 3 /* 64 state rows per CTA (two CTAs per
+                                    (sequence, head) when dv = 128) */
+#define GDN_PATH_TCGEN05_WHOLE 4 /* 128 state rows per CTA, state in TMEM
+                                    lanes (zero-padded when dv = 64) */
 
 /*
  * gdn_chunk_fwd -- chunkwise forward pass, bf16 q/k/v/out.
@@ -116,7 +122,7 @@ int gdn_chunk_fwd_f32(const float* q, const float* k, const float* v,
  * gdn_chunk_fwd_ex -- gdn_chunk_fwd with explicit options.
  *   dtype      GDN_DTYPE_BF16 or GDN_DTYPE_F32 (q, k, v, out)
  *   variant    GDN_GATE_BEFORE_PREDICT or GDN_GATE_AFTER_PREDICT
- *   path       GDN_PATH_* (GDN_PATH_TCGEN05 requires bf16)
+ *   path       GDN_PATH_* (the GDN_PATH_TCGEN05* paths require bf16)
  *   sp_parts   sequence-parallel split: 0 = automatic, 1 = never split,
  *              P >= 2 = split every sequence into P sub-sequences of whole
  *              chunks (incremental state from zero + scaling matrix, then the
@@ -145,16 +151,19 @@ int gdn_chunk_fwd_ex(const void* q, const void* k, const void* v,
  *   norm_weight fp32 [dv] (device) or NULL: no output normalisation
  *   gate        bf16 [B, T, H, dv] (device) or NULL: no output gate
  *   eps         >= 0, added to the mean of squares
+ *   path        GDN_PATH_AUTO or GDN_PATH_TCGEN05 (the same here),
+ *               GDN_PATH_TCGEN05_SPLIT or GDN_PATH_TCGEN05_WHOLE
  * Other arguments as gdn_chunk_fwd (decay before the prediction, automatic
  * sequence-parallel split). Served by the bf16 tensor-core path only:
- * dk = 128 and dv in {64, 128}; other shapes return GDN_ERR_UNSUPPORTED.
- * The pages print no interface; this one is the library's.
+ * dk = 128 and dv in {64, 128}; other shapes (and GDN_PATH_SIMT) return
+ * GDN_ERR_UNSUPPORTED. The pages print no interface; this one is the
+ * library's.
  */
 int gdn_chunk_fwd_fused(const void* q, const void* k, const void* v,
                         const float* a, const float* b, const float* h0,
                         void* out, float* hT, const int32_t* cu_seqlens,
                         const float* norm_weight, const void* gate, float eps,
-                        int B, int H, int T, int dk, int dv, int C,
+                        int B, int H, int T, int dk, int dv, int C, int path,
                         gdn_stream_t stream);
 
 /*
@@ -232,12 +241,13 @@ typedef enum {
   GDN_KERNEL_CHUNK_PREP = 0,    /* tensor-core path: state-independent part
                                    of every (chunk, head) */
   GDN_KERNEL_CHUNK_CHAIN = 1,   /* tensor-core path: chunk-to-chunk state
-                                   chain and outputs */
+                                   chain and outputs, 64 rows per CTA */
   GDN_KERNEL_CHUNK_SIMT = 2,    /* fp32-arithmetic chunk kernel */
   GDN_KERNEL_SP_CHAIN = 3,      /* sequence-parallel start-state chain */
   GDN_KERNEL_DECODE = 4,        /* single-token recurrent step */
   GDN_KERNEL_CHUNK_OFFSETS = 5, /* chunk offsets of packed sequences */
-  GDN_KERNEL_COUNT = 6
+  GDN_KERNEL_CHUNK_CHAIN_WHOLE = 6, /* the same chain, 128 rows per CTA */
+  GDN_KERNEL_COUNT = 7
 } gdn_kernel_t;
 
 /* gdn_timing_enable -- per-kernel device timing on (nonzero) or off (0).

@@ -91,6 +91,9 @@ def chunk(so, q=A, k=A + 0x1000, v=A + 0x2000, g=A + 0x3000, beta=A + 0x4000,
     (dict(dtype=5), INVALID),
     (dict(sp_parts=-1), INVALID),
     (dict(dtype=1, path=2), UNSUPPORTED),  # tensor-core path is bf16 only
+    (dict(dtype=1, path=3), UNSUPPORTED),
+    (dict(dtype=1, path=4), UNSUPPORTED),
+    (dict(path=5), INVALID),
 ])
 def test_chunk_fwd_rejects_on_host(lib, kw, expect):
     assert chunk(lib.library(), **kw) == expect
@@ -150,10 +153,11 @@ def test_timing_switch_and_read_on_host(lib):
 
 def fused(so, q=A, k=A + 0x1000, v=A + 0x2000, a=A + 0x3000, b=A + 0x4000,
           h0=None, out=A + 0x5000, hT=None, cu=None, w=A + 0x7000,
-          gate=A + 0x8000, eps=1e-6, B=1, H=1, T=64, dk=128, dv=128, C=64):
+          gate=A + 0x8000, eps=1e-6, B=1, H=1, T=64, dk=128, dv=128, C=64,
+          path=0):
     return so.gdn_chunk_fwd_fused(q, k, v, a, b, h0, out, hT, cu, w, gate,
                                   ctypes.c_float(eps), B, H, T, dk, dv, C,
-                                  None)
+                                  path, None)
 
 
 @pytest.mark.parametrize("kw,expect", [
@@ -166,6 +170,9 @@ def fused(so, q=A, k=A + 0x1000, v=A + 0x2000, a=A + 0x3000, b=A + 0x4000,
     (dict(gate=ODD), MISALIGNED),
     (dict(gate=A + 0x5000), INVALID),    # gate aliases out
     (dict(C=32), UNSUPPORTED),
+    (dict(path=1), UNSUPPORTED),         # no fp32 CUDA-core fused path
+    (dict(path=5), INVALID),
+    (dict(path=-1), INVALID),
 ])
 def test_fused_rejects_on_host(lib, kw, expect):
     assert fused(lib.library(), **kw) == expect

@@ -14,6 +14,10 @@ from gated_deltanet_chunkwise_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
+# both chain kernels of the tensor-core path: 64 state rows per CTA (two
+# CTAs per head when dv = 128, a cluster pair for the fused epilogue) and
+# 128 rows per CTA (the whole state in TMEM lanes)
+CHAINS = [3, 4]
 
 
 def rel_err(x, ref):
@@ -21,20 +25,20 @@ def rel_err(x, ref):
     return float(np.max(np.abs(x - ref)) / max(np.max(np.abs(ref)), 1e-30))
 
 
-def run(lib, dev, d, eps=1e-6):
+def run(lib, dev, d, eps=1e-6, path=0):
     g = lambda t: None if t is None else t.to(dev)
     out = torch.full(d["v"].shape, float("nan"), dtype=torch.bfloat16, device=dev)
     o, hT = lib.gdn_chunk_fwd_fused(
         g(d["q"]), g(d["k"]), g(d["v"]), g(d["a"]), g(d["b"]), g(d["h0"]),
         g(d["cu_seqlens"]), norm_weight=g(d["norm_weight"]), gate=g(d["gate"]),
-        eps=eps, out=out)
+        eps=eps, out=out, path=path)
     torch.cuda.synchronize(dev)
     assert lib.gdn_device_status() == 0
     return o, hT
 
 
-def check(lib, dev, d, eps=1e-6):
-    o, hT = run(lib, dev, d, eps)
+def check(lib, dev, d, eps=1e-6, path=0):
+    o, hT = run(lib, dev, d, eps, path)
     o_ref, h_ref = sublayer.fused_forward(
         d["q"], d["k"], d["v"], d["a"], d["b"], d["h0"],
         cu_seqlens=d["cu_seqlens"], weight=d["norm_weight"], gate=d["gate"],
@@ -43,31 +47,35 @@ def check(lib, dev, d, eps=1e-6):
     assert rel_err(hT, h_ref) <= TOL, rel_err(hT, h_ref)
 
 
+@pytest.mark.parametrize("path", CHAINS)
 @pytest.mark.parametrize("dv", [64, 128])
 @pytest.mark.parametrize("weight,gate", [(True, True), (True, False),
                                          (False, True), (False, False)])
-def test_fused_matches_oracle(lib, cuda_device, dv, weight, gate):
+def test_fused_matches_oracle(lib, cuda_device, dv, weight, gate, path):
     d = inputs.fused_inputs(2, 3, 200, 128, dv, seed=11, h0=True,
                             weight=weight, gate=gate)
-    check(lib, cuda_device, d)
+    check(lib, cuda_device, d, path=path)
 
 
+@pytest.mark.parametrize("path", CHAINS)
 @pytest.mark.parametrize("T", [1, 63, 65, 130])
-def test_fused_short_and_ragged(lib, cuda_device, T):
+def test_fused_short_and_ragged(lib, cuda_device, T, path):
     d = inputs.fused_inputs(1, 2, T, 128, 128, seed=12)
-    check(lib, cuda_device, d)
+    check(lib, cuda_device, d, path=path)
 
 
-def test_fused_packed(lib, cuda_device):
+@pytest.mark.parametrize("path", CHAINS)
+def test_fused_packed(lib, cuda_device, path):
     d = inputs.fused_inputs(0, 4, 0, 128, 128, seed=13, h0=True,
                             lengths=[70, 1, 0, 300, 64, 129])
-    check(lib, cuda_device, d)
+    check(lib, cuda_device, d, path=path)
 
 
-def test_fused_long_sequence_split(lib, cuda_device):
+@pytest.mark.parametrize("path", [0] + CHAINS)
+def test_fused_long_sequence_split(lib, cuda_device, path):
     # long enough for the automatic sequence-parallel split
     d = inputs.fused_inputs(1, 2, 6000, 128, 128, seed=14, h0=True)
-    check(lib, cuda_device, d)
+    check(lib, cuda_device, d, path=path)
 
 
 def test_fused_unit_inputs_reduce_to_the_plain_path(lib, cuda_device):

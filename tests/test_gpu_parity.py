@@ -186,43 +186,51 @@ def test_recurrent_step_matches_chunk_path_single_token(lib, cuda_device):
 
 # ---- tensor-core (tcgen05) path, forced ----
 TC = 2
+# its two chain kernels, forced: 64 state rows per CTA, 128 rows per CTA
+CHAINS = [3, 4]
 
 
+@pytest.mark.parametrize("path", [TC] + CHAINS)
 @pytest.mark.parametrize("dv", [64, 128])
 @pytest.mark.parametrize("variant", [0, 1])
-def test_tensor_core_path(lib, cuda_device, dv, variant):
+def test_tensor_core_path(lib, cuda_device, dv, variant, path):
     d = inputs.chunk_inputs(2, 3, 64 * 4 + 29, 128, dv, dtype="bf16", seed=12,
                             h0=True)
-    check(lib, cuda_device, d, "bf16", variant=variant, path=TC)
+    check(lib, cuda_device, d, "bf16", variant=variant, path=path)
 
 
-def test_tensor_core_alpha_one_single_chunk(lib, cuda_device):
+@pytest.mark.parametrize("path", CHAINS)
+def test_tensor_core_alpha_one_single_chunk(lib, cuda_device, path):
     d = inputs.chunk_inputs(1, 2, 64, 128, 128, dtype="bf16", seed=13,
                             gated=False)
-    check(lib, cuda_device, d, "bf16", path=TC)
+    check(lib, cuda_device, d, "bf16", path=path)
 
 
+@pytest.mark.parametrize("path", CHAINS)
 @pytest.mark.parametrize("T", [1, 17, 63, 65, 128])
-def test_tensor_core_short_lengths(lib, cuda_device, T):
+def test_tensor_core_short_lengths(lib, cuda_device, T, path):
     d = inputs.chunk_inputs(2, 2, T, 128, 128, dtype="bf16", seed=14, h0=True)
-    check(lib, cuda_device, d, "bf16", path=TC)
+    check(lib, cuda_device, d, "bf16", path=path)
 
 
+@pytest.mark.parametrize("path", CHAINS)
+@pytest.mark.parametrize("dv", [64, 128])
 @pytest.mark.parametrize("parts", [2, 3, 5])
-def test_tensor_core_sequence_parallel(lib, cuda_device, parts):
-    d = inputs.chunk_inputs(1, 2, 64 * 9 + 40, 128, 128, dtype="bf16", seed=15,
+def test_tensor_core_sequence_parallel(lib, cuda_device, parts, dv, path):
+    d = inputs.chunk_inputs(1, 2, 64 * 9 + 40, 128, dv, dtype="bf16", seed=15,
                             h0=True)
-    check(lib, cuda_device, d, "bf16", path=TC, sp_parts=parts)
+    check(lib, cuda_device, d, "bf16", path=path, sp_parts=parts)
 
 
-def test_tensor_core_packed(lib, cuda_device):
+@pytest.mark.parametrize("path", CHAINS)
+def test_tensor_core_packed(lib, cuda_device, path):
     lengths = [70, 0, 1, 64, 200, 3, 129]
     d = inputs.chunk_inputs(len(lengths), 2, 0, 128, 128, dtype="bf16",
                             seed=16, h0=True, lengths=lengths)
-    check(lib, cuda_device, d, "bf16", path=TC)
+    check(lib, cuda_device, d, "bf16", path=path)
 
 
-@pytest.mark.parametrize("path", [1, TC])
+@pytest.mark.parametrize("path", [1] + CHAINS)
 def test_strong_gates_chunk_decay_beyond_fp32_range(lib, cuda_device, path):
     """Log-gates ~6x stronger than the workload's, so a chunk's total decay
     exceeds e^-87: the tensor-core kernel must switch from factored decays
@@ -239,7 +247,8 @@ def test_mixed_gate_strength_across_chunks(lib, cuda_device):
                             h0=True)
     d["g"][:, 64:128] *= 8.0
     d["g"][:, 192:] *= 5.0
-    check(lib, cuda_device, d, "bf16", path=TC)
+    for path in CHAINS:
+        check(lib, cuda_device, d, "bf16", path=path)
 
 
 @pytest.mark.gpu
@@ -248,12 +257,14 @@ def test_kernel_timing_counts_the_launches(lib, cuda_device):
     d = inputs.chunk_inputs(2, 4, 200, 128, 128, dtype="bf16", seed=5)
     lib.gdn_timing_enable(True)
     try:
-        run_gpu(lib, d, cuda_device, "bf16", path=2, sp_parts=1)
+        run_gpu(lib, d, cuda_device, "bf16", path=3, sp_parts=1)
+        run_gpu(lib, d, cuda_device, "bf16", path=4, sp_parts=1)
         run_gpu(lib, d, cuda_device, "bf16", path=1, sp_parts=1)
         t = lib.kernel_timings()
     finally:
         lib.gdn_timing_enable(False)
-    assert t["ut_prep_kernel"][0] == 1
+    assert t["ut_prep_kernel"][0] == 2
     assert t["chunk_tc_kernel"][0] == 1
+    assert t["chain_tx_kernel"][0] == 1
     assert t["chunk_simt_kernel"][0] == 1
     assert all(ms > 0 for _, ms in t.values())
