@@ -90,7 +90,9 @@ WORKLOADS = {
 # hash of the kernel source it was taken on; a changed kernel reports null.
 MEASURED_TRAFFIC = {
     # chunk_tc_kernel, W1, one launch (ncu --set full, caches flushed)
-    "w1:63877aff79eb014b": 168908032 + 23252992,
+    "w1:582e4a3241d2a6be": 168930560 + 20267008,
+    # chain_tx_kernel, W3 (packed, 512 sequence-heads), one launch
+    "w3:582e4a3241d2a6be": 2999533312 + 598896640,
     # decode_kernel captured with --sequences 128 and scaled x4 to N=512:
     # its traffic is proportional to the sequences processed
     "w4:83c7aa23b4500b6b": 4 * (271642880 + 210279936),
