@@ -246,42 +246,105 @@ __global__ void __launch_bounds__(kThreads)
 // Serial correction chain over sub-sequences (the CP=4 chain of the sequence
 // parallelism note): S_start(p + 1) = dS_end(p) + S_start(p) M_end(p) for
 // p = 1 .. parts - 2; S_start(1) was written by part 0 of the split pass.
+// One CTA per (sequence, head, kSpRows state rows); M_end(p) (dk x dk) is staged
+// in shared memory by asynchronous copies, the next part's while this one is
+// multiplied, and each thread forms a RPT x 4 block of the product in fp32
+// registers (rows from a broadcast, four columns per 16-byte load).
+constexpr int kSpRows = 16;
+template <int DK>
+struct SpChainSmem {
+  static constexpr int kS = kSpRows * (DK + 4);  // start rows, padded
+  static constexpr size_t kBytes = (size_t)(kS + 2 * DK * DK) * sizeof(float);
+};
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(smem)),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 template <int DK>
 __global__ void __launch_bounds__(kThreads) sp_chain_kernel(const ChunkParams p) {
-  __shared__ float sS[kDVT][DK + 1];
+  constexpr int CG = DK / 4;             // column groups of four
+  constexpr int RG = kThreads / CG;      // row groups
+  constexpr int RPT = kSpRows / RG;         // rows per thread
+  static_assert(RG * RPT == kSpRows && CG * RG == kThreads, "sp chain tiling");
+  constexpr int SP = DK + 4;             // padded pitch of the start rows
+  extern __shared__ float sp_smem[];
+  float* sS = sp_smem;                   // [kSpRows][SP]
+  float* sM0 = sp_smem + SpChainSmem<DK>::kS;  // [2][DK][DK]
   const int tid = threadIdx.x;
+  const int cg = tid % CG, rg = tid / CG;
   const int h = blockIdx.y, n = blockIdx.z;
-  const int row0 = blockIdx.x * kDVT;
+  const int row0 = blockIdx.x * kSpRows;
   const int dv = p.dv;
   const size_t nh = (size_t)n * p.H + h;
   if (p.cu_seqlens) {
     long long bos, eos;
     if (!sequence_range(p, n, bos, eos)) return;
   }
-  for (int idx = tid; idx < kDVT * DK; idx += kThreads) {
-    const int c = idx / DK, i = idx % DK;
-    sS[c][i] = p.ws_start[((nh * p.parts + 1) * dv + row0 + c) * DK + i];
+  for (int idx = tid; idx < kSpRows * DK / 4; idx += kThreads) {
+    const int c = idx / (DK / 4), i4 = idx % (DK / 4);
+    *reinterpret_cast<float4*>(sS + c * SP + 4 * i4) =
+        reinterpret_cast<const float4*>(
+            p.ws_start + ((nh * p.parts + 1) * dv + row0 + c) * DK)[i4];
   }
+  auto stage_m = [&](int part) {
+    const float4* M4 = reinterpret_cast<const float4*>(
+        p.ws_end + (nh * p.parts + part) * (size_t)(dv + DK) * DK + (size_t)dv * DK);
+    float4* dst = reinterpret_cast<float4*>(sM0 + (part & 1) * DK * DK);
+    for (int idx = tid; idx < DK * DK / 4; idx += kThreads)
+      cp_async16(dst + idx, M4 + idx);
+    cp_async_commit();
+  };
+  if (p.parts > 2) stage_m(1);
   for (int part = 1; part + 1 < p.parts; ++part) {
-    __syncthreads();
     const float* end = p.ws_end + (nh * p.parts + part) * (size_t)(dv + DK) * DK;
-    const float* M = end + (size_t)dv * DK;
-    float acc[kDVT * DK / kThreads];
-#pragma unroll
-    for (int e = 0; e < kDVT * DK / kThreads; ++e) {
-      const int idx = tid + e * kThreads;
-      const int c = idx / DK, j = idx % DK;
-      float s = end[(size_t)(row0 + c) * DK + j];
-      for (int i = 0; i < DK; ++i) s = fmaf(sS[c][i], M[(size_t)i * DK + j], s);
-      acc[e] = s;
+    const float* sM = sM0 + (part & 1) * DK * DK;
+    // the other buffer was last read before the barrier that ended the
+    // previous part
+    if (part + 2 < p.parts) {
+      stage_m(part + 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
-    __syncthreads();
+    float acc[RPT][4];
 #pragma unroll
-    for (int e = 0; e < kDVT * DK / kThreads; ++e) {
-      const int idx = tid + e * kThreads;
-      const int c = idx / DK, j = idx % DK;
-      sS[c][j] = acc[e];
-      p.ws_start[((nh * p.parts + part + 1) * dv + row0 + c) * DK + j] = acc[e];
+    for (int a = 0; a < RPT; ++a) {
+      const float4 d4 = reinterpret_cast<const float4*>(
+          end + (size_t)(row0 + rg * RPT + a) * DK)[cg];
+      acc[a][0] = d4.x; acc[a][1] = d4.y; acc[a][2] = d4.z; acc[a][3] = d4.w;
+    }
+    __syncthreads();  // M staged (and the start rows of this part)
+#pragma unroll 4
+    for (int i = 0; i < DK; ++i) {
+      const float4 m = reinterpret_cast<const float4*>(sM + i * DK)[cg];
+#pragma unroll
+      for (int a = 0; a < RPT; ++a) {
+        const float sv = sS[(rg * RPT + a) * SP + i];
+        acc[a][0] = fmaf(sv, m.x, acc[a][0]);
+        acc[a][1] = fmaf(sv, m.y, acc[a][1]);
+        acc[a][2] = fmaf(sv, m.z, acc[a][2]);
+        acc[a][3] = fmaf(sv, m.w, acc[a][3]);
+      }
+    }
+    __syncthreads();  // every thread done with S and M of this part
+#pragma unroll
+    for (int a = 0; a < RPT; ++a) {
+      const int c = rg * RPT + a;
+      const float4 v4 = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+      *reinterpret_cast<float4*>(sS + c * SP + 4 * cg) = v4;
+      reinterpret_cast<float4*>(
+          p.ws_start + ((nh * p.parts + part + 1) * dv + row0 + c) * DK)[cg] = v4;
     }
   }
 }
@@ -323,13 +386,23 @@ cudaError_t launch_chunk_simt(const ChunkParams& p, bool bf16,
 
 cudaError_t launch_sp_chain(const ChunkParams& p, cudaStream_t stream) {
   if (p.parts < 3) return cudaSuccess;
-  dim3 grid(p.dv / kDVT, p.H, p.N);
+  dim3 grid(p.dv / kSpRows, p.H, p.N);
   const int t = timing_start(GDN_KERNEL_SP_CHAIN, stream);
-  if (p.dk == 64)
-    sp_chain_kernel<64><<<grid, kThreads, 0, stream>>>(p);
-  else
-    sp_chain_kernel<128><<<grid, kThreads, 0, stream>>>(p);
-  const cudaError_t e = cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  if (p.dk == 64) {
+    e = cudaFuncSetAttribute(sp_chain_kernel<64>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SpChainSmem<64>::kBytes);
+    if (e == cudaSuccess)
+      sp_chain_kernel<64><<<grid, kThreads, SpChainSmem<64>::kBytes, stream>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(sp_chain_kernel<128>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SpChainSmem<128>::kBytes);
+    if (e == cudaSuccess)
+      sp_chain_kernel<128><<<grid, kThreads, SpChainSmem<128>::kBytes, stream>>>(p);
+  }
+  if (e == cudaSuccess) e = cudaGetLastError();
   timing_stop(t, stream, e);
   return e;
 }
