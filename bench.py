@@ -244,6 +244,8 @@ def run_ours(args, w, device, dist, rank, ws):
     tokens, tok_heads, nseq = _units(w, d_host)
     dk, dv, H = w["dk"], w["dv"], w["H"]
     d = {k: (None if v is None else v.to(device)) for k, v in d_host.items()}
+    sp_flag = {"auto": 0, "chain": gdn.GDN_SP_CHAIN,
+               "scan": gdn.GDN_SP_SCAN}[args.sp_combine]
     stream = torch.cuda.current_stream(device)
     flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     flush_r = torch.zeros(FLUSH_BYTES, dtype=torch.uint8, device=device)
@@ -273,6 +275,14 @@ def run_ours(args, w, device, dist, rank, ws):
                     d["cu_seqlens"], norm_weight=d["norm_weight"],
                     gate=d["gate"], out=out, hT=hT if want_hT else None,
                     output_final_state=want_hT)
+                return
+            if sp_flag or args.sp_parts:
+                # the sub-sequence combination or split count fixed
+                gdn.gdn_chunk_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                     d["h0"], d["cu_seqlens"], out=out,
+                                     hT=hT if want_hT else None,
+                                     output_final_state=want_hT,
+                                     path=sp_flag, sp_parts=args.sp_parts)
                 return
             gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
                               d["h0"], d["cu_seqlens"], out=out,
@@ -434,7 +444,10 @@ def run_ours(args, w, device, dist, rank, ws):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), "
                 "g=-softplus(N(0,1)), beta=sigmoid(N(0,1)))",
-        "config": {"workload": w["desc"],
+        "config": {"workload": w["desc"] + (
+                       f" [sub-sequences: {args.sp_combine}"
+                       f"{', P=%d' % args.sp_parts if args.sp_parts else ''}]"
+                       if sp_flag or args.sp_parts else ""),
                    "l2": "flushed before every timed step: 256 MiB memset, then a "
                          "256 MiB read (write-back of the memset outside the "
                          "timed events)",
@@ -566,6 +579,12 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="w1")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sp-combine", choices=["auto", "chain", "scan"],
+                    default="auto",
+                    help="how sub-sequences of a sequence-parallel split are "
+                         "combined (the library chooses by default)")
+    ap.add_argument("--sp-parts", type=int, default=0,
+                    help="sequence-parallel split count (0 = automatic)")
     ap.add_argument("--sequences", type=int, default=0,
                     help="override the number of sequences of the workload "
                          "(smaller cases for profiler captures)")

@@ -19,7 +19,8 @@ _ABI_NAMES = (
     "GDN_KERNEL_SP_CHAIN", "GDN_KERNEL_DECODE", "GDN_KERNEL_CHUNK_OFFSETS",
     "GDN_KERNEL_CHUNK_CHAIN_WHOLE", "GDN_KERNEL_COUNT", "KERNEL_NAMES",
     "GDN_PATH_AUTO", "GDN_PATH_SIMT", "GDN_PATH_TCGEN05",
-    "GDN_PATH_TCGEN05_SPLIT", "GDN_PATH_TCGEN05_WHOLE",
+    "GDN_PATH_TCGEN05_SPLIT", "GDN_PATH_TCGEN05_WHOLE", "GDN_SP_CHAIN",
+    "GDN_SP_SCAN",
 )
 
 

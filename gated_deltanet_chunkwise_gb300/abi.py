@@ -27,6 +27,8 @@ GDN_PATH_SIMT = 1
 GDN_PATH_TCGEN05 = 2
 GDN_PATH_TCGEN05_SPLIT = 3
 GDN_PATH_TCGEN05_WHOLE = 4
+GDN_SP_CHAIN = 0x100
+GDN_SP_SCAN = 0x200
 # kernel families for per-kernel timing (gdn_kernel_t)
 GDN_KERNEL_CHUNK_PREP = 0
 GDN_KERNEL_CHUNK_CHAIN = 1

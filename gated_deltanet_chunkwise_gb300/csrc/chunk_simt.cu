@@ -349,6 +349,101 @@ __global__ void __launch_bounds__(kThreads) sp_chain_kernel(const ChunkParams p)
   }
 }
 
+// Associative-scan alternative to the serial chain ([lqnn] section 3.4: the
+// chunk-level prefix scan, Hillis-Steele). Sub-sequence p >= 1 of the split
+// pass is the affine map f_p(S) = S M_p + dS_p (ws_end entry p: dS rows
+// 0 .. dv-1, M rows dv .. dv+dk-1). Maps compose associatively,
+//   f_b after f_a = (M_a M_b, dS_a M_b + dS_b),
+// so the inclusive prefixes G_p = f_p after ... after f_1, p = 1 .. L = P-2,
+// take ceil(log2 L) rounds: in the round with offset d every map p > d
+// becomes G_{p-d}-part after it. Then S_start(p + 1) = S_start(1) M^G_p +
+// dS^G_p. One kernel does both: rows of X times M plus an added row, for
+// kScanRows rows of one map per CTA (every CTA stages the map's whole M, so
+// the rows per CTA set how often M is read).
+//   combine: X = src[p - d] (all dv + dk rows), M = src[p].M, added row =
+//            src[p].dS (dS rows only); maps p <= d are copied
+//   apply:   X = ws_start[1] (dv rows), M = src[p].M, added row = src[p].dS,
+//            written to ws_start[p + 1]
+constexpr int kScanRows = 64;
+template <int DK>
+struct SpAffineSmem {
+  static constexpr int kS = kScanRows * (DK + 4);
+  static constexpr size_t kBytes = (size_t)(kS + DK * DK) * sizeof(float);
+};
+
+template <int DK>
+__global__ void __launch_bounds__(kThreads)
+    sp_affine_kernel(const ChunkParams p, const float* src, float* dst, int d,
+                     int apply) {
+  constexpr int CG = DK / 4, RG = kThreads / CG, RPT = kScanRows / RG;
+  static_assert(RG * RPT == kScanRows && CG * RG == kThreads, "tiling");
+  constexpr int SP = DK + 4;
+  extern __shared__ float af_smem[];
+  float* sX = af_smem;                          // [kScanRows][SP]
+  float* sM = af_smem + SpAffineSmem<DK>::kS;   // [DK][DK]
+  const int tid = threadIdx.x;
+  const int cg = tid % CG, rg = tid / CG;
+  const int dv = p.dv, L = p.parts - 2;
+  const int h = blockIdx.y, n = blockIdx.z / L, m = blockIdx.z % L + 1;
+  const int row0 = blockIdx.x * kScanRows;
+  if (p.cu_seqlens) {
+    long long bos, eos;
+    if (!sequence_range(p, n, bos, eos)) return;
+  }
+  const size_t nh = (size_t)n * p.H + h;
+  const size_t entry = (size_t)(dv + DK) * DK;
+  const float* sp = src + (nh * p.parts + m) * entry;  // map m
+  float* out;
+  const float* xr;
+  if (apply) {
+    out = p.ws_start + ((nh * p.parts + m + 1) * dv + row0) * DK;
+    xr = p.ws_start + ((nh * p.parts + 1) * dv + row0) * DK;
+  } else {
+    out = dst + (nh * p.parts + m) * entry + (size_t)row0 * DK;
+    if (m <= d) {
+      // already a full prefix: carried over
+      for (int idx = tid; idx < kScanRows * DK / 4; idx += kThreads)
+        reinterpret_cast<float4*>(out)[idx] =
+            reinterpret_cast<const float4*>(sp + (size_t)row0 * DK)[idx];
+      return;
+    }
+    xr = src + (nh * p.parts + m - d) * entry + (size_t)row0 * DK;
+  }
+  for (int idx = tid; idx < kScanRows * DK / 4; idx += kThreads) {
+    const int c = idx / (DK / 4), i4 = idx % (DK / 4);
+    *reinterpret_cast<float4*>(sX + c * SP + 4 * i4) =
+        reinterpret_cast<const float4*>(xr + (size_t)c * DK)[i4];
+  }
+  const float4* M4 = reinterpret_cast<const float4*>(sp + (size_t)dv * DK);
+  for (int idx = tid; idx < DK * DK / 4; idx += kThreads)
+    reinterpret_cast<float4*>(sM)[idx] = M4[idx];
+  float acc[RPT][4];
+#pragma unroll
+  for (int a = 0; a < RPT; ++a) {
+    const int r = row0 + rg * RPT + a;  // row of the map (dS rows first)
+    float4 d4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < dv) d4 = reinterpret_cast<const float4*>(sp + (size_t)r * DK)[cg];
+    acc[a][0] = d4.x; acc[a][1] = d4.y; acc[a][2] = d4.z; acc[a][3] = d4.w;
+  }
+  __syncthreads();
+#pragma unroll 4
+  for (int i = 0; i < DK; ++i) {
+    const float4 mv = reinterpret_cast<const float4*>(sM + i * DK)[cg];
+#pragma unroll
+    for (int a = 0; a < RPT; ++a) {
+      const float xv = sX[(rg * RPT + a) * SP + i];
+      acc[a][0] = fmaf(xv, mv.x, acc[a][0]);
+      acc[a][1] = fmaf(xv, mv.y, acc[a][1]);
+      acc[a][2] = fmaf(xv, mv.z, acc[a][2]);
+      acc[a][3] = fmaf(xv, mv.w, acc[a][3]);
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < RPT; ++a)
+    reinterpret_cast<float4*>(out + (size_t)(rg * RPT + a) * DK)[cg] =
+        make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+}
+
 template <typename InT, int DK, int VARIANT>
 cudaError_t launch_typed(const ChunkParams& p, cudaStream_t stream) {
   constexpr int C = 64;
@@ -404,6 +499,42 @@ cudaError_t launch_sp_chain(const ChunkParams& p, cudaStream_t stream) {
   }
   if (e == cudaSuccess) e = cudaGetLastError();
   timing_stop(t, stream, e);
+  return e;
+}
+
+// The associative-scan combination (sp_affine_kernel): ceil(log2 L) combine
+// rounds ping-ponging between ws_end and `buf` (same size as ws_end), then
+// the apply launch. Returns the launch result; *launches counts launches.
+cudaError_t launch_sp_scan(const ChunkParams& p, float* buf,
+                           cudaStream_t stream, int* launches) {
+  *launches = 0;
+  if (p.parts < 3) return cudaSuccess;
+  const int L = p.parts - 2;
+  auto kern = p.dk == 64 ? sp_affine_kernel<64> : sp_affine_kernel<128>;
+  const size_t bytes = p.dk == 64 ? SpAffineSmem<64>::kBytes
+                                  : SpAffineSmem<128>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  const float* src = p.ws_end;
+  float* dst = buf;
+  for (int d = 1; d < L; d *= 2) {
+    const int t = timing_start(GDN_KERNEL_SP_CHAIN, stream);
+    kern<<<dim3((p.dv + p.dk) / kScanRows, p.H, p.N * L), kThreads, bytes,
+           stream>>>(p, src, dst, d, 0);
+    e = cudaGetLastError();
+    timing_stop(t, stream, e);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    src = dst;
+    dst = dst == buf ? p.ws_end : buf;
+  }
+  const int t = timing_start(GDN_KERNEL_SP_CHAIN, stream);
+  kern<<<dim3(p.dv / kScanRows, p.H, p.N * L), kThreads, bytes, stream>>>(
+      p, src, nullptr, 0, 1);
+  e = cudaGetLastError();
+  timing_stop(t, stream, e);
+  if (e == cudaSuccess) ++*launches;
   return e;
 }
 

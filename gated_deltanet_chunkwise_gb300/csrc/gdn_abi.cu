@@ -116,18 +116,23 @@ long long parts_cost_tc(int requested, int N, int H, int T, int dv, int C,
   const long long nh = (long long)N * H, tv = (dv + rows - 1) / rows,
                   tk = (128 + rows - 1) / rows;
   auto waves = [&](long long ctas) { return (ctas + sms - 1) / sms; };
-  // packed calls: one pass over the longest possible sequence
-  long long best = waves(nh * tv) * (packed ? (long long)T / C + 1 : nch);
-  int best_p = 1;
-  if (requested > 0 || packed) {
-    *parts_out = requested > 0 ? requested : 1;
-    return best;
-  }
-  for (int P = 2; P <= 64 && P <= nch; ++P) {
-    const long long per = (nch + P - 1) / P;
+  // packed calls: passes over the longest possible sequence
+  const long long len = packed ? (long long)T / C + 1 : nch;
+  auto cost_at = [&](int P) {
+    if (P <= 1) return waves(nh * tv) * len;
+    const long long per = (len + P - 1) / P;
     const long long split = nh * (tv + (long long)(P - 2) * (tv + tk));
     const long long outp = nh * (P - 1) * tv;
-    const long long cost = (waves(split) + waves(outp)) * per;
+    return (waves(split) + waves(outp)) * per;
+  };
+  if (requested > 0 || packed) {
+    *parts_out = requested > 0 ? requested : 1;
+    return cost_at(*parts_out);
+  }
+  long long best = cost_at(1);
+  int best_p = 1;
+  for (int P = 2; P <= 64 && P <= nch; ++P) {
+    const long long cost = cost_at(P);
     if (cost < best) {
       best = cost;
       best_p = P;
@@ -172,6 +177,12 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
               const int32_t* cu_seqlens, int B, int H, int T, int dk, int dv,
               int C, int dtype, int variant, int path, int sp_parts,
               cudaStream_t stream, const Sublayer& sub = Sublayer{}) {
+  // combination of sub-sequences (flags above the path)
+  const int sp_mode = path & (GDN_SP_CHAIN | GDN_SP_SCAN);
+  if ((path & ~0xFF & ~(GDN_SP_CHAIN | GDN_SP_SCAN)) != 0 ||
+      sp_mode == (GDN_SP_CHAIN | GDN_SP_SCAN))
+    return GDN_ERR_INVALID_ARG;
+  path &= 0xFF;
   int rc = check_chunk_args(q, k, v, g, beta, h0, out, hT, cu_seqlens, B, H,
                             T, dk, dv, C, dtype, variant, path, sp_parts);
   if (rc != GDN_OK) return rc;
@@ -218,15 +229,40 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
   else
     parts = choose_parts(sp_parts, B, H, T, dv, C, cu_seqlens != nullptr);
   p.parts = parts;
+  // Combination of the sub-sequences: the scan when forced, or when its
+  // rounds of parallel work (64-row CTAs, two per SM, each worth four of the
+  // chain's 16-row steps) take less time than the chain's P - 2 dependent
+  // steps.
+  bool use_scan = false;
+  if (parts > 2 && sp_mode != GDN_SP_CHAIN) {
+    if (sp_mode == GDN_SP_SCAN) {
+      use_scan = true;
+    } else {
+      int sms = 148, dev = 0, v = 0;
+      if (cudaGetDevice(&dev) == cudaSuccess &&
+          cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
+              cudaSuccess && v > 0)
+        sms = v;
+      const long long L = parts - 2, slots = 2ll * sms;
+      const long long nh = (long long)B * H;
+      long long scan = 4 * ((nh * L * (dv / 64) + slots - 1) / slots);  // apply
+      for (long long d = 1; d < L; d *= 2)
+        scan += 4 * ((nh * L * ((dv + dk) / 64) + slots - 1) / slots);
+      use_scan = scan < L;
+    }
+  }
 
-  // Workspace: UT factors (tensor-core path) and sequence-parallel states.
+  // Workspace: UT factors (tensor-core path) and sequence-parallel states
+  // (and the scan's second buffer of sub-sequence maps).
   const size_t nhp = (size_t)B * H * parts;
   const size_t end_bytes =
       parts > 1 ? nhp * (size_t)(dv + dk) * dk * sizeof(float) : 0;
   const size_t start_bytes =
       parts > 1 ? nhp * (size_t)dv * dk * sizeof(float) : 0;
   const size_t tc_bytes = use_tc ? chunk_tc_workspace_bytes(p) : 0;
-  const size_t total = end_bytes + start_bytes + tc_bytes;
+  const size_t scan_off = (end_bytes + start_bytes + tc_bytes + 255) & ~(size_t)255;
+  const size_t total =
+      use_scan ? scan_off + end_bytes : end_bytes + start_bytes + tc_bytes;
   void* ws = nullptr;
   if (total > 0 && cudaMallocAsync(&ws, total, stream) != cudaSuccess)
     return GDN_ERR_CUDA;
@@ -236,6 +272,8 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
     p.ws_start = reinterpret_cast<float*>(wsc + end_bytes);
   }
   if (use_tc) chunk_tc_bind_workspace(p, wsc + end_bytes + start_bytes);
+  float* scan_buf =
+      use_scan ? reinterpret_cast<float*>(wsc + scan_off) : nullptr;
 
   cudaError_t e = cudaSuccess;
   if (use_tc) {
@@ -251,8 +289,15 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
       // split pass, correction chain, corrected output pass
       p.mode = kModeSplit; p.part_begin = 0; p.part_count = parts - 1;
       e = counted(launch(p), 1);
-      if (e == cudaSuccess && parts > 2)
-        e = counted(launch_sp_chain(p, stream), 1);
+      if (e == cudaSuccess && parts > 2) {
+        if (use_scan) {
+          int n_scan = 0;
+          e = launch_sp_scan(p, scan_buf, stream, &n_scan);
+          counted(e, n_scan);
+        } else {
+          e = counted(launch_sp_chain(p, stream), 1);
+        }
+      }
       if (e == cudaSuccess) {
         p.mode = kModeOutput; p.part_begin = 1; p.part_count = parts - 1;
         e = counted(launch(p), 1);

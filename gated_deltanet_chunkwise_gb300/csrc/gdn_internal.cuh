@@ -83,6 +83,10 @@ struct DecodeParams {
 cudaError_t launch_chunk_simt(const ChunkParams& p, bool bf16,
                               cudaStream_t stream);
 cudaError_t launch_sp_chain(const ChunkParams& p, cudaStream_t stream);
+// The same correction by an associative scan over the sub-sequence maps;
+// `buf` holds as many bytes as ws_end.
+cudaError_t launch_sp_scan(const ChunkParams& p, float* buf,
+                           cudaStream_t stream, int* launches);
 // Tensor-core (tcgen05) path: bf16, dk = 128, dv in {64, 128}. A call takes
 // chunk_tc_workspace_bytes of workspace (bound with chunk_tc_bind_workspace),
 // runs launch_ut_prep once, then launch_chunk_tc for each pass.

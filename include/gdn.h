@@ -80,6 +80,12 @@ typedef enum {
                                     (sequence, head) when dv = 128) */
 #define GDN_PATH_TCGEN05_WHOLE 4 /* 128 state rows per CTA, state in TMEM
                                     lanes (zero-padded when dv = 64) */
+/* How the sub-sequences of a sequence-parallel split are combined, OR-ed into
+ * `path` of gdn_chunk_fwd_ex (default: the library's choice by a cost model,
+ * in practice the serial chain): */
+#define GDN_SP_CHAIN 0x100 /* serial chain, P - 2 dependent steps */
+#define GDN_SP_SCAN 0x200  /* associative (Hillis-Steele) scan over the
+                              sub-sequence maps, ceil(log2(P - 2)) rounds */
 
 /*
  * gdn_chunk_fwd -- chunkwise forward pass, bf16 q/k/v/out.
@@ -122,11 +128,13 @@ int gdn_chunk_fwd_f32(const float* q, const float* k, const float* v,
  * gdn_chunk_fwd_ex -- gdn_chunk_fwd with explicit options.
  *   dtype      GDN_DTYPE_BF16 or GDN_DTYPE_F32 (q, k, v, out)
  *   variant    GDN_GATE_BEFORE_PREDICT or GDN_GATE_AFTER_PREDICT
- *   path       GDN_PATH_* (the GDN_PATH_TCGEN05* paths require bf16)
+ *   path       GDN_PATH_* (the GDN_PATH_TCGEN05* paths require bf16),
+ *              optionally OR GDN_SP_CHAIN or GDN_SP_SCAN (not both)
  *   sp_parts   sequence-parallel split: 0 = automatic, 1 = never split,
  *              P >= 2 = split every sequence into P sub-sequences of whole
  *              chunks (incremental state from zero + scaling matrix, then the
- *              serial correction chain and the fused corrected output)
+ *              correction of the start states, by the serial chain or the
+ *              associative scan, and the fused corrected output)
  * Other arguments as gdn_chunk_fwd.
  */
 int gdn_chunk_fwd_ex(const void* q, const void* k, const void* v,

@@ -227,10 +227,33 @@ def wy_forward(q, k, v, g, beta, h0=None, cu_seqlens=None, chunk=64,
 #    state is Delta S_[i] + S_start M_[i]; the starts form a serial chain.
 #    The gated Phi_i = gamma_i I - W_i^T Kbar_i reduces to I - W^T K at
 #    alpha = 1, the page's form.
+#    combine="scan": the starts by an inclusive prefix scan instead of the
+#    chain ("GPU parallelisation of Gated DeltaNet", section 3.4: the
+#    chunk-level scan of affine maps, Hillis-Steele order). Sub-sequence p
+#    maps its start to its end, S -> S M_p + dS_p; applying map a, then map
+#    b, is S -> S (M_a M_b) + (dS_a M_b + dS_b), an associative product, so
+#    after the rounds with offsets 1, 2, 4, ... entry p holds the map of
+#    sub-sequences 0 .. p.
 # ---------------------------------------------------------------------------
 
+def scan_maps(maps):
+    """Inclusive Hillis-Steele scan of [(M, dS), ...] under 'apply the
+    earlier map, then the later one'."""
+    pref = list(maps)
+    d = 1
+    while d < len(pref):
+        nxt = list(pref)
+        for p in range(d, len(pref)):
+            Ma, dSa = pref[p - d]
+            Mb, dSb = pref[p]
+            nxt[p] = (Ma @ Mb, dSa @ Mb + dSb)
+        pref = nxt
+        d *= 2
+    return pref
+
+
 def sp_forward(q, k, v, g, beta, h0=None, cu_seqlens=None, chunk=64, parts=2,
-               variant=G1):
+               variant=G1, combine="chain"):
     q, k, v, g, beta, h0 = map(_f64, (q, k, v, g, beta, h0))
     B, T, H, dk = q.shape
     dv = v.shape[-1]
@@ -261,17 +284,23 @@ def sp_forward(q, k, v, g, beta, h0=None, cu_seqlens=None, chunk=64, parts=2,
                     dS = dS @ Phi + Psi
                     M = M @ Phi
                 records.append((rec, dS, M))
-            # phase 2 (serial chain over sub-sequences): true start states
-            S_start = S0
-            for rec, dS_end, M_end in records:
-                # phase 3 (independent per chunk): correct, then output
+            # phase 2: true start states, by the serial chain over
+            # sub-sequences or by the prefix scan of their maps
+            if combine == "scan":
+                pref = scan_maps([(M_end, dS_end) for _, dS_end, M_end in records])
+                starts = [S0] + [S0 @ M + dS for M, dS in pref]
+            else:
+                starts = [S0]
+                for _, dS_end, M_end in records:
+                    starts.append(dS_end + starts[-1] @ M_end)
+            # phase 3 (independent per chunk): correct, then output
+            for (rec, _, _), S_start in zip(records, starts):
                 for c, dS_i, M_i in rec:
                     S_i = dS_i + S_start @ M_i
                     O, _ = wy_chunk_step(S_i, qf[c, h], kf[c, h], vf[c, h],
                                          gf[c, h], bf[c, h], variant)
                     out[c, h] = O
-                S_start = dS_end + S_start @ M_end
-            hT[n, h] = S_start.T
+            hT[n, h] = starts[-1].T
     return out.reshape(B, T, H, dv), hT
 
 

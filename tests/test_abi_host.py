@@ -88,6 +88,8 @@ def chunk(so, q=A, k=A + 0x1000, v=A + 0x2000, g=A + 0x3000, beta=A + 0x4000,
     (dict(cu=A + 0x6000, B=0), INVALID),  # packed batch needs >= 1 sequence
     (dict(variant=7), INVALID),
     (dict(path=9), INVALID),
+    (dict(path=0x300), INVALID),         # chain and scan both requested
+    (dict(path=0x400), INVALID),         # unknown flag
     (dict(dtype=5), INVALID),
     (dict(sp_parts=-1), INVALID),
     (dict(dtype=1, path=2), UNSUPPORTED),  # tensor-core path is bf16 only

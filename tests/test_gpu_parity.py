@@ -122,6 +122,33 @@ def test_packed_sequences_sequence_parallel(lib, cuda_device):
     check(lib, cuda_device, d, "f32", sp_parts=3)
 
 
+# ---- sub-sequences combined by the associative scan (GDN_SP_SCAN) ----
+SP_SCAN = 0x200
+
+
+@pytest.mark.parametrize("parts", [3, 4, 6, 11])
+@pytest.mark.parametrize("dtype,dk", [("f32", 64), ("f32", 128), ("bf16", 128)])
+def test_sequence_parallel_scan_matches_oracle(lib, cuda_device, parts, dtype,
+                                               dk):
+    d = inputs.chunk_inputs(2, 2, 64 * 13 + 21, dk, 64, dtype=dtype, seed=19,
+                            h0=True)
+    check(lib, cuda_device, d, dtype, path=SP_SCAN, sp_parts=parts)
+
+
+@pytest.mark.parametrize("path", [3, 4])
+def test_sequence_parallel_scan_tensor_core(lib, cuda_device, path):
+    d = inputs.chunk_inputs(1, 2, 64 * 19 + 40, 128, 128, dtype="bf16",
+                            seed=20, h0=True)
+    check(lib, cuda_device, d, "bf16", path=path | SP_SCAN, sp_parts=9)
+
+
+def test_packed_sequences_scan(lib, cuda_device):
+    lengths = [300, 5, 640, 0, 129]
+    d = inputs.chunk_inputs(len(lengths), 2, 0, 64, 64, dtype="f32", seed=21,
+                            h0=True, lengths=lengths)
+    check(lib, cuda_device, d, "f32", path=SP_SCAN, sp_parts=7)
+
+
 def test_resume_through_final_state(lib, cuda_device):
     d = inputs.chunk_inputs(2, 2, 300, 128, 128, dtype="f32", seed=8, h0=True)
     x = to_dev(d, cuda_device)

@@ -286,13 +286,14 @@ def test_wy_representation_of_chunk_transform():
     np.testing.assert_allclose(np.diag(Tm), 1, atol=1e-14)
 
 
-@pytest.mark.parametrize("parts", [2, 4, 8])
+@pytest.mark.parametrize("combine", ["chain", "scan"])
+@pytest.mark.parametrize("parts", [2, 4, 8, 9])
 @pytest.mark.parametrize("gated", [True, False])
-def test_sequence_parallel_correction_equals_serial(parts, gated):
+def test_sequence_parallel_correction_equals_serial(parts, gated, combine):
     d = _batch(12, B=1, T=8 * 16 + 5, H=2, gated=gated)
     args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
     o_ref, h_ref = oracle.forward(*args)
-    o, h = chunked.sp_forward(*args, chunk=16, parts=parts)
+    o, h = chunked.sp_forward(*args, chunk=16, parts=parts, combine=combine)
     np.testing.assert_allclose(o, o_ref, rtol=1e-10, atol=1e-11)
     np.testing.assert_allclose(h, h_ref, rtol=1e-10, atol=1e-11)
 
@@ -379,3 +380,22 @@ def test_oracle_rejects_bad_packing():
     with pytest.raises(ValueError):
         oracle.forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"],
                        cu_seqlens=cu)
+
+
+def test_map_scan_matches_left_fold():
+    """The Hillis-Steele prefixes equal the left fold of the composition, and
+    composing a map with the identity map (I, 0) changes nothing."""
+    rng = np.random.default_rng(21)
+    dk, dv = 5, 3
+    maps = [(rng.standard_normal((dk, dk)), rng.standard_normal((dv, dk)))
+            for _ in range(11)]
+    pref = chunked.scan_maps(maps)
+    S = rng.standard_normal((dv, dk))
+    x = S
+    for (M, dS), (Mp, dSp) in zip(maps, pref):
+        x = x @ M + dS          # apply the maps one after another
+        np.testing.assert_allclose(S @ Mp + dSp, x, rtol=1e-10, atol=1e-10)
+    ident = (np.eye(dk), np.zeros((dv, dk)))
+    for M, dS in chunked.scan_maps([ident, maps[0]])[-1:]:
+        np.testing.assert_allclose(M, maps[0][0], atol=0)
+        np.testing.assert_allclose(dS, maps[0][1], atol=0)
