@@ -19,6 +19,8 @@ Two parts:
   RMS normalisation and sigmoid gate of the output) and ``fused_forward``,
   which wraps ``forward`` with them; pinned in
   ``tests/test_oracle_sublayer_pins.py``.
+* ``oracle.kda`` -- the delta rule with a per-channel decay (KDA) in fp64,
+  token by token; pinned in ``tests/test_oracle_kda_pins.py``.
 
 Pins (all in ``tests/test_oracle_pins.py``): worked numbers of the illustrated
 DeltaNet page (delta-rule 1.5/2.25/2.625, the 2-D example, prediction/error,
