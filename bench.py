@@ -38,6 +38,14 @@ sys.path.insert(0, str(ROOT))
 METRIC = "GDN chunk-fwd tokens/s + % of GB300 tensor/HBM roofline, 1 GPU"
 FLUSH_BYTES = 256 << 20
 
+
+def _metric(w):
+    if w["kind"] == "decode":
+        return "GDN decode-step token-heads/s + % of GB300 HBM roofline, 1 GPU"
+    if w["kind"] == "kda":
+        return "KDA (per-channel decay) forward tokens/s + % of GB300 fp32 ALU peak, 1 GPU"
+    return METRIC
+
 # Algorithmic work per token-head of the chunked forward pass:
 #   flops  = 2 C (3 dk + 2 dv) + 6 dk dv   (K K^T, Q K^T, T.K, T.V, P.U;
 #            W S^T, U^T Kbar, Q S^T)
@@ -80,6 +88,9 @@ WORKLOADS = {
                 desc="gdn_chunk_fwd_fused B=4 H=16 T=2048 dk=dv=128 C=64 bf16: "
                      "raw q/k (L2 norm in the kernels), gate and step logits, "
                      "output RMSNorm (weight [dv]) and sigmoid gate, h0=0"),
+    "kda1": dict(kind="kda", B=4, H=16, T=2048, dk=128, dv=128, h0=False,
+                 desc="gdn_kda_fwd B=4 H=16 T=2048 dk=dv=128 bf16, per-channel "
+                      "log-decays max(-softplus(N(0,1)), -5), h0=0"),
     "w4": dict(kind="decode", N=512, H=32, dk=128, dv=128,
                desc="gdn_recurrent_step N=512 H=32 dk=dv=128 bf16 token, "
                     "fp32 state in place"),
@@ -101,7 +112,7 @@ MEASURED_TRAFFIC = {
 
 def _kernel_source_hash(kind):
     csrc = ROOT / "gated_deltanet_chunkwise_gb300" / "csrc"
-    files = ["decode.cu"] if kind == "decode" else sorted(
+    files = ["decode.cu"] if kind == "decode" else ["kda.cu"] if kind == "kda" else sorted(
         p.name for p in csrc.glob("chunk_*.cu"))
     h = hashlib.sha256()
     for f in files:
@@ -115,6 +126,15 @@ def _peaks():
         d = json.loads(p.read_text())
         return d["hbm_gbs"], d["bf16_tflops"], "measured"
     return 6800.0, 1900.0, "fallback"
+
+
+def _sm_max_mhz():
+    """Maximum SM clock of the GB300s (measured file, else the
+    part's nominal 2070 MHz)."""
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        return float(json.loads(p.read_text()).get("sm_max_mhz", 2070.0))
+    return 2070.0
 
 
 class ClockSampler:
@@ -222,6 +242,9 @@ def _make_inputs(w, seed=0):
     if w["kind"] == "fused":
         return inputs.fused_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
                                    seed=seed, h0=w["h0"])
+    if w["kind"] == "kda":
+        return inputs.kda_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
+                                 seed=seed, h0=w["h0"])
     return inputs.chunk_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
                                dtype="bf16", seed=seed, h0=w["h0"],
                                length_range=w.get("lengths"))
@@ -269,6 +292,12 @@ def run_ours(args, w, device, dist, rank, ws):
         want_hT = w["h0"]
 
         def step():
+            if w["kind"] == "kda":
+                gdn.gdn_kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                d["h0"], d["cu_seqlens"], out=out,
+                                hT=hT if want_hT else None,
+                                output_final_state=want_hT)
+                return
             if w["kind"] == "fused":
                 gdn.gdn_chunk_fwd_fused(
                     d["q"], d["k"], d["v"], d["a"], d["b"], d["h0"],
@@ -392,6 +421,27 @@ def run_ours(args, w, device, dist, rank, ws):
         value = units_all / (ms * 1e-3) * (tok_heads / tokens)  # heads/s
         unit = "token-heads/s"
         e2e_val = units_all / (e2e_ms * 1e-3) * (tok_heads / tokens)
+    elif w["kind"] == "kda":
+        # fp32 CUDA-core arithmetic per token-head: the decay d_k d_v
+        # multiplies, then the prediction S k, the rank-1 update and the read
+        # S q at 2 d_k d_v each; against the fp32 FMA peak of the SMs
+        n_k, ms_k = kern.get("kda_kernel", (0, 0.0))
+        k_ms = ms_k / n_k if n_k else ms
+        flops = 7 * dk * dv * tok_heads
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        mhz = _sm_max_mhz()
+        alu_tflops = sms * 128 * 2 * mhz * 1e6 / 1e12
+        achieved = flops / (k_ms * 1e-3) / 1e12
+        roof = {"bound": "alu", "kernel": "kda_kernel",
+                "achieved": round(achieved, 2), "peak": round(alu_tflops, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / alu_tflops, 4),
+                "peak_source": f"derived: {sms} SMs x 128 fp32 FMA/cycle x 2 "
+                               f"x {mhz:.0f} MHz (max SM clock)",
+                "algorithmic_flops_per_launch": flops,
+                "launches_per_step": n_k / steps, "ms_per_launch": k_ms}
+        value = units_all / (ms * 1e-3)
+        unit = "tokens/s"
+        e2e_val = units_all / (e2e_ms * 1e-3)
     else:
         # roofline of the dominant kernel (the chain), from the library's own
         # CUDA events around each of its launches in the timed region
@@ -437,13 +487,14 @@ def run_ours(args, w, device, dist, rank, ws):
         d["state"].copy_(state0)
 
     line = {
-        "metric": METRIC if w["kind"] != "decode" else
-        "GDN decode-step token-heads/s + % of GB300 HBM roofline, 1 GPU",
+        "metric": _metric(w),
         "value": value, "unit": unit, "n_gpus": ws, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32" if w["kind"] == "kda" else "bf16",
         "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), "
-                "g=-softplus(N(0,1)), beta=sigmoid(N(0,1)))",
+                + ("per-channel g=max(-softplus(N(0,1)),-5)"
+                   if w["kind"] == "kda" else "g=-softplus(N(0,1))")
+                + ", beta=sigmoid(N(0,1)))",
         "config": {"workload": w["desc"] + (
                        f" [sub-sequences: {args.sp_combine}"
                        f"{', P=%d' % args.sp_parts if args.sp_parts else ''}]"
@@ -494,6 +545,20 @@ def cpu_baseline(w, d_host, budget_s=20.0):
                 "kind": "oracle",
                 "sample": f"full workload, oracle with the steps either side",
                 "seconds": round(dt, 3)}
+    if w["kind"] == "kda":
+        from oracle import kda
+        take = 1
+        Tsub = d_host["q"].shape[1]
+        sl = lambda x: x[:take, :Tsub]
+        t0 = time.perf_counter()
+        kda.forward(sl(d_host["q"]), sl(d_host["k"]), sl(d_host["v"]),
+                    sl(d_host["g"]), sl(d_host["beta"]), None)
+        dt = time.perf_counter() - t0
+        return {"value": take * Tsub / dt, "unit": "tokens/s", "cores": 1,
+                "kind": "oracle",
+                "sample": f"1 of {d_host['q'].shape[0]} sequences ({Tsub} "
+                          f"tokens) x all {w['H']} heads (token loop, numpy)",
+                "seconds": round(dt, 3)}
     # dense: whole sequences (all heads); packed: the first sequences
     if d_host["cu_seqlens"] is None:
         nb = d_host["q"].shape[0]
@@ -535,6 +600,15 @@ def run_reference(args, w):
                                   d["state"])
         units, unit, sample = 64 * w["H"], "token-heads/s", \
             f"64 of {w['N']} sequences x {w['H']} heads, one token"
+    elif w["kind"] == "kda":
+        from oracle import kda
+        T = 256
+        d = inputs.kda_inputs(1, w["H"], T, w["dk"], w["dv"], seed=0)
+
+        def step():
+            kda.forward(d["q"], d["k"], d["v"], d["g"], d["beta"], None)
+        units, unit, sample = T, "tokens/s", \
+            f"one sequence of {T} tokens x all {w['H']} heads (token loop)"
     else:
         T = w["T"] if w["T"] else 4096
         T = min(T, 4096)
@@ -556,8 +630,7 @@ def run_reference(args, w):
     value = units / sec
     cores = oracle.max_threads()
     return {
-        "impl": "reference", "metric": METRIC if w["kind"] == "chunk" else
-        "GDN decode-step token-heads/s + % of GB300 HBM roofline, 1 GPU",
+        "impl": "reference", "metric": _metric(w),
         "value": value, "unit": unit, "n_gpus": 1, "steps": len(times),
         "warmup": args.warmup, "ms_per_step": sec * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -37,7 +37,8 @@ GDN_KERNEL_SP_CHAIN = 3
 GDN_KERNEL_DECODE = 4
 GDN_KERNEL_CHUNK_OFFSETS = 5
 GDN_KERNEL_CHUNK_CHAIN_WHOLE = 6
-GDN_KERNEL_COUNT = 7
+GDN_KERNEL_KDA = 7
+GDN_KERNEL_COUNT = 8
 KERNEL_NAMES = {
     GDN_KERNEL_CHUNK_PREP: "ut_prep_kernel",
     GDN_KERNEL_CHUNK_CHAIN: "chunk_tc_kernel",
@@ -46,6 +47,7 @@ KERNEL_NAMES = {
     GDN_KERNEL_DECODE: "decode_kernel",
     GDN_KERNEL_CHUNK_OFFSETS: "chunk_offsets_kernel",
     GDN_KERNEL_CHUNK_CHAIN_WHOLE: "chain_tx_kernel",
+    GDN_KERNEL_KDA: "kda_kernel",
 }
 
 _lib = None
@@ -85,6 +87,9 @@ def library():
     lib.gdn_recurrent_step.argtypes = [vp, vp, vp, fp, fp, fp, vp, i, i, i, i,
                                        vp]
     lib.gdn_recurrent_step.restype = i
+    lib.gdn_kda_fwd.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, ip, i, i, i, i,
+                                i, vp]
+    lib.gdn_kda_fwd.restype = i
     lib.gdn_device_status.argtypes = [vp]
     lib.gdn_device_status.restype = i
     lib.gdn_status_string.argtypes = [i]
@@ -218,6 +223,52 @@ def gdn_chunk_fwd_ex(q, k, v, g, beta, h0=None, cu_seqlens=None, *, out=None,
     return _chunk_call("gdn_chunk_fwd_ex", q, k, v, g, beta, h0, cu_seqlens,
                        out, hT, output_final_state, C, stream, q.dtype,
                        extra=(dtype, int(variant), int(path), int(sp_parts)))
+
+
+def gdn_kda_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, out=None,
+                hT=None, output_final_state=True, stream=None):
+    """The delta rule with a per-channel decay: q, k bf16 [B, T, H, dk], v
+    bf16 [B, T, H, dv], g fp32 [B, T, H, dk] log-decays, beta fp32 [B, T,
+    H]. Returns (out bf16 like v, hT fp32 [N, H, dk, dv] or None); ``hT``
+    may be ``h0`` (in-place state update)."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, None)
+    _need(k, "k", torch.bfloat16, dev)
+    _need(v, "v", torch.bfloat16, dev)
+    _need(g, "g", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    Bt, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != (Bt, T, H) or g.shape != q.shape:
+        raise ValueError("q/k/g must be [B, T, H, dk] and v [B, T, H, dv]")
+    if beta.shape != (Bt, T, H):
+        raise ValueError("beta must be [B, T, H]")
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        if Bt != 1:
+            raise ValueError("packed sequences are passed as [1, T, H, ...]")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = Bt
+    for name, st in (("h0", h0), ("hT", hT)):
+        if st is not None:
+            _need(st, name, torch.float32, dev)
+            if st.shape != (N, H, dk, dv):
+                raise ValueError(f"{name} must be [{N}, {H}, {dk}, {dv}]")
+    if out is None:
+        out = torch.empty_like(v)
+    else:
+        _need(out, "out", torch.bfloat16, dev)
+    if hT is None and output_final_state:
+        hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        rc = library().gdn_kda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                   _ptr(beta), _ptr(h0), _ptr(out), _ptr(hT),
+                                   _ptr(cu_seqlens), N, H, T, dk, dv,
+                                   _stream(stream))
+    if rc != GDN_OK:
+        raise GdnError(rc, "gdn_kda_fwd")
+    return out, hT
 
 
 def gdn_chunk_fwd_fused(q, k, v, a, b, h0=None, cu_seqlens=None, *,

@@ -468,6 +468,35 @@ int gdn_recurrent_step(const void* q, const void* k, const void* v,
              : GDN_ERR_CUDA;
 }
 
+int gdn_kda_fwd(const void* q, const void* k, const void* v, const float* g,
+                const float* beta, const float* h0, void* out, float* hT,
+                const int32_t* cu_seqlens, int B, int H, int T, int dk, int dv,
+                gdn_stream_t stream) {
+  if (B < 0 || H <= 0 || T < 0) return GDN_ERR_INVALID_ARG;
+  if (cu_seqlens && B == 0) return GDN_ERR_INVALID_ARG;
+  if (!gdn::head_dim_ok(dk) || !gdn::head_dim_ok(dv)) return GDN_ERR_UNSUPPORTED;
+  const long long tokens = cu_seqlens ? (long long)T : (long long)B * T;
+  if (B == 0) return GDN_OK;
+  if (tokens > 0 && (!q || !k || !v || !g || !beta || !out))
+    return GDN_ERR_INVALID_ARG;
+  if ((long long)tokens * H > (1ll << 40) || (long long)B * H > 0x7fffffffll)
+    return GDN_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q, k, v, g, beta, h0, out, hT, cu_seqlens};
+  for (const void* p : ptrs)
+    if (p && !gdn::aligned16(p)) return GDN_ERR_MISALIGNED;
+  if (out && (out == q || out == k || out == v)) return GDN_ERR_INVALID_ARG;
+  int* status = nullptr;
+  int rc = gdn::current_status_ptr(&status);
+  if (rc != GDN_OK) return rc;
+  gdn::KdaParams p{};
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.h0 = h0;
+  p.out = out; p.hT = hT; p.cu_seqlens = cu_seqlens;
+  p.N = B; p.H = H; p.T = T; p.dk = dk; p.dv = dv; p.status = status;
+  return gdn::counted(gdn::launch_kda(p, stream), 1) == cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_CUDA;
+}
+
 int gdn_device_status(gdn_stream_t stream) {
   int* status = nullptr;
   int rc = gdn::current_status_ptr(&status);

@@ -79,6 +79,21 @@ struct DecodeParams {
   int variant;
 };
 
+// The delta rule with a per-channel decay (gdn_kda_fwd).
+struct KdaParams {
+  const void* q;        // bf16 [tokens, H, dk]
+  const void* k;        // bf16 [tokens, H, dk]
+  const void* v;        // bf16 [tokens, H, dv]
+  const float* g;       // fp32 [tokens, H, dk] log-decays
+  const float* beta;    // fp32 [tokens, H]
+  const float* h0;      // fp32 [N, H, dk, dv] or null
+  void* out;            // bf16 [tokens, H, dv]
+  float* hT;            // fp32 [N, H, dk, dv] or null (may be h0)
+  const int32_t* cu_seqlens;
+  int N, H, T, dk, dv;
+  int* status;          // device status word
+};
+
 // Launchers (return a cudaError_t from the launch itself).
 cudaError_t launch_chunk_simt(const ChunkParams& p, bool bf16,
                               cudaStream_t stream);
@@ -97,6 +112,7 @@ cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
                            int* launches);
 cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_kda(const KdaParams& p, cudaStream_t stream);
 
 // Host helpers owned by gdn_abi.cu.
 int validate_chunk_args(const void* q, const void* k, const void* v,

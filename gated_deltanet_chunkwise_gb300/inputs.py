@@ -140,3 +140,19 @@ def fused_inputs(B, H, T, dk, dv, *, seed=0, h0=False, lengths=None,
         "norm_weight": None if w is None else t(w),
         "gate": None if z is None else bf(z),
     }
+
+
+def kda_inputs(B, H, T, dk, dv, *, seed=0, h0=False, lengths=None,
+               length_range=None):
+    """Inputs for the per-channel-decay recurrence (gdn_kda_fwd): as
+    ``chunk_inputs`` (bf16 q, k unit rows, v; fp32 beta; optional h0 and
+    packing) but with log-decays per key channel, g [.., H, dk] =
+    max(-softplus(N(0, 1)), -5): each step's log-decay in (-5, 0), the range
+    the walk-through quotes for a KDA model's gates."""
+    d = chunk_inputs(B, H, T, dk, dv, dtype="bf16", seed=seed, h0=h0,
+                     lengths=lengths, length_range=length_range)
+    rng = np.random.Generator(np.random.PCG64(seed + 7919))
+    shape = tuple(d["q"].shape)
+    g = np.maximum(-_softplus(_normal(rng, shape)), np.float32(-5.0))
+    d["g"] = torch.from_numpy(g.astype(np.float32))
+    return d

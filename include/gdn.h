@@ -189,6 +189,33 @@ int gdn_recurrent_step(const void* q, const void* k, const void* v,
                        gdn_stream_t stream);
 
 /*
+ * gdn_kda_fwd -- the delta rule with a per-channel decay (KDA; illustrated
+ * DeltaNet walk-through, KDA paragraphs of its hybrid-architecture section),
+ * token by token, state in fp32:
+ *   S_bar = S_{t-1} diag(exp(g_t))          (key channel c of the d_v x d_k
+ *                                             state scaled by exp(g_{t,c}))
+ *   S_t = S_bar + beta_t (v_t - S_bar k_t) k_t^T,   o_t = S_t q_t
+ * With every g_{t,c} equal this is gdn_chunk_fwd's recurrence.
+ *   q, k   bf16 [B, T, H, dk]     v, out  bf16 [B, T, H, dv]   (device)
+ *   g      fp32 [B, T, H, dk] log-decays (<= 0 for a decay; any value is
+ *          evaluated as given, no rescaling is involved)
+ *   beta   fp32 [B, T, H]
+ *   h0     fp32 [N, H, dk, dv] or NULL (zero); hT likewise or NULL; element
+ *          (i, j) is S[j][i]; hT may be the same buffer as h0, which makes a
+ *          call with T = 1 a decode step that updates the state in place
+ *   cu_seqlens  as for gdn_chunk_fwd (B = N sequences, T = total tokens)
+ *   dk, dv 64 or 128
+ * One CTA per (32 value rows, head, sequence); the call is asynchronous on
+ * `stream`; an invalid packing is recorded in the status word
+ * (gdn_device_status). Returns GDN_OK, GDN_ERR_INVALID_ARG,
+ * GDN_ERR_UNSUPPORTED, GDN_ERR_MISALIGNED or GDN_ERR_CUDA.
+ */
+int gdn_kda_fwd(const void* q, const void* k, const void* v, const float* g,
+                const float* beta, const float* h0, void* out, float* hT,
+                const int32_t* cu_seqlens, int B, int H, int T, int dk, int dv,
+                gdn_stream_t stream);
+
+/*
  * gdn_chunk_fwd_sp_noalloc -- the sequence-parallel forward pass of
  * gdn_chunk_fwd_ex (path GDN_PATH_SIMT, sp_parts >= 2) for callers that may
  * not allocate device memory while they enqueue work (for example a plugin
@@ -255,7 +282,8 @@ typedef enum {
   GDN_KERNEL_DECODE = 4,        /* single-token recurrent step */
   GDN_KERNEL_CHUNK_OFFSETS = 5, /* chunk offsets of packed sequences */
   GDN_KERNEL_CHUNK_CHAIN_WHOLE = 6, /* the same chain, 128 rows per CTA */
-  GDN_KERNEL_COUNT = 7
+  GDN_KERNEL_KDA = 7,           /* per-channel-decay recurrence */
+  GDN_KERNEL_COUNT = 8
 } gdn_kernel_t;
 
 /* gdn_timing_enable -- per-kernel device timing on (nonzero) or off (0).

@@ -182,3 +182,24 @@ def test_fused_rejects_on_host(lib, kw, expect):
 
 def test_fused_empty_batch_is_a_no_op(lib):
     assert fused(lib.library(), B=0) == OK
+
+
+def kda(so, q=A, k=A + 0x1000, v=A + 0x2000, g=A + 0x3000, b=A + 0x4000,
+        h0=None, out=A + 0x5000, hT=None, cu=None, B=1, H=1, T=16, dk=128,
+        dv=128):
+    return so.gdn_kda_fwd(q, k, v, g, b, h0, out, hT, cu, B, H, T, dk, dv, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(B=-1), INVALID), (dict(H=0), INVALID), (dict(T=-1), INVALID),
+    (dict(q=None), INVALID), (dict(dk=96), UNSUPPORTED),
+    (dict(dv=32), UNSUPPORTED), (dict(g=ODD), MISALIGNED),
+    (dict(h0=ODD), MISALIGNED), (dict(out=A), INVALID),
+    (dict(cu=A + 0x6000, B=0), INVALID),
+])
+def test_kda_rejects_on_host(lib, kw, expect):
+    assert kda(lib.library(), **kw) == expect
+
+
+def test_kda_empty_batch_is_a_no_op(lib):
+    assert kda(lib.library(), B=0) == OK
