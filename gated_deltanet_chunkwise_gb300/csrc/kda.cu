@@ -19,10 +19,6 @@
 // (no rescaling).
 #include "gdn_internal.cuh"
 
-
-
-
-
 namespace gdn {
 namespace {
 
