@@ -38,7 +38,8 @@ GDN_KERNEL_DECODE = 4
 GDN_KERNEL_CHUNK_OFFSETS = 5
 GDN_KERNEL_CHUNK_CHAIN_WHOLE = 6
 GDN_KERNEL_KDA = 7
-GDN_KERNEL_COUNT = 8
+GDN_KERNEL_KDA_PREP = 8
+GDN_KERNEL_COUNT = 9
 KERNEL_NAMES = {
     GDN_KERNEL_CHUNK_PREP: "ut_prep_kernel",
     GDN_KERNEL_CHUNK_CHAIN: "chunk_tc_kernel",
@@ -48,6 +49,7 @@ KERNEL_NAMES = {
     GDN_KERNEL_CHUNK_OFFSETS: "chunk_offsets_kernel",
     GDN_KERNEL_CHUNK_CHAIN_WHOLE: "chain_tx_kernel",
     GDN_KERNEL_KDA: "kda_kernel",
+    GDN_KERNEL_KDA_PREP: "kda_prep_kernel",
 }
 
 _lib = None
@@ -90,6 +92,9 @@ def library():
     lib.gdn_kda_fwd.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, ip, i, i, i, i,
                                 i, vp]
     lib.gdn_kda_fwd.restype = i
+    lib.gdn_kda_fwd_ex.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, ip, i, i, i,
+                                   i, i, i, i, vp]
+    lib.gdn_kda_fwd_ex.restype = i
     lib.gdn_device_status.argtypes = [vp]
     lib.gdn_device_status.restype = i
     lib.gdn_status_string.argtypes = [i]
@@ -227,10 +232,28 @@ def gdn_chunk_fwd_ex(q, k, v, g, beta, h0=None, cu_seqlens=None, *, out=None,
 
 def gdn_kda_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, out=None,
                 hT=None, output_final_state=True, stream=None):
-    """The delta rule with a per-channel decay: q, k bf16 [B, T, H, dk], v
-    bf16 [B, T, H, dv], g fp32 [B, T, H, dk] log-decays, beta fp32 [B, T,
-    H]. Returns (out bf16 like v, hT fp32 [N, H, dk, dv] or None); ``hT``
-    may be ``h0`` (in-place state update)."""
+    """The delta rule with a per-channel decay, token by token: q, k bf16
+    [B, T, H, dk], v bf16 [B, T, H, dv], g fp32 [B, T, H, dk] log-decays,
+    beta fp32 [B, T, H]. Returns (out bf16 like v, hT fp32 [N, H, dk, dv] or
+    None); ``hT`` may be ``h0`` (in-place state update)."""
+    return _kda("gdn_kda_fwd", q, k, v, g, beta, h0, cu_seqlens, out, hT,
+                output_final_state, stream, ())
+
+
+def gdn_kda_fwd_ex(q, k, v, g, beta, h0=None, cu_seqlens=None, *, out=None,
+                   hT=None, output_final_state=True, path=GDN_PATH_AUTO,
+                   sp_parts=0, stream=None):
+    """gdn_kda_fwd with a choice of kernels: ``path`` GDN_PATH_AUTO (the
+    chunk form on the tensor cores where it applies), GDN_PATH_SIMT (token by
+    token) or GDN_PATH_TCGEN05 (the chunk form), optionally or-ed with
+    GDN_SP_CHAIN / GDN_SP_SCAN; ``sp_parts`` the sequence-parallel split of
+    the chunk form (0: automatic)."""
+    return _kda("gdn_kda_fwd_ex", q, k, v, g, beta, h0, cu_seqlens, out, hT,
+                output_final_state, stream, (int(path), int(sp_parts)))
+
+
+def _kda(fn, q, k, v, g, beta, h0, cu_seqlens, out, hT, output_final_state,
+         stream, extra):
     dev = q.device
     _need(q, "q", torch.bfloat16, None)
     _need(k, "k", torch.bfloat16, dev)
@@ -262,12 +285,12 @@ def gdn_kda_fwd(q, k, v, g, beta, h0=None, cu_seqlens=None, *, out=None,
     if hT is None and output_final_state:
         hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
-        rc = library().gdn_kda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g),
-                                   _ptr(beta), _ptr(h0), _ptr(out), _ptr(hT),
-                                   _ptr(cu_seqlens), N, H, T, dk, dv,
-                                   _stream(stream))
+        rc = getattr(library(), fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                      _ptr(beta), _ptr(h0), _ptr(out),
+                                      _ptr(hT), _ptr(cu_seqlens), N, H, T, dk,
+                                      dv, *extra, _stream(stream))
     if rc != GDN_OK:
-        raise GdnError(rc, "gdn_kda_fwd")
+        raise GdnError(rc, fn)
     return out, hT
 
 

@@ -44,30 +44,11 @@
 #include "gdn_internal.cuh"
 #include "gdn_selftest.h"
 #include "tc_ptx.cuh"
+#include "chunk_tiles.cuh"
 
 namespace gdn {
 namespace {
 using namespace tc;
-
-
-constexpr int C = 64;
-constexpr int DK = 128;
-constexpr int DVT = 64;
-constexpr int AP = 68;  // fp32 row pitch of the solve buffer
-
-// Gate vectors of one chunk (written by one warp): cumulative log gate G,
-// alpha = e^g, e^G, beta e^{G'}, beta, e^{G_L - G}, e^{-G}, gamma = e^{G_L},
-// and whether e^{G_r} e^{-G_j} stays in the normal fp32 range; then the
-// inverse lengths of the chunk's k and q rows (1 when they come normalised).
-constexpr int VEC_G = 0, VEC_ALPHA = 64, VEC_EG = 128, VEC_EGPB = 192,
-              VEC_BETA = 256, VEC_DEC = 320, VEC_IEG = 384, VEC_GAMMA = 448,
-              VEC_SAFE = 449, VEC_SK = 452, VEC_SQ = 516, VEC_FLOATS = 580;
-// The part of them the chain kernel reads, per (chunk, head) in the
-// workspace: e^G, e^{G_L - G}, gamma (padded to a multiple of 16 bytes).
-constexpr int CV_EG = 0, CV_DEC = 64, CV_GAMMA = 128, CV_FLOATS = 132;
-constexpr uint32_t CV_BYTES = CV_FLOATS * 4;
-
-
 
 // log alpha = -softplus(a) and beta = sigmoid(b) from the logits.
 __device__ __forceinline__ float neg_softplus(float a) {
@@ -143,244 +124,6 @@ __device__ __forceinline__ void gate_vectors(const float* g, const float* beta,
   }
 }
 
-// Chunk `c` of the whole call -> (sequence n, chunk index within n).
-__device__ __forceinline__ void locate_chunk(const ChunkParams& p, int c,
-                                             int nch_dense, int& n, int& lc) {
-  if (!p.chunk_off) {
-    n = c / nch_dense;
-    lc = c - n * nch_dense;
-    return;
-  }
-  int lo = 0, hi = p.N;  // chunk_off[lo] <= c < chunk_off[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (p.chunk_off[mid] <= c) lo = mid; else hi = mid;
-  }
-  n = lo;
-  lc = c - p.chunk_off[lo];
-}
-
-__device__ __forceinline__ int chunk_base(const ChunkParams& p, int n,
-                                          int nch_dense) {
-  return p.chunk_off ? p.chunk_off[n] : n * nch_dense;
-}
-
-// AND of `v` over the threads of named barrier `id` (also a barrier).
-
-__device__ __forceinline__ bool bar_and(int id, int count, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred q, p;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.and.pred p, %2, %3, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
-
-__device__ __forceinline__ bool wait_ignoring_abort(uint64_t* bar,
-                                                    uint32_t parity) {
-  int local = 0;
-  return mbar_wait(bar, parity, &local);
-}
-
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
-  float (&lo)[32] = *reinterpret_cast<float(*)[32]>(&x[0]);
-  float (&hi)[32] = *reinterpret_cast<float(*)[32]>(&x[32]);
-  tmem_ld32(taddr, lo);
-  tmem_ld32(taddr + 32, hi);
-  tmem_ld_wait();
-}
-
-// ---------------------------------------------------------------------------
-// Small tensor-core products for the triangular solve: mma.sync m16n8k8 with
-// tf32 inputs and fp32 accumulation, fragments loaded from row-major fp32
-// tiles of pitch AP (conflict-free for the A fragment since AP = 4 mod 32).
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-
-struct FragA { uint32_t a[4]; };
-struct FragB { uint32_t b[2]; };
-
-// 16 x 8 tile of a row-major matrix at (r0, c0).
-__device__ __forceinline__ FragA load_frag_a(const float* X, int r0, int c0,
-                                             int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  FragA f;
-  f.a[0] = to_tf32(X[(r0 + g) * AP + c0 + t]);
-  f.a[1] = to_tf32(X[(r0 + g + 8) * AP + c0 + t]);
-  f.a[2] = to_tf32(X[(r0 + g) * AP + c0 + t + 4]);
-  f.a[3] = to_tf32(X[(r0 + g + 8) * AP + c0 + t + 4]);
-  return f;
-}
-
-// 8 x 8 tile (k rows, n columns) of a row-major matrix at (k0, n0).
-__device__ __forceinline__ FragB load_frag_b(const float* X, int k0, int n0,
-                                             int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  FragB f;
-  f.b[0] = to_tf32(X[(k0 + t) * AP + n0 + g]);
-  f.b[1] = to_tf32(X[(k0 + t + 4) * AP + n0 + g]);
-  return f;
-}
-
-__device__ __forceinline__ void mma_tf32(float (&c)[4], const FragA& a,
-                                         const FragB& b) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
-      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a.a[0]), "r"(a.a[1]), "r"(a.a[2]), "r"(a.a[3]), "r"(b.b[0]),
-        "r"(b.b[1]));
-}
-
-// Store s * C (16 x 8 accumulator tile) at (r0, c0) of a row-major matrix.
-__device__ __forceinline__ void store_frag_c(float* X, int r0, int c0,
-                                             const float (&c)[4], float s,
-                                             int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  *reinterpret_cast<float2*>(X + (r0 + g) * AP + c0 + 2 * t) =
-      make_float2(s * c[0], s * c[1]);
-  *reinterpret_cast<float2*>(X + (r0 + g + 8) * AP + c0 + 2 * t) =
-      make_float2(s * c[2], s * c[3]);
-}
-
-// D(16 x 16 at (dr, dc)) = s * X(16 x K at (xr, xc)) Y(K x 16 at (yr, yc)).
-template <int K>
-__device__ __forceinline__ void mm16x16(float* D, int dr, int dc, const float* X,
-                                        int xr, int xc, const float* Y, int yr,
-                                        int yc, float s, int lane) {
-  float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int k = 0; k < K; k += 8) {
-    const FragA a = load_frag_a(X, xr, xc + k, lane);
-    mma_tf32(c0, a, load_frag_b(Y, yr + k, yc, lane));
-    mma_tf32(c1, a, load_frag_b(Y, yr + k, yc + 8, lane));
-  }
-  store_frag_c(D, dr, dc, c0, s, lane);
-  store_frag_c(D, dr, dc + 8, c1, s, lane);
-}
-
-// (I + A)^{-1} for the strictly lower 64 x 64 A, in place: on entry AT holds
-// A row-major (zeros on and above the diagonal), on exit its lower triangle
-// holds T with a unit diagonal, and its 16 x 16 blocks above the diagonal
-// blocks are zero except the upper-right 32 x 32 block, which is scratch.
-// Blocked in powers of two: the four 16 x 16 diagonal blocks by substitution,
-// then T_10 = -T_11 A_10 T_00 at 16 and at 32 with the products on the tensor
-// cores (tf32). All 128 prep threads take part.
-__device__ __forceinline__ void solve_unit_lower(float* AT, int tid) {
-  const int warp = tid >> 5, lane = tid & 31;
-  // 1. diagonal 16 x 16 blocks: one per warp, lane l < 16 owns column l,
-  //    x_m = delta_ml - sum_{j<m} A_mj x_j
-  {
-    const int b = 16 * warp;
-    float xs[16];
-    if (lane < 16) {
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const float4* arow = reinterpret_cast<const float4*>(AT + (b + m) * AP + b);
-        float acc = (m == lane) ? 1.f : 0.f;
-#pragma unroll
-        for (int q = 0; q < (m + 3) / 4; ++q) {
-          const float4 a = arow[q];  // one broadcast load for four terms
-          if (4 * q < m) acc = fmaf(-a.x, xs[4 * q], acc);
-          if (4 * q + 1 < m) acc = fmaf(-a.y, xs[4 * q + 1], acc);
-          if (4 * q + 2 < m) acc = fmaf(-a.z, xs[4 * q + 2], acc);
-          if (4 * q + 3 < m) acc = fmaf(-a.w, xs[4 * q + 3], acc);
-        }
-        xs[m] = acc;
-      }
-    }
-    __syncwarp();  // the whole block is read before it is overwritten
-    if (lane < 16) {
-#pragma unroll
-      for (int m = 0; m < 16; ++m) AT[(b + m) * AP + b + lane] = xs[m];
-    }
-  }
-  named_bar(1, 128);
-  // 2. 16 -> 32: warp p in {0, 1} merges diagonal blocks (2p, 2p+1); the
-  //    product X = A_10 T_00 goes to rows 16p.., columns 32+16p.. (scratch)
-  if (warp < 2) {
-    const int kb = 32 * warp, xr = 16 * warp, xc = 32 + 16 * warp;
-    mm16x16<16>(AT, xr, xc, AT, kb + 16, kb, AT, kb, kb, 1.f, lane);
-    __syncwarp();
-    mm16x16<16>(AT, kb + 16, kb, AT, kb + 16, kb + 16, AT, xr, xc, -1.f,
-                lane);
-  }
-  named_bar(1, 128);
-  // 3. 32 -> 64: X = A_21 T_11 into rows 0-31, columns 32-63, then
-  //    T_21 = -T_22 X; warp w owns rows 16 (w >> 1), columns 16 (w & 1)
-  {
-    const int mr = 16 * (warp >> 1), nc = 16 * (warp & 1);
-    mm16x16<32>(AT, mr, 32 + nc, AT, 32 + mr, 0, AT, 0, nc, 1.f, lane);
-    named_bar(1, 128);
-    mm16x16<32>(AT, 32 + mr, nc, AT, 32 + mr, 32, AT, 0, 32 + nc, -1.f, lane);
-  }
-  named_bar(1, 128);
-}
-
-
-
-// Write 32 fp32 values as bf16 into 16-byte chunks 4 hf .. 4 hf + 3 of row r
-// of a 128-byte-row swizzled tile.
-__device__ __forceinline__ void store_half_bf16(uint8_t* tile, int r, int hf,
-                                                const float (&x)[32]) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint4 w;
-    w.x = pack_bf16x2(x[8 * c + 0], x[8 * c + 1]);
-    w.y = pack_bf16x2(x[8 * c + 2], x[8 * c + 3]);
-    w.z = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]);
-    w.w = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
-    *reinterpret_cast<uint4*>(tile + sw128(r, 4 * hf + c)) = w;
-  }
-}
-
-// kN fp32 values as bf16 into 16-byte chunks c0 .. c0 + kN / 8 - 1 of row r
-// of a 128-byte-row swizzled tile.
-template <int kN>
-__device__ __forceinline__ void store_cols_bf16(uint8_t* tile, int r, int c0,
-                                                const float (&x)[kN]) {
-#pragma unroll
-  for (int c = 0; c < kN / 8; ++c) {
-    uint4 w;
-    w.x = pack_bf16x2(x[8 * c + 0], x[8 * c + 1]);
-    w.y = pack_bf16x2(x[8 * c + 2], x[8 * c + 3]);
-    w.z = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]);
-    w.w = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
-    *reinterpret_cast<uint4*>(tile + sw128(r, c0 + c)) = w;
-  }
-}
-
-// As store_half_bf16, scaled by s.
-__device__ __forceinline__ void store_half_bf16_scaled(uint8_t* tile, int r,
-                                                       int hf,
-                                                       const float (&x)[32],
-                                                       float s) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint4 w;
-    w.x = pack_bf16x2(s * x[8 * c + 0], s * x[8 * c + 1]);
-    w.y = pack_bf16x2(s * x[8 * c + 2], s * x[8 * c + 3]);
-    w.z = pack_bf16x2(s * x[8 * c + 4], s * x[8 * c + 5]);
-    w.w = pack_bf16x2(s * x[8 * c + 6], s * x[8 * c + 7]);
-    *reinterpret_cast<uint4*>(tile + sw128(r, 4 * hf + c)) = w;
-  }
-}
-
-// Per-(chunk, head) operands the preparation writes for the chain kernel,
-// each the exact image of a 1024-byte-aligned shared-memory tile (64 rows of
-// 128 bytes, 128-byte swizzle) so that both sides move them with plain bulk
-// copies: -W as two 64-column blocks, P, T_U.
-constexpr uint32_t TILE_BYTES = 8192;
-constexpr uint32_t WS_W_BYTES = 2 * TILE_BYTES;
-constexpr uint32_t WS_P_BYTES = TILE_BYTES;
-constexpr uint32_t WS_TU_BYTES = TILE_BYTES;
 
 // ---------------------------------------------------------------------------
 // ut_prep_kernel: the state-independent part of every (chunk, head).
@@ -1441,7 +1184,10 @@ constexpr uint32_t TX_C_BYTES = 16384 + TILE_BYTES + CV_BYTES;  // K, P, cv
 constexpr uint32_t TXO_OUT = 2 * TX_STAGE;
 constexpr uint32_t TXO_RED = TXO_OUT + 2 * 16384;
 constexpr uint32_t TXO_RS = TXO_RED + 4 * 64 * 4;
-constexpr uint32_t TXO_BAR = TXO_RS + 64 * 4;
+// KDA: each chain warp's 64 values of gamma (per key channel), copied out
+// of the stage before it is released
+constexpr uint32_t TXO_GAM = TXO_RS + 64 * 4;
+constexpr uint32_t TXO_BAR = TXO_GAM + 8 * 64 * 4;
 enum {
   TB_FULLA0, TB_FULLA1, TB_FULLB0, TB_FULLB1, TB_FULLC0, TB_FULLC1,
   TB_EMPTYA0, TB_EMPTYA1, TB_EMPTYB0, TB_EMPTYB1, TB_EMPTYC0, TB_EMPTYC1,
@@ -1451,7 +1197,7 @@ enum {
 };
 constexpr uint32_t TXO_MISC = TXO_BAR + TB_COUNT * 8;
 constexpr uint32_t TX_SMEM = TXO_MISC + 16 + 1024;
-static_assert(TX_CV + CV_BYTES <= TX_STAGE && TX_STAGE % 1024 == 0,
+static_assert(TX_CV + KCV_BYTES <= TX_STAGE && TX_STAGE % 1024 == 0,
               "transposed stage layout");
 static_assert(TX_SMEM <= 232448, "shared memory budget");
 // TMEM columns: two accumulators [U^T -> U^T P^T | H^T] (128 each),
@@ -1508,6 +1254,9 @@ __device__ __forceinline__ void tx_scale_rows(uint8_t* tile, uint32_t blk,
   }
 }
 
+// KDA: per-channel decays (the Q_g / K_d images from the workspace, the
+// state decayed column by column); otherwise the scalar gate.
+template <bool KDA>
 __global__ void __launch_bounds__(kTxThreads, 1)
     chain_tx_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk,
@@ -1590,21 +1339,31 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       const uint8_t* wimg = static_cast<const uint8_t*>(p.wneg);
       const uint8_t* pimg = static_cast<const uint8_t*>(p.pm);
       const uint8_t* uimg = static_cast<const uint8_t*>(p.tu);
+      const uint8_t* qimg = static_cast<const uint8_t*>(p.qg);
+      const uint8_t* kimg = static_cast<const uint8_t*>(p.kd);
+      const bool kda = KDA;
+      const int cvf = kda ? KCV_FLOATS : CV_FLOATS;
+      const uint32_t cvb = kda ? KCV_BYTES : CV_BYTES;
       auto prefetch = [&](int i) {
         const int tok = (int)(bos + (long long)(c_begin + i) * C);
         const size_t tz = (size_t)min((cbase + i) * H + h, tiles - 1);
-        prefetch_l2_3d(&tmk, 0, h, tok);
-        prefetch_l2_3d(&tmk, 64, h, tok);
-        if (emit) {
-          prefetch_l2_3d(&tmq, 0, h, tok);
-          prefetch_l2_3d(&tmq, 64, h, tok);
+        if (kda) {
+          prefetch_l2(kimg + tz * WS_KD_BYTES, WS_KD_BYTES);
+          if (emit) prefetch_l2(qimg + tz * WS_QG_BYTES, WS_QG_BYTES);
+        } else {
+          prefetch_l2_3d(&tmk, 0, h, tok);
+          prefetch_l2_3d(&tmk, 64, h, tok);
+          if (emit) {
+            prefetch_l2_3d(&tmq, 0, h, tok);
+            prefetch_l2_3d(&tmq, 64, h, tok);
+          }
         }
         if (!scale_rows) prefetch_l2_3d(&tmv, 0, h, tok);
         if (!scale_rows && dv > 64) prefetch_l2_3d(&tmv, 64, h, tok);
         prefetch_l2(wimg + tz * WS_W_BYTES, WS_W_BYTES);
         prefetch_l2(pimg + tz * WS_P_BYTES, WS_P_BYTES);
         prefetch_l2(uimg + tz * WS_TU_BYTES, WS_TU_BYTES);
-        prefetch_l2(p.cv + tz * CV_FLOATS, CV_BYTES);
+        prefetch_l2(p.cv + tz * cvf, cvb);
       };
       if (nloc > 0) prefetch(0);
       if (nloc > 1) prefetch(1);
@@ -1630,18 +1389,28 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         bulk_load(st + TX_W, wimg + tz * WS_W_BYTES, TILE_BYTES, fb);
         bulk_load(st + TX_W + TX_WQ_CB, wimg + tz * WS_W_BYTES + TILE_BYTES,
                   TILE_BYTES, fb);
-        tma_load_3d(st + TX_Q, &tmq, fb, 0, h, tok);
-        tma_load_3d(st + TX_Q + TX_WQ_CB, &tmq, fb, 64, h, tok);
+        if (kda) {
+          bulk_load(st + TX_Q, qimg + tz * WS_QG_BYTES, TILE_BYTES, fb);
+          bulk_load(st + TX_Q + TX_WQ_CB, qimg + tz * WS_QG_BYTES + TILE_BYTES,
+                    TILE_BYTES, fb);
+        } else {
+          tma_load_3d(st + TX_Q, &tmq, fb, 0, h, tok);
+          tma_load_3d(st + TX_Q + TX_WQ_CB, &tmq, fb, 64, h, tok);
+        }
         if (i >= 2 && !mbar_wait(&bars[TB_EMPTYC0 + s], ph, abort_flag)) {
           part_groups = 2;  // groups A and B of chunk i are in flight
           break;
         }
         uint64_t* fc = &bars[TB_FULLC0 + s];
-        mbar_arrive_expect_tx(fc, TX_C_BYTES);
-        tma_load_3d(st + TX_K, &tmk, fc, 0, h, tok);
-        tma_load_3d(st + TX_K + 8192, &tmk, fc, 64, h, tok);
+        mbar_arrive_expect_tx(fc, TX_C_BYTES - CV_BYTES + cvb);
+        if (kda) {
+          bulk_load(st + TX_K, kimg + tz * WS_KD_BYTES, WS_KD_BYTES, fc);
+        } else {
+          tma_load_3d(st + TX_K, &tmk, fc, 0, h, tok);
+          tma_load_3d(st + TX_K + 8192, &tmk, fc, 64, h, tok);
+        }
         bulk_load(st + TX_P, pimg + tz * WS_P_BYTES, TILE_BYTES, fc);
-        bulk_load(st + TX_CV, p.cv + tz * CV_FLOATS, CV_BYTES, fc);
+        bulk_load(st + TX_CV, p.cv + tz * cvf, cvb, fc);
         if (i + 2 < nloc) prefetch(i + 2);
         issued = i + 1;
       }
@@ -1789,19 +1558,27 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       if (lane == 0) mbar_arrive(&bars[TB_SREADY]);
     };
     bool ok = true;
+    const bool kda = KDA;
+    float* gv = reinterpret_cast<float*>(sm + TXO_GAM) + 64 * warp;
     put_s();
     for (int i = 0; ok && i < nloc; ++i) {
       const int b = i & 1;
+      const float* cvs = reinterpret_cast<const float*>(sm + b * TX_STAGE + TX_CV);
       ok = __all_sync(0xffffffffu,
                       ok && mbar_wait(&bars[TB_FULLC0 + b], (i >> 1) & 1, abort_flag));
       if (!ok) break;
-      const float gam =
-          reinterpret_cast<const float*>(sm + b * TX_STAGE + TX_CV)[CV_GAMMA];
+      if (kda) {
+        // this warp's half of gamma (per key channel) out of the stage
+        // before it is released; read back in the state update below
+        gv[lane] = cvs[CV_GAMMA + 64 * ch + lane];
+        gv[lane + 32] = cvs[CV_GAMMA + 64 * ch + 32 + lane];
+        __syncwarp();
+      }
+      const float gam = cvs[CV_GAMMA];
       // K -> K_d in place while the [-W;Q] product runs (the stage is
-      // released only after the products that read K_d have completed)
-      tx_scale_rows(sm + b * TX_STAGE + TX_K, 8192,
-                    reinterpret_cast<const float*>(sm + b * TX_STAGE + TX_CV) + CV_DEC,
-                    tid);
+      // released only after the products that read K_d have completed);
+      // KDA's K_d arrives as an image
+      if (!kda) tx_scale_rows(sm + b * TX_STAGE + TX_K, 8192, cvs + CV_DEC, tid);
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[TB_EMPTYC0 + b]);
@@ -1836,12 +1613,22 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         float d[32];
         tmem_ldn<32>(tmem + TX_D2 + lanes + 64 * ch, d);
         tmem_ld_wait();
+        if (kda) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) S[c] = fmaf(gam, S[c], d[c]);
+          for (int c = 0; c < 32; ++c) S[c] = fmaf(gv[c], S[c], d[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) S[c] = fmaf(gam, S[c], d[c]);
+        }
         tmem_ldn<32>(tmem + TX_D2 + lanes + 64 * ch + 32, d);
         tmem_ld_wait();
+        if (kda) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) S[32 + c] = fmaf(gam, S[32 + c], d[c]);
+          for (int c = 0; c < 32; ++c) S[32 + c] = fmaf(gv[32 + c], S[32 + c], d[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) S[32 + c] = fmaf(gam, S[32 + c], d[c]);
+        }
       }
       put_s();
     }
@@ -2211,7 +1998,9 @@ long long chunk_tc_chunks_bound(const ChunkParams& p) {
 
 size_t chunk_tc_workspace_bytes(const ChunkParams& p) {
   const size_t tiles = (size_t)chunk_tc_chunks_bound(p) * p.H;
-  size_t bytes = tiles * (WS_W_BYTES + WS_P_BYTES + WS_TU_BYTES + CV_BYTES);
+  size_t bytes = tiles * (WS_W_BYTES + WS_P_BYTES + WS_TU_BYTES +
+                          (p.kda ? KCV_BYTES + WS_QG_BYTES + WS_KD_BYTES
+                                 : CV_BYTES));
   if (p.cu_seqlens) bytes += ((size_t)p.N + 1) * sizeof(int32_t) + 256;
   return bytes;
 }
@@ -2226,23 +2015,35 @@ void chunk_tc_bind_workspace(ChunkParams& p, void* ws) {
   p.tu = c;
   c += tiles * WS_TU_BYTES;
   p.cv = reinterpret_cast<float*>(c);
-  c += tiles * CV_BYTES;
+  c += tiles * (p.kda ? KCV_BYTES : CV_BYTES);
+  if (p.kda) {
+    p.qg = c;
+    c += tiles * WS_QG_BYTES;
+    p.kd = c;
+    c += tiles * WS_KD_BYTES;
+  }
   p.chunk_off = p.cu_seqlens ? reinterpret_cast<int32_t*>(c) : nullptr;
+}
+
+// Chunk offsets of packed calls (nothing for dense ones).
+cudaError_t launch_chunk_offsets(const ChunkParams& p, cudaStream_t stream,
+                                 int* launches) {
+  *launches = 0;
+  if (!p.cu_seqlens) return cudaSuccess;
+  const int t = timing_start(GDN_KERNEL_CHUNK_OFFSETS, stream);
+  chunk_offsets_kernel<<<1, 1024, 0, stream>>>(
+      p.cu_seqlens, p.N, p.T, const_cast<int32_t*>(p.chunk_off), p.status);
+  cudaError_t e = cudaGetLastError();
+  timing_stop(t, stream, e);
+  if (e == cudaSuccess) ++*launches;
+  return e;
 }
 
 // Chunk offsets (packed calls) and the preparation of every chunk.
 cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
                            int* launches) {
-  *launches = 0;
-  if (p.cu_seqlens) {
-    const int t = timing_start(GDN_KERNEL_CHUNK_OFFSETS, stream);
-    chunk_offsets_kernel<<<1, 1024, 0, stream>>>(
-        p.cu_seqlens, p.N, p.T, const_cast<int32_t*>(p.chunk_off), p.status);
-    cudaError_t e = cudaGetLastError();
-    timing_stop(t, stream, e);
-    if (e != cudaSuccess) return e;
-    ++*launches;
-  }
+  cudaError_t e0 = launch_chunk_offsets(p, stream, launches);
+  if (e0 != cudaSuccess) return e0;
   CUtensorMap mk, mq;
   if (!make_map(&mk, p.k, p.dk, p.H, call_tokens(p), 1, 64) ||
       !make_map(&mq, p.q, p.dk, p.H, call_tokens(p), 1, 64))
@@ -2284,9 +2085,9 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream) {
   if (p.chain_rows == TXR) {
     // one CTA per 128 state rows: the value rows, and in a split pass the
     // rows of the scaling matrix
+    auto kern = p.kda ? chain_tx_kernel<true> : chain_tx_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(
-        chain_tx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        (int)TX_SMEM);
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TX_SMEM);
     if (e != cudaSuccess) return e;
     const int blocks = p.mode == kModeSplit ? 2 : 1;
     const int t = timing_start(GDN_KERNEL_CHUNK_CHAIN_WHOLE, stream);
@@ -2300,7 +2101,7 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, chain_tx_kernel, p, mq, mk, mv, mo, mg, nchd,
+    e = cudaLaunchKernelEx(&cfg, kern, p, mq, mk, mv, mo, mg, nchd,
                            (int)tiles);
     if (e == cudaSuccess) e = cudaGetLastError();
     timing_stop(t, stream, e);

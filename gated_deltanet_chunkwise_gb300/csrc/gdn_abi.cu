@@ -176,7 +176,8 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
               const float* beta, const float* h0, void* out, float* hT,
               const int32_t* cu_seqlens, int B, int H, int T, int dk, int dv,
               int C, int dtype, int variant, int path, int sp_parts,
-              cudaStream_t stream, const Sublayer& sub = Sublayer{}) {
+              cudaStream_t stream, const Sublayer& sub = Sublayer{},
+              bool kda = false) {
   // combination of sub-sequences (flags above the path)
   const int sp_mode = path & (GDN_SP_CHAIN | GDN_SP_SCAN);
   if ((path & ~0xFF & ~(GDN_SP_CHAIN | GDN_SP_SCAN)) != 0 ||
@@ -197,6 +198,14 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
     if (sub.gate && sub.gate == out) return GDN_ERR_INVALID_ARG;
   }
   if (B == 0 || H == 0) return GDN_OK;
+  const bool bf16 = dtype == GDN_DTYPE_BF16;
+  const long long tokens = cu_seqlens ? (long long)T : (long long)B * T;
+  const bool tc_ok = bf16 && chunk_tc_supported(dk, dv, tokens, B, H);
+  if ((path >= GDN_PATH_TCGEN05 || sub.on || kda) && !tc_ok)
+    return GDN_ERR_UNSUPPORTED;
+  // KDA runs on the whole-state chain only (its column-wise state decay)
+  if (kda && (path == GDN_PATH_SIMT || path == GDN_PATH_TCGEN05_SPLIT))
+    return GDN_ERR_UNSUPPORTED;
   int* status = nullptr;
   if ((rc = current_status_ptr(&status)) != GDN_OK) return rc;
 
@@ -206,11 +215,8 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
   p.N = B; p.H = H; p.T = T; p.dk = dk; p.dv = dv; p.C = C;
   p.variant = variant;
   p.status = status;
-  const bool bf16 = dtype == GDN_DTYPE_BF16;
-  const long long tokens = cu_seqlens ? (long long)T : (long long)B * T;
-  const bool tc_ok = bf16 && chunk_tc_supported(dk, dv, tokens, B, H);
-  if ((path >= GDN_PATH_TCGEN05 || sub.on) && !tc_ok) return GDN_ERR_UNSUPPORTED;
   const bool use_tc = tc_ok && path != GDN_PATH_SIMT;
+  p.kda = kda ? 1 : 0;
   if (sub.on) {
     p.prologue = 1;
     p.epilogue = (sub.norm_w || sub.gate) ? 1 : 0;
@@ -224,8 +230,8 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
   };
   int parts = 1;
   if (use_tc)
-    choose_chain_tc(path, sp_parts, B, H, T, dv, C, cu_seqlens != nullptr,
-                    &p.chain_rows, &parts);
+    choose_chain_tc(kda ? GDN_PATH_TCGEN05_WHOLE : path, sp_parts, B, H, T,
+                    dv, C, cu_seqlens != nullptr, &p.chain_rows, &parts);
   else
     parts = choose_parts(sp_parts, B, H, T, dv, C, cu_seqlens != nullptr);
   p.parts = parts;
@@ -278,7 +284,8 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
   cudaError_t e = cudaSuccess;
   if (use_tc) {
     int n_prep = 0;
-    e = launch_ut_prep(p, stream, &n_prep);
+    e = kda ? launch_kda_prep(p, stream, &n_prep)
+            : launch_ut_prep(p, stream, &n_prep);
     counted(e, n_prep);
   }
   if (e == cudaSuccess) {
@@ -495,6 +502,30 @@ int gdn_kda_fwd(const void* q, const void* k, const void* v, const float* g,
   return gdn::counted(gdn::launch_kda(p, stream), 1) == cudaSuccess
              ? GDN_OK
              : GDN_ERR_CUDA;
+}
+
+int gdn_kda_fwd_ex(const void* q, const void* k, const void* v,
+                   const float* g, const float* beta, const float* h0,
+                   void* out, float* hT, const int32_t* cu_seqlens, int B,
+                   int H, int T, int dk, int dv, int path, int sp_parts,
+                   gdn_stream_t stream) {
+  const int sp_mode = path & (GDN_SP_CHAIN | GDN_SP_SCAN);
+  const int kernels = path & ~(GDN_SP_CHAIN | GDN_SP_SCAN);
+  if (kernels < GDN_PATH_AUTO || kernels > GDN_PATH_TCGEN05_WHOLE)
+    return GDN_ERR_INVALID_ARG;
+  if (kernels == GDN_PATH_TCGEN05_SPLIT) return GDN_ERR_UNSUPPORTED;
+  const long long tokens = cu_seqlens ? (long long)T : (long long)B * T;
+  // nothing to compute but the state copy: the token-by-token kernel
+  if (kernels == GDN_PATH_SIMT || B <= 0 || H <= 0 || T <= 0 || tokens <= 0 ||
+      (kernels == GDN_PATH_AUTO &&
+       !gdn::chunk_tc_supported(dk, dv, tokens, B, H)))
+    return gdn_kda_fwd(q, k, v, g, beta, h0, out, hT, cu_seqlens, B, H, T, dk,
+                       dv, stream);
+  return gdn::run_chunk(q, k, v, g, beta, h0, out, hT, cu_seqlens, B, H, T, dk,
+                        dv, 64, GDN_DTYPE_BF16, GDN_GATE_BEFORE_PREDICT,
+                        (kernels == GDN_PATH_AUTO ? GDN_PATH_TCGEN05 : kernels) |
+                            sp_mode,
+                        sp_parts, stream, gdn::Sublayer{}, true);
 }
 
 int gdn_device_status(gdn_stream_t stream) {

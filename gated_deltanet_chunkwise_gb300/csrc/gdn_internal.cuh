@@ -53,6 +53,13 @@ struct ChunkParams {
   void* pm;                  // [chunks, H, 64, 64] bf16, (Q K^T) (.) D (.) M
   void* tu;                  // [chunks, H, 64, 64] bf16, T diag(beta)
   float* cv;                 // [chunks, H, 132] fp32, e^G, e^{G_L-G}, gamma
+                             // (KDA: [chunks, H, 256], gamma per key channel)
+  // KDA (gdn_kda_fwd_ex on the tensor-core path): per-channel decays, so the
+  // preparation also writes Q_g = Q (.) e^G and K_d = K (.) e^{G_L - G} as
+  // bf16 tile images, and the chain decays the state column by column
+  int kda;
+  void* qg;                  // [chunks, H, 64, dk] bf16
+  void* kd;                  // [chunks, H, 64, dk] bf16
   // steps either side of the recurrence (gdn_chunk_fwd_fused; tensor-core
   // path only): with `prologue` set, q and k are raw (normalised in the
   // kernels), g holds the gate logits a (g = -softplus(a)) and beta the step
@@ -110,6 +117,15 @@ size_t chunk_tc_workspace_bytes(const ChunkParams& p);
 void chunk_tc_bind_workspace(ChunkParams& p, void* ws);
 cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
                            int* launches);
+// Chunk offsets of a packed call (part of launch_ut_prep / launch_kda_prep).
+cudaError_t launch_chunk_offsets(const ChunkParams& p, cudaStream_t stream,
+                                 int* launches);
+// KDA on the tensor-core path (p.kda set; workspace bound as above): the
+// preparation of every (chunk, head), then launch_chunk_tc with 128 rows.
+cudaError_t launch_kda_prep(const ChunkParams& p, cudaStream_t stream,
+                            int* launches);
+long long chunk_tc_chunks_bound(const ChunkParams& p);
+int chunk_tc_nch_dense(const ChunkParams& p);
 cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_kda(const KdaParams& p, cudaStream_t stream);

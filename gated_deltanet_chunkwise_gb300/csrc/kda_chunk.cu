@@ -1,0 +1,493 @@
+// Chunked KDA (per-channel decay) for the tensor-core chain: the preparation
+// of every (chunk, head).
+//
+// Illustrated DeltaNet walk-through: the KDA paragraphs of its
+// hybrid-architecture section give the recurrence
+//   S_t = S_{t-1} diag(e^{g_t}) (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+//   o_t = S_t q_t,
+// its UT transform and WY sections the chunk form, and its GLA section the
+// per-channel cumulative gates with the rescaling over 16-token sub-chunks.
+// With Gamma_t = sum_{s <= t} g_s the chunk-local cumulative log-decay (a
+// vector over the key channels; the decay of token t acts before its
+// prediction) one chunk of C = 64 tokens from the state S_0 is
+//   A_rs = beta_r sum_c k_rc k_sc e^{Gamma_rc - Gamma_sc}      (s < r)
+//   P_rs = sum_c q_rc k_sc e^{Gamma_rc - Gamma_sc}             (s <= r)
+//   T = (I + A)^{-1},  T_U = T diag(beta),  W = T_U (K (.) e^Gamma)
+//   U = T_U V - W S_0^T,   O = (Q (.) e^Gamma) S_0^T + P U
+//   S_C = S_0 diag(e^{Gamma_L}) + U^T (K (.) e^{Gamma_L - Gamma})
+// (Gamma_L: the chunk's last token). That is the scalar-gate chunk form with
+// Q_g = Q (.) e^Gamma, K_d = K (.) e^{Gamma_L - Gamma} and a decay vector
+// gamma = e^{Gamma_L}, so the whole-state chain kernel runs it unchanged but
+// for the column-wise decay of the state; this kernel writes -W, P, T_U, Q_g
+// and K_d as bf16 tile images and e^{Gamma_L} as the chunk's decay record.
+//
+// A and P need e^{Gamma_r - Gamma_s} channel by channel. With b(t) the first
+// token of t's 16-token block the kernel factors it as
+//   e^{Gamma_r - Gamma_b(r)}  x  e^{Gamma_b(r) - Gamma_b(s)}  x  e^{Gamma_b(s) - Gamma_s}
+// (left table K_E = K (.) e^{Gamma - Gamma_b}, Q_E likewise, right table
+// K_B = K (.) e^{Gamma_b - Gamma}, one vector per pair of blocks), so every
+// block of A and P is one bf16 tensor-core product over d_k. All factors but
+// the right table's lie in (0, 1] for decays (g <= 0); the right table grows
+// by at most the decay across one block. A chunk in which some channel decays
+// by more than 2^120 across one block (or grows by that much between two)
+// takes the exact pairwise sum instead (one exp per term; slow, but only for
+// such chunks).
+//
+// One CTA of 256 threads per (chunk, head) at a time, two CTAs per SM; plain
+// loads in (the rows are 256 / 512 contiguous bytes), tensor-core products
+// with mma.sync m16n8k16 (bf16 in, fp32 accumulate) from ldmatrix fragments,
+// the inverse by the blocked substitution shared with the scalar-gate
+// preparation, images out by bulk copies (P, T_U, -W) or direct stores (Q_g,
+// K_d: each thread owns one key channel).
+#include "chunk_tiles.cuh"
+
+namespace gdn {
+namespace {
+using namespace tc;
+
+constexpr int kKpThreads = 256;
+constexpr int kKpCtas = 2;
+// bf16 operand tables, 64 rows of 136 values (the 16-byte pad makes the
+// eight rows of an ldmatrix tile hit distinct banks)
+constexpr int KP_PITCH = 272;
+constexpr uint32_t KP_TAB = 64 * KP_PITCH;
+constexpr uint32_t KP_KE = 0, KP_QE = KP_TAB, KP_KB = 2 * KP_TAB,
+                   KP_KG = 3 * KP_TAB;
+// exact fallback: Gamma in fp32 over K_E / Q_E, raw K in the K_B table
+constexpr int GP = 132;
+constexpr uint32_t KP_GAM = 0;
+// -W image after the solve, over K_E / Q_E
+constexpr uint32_t KP_W = 0;
+constexpr uint32_t KP_AT = 4 * KP_TAB;             // fp32 A, then T (pitch AP)
+constexpr uint32_t KP_P = KP_AT + 64 * AP * 4;     // P image
+constexpr uint32_t KP_TU = KP_P + TILE_BYTES;      // T_U image
+constexpr uint32_t KP_V = KP_TU + TILE_BYTES;      // 6 pair vectors x 128
+constexpr uint32_t KP_GB = KP_V + 6 * DK * 4;      // Gamma at the 4 block starts
+constexpr uint32_t KP_HT = KP_GB + 4 * DK * 4;     // first-half totals
+constexpr uint32_t KP_GL = KP_HT + DK * 4;         // Gamma_L
+constexpr uint32_t KP_BETA = KP_GL + DK * 4;       // beta (0 past the end)
+constexpr uint32_t KP_SMEM = KP_BETA + 64 * 4 + 1024;
+static_assert(64 * GP * 4 <= KP_KB, "Gamma table overlaps the raw K table");
+static_assert(2 * WS_W_BYTES <= KP_KB, "-W image overlaps K_G");
+static_assert(KP_P % 1024 == 0 && KP_TU % 1024 == 0, "image alignment");
+static_assert(kKpCtas * (KP_SMEM + 1024) <= 233472, "two CTAs per SM");
+// largest |log2 factor| a table entry may carry
+constexpr float kSpanLimit = 120.f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(addr)
+      : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(addr)
+      : "memory");
+}
+// c += a b (m16n8k16, bf16 inputs, fp32 accumulators)
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4],
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t u, float2 s) {
+  const float lo = __uint_as_float(u << 16), hi = __uint_as_float(u & 0xffff0000u);
+  return pack_bf16x2(lo * s.x, hi * s.y);
+}
+__device__ __forceinline__ float bf16_bits(uint32_t b) {
+  return __uint_as_float(b << 16);
+}
+__device__ __forceinline__ void st_bf16(uint8_t* p, float v) {
+  *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
+}
+
+__global__ void __launch_bounds__(kKpThreads, kKpCtas)
+    kda_prep_kernel(const ChunkParams p, int nch_dense, int total_chunks_bound) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = p.H;
+  // an invalid packing (already recorded as GDN_ERR_INVALID_ARG) can count
+  // more chunks than the workspace holds: never write past it
+  const int total_chunks =
+      p.chunk_off ? min(p.chunk_off[p.N], total_chunks_bound) : total_chunks_bound;
+  const int items = total_chunks * H;
+  // the chain kernel behind this one may be scheduled from here on; it waits
+  // for this grid to complete before it reads the images
+  griddep_launch_dependents();
+
+  float* AT = reinterpret_cast<float*>(sm + KP_AT);
+  float* vpair = reinterpret_cast<float*>(sm + KP_V);
+  float* gbs = reinterpret_cast<float*>(sm + KP_GB);
+  float* htot = reinterpret_cast<float*>(sm + KP_HT);
+  float* gend = reinterpret_cast<float*>(sm + KP_GL);
+  float* bet = reinterpret_cast<float*>(sm + KP_BETA);
+  const uint16_t* kin = static_cast<const uint16_t*>(p.k);
+  const uint16_t* qin = static_cast<const uint16_t*>(p.q);
+
+  auto chunk_of = [&](int it, int& h, long long& t0, int& len) {
+    const int cidx = it / H;
+    h = it - cidx * H;
+    int n, lc;
+    locate_chunk(p, cidx, nch_dense, n, lc);
+    long long bos, eos;
+    if (!sequence_range(p, n, bos, eos)) bos = eos = 0;
+    t0 = bos + (long long)lc * C;
+    len = (int)max(0ll, min((long long)C, eos - t0));
+  };
+
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    int h, len;
+    long long t0;
+    chunk_of(it, h, t0, len);
+    // the CTA's next item into L2 while this one is processed: its rows of
+    // g (512 bytes), k and q (256 bytes each)
+    if (warp == 7 && it + (int)gridDim.x < items) {
+      int h2, len2;
+      long long t2;
+      chunk_of(it + gridDim.x, h2, t2, len2);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int t = lane + 32 * hf;
+        if (t < len2) {
+          const size_t e = ((size_t)(t2 + t) * H + h2) * DK;
+          prefetch_l2(p.g + e, DK * 4);
+          prefetch_l2(kin + e, DK * 2);
+          prefetch_l2(qin + e, DK * 2);
+        }
+      }
+    }
+    // the previous item's bulk copies have read their images
+    if (tid == 0) bulk_wait_read();
+    __syncthreads();
+
+    // ---- 1. cumulative log2-decay of key channel c over the chunk --------
+    const int c = tid & 127, hh = tid >> 7;  // tokens 32 hh .. 32 hh + 31
+    float x[32];
+    uint32_t kq[32];  // raw k (low 16 bits) and q (high 16 bits)
+    {
+      const size_t row0 = ((size_t)(t0 + 32 * hh)) * H + h;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float gv = 0.f;
+        uint32_t kb = 0, qb = 0;
+        if (32 * hh + j < len) {
+          const size_t e = (row0 + (size_t)j * H) * DK + c;
+          gv = __ldg(p.g + e);
+          kb = __ldg(kin + e);
+          qb = __ldg(qin + e);
+        }
+        x[j] = gv * kLog2e;
+        kq[j] = kb | (qb << 16);
+      }
+    }
+#pragma unroll
+    for (int j = 1; j < 32; ++j) x[j] += x[j - 1];
+    if (hh == 0) htot[c] = x[31];
+    if (tid < 64) bet[tid] = tid < len ? __ldg(p.beta + ((size_t)(t0 + tid) * H + h)) : 0.f;
+    __syncthreads();
+    if (hh == 1) {
+      const float o = htot[c];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] += o;
+      gend[c] = x[31];
+    }
+    gbs[(2 * hh) * DK + c] = x[0];
+    gbs[(2 * hh + 1) * DK + c] = x[16];
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) bad |= fabsf(x[j] - x[j & 16]) > kSpanLimit;
+    __syncthreads();
+    const float xl = gend[c];
+    // e^{Gamma_b(R) - Gamma_b(S)} for the block pairs S < R:
+    // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+#pragma unroll
+    for (int m = 0; m < 3; ++m) {
+      const int idx = tid + kKpThreads * m, pr = idx >> 7, ch = idx & 127;
+      const int R = pr < 1 ? 1 : (pr < 3 ? 2 : 3);
+      const int S = pr - R * (R - 1) / 2;
+      const float e = gbs[R * DK + ch] - gbs[S * DK + ch];
+      bad |= e > kSpanLimit;
+      vpair[pr * DK + ch] = exp2f(e);
+    }
+    const bool exact = __syncthreads_or(bad) != 0;
+
+    // ---- 2. operand tables, the Q_g / K_d images, the decay record -------
+    {
+      float* cv = p.cv + (size_t)it * KCV_FLOATS;
+      // e^G = 1 for the chain's read-out (the decay is inside Q_g)
+      if (hh == 0) cv[c] = 1.f;
+      else cv[CV_GAMMA + c] = exp2f(xl);
+      uint8_t* qimg = static_cast<uint8_t*>(p.qg) + (size_t)it * WS_QG_BYTES;
+      uint8_t* kimg = static_cast<uint8_t*>(p.kd) + (size_t)it * WS_KD_BYTES;
+      const uint32_t cblk = (uint32_t)((c >> 6) * TILE_BYTES) + (c & 7) * 2;
+      const int cchunk = (c & 63) >> 3;
+      float* gam = reinterpret_cast<float*>(sm + KP_GAM);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int t = 32 * hh + j;
+        const float kv = bf16_bits(kq[j] & 0xffffu), qv = bf16_bits(kq[j] >> 16);
+        const float eg = exp2f(x[j]), ed = exp2f(xl - x[j]);
+        const uint32_t off = cblk + sw128(t, cchunk);
+        st_bf16(qimg + off, qv * eg);
+        st_bf16(kimg + off, kv * ed);
+        st_bf16(sm + KP_KG + t * KP_PITCH + c * 2, kv * eg);
+        if (!exact) {
+          const float e = x[j] - x[j & 16];
+          const float E = exp2f(e), Ei = exp2f(-e);
+          st_bf16(sm + KP_KE + t * KP_PITCH + c * 2, kv * E);
+          st_bf16(sm + KP_QE + t * KP_PITCH + c * 2, qv * E);
+          st_bf16(sm + KP_KB + t * KP_PITCH + c * 2, kv * Ei);
+        } else {
+          gam[t * GP + c] = x[j];
+          *reinterpret_cast<uint16_t*>(sm + KP_KB + t * KP_PITCH + c * 2) =
+              (uint16_t)(kq[j] & 0xffffu);
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- 3. A and P, one warp per (matrix, 16-row block R) ---------------
+    {
+      const int mat = warp >> 2, R = warp & 3;  // mat 0: A, 1: P
+      const int g = lane >> 2, t4 = lane & 3;
+      const int r0 = 16 * R + g, r1 = r0 + 8;
+      uint8_t* pimg = sm + KP_P;
+      float acc[2][4];
+      // block (R, S) out of the accumulators: A (times beta_r, s < r) into
+      // the solve buffer, P (s <= r) into its bf16 image
+      auto put_block = [&](int S) {
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          const int s = 16 * S + 8 * n + 2 * t4;
+          if (mat == 0) {
+            const float b0 = bet[r0], b1 = bet[r1];
+            *reinterpret_cast<float2*>(AT + r0 * AP + s) =
+                make_float2(s < r0 ? b0 * acc[n][0] : 0.f,
+                            s + 1 < r0 ? b0 * acc[n][1] : 0.f);
+            *reinterpret_cast<float2*>(AT + r1 * AP + s) =
+                make_float2(s < r1 ? b1 * acc[n][2] : 0.f,
+                            s + 1 < r1 ? b1 * acc[n][3] : 0.f);
+          } else {
+            *reinterpret_cast<uint32_t*>(pimg + sw128(r0, s >> 3) + (s & 7) * 2) =
+                pack_bf16x2(s <= r0 ? acc[n][0] : 0.f, s + 1 <= r0 ? acc[n][1] : 0.f);
+            *reinterpret_cast<uint32_t*>(pimg + sw128(r1, s >> 3) + (s & 7) * 2) =
+                pack_bf16x2(s <= r1 ? acc[n][2] : 0.f, s + 1 <= r1 ? acc[n][3] : 0.f);
+          }
+        }
+      };
+      if (!exact) {
+        // left fragments of rows 16 R.. (K_E or Q_E), all of d_k
+        uint32_t a[8][4];
+        const uint32_t tab = base + (mat ? KP_QE : KP_KE);
+        const int ar = 16 * R + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ldsm_x4(tab + ar * KP_PITCH + (16 * kk + (lane >> 4) * 8) * 2, a[kk]);
+        const int br = (lane & 7) + (lane >> 4) * 8, bc = ((lane >> 3) & 1) * 8;
+        for (int S = 0; S <= R; ++S) {
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+          const float* vp = vpair + (R * (R - 1) / 2 + S) * DK;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // right fragments: rows 16 S.. of K_B (two 8-row n tiles),
+            // times the pair vector off the diagonal
+            uint32_t b[4];
+            ldsm_x4(base + KP_KB + (16 * S + br) * KP_PITCH + (16 * kk + bc) * 2, b);
+            if (S < R) {
+              const float2 v0 = *reinterpret_cast<const float2*>(vp + 16 * kk + 2 * t4);
+              const float2 v1 = *reinterpret_cast<const float2*>(vp + 16 * kk + 2 * t4 + 8);
+              b[0] = scale_bf16x2(b[0], v0);
+              b[1] = scale_bf16x2(b[1], v1);
+              b[2] = scale_bf16x2(b[2], v0);
+              b[3] = scale_bf16x2(b[3], v1);
+            }
+            mma16816(acc[0], a[kk], b[0], b[1]);
+            mma16816(acc[1], a[kk], b[2], b[3]);
+          }
+          put_block(S);
+        }
+      } else {
+        // exact sum: each lane's 8 entries of the block, channel by channel
+        const float* gam = reinterpret_cast<const float*>(sm + KP_GAM);
+        const uint16_t* kraw = reinterpret_cast<const uint16_t*>(sm + KP_KB);
+        const int kp = KP_PITCH / 2;
+        for (int S = 0; S <= R; ++S) {
+#pragma unroll
+          for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+          for (int ch = 0; ch < DK; ++ch) {
+            const float gr0 = gam[r0 * GP + ch], gr1 = gam[r1 * GP + ch];
+            float x0, x1;
+            if (mat == 0) {
+              x0 = bf16_bits(kraw[r0 * kp + ch]);
+              x1 = bf16_bits(kraw[r1 * kp + ch]);
+            } else {
+              x0 = r0 < len ? bf16_bits(__ldg(qin + ((size_t)(t0 + r0) * H + h) * DK + ch)) : 0.f;
+              x1 = r1 < len ? bf16_bits(__ldg(qin + ((size_t)(t0 + r1) * H + h) * DK + ch)) : 0.f;
+            }
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int s = 16 * S + 8 * n + 2 * t4 + e;
+                const float ks = bf16_bits(kraw[s * kp + ch]), gs = gam[s * GP + ch];
+                acc[n][e] = fmaf(x0 * ks, exp2f(gr0 - gs), acc[n][e]);
+                acc[n][2 + e] = fmaf(x1 * ks, exp2f(gr1 - gs), acc[n][2 + e]);
+              }
+          }
+          put_block(S);
+        }
+      }
+      // blocks above the diagonal are zero
+      for (int S = R + 1; S < 4; ++S) {
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+        put_block(S);
+      }
+      fence_proxy_async();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      bulk_store(static_cast<uint8_t*>(p.pm) + (size_t)it * WS_P_BYTES, sm + KP_P,
+                 TILE_BYTES);
+      bulk_commit();
+    }
+
+    // ---- 4. T = (I + A)^{-1}; T_U = T diag(beta) -------------------------
+    if (warp < 4) solve_unit_lower(AT, tid);
+    __syncthreads();
+    {
+      const int r = tid >> 2, q4 = tid & 3;  // row r, columns 16 q4 ..
+      float tv[16];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const float4 v = *reinterpret_cast<const float4*>(AT + r * AP + 16 * q4 + 4 * c4);
+        tv[4 * c4] = v.x; tv[4 * c4 + 1] = v.y; tv[4 * c4 + 2] = v.z; tv[4 * c4 + 3] = v.w;
+      }
+      uint8_t* tu = sm + KP_TU;
+#pragma unroll
+      for (int h8 = 0; h8 < 2; ++h8) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int col = 16 * q4 + 8 * h8 + e;
+          const float t = col < r ? tv[8 * h8 + e] : (col == r ? 1.f : 0.f);
+          y[e] = t * bet[col];
+        }
+        uint4 w;
+        w.x = pack_bf16x2(y[0], y[1]);
+        w.y = pack_bf16x2(y[2], y[3]);
+        w.z = pack_bf16x2(y[4], y[5]);
+        w.w = pack_bf16x2(y[6], y[7]);
+        *reinterpret_cast<uint4*>(tu + sw128(r, 2 * q4 + h8)) = w;
+      }
+      fence_proxy_async();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      bulk_store(static_cast<uint8_t*>(p.tu) + (size_t)it * WS_TU_BYTES, sm + KP_TU,
+                 TILE_BYTES);
+      bulk_commit();
+    }
+
+    // ---- 5. W = T_U K_G; -W image ----------------------------------------
+    {
+      const int R = warp & 3, nh = warp >> 2;  // rows 16 R.., columns 64 nh..
+      const int g = lane >> 2, t4 = lane & 3;
+      uint32_t a[4][4];
+      const int ar = 16 * R + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        ldsm_x4(base + KP_TU + sw128(ar, 2 * kk + (lane >> 4)), a[kk]);
+      float acc[8][4];
+#pragma unroll
+      for (int n = 0; n < 8; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+      const int br = (lane & 7) + ((lane >> 3) & 1) * 8, bc = (lane >> 4) * 8;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+          uint32_t b[4];
+          ldsm_x4_t(base + KP_KG + (16 * kk + br) * KP_PITCH +
+                        (64 * nh + 16 * np + bc) * 2,
+                    b);
+          mma16816(acc[2 * np], a[kk], b[0], b[1]);
+          mma16816(acc[2 * np + 1], a[kk], b[2], b[3]);
+        }
+      }
+      uint8_t* wimg = sm + KP_W + nh * TILE_BYTES;
+      const int r0 = 16 * R + g, r1 = r0 + 8;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        const int cc = 8 * n + 2 * t4;
+        *reinterpret_cast<uint32_t*>(wimg + sw128(r0, cc >> 3) + (cc & 7) * 2) =
+            pack_bf16x2(-acc[n][0], -acc[n][1]);
+        *reinterpret_cast<uint32_t*>(wimg + sw128(r1, cc >> 3) + (cc & 7) * 2) =
+            pack_bf16x2(-acc[n][2], -acc[n][3]);
+      }
+      fence_proxy_async();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      bulk_store(static_cast<uint8_t*>(p.wneg) + (size_t)it * WS_W_BYTES, sm + KP_W,
+                 WS_W_BYTES);
+      bulk_commit();
+    }
+  }
+  if (tid == 0) bulk_wait_all();
+}
+
+int sm_count_kp() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
+          cudaSuccess &&
+      v > 0)
+    return v;
+  return 148;
+}
+
+}  // namespace
+
+cudaError_t launch_kda_prep(const ChunkParams& p, cudaStream_t stream,
+                            int* launches) {
+  cudaError_t e = launch_chunk_offsets(p, stream, launches);
+  if (e != cudaSuccess) return e;
+  const long long bound = chunk_tc_chunks_bound(p);
+  const long long items = bound * p.H;
+  if (items <= 0) return cudaSuccess;
+  const int grid =
+      (int)std::min<long long>(items, (long long)kKpCtas * sm_count_kp());
+  e = cudaFuncSetAttribute(kda_prep_kernel,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)KP_SMEM);
+  if (e != cudaSuccess) return e;
+  const int t = timing_start(GDN_KERNEL_KDA_PREP, stream);
+  kda_prep_kernel<<<grid, kKpThreads, KP_SMEM, stream>>>(
+      p, chunk_tc_nch_dense(p), (int)bound);
+  e = cudaGetLastError();
+  timing_stop(t, stream, e);
+  if (e == cudaSuccess) ++*launches;
+  return e;
+}
+
+}  // namespace gdn

@@ -216,6 +216,35 @@ int gdn_kda_fwd(const void* q, const void* k, const void* v, const float* g,
                 gdn_stream_t stream);
 
 /*
+ * gdn_kda_fwd_ex -- gdn_kda_fwd with a choice of kernels. Arguments and
+ * results as for gdn_kda_fwd, plus:
+ *   path      GDN_PATH_SIMT: the token-by-token kernel of gdn_kda_fwd.
+ *             GDN_PATH_TCGEN05 (or GDN_PATH_TCGEN05_WHOLE): the chunk form
+ *             on the tensor cores (walk-through: UT transform and WY
+ *             sections with the per-channel gates of the GLA section;
+ *             chunks of 64 tokens, bf16 operands, fp32 state and
+ *             accumulation), dk = 128 and dv in {64, 128} only (otherwise
+ *             GDN_ERR_UNSUPPORTED). Inside a chunk the decay of token r
+ *             relative to token s is factored through 16-token blocks; a
+ *             chunk in which some channel decays by more than 2^120 within
+ *             one such block takes an exact pairwise sum instead (slower,
+ *             same result).
+ *             GDN_PATH_AUTO: the chunk form where it applies (at least one
+ *             token, dk = 128, dv in {64, 128}), else the token-by-token
+ *             kernel. GDN_PATH_TCGEN05_SPLIT: GDN_ERR_UNSUPPORTED.
+ *             GDN_SP_CHAIN / GDN_SP_SCAN may be or-ed in as for
+ *             gdn_chunk_fwd_ex.
+ *   sp_parts  sequence-parallel split of the chunk form as for
+ *             gdn_chunk_fwd_ex (0: automatic); ignored by GDN_PATH_SIMT.
+ * The chunk form allocates its workspace with cudaMallocAsync on `stream`
+ * (about 65 KB per chunk and head).
+ */
+int gdn_kda_fwd_ex(const void* q, const void* k, const void* v, const float* g,
+                   const float* beta, const float* h0, void* out, float* hT,
+                   const int32_t* cu_seqlens, int B, int H, int T, int dk,
+                   int dv, int path, int sp_parts, gdn_stream_t stream);
+
+/*
  * gdn_chunk_fwd_sp_noalloc -- the sequence-parallel forward pass of
  * gdn_chunk_fwd_ex (path GDN_PATH_SIMT, sp_parts >= 2) for callers that may
  * not allocate device memory while they enqueue work (for example a plugin
@@ -282,8 +311,11 @@ typedef enum {
   GDN_KERNEL_DECODE = 4,        /* single-token recurrent step */
   GDN_KERNEL_CHUNK_OFFSETS = 5, /* chunk offsets of packed sequences */
   GDN_KERNEL_CHUNK_CHAIN_WHOLE = 6, /* the same chain, 128 rows per CTA */
-  GDN_KERNEL_KDA = 7,           /* per-channel-decay recurrence */
-  GDN_KERNEL_COUNT = 8
+  GDN_KERNEL_KDA = 7,           /* per-channel-decay recurrence, token by
+                                   token */
+  GDN_KERNEL_KDA_PREP = 8,      /* chunked KDA: state-independent part of
+                                   every chunk (its chain is kernel 6) */
+  GDN_KERNEL_COUNT = 9
 } gdn_kernel_t;
 
 /* gdn_timing_enable -- per-kernel device timing on (nonzero) or off (0).

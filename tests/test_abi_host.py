@@ -203,3 +203,32 @@ def test_kda_rejects_on_host(lib, kw, expect):
 
 def test_kda_empty_batch_is_a_no_op(lib):
     assert kda(lib.library(), B=0) == OK
+
+
+def kda_ex(so, path=0, sp=0, **kw):
+    a = dict(q=A, k=A + 0x1000, v=A + 0x2000, g=A + 0x3000, b=A + 0x4000,
+             h0=None, out=A + 0x5000, hT=None, cu=None, B=1, H=1, T=16,
+             dk=128, dv=128)
+    a.update(kw)
+    return so.gdn_kda_fwd_ex(a["q"], a["k"], a["v"], a["g"], a["b"], a["h0"],
+                             a["out"], a["hT"], a["cu"], a["B"], a["H"],
+                             a["T"], a["dk"], a["dv"], path, sp, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(path=-1), INVALID), (dict(path=5), INVALID),
+    (dict(path=0x300), INVALID), (dict(path=0x400), INVALID),
+    (dict(path=3), UNSUPPORTED),                 # split chain: scalar gate only
+    (dict(path=2, dk=64), UNSUPPORTED),          # chunk form: dk = 128 only
+    (dict(path=4, dv=32), UNSUPPORTED),
+    (dict(path=2, q=None), INVALID), (dict(path=2, out=A), INVALID),
+    (dict(path=2, sp=-1), INVALID), (dict(path=2, g=ODD), MISALIGNED),
+    (dict(path=0, dk=96), UNSUPPORTED), (dict(path=1, B=-1), INVALID),
+])
+def test_kda_ex_rejects_on_host(lib, kw, expect):
+    assert kda_ex(lib.library(), **kw) == expect
+
+
+@pytest.mark.parametrize("path", [0, 1, 2, 4])
+def test_kda_ex_empty_batch_is_a_no_op(lib, path):
+    assert kda_ex(lib.library(), path=path, B=0) == OK
