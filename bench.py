@@ -43,7 +43,7 @@ def _metric(w):
     if w["kind"] == "decode":
         return "GDN decode-step token-heads/s + % of GB300 HBM roofline, 1 GPU"
     if w["kind"] == "kda":
-        return "KDA (per-channel decay) forward tokens/s + % of GB300 fp32 ALU peak, 1 GPU"
+        return "KDA (per-channel decay) forward tokens/s + % of GB300 roofline, 1 GPU"
     return METRIC
 
 # Algorithmic work per token-head of the chunked forward pass:
@@ -69,8 +69,10 @@ def chain_flops(tok_heads, dk, dv, C=64):
     return tok_heads * (4 * C * dv + 6 * dk * dv)
 
 
-def chunk_bytes(tok_heads, dk, dv, n_states, elem=2):
-    return tok_heads * (elem * (2 * dk + dv) + elem * dv + 8) + \
+def chunk_bytes(tok_heads, dk, dv, n_states, elem=2, gate_floats=1):
+    # gate_floats: log-decays per token-head (1, or d_k for KDA's per-channel
+    # decays), plus beta
+    return tok_heads * (elem * (2 * dk + dv) + elem * dv + 4 * gate_floats + 4) + \
         n_states * 4 * dk * dv
 
 
@@ -89,8 +91,8 @@ WORKLOADS = {
                      "raw q/k (L2 norm in the kernels), gate and step logits, "
                      "output RMSNorm (weight [dv]) and sigmoid gate, h0=0"),
     "kda1": dict(kind="kda", B=4, H=16, T=2048, dk=128, dv=128, h0=False,
-                 desc="gdn_kda_fwd B=4 H=16 T=2048 dk=dv=128 bf16, per-channel "
-                      "log-decays max(-softplus(N(0,1)), -5), h0=0"),
+                 desc="gdn_kda_fwd_ex B=4 H=16 T=2048 dk=dv=128 bf16, "
+                      "per-channel log-decays max(-softplus(N(0,1)), -5), h0=0"),
     "w4": dict(kind="decode", N=512, H=32, dk=128, dv=128,
                desc="gdn_recurrent_step N=512 H=32 dk=dv=128 bf16 token, "
                     "fp32 state in place"),
@@ -112,8 +114,9 @@ MEASURED_TRAFFIC = {
 
 def _kernel_source_hash(kind):
     csrc = ROOT / "gated_deltanet_chunkwise_gb300" / "csrc"
-    files = ["decode.cu"] if kind == "decode" else ["kda.cu"] if kind == "kda" else sorted(
-        p.name for p in csrc.glob("chunk_*.cu"))
+    files = (["decode.cu"] if kind == "decode"
+             else ["kda.cu", "kda_chunk.cu", "chunk_tc.cu"] if kind == "kda"
+             else sorted(p.name for p in csrc.glob("chunk_*.cu")))
     h = hashlib.sha256()
     for f in files:
         h.update((csrc / f).read_bytes())
@@ -269,6 +272,7 @@ def run_ours(args, w, device, dist, rank, ws):
     d = {k: (None if v is None else v.to(device)) for k, v in d_host.items()}
     sp_flag = {"auto": 0, "chain": gdn.GDN_SP_CHAIN,
                "scan": gdn.GDN_SP_SCAN}[args.sp_combine]
+    kda_path = gdn.GDN_PATH_SIMT if args.kda_path == "serial" else gdn.GDN_PATH_AUTO
     stream = torch.cuda.current_stream(device)
     flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     flush_r = torch.zeros(FLUSH_BYTES, dtype=torch.uint8, device=device)
@@ -293,10 +297,12 @@ def run_ours(args, w, device, dist, rank, ws):
 
         def step():
             if w["kind"] == "kda":
-                gdn.gdn_kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
-                                d["h0"], d["cu_seqlens"], out=out,
-                                hT=hT if want_hT else None,
-                                output_final_state=want_hT)
+                gdn.gdn_kda_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                   d["h0"], d["cu_seqlens"], out=out,
+                                   hT=hT if want_hT else None,
+                                   output_final_state=want_hT,
+                                   path=kda_path | sp_flag,
+                                   sp_parts=args.sp_parts)
                 return
             if w["kind"] == "fused":
                 gdn.gdn_chunk_fwd_fused(
@@ -421,7 +427,7 @@ def run_ours(args, w, device, dist, rank, ws):
         value = units_all / (ms * 1e-3) * (tok_heads / tokens)  # heads/s
         unit = "token-heads/s"
         e2e_val = units_all / (e2e_ms * 1e-3) * (tok_heads / tokens)
-    elif w["kind"] == "kda":
+    elif w["kind"] == "kda" and args.kda_path == "serial":
         # fp32 CUDA-core arithmetic per token-head: the decay d_k d_v
         # multiplies, then the prediction S k, the rank-1 update and the read
         # S q at 2 d_k d_v each; against the fp32 FMA peak of the SMs
@@ -460,17 +466,28 @@ def run_ours(args, w, device, dist, rank, ws):
                 "algorithmic_flops_per_launch": flops * steps // max(n_chain, 1),
                 "launches_per_step": n_chain / steps,
                 "ms_per_launch": ms_chain / max(n_chain, 1)}
-        n_prep, ms_prep = kern.get("ut_prep_kernel", (0, 0.0))
+        prep_name = "kda_prep_kernel" if w["kind"] == "kda" else "ut_prep_kernel"
+        n_prep, ms_prep = kern.get(prep_name, (0, 0.0))
         if n_prep:
             pf = prep_flops(tok_heads, dk, dv)
             pa = pf / (ms_prep / steps * 1e-3) / 1e12
-            roof["other_kernels"] = {"ut_prep_kernel": {
-                "bound": "tensor", "achieved": round(pa, 2),
-                "frac": round(pa / bf16_tflops, 4), "unit": "TFLOP/s",
-                "algorithmic_flops_per_launch": pf * steps // n_prep,
-                "ms_per_launch": ms_prep / n_prep}}
+            prep = {"bound": "tensor", "kernel": prep_name,
+                    "achieved": round(pa, 2), "peak": bf16_tflops,
+                    "unit": "TFLOP/s", "frac": round(pa / bf16_tflops, 4),
+                    "peak_source": f"{peak_kind} bf16_tflops (burst)",
+                    "algorithmic_flops_per_launch": pf * steps // n_prep,
+                    "launches_per_step": n_prep / steps,
+                    "ms_per_launch": ms_prep / n_prep}
+            if ms_prep > ms_chain:
+                # the preparation takes longer: it is the dominant kernel
+                chain = dict(roof)
+                roof = prep
+                roof["other_kernels"] = {chain_name: chain}
+            else:
+                roof["other_kernels"] = {prep_name: prep}
         tf = chunk_flops(tok_heads, dk, dv)
-        nbytes = chunk_bytes(tok_heads, dk, dv, n_states)
+        nbytes = chunk_bytes(tok_heads, dk, dv, n_states,
+                             gate_floats=dk if w["kind"] == "kda" else 1)
         roof["whole_step"] = {
             "tflops": round(tf / (ms * 1e-3) / 1e12, 2),
             "frac": round(tf / (ms * 1e-3) / 1e12 / bf16_tflops, 4),
@@ -490,7 +507,8 @@ def run_ours(args, w, device, dist, rank, ws):
         "metric": _metric(w),
         "value": value, "unit": unit, "n_gpus": ws, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32" if w["kind"] == "kda" else "bf16",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if (w["kind"] == "kda" and args.kda_path == "serial") else "bf16",
         "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), "
                 + ("per-channel g=max(-softplus(N(0,1)),-5)"
                    if w["kind"] == "kda" else "g=-softplus(N(0,1))")
@@ -498,7 +516,10 @@ def run_ours(args, w, device, dist, rank, ws):
         "config": {"workload": w["desc"] + (
                        f" [sub-sequences: {args.sp_combine}"
                        f"{', P=%d' % args.sp_parts if args.sp_parts else ''}]"
-                       if sp_flag or args.sp_parts else ""),
+                       if sp_flag or args.sp_parts else "") + (
+                       (" [token-by-token kernel]" if args.kda_path == "serial"
+                        else " [chunk form, tensor cores]")
+                       if w["kind"] == "kda" else ""),
                    "l2": "flushed before every timed step: 256 MiB memset, then a "
                          "256 MiB read (write-back of the memset outside the "
                          "timed events)",
@@ -658,6 +679,9 @@ def main(argv=None):
                          "combined (the library chooses by default)")
     ap.add_argument("--sp-parts", type=int, default=0,
                     help="sequence-parallel split count (0 = automatic)")
+    ap.add_argument("--kda-path", choices=["auto", "serial"], default="auto",
+                    help="KDA workload: the chunk form on the tensor cores "
+                         "(auto) or the token-by-token kernel (serial)")
     ap.add_argument("--sequences", type=int, default=0,
                     help="override the number of sequences of the workload "
                          "(smaller cases for profiler captures)")

@@ -21,12 +21,13 @@
 // for the column-wise decay of the state; this kernel writes -W, P, T_U, Q_g
 // and K_d as bf16 tile images and e^{Gamma_L} as the chunk's decay record.
 //
-// A and P need e^{Gamma_r - Gamma_s} channel by channel. With b(t) the first
-// token of t's 16-token block the kernel factors it as
-//   e^{Gamma_r - Gamma_b(r)}  x  e^{Gamma_b(r) - Gamma_b(s)}  x  e^{Gamma_b(s) - Gamma_s}
-// (left table K_E = K (.) e^{Gamma - Gamma_b}, Q_E likewise, right table
-// K_B = K (.) e^{Gamma_b - Gamma}, one vector per pair of blocks), so every
-// block of A and P is one bf16 tensor-core product over d_k. All factors but
+// A and P need e^{Gamma_r - Gamma_s} channel by channel. With ref(t) the
+// cumulative decay before the first token of t's 16-token block the kernel
+// factors it as
+//   e^{Gamma_r - ref(r)}  x  e^{ref(r) - ref(s)}  x  e^{ref(s) - Gamma_s}
+// (left table K_E = K (.) e^{Gamma - ref}, Q_E likewise, right table
+// K_B = K (.) e^{ref - Gamma}, one vector per pair of blocks), so every block
+// of A and P is one bf16 tensor-core product over d_k. All factors but
 // the right table's lie in (0, 1] for decays (g <= 0); the right table grows
 // by at most the decay across one block. A chunk in which some channel decays
 // by more than 2^120 across one block (or grows by that much between two)
@@ -38,7 +39,7 @@
 // with mma.sync m16n8k16 (bf16 in, fp32 accumulate) from ldmatrix fragments,
 // the inverse by the blocked substitution shared with the scalar-gate
 // preparation, images out by bulk copies (P, T_U, -W) or direct stores (Q_g,
-// K_d: each thread owns one key channel).
+// K_d: each thread owns two key channels of one 16-token block).
 #include "chunk_tiles.cuh"
 
 namespace gdn {
@@ -62,10 +63,8 @@ constexpr uint32_t KP_AT = 4 * KP_TAB;             // fp32 A, then T (pitch AP)
 constexpr uint32_t KP_P = KP_AT + 64 * AP * 4;     // P image
 constexpr uint32_t KP_TU = KP_P + TILE_BYTES;      // T_U image
 constexpr uint32_t KP_V = KP_TU + TILE_BYTES;      // 6 pair vectors x 128
-constexpr uint32_t KP_GB = KP_V + 6 * DK * 4;      // Gamma at the 4 block starts
-constexpr uint32_t KP_HT = KP_GB + 4 * DK * 4;     // first-half totals
-constexpr uint32_t KP_GL = KP_HT + DK * 4;         // Gamma_L
-constexpr uint32_t KP_BETA = KP_GL + DK * 4;       // beta (0 past the end)
+constexpr uint32_t KP_QT = KP_V + 6 * DK * 4;      // per-block decay totals
+constexpr uint32_t KP_BETA = KP_QT + 4 * DK * 4;    // beta (0 past the end)
 constexpr uint32_t KP_SMEM = KP_BETA + 64 * 4 + 1024;
 static_assert(64 * GP * 4 <= KP_KB, "Gamma table overlaps the raw K table");
 static_assert(2 * WS_W_BYTES <= KP_KB, "-W image overlaps K_G");
@@ -102,11 +101,14 @@ __device__ __forceinline__ uint32_t scale_bf16x2(uint32_t u, float2 s) {
   const float lo = __uint_as_float(u << 16), hi = __uint_as_float(u & 0xffff0000u);
   return pack_bf16x2(lo * s.x, hi * s.y);
 }
+// 2^x on the special-function unit (flushes results below 2^-126 to 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float bf16_bits(uint32_t b) {
   return __uint_as_float(b << 16);
-}
-__device__ __forceinline__ void st_bf16(uint8_t* p, float v) {
-  *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(v);
 }
 
 __global__ void __launch_bounds__(kKpThreads, kKpCtas)
@@ -128,9 +130,6 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
 
   float* AT = reinterpret_cast<float*>(sm + KP_AT);
   float* vpair = reinterpret_cast<float*>(sm + KP_V);
-  float* gbs = reinterpret_cast<float*>(sm + KP_GB);
-  float* htot = reinterpret_cast<float*>(sm + KP_HT);
-  float* gend = reinterpret_cast<float*>(sm + KP_GL);
   float* bet = reinterpret_cast<float*>(sm + KP_BETA);
   const uint16_t* kin = static_cast<const uint16_t*>(p.k);
   const uint16_t* qin = static_cast<const uint16_t*>(p.q);
@@ -171,54 +170,66 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
     if (tid == 0) bulk_wait_read();
     __syncthreads();
 
-    // ---- 1. cumulative log2-decay of key channel c over the chunk --------
-    const int c = tid & 127, hh = tid >> 7;  // tokens 32 hh .. 32 hh + 31
-    float x[32];
-    uint32_t kq[32];  // raw k (low 16 bits) and q (high 16 bits)
+    // ---- 1. cumulative log2-decay over the chunk --------------------------
+    // thread (block R1 = tid >> 6, channel pair cp = tid & 63): tokens
+    // 16 R1 .. 16 R1 + 15 of key channels 2 cp and 2 cp + 1. Each block is
+    // referred to the cumulative decay before its first token, ref_R1.
+    const int R1 = tid >> 6, cp = tid & 63, c0 = 2 * cp;
+    float2 x[16];           // Gamma_t - ref_R1 (log2 units)
+    uint32_t kk2[16], qq2[16];  // raw k and q, two channels each
     {
-      const size_t row0 = ((size_t)(t0 + 32 * hh)) * H + h;
+      const size_t e0 = ((size_t)(t0 + 16 * R1) * H + h) * DK + c0;
+      const size_t rs = (size_t)H * DK;  // token stride in elements
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float gv = 0.f;
+      for (int j = 0; j < 16; ++j) {
+        float2 gv = make_float2(0.f, 0.f);
         uint32_t kb = 0, qb = 0;
-        if (32 * hh + j < len) {
-          const size_t e = (row0 + (size_t)j * H) * DK + c;
-          gv = __ldg(p.g + e);
-          kb = __ldg(kin + e);
-          qb = __ldg(qin + e);
+        if (16 * R1 + j < len) {
+          const size_t e = e0 + (size_t)j * rs;
+          gv = __ldg(reinterpret_cast<const float2*>(p.g + e));
+          kb = __ldg(reinterpret_cast<const uint32_t*>(kin + e));
+          qb = __ldg(reinterpret_cast<const uint32_t*>(qin + e));
         }
-        x[j] = gv * kLog2e;
-        kq[j] = kb | (qb << 16);
+        x[j] = make_float2(gv.x * kLog2e, gv.y * kLog2e);
+        kk2[j] = kb;
+        qq2[j] = qb;
       }
     }
 #pragma unroll
-    for (int j = 1; j < 32; ++j) x[j] += x[j - 1];
-    if (hh == 0) htot[c] = x[31];
+    for (int j = 1; j < 16; ++j) {
+      x[j].x += x[j - 1].x;
+      x[j].y += x[j - 1].y;
+    }
+    float2* qtot = reinterpret_cast<float2*>(sm + KP_QT);  // [4 blocks][64 pairs]
+    qtot[R1 * 64 + cp] = x[15];
     if (tid < 64) bet[tid] = tid < len ? __ldg(p.beta + ((size_t)(t0 + tid) * H + h)) : 0.f;
     __syncthreads();
-    if (hh == 1) {
-      const float o = htot[c];
+    float2 own = make_float2(0.f, 0.f), xl = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) x[j] += o;
-      gend[c] = x[31];
+    for (int q = 0; q < 4; ++q) {
+      const float2 v = qtot[q * 64 + cp];
+      if (q < R1) {
+        own.x += v.x;
+        own.y += v.y;
+      }
+      xl.x += v.x;
+      xl.y += v.y;
     }
-    gbs[(2 * hh) * DK + c] = x[0];
-    gbs[(2 * hh + 1) * DK + c] = x[16];
     bool bad = false;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) bad |= fabsf(x[j] - x[j & 16]) > kSpanLimit;
-    __syncthreads();
-    const float xl = gend[c];
-    // e^{Gamma_b(R) - Gamma_b(S)} for the block pairs S < R:
-    // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
-#pragma unroll
-    for (int m = 0; m < 3; ++m) {
-      const int idx = tid + kKpThreads * m, pr = idx >> 7, ch = idx & 127;
-      const int R = pr < 1 ? 1 : (pr < 3 ? 2 : 3);
-      const int S = pr - R * (R - 1) / 2;
-      const float e = gbs[R * DK + ch] - gbs[S * DK + ch];
-      bad |= e > kSpanLimit;
-      vpair[pr * DK + ch] = exp2f(e);
+    for (int j = 0; j < 16; ++j)
+      bad |= fabsf(x[j].x) > kSpanLimit || fabsf(x[j].y) > kSpanLimit;
+    {
+      // 2^{ref_R1 - ref_S} for the blocks S < R1: the pair vectors
+      float2 acc = make_float2(0.f, 0.f);
+      for (int S = R1 - 1; S >= 0; --S) {
+        const float2 v = qtot[S * 64 + cp];
+        acc.x += v.x;
+        acc.y += v.y;
+        bad |= acc.x > kSpanLimit || acc.y > kSpanLimit;
+        *reinterpret_cast<float2*>(vpair + (R1 * (R1 - 1) / 2 + S) * DK + c0) =
+            make_float2(ex2(acc.x), ex2(acc.y));
+      }
     }
     const bool exact = __syncthreads_or(bad) != 0;
 
@@ -226,32 +237,37 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
     {
       float* cv = p.cv + (size_t)it * KCV_FLOATS;
       // e^G = 1 for the chain's read-out (the decay is inside Q_g)
-      if (hh == 0) cv[c] = 1.f;
-      else cv[CV_GAMMA + c] = exp2f(xl);
-      uint8_t* qimg = static_cast<uint8_t*>(p.qg) + (size_t)it * WS_QG_BYTES;
-      uint8_t* kimg = static_cast<uint8_t*>(p.kd) + (size_t)it * WS_KD_BYTES;
-      const uint32_t cblk = (uint32_t)((c >> 6) * TILE_BYTES) + (c & 7) * 2;
-      const int cchunk = (c & 63) >> 3;
-      float* gam = reinterpret_cast<float*>(sm + KP_GAM);
+      if (R1 == 1) *reinterpret_cast<float2*>(cv + c0) = make_float2(1.f, 1.f);
+      if (R1 == 0)
+        *reinterpret_cast<float2*>(cv + CV_GAMMA + c0) = make_float2(ex2(xl.x), ex2(xl.y));
+      uint8_t* qimg = static_cast<uint8_t*>(p.qg) + (size_t)it * WS_QG_BYTES +
+                      (c0 >> 6) * TILE_BYTES + (c0 & 7) * 2;
+      uint8_t* kimg = static_cast<uint8_t*>(p.kd) + (size_t)it * WS_KD_BYTES +
+                      (c0 >> 6) * TILE_BYTES + (c0 & 7) * 2;
+      const int cchunk = (c0 & 63) >> 3;
+      const float2 eown = make_float2(ex2(own.x), ex2(own.y));
+      float2* gam = reinterpret_cast<float2*>(sm + KP_GAM);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int t = 32 * hh + j;
-        const float kv = bf16_bits(kq[j] & 0xffffu), qv = bf16_bits(kq[j] >> 16);
-        const float eg = exp2f(x[j]), ed = exp2f(xl - x[j]);
-        const uint32_t off = cblk + sw128(t, cchunk);
-        st_bf16(qimg + off, qv * eg);
-        st_bf16(kimg + off, kv * ed);
-        st_bf16(sm + KP_KG + t * KP_PITCH + c * 2, kv * eg);
+      for (int j = 0; j < 16; ++j) {
+        const int t = 16 * R1 + j;
+        const float k0 = bf16_bits(kk2[j] & 0xffffu), k1 = bf16_bits(kk2[j] >> 16);
+        const float q0 = bf16_bits(qq2[j] & 0xffffu), q1 = bf16_bits(qq2[j] >> 16);
+        const float E0 = ex2(x[j].x), E1 = ex2(x[j].y);
+        const float g0 = E0 * eown.x, g1 = E1 * eown.y;  // e^{Gamma_t}
+        const float d0 = ex2(xl.x - own.x - x[j].x), d1 = ex2(xl.y - own.y - x[j].y);
+        const uint32_t off = sw128(t, cchunk);
+        *reinterpret_cast<uint32_t*>(qimg + off) = pack_bf16x2(q0 * g0, q1 * g1);
+        *reinterpret_cast<uint32_t*>(kimg + off) = pack_bf16x2(k0 * d0, k1 * d1);
+        const uint32_t row = t * KP_PITCH + c0 * 2;
+        *reinterpret_cast<uint32_t*>(sm + KP_KG + row) = pack_bf16x2(k0 * g0, k1 * g1);
         if (!exact) {
-          const float e = x[j] - x[j & 16];
-          const float E = exp2f(e), Ei = exp2f(-e);
-          st_bf16(sm + KP_KE + t * KP_PITCH + c * 2, kv * E);
-          st_bf16(sm + KP_QE + t * KP_PITCH + c * 2, qv * E);
-          st_bf16(sm + KP_KB + t * KP_PITCH + c * 2, kv * Ei);
+          const float I0 = ex2(-x[j].x), I1 = ex2(-x[j].y);
+          *reinterpret_cast<uint32_t*>(sm + KP_KE + row) = pack_bf16x2(k0 * E0, k1 * E1);
+          *reinterpret_cast<uint32_t*>(sm + KP_QE + row) = pack_bf16x2(q0 * E0, q1 * E1);
+          *reinterpret_cast<uint32_t*>(sm + KP_KB + row) = pack_bf16x2(k0 * I0, k1 * I1);
         } else {
-          gam[t * GP + c] = x[j];
-          *reinterpret_cast<uint16_t*>(sm + KP_KB + t * KP_PITCH + c * 2) =
-              (uint16_t)(kq[j] & 0xffffu);
+          gam[(t * GP + c0) >> 1] = make_float2(x[j].x + own.x, x[j].y + own.y);
+          *reinterpret_cast<uint32_t*>(sm + KP_KB + row) = kk2[j];
         }
       }
     }
