@@ -273,16 +273,18 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
     }
     __syncthreads();
 
-    // ---- 3. A and P, one warp per (matrix, 16-row block R) ---------------
+    // ---- 3. A and P in 16 x 16 blocks, spread over the warps --------------
+    // 20 blocks on or below the diagonal (12 off it first: those carry the
+    // pair vectors), then the 12 zero blocks above it; warp w takes jobs
+    // w, w + 8, ..
     {
-      const int mat = warp >> 2, R = warp & 3;  // mat 0: A, 1: P
       const int g = lane >> 2, t4 = lane & 3;
-      const int r0 = 16 * R + g, r1 = r0 + 8;
       uint8_t* pimg = sm + KP_P;
       float acc[2][4];
-      // block (R, S) out of the accumulators: A (times beta_r, s < r) into
-      // the solve buffer, P (s <= r) into its bf16 image
-      auto put_block = [&](int S) {
+      // block (mat, R, S) out of the accumulators: A (times beta_r, s < r)
+      // into the solve buffer, P (s <= r) into its bf16 image
+      auto put_block = [&](int mat, int R, int S) {
+        const int r0 = 16 * R + g, r1 = r0 + 8;
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
           const int s = 16 * S + 8 * n + 2 * t4;
@@ -302,50 +304,57 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
           }
         }
       };
-      if (!exact) {
-        // left fragments of rows 16 R.. (K_E or Q_E), all of d_k
-        uint32_t a[8][4];
-        const uint32_t tab = base + (mat ? KP_QE : KP_KE);
-        const int ar = 16 * R + (lane & 7) + ((lane >> 3) & 1) * 8;
+      // pair index pr (0..5) -> (R, S), S < R: (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+      auto pair_rs = [](int pr, int& R, int& S) {
+        R = pr < 1 ? 1 : (pr < 3 ? 2 : 3);
+        S = pr - R * (R - 1) / 2;
+      };
+      for (int job = warp; job < 32; job += 8) {
+        int mat, R, S;
+        if (job < 12) {
+          mat = job / 6;
+          pair_rs(job % 6, R, S);
+        } else if (job < 20) {
+          mat = (job - 12) >> 2;
+          R = S = (job - 12) & 3;
+        } else {
+          mat = (job - 20) / 6;
+          pair_rs((job - 20) % 6, S, R);  // mirrored: above the diagonal
+        }
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ldsm_x4(tab + ar * KP_PITCH + (16 * kk + (lane >> 4) * 8) * 2, a[kk]);
-        const int br = (lane & 7) + (lane >> 4) * 8, bc = ((lane >> 3) & 1) * 8;
-        for (int S = 0; S <= R; ++S) {
+        for (int n = 0; n < 2; ++n)
 #pragma unroll
-          for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
-          const float* vp = vpair + (R * (R - 1) / 2 + S) * DK;
+          for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+        if (job < 20 && !exact) {
+          // left rows 16 R.. (K_E or Q_E), right rows 16 S.. of K_B (two
+          // 8-row n tiles, times the pair vector off the diagonal)
+          const uint32_t tab = base + (mat ? KP_QE : KP_KE);
+          const int ar = 16 * R + (lane & 7) + ((lane >> 3) & 1) * 8;
+          const int br = 16 * S + (lane & 7) + (lane >> 4) * 8;
+          const int ac = (lane >> 4) * 8, bc = ((lane >> 3) & 1) * 8;
+          const float* vp = vpair + (R * (R - 1) / 2 + S) * DK + 2 * t4;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            // right fragments: rows 16 S.. of K_B (two 8-row n tiles),
-            // times the pair vector off the diagonal
-            uint32_t b[4];
-            ldsm_x4(base + KP_KB + (16 * S + br) * KP_PITCH + (16 * kk + bc) * 2, b);
+            uint32_t a[4], b[4];
+            ldsm_x4(tab + ar * KP_PITCH + (16 * kk + ac) * 2, a);
+            ldsm_x4(base + KP_KB + br * KP_PITCH + (16 * kk + bc) * 2, b);
             if (S < R) {
-              const float2 v0 = *reinterpret_cast<const float2*>(vp + 16 * kk + 2 * t4);
-              const float2 v1 = *reinterpret_cast<const float2*>(vp + 16 * kk + 2 * t4 + 8);
+              const float2 v0 = *reinterpret_cast<const float2*>(vp + 16 * kk);
+              const float2 v1 = *reinterpret_cast<const float2*>(vp + 16 * kk + 8);
               b[0] = scale_bf16x2(b[0], v0);
               b[1] = scale_bf16x2(b[1], v1);
               b[2] = scale_bf16x2(b[2], v0);
               b[3] = scale_bf16x2(b[3], v1);
             }
-            mma16816(acc[0], a[kk], b[0], b[1]);
-            mma16816(acc[1], a[kk], b[2], b[3]);
+            mma16816(acc[0], a, b[0], b[1]);
+            mma16816(acc[1], a, b[2], b[3]);
           }
-          put_block(S);
-        }
-      } else {
-        // exact sum: each lane's 8 entries of the block, channel by channel
-        const float* gam = reinterpret_cast<const float*>(sm + KP_GAM);
-        const uint16_t* kraw = reinterpret_cast<const uint16_t*>(sm + KP_KB);
-        const int kp = KP_PITCH / 2;
-        for (int S = 0; S <= R; ++S) {
-#pragma unroll
-          for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+        } else if (job < 20) {
+          // exact sum: each lane's 8 entries of the block, channel by channel
+          const float* gam = reinterpret_cast<const float*>(sm + KP_GAM);
+          const uint16_t* kraw = reinterpret_cast<const uint16_t*>(sm + KP_KB);
+          const int kp = KP_PITCH / 2;
+          const int r0 = 16 * R + g, r1 = r0 + 8;
           for (int ch = 0; ch < DK; ++ch) {
             const float gr0 = gam[r0 * GP + ch], gr1 = gam[r1 * GP + ch];
             float x0, x1;
@@ -366,16 +375,8 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
                 acc[n][2 + e] = fmaf(x1 * ks, exp2f(gr1 - gs), acc[n][2 + e]);
               }
           }
-          put_block(S);
         }
-      }
-      // blocks above the diagonal are zero
-      for (int S = R + 1; S < 4; ++S) {
-#pragma unroll
-        for (int n = 0; n < 2; ++n)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
-        put_block(S);
+        put_block(mat, R, S);
       }
       fence_proxy_async();
     }
