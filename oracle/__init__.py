@@ -21,6 +21,11 @@ Two parts:
   ``tests/test_oracle_sublayer_pins.py``.
 * ``oracle.kda`` -- the delta rule with a per-channel decay (KDA) in fp64,
   token by token; pinned in ``tests/test_oracle_kda_pins.py``.
+* ``oracle.backward`` -- gradients of both (per-channel and scalar gate,
+  decay before the prediction) by the reverse sweep of the token loop in
+  fp64; pinned in ``tests/test_oracle_backward_pins.py`` (finite differences
+  through the forward oracles, closed forms, automatic differentiation of an
+  independent PyTorch forward).
 
 Pins (all in ``tests/test_oracle_pins.py``): worked numbers of the illustrated
 DeltaNet page (delta-rule 1.5/2.25/2.625, the 2-D example, prediction/error,

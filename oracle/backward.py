@@ -1,0 +1,109 @@
+"""Gradients of the forward pass in fp64 (oracle; TEST INFRASTRUCTURE ONLY,
+see ``oracle/__init__.py``).
+
+The backward pass of the pages (illustrated DeltaNet walk-through, the cost
+table and memory paragraphs: a chunkwise model keeps only the state at each
+chunk boundary and recomputes the rest for the gradient; the lqnn.cn page,
+section on the chunk form, block recompute) has a plain definition: the
+derivative of the forward map. Here that derivative is written out as the
+reverse sweep of the token recurrence, with every intermediate kept (no
+recomputation: the oracle holds all states). For a per-channel decay (KDA,
+the walk-through's hybrid-architecture section; the scalar gate is every
+channel equal) one token is
+    S_bar = S diag(a),  a = e^{g_t}     e = v_t - S_bar k_t,  u = beta_t e
+    S_t = S_bar + u k_t^T               o_t = S_t q_t
+and, given dS (the gradient arriving at S_t) and do_t, its adjoint is
+    dq_t = S_t^T do_t                   dS += do_t q_t^T
+    du = dS k_t,  dk_t = dS^T u - beta_t S_bar^T du
+    dbeta_t = du . e,  dv_t = beta_t du
+    dS_bar = dS - beta_t du k_t^T
+    dg_t = colsum(dS_bar (.) S_bar)     dS_{t-1} = dS_bar diag(a).
+The loss these gradients belong to is L = sum(dout (.) out) + sum(dhT (.)
+hT); tests/test_oracle_backward_pins.py pins the sweep against central
+finite differences of that loss computed with the forward oracles, against
+closed forms, and against automatic differentiation of an independent
+PyTorch statement of the forward map.
+
+State layout as in ``oracle.kda``: S is d_v x d_k, h0 / hT hold S^T.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _f64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        x = x.detach().cpu()
+        if str(x.dtype) == "torch.bfloat16":
+            x = x.float()
+        x = x.numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def _sequences(B, T, cu_seqlens):
+    if cu_seqlens is not None:
+        cu = [int(x) for x in np.asarray(cu_seqlens)]
+        return [slice(cu[i], cu[i + 1]) for i in range(len(cu) - 1)]
+    return [slice(n * T, (n + 1) * T) for n in range(B)]
+
+
+def kda_backward(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None):
+    """Gradients of L = sum(dout * out) + sum(dhT * hT) for the per-channel
+    forward (``oracle.kda.forward``). q, k, g [B, T, H, dk]; v, dout [B, T,
+    H, dv]; beta [B, T, H]; h0, dhT [N, H, dk, dv] or None. Returns a dict
+    dq, dk, dv, dg, dbeta (shapes of the inputs) and dh0 [N, H, dk, dv]."""
+    q, k, v, g, beta, h0, dout, dhT = map(
+        _f64, (q, k, v, g, beta, h0, dout, dhT))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    flat = lambda x: x.reshape(B * T, H, -1)
+    qf, kf, vf, gf, of = map(flat, (q, k, v, g, dout))
+    bf = beta.reshape(B * T, H)
+    seqs = _sequences(B, T, cu_seqlens)
+    grads = {n: np.zeros_like(x) for n, x in
+             (("dq", qf), ("dk", kf), ("dv", vf), ("dg", gf))}
+    grads["dbeta"] = np.zeros_like(bf)
+    dh0 = np.zeros((len(seqs), H, dk, dv))
+    for n, sl in enumerate(seqs):
+        for h in range(H):
+            S = np.zeros((dv, dk)) if h0 is None else h0[n, h].T.copy()
+            keep = []  # (S_bar, e, S_t) per token
+            for t in range(sl.start, sl.stop):
+                Sb = S * np.exp(gf[t, h])[None, :]
+                e = vf[t, h] - Sb @ kf[t, h]
+                S = Sb + np.outer(bf[t, h] * e, kf[t, h])
+                keep.append((Sb, e, S))
+            dS = np.zeros((dv, dk)) if dhT is None else dhT[n, h].T.copy()
+            for i in range(len(keep) - 1, -1, -1):
+                t = sl.start + i
+                Sb, e, St = keep[i]
+                qt, kt, b = qf[t, h], kf[t, h], bf[t, h]
+                grads["dq"][t, h] = St.T @ of[t, h]
+                dS = dS + np.outer(of[t, h], qt)
+                u = b * e
+                du = dS @ kt
+                grads["dk"][t, h] = dS.T @ u - b * (Sb.T @ du)
+                grads["dbeta"][t, h] = du @ e
+                grads["dv"][t, h] = b * du
+                dSb = dS - b * np.outer(du, kt)
+                grads["dg"][t, h] = (dSb * Sb).sum(axis=0)
+                dS = dSb * np.exp(gf[t, h])[None, :]
+            dh0[n, h] = dS.T
+    out = {n: x.reshape(B, T, H, -1) for n, x in grads.items()}
+    out["dbeta"] = grads["dbeta"].reshape(B, T, H)
+    out["dh0"] = dh0
+    return out
+
+
+def backward(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None):
+    """The same for the scalar gate with the decay before the prediction
+    (``oracle.forward`` with variant G1): g [B, T, H] is every channel's
+    log-decay, so dg is the sum over channels of the per-channel one."""
+    g = _f64(g)
+    dk = np.asarray(_f64(q)).shape[-1]
+    gk = np.repeat(g[..., None], dk, axis=-1)
+    out = kda_backward(q, k, v, gk, beta, h0, dout, dhT, cu_seqlens)
+    out["dg"] = out["dg"].sum(axis=-1)
+    return out
