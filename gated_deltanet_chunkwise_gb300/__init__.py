@@ -12,14 +12,14 @@ from __future__ import annotations
 _ABI_NAMES = (
     "gdn_chunk_fwd", "gdn_chunk_fwd_f32", "gdn_chunk_fwd_ex",
     "gdn_recurrent_step", "gdn_chunk_fwd_fused", "gdn_kda_fwd",
-    "gdn_kda_fwd_ex",
+    "gdn_kda_fwd_ex", "gdn_kda_bwd", "gdn_chunk_bwd",
     "gdn_status_string",
     "GdnError", "library_path",
     "library", "kernel_counters", "gdn_device_status", "gdn_selftest_mma",
     "gdn_timing_enable", "gdn_timing_read", "kernel_timings",
     "GDN_KERNEL_CHUNK_PREP", "GDN_KERNEL_CHUNK_CHAIN", "GDN_KERNEL_CHUNK_SIMT",
     "GDN_KERNEL_SP_CHAIN", "GDN_KERNEL_DECODE", "GDN_KERNEL_CHUNK_OFFSETS",
-    "GDN_KERNEL_CHUNK_CHAIN_WHOLE", "GDN_KERNEL_KDA", "GDN_KERNEL_KDA_PREP",
+    "GDN_KERNEL_CHUNK_CHAIN_WHOLE", "GDN_KERNEL_KDA", "GDN_KERNEL_KDA_PREP", "GDN_KERNEL_BWD", "GDN_KERNEL_BWD_FINALIZE",
     "GDN_KERNEL_COUNT",
     "KERNEL_NAMES",
     "GDN_PATH_AUTO", "GDN_PATH_SIMT", "GDN_PATH_TCGEN05",

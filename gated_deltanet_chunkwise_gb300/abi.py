@@ -39,7 +39,9 @@ GDN_KERNEL_CHUNK_OFFSETS = 5
 GDN_KERNEL_CHUNK_CHAIN_WHOLE = 6
 GDN_KERNEL_KDA = 7
 GDN_KERNEL_KDA_PREP = 8
-GDN_KERNEL_COUNT = 9
+GDN_KERNEL_BWD = 9
+GDN_KERNEL_BWD_FINALIZE = 10
+GDN_KERNEL_COUNT = 11
 KERNEL_NAMES = {
     GDN_KERNEL_CHUNK_PREP: "ut_prep_kernel",
     GDN_KERNEL_CHUNK_CHAIN: "chunk_tc_kernel",
@@ -50,6 +52,8 @@ KERNEL_NAMES = {
     GDN_KERNEL_CHUNK_CHAIN_WHOLE: "chain_tx_kernel",
     GDN_KERNEL_KDA: "kda_kernel",
     GDN_KERNEL_KDA_PREP: "kda_prep_kernel",
+    GDN_KERNEL_BWD: "bwd_kernel",
+    GDN_KERNEL_BWD_FINALIZE: "bwd_finalize_kernel",
 }
 
 _lib = None
@@ -95,6 +99,10 @@ def library():
     lib.gdn_kda_fwd_ex.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, ip, i, i, i,
                                    i, i, i, i, vp]
     lib.gdn_kda_fwd_ex.restype = i
+    for name in ("gdn_kda_bwd", "gdn_chunk_bwd"):
+        getattr(lib, name).argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, fp,
+                                       fp, fp, fp, fp, ip, i, i, i, i, i, vp]
+        getattr(lib, name).restype = i
     lib.gdn_device_status.argtypes = [vp]
     lib.gdn_device_status.restype = i
     lib.gdn_status_string.argtypes = [i]
@@ -250,6 +258,67 @@ def gdn_kda_fwd_ex(q, k, v, g, beta, h0=None, cu_seqlens=None, *, out=None,
     the chunk form (0: automatic)."""
     return _kda("gdn_kda_fwd_ex", q, k, v, g, beta, h0, cu_seqlens, out, hT,
                 output_final_state, stream, (int(path), int(sp_parts)))
+
+
+def gdn_kda_bwd(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None, *,
+                want_dh0=True, stream=None):
+    """Gradients of gdn_kda_fwd for L = sum(dout * out) + sum(dhT * hT):
+    returns dict dq, dk [B, T, H, dk], dv [B, T, H, dv], dg [B, T, H, dk],
+    dbeta [B, T, H] (fp32) and dh0 [N, H, dk, dv] (fp32, or None)."""
+    return _bwd("gdn_kda_bwd", q, k, v, g, beta, h0, dout, dhT, cu_seqlens,
+                want_dh0, stream, per_channel=True)
+
+
+def gdn_chunk_bwd(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None, *,
+                  want_dh0=True, stream=None):
+    """Gradients of gdn_chunk_fwd (scalar gate, decay before the prediction):
+    as gdn_kda_bwd with g and dg [B, T, H]."""
+    return _bwd("gdn_chunk_bwd", q, k, v, g, beta, h0, dout, dhT, cu_seqlens,
+                want_dh0, stream, per_channel=False)
+
+
+def _bwd(fn, q, k, v, g, beta, h0, dout, dhT, cu_seqlens, want_dh0, stream,
+         per_channel):
+    dev = q.device
+    _need(q, "q", torch.bfloat16, None)
+    for name, t in (("k", k), ("v", v), ("dout", dout)):
+        _need(t, name, torch.bfloat16, dev)
+    _need(g, "g", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    Bt, T, H, dk = q.shape
+    dv = v.shape[-1]
+    gshape = q.shape if per_channel else q.shape[:3]
+    if k.shape != q.shape or v.shape[:3] != (Bt, T, H) or dout.shape != v.shape:
+        raise ValueError("q/k must be [B, T, H, dk], v/dout [B, T, H, dv]")
+    if g.shape != gshape or beta.shape != (Bt, T, H):
+        raise ValueError(f"g must be {tuple(gshape)} and beta [B, T, H]")
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        if Bt != 1:
+            raise ValueError("packed sequences are passed as [1, T, H, ...]")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = Bt
+    for name, st in (("h0", h0), ("dhT", dhT)):
+        if st is not None:
+            _need(st, name, torch.float32, dev)
+            if st.shape != (N, H, dk, dv):
+                raise ValueError(f"{name} must be [{N}, {H}, {dk}, {dv}]")
+    f32 = dict(dtype=torch.float32, device=dev)
+    res = {"dq": torch.empty(q.shape, **f32), "dk": torch.empty(q.shape, **f32),
+           "dv": torch.empty(v.shape, **f32), "dg": torch.empty(gshape, **f32),
+           "dbeta": torch.empty(beta.shape, **f32),
+           "dh0": torch.empty((N, H, dk, dv), **f32) if want_dh0 else None}
+    with torch.cuda.device(dev):
+        rc = getattr(library(), fn)(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+            _ptr(dout), _ptr(dhT), _ptr(res["dq"]), _ptr(res["dk"]),
+            _ptr(res["dv"]), _ptr(res["dg"]), _ptr(res["dbeta"]),
+            _ptr(res["dh0"]), _ptr(cu_seqlens), N, H, T, dk, dv,
+            _stream(stream))
+    if rc != GDN_OK:
+        raise GdnError(rc, fn)
+    return res
 
 
 def _kda(fn, q, k, v, g, beta, h0, cu_seqlens, out, hT, output_final_state,

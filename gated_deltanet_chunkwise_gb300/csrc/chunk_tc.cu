@@ -521,10 +521,10 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtas)
   if (tid == 0 && *abort_flag) record_status(p.status, GDN_ERR_TIMEOUT);
 }
 
-// Exclusive prefix of per-sequence chunk counts: chunk_off[n] = sum_{m<n}
-// ceil(len_m / C), chunk_off[N] = total. One CTA.
+// Exclusive prefix of per-sequence block counts: chunk_off[n] = sum_{m<n}
+// ceil(len_m / L) (L = C for chunks), chunk_off[N] = total. One CTA.
 __global__ void __launch_bounds__(1024)
-    chunk_offsets_kernel(const int32_t* cu_seqlens, int N, int T,
+    chunk_offsets_kernel(const int32_t* cu_seqlens, int N, int T, int L,
                          int32_t* chunk_off, int* status) {
   __shared__ int carry;
   __shared__ int warp_sums[32];
@@ -539,7 +539,7 @@ __global__ void __launch_bounds__(1024)
       if (b < 0 || e < b || e > T) {
         record_status(status, GDN_ERR_INVALID_ARG);
       } else {
-        v = (e - b + C - 1) / C;
+        v = (e - b + L - 1) / L;
       }
     }
     int x = v;
@@ -2032,10 +2032,21 @@ cudaError_t launch_chunk_offsets(const ChunkParams& p, cudaStream_t stream,
   if (!p.cu_seqlens) return cudaSuccess;
   const int t = timing_start(GDN_KERNEL_CHUNK_OFFSETS, stream);
   chunk_offsets_kernel<<<1, 1024, 0, stream>>>(
-      p.cu_seqlens, p.N, p.T, const_cast<int32_t*>(p.chunk_off), p.status);
+      p.cu_seqlens, p.N, p.T, C, const_cast<int32_t*>(p.chunk_off), p.status);
   cudaError_t e = cudaGetLastError();
   timing_stop(t, stream, e);
   if (e == cudaSuccess) ++*launches;
+  return e;
+}
+
+// Prefix of ceil(len / L) over the packed sequences (one CTA).
+cudaError_t launch_block_offsets(const int32_t* cu_seqlens, int N, int T,
+                                 int L, int32_t* out, int* status,
+                                 cudaStream_t stream) {
+  const int t = timing_start(GDN_KERNEL_CHUNK_OFFSETS, stream);
+  chunk_offsets_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, T, L, out, status);
+  cudaError_t e = cudaGetLastError();
+  timing_stop(t, stream, e);
   return e;
 }
 

@@ -125,6 +125,11 @@ cudaError_t launch_chunk_offsets(const ChunkParams& p, cudaStream_t stream,
 cudaError_t launch_kda_prep(const ChunkParams& p, cudaStream_t stream,
                             int* launches);
 long long chunk_tc_chunks_bound(const ChunkParams& p);
+// Exclusive prefix of ceil(len_n / L) over the sequences of a packed call,
+// out[N] the total (one launch).
+cudaError_t launch_block_offsets(const int32_t* cu_seqlens, int N, int T,
+                                 int L, int32_t* out, int* status,
+                                 cudaStream_t stream);
 int chunk_tc_nch_dense(const ChunkParams& p);
 cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);

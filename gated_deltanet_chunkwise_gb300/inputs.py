@@ -156,3 +156,18 @@ def kda_inputs(B, H, T, dk, dv, *, seed=0, h0=False, lengths=None,
     g = np.maximum(-_softplus(_normal(rng, shape)), np.float32(-5.0))
     d["g"] = torch.from_numpy(g.astype(np.float32))
     return d
+
+
+def grad_inputs(d, *, seed=0, dhT=True):
+    """Upstream gradients for a backward call on the forward inputs ``d``:
+    dout bf16 shaped like v ~ N(0, 1), and dhT fp32 [N, H, dk, dv] ~ 0.1 N(0,
+    1) (None with ``dhT=False``)."""
+    rng = np.random.Generator(np.random.PCG64(seed + 104729))
+    v = d["v"]
+    dout = torch.from_numpy(_normal(rng, tuple(v.shape))).to(torch.bfloat16)
+    N = (d["cu_seqlens"].numel() - 1) if d.get("cu_seqlens") is not None else v.shape[0]
+    H, dk, dv = v.shape[2], d["q"].shape[-1], v.shape[-1]
+    g = None
+    if dhT:
+        g = torch.from_numpy((0.1 * _normal(rng, (N, H, dk, dv))).astype(np.float32))
+    return dout, g

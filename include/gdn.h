@@ -245,6 +245,51 @@ int gdn_kda_fwd_ex(const void* q, const void* k, const void* v, const float* g,
                    int dv, int path, int sp_parts, gdn_stream_t stream);
 
 /*
+ * gdn_kda_bwd -- gradients of gdn_kda_fwd (walk-through: cost table and
+ * memory paragraphs, a chunked model keeps only chunk-boundary states and
+ * recomputes the rest; the lqnn.cn page: block recompute). For the loss
+ * L = sum(dout * out) + sum(dhT * hT) it returns dL/dq, dk, dv, dg, dbeta and
+ * dL/dh0. One token's adjoint, for the gradient dS arriving at S_t:
+ *   dq_t = S_t^T do_t;  dS += do_t q_t^T;  du = dS k_t;
+ *   dk_t = dS^T u - beta_t S_bar^T du;  dbeta_t = du . (v_t - S_bar k_t);
+ *   dv_t = beta_t du;  dS_bar = dS - beta_t du k_t^T;
+ *   dg_t = column sums of dS_bar (.) S_bar;  dS_{t-1} = dS_bar diag(e^{g_t}).
+ * Inputs as gdn_kda_fwd (q, k, v bf16; g fp32 [B, T, H, dk]; beta fp32;
+ * h0 fp32 [N, H, dk, dv] or NULL), plus
+ *   dout   bf16 [B, T, H, dv], the gradient of out (device)
+ *   dhT    fp32 [N, H, dk, dv] or NULL (zero), the gradient of hT
+ * Outputs (device, fp32, written completely): dq, dk [B, T, H, dk]; dv
+ * [B, T, H, dv]; dg [B, T, H, dk]; dbeta [B, T, H]; dh0 [N, H, dk, dv] or
+ * NULL (not wanted; may be the dhT buffer). No output may alias an input
+ * other than dh0 = dhT.
+ * The forward state is recomputed on the GPU in fp32: a forward sweep keeps
+ * the state every 16 tokens, then each 16-token block is recomputed from its
+ * checkpoint and swept backwards. Scratch (cudaMallocAsync on `stream`):
+ * about 1 KB per token and 32 value rows for the checkpoints, plus 3 dk + 1
+ * floats per token, head and 32 value rows of partial sums. Asynchronous on
+ * `stream`; an invalid packing is recorded in the status word. Returns GDN_OK,
+ * GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED (head dims other than 64 / 128,
+ * more than 65535 sequences), GDN_ERR_MISALIGNED or GDN_ERR_CUDA.
+ */
+int gdn_kda_bwd(const void* q, const void* k, const void* v, const float* g,
+                const float* beta, const float* h0, const void* dout,
+                const float* dhT, float* dq, float* dk, float* dv, float* dg,
+                float* dbeta, float* dh0, const int32_t* cu_seqlens, int B,
+                int H, int T, int dk_dim, int dv_dim, gdn_stream_t stream);
+
+/*
+ * gdn_chunk_bwd -- the same for gdn_chunk_fwd's scalar gate (decay before
+ * the prediction): g and dg are fp32 [B, T, H] (every key channel shares the
+ * token's log-decay; dg is the sum of the per-channel gradient over the
+ * channels). Everything else as gdn_kda_bwd.
+ */
+int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
+                  const float* beta, const float* h0, const void* dout,
+                  const float* dhT, float* dq, float* dk, float* dv, float* dg,
+                  float* dbeta, float* dh0, const int32_t* cu_seqlens, int B,
+                  int H, int T, int dk_dim, int dv_dim, gdn_stream_t stream);
+
+/*
  * gdn_chunk_fwd_sp_noalloc -- the sequence-parallel forward pass of
  * gdn_chunk_fwd_ex (path GDN_PATH_SIMT, sp_parts >= 2) for callers that may
  * not allocate device memory while they enqueue work (for example a plugin
@@ -315,7 +360,10 @@ typedef enum {
                                    token */
   GDN_KERNEL_KDA_PREP = 8,      /* chunked KDA: state-independent part of
                                    every chunk (its chain is kernel 6) */
-  GDN_KERNEL_COUNT = 9
+  GDN_KERNEL_BWD = 9,           /* backward pass: checkpoints, recomputation
+                                   and the reverse sweep */
+  GDN_KERNEL_BWD_FINALIZE = 10, /* backward pass: sums over row blocks */
+  GDN_KERNEL_COUNT = 11
 } gdn_kernel_t;
 
 /* gdn_timing_enable -- per-kernel device timing on (nonzero) or off (0).

@@ -232,3 +232,33 @@ def test_kda_ex_rejects_on_host(lib, kw, expect):
 @pytest.mark.parametrize("path", [0, 1, 2, 4])
 def test_kda_ex_empty_batch_is_a_no_op(lib, path):
     assert kda_ex(lib.library(), path=path, B=0) == OK
+
+
+def bwd(so, fn="gdn_chunk_bwd", **kw):
+    a = dict(q=A, k=A + 0x1000, v=A + 0x2000, g=A + 0x3000, b=A + 0x4000,
+             h0=None, do=A + 0x5000, dhT=None, dq=A + 0x6000, dk=A + 0x7000,
+             dv=A + 0x8000, dg=A + 0x9000, db=A + 0xa000, dh0=None, cu=None,
+             B=1, H=1, T=16, dk_=128, dv_=128)
+    a.update(kw)
+    return getattr(so, fn)(a["q"], a["k"], a["v"], a["g"], a["b"], a["h0"],
+                           a["do"], a["dhT"], a["dq"], a["dk"], a["dv"],
+                           a["dg"], a["db"], a["dh0"], a["cu"], a["B"], a["H"],
+                           a["T"], a["dk_"], a["dv_"], None)
+
+
+@pytest.mark.parametrize("fn", ["gdn_chunk_bwd", "gdn_kda_bwd"])
+@pytest.mark.parametrize("kw,expect", [
+    (dict(B=-1), INVALID), (dict(H=0), INVALID), (dict(T=-1), INVALID),
+    (dict(q=None), INVALID), (dict(do=None), INVALID), (dict(dg=None), INVALID),
+    (dict(dk_=96), UNSUPPORTED), (dict(dv_=32), UNSUPPORTED),
+    (dict(B=70000), UNSUPPORTED), (dict(g=ODD), MISALIGNED),
+    (dict(dh0=ODD), MISALIGNED), (dict(dq=A), INVALID),
+    (dict(dv=A + 0x5000), INVALID), (dict(cu=A + 0xb000, B=0), INVALID),
+])
+def test_bwd_rejects_on_host(lib, fn, kw, expect):
+    assert bwd(lib.library(), fn, **kw) == expect
+
+
+@pytest.mark.parametrize("fn", ["gdn_chunk_bwd", "gdn_kda_bwd"])
+def test_bwd_empty_batch_is_a_no_op(lib, fn):
+    assert bwd(lib.library(), fn, B=0) == OK
