@@ -44,6 +44,8 @@ def _metric(w):
         return "GDN decode-step token-heads/s + % of GB300 HBM roofline, 1 GPU"
     if w["kind"] == "kda":
         return "KDA (per-channel decay) forward tokens/s + % of GB300 roofline, 1 GPU"
+    if w["kind"] == "bwd":
+        return "GDN backward tokens/s + % of GB300 fp32 ALU peak, 1 GPU"
     return METRIC
 
 # Algorithmic work per token-head of the chunked forward pass:
@@ -93,6 +95,10 @@ WORKLOADS = {
     "kda1": dict(kind="kda", B=4, H=16, T=2048, dk=128, dv=128, h0=False,
                  desc="gdn_kda_fwd_ex B=4 H=16 T=2048 dk=dv=128 bf16, "
                       "per-channel log-decays max(-softplus(N(0,1)), -5), h0=0"),
+    "bwd1": dict(kind="bwd", B=4, H=16, T=2048, dk=128, dv=128, h0=False,
+                 desc="gdn_chunk_bwd B=4 H=16 T=2048 dk=dv=128 bf16 inputs, "
+                      "fp32 gradients of out (dout ~ N(0,1) bf16), h0=0, "
+                      "no dhT"),
     "w4": dict(kind="decode", N=512, H=32, dk=128, dv=128,
                desc="gdn_recurrent_step N=512 H=32 dk=dv=128 bf16 token, "
                     "fp32 state in place"),
@@ -115,6 +121,7 @@ MEASURED_TRAFFIC = {
 def _kernel_source_hash(kind):
     csrc = ROOT / "gated_deltanet_chunkwise_gb300" / "csrc"
     files = (["decode.cu"] if kind == "decode"
+             else ["bwd.cu"] if kind == "bwd"
              else ["kda.cu", "kda_chunk.cu", "chunk_tc.cu"] if kind == "kda"
              else sorted(p.name for p in csrc.glob("chunk_*.cu")))
     h = hashlib.sha256()
@@ -248,6 +255,11 @@ def _make_inputs(w, seed=0):
     if w["kind"] == "kda":
         return inputs.kda_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
                                  seed=seed, h0=w["h0"])
+    if w["kind"] == "bwd":
+        d = inputs.chunk_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
+                                dtype="bf16", seed=seed, h0=w["h0"])
+        d["dout"], _ = inputs.grad_inputs(d, seed=seed, dhT=False)
+        return d
     return inputs.chunk_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
                                dtype="bf16", seed=seed, h0=w["h0"],
                                length_range=w.get("lengths"))
@@ -294,8 +306,14 @@ def run_ours(args, w, device, dist, rank, ws):
         N = nseq
         hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=device)
         want_hT = w["h0"]
+        last = {}  # the latest gradients of a backward step
 
         def step():
+            if w["kind"] == "bwd":
+                last["grads"] = gdn.gdn_chunk_bwd(
+                    d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"],
+                    d["dout"], None, want_dh0=False)
+                return
             if w["kind"] == "kda":
                 gdn.gdn_kda_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"],
                                    d["h0"], d["cu_seqlens"], out=out,
@@ -382,6 +400,12 @@ def run_ours(args, w, device, dist, rank, ws):
     h2d = sum(v.numel() * v.element_size() for v in pinned.values()
               if v is not None)
     d2h = out_host.numel() * out_host.element_size()
+    grads_host = {}
+    if w["kind"] == "bwd":
+        # the step's results are the gradients (no out)
+        grads_host = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                      for n, t in last["grads"].items() if t is not None}
+        d2h = sum(t.numel() * t.element_size() for t in grads_host.values())
     hT_host = None
     if w["kind"] != "decode" and w["h0"]:
         hT_host = torch.empty(hT.shape, dtype=torch.float32).pin_memory()
@@ -400,7 +424,11 @@ def run_ours(args, w, device, dist, rank, ws):
             if v_ is not None:
                 d[k_].copy_(v_, non_blocking=True)
         step()
-        out_host.copy_(out, non_blocking=True)
+        if grads_host:
+            for n_, t_ in grads_host.items():
+                t_.copy_(last["grads"][n_], non_blocking=True)
+        else:
+            out_host.copy_(out, non_blocking=True)
         if hT_host is not None:
             hT_host.copy_(hT, non_blocking=True)
         if w["kind"] == "decode":
@@ -427,6 +455,29 @@ def run_ours(args, w, device, dist, rank, ws):
         value = units_all / (ms * 1e-3) * (tok_heads / tokens)  # heads/s
         unit = "token-heads/s"
         e2e_val = units_all / (e2e_ms * 1e-3) * (tok_heads / tokens)
+    elif w["kind"] == "bwd":
+        # fp32 CUDA-core arithmetic per token-head: the forward states (decay
+        # d_k d_v, prediction and update 2 d_k d_v each) and the adjoint
+        # (S_t, dq, dS += do q^T, du, dS_bar, dg at 2 d_k d_v each, dk at 4,
+        # the decay of dS at 1): 22 d_k d_v; the recomputation of each block
+        # (5 d_k d_v more) is not counted
+        n_k, ms_k = kern.get("bwd_kernel", (0, 0.0))
+        k_ms = ms_k / n_k if n_k else ms
+        flops = 22 * dk * dv * tok_heads
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        mhz = _sm_max_mhz()
+        alu_tflops = sms * 128 * 2 * mhz * 1e6 / 1e12
+        achieved = flops / (k_ms * 1e-3) / 1e12
+        roof = {"bound": "alu", "kernel": "bwd_kernel",
+                "achieved": round(achieved, 2), "peak": round(alu_tflops, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / alu_tflops, 4),
+                "peak_source": f"derived: {sms} SMs x 128 fp32 FMA/cycle x 2 "
+                               f"x {mhz:.0f} MHz (max SM clock)",
+                "algorithmic_flops_per_launch": flops,
+                "launches_per_step": n_k / steps, "ms_per_launch": k_ms}
+        value = units_all / (ms * 1e-3)
+        unit = "tokens/s"
+        e2e_val = units_all / (e2e_ms * 1e-3)
     elif w["kind"] == "kda" and args.kda_path == "serial":
         # fp32 CUDA-core arithmetic per token-head: the decay d_k d_v
         # multiplies, then the prediction S k, the rank-1 update and the read
@@ -508,7 +559,8 @@ def run_ours(args, w, device, dist, rank, ws):
         "value": value, "unit": unit, "n_gpus": ws, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32" if (w["kind"] == "kda" and args.kda_path == "serial") else "bf16",
+        "dtype": "f32" if ((w["kind"] == "kda" and args.kda_path == "serial")
+                           or w["kind"] == "bwd") else "bf16",
         "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), "
                 + ("per-channel g=max(-softplus(N(0,1)),-5)"
                    if w["kind"] == "kda" else "g=-softplus(N(0,1))")
@@ -566,6 +618,20 @@ def cpu_baseline(w, d_host, budget_s=20.0):
                 "kind": "oracle",
                 "sample": f"full workload, oracle with the steps either side",
                 "seconds": round(dt, 3)}
+    if w["kind"] == "bwd":
+        from oracle import backward
+        Tsub = 512
+        sl = lambda x: x[:1, :Tsub, :1]
+        t0 = time.perf_counter()
+        backward.backward(sl(d_host["q"]), sl(d_host["k"]), sl(d_host["v"]),
+                          sl(d_host["g"]), sl(d_host["beta"]), None,
+                          sl(d_host["dout"]))
+        dt = time.perf_counter() - t0
+        return {"value": Tsub / w["H"] / dt, "unit": "tokens/s", "cores": 1,
+                "kind": "oracle",
+                "sample": f"1 sequence x 1 of {w['H']} heads x {Tsub} tokens "
+                          f"(reverse sweep, numpy), scaled to all heads",
+                "seconds": round(dt, 3)}
     if w["kind"] == "kda":
         from oracle import kda
         take = 1
@@ -621,6 +687,18 @@ def run_reference(args, w):
                                   d["state"])
         units, unit, sample = 64 * w["H"], "token-heads/s", \
             f"64 of {w['N']} sequences x {w['H']} heads, one token"
+    elif w["kind"] == "bwd":
+        from oracle import backward
+        T = 256
+        d = inputs.chunk_inputs(1, w["H"], T, w["dk"], w["dv"], dtype="bf16",
+                                seed=0)
+        dout, _ = inputs.grad_inputs(d, seed=0, dhT=False)
+
+        def step():
+            backward.backward(d["q"], d["k"], d["v"], d["g"], d["beta"], None,
+                              dout)
+        units, unit, sample = T, "tokens/s", \
+            f"one sequence of {T} tokens x all {w['H']} heads (reverse sweep)"
     elif w["kind"] == "kda":
         from oracle import kda
         T = 256
