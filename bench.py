@@ -108,13 +108,18 @@ WORKLOADS = {
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and the
 # hash of the kernel source it was taken on; a changed kernel reports null.
 MEASURED_TRAFFIC = {
-    # chunk_tc_kernel, W1, one launch (ncu --set full, caches flushed)
-    "w1:582e4a3241d2a6be": 168930560 + 20267008,
+    # chunk_tc_kernel, W1, one launch (caches flushed by the bench)
+    "w1:5c9f8f9802316b22": 168918272 + 19576832,
     # chain_tx_kernel, W3 (packed, 512 sequence-heads), one launch
-    "w3:582e4a3241d2a6be": 2999533312 + 598896640,
+    "w3:5c9f8f9802316b22": 2998424320 + 599070464,
     # decode_kernel captured with --sequences 128 and scaled x4 to N=512:
     # its traffic is proportional to the sequences processed
     "w4:83c7aa23b4500b6b": 4 * (271642880 + 210279936),
+    # kda_prep_kernel, kda1, one launch
+    "kda1:c10483a73ae27d16": 135346432 + 88019456,
+    # bwd_kernel, bwd1, one launch (the per-CTA windows of S_bar do not all
+    # stay in L2: most of the writes)
+    "bwd1:1e4b88f9f132c0dd": 762744832 + 4728071168,
 }
 
 
