@@ -96,3 +96,19 @@ def test_fused_unit_inputs_reduce_to_the_plain_path(lib, cuda_device):
     torch.cuda.synchronize(dev)
     h_ref = h2.cpu().numpy().astype(np.float64)
     assert rel_err(hT, h_ref) <= TOL
+
+
+def test_fused_bench_size_sampled(lib, cuda_device):
+    """B=4, H=16, T=2048 (the fused bench workload) in the bench's launch
+    configuration; two (sequence, head) pairs checked against the oracle
+    (heads are independent and the norm weight is shared, so the oracle runs
+    on their slices only)."""
+    d = inputs.fused_inputs(4, 16, 2048, 128, 128, seed=12, h0=False)
+    o, hT = run(lib, cuda_device, d)
+    for n, h in ((0, 0), (2, 9)):
+        sl = lambda t: None if t is None else t[n:n + 1, :, h:h + 1]
+        o_ref, h_ref = sublayer.fused_forward(
+            sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["a"]), sl(d["b"]), None,
+            weight=d["norm_weight"], gate=sl(d["gate"]), eps=1e-6)
+        assert rel_err(o[n:n + 1, :, h:h + 1], o_ref) <= TOL
+        assert rel_err(hT[n:n + 1, h:h + 1], h_ref) <= TOL
