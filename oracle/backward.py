@@ -18,6 +18,12 @@ and, given dS (the gradient arriving at S_t) and do_t, its adjoint is
     dbeta_t = du . e,  dv_t = beta_t du
     dS_bar = dS - beta_t du k_t^T
     dg_t = colsum(dS_bar (.) S_bar)     dS_{t-1} = dS_bar diag(a).
+With the other gate placement of the scalar gate (the lqnn.cn page, section
+1.2: correct against the undecayed state, then decay), one token is
+    e = v_t - S k_t,  u = beta_t e,  S_t = S diag(a) + u k_t^T,  o_t = S_t q_t
+and its adjoint differs in the last three steps:
+    dk_t = dS^T u - beta_t S^T du;  dg_t = colsum(dS (.) S diag(a));
+    dS_{t-1} = dS diag(a) - beta_t du k_t^T.
 The loss these gradients belong to is L = sum(dout (.) out) + sum(dhT (.)
 hT); tests/test_oracle_backward_pins.py pins the sweep against central
 finite differences of that loss computed with the forward oracles, against
@@ -49,11 +55,14 @@ def _sequences(B, T, cu_seqlens):
     return [slice(n * T, (n + 1) * T) for n in range(B)]
 
 
-def kda_backward(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None):
+def kda_backward(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None,
+                 decay_first=True):
     """Gradients of L = sum(dout * out) + sum(dhT * hT) for the per-channel
-    forward (``oracle.kda.forward``). q, k, g [B, T, H, dk]; v, dout [B, T,
-    H, dv]; beta [B, T, H]; h0, dhT [N, H, dk, dv] or None. Returns a dict
-    dq, dk, dv, dg, dbeta (shapes of the inputs) and dh0 [N, H, dk, dv]."""
+    forward (``oracle.kda.forward``; ``decay_first=False``: the placement
+    that predicts with the undecayed state). q, k, g [B, T, H, dk]; v, dout
+    [B, T, H, dv]; beta [B, T, H]; h0, dhT [N, H, dk, dv] or None. Returns a
+    dict dq, dk, dv, dg, dbeta (shapes of the inputs) and dh0 [N, H, dk,
+    dv]."""
     q, k, v, g, beta, h0, dout, dhT = map(
         _f64, (q, k, v, g, beta, h0, dout, dhT))
     B, T, H, dk = q.shape
@@ -69,12 +78,13 @@ def kda_backward(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None):
     for n, sl in enumerate(seqs):
         for h in range(H):
             S = np.zeros((dv, dk)) if h0 is None else h0[n, h].T.copy()
-            keep = []  # (S_bar, e, S_t) per token
+            keep = []  # (state the prediction reads, e, S_t) per token
             for t in range(sl.start, sl.stop):
-                Sb = S * np.exp(gf[t, h])[None, :]
-                e = vf[t, h] - Sb @ kf[t, h]
-                S = Sb + np.outer(bf[t, h] * e, kf[t, h])
-                keep.append((Sb, e, S))
+                a = np.exp(gf[t, h])[None, :]
+                Sp = S * a if decay_first else S
+                e = vf[t, h] - Sp @ kf[t, h]
+                S = (Sp if decay_first else S * a) + np.outer(bf[t, h] * e, kf[t, h])
+                keep.append((Sp, e, S))
             dS = np.zeros((dv, dk)) if dhT is None else dhT[n, h].T.copy()
             for i in range(len(keep) - 1, -1, -1):
                 t = sl.start + i
@@ -87,9 +97,14 @@ def kda_backward(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None):
                 grads["dk"][t, h] = dS.T @ u - b * (Sb.T @ du)
                 grads["dbeta"][t, h] = du @ e
                 grads["dv"][t, h] = b * du
-                dSb = dS - b * np.outer(du, kt)
-                grads["dg"][t, h] = (dSb * Sb).sum(axis=0)
-                dS = dSb * np.exp(gf[t, h])[None, :]
+                a = np.exp(gf[t, h])[None, :]
+                if decay_first:
+                    dSb = dS - b * np.outer(du, kt)
+                    grads["dg"][t, h] = (dSb * Sb).sum(axis=0)
+                    dS = dSb * a
+                else:
+                    grads["dg"][t, h] = (dS * Sb * a).sum(axis=0)
+                    dS = dS * a - b * np.outer(du, kt)
             dh0[n, h] = dS.T
     out = {n: x.reshape(B, T, H, -1) for n, x in grads.items()}
     out["dbeta"] = grads["dbeta"].reshape(B, T, H)
@@ -97,13 +112,15 @@ def kda_backward(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None):
     return out
 
 
-def backward(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None):
-    """The same for the scalar gate with the decay before the prediction
-    (``oracle.forward`` with variant G1): g [B, T, H] is every channel's
+def backward(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None,
+             variant=1):
+    """The same for the scalar gate (``oracle.forward``; variant 1 = G1,
+    decay before the prediction, 0 = G0): g [B, T, H] is every channel's
     log-decay, so dg is the sum over channels of the per-channel one."""
     g = _f64(g)
     dk = np.asarray(_f64(q)).shape[-1]
     gk = np.repeat(g[..., None], dk, axis=-1)
-    out = kda_backward(q, k, v, gk, beta, h0, dout, dhT, cu_seqlens)
+    out = kda_backward(q, k, v, gk, beta, h0, dout, dhT, cu_seqlens,
+                       decay_first=(variant == 1))
     out["dg"] = out["dg"].sum(axis=-1)
     return out

@@ -87,6 +87,31 @@ def test_scalar_gate_gradients_match_finite_differences_of_the_c_oracle():
     check_fd(c, grads, fwd)
 
 
+def test_g0_placement_gradients_match_finite_differences_of_the_c_oracle():
+    """The other gate placement (predict with the undecayed state, then
+    decay) against the C token loop with variant G0."""
+    c = rand_case(2, 6, 1, 3, 2, seed=7, scalar=True)
+    grads = backward.backward(c["q"], c["k"], c["v"], c["g"], c["beta"],
+                              c["h0"], c["dout"], c["dhT"], variant=oracle.G0)
+    fwd = lambda *a, cu_seqlens=None: oracle.forward(*a, cu_seqlens=cu_seqlens,
+                                                     variant=oracle.G0)
+    check_fd(c, grads, fwd)
+
+
+def test_g0_and_g1_gradients_agree_without_decay():
+    """g = 0: the two placements are the same map (plain DeltaNet), so all
+    gradients but dg agree (dg does not: the maps differ for g != 0)."""
+    c = rand_case(1, 6, 2, 4, 3, seed=8, scalar=True)
+    c["g"][:] = 0.0
+    g1 = backward.backward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"],
+                           c["dout"], c["dhT"], variant=oracle.G1)
+    g0 = backward.backward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["h0"],
+                           c["dout"], c["dhT"], variant=oracle.G0)
+    for n in ("dq", "dk", "dv", "dbeta", "dh0"):
+        assert np.allclose(g0[n], g1[n], atol=1e-12), n
+    assert not np.allclose(g0["dg"], g1["dg"])
+
+
 def test_closed_form_without_writes_or_decay():
     """beta = 0, g = 0: S_t = S_0 for every t, so dq_t = S_0^T dout_t,
     dh0 = dhT + sum_t q_t dout_t^T (as d_k x d_v), dk = dv = 0, and with
