@@ -99,10 +99,12 @@ def library():
     lib.gdn_kda_fwd_ex.argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, ip, i, i, i,
                                    i, i, i, i, vp]
     lib.gdn_kda_fwd_ex.restype = i
-    for name in ("gdn_kda_bwd", "gdn_chunk_bwd"):
-        getattr(lib, name).argtypes = [vp, vp, vp, fp, fp, fp, vp, fp, fp, fp,
-                                       fp, fp, fp, fp, ip, i, i, i, i, i, vp]
-        getattr(lib, name).restype = i
+    bwd_args = [vp, vp, vp, fp, fp, fp, vp, fp, fp, fp, fp, fp, fp, fp, ip, i,
+                i, i, i, i]
+    lib.gdn_kda_bwd.argtypes = bwd_args + [vp]
+    lib.gdn_kda_bwd.restype = i
+    lib.gdn_chunk_bwd.argtypes = bwd_args + [i, vp]
+    lib.gdn_chunk_bwd.restype = i
     lib.gdn_device_status.argtypes = [vp]
     lib.gdn_device_status.restype = i
     lib.gdn_status_string.argtypes = [i]
@@ -270,15 +272,15 @@ def gdn_kda_bwd(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None, *,
 
 
 def gdn_chunk_bwd(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None, *,
-                  want_dh0=True, stream=None):
-    """Gradients of gdn_chunk_fwd (scalar gate, decay before the prediction):
-    as gdn_kda_bwd with g and dg [B, T, H]."""
+                  variant=GDN_GATE_BEFORE_PREDICT, want_dh0=True, stream=None):
+    """Gradients of gdn_chunk_fwd_ex (scalar gate; ``variant`` the forward's
+    gate placement): as gdn_kda_bwd with g and dg [B, T, H]."""
     return _bwd("gdn_chunk_bwd", q, k, v, g, beta, h0, dout, dhT, cu_seqlens,
-                want_dh0, stream, per_channel=False)
+                want_dh0, stream, per_channel=False, extra=(int(variant),))
 
 
 def _bwd(fn, q, k, v, g, beta, h0, dout, dhT, cu_seqlens, want_dh0, stream,
-         per_channel):
+         per_channel, extra=()):
     dev = q.device
     _need(q, "q", torch.bfloat16, None)
     for name, t in (("k", k), ("v", v), ("dout", dout)):
@@ -314,7 +316,7 @@ def _bwd(fn, q, k, v, g, beta, h0, dout, dhT, cu_seqlens, want_dh0, stream,
             _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
             _ptr(dout), _ptr(dhT), _ptr(res["dq"]), _ptr(res["dk"]),
             _ptr(res["dv"]), _ptr(res["dg"]), _ptr(res["dbeta"]),
-            _ptr(res["dh0"]), _ptr(cu_seqlens), N, H, T, dk, dv,
+            _ptr(res["dh0"]), _ptr(cu_seqlens), N, H, T, dk, dv, *extra,
             _stream(stream))
     if rc != GDN_OK:
         raise GdnError(rc, fn)

@@ -27,6 +27,11 @@
 // a fixed-order sum, so the result does not depend on warp timing) and leave
 // as one partial per row block; a second kernel adds the row blocks' partials
 // (and, for the scalar gate, the channels of dg).
+//
+// With the other gate placement (predict with the undecayed state S, then
+// decay: S_t = S diag(a_t) + u k_t^T) the window keeps S instead of S_bar and
+// the adjoint's last steps become dk_t = dS^T u - beta_t S^T du, dg_t =
+// colsum(dS (.) S diag(a_t)), dS_{t-1} = dS diag(a_t) - beta_t du k_t^T.
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -55,6 +60,7 @@ struct BwdArgs {
   const int32_t* cu_seqlens;
   const int32_t* blk_off;  // [N + 1] first 16-token block of each sequence
   int N, H, T, dv, g_chan;  // g_chan: dk (per channel) or 1 (scalar gate)
+  int decay_first;          // 1: decay, then predict; 0: predict, then decay
   long long rows;           // tokens * H
   int* status;
 };
@@ -239,7 +245,9 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
 #pragma unroll
     for (int r = 0; r < kBwRpw; ++r) ld_slice<CPT>(src + CPT * r, X[r]);
   };
-  // one forward token on S (registers); returns e for row rr in `e_rr`
+  const bool dfirst = a.decay_first != 0;
+  // one forward token on S (registers); `save` receives the state the
+  // prediction reads; returns e for row rr
   auto forward_token = [&](int tt, float* save) {
     float av[CPT], kv[CPT];
     ld_slice<CPT>(&sm[L::SA + tt * DK + CPT * lane], av);
@@ -250,7 +258,7 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
       p[r] = 0.f;
 #pragma unroll
       for (int j = 0; j < CPT; ++j) {
-        S[r][j] *= av[j];
+        if (dfirst) S[r][j] *= av[j];
         p[r] = fmaf(S[r][j], kv[j], p[r]);
       }
     }
@@ -262,7 +270,8 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
     for (int r = 0; r < kBwRpw; ++r) {
       const float u = __shfl_sync(0xffffffffu, ur, 8 * r);
 #pragma unroll
-      for (int j = 0; j < CPT; ++j) S[r][j] = fmaf(u, kv[j], S[r][j]);
+      for (int j = 0; j < CPT; ++j)
+        S[r][j] = fmaf(u, kv[j], dfirst ? S[r][j] : S[r][j] * av[j]);
     }
     return e;
   };
@@ -325,7 +334,8 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
         pdu[r] = 0.f;
 #pragma unroll
         for (int j = 0; j < CPT; ++j) {
-          dq[j] = fmaf(fmaf(u, kv[j], Sb[r][j]), dor[r], dq[j]);  // S_t^T do
+          const float st = fmaf(u, kv[j], dfirst ? Sb[r][j] : Sb[r][j] * av[j]);
+          dq[j] = fmaf(st, dor[r], dq[j]);  // S_t^T do
           dS[r][j] = fmaf(dor[r], qv[j], dS[r][j]);
           pdu[r] = fmaf(dS[r][j], kv[j], pdu[r]);
         }
@@ -341,9 +351,15 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
         for (int j = 0; j < CPT; ++j) {
           dkk[j] = fmaf(dS[r][j], u, dkk[j]);
           dkk[j] = fmaf(-bdu, Sb[r][j], dkk[j]);
-          const float dsb = fmaf(-bdu, kv[j], dS[r][j]);
-          dg[j] = fmaf(dsb, Sb[r][j], dg[j]);
-          dS[r][j] = dsb * av[j];
+          if (dfirst) {
+            const float dsb = fmaf(-bdu, kv[j], dS[r][j]);
+            dg[j] = fmaf(dsb, Sb[r][j], dg[j]);
+            dS[r][j] = dsb * av[j];
+          } else {
+            const float ds = dS[r][j] * av[j];
+            dg[j] = fmaf(ds, Sb[r][j], dg[j]);
+            dS[r][j] = fmaf(-bdu, kv[j], ds);
+          }
         }
       }
       if ((lane & 7) == 0) sm[L::SDV + tt * kBwRows + kBwRpw * w + rr] = bt * du_rr;
@@ -444,8 +460,11 @@ int run_bwd(const void* q, const void* k, const void* v, const float* g,
             const float* beta, const float* h0, const void* dout,
             const float* dhT, float* dq, float* dk, float* dvo, float* dg,
             float* dbeta, float* dh0, const int32_t* cu_seqlens, int B, int H,
-            int T, int dk_, int dv, bool per_channel, cudaStream_t stream) {
+            int T, int dk_, int dv, bool per_channel, int variant,
+            cudaStream_t stream) {
   if (B < 0 || H <= 0 || T < 0) return GDN_ERR_INVALID_ARG;
+  if (variant != GDN_GATE_BEFORE_PREDICT && variant != GDN_GATE_AFTER_PREDICT)
+    return GDN_ERR_INVALID_ARG;
   if (cu_seqlens && B == 0) return GDN_ERR_INVALID_ARG;
   if ((dk_ != 64 && dk_ != 128) || (dv != 64 && dv != 128))
     return GDN_ERR_UNSUPPORTED;
@@ -497,6 +516,7 @@ int run_bwd(const void* q, const void* k, const void* v, const float* g,
   a.cu_seqlens = cu_seqlens;
   a.N = B; a.H = H; a.T = T; a.dv = dv;
   a.g_chan = per_channel ? dk_ : 1;
+  a.decay_first = variant == GDN_GATE_BEFORE_PREDICT ? 1 : 0;
   a.rows = (long long)rows;
   a.status = status;
   cudaError_t e = cudaSuccess;
@@ -544,7 +564,7 @@ extern "C" int gdn_kda_bwd(const void* q, const void* k, const void* v,
                            int T, int dk_, int dv_, gdn_stream_t stream) {
   return gdn::run_bwd(q, k, v, g, beta, h0, dout, dhT, dq, dk, dv, dg, dbeta, dh0,
                       cu_seqlens, B, H, T, dk_, dv_, true,
-                      static_cast<cudaStream_t>(stream));
+                      GDN_GATE_BEFORE_PREDICT, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int gdn_chunk_bwd(const void* q, const void* k, const void* v,
@@ -552,9 +572,9 @@ extern "C" int gdn_chunk_bwd(const void* q, const void* k, const void* v,
                              const void* dout, const float* dhT, float* dq,
                              float* dk, float* dv, float* dg, float* dbeta,
                              float* dh0, const int32_t* cu_seqlens, int B,
-                             int H, int T, int dk_, int dv_,
+                             int H, int T, int dk_, int dv_, int variant,
                              gdn_stream_t stream) {
   return gdn::run_bwd(q, k, v, g, beta, h0, dout, dhT, dq, dk, dv, dg, dbeta, dh0,
-                      cu_seqlens, B, H, T, dk_, dv_, false,
+                      cu_seqlens, B, H, T, dk_, dv_, false, variant,
                       static_cast<cudaStream_t>(stream));
 }

@@ -278,16 +278,22 @@ int gdn_kda_bwd(const void* q, const void* k, const void* v, const float* g,
                 int H, int T, int dk_dim, int dv_dim, gdn_stream_t stream);
 
 /*
- * gdn_chunk_bwd -- the same for gdn_chunk_fwd's scalar gate (decay before
- * the prediction): g and dg are fp32 [B, T, H] (every key channel shares the
- * token's log-decay; dg is the sum of the per-channel gradient over the
- * channels). Everything else as gdn_kda_bwd.
+ * gdn_chunk_bwd -- the same for gdn_chunk_fwd_ex's scalar gate: g and dg are
+ * fp32 [B, T, H] (every key channel shares the token's log-decay; dg is the
+ * sum of the per-channel gradient over the channels), and `variant` is the
+ * gate placement of the forward pass: GDN_GATE_BEFORE_PREDICT (gdn_chunk_fwd's
+ * default) or GDN_GATE_AFTER_PREDICT (predict with the undecayed state, then
+ * decay; the adjoint's last steps become dk_t = dS^T u - beta_t S^T du,
+ * dg_t = sum(dS (.) S) e^{g_t}, dS_{t-1} = e^{g_t} dS - beta_t du k_t^T with
+ * S = S_{t-1}); anything else returns GDN_ERR_INVALID_ARG. Everything else
+ * as gdn_kda_bwd.
  */
 int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
                   const float* beta, const float* h0, const void* dout,
                   const float* dhT, float* dq, float* dk, float* dv, float* dg,
                   float* dbeta, float* dh0, const int32_t* cu_seqlens, int B,
-                  int H, int T, int dk_dim, int dv_dim, gdn_stream_t stream);
+                  int H, int T, int dk_dim, int dv_dim, int variant,
+                  gdn_stream_t stream);
 
 /*
  * gdn_chunk_fwd_sp_noalloc -- the sequence-parallel forward pass of

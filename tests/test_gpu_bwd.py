@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from oracle import backward
 from gated_deltanet_chunkwise_gb300 import inputs
 
@@ -23,17 +24,27 @@ def rel_err(x, ref):
     return float(np.max(np.abs(x - ref)) / max(np.max(np.abs(ref)), 1e-30))
 
 
-def run_and_check(lib, dev, d, scalar, *, dhT=True, seed=0):
+def run_and_check(lib, dev, d, scalar, *, dhT=True, seed=0, after=False):
+    """after: the gate placement that predicts with the undecayed state
+    (GDN_GATE_AFTER_PREDICT; the oracle's G0)."""
     dout, dh = inputs.grad_inputs(d, seed=seed, dhT=dhT)
     x = lambda t: None if t is None else t.to(dev)
-    fn = lib.gdn_chunk_bwd if scalar else lib.gdn_kda_bwd
-    got = fn(x(d["q"]), x(d["k"]), x(d["v"]), x(d["g"]), x(d["beta"]),
-             x(d["h0"]), x(dout), x(dh), x(d["cu_seqlens"]))
+    args = (x(d["q"]), x(d["k"]), x(d["v"]), x(d["g"]), x(d["beta"]),
+            x(d["h0"]), x(dout), x(dh), x(d["cu_seqlens"]))
+    if scalar:
+        got = lib.gdn_chunk_bwd(*args, variant=lib.GDN_GATE_AFTER_PREDICT if after
+                                else lib.GDN_GATE_BEFORE_PREDICT)
+    else:
+        got = lib.gdn_kda_bwd(*args)
     torch.cuda.synchronize(dev)
     assert lib.gdn_device_status() == 0
-    ref_fn = backward.backward if scalar else backward.kda_backward
-    ref = ref_fn(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], dout, dh,
-                 cu_seqlens=d["cu_seqlens"])
+    if scalar:
+        ref = backward.backward(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                d["h0"], dout, dh, cu_seqlens=d["cu_seqlens"],
+                                variant=oracle.G0 if after else oracle.G1)
+    else:
+        ref = backward.kda_backward(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                    d["h0"], dout, dh, cu_seqlens=d["cu_seqlens"])
     errs = {n: rel_err(got[n], ref[n]) for n in GRADS + ("dh0",)}
     assert all(e <= TOL for e in errs.values()), errs
     return errs
@@ -50,6 +61,18 @@ def test_kda_bwd_matches_oracle(lib, cuda_device, dk, dv, h0):
 def test_scalar_bwd_lengths(lib, cuda_device, T):
     d = inputs.chunk_inputs(1, 2, T, 128, 128, dtype="bf16", seed=62, h0=True)
     run_and_check(lib, cuda_device, d, scalar=True, seed=2)
+
+
+@pytest.mark.parametrize("T", [1, 17, 200])
+def test_scalar_bwd_other_gate_placement(lib, cuda_device, T):
+    d = inputs.chunk_inputs(2, 2, T, 128, 128, dtype="bf16", seed=68, h0=True)
+    run_and_check(lib, cuda_device, d, scalar=True, seed=7, after=True)
+
+
+def test_scalar_bwd_other_gate_placement_packed(lib, cuda_device):
+    d = inputs.chunk_inputs(0, 2, 0, 128, 64, dtype="bf16", seed=69, h0=True,
+                            lengths=[33, 0, 70, 5])
+    run_and_check(lib, cuda_device, d, scalar=True, seed=8, after=True)
 
 
 def test_scalar_bwd_without_dhT(lib, cuda_device):
