@@ -112,7 +112,8 @@ struct BwSmem {
                        SV = SA + kBwTok * DK, SDO = SV + kBwTok * kBwRows,
                        SE = SDO + kBwTok * kBwRows, SDV = SE + kBwTok * kBwRows,
                        SB = SDV + kBwTok * kBwRows;
-  static constexpr int RW = 3 * DK + 1;  // one warp's partial: dq, dk, dg, dbeta
+  // one warp's partial: dq, dk, dg, dbeta (padded to 16-byte rows)
+  static constexpr int RW = 3 * DK + 4;
   static constexpr int SLOT = SB + kBwTok, ACC = SLOT + 2 * 8 * RW,
                        TOTAL = ACC + kBwTok * RW;
 };
@@ -122,6 +123,9 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
   constexpr int CPT = DK / 32;            // channels per lane
   constexpr int NS = kBwRpw * CPT;        // state floats per thread
   using L = BwSmem<DK>;
+  static_assert(L::SLOT % 4 == 0 && L::RW % 4 == 0 && L::SDO % 4 == 0 &&
+                    L::SE % 4 == 0 && L::SA % 4 == 0,
+                "16-byte shared-memory accesses");
   extern __shared__ float4 smem4[];
   float* sm = reinterpret_cast<float*>(smem4);
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -320,11 +324,8 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
       ld_slice<CPT>(&sm[L::SQ + tt * DK + CPT * lane], qv);
       const float bt = sm[L::SB + tt];
       float dor[kBwRpw], er[kBwRpw];
-#pragma unroll
-      for (int r = 0; r < kBwRpw; ++r) {
-        dor[r] = sm[L::SDO + tt * kBwRows + kBwRpw * w + r];
-        er[r] = sm[L::SE + tt * kBwRows + kBwRpw * w + r];
-      }
+      ld_slice<kBwRpw>(&sm[L::SDO + tt * kBwRows + kBwRpw * w], dor);
+      ld_slice<kBwRpw>(&sm[L::SE + tt * kBwRows + kBwRpw * w], er);
       float dq[CPT], dkk[CPT], dg[CPT], pdu[kBwRpw];
 #pragma unroll
       for (int j = 0; j < CPT; ++j) dq[j] = dkk[j] = dg[j] = 0.f;
@@ -366,16 +367,19 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
       // this warp's partial into its slot, then a fixed-order sum over the
       // eight warps (slots alternate between tokens: one barrier each)
       float* slot = sm + L::SLOT + (tt & 1) * 8 * L::RW + w * L::RW;
-#pragma unroll
-      for (int j = 0; j < CPT; ++j) {
-        slot[CPT * lane + j] = dq[j];
-        slot[DK + CPT * lane + j] = dkk[j];
-        slot[2 * DK + CPT * lane + j] = dg[j];
-      }
+      auto st_slice = [&](float* dst, const float (&x)[CPT]) {
+        if constexpr (CPT == 4)
+          *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
+        else
+          *reinterpret_cast<float2*>(dst) = make_float2(x[0], x[1]);
+      };
+      st_slice(slot + CPT * lane, dq);
+      st_slice(slot + DK + CPT * lane, dkk);
+      st_slice(slot + 2 * DK + CPT * lane, dg);
       if (lane == 0) slot[3 * DK] = dbeta;
       __syncthreads();
       const float* s0 = sm + L::SLOT + (tt & 1) * 8 * L::RW;
-      for (int idx = tid; idx < L::RW; idx += kBwThreads) {
+      for (int idx = tid; idx < 3 * DK + 1; idx += kBwThreads) {
         float acc = 0.f;
 #pragma unroll
         for (int ww = 0; ww < 8; ++ww) acc += s0[ww * L::RW + idx];
