@@ -119,7 +119,7 @@ MEASURED_TRAFFIC = {
     "kda1:c10483a73ae27d16": 135346432 + 88019456,
     # bwd_kernel, bwd1, one launch (the per-CTA windows of S_bar do not all
     # stay in L2: most of the writes)
-    "bwd1:1e4b88f9f132c0dd": 762744832 + 4728071168,
+    "bwd1:f86ac4026bf4de8b": 763373312 + 4999033088,
 }
 
 
