@@ -53,7 +53,8 @@ def test_forward_random(lib, cuda_device, seed):
     d = inputs.chunk_inputs(cfg["B"], cfg["H"], cfg["T"], 128, cfg["dv"],
                             dtype="bf16", seed=seed, h0=cfg["h0"], **kw(cfg))
     x = lambda t: None if t is None else t.to(cuda_device)
-    # a split needs one sequence of enough chunks; packed calls take it too
+    # sp > 0 forces that many sub-sequences (parts past a short sequence's end
+    # stay empty)
     path = cfg["path"] | (cfg["combine"] if cfg["sp"] else 0)
     o, hT = lib.gdn_chunk_fwd_ex(x(d["q"]), x(d["k"]), x(d["v"]), x(d["g"]),
                                  x(d["beta"]), x(d["h0"]), x(d["cu_seqlens"]),
