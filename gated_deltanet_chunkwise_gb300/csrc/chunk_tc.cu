@@ -1981,6 +1981,23 @@ int sm_count() {
 
 }  // namespace
 
+bool make_rows_map(CUtensorMap* map, const void* ptr, bool fp32, long long d0,
+                   long long d1, long long d2, uint32_t b0, uint32_t b2) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const long long es = fp32 ? 4 : 2;
+  cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+  cuuint64_t strides[2] = {(cuuint64_t)(d0 * es), (cuuint64_t)(d0 * d1 * es)};
+  cuuint32_t box[3] = {b0, 1, b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map,
+             fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+             3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool chunk_tc_supported(int dk, int dv, long long tokens, int N, int H) {
   // chunk-tile indices (chunk * H + head) and token rows stay in int
   return dk == DK && (dv == 64 || dv == 128) && tokens > 0 &&

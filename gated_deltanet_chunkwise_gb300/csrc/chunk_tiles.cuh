@@ -275,4 +275,11 @@ constexpr int KCV_FLOATS = 256;
 constexpr uint32_t KCV_BYTES = KCV_FLOATS * 4;
 
 }  // namespace
+
+// Tensor map over a [d2][d1][d0] row-major tensor (bf16, or fp32 when
+// `fp32`) whose box is b0 x 1 x b2 elements with no swizzle: the box lands
+// in shared memory as b2 rows of b0 contiguous elements (host side).
+bool make_rows_map(CUtensorMap* map, const void* ptr, bool fp32, long long d0,
+                   long long d1, long long d2, uint32_t b0, uint32_t b2);
+
 }  // namespace gdn

@@ -34,12 +34,16 @@
 // takes the exact pairwise sum instead (one exp per term; slow, but only for
 // such chunks).
 //
-// One CTA of 256 threads per (chunk, head) at a time, two CTAs per SM; plain
-// loads in (the rows are 256 / 512 contiguous bytes), tensor-core products
-// with mma.sync m16n8k16 (bf16 in, fp32 accumulate) from ldmatrix fragments,
-// the inverse by the blocked substitution shared with the scalar-gate
-// preparation, images out by bulk copies (P, T_U, -W) or direct stores (Q_g,
-// K_d: each thread owns two key channels of one 16-token block).
+// One CTA of 256 threads per (chunk, head) at a time, two CTAs per SM,
+// persistent. The g and k rows of the CTA's next item arrive by two
+// tensor-map copies into the operand tables' space once the A and P products
+// have read them (per-thread loads of those rows were held to about 2.5 TB/s
+// by the requests an SM keeps in flight); q rows by per-thread loads.
+// Tensor-core products with mma.sync m16n8k16 (bf16 in, fp32 accumulate)
+// from ldmatrix fragments, the inverse by the blocked substitution shared
+// with the scalar-gate preparation; images out by a bulk copy (P) or plain
+// stores (T_U, -W, Q_g, K_d: a proxy fence while the next rows land would
+// wait for them).
 #include "chunk_tiles.cuh"
 
 namespace gdn {
@@ -57,17 +61,24 @@ constexpr uint32_t KP_KE = 0, KP_QE = KP_TAB, KP_KB = 2 * KP_TAB,
 // exact fallback: Gamma in fp32 over K_E / Q_E, raw K in the K_B table
 constexpr int GP = 132;
 constexpr uint32_t KP_GAM = 0;
-// -W image after the solve, over K_E / Q_E
-constexpr uint32_t KP_W = 0;
 constexpr uint32_t KP_AT = 4 * KP_TAB;             // fp32 A, then T (pitch AP)
+// -W image after T_U is built, over the solve buffer
+constexpr uint32_t KP_W = KP_AT;
+// The next item's g rows (fp32 [64][d_k]) and k rows (bf16 [64][d_k]) arrive
+// by bulk copies over K_E / Q_E and K_B once the A and P products are done
+constexpr uint32_t KP_SG = 0, KP_SK = KP_KB;
 constexpr uint32_t KP_P = KP_AT + 64 * AP * 4;     // P image
 constexpr uint32_t KP_TU = KP_P + TILE_BYTES;      // T_U image
 constexpr uint32_t KP_V = KP_TU + TILE_BYTES;      // 6 pair vectors x 128
 constexpr uint32_t KP_QT = KP_V + 6 * DK * 4;      // per-block decay totals
 constexpr uint32_t KP_BETA = KP_QT + 4 * DK * 4;    // beta (0 past the end)
-constexpr uint32_t KP_SMEM = KP_BETA + 64 * 4 + 1024;
+constexpr uint32_t KP_BAR = KP_BETA + 64 * 4;       // stage mbarrier, abort flag
+constexpr uint32_t KP_SMEM = KP_BAR + 16 + 1024;
 static_assert(64 * GP * 4 <= KP_KB, "Gamma table overlaps the raw K table");
-static_assert(2 * WS_W_BYTES <= KP_KB, "-W image overlaps K_G");
+static_assert(WS_W_BYTES <= 64 * AP * 4, "-W image fits the solve buffer");
+static_assert(64 * DK * 4 <= KP_KB && KP_SK + 64 * DK * 2 <= KP_KG,
+              "row stage fits the operand tables");
+static_assert(KP_BAR % 8 == 0, "mbarrier alignment");
 static_assert(KP_P % 1024 == 0 && KP_TU % 1024 == 0, "image alignment");
 static_assert(kKpCtas * (KP_SMEM + 1024) <= 233472, "two CTAs per SM");
 // largest |log2 factor| a table entry may carry
@@ -112,7 +123,10 @@ __device__ __forceinline__ float bf16_bits(uint32_t b) {
 }
 
 __global__ void __launch_bounds__(kKpThreads, kKpCtas)
-    kda_prep_kernel(const ChunkParams p, int nch_dense, int total_chunks_bound) {
+    kda_prep_kernel(const ChunkParams p,
+                    const __grid_constant__ CUtensorMap tmg,
+                    const __grid_constant__ CUtensorMap tmk, int nch_dense,
+                    int total_chunks_bound) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -144,13 +158,43 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
     t0 = bos + (long long)lc * C;
     len = (int)max(0ll, min((long long)C, eos - t0));
   };
+  uint64_t* sbar = reinterpret_cast<uint64_t*>(sm + KP_BAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + KP_BAR + 8);
+  if (tid == 0) {
+    mbar_init(sbar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // Item it_'s g and k rows (64 tokens of one head: tiles of d_k x 64,
+  // rows past the tensor's end zero-filled, rows past the sequence's end
+  // unused) into the stage by two tensor-map copies that complete on the
+  // stage barrier; one thread. q is loaded per thread: the tables leave no
+  // room for its rows.
+  auto issue_stage = [&](int it_) {
+    int h_, len_;
+    long long t0_;
+    chunk_of(it_, h_, t0_, len_);
+    mbar_arrive_expect_tx(sbar, 64 * DK * 4 + 64 * DK * 2);
+    tma_load_3d(sm + KP_SG, &tmg, sbar, 0, h_, (int)t0_);
+    tma_load_3d(sm + KP_SK, &tmk, sbar, 0, h_, (int)t0_);
+  };
+  int staged = 0, li = 0;  // stages issued, stages consumed (same in every thread)
+  if (blockIdx.x < items) {
+    if (tid == 0) {
+      prefetch_tmap(&tmg);
+      prefetch_tmap(&tmk);
+      issue_stage(blockIdx.x);
+    }
+    ++staged;
+  }
 
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
     int h, len;
     long long t0;
     chunk_of(it, h, t0, len);
-    // the CTA's next item into L2 while this one is processed: its rows of
-    // g (512 bytes), k and q (256 bytes each)
+    // the CTA's next item's q rows (256 bytes each) into L2 while this one
+    // is processed (its g and k rows come by the stage)
     if (warp == 7 && it + (int)gridDim.x < items) {
       int h2, len2;
       long long t2;
@@ -160,15 +204,16 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
         const int t = lane + 32 * hf;
         if (t < len2) {
           const size_t e = ((size_t)(t2 + t) * H + h2) * DK;
-          prefetch_l2(p.g + e, DK * 4);
-          prefetch_l2(kin + e, DK * 2);
           prefetch_l2(qin + e, DK * 2);
         }
       }
     }
-    // the previous item's bulk copies have read their images
+    // the previous item's bulk copies have read their images; this item's
+    // rows have landed
     if (tid == 0) bulk_wait_read();
-    __syncthreads();
+    const bool landed = mbar_wait(sbar, li & 1, abort_flag);
+    if (!bar_and(2, kKpThreads, landed)) break;
+    ++li;
 
     // ---- 1. cumulative log2-decay over the chunk --------------------------
     // thread (block R1 = tid >> 6, channel pair cp = tid & 63): tokens
@@ -184,11 +229,11 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
       for (int j = 0; j < 16; ++j) {
         float2 gv = make_float2(0.f, 0.f);
         uint32_t kb = 0, qb = 0;
-        if (16 * R1 + j < len) {
-          const size_t e = e0 + (size_t)j * rs;
-          gv = __ldg(reinterpret_cast<const float2*>(p.g + e));
-          kb = __ldg(reinterpret_cast<const uint32_t*>(kin + e));
-          qb = __ldg(reinterpret_cast<const uint32_t*>(qin + e));
+        const int t = 16 * R1 + j;
+        if (t < len) {
+          gv = *reinterpret_cast<const float2*>(sm + KP_SG + t * (DK * 4) + c0 * 4);
+          kb = *reinterpret_cast<const uint32_t*>(sm + KP_SK + t * (DK * 2) + c0 * 2);
+          qb = __ldg(reinterpret_cast<const uint32_t*>(qin + e0 + (size_t)j * rs));
         }
         x[j] = make_float2(gv.x * kLog2e, gv.y * kLog2e);
         kk2[j] = kb;
@@ -386,6 +431,15 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
                  TILE_BYTES);
       bulk_commit();
     }
+    // the operand tables are read: the next item's rows may land over them
+    // while the inverse and W run (warp 7 does not take part in the solve)
+    if (it + (int)gridDim.x < items) {
+      if (tid == 7 * 32) {
+        fence_proxy_async();
+        issue_stage(it + gridDim.x);
+      }
+      ++staged;
+    }
 
     // ---- 4. T = (I + A)^{-1}; T_U = T diag(beta) -------------------------
     if (warp < 4) solve_unit_lower(AT, tid);
@@ -398,7 +452,11 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
         const float4 v = *reinterpret_cast<const float4*>(AT + r * AP + 16 * q4 + 4 * c4);
         tv[4 * c4] = v.x; tv[4 * c4 + 1] = v.y; tv[4 * c4 + 2] = v.z; tv[4 * c4 + 3] = v.w;
       }
+      // to shared memory (the W product's operand) and straight to the
+      // workspace: plain stores, since a proxy fence here would wait for the
+      // next item's rows still landing
       uint8_t* tu = sm + KP_TU;
+      uint8_t* tug = static_cast<uint8_t*>(p.tu) + (size_t)it * WS_TU_BYTES;
 #pragma unroll
       for (int h8 = 0; h8 < 2; ++h8) {
         float y[8];
@@ -414,15 +472,10 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
         w.z = pack_bf16x2(y[4], y[5]);
         w.w = pack_bf16x2(y[6], y[7]);
         *reinterpret_cast<uint4*>(tu + sw128(r, 2 * q4 + h8)) = w;
+        *reinterpret_cast<uint4*>(tug + sw128(r, 2 * q4 + h8)) = w;
       }
-      fence_proxy_async();
     }
     __syncthreads();
-    if (tid == 0) {
-      bulk_store(static_cast<uint8_t*>(p.tu) + (size_t)it * WS_TU_BYTES, sm + KP_TU,
-                 TILE_BYTES);
-      bulk_commit();
-    }
 
     // ---- 5. W = T_U K_G; -W image ----------------------------------------
     {
@@ -461,16 +514,25 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
         *reinterpret_cast<uint32_t*>(wimg + sw128(r1, cc >> 3) + (cc & 7) * 2) =
             pack_bf16x2(-acc[n][2], -acc[n][3]);
       }
-      fence_proxy_async();
     }
     __syncthreads();
-    if (tid == 0) {
-      bulk_store(static_cast<uint8_t*>(p.wneg) + (size_t)it * WS_W_BYTES, sm + KP_W,
-                 WS_W_BYTES);
-      bulk_commit();
+    {
+      // the image out with 16-byte stores (no proxy fence, as for T_U)
+      const uint4* src = reinterpret_cast<const uint4*>(sm + KP_W);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.wneg) +
+                                            (size_t)it * WS_W_BYTES);
+#pragma unroll
+      for (int i = 0; i < (int)(WS_W_BYTES / 16 / kKpThreads); ++i)
+        dst[tid + i * kKpThreads] = src[tid + i * kKpThreads];
     }
   }
-  if (tid == 0) bulk_wait_all();
+  if (tid == 0) {
+    // never leave with a row copy still landing (an item cut short by a
+    // timeout), nor with an image copy still reading
+    if (staged > li) wait_ignoring_abort(sbar, li & 1);
+    bulk_wait_all();
+    if (*abort_flag) record_status(p.status, GDN_ERR_TIMEOUT);
+  }
 }
 
 int sm_count_kp() {
@@ -494,13 +556,18 @@ cudaError_t launch_kda_prep(const ChunkParams& p, cudaStream_t stream,
   if (items <= 0) return cudaSuccess;
   const int grid =
       (int)std::min<long long>(items, (long long)kKpCtas * sm_count_kp());
+  const long long tokens = p.cu_seqlens ? (long long)p.T : (long long)p.N * p.T;
+  CUtensorMap mg, mk;
+  if (!make_rows_map(&mg, p.g, true, DK, p.H, tokens, DK, C) ||
+      !make_rows_map(&mk, p.k, false, DK, p.H, tokens, DK, C))
+    return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(kda_prep_kernel,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)KP_SMEM);
   if (e != cudaSuccess) return e;
   const int t = timing_start(GDN_KERNEL_KDA_PREP, stream);
   kda_prep_kernel<<<grid, kKpThreads, KP_SMEM, stream>>>(
-      p, chunk_tc_nch_dense(p), (int)bound);
+      p, mg, mk, chunk_tc_nch_dense(p), (int)bound);
   e = cudaGetLastError();
   timing_stop(t, stream, e);
   if (e == cudaSuccess) ++*launches;
