@@ -208,13 +208,6 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
         }
       }
     }
-    // the previous item's bulk copies have read their images; this item's
-    // rows have landed
-    if (tid == 0) bulk_wait_read();
-    const bool landed = mbar_wait(sbar, li & 1, abort_flag);
-    if (!bar_and(2, kKpThreads, landed)) break;
-    ++li;
-
     // ---- 1. cumulative log2-decay over the chunk --------------------------
     // thread (block R1 = tid >> 6, channel pair cp = tid & 63): tokens
     // 16 R1 .. 16 R1 + 15 of key channels 2 cp and 2 cp + 1. Each block is
@@ -223,22 +216,32 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
     float2 x[16];           // Gamma_t - ref_R1 (log2 units)
     uint32_t kk2[16], qq2[16];  // raw k and q, two channels each
     {
+      // the q rows first, so that they travel while the stage is awaited
       const size_t e0 = ((size_t)(t0 + 16 * R1) * H + h) * DK + c0;
       const size_t rs = (size_t)H * DK;  // token stride in elements
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float2 gv = make_float2(0.f, 0.f);
-        uint32_t kb = 0, qb = 0;
-        const int t = 16 * R1 + j;
-        if (t < len) {
-          gv = *reinterpret_cast<const float2*>(sm + KP_SG + t * (DK * 4) + c0 * 4);
-          kb = *reinterpret_cast<const uint32_t*>(sm + KP_SK + t * (DK * 2) + c0 * 2);
-          qb = __ldg(reinterpret_cast<const uint32_t*>(qin + e0 + (size_t)j * rs));
-        }
-        x[j] = make_float2(gv.x * kLog2e, gv.y * kLog2e);
-        kk2[j] = kb;
-        qq2[j] = qb;
+      for (int j = 0; j < 16; ++j)
+        qq2[j] = 16 * R1 + j < len
+                     ? __ldg(reinterpret_cast<const uint32_t*>(qin + e0 + (size_t)j * rs))
+                     : 0u;
+    }
+    // the previous item's bulk copies have read their images; this item's
+    // g and k rows have landed
+    if (tid == 0) bulk_wait_read();
+    const bool landed = mbar_wait(sbar, li & 1, abort_flag);
+    if (!bar_and(2, kKpThreads, landed)) break;
+    ++li;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float2 gv = make_float2(0.f, 0.f);
+      uint32_t kb = 0;
+      const int t = 16 * R1 + j;
+      if (t < len) {
+        gv = *reinterpret_cast<const float2*>(sm + KP_SG + t * (DK * 4) + c0 * 4);
+        kb = *reinterpret_cast<const uint32_t*>(sm + KP_SK + t * (DK * 2) + c0 * 2);
       }
+      x[j] = make_float2(gv.x * kLog2e, gv.y * kLog2e);
+      kk2[j] = kb;
     }
 #pragma unroll
     for (int j = 1; j < 16; ++j) {
