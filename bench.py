@@ -116,7 +116,7 @@ MEASURED_TRAFFIC = {
     # its traffic is proportional to the sequences processed
     "w4:83c7aa23b4500b6b": 4 * (271642880 + 210279936),
     # kda_prep_kernel, kda1, one launch
-    "kda1:1ec3a64713b9ec79": 134888448 + 84576256,
+    "kda1:bfc7eb5c04d6e496": 134888448 + 84576256,
     # bwd_kernel, bwd1, one launch (the per-CTA windows of S_bar do not all
     # stay in L2: most of the writes)
     "bwd1:f86ac4026bf4de8b": 763373312 + 4999033088,
