@@ -65,7 +65,8 @@ constexpr uint32_t KP_AT = 4 * KP_TAB;             // fp32 A, then T (pitch AP)
 // -W image after T_U is built, over the solve buffer
 constexpr uint32_t KP_W = KP_AT;
 // The next item's g rows (fp32 [64][d_k]) and k rows (bf16 [64][d_k]) arrive
-// by bulk copies over K_E / Q_E and K_B once the A and P products are done
+// by tensor-map copies over K_E / Q_E and K_B once the A and P products are
+// done
 constexpr uint32_t KP_SG = 0, KP_SK = KP_KB;
 constexpr uint32_t KP_P = KP_AT + 64 * AP * 4;     // P image
 constexpr uint32_t KP_TU = KP_P + TILE_BYTES;      // T_U image
@@ -145,7 +146,6 @@ __global__ void __launch_bounds__(kKpThreads, kKpCtas)
   float* AT = reinterpret_cast<float*>(sm + KP_AT);
   float* vpair = reinterpret_cast<float*>(sm + KP_V);
   float* bet = reinterpret_cast<float*>(sm + KP_BETA);
-  const uint16_t* kin = static_cast<const uint16_t*>(p.k);
   const uint16_t* qin = static_cast<const uint16_t*>(p.q);
 
   auto chunk_of = [&](int it, int& h, long long& t0, int& len) {
