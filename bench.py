@@ -109,17 +109,17 @@ WORKLOADS = {
 # hash of the kernel source it was taken on; a changed kernel reports null.
 MEASURED_TRAFFIC = {
     # chunk_tc_kernel, W1, one launch (caches flushed by the bench)
-    "w1:5c9f8f9802316b22": 168918272 + 19576832,
+    "w1:5fe6b52b69a8c778": 168942592 + 19785984,
     # chain_tx_kernel, W3 (packed, 512 sequence-heads), one launch
-    "w3:5c9f8f9802316b22": 2998424320 + 599070464,
+    "w3:5fe6b52b69a8c778": 2996173056 + 598289920,
     # decode_kernel captured with --sequences 128 and scaled x4 to N=512:
     # its traffic is proportional to the sequences processed
     "w4:83c7aa23b4500b6b": 4 * (271642880 + 210279936),
     # kda_prep_kernel, kda1, one launch
-    "kda1:bfc7eb5c04d6e496": 134888448 + 84576256,
+    "kda1:21af4a2a3fb88473": 134819328 + 84282112,
     # bwd_kernel, bwd1, one launch (the per-CTA windows of S_bar do not all
     # stay in L2: most of the writes)
-    "bwd1:f86ac4026bf4de8b": 763373312 + 4999033088,
+    "bwd1:f86ac4026bf4de8b": 762707456 + 5007061504,
 }
 
 
