@@ -105,6 +105,8 @@ def library():
     lib.gdn_kda_bwd.restype = i
     lib.gdn_chunk_bwd.argtypes = bwd_args + [i, vp]
     lib.gdn_chunk_bwd.restype = i
+    lib.gdn_chunk_bwd_f32.argtypes = bwd_args + [i, vp]
+    lib.gdn_chunk_bwd_f32.restype = i
     lib.gdn_device_status.argtypes = [vp]
     lib.gdn_device_status.restype = i
     lib.gdn_status_string.argtypes = [i]
@@ -279,12 +281,21 @@ def gdn_chunk_bwd(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None, *,
                 want_dh0, stream, per_channel=False, extra=(int(variant),))
 
 
+def gdn_chunk_bwd_f32(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None,
+                      *, variant=GDN_GATE_BEFORE_PREDICT, want_dh0=True,
+                      stream=None):
+    """gdn_chunk_bwd for fp32 q, k, v and dout."""
+    return _bwd("gdn_chunk_bwd_f32", q, k, v, g, beta, h0, dout, dhT,
+                cu_seqlens, want_dh0, stream, per_channel=False,
+                extra=(int(variant),), in_dtype=torch.float32)
+
+
 def _bwd(fn, q, k, v, g, beta, h0, dout, dhT, cu_seqlens, want_dh0, stream,
-         per_channel, extra=()):
+         per_channel, extra=(), in_dtype=torch.bfloat16):
     dev = q.device
-    _need(q, "q", torch.bfloat16, None)
+    _need(q, "q", in_dtype, None)
     for name, t in (("k", k), ("v", v), ("dout", dout)):
-        _need(t, name, torch.bfloat16, dev)
+        _need(t, name, in_dtype, dev)
     _need(g, "g", torch.float32, dev)
     _need(beta, "beta", torch.float32, dev)
     Bt, T, H, dk = q.shape

@@ -32,6 +32,8 @@
 // decay: S_t = S diag(a_t) + u k_t^T) the window keeps S instead of S_bar and
 // the adjoint's last steps become dk_t = dS^T u - beta_t S^T du, dg_t =
 // colsum(dS (.) S diag(a_t)), dS_{t-1} = dS diag(a_t) - beta_t du k_t^T.
+#include <type_traits>
+
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -43,13 +45,13 @@ constexpr int kBwThreads = 256;
 constexpr int kBwTok = 16;                 // tokens per block (checkpoint spacing)
 
 struct BwdArgs {
-  const __nv_bfloat16* q;
-  const __nv_bfloat16* k;
-  const __nv_bfloat16* v;
+  const void* q;          // bf16 or fp32 (the kernel's input type), as k, v, dout
+  const void* k;
+  const void* v;
   const float* g;         // [tokens, H, dk] (per channel) or [tokens, H]
   const float* beta;      // [tokens, H]
   const float* h0;        // [N, H, dk, dv] or null
-  const __nv_bfloat16* dout;  // [tokens, H, dv]
+  const void* dout;       // [tokens, H, dv]
   const float* dhT;       // [N, H, dk, dv] or null
   float* dv_out;          // [tokens, H, dv]
   float* dh0;             // [N, H, dk, dv] or null
@@ -118,8 +120,16 @@ struct BwSmem {
                        TOTAL = ACC + kBwTok * RW;
 };
 
-template <int DK>
+// TI: the type of q, k, v and dout (bf16, or fp32 for gdn_chunk_bwd_f32;
+// fp32 rows are staged straight from global memory, bf16 rows one block
+// ahead through registers)
+template <int DK, typename TI>
 __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
+  constexpr bool kF32 = std::is_same<TI, float>::value;
+  const TI* gq = static_cast<const TI*>(a.q);
+  const TI* gk = static_cast<const TI*>(a.k);
+  const TI* gv = static_cast<const TI*>(a.v);
+  const TI* gdo = static_cast<const TI*>(a.dout);
   constexpr int CPT = DK / 32;            // channels per lane
   constexpr int NS = kBwRpw * CPT;        // state floats per thread
   using L = BwSmem<DK>;
@@ -167,10 +177,10 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
     for (int j = 0; j < KCH; ++j) {
       const int e = tid + j * kBwThreads, tt = e / (DK / 8), c8 = e % (DK / 8);
       rk[j] = rq[j] = make_uint4(0, 0, 0, 0);
-      if (e < KTOT && tt < nt) {
+      if (!kF32 && e < KTOT && tt < nt) {
         const size_t r = ((size_t)(t0 + tt) * H + h) * DK + 8 * c8;
-        rk[j] = *reinterpret_cast<const uint4*>(a.k + r);
-        if (back) rq[j] = *reinterpret_cast<const uint4*>(a.q + r);
+        rk[j] = *reinterpret_cast<const uint4*>(gk + r);
+        if (back) rq[j] = *reinterpret_cast<const uint4*>(gq + r);
       }
     }
 #pragma unroll
@@ -187,26 +197,49 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
       }
     }
     rv = rdo = make_uint4(0, 0, 0, 0);
-    if (tid < kBwTok * kBwRows / 8) {
+    if (!kF32 && tid < kBwTok * kBwRows / 8) {
       const int tt = tid / (kBwRows / 8), r8 = tid % (kBwRows / 8);
       if (tt < nt) {
         const size_t r = ((size_t)(t0 + tt) * H + h) * dv + row0 + 8 * r8;
-        rv = *reinterpret_cast<const uint4*>(a.v + r);
-        if (back) rdo = *reinterpret_cast<const uint4*>(a.dout + r);
+        rv = *reinterpret_cast<const uint4*>(gv + r);
+        if (back) rdo = *reinterpret_cast<const uint4*>(gdo + r);
       }
     }
     if (tid < kBwTok) rbeta = tid < nt ? a.beta[(size_t)(t0 + tid) * H + h] : 0.f;
   };
-  auto stage = [&]() {
+  // 8 consecutive fp32 values (zeros past the block's end)
+  auto ld8f = [&](const TI* src, bool live, float (&f)[8]) {
+    if constexpr (kF32) {
+      float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+      if (live) {
+        x0 = *reinterpret_cast<const float4*>(src);
+        x1 = *reinterpret_cast<const float4*>(src + 4);
+      }
+      f[0] = x0.x; f[1] = x0.y; f[2] = x0.z; f[3] = x0.w;
+      f[4] = x1.x; f[5] = x1.y; f[6] = x1.z; f[7] = x1.w;
+    }
+  };
+  auto stage = [&](long long t0, bool back) {
+    const int nt = (int)max(0ll, min((long long)kBwTok, eos - t0));
 #pragma unroll
     for (int j = 0; j < KCH; ++j) {
       const int e = tid + j * kBwThreads, tt = e / (DK / 8), c8 = e % (DK / 8);
       if (e >= KTOT) continue;
       float f[8];
-      unpack8(rk[j], f);
+      if constexpr (kF32) {
+        const size_t r = ((size_t)(t0 + tt) * H + h) * DK + 8 * c8;
+        ld8f(gk + r, tt < nt, f);
+      } else {
+        unpack8(rk[j], f);
+      }
 #pragma unroll
       for (int x = 0; x < 8; ++x) sm[L::SK + tt * DK + 8 * c8 + x] = f[x];
-      unpack8(rq[j], f);
+      if constexpr (kF32) {
+        const size_t r = ((size_t)(t0 + tt) * H + h) * DK + 8 * c8;
+        ld8f(gq + r, back && tt < nt, f);
+      } else {
+        unpack8(rq[j], f);
+      }
 #pragma unroll
       for (int x = 0; x < 8; ++x) sm[L::SQ + tt * DK + 8 * c8 + x] = f[x];
     }
@@ -219,11 +252,12 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
     }
     if (tid < kBwTok * kBwRows / 8) {
       const int tt = tid / (kBwRows / 8), r8 = tid % (kBwRows / 8);
+      const size_t r = ((size_t)(t0 + tt) * H + h) * dv + row0 + 8 * r8;
       float f[8];
-      unpack8(rv, f);
+      if constexpr (kF32) ld8f(gv + r, tt < nt, f); else unpack8(rv, f);
 #pragma unroll
       for (int x = 0; x < 8; ++x) sm[L::SV + tt * kBwRows + 8 * r8 + x] = f[x];
-      unpack8(rdo, f);
+      if constexpr (kF32) ld8f(gdo + r, back && tt < nt, f); else unpack8(rdo, f);
 #pragma unroll
       for (int x = 0; x < 8; ++x) sm[L::SDO + tt * kBwRows + 8 * r8 + x] = f[x];
     }
@@ -284,7 +318,7 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
     const long long t0 = bos + (long long)b * kBwTok;
     const int nt = (int)min((long long)kBwTok, eos - t0);
     __syncthreads();
-    stage();
+    stage(t0, false);
     __syncthreads();
     if (b + 1 < nblk) fetch(t0 + kBwTok, false);
     put(ckpt(b));
@@ -303,7 +337,7 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
     const long long t0 = bos + (long long)b * kBwTok;
     const int nt = (int)min((long long)kBwTok, eos - t0);
     __syncthreads();  // the previous block's shared data has been written out
-    stage();
+    stage(t0, true);
     __syncthreads();
     if (b > 0) fetch(t0 - kBwTok, true);
     // recompute the block: S_bar of each token into the window, e of each
@@ -464,7 +498,7 @@ int run_bwd(const void* q, const void* k, const void* v, const float* g,
             const float* beta, const float* h0, const void* dout,
             const float* dhT, float* dq, float* dk, float* dvo, float* dg,
             float* dbeta, float* dh0, const int32_t* cu_seqlens, int B, int H,
-            int T, int dk_, int dv, bool per_channel, int variant,
+            int T, int dk_, int dv, bool per_channel, int variant, bool f32,
             cudaStream_t stream) {
   if (B < 0 || H <= 0 || T < 0) return GDN_ERR_INVALID_ARG;
   if (variant != GDN_GATE_BEFORE_PREDICT && variant != GDN_GATE_AFTER_PREDICT)
@@ -506,11 +540,11 @@ int run_bwd(const void* q, const void* k, const void* v, const float* g,
   if (cudaMallocAsync(reinterpret_cast<void**>(&ws), total, stream) != cudaSuccess)
     return GDN_ERR_CUDA;
   BwdArgs a{};
-  a.q = static_cast<const __nv_bfloat16*>(q);
-  a.k = static_cast<const __nv_bfloat16*>(k);
-  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.q = q;
+  a.k = k;
+  a.v = v;
   a.g = g; a.beta = beta; a.h0 = h0;
-  a.dout = static_cast<const __nv_bfloat16*>(dout);
+  a.dout = dout;
   a.dhT = dhT; a.dv_out = dvo; a.dh0 = dh0;
   a.blk_off = cu_seqlens ? reinterpret_cast<const int32_t*>(ws) : nullptr;
   a.ckpt = reinterpret_cast<float*>(ws + off_b);
@@ -550,9 +584,14 @@ int run_bwd(const void* q, const void* k, const void* v, const float* g,
     if (x == cudaSuccess) ++launches;
     return x;
   };
-  if (e == cudaSuccess)
-    e = dk_ == 64 ? go(bwd_kernel<64>, bwd_finalize_kernel<64>, 64)
-                  : go(bwd_kernel<128>, bwd_finalize_kernel<128>, 128);
+  if (e == cudaSuccess) {
+    if (f32)
+      e = dk_ == 64 ? go(bwd_kernel<64, float>, bwd_finalize_kernel<64>, 64)
+                    : go(bwd_kernel<128, float>, bwd_finalize_kernel<128>, 128);
+    else
+      e = dk_ == 64 ? go(bwd_kernel<64, __nv_bfloat16>, bwd_finalize_kernel<64>, 64)
+                    : go(bwd_kernel<128, __nv_bfloat16>, bwd_finalize_kernel<128>, 128);
+  }
   count_launches(e, launches);
   const cudaError_t f = cudaFreeAsync(ws, stream);
   return (e == cudaSuccess && f == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
@@ -568,7 +607,8 @@ extern "C" int gdn_kda_bwd(const void* q, const void* k, const void* v,
                            int T, int dk_, int dv_, gdn_stream_t stream) {
   return gdn::run_bwd(q, k, v, g, beta, h0, dout, dhT, dq, dk, dv, dg, dbeta, dh0,
                       cu_seqlens, B, H, T, dk_, dv_, true,
-                      GDN_GATE_BEFORE_PREDICT, static_cast<cudaStream_t>(stream));
+                      GDN_GATE_BEFORE_PREDICT, false,
+                      static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int gdn_chunk_bwd(const void* q, const void* k, const void* v,
@@ -579,6 +619,19 @@ extern "C" int gdn_chunk_bwd(const void* q, const void* k, const void* v,
                              int H, int T, int dk_, int dv_, int variant,
                              gdn_stream_t stream) {
   return gdn::run_bwd(q, k, v, g, beta, h0, dout, dhT, dq, dk, dv, dg, dbeta, dh0,
-                      cu_seqlens, B, H, T, dk_, dv_, false, variant,
+                      cu_seqlens, B, H, T, dk_, dv_, false, variant, false,
+                      static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gdn_chunk_bwd_f32(const float* q, const float* k, const float* v,
+                                 const float* g, const float* beta,
+                                 const float* h0, const float* dout,
+                                 const float* dhT, float* dq, float* dk,
+                                 float* dv, float* dg, float* dbeta, float* dh0,
+                                 const int32_t* cu_seqlens, int B, int H, int T,
+                                 int dk_, int dv_, int variant,
+                                 gdn_stream_t stream) {
+  return gdn::run_bwd(q, k, v, g, beta, h0, dout, dhT, dq, dk, dv, dg, dbeta, dh0,
+                      cu_seqlens, B, H, T, dk_, dv_, false, variant, true,
                       static_cast<cudaStream_t>(stream));
 }

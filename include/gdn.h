@@ -295,6 +295,16 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
                   int H, int T, int dk_dim, int dv_dim, int variant,
                   gdn_stream_t stream);
 
+/* gdn_chunk_bwd_f32 -- gdn_chunk_bwd for fp32 q, k, v and dout (the inputs
+ * of gdn_chunk_fwd_f32 / gdn_chunk_fwd_ex with GDN_DTYPE_F32); everything
+ * else, outputs included, as gdn_chunk_bwd. */
+int gdn_chunk_bwd_f32(const float* q, const float* k, const float* v,
+                      const float* g, const float* beta, const float* h0,
+                      const float* dout, const float* dhT, float* dq, float* dk,
+                      float* dv, float* dg, float* dbeta, float* dh0,
+                      const int32_t* cu_seqlens, int B, int H, int T,
+                      int dk_dim, int dv_dim, int variant, gdn_stream_t stream);
+
 /*
  * gdn_chunk_fwd_sp_noalloc -- the sequence-parallel forward pass of
  * gdn_chunk_fwd_ex (path GDN_PATH_SIMT, sp_parts >= 2) for callers that may

@@ -240,14 +240,14 @@ def bwd(so, fn="gdn_chunk_bwd", **kw):
              dv=A + 0x8000, dg=A + 0x9000, db=A + 0xa000, dh0=None, cu=None,
              B=1, H=1, T=16, dk_=128, dv_=128)
     a.update(kw)
-    extra = (a.get("variant", 0),) if fn == "gdn_chunk_bwd" else ()
+    extra = (a.get("variant", 0),) if fn != "gdn_kda_bwd" else ()
     return getattr(so, fn)(a["q"], a["k"], a["v"], a["g"], a["b"], a["h0"],
                            a["do"], a["dhT"], a["dq"], a["dk"], a["dv"],
                            a["dg"], a["db"], a["dh0"], a["cu"], a["B"], a["H"],
                            a["T"], a["dk_"], a["dv_"], *extra, None)
 
 
-@pytest.mark.parametrize("fn", ["gdn_chunk_bwd", "gdn_kda_bwd"])
+@pytest.mark.parametrize("fn", ["gdn_chunk_bwd", "gdn_kda_bwd", "gdn_chunk_bwd_f32"])
 @pytest.mark.parametrize("kw,expect", [
     (dict(B=-1), INVALID), (dict(H=0), INVALID), (dict(T=-1), INVALID),
     (dict(q=None), INVALID), (dict(do=None), INVALID), (dict(dg=None), INVALID),
@@ -260,11 +260,12 @@ def test_bwd_rejects_on_host(lib, fn, kw, expect):
     assert bwd(lib.library(), fn, **kw) == expect
 
 
+@pytest.mark.parametrize("fn", ["gdn_chunk_bwd", "gdn_chunk_bwd_f32"])
 @pytest.mark.parametrize("variant", [-1, 2])
-def test_chunk_bwd_rejects_unknown_gate_placement(lib, variant):
-    assert bwd(lib.library(), "gdn_chunk_bwd", variant=variant) == INVALID
+def test_chunk_bwd_rejects_unknown_gate_placement(lib, fn, variant):
+    assert bwd(lib.library(), fn, variant=variant) == INVALID
 
 
-@pytest.mark.parametrize("fn", ["gdn_chunk_bwd", "gdn_kda_bwd"])
+@pytest.mark.parametrize("fn", ["gdn_chunk_bwd", "gdn_kda_bwd", "gdn_chunk_bwd_f32"])
 def test_bwd_empty_batch_is_a_no_op(lib, fn):
     assert bwd(lib.library(), fn, B=0) == OK

@@ -75,6 +75,33 @@ def test_scalar_bwd_other_gate_placement_packed(lib, cuda_device):
     run_and_check(lib, cuda_device, d, scalar=True, seed=8, after=True)
 
 
+@pytest.mark.parametrize("after", [False, True])
+@pytest.mark.parametrize("lengths", [None, [40, 0, 1, 129, 7]])
+def test_f32_bwd_matches_oracle(lib, cuda_device, after, lengths):
+    """fp32 q, k, v, dout (gdn_chunk_bwd_f32), dense and packed, both gate
+    placements."""
+    if lengths is None:
+        d = inputs.chunk_inputs(2, 2, 97, 128, 128, dtype="f32", seed=71, h0=True)
+    else:
+        d = inputs.chunk_inputs(0, 2, 0, 128, 64, dtype="f32", seed=72, h0=True,
+                                lengths=lengths)
+    dout, dh = inputs.grad_inputs(d, seed=9)
+    dout = dout.float()
+    x = lambda t: None if t is None else t.to(cuda_device)
+    got = lib.gdn_chunk_bwd_f32(x(d["q"]), x(d["k"]), x(d["v"]), x(d["g"]),
+                                x(d["beta"]), x(d["h0"]), x(dout), x(dh),
+                                x(d["cu_seqlens"]),
+                                variant=lib.GDN_GATE_AFTER_PREDICT if after
+                                else lib.GDN_GATE_BEFORE_PREDICT)
+    torch.cuda.synchronize(cuda_device)
+    assert lib.gdn_device_status() == 0
+    ref = backward.backward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"],
+                            dout, dh, cu_seqlens=d["cu_seqlens"],
+                            variant=oracle.G0 if after else oracle.G1)
+    errs = {n: rel_err(got[n], ref[n]) for n in GRADS + ("dh0",)}
+    assert all(e <= TOL for e in errs.values()), errs
+
+
 def test_scalar_bwd_without_dhT(lib, cuda_device):
     d = inputs.chunk_inputs(2, 3, 90, 128, 128, dtype="bf16", seed=63, h0=True)
     run_and_check(lib, cuda_device, d, scalar=True, dhT=False, seed=3)
