@@ -124,3 +124,51 @@ def backward(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None,
                        decay_first=(variant == 1))
     out["dg"] = out["dg"].sum(axis=-1)
     return out
+
+
+def fused_backward(q_raw, k_raw, v, a, b, h0, dout, dhT=None, cu_seqlens=None,
+                   weight=None, gate=None, eps=1e-6):
+    """Gradients of ``oracle.sublayer.fused_forward`` (the recurrence with the
+    steps either side, decay before the prediction) for L = sum(dout * out)
+    + sum(dhT * hT). The steps' adjoints, written out:
+      out = y * sigmoid(z), y = n * w, n = o r, r = (mean(o^2) + eps)^(-1/2):
+        dz = dout * y * s (1 - s);  dy = dout * s;  dw = sum over rows of dy * n;
+        do = r (dn - n mean(dn * n)),  dn = dy * w
+      q = q_raw / |q_raw|:  dq_raw = (dq - q (q . dq)) / |q_raw|  (k alike)
+      g = -softplus(a):  da = -dg sigmoid(a);  beta = sigmoid(b):  db = dbeta beta (1 - beta).
+    Returns dq, dk, dv, da, db, dh0, and dweight / dgate (None when that step
+    is absent)."""
+    from . import forward
+    from . import sublayer as sl
+    q, k, g, beta = sl.prologue(q_raw, k_raw, a, b)
+    o, _ = forward(q, k, v, g, beta, h0, cu_seqlens=cu_seqlens, variant=1)
+    dy = _f64(dout)
+    res = {"dweight": None, "dgate": None}
+    pre = o if weight is None else sl.rms_norm(o, weight, eps)
+    if gate is not None:
+        s = sl.sigmoid(gate)
+        res["dgate"] = dy * pre * s * (1.0 - s)
+        dy = dy * s
+    if weight is not None:
+        r = 1.0 / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
+        n = o * r
+        res["dweight"] = (dy * n).reshape(-1, o.shape[-1]).sum(axis=0)
+        dn = dy * _f64(weight)
+        do = r * (dn - n * np.mean(dn * n, axis=-1, keepdims=True))
+    else:
+        do = dy
+    core = backward(q, k, v, g, beta, h0, do, dhT, cu_seqlens, variant=1)
+
+    def unnorm(x_raw, x_hat, dx_hat):
+        x_raw = _f64(x_raw)
+        ln = np.sqrt(np.sum(x_raw * x_raw, axis=-1, keepdims=True))
+        proj = dx_hat - x_hat * np.sum(x_hat * dx_hat, axis=-1, keepdims=True)
+        return np.divide(proj, ln, out=np.zeros_like(proj), where=ln > 0)
+
+    res["dq"] = unnorm(q_raw, q, core["dq"])
+    res["dk"] = unnorm(k_raw, k, core["dk"])
+    res["dv"] = core["dv"]
+    res["da"] = -core["dg"] * sl.sigmoid(a)
+    res["db"] = core["dbeta"] * beta * (1.0 - beta)
+    res["dh0"] = core["dh0"]
+    return res

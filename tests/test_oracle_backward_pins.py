@@ -188,3 +188,48 @@ def test_a_planted_mistake_is_caught(plant):
         bad["dv"] = bad["dv"] / c["beta"][..., None]
     with pytest.raises(AssertionError):
         check_fd(c, bad, kda.forward)
+
+
+@pytest.mark.parametrize("weight,gate", [(True, True), (True, False),
+                                         (False, True), (False, False)])
+def test_fused_gradients_match_finite_differences(weight, gate):
+    """The steps either side of the recurrence (L2 norms, softplus and
+    sigmoid activations, RMSNorm with a weight, sigmoid output gate) against
+    central differences through the fused forward oracle."""
+    from oracle import sublayer
+    rng = np.random.default_rng(9)
+    B, T, H, dk, dv = 2, 5, 1, 3, 4
+    c = {"q": rng.normal(size=(B, T, H, dk)) * 2.0,
+         "k": rng.normal(size=(B, T, H, dk)),
+         "v": rng.normal(size=(B, T, H, dv)),
+         "a": rng.normal(size=(B, T, H)), "b": rng.normal(size=(B, T, H)),
+         "h0": rng.normal(size=(B, H, dk, dv)),
+         "w": 1.0 + 0.3 * rng.normal(size=dv) if weight else None,
+         "z": rng.normal(size=(B, T, H, dv)) if gate else None}
+    dout = rng.normal(size=(B, T, H, dv))
+    dhT = rng.normal(size=(B, H, dk, dv))
+    names = ["q", "k", "v", "a", "b", "h0"] + (["w"] if weight else []) + (["z"] if gate else [])
+
+    def L(**over):
+        x = {n: over.get(n, c[n]) for n in c}
+        out, hT = sublayer.fused_forward(x["q"], x["k"], x["v"], x["a"], x["b"],
+                                         x["h0"], weight=x["w"], gate=x["z"],
+                                         eps=1e-6)
+        return float((dout * out).sum() + (dhT * hT).sum())
+
+    got = backward.fused_backward(c["q"], c["k"], c["v"], c["a"], c["b"], c["h0"],
+                                  dout, dhT, weight=c["w"], gate=c["z"], eps=1e-6)
+    key = {"q": "dq", "k": "dk", "v": "dv", "a": "da", "b": "db", "h0": "dh0",
+           "w": "dweight", "z": "dgate"}
+    for n in names:
+        base = c[n]
+        fd = np.zeros_like(base)
+        it = np.nditer(base, flags=["multi_index"])
+        for _ in it:
+            i = it.multi_index
+            xp, xm = base.copy(), base.copy()
+            xp[i] += 1e-6
+            xm[i] -= 1e-6
+            fd[i] = (L(**{n: xp}) - L(**{n: xm})) / 2e-6
+        an = got[key[n]]
+        assert np.abs(an - fd).max() / max(np.abs(fd).max(), 1e-12) < 1e-6, n
