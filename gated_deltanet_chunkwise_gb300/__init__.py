@@ -13,6 +13,7 @@ _ABI_NAMES = (
     "gdn_chunk_fwd", "gdn_chunk_fwd_f32", "gdn_chunk_fwd_ex",
     "gdn_recurrent_step", "gdn_chunk_fwd_fused", "gdn_kda_fwd",
     "gdn_kda_fwd_ex", "gdn_kda_bwd", "gdn_chunk_bwd", "gdn_chunk_bwd_f32",
+    "gdn_chunk_bwd_fused",
     "GDN_GATE_BEFORE_PREDICT", "GDN_GATE_AFTER_PREDICT",
     "gdn_status_string",
     "GdnError", "library_path",

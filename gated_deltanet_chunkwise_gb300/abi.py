@@ -107,6 +107,10 @@ def library():
     lib.gdn_chunk_bwd.restype = i
     lib.gdn_chunk_bwd_f32.argtypes = bwd_args + [i, vp]
     lib.gdn_chunk_bwd_f32.restype = i
+    lib.gdn_chunk_bwd_fused.argtypes = [vp, vp, vp, fp, fp, fp, ip, fp, vp,
+                                        ctypes.c_float, vp, fp, fp, fp, fp, fp,
+                                        fp, fp, fp, fp, i, i, i, i, i, vp]
+    lib.gdn_chunk_bwd_fused.restype = i
     lib.gdn_device_status.argtypes = [vp]
     lib.gdn_device_status.restype = i
     lib.gdn_status_string.argtypes = [i]
@@ -288,6 +292,52 @@ def gdn_chunk_bwd_f32(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None,
     return _bwd("gdn_chunk_bwd_f32", q, k, v, g, beta, h0, dout, dhT,
                 cu_seqlens, want_dh0, stream, per_channel=False,
                 extra=(int(variant),), in_dtype=torch.float32)
+
+
+def gdn_chunk_bwd_fused(q, k, v, a, b, h0, dout, dhT=None, cu_seqlens=None, *,
+                        norm_weight=None, gate=None, eps=1e-6, want_dh0=True,
+                        stream=None):
+    """Gradients of gdn_chunk_fwd_fused for L = sum(dout * out) + sum(dhT *
+    hT): dict dq, dk, dv, da, db, dh0 (or None), dweight (with norm_weight,
+    else None), dgate (with gate, else None); all fp32."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, None)
+    for name, t in (("k", k), ("v", v), ("dout", dout)):
+        _need(t, name, torch.bfloat16, dev)
+    _need(a, "a", torch.float32, dev)
+    _need(b, "b", torch.float32, dev)
+    Bt, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = Bt
+    if norm_weight is not None:
+        _need(norm_weight, "norm_weight", torch.float32, dev)
+    if gate is not None:
+        _need(gate, "gate", torch.bfloat16, dev)
+    for name, st in (("h0", h0), ("dhT", dhT)):
+        if st is not None:
+            _need(st, name, torch.float32, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    res = {"dq": torch.empty(q.shape, **f32), "dk": torch.empty(q.shape, **f32),
+           "dv": torch.empty(v.shape, **f32), "da": torch.empty(a.shape, **f32),
+           "db": torch.empty(b.shape, **f32),
+           "dh0": torch.empty((N, H, dk, dv), **f32) if want_dh0 else None,
+           "dweight": torch.empty((dv,), **f32) if norm_weight is not None else None,
+           "dgate": torch.empty(v.shape, **f32) if gate is not None else None}
+    with torch.cuda.device(dev):
+        rc = library().gdn_chunk_bwd_fused(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(h0),
+            _ptr(cu_seqlens), _ptr(norm_weight), _ptr(gate), float(eps),
+            _ptr(dout), _ptr(dhT), _ptr(res["dq"]), _ptr(res["dk"]),
+            _ptr(res["dv"]), _ptr(res["da"]), _ptr(res["db"]),
+            _ptr(res["dh0"]), _ptr(res["dweight"]), _ptr(res["dgate"]), N, H,
+            T, dk, dv, _stream(stream))
+    if rc != GDN_OK:
+        raise GdnError(rc, "gdn_chunk_bwd_fused")
+    return res
 
 
 def _bwd(fn, q, k, v, g, beta, h0, dout, dhT, cu_seqlens, want_dh0, stream,

@@ -451,6 +451,75 @@ int gdn_chunk_fwd_fused(const void* q, const void* k, const void* v,
                         stream, sub);
 }
 
+int gdn_chunk_bwd_fused(const void* q, const void* k, const void* v,
+                        const float* a, const float* b, const float* h0,
+                        const int32_t* cu_seqlens, const float* norm_weight,
+                        const void* gate, float eps, const void* dout,
+                        const float* dhT, float* dq, float* dk, float* dv,
+                        float* da, float* db, float* dh0, float* dweight,
+                        float* dgate, int B, int H, int T, int dk_dim,
+                        int dv_dim, gdn_stream_t stream) {
+  using namespace gdn;
+  if (B < 0 || H <= 0 || T < 0) return GDN_ERR_INVALID_ARG;
+  if (cu_seqlens && B == 0) return GDN_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || eps > 3.0e38f) return GDN_ERR_INVALID_ARG;
+  if (!head_dim_ok(dk_dim) || !head_dim_ok(dv_dim)) return GDN_ERR_UNSUPPORTED;
+  const long long tokens = cu_seqlens ? (long long)T : (long long)B * T;
+  if (tokens > 0 && (!q || !k || !v || !a || !b || !dout || !dq || !dk || !dv ||
+                     !da || !db))
+    return GDN_ERR_INVALID_ARG;
+  if ((dweight && !norm_weight) || (dgate && !gate)) return GDN_ERR_INVALID_ARG;
+  if (B > 65535 || tokens * H > (1ll << 40) || (long long)B * H > 0x7fffffffll)
+    return GDN_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q, k, v, a, b, h0, cu_seqlens, norm_weight, gate, dout,
+                        dhT, dq, dk, dv, da, db, dh0, dweight, dgate};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return GDN_ERR_MISALIGNED;
+  const void* ins[] = {q, k, v, a, b, h0, norm_weight, gate, dout};
+  const void* outs[] = {dq, dk, dv, da, db, dweight, dgate};
+  for (const void* o : outs)
+    for (const void* in : ins)
+      if (o && o == in) return GDN_ERR_INVALID_ARG;
+  if (B == 0) return GDN_OK;
+  int* status = nullptr;
+  int rc = current_status_ptr(&status);
+  if (rc != GDN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long rows = tokens * H;
+  FusedBwdBufs f{};
+  const size_t bytes = fused_bwd_bind(f, nullptr, rows, dk_dim, dv_dim);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) return GDN_ERR_CUDA;
+  fused_bwd_bind(f, ws, rows, dk_dim, dv_dim);
+  // the steps before the recurrence, the recurrence's output in fp32, the
+  // adjoints of the steps after it, the recurrence's backward, the adjoints
+  // of the steps before it
+  cudaError_t e = counted(launch_sub_prologue(f, q, k, v, a, b, rows, dk_dim,
+                                              dv_dim, st), rows > 0 ? 1 : 0);
+  if (e == cudaSuccess) {
+    rc = run_chunk(f.qh, f.kh, f.vf, f.g, f.beta, h0, f.o, nullptr, cu_seqlens, B,
+                   H, T, dk_dim, dv_dim, 64, GDN_DTYPE_F32,
+                   GDN_GATE_BEFORE_PREDICT, GDN_PATH_SIMT, 0, st);
+    if (rc != GDN_OK) e = cudaErrorUnknown;
+  }
+  if (e == cudaSuccess)
+    e = counted(launch_sub_epilogue_bwd(f, dout, norm_weight, gate, eps, rows,
+                                        dv_dim, dgate, dweight, st),
+                rows > 0 ? (dweight ? 2 : 1) : 0);
+  if (e == cudaSuccess) {
+    rc = run_bwd(f.qh, f.kh, f.vf, f.g, f.beta, h0, f.dO, dhT, f.dqh, f.dkh, dv,
+                 f.dg, f.dbeta, dh0, cu_seqlens, B, H, T, dk_dim, dv_dim, false,
+                 GDN_GATE_BEFORE_PREDICT, true, st);
+    if (rc != GDN_OK) e = cudaErrorUnknown;
+  }
+  if (e == cudaSuccess)
+    e = counted(launch_sub_prologue_bwd(f, a, rows, dk_dim, dq, dk, da, db, st),
+                rows > 0 ? 1 : 0);
+  const cudaError_t fr = cudaFreeAsync(ws, st);
+  if (rc != GDN_OK) return rc;
+  return (e == cudaSuccess && fr == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
+}
+
 int gdn_recurrent_step(const void* q, const void* k, const void* v,
                        const float* g, const float* beta, float* state,
                        void* out, int N, int H, int dk, int dv,

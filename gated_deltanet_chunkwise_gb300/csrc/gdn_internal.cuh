@@ -135,6 +135,38 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_kda(const KdaParams& p, cudaStream_t stream);
 
+// Backward pass (bwd.cu): gradients of the recurrence; per_channel: KDA's
+// g [tokens, H, dk] (else the scalar gate); f32: fp32 q, k, v, dout (else
+// bf16); variant: the gate placement.
+int run_bwd(const void* q, const void* k, const void* v, const float* g,
+            const float* beta, const float* h0, const void* dout,
+            const float* dhT, float* dq, float* dk, float* dvo, float* dg,
+            float* dbeta, float* dh0, const int32_t* cu_seqlens, int B, int H,
+            int T, int dk_, int dv, bool per_channel, int variant, bool f32,
+            cudaStream_t stream);
+
+// Backward of the steps either side of the recurrence (fused_bwd.cu):
+// scratch buffers, fp32, per (token, head) row.
+struct FusedBwdBufs {
+  float *qh, *kh, *vf, *g, *beta, *invq, *invk;  // prologue outputs
+  float *o, *dO;                                 // recurrence output, its gradient
+  float *dqh, *dkh, *dg, *dbeta;                 // the recurrence's gradients
+  float* wpart;                                  // weight-gradient partials
+};
+size_t fused_bwd_bind(FusedBwdBufs& f, void* ws, long long rows, int dk, int dv);
+cudaError_t launch_sub_prologue(const FusedBwdBufs& f, const void* q,
+                                const void* k, const void* v, const float* a,
+                                const float* b, long long rows, int dk, int dv,
+                                cudaStream_t stream);
+cudaError_t launch_sub_epilogue_bwd(const FusedBwdBufs& f, const void* dout,
+                                    const float* w, const void* z, float eps,
+                                    long long rows, int dv, float* dgate,
+                                    float* dweight, cudaStream_t stream);
+cudaError_t launch_sub_prologue_bwd(const FusedBwdBufs& f, const float* a,
+                                    long long rows, int dk, float* dq,
+                                    float* dk_out, float* da, float* db,
+                                    cudaStream_t stream);
+
 // Host helpers owned by gdn_abi.cu.
 int validate_chunk_args(const void* q, const void* k, const void* v,
                         const float* g, const float* beta, const float* h0,

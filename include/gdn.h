@@ -295,6 +295,36 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
                   int H, int T, int dk_dim, int dv_dim, int variant,
                   gdn_stream_t stream);
 
+/*
+ * gdn_chunk_bwd_fused -- gradients of gdn_chunk_fwd_fused (the recurrence with
+ * the steps either side: q, k L2-normalised, g = -softplus(a), beta =
+ * sigmoid(b); out = RMSNorm(o) * norm_weight (when given) * sigmoid(gate)
+ * (when given)) for L = sum(dout * out) + sum(dhT * hT). The steps' adjoints,
+ * per (token, head): dgate = dout * y * s (1 - s) with y the normalised,
+ * weighted output and s = sigmoid(gate); dweight = sum over rows of
+ * dout * s * o r; do = r (dn - n mean(dn * n)) with n = o r, dn = dout * s *
+ * w, r = (mean(o^2) + eps)^(-1/2); then the recurrence's backward
+ * (gdn_chunk_bwd); then dq_raw = (dq - q (q . dq)) / |q_raw| (k alike;
+ * zero rows get zero), da = -dg sigmoid(a), db = dbeta beta (1 - beta).
+ * Inputs as gdn_chunk_fwd_fused (q, k, v, gate, dout bf16; a, b, norm_weight,
+ * h0, dhT fp32; eps >= 0); outputs fp32: dq, dk [B, T, H, dk], dv
+ * [B, T, H, dv], da, db [B, T, H], dh0 [N, H, dk, dv] or NULL, dweight
+ * [dv] (only with norm_weight) or NULL, dgate like v (only with gate) or
+ * NULL. The recurrence's output is recomputed in fp32 (gdn_chunk_fwd_f32's
+ * path) and its backward runs on the fp32 normalised inputs, so these are the
+ * gradients of the exact map. dk, dv in {64, 128}. Scratch: about 4 (4 dk +
+ * 3 dv) bytes per token and head (cudaMallocAsync on `stream`). Returns as
+ * gdn_chunk_bwd.
+ */
+int gdn_chunk_bwd_fused(const void* q, const void* k, const void* v,
+                        const float* a, const float* b, const float* h0,
+                        const int32_t* cu_seqlens, const float* norm_weight,
+                        const void* gate, float eps, const void* dout,
+                        const float* dhT, float* dq, float* dk, float* dv,
+                        float* da, float* db, float* dh0, float* dweight,
+                        float* dgate, int B, int H, int T, int dk_dim,
+                        int dv_dim, gdn_stream_t stream);
+
 /* gdn_chunk_bwd_f32 -- gdn_chunk_bwd for fp32 q, k, v and dout (the inputs
  * of gdn_chunk_fwd_f32 / gdn_chunk_fwd_ex with GDN_DTYPE_F32); everything
  * else, outputs included, as gdn_chunk_bwd. */

@@ -269,3 +269,34 @@ def test_chunk_bwd_rejects_unknown_gate_placement(lib, fn, variant):
 @pytest.mark.parametrize("fn", ["gdn_chunk_bwd", "gdn_kda_bwd", "gdn_chunk_bwd_f32"])
 def test_bwd_empty_batch_is_a_no_op(lib, fn):
     assert bwd(lib.library(), fn, B=0) == OK
+
+
+def bwd_fused(so, **kw):
+    a = dict(q=A, k=A + 0x1000, v=A + 0x2000, a=A + 0x3000, b=A + 0x4000,
+             h0=None, cu=None, w=None, z=None, eps=1e-6, do=A + 0x5000,
+             dhT=None, dq=A + 0x6000, dk=A + 0x7000, dv=A + 0x8000,
+             da=A + 0x9000, db=A + 0xa000, dh0=None, dw=None, dz=None,
+             B=1, H=1, T=16, dk_=128, dv_=128)
+    a.update(kw)
+    return so.gdn_chunk_bwd_fused(a["q"], a["k"], a["v"], a["a"], a["b"], a["h0"],
+                                  a["cu"], a["w"], a["z"], a["eps"], a["do"],
+                                  a["dhT"], a["dq"], a["dk"], a["dv"], a["da"],
+                                  a["db"], a["dh0"], a["dw"], a["dz"], a["B"],
+                                  a["H"], a["T"], a["dk_"], a["dv_"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(B=-1), INVALID), (dict(H=0), INVALID), (dict(eps=-1.0), INVALID),
+    (dict(q=None), INVALID), (dict(da=None), INVALID), (dict(do=None), INVALID),
+    (dict(dw=A + 0xb000), INVALID),              # dweight without a weight
+    (dict(dz=A + 0xb000), INVALID),              # dgate without a gate
+    (dict(dk_=96), UNSUPPORTED), (dict(dv_=32), UNSUPPORTED),
+    (dict(a=ODD), MISALIGNED), (dict(w=ODD), MISALIGNED),
+    (dict(dq=A), INVALID), (dict(cu=A + 0xb000, B=0), INVALID),
+])
+def test_bwd_fused_rejects_on_host(lib, kw, expect):
+    assert bwd_fused(lib.library(), **kw) == expect
+
+
+def test_bwd_fused_empty_batch_is_a_no_op(lib):
+    assert bwd_fused(lib.library(), B=0) == OK

@@ -172,3 +172,50 @@ def test_bwd_bench_size_sampled(lib, cuda_device):
         for name in GRADS:
             assert rel_err(sl(got[name]), ref[name]) <= TOL, (name, n, h)
         assert rel_err(got["dh0"][n:n + 1, h:h + 1], ref["dh0"]) <= TOL
+
+
+@pytest.mark.parametrize("weight,gate", [(True, True), (True, False),
+                                         (False, True), (False, False)])
+@pytest.mark.parametrize("dv", [64, 128])
+def test_fused_bwd_matches_oracle(lib, cuda_device, weight, gate, dv):
+    """gdn_chunk_bwd_fused against the fused-sublayer gradient oracle (raw q,
+    k with lengths in [0.25, 4), gate and step logits, RMSNorm weight and
+    output gate when present)."""
+    d = inputs.fused_inputs(2, 2, 77, 128, dv, seed=73, h0=True, weight=weight,
+                            gate=gate)
+    dout, dh = inputs.grad_inputs(d, seed=10)
+    x = lambda t: None if t is None else t.to(cuda_device)
+    got = lib.gdn_chunk_bwd_fused(x(d["q"]), x(d["k"]), x(d["v"]), x(d["a"]),
+                                  x(d["b"]), x(d["h0"]), x(dout), x(dh),
+                                  norm_weight=x(d["norm_weight"]),
+                                  gate=x(d["gate"]), eps=1e-6)
+    torch.cuda.synchronize(cuda_device)
+    assert lib.gdn_device_status() == 0
+    ref = backward.fused_backward(d["q"], d["k"], d["v"], d["a"], d["b"],
+                                  d["h0"], dout, dh, weight=d["norm_weight"],
+                                  gate=d["gate"], eps=1e-6)
+    names = ["dq", "dk", "dv", "da", "db", "dh0"]
+    names += ["dweight"] if weight else []
+    names += ["dgate"] if gate else []
+    errs = {n: rel_err(got[n], ref[n]) for n in names}
+    assert all(e <= TOL for e in errs.values()), errs
+
+
+def test_fused_bwd_packed(lib, cuda_device):
+    d = inputs.fused_inputs(0, 2, 0, 128, 128, seed=74, h0=True,
+                            lengths=[30, 0, 70, 1])
+    dout, dh = inputs.grad_inputs(d, seed=11)
+    x = lambda t: None if t is None else t.to(cuda_device)
+    got = lib.gdn_chunk_bwd_fused(x(d["q"]), x(d["k"]), x(d["v"]), x(d["a"]),
+                                  x(d["b"]), x(d["h0"]), x(dout), x(dh),
+                                  x(d["cu_seqlens"]),
+                                  norm_weight=x(d["norm_weight"]),
+                                  gate=x(d["gate"]), eps=1e-6)
+    torch.cuda.synchronize(cuda_device)
+    assert lib.gdn_device_status() == 0
+    ref = backward.fused_backward(d["q"], d["k"], d["v"], d["a"], d["b"],
+                                  d["h0"], dout, dh, cu_seqlens=d["cu_seqlens"],
+                                  weight=d["norm_weight"], gate=d["gate"],
+                                  eps=1e-6)
+    for n in ("dq", "dk", "dv", "da", "db", "dh0", "dweight", "dgate"):
+        assert rel_err(got[n], ref[n]) <= TOL, n
