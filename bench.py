@@ -44,7 +44,7 @@ def _metric(w):
         return "GDN decode-step token-heads/s + % of GB300 HBM roofline, 1 GPU"
     if w["kind"] == "kda":
         return "KDA (per-channel decay) forward tokens/s + % of GB300 roofline, 1 GPU"
-    if w["kind"] == "bwd":
+    if w["kind"] in ("bwd", "bwdf"):
         return "GDN backward tokens/s + % of GB300 fp32 ALU peak, 1 GPU"
     return METRIC
 
@@ -99,6 +99,10 @@ WORKLOADS = {
                  desc="gdn_chunk_bwd B=4 H=16 T=2048 dk=dv=128 bf16 inputs, "
                       "fp32 gradients of out (dout ~ N(0,1) bf16), h0=0, "
                       "no dhT"),
+    "bwd1f": dict(kind="bwdf", B=4, H=16, T=2048, dk=128, dv=128, h0=False,
+                  desc="gdn_chunk_bwd_fused B=4 H=16 T=2048 dk=dv=128: raw "
+                       "q/k, gate and step logits, RMSNorm weight and output "
+                       "gate; fp32 gradients of out (dout ~ N(0,1) bf16), h0=0"),
     "w4": dict(kind="decode", N=512, H=32, dk=128, dv=128,
                desc="gdn_recurrent_step N=512 H=32 dk=dv=128 bf16 token, "
                     "fp32 state in place"),
@@ -127,6 +131,7 @@ def _kernel_source_hash(kind):
     csrc = ROOT / "gated_deltanet_chunkwise_gb300" / "csrc"
     files = (["decode.cu"] if kind == "decode"
              else ["bwd.cu"] if kind == "bwd"
+             else ["bwd.cu", "fused_bwd.cu"] if kind == "bwdf"
              else ["kda.cu", "kda_chunk.cu", "chunk_tc.cu"] if kind == "kda"
              else sorted(p.name for p in csrc.glob("chunk_*.cu")))
     h = hashlib.sha256()
@@ -265,6 +270,11 @@ def _make_inputs(w, seed=0):
                                 dtype="bf16", seed=seed, h0=w["h0"])
         d["dout"], _ = inputs.grad_inputs(d, seed=seed, dhT=False)
         return d
+    if w["kind"] == "bwdf":
+        d = inputs.fused_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
+                                seed=seed, h0=w["h0"])
+        d["dout"], _ = inputs.grad_inputs(d, seed=seed, dhT=False)
+        return d
     return inputs.chunk_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
                                dtype="bf16", seed=seed, h0=w["h0"],
                                length_range=w.get("lengths"))
@@ -318,6 +328,12 @@ def run_ours(args, w, device, dist, rank, ws):
                 last["grads"] = gdn.gdn_chunk_bwd(
                     d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"],
                     d["dout"], None, want_dh0=False)
+                return
+            if w["kind"] == "bwdf":
+                last["grads"] = gdn.gdn_chunk_bwd_fused(
+                    d["q"], d["k"], d["v"], d["a"], d["b"], d["h0"],
+                    d["dout"], None, norm_weight=d["norm_weight"],
+                    gate=d["gate"], want_dh0=False)
                 return
             if w["kind"] == "kda":
                 gdn.gdn_kda_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"],
@@ -406,7 +422,7 @@ def run_ours(args, w, device, dist, rank, ws):
               if v is not None)
     d2h = out_host.numel() * out_host.element_size()
     grads_host = {}
-    if w["kind"] == "bwd":
+    if w["kind"] in ("bwd", "bwdf"):
         # the step's results are the gradients (no out)
         grads_host = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
                       for n, t in last["grads"].items() if t is not None}
@@ -460,14 +476,16 @@ def run_ours(args, w, device, dist, rank, ws):
         value = units_all / (ms * 1e-3) * (tok_heads / tokens)  # heads/s
         unit = "token-heads/s"
         e2e_val = units_all / (e2e_ms * 1e-3) * (tok_heads / tokens)
-    elif w["kind"] == "bwd":
+    elif w["kind"] in ("bwd", "bwdf"):
         # fp32 CUDA-core arithmetic per token-head: the forward states (decay
         # d_k d_v, prediction and update 2 d_k d_v each) and the adjoint
         # (S_t, dq, dS += do q^T, du, dS_bar, dg at 2 d_k d_v each, dk at 4,
         # the decay of dS at 1): 22 d_k d_v; the recomputation of each block
-        # (5 d_k d_v more) is not counted
+        # (5 d_k d_v more) is not counted. The fused sublayer's backward runs
+        # the kernel's two sweeps as two launches (its output gradient is
+        # made between them): the kernel's time per step covers both.
         n_k, ms_k = kern.get("bwd_kernel", (0, 0.0))
-        k_ms = ms_k / n_k if n_k else ms
+        k_ms = ms_k / steps if n_k else ms
         flops = 22 * dk * dv * tok_heads
         sms = torch.cuda.get_device_properties(device).multi_processor_count
         mhz = _sm_max_mhz()
@@ -478,8 +496,8 @@ def run_ours(args, w, device, dist, rank, ws):
                 "unit": "TFLOP/s", "frac": round(achieved / alu_tflops, 4),
                 "peak_source": f"derived: {sms} SMs x 128 fp32 FMA/cycle x 2 "
                                f"x {mhz:.0f} MHz (max SM clock)",
-                "algorithmic_flops_per_launch": flops,
-                "launches_per_step": n_k / steps, "ms_per_launch": k_ms}
+                "algorithmic_flops_per_step": flops,
+                "launches_per_step": n_k / steps, "ms_per_step": k_ms}
         value = units_all / (ms * 1e-3)
         unit = "tokens/s"
         e2e_val = units_all / (e2e_ms * 1e-3)
@@ -565,7 +583,7 @@ def run_ours(args, w, device, dist, rank, ws):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if ((w["kind"] == "kda" and args.kda_path == "serial")
-                           or w["kind"] == "bwd") else "bf16",
+                           or w["kind"] in ("bwd", "bwdf")) else "bf16",
         "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), "
                 + ("per-channel g=max(-softplus(N(0,1)),-5)"
                    if w["kind"] == "kda" else "g=-softplus(N(0,1))")
@@ -622,6 +640,22 @@ def cpu_baseline(w, d_host, budget_s=20.0):
         return {"value": tokens / dt, "unit": "tokens/s", "cores": cores,
                 "kind": "oracle",
                 "sample": f"full workload, oracle with the steps either side",
+                "seconds": round(dt, 3)}
+    if w["kind"] == "bwdf":
+        from oracle import backward
+        Tsub = 256
+        sl = lambda x: None if x is None else x[:1, :Tsub, :1]
+        t0 = time.perf_counter()
+        backward.fused_backward(sl(d_host["q"]), sl(d_host["k"]), sl(d_host["v"]),
+                                sl(d_host["a"]), sl(d_host["b"]), None,
+                                sl(d_host["dout"]), weight=d_host["norm_weight"],
+                                gate=sl(d_host["gate"]))
+        dt = time.perf_counter() - t0
+        return {"value": Tsub / w["H"] / dt, "unit": "tokens/s", "cores": 1,
+                "kind": "oracle",
+                "sample": f"1 sequence x 1 of {w['H']} heads x {Tsub} tokens "
+                          f"(fused forward and reverse sweep, numpy), scaled to "
+                          f"all heads",
                 "seconds": round(dt, 3)}
     if w["kind"] == "bwd":
         from oracle import backward
@@ -692,6 +726,17 @@ def run_reference(args, w):
                                   d["state"])
         units, unit, sample = 64 * w["H"], "token-heads/s", \
             f"64 of {w['N']} sequences x {w['H']} heads, one token"
+    elif w["kind"] == "bwdf":
+        from oracle import backward
+        T = 256
+        d = inputs.fused_inputs(1, w["H"], T, w["dk"], w["dv"], seed=0)
+        dout, _ = inputs.grad_inputs(d, seed=0, dhT=False)
+
+        def step():
+            backward.fused_backward(d["q"], d["k"], d["v"], d["a"], d["b"], None,
+                                    dout, weight=d["norm_weight"], gate=d["gate"])
+        units, unit, sample = T, "tokens/s", \
+            f"one sequence of {T} tokens x all {w['H']} heads (fused reverse sweep)"
     elif w["kind"] == "bwd":
         from oracle import backward
         T = 256

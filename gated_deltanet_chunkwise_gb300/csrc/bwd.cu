@@ -32,6 +32,7 @@
 // decay: S_t = S diag(a_t) + u k_t^T) the window keeps S instead of S_bar and
 // the adjoint's last steps become dk_t = dS^T u - beta_t S^T du, dg_t =
 // colsum(dS (.) S diag(a_t)), dS_{t-1} = dS diag(a_t) - beta_t du k_t^T.
+#include <functional>
 #include <type_traits>
 
 #include "gdn_internal.cuh"
@@ -65,6 +66,8 @@ struct BwdArgs {
   int decay_first;          // 1: decay, then predict; 0: predict, then decay
   long long rows;           // tokens * H
   int* status;
+  int passes;               // 1: forward sweep, 2: reverse sweep, 3: both
+  float* o_out;             // [tokens, H, dv] fp32: o_t from the forward sweep, or null
 };
 
 __device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
@@ -171,7 +174,7 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
   uint4 rk[KCH], rq[KCH], rv, rdo;
   float4 rg[GCH];
   float rbeta = 0.f;
-  auto fetch = [&](long long t0, bool back) {
+  auto fetch = [&](long long t0, bool with_q, bool back) {
     const int nt = (int)max(0ll, min((long long)kBwTok, eos - t0));
 #pragma unroll
     for (int j = 0; j < KCH; ++j) {
@@ -180,7 +183,7 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
       if (!kF32 && e < KTOT && tt < nt) {
         const size_t r = ((size_t)(t0 + tt) * H + h) * DK + 8 * c8;
         rk[j] = *reinterpret_cast<const uint4*>(gk + r);
-        if (back) rq[j] = *reinterpret_cast<const uint4*>(gq + r);
+        if (with_q) rq[j] = *reinterpret_cast<const uint4*>(gq + r);
       }
     }
 #pragma unroll
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
       f[4] = x1.x; f[5] = x1.y; f[6] = x1.z; f[7] = x1.w;
     }
   };
-  auto stage = [&](long long t0, bool back) {
+  auto stage = [&](long long t0, bool with_q, bool back) {
     const int nt = (int)max(0ll, min((long long)kBwTok, eos - t0));
 #pragma unroll
     for (int j = 0; j < KCH; ++j) {
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
       for (int x = 0; x < 8; ++x) sm[L::SK + tt * DK + 8 * c8 + x] = f[x];
       if constexpr (kF32) {
         const size_t r = ((size_t)(t0 + tt) * H + h) * DK + 8 * c8;
-        ld8f(gq + r, back && tt < nt, f);
+        ld8f(gq + r, with_q && tt < nt, f);
       } else {
         unpack8(rq[j], f);
       }
@@ -313,17 +316,44 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
     }
     return e;
   };
-  fetch(bos, false);
-  for (int b = 0; b < nblk; ++b) {
-    const long long t0 = bos + (long long)b * kBwTok;
-    const int nt = (int)min((long long)kBwTok, eos - t0);
-    __syncthreads();
-    stage(t0, false);
-    __syncthreads();
-    if (b + 1 < nblk) fetch(t0 + kBwTok, false);
-    put(ckpt(b));
-    for (int tt = 0; tt < nt; ++tt) forward_token(tt, nullptr);
+  const bool want_o = a.o_out != nullptr;
+  if (a.passes & 1) {
+    fetch(bos, want_o, false);
+    for (int b = 0; b < nblk; ++b) {
+      const long long t0 = bos + (long long)b * kBwTok;
+      const int nt = (int)min((long long)kBwTok, eos - t0);
+      __syncthreads();
+      stage(t0, want_o, false);
+      __syncthreads();
+      if (b + 1 < nblk) fetch(t0 + kBwTok, want_o, false);
+      put(ckpt(b));
+      for (int tt = 0; tt < nt; ++tt) {
+        forward_token(tt, nullptr);
+        if (want_o) {
+          // o_t = S_t q_t, this warp's rows
+          float qv[CPT], p[kBwRpw];
+          ld_slice<CPT>(&sm[L::SQ + tt * DK + CPT * lane], qv);
+#pragma unroll
+          for (int r = 0; r < kBwRpw; ++r) {
+            p[r] = 0.f;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) p[r] = fmaf(S[r][j], qv[j], p[r]);
+          }
+          const float orow = rowsum4(p, lane);
+          if ((lane & 7) == 0) sm[L::SDV + tt * kBwRows + kBwRpw * w + rr] = orow;
+        }
+      }
+      if (want_o) {
+        __syncthreads();
+        for (int idx = tid; idx < nt * kBwRows; idx += kBwThreads) {
+          const int tt = idx / kBwRows, r = idx - tt * kBwRows;
+          a.o_out[((size_t)(t0 + tt) * H + h) * dv + row0 + r] =
+              sm[L::SDV + tt * kBwRows + r];
+        }
+      }
+    }
   }
+  if (!(a.passes & 2)) return;
 
   // ---- pass 2: the blocks in reverse ------------------------------------
   float dS[kBwRpw][CPT];
@@ -332,14 +362,14 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
 #pragma unroll
     for (int j = 0; j < CPT; ++j)
       dS[r][j] = a.dhT ? a.dhT[(nh * DK + CPT * lane + j) * dv + a0 + r] : 0.f;
-  if (nblk > 0) fetch(bos + (long long)(nblk - 1) * kBwTok, true);
+  if (nblk > 0) fetch(bos + (long long)(nblk - 1) * kBwTok, true, true);
   for (int b = nblk - 1; b >= 0; --b) {
     const long long t0 = bos + (long long)b * kBwTok;
     const int nt = (int)min((long long)kBwTok, eos - t0);
     __syncthreads();  // the previous block's shared data has been written out
-    stage(t0, true);
+    stage(t0, true, true);
     __syncthreads();
-    if (b > 0) fetch(t0 - kBwTok, true);
+    if (b > 0) fetch(t0 - kBwTok, true, true);
     // recompute the block: S_bar of each token into the window, e of each
     // row into shared memory
     get(ckpt(b), S);
@@ -499,7 +529,8 @@ int run_bwd(const void* q, const void* k, const void* v, const float* g,
             const float* dhT, float* dq, float* dk, float* dvo, float* dg,
             float* dbeta, float* dh0, const int32_t* cu_seqlens, int B, int H,
             int T, int dk_, int dv, bool per_channel, int variant, bool f32,
-            cudaStream_t stream) {
+            cudaStream_t stream, float* o_out,
+            const std::function<cudaError_t()>* between) {
   if (B < 0 || H <= 0 || T < 0) return GDN_ERR_INVALID_ARG;
   if (variant != GDN_GATE_BEFORE_PREDICT && variant != GDN_GATE_AFTER_PREDICT)
     return GDN_ERR_INVALID_ARG;
@@ -568,12 +599,31 @@ int run_bwd(const void* q, const void* k, const void* v, const float* g,
     const int smem = (DKv == 64 ? BwSmem<64>::TOTAL : BwSmem<128>::TOTAL) * (int)sizeof(float);
     cudaError_t x = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (x != cudaSuccess) return x;
+    // both sweeps in one launch, or (with work to do between them: the
+    // gradient of the output from o) the forward sweep, that work, and the
+    // reverse sweep
+    BwdArgs a1 = a;
+    a1.passes = between ? 1 : 3;
+    a1.o_out = o_out;
     int t = timing_start(GDN_KERNEL_BWD, stream);
-    kern<<<dim3(RB, H, B), kBwThreads, smem, stream>>>(a);
+    kern<<<dim3(RB, H, B), kBwThreads, smem, stream>>>(a1);
     x = cudaGetLastError();
     timing_stop(t, stream, x);
     if (x != cudaSuccess) return x;
     ++launches;
+    if (between) {
+      x = (*between)();
+      if (x != cudaSuccess) return x;
+      BwdArgs a2 = a;
+      a2.passes = 2;
+      a2.o_out = nullptr;
+      t = timing_start(GDN_KERNEL_BWD, stream);
+      kern<<<dim3(RB, H, B), kBwThreads, smem, stream>>>(a2);
+      x = cudaGetLastError();
+      timing_stop(t, stream, x);
+      if (x != cudaSuccess) return x;
+      ++launches;
+    }
     if (rows == 0) return cudaSuccess;
     const long long grid = std::min<long long>((long long)rows, 152ll * 32);
     t = timing_start(GDN_KERNEL_BWD_FINALIZE, stream);
@@ -608,7 +658,7 @@ extern "C" int gdn_kda_bwd(const void* q, const void* k, const void* v,
   return gdn::run_bwd(q, k, v, g, beta, h0, dout, dhT, dq, dk, dv, dg, dbeta, dh0,
                       cu_seqlens, B, H, T, dk_, dv_, true,
                       GDN_GATE_BEFORE_PREDICT, false,
-                      static_cast<cudaStream_t>(stream));
+                      static_cast<cudaStream_t>(stream), nullptr, nullptr);
 }
 
 extern "C" int gdn_chunk_bwd(const void* q, const void* k, const void* v,
@@ -620,7 +670,7 @@ extern "C" int gdn_chunk_bwd(const void* q, const void* k, const void* v,
                              gdn_stream_t stream) {
   return gdn::run_bwd(q, k, v, g, beta, h0, dout, dhT, dq, dk, dv, dg, dbeta, dh0,
                       cu_seqlens, B, H, T, dk_, dv_, false, variant, false,
-                      static_cast<cudaStream_t>(stream));
+                      static_cast<cudaStream_t>(stream), nullptr, nullptr);
 }
 
 extern "C" int gdn_chunk_bwd_f32(const float* q, const float* k, const float* v,
@@ -633,5 +683,5 @@ extern "C" int gdn_chunk_bwd_f32(const float* q, const float* k, const float* v,
                                  gdn_stream_t stream) {
   return gdn::run_bwd(q, k, v, g, beta, h0, dout, dhT, dq, dk, dv, dg, dbeta, dh0,
                       cu_seqlens, B, H, T, dk_, dv_, false, variant, true,
-                      static_cast<cudaStream_t>(stream));
+                      static_cast<cudaStream_t>(stream), nullptr, nullptr);
 }

@@ -497,19 +497,17 @@ int gdn_chunk_bwd_fused(const void* q, const void* k, const void* v,
   cudaError_t e = counted(launch_sub_prologue(f, q, k, v, a, b, rows, dk_dim,
                                               dv_dim, st), rows > 0 ? 1 : 0);
   if (e == cudaSuccess) {
-    rc = run_chunk(f.qh, f.kh, f.vf, f.g, f.beta, h0, f.o, nullptr, cu_seqlens, B,
-                   H, T, dk_dim, dv_dim, 64, GDN_DTYPE_F32,
-                   GDN_GATE_BEFORE_PREDICT, GDN_PATH_SIMT, 0, st);
-    if (rc != GDN_OK) e = cudaErrorUnknown;
-  }
-  if (e == cudaSuccess)
-    e = counted(launch_sub_epilogue_bwd(f, dout, norm_weight, gate, eps, rows,
-                                        dv_dim, dgate, dweight, st),
-                rows > 0 ? (dweight ? 2 : 1) : 0);
-  if (e == cudaSuccess) {
+    // the recurrence's backward, whose forward sweep also yields o: the
+    // epilogue's adjoint runs between its two sweeps and produces the
+    // output gradient the reverse sweep reads
+    const std::function<cudaError_t()> between = [&]() {
+      return counted(launch_sub_epilogue_bwd(f, dout, norm_weight, gate, eps,
+                                             rows, dv_dim, dgate, dweight, st),
+                     rows > 0 ? (dweight ? 2 : 1) : 0);
+    };
     rc = run_bwd(f.qh, f.kh, f.vf, f.g, f.beta, h0, f.dO, dhT, f.dqh, f.dkh, dv,
                  f.dg, f.dbeta, dh0, cu_seqlens, B, H, T, dk_dim, dv_dim, false,
-                 GDN_GATE_BEFORE_PREDICT, true, st);
+                 GDN_GATE_BEFORE_PREDICT, true, st, f.o, &between);
     if (rc != GDN_OK) e = cudaErrorUnknown;
   }
   if (e == cudaSuccess)

@@ -1,6 +1,8 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <functional>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -137,13 +139,16 @@ cudaError_t launch_kda(const KdaParams& p, cudaStream_t stream);
 
 // Backward pass (bwd.cu): gradients of the recurrence; per_channel: KDA's
 // g [tokens, H, dk] (else the scalar gate); f32: fp32 q, k, v, dout (else
-// bf16); variant: the gate placement.
+// bf16); variant: the gate placement. With `between`, the kernel's forward
+// sweep (writing o_t to o_out when not null) and its reverse sweep are two
+// launches with `between` enqueued between them (dout may be produced there).
 int run_bwd(const void* q, const void* k, const void* v, const float* g,
             const float* beta, const float* h0, const void* dout,
             const float* dhT, float* dq, float* dk, float* dvo, float* dg,
             float* dbeta, float* dh0, const int32_t* cu_seqlens, int B, int H,
             int T, int dk_, int dv, bool per_channel, int variant, bool f32,
-            cudaStream_t stream);
+            cudaStream_t stream, float* o_out,
+            const std::function<cudaError_t()>* between);
 
 // Backward of the steps either side of the recurrence (fused_bwd.cu):
 // scratch buffers, fp32, per (token, head) row.
