@@ -123,7 +123,10 @@ MEASURED_TRAFFIC = {
     "kda1:21af4a2a3fb88473": 134819328 + 84282112,
     # bwd_kernel, bwd1, one launch (the per-CTA windows of S_bar do not all
     # stay in L2: most of the writes)
-    "bwd1:f86ac4026bf4de8b": 762707456 + 5007061504,
+    "bwd1:79feb7513035267b": 760394496 + 5006012672,
+    # bwd_kernel, bwd1f: its two launches of one step (the forward sweep,
+    # then the reverse sweep), summed: the backward roofline is per step
+    "bwd1f:3ec4992c980e6c1e": (202552832 + 547896064) + (854766336 + 4750786816),
 }
 
 

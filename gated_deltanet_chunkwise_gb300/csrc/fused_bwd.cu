@@ -11,9 +11,11 @@
 //   prologue:  dq_raw = (dq - q (q . dq)) / |q_raw|  (k alike),
 //              da = -dg sigmoid(a),  db = dbeta beta (1 - beta).
 // Three row kernels (one warp per (token, head) row, d / 32 values per lane)
-// and a fixed-order sum of the weight gradient's per-CTA partials; the
-// recurrence's forward output o is recomputed in fp32 by the library's
-// fp32 path, so the gradients are those of the exact (unrounded) map.
+// and a fixed-order sum of the weight gradient's per-CTA partials. The
+// recurrence's forward output o comes in fp32 from the forward sweep of the
+// backward kernel (a launch of its own; the epilogue's adjoint runs between
+// it and the reverse sweep), so the gradients are those of the exact
+// (unrounded) map.
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -136,14 +138,35 @@ __global__ void __launch_bounds__(kRowThreads)
   }
 }
 
-// dweight[c] = sum of the CTAs' partials, in CTA order.
-__global__ void sub_weight_sum_kernel(const float* wpart, int parts, int dv,
-                                      float* dw) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= dv) return;
+// dweight[c] = sum of the CTAs' partials in a fixed order: one CTA of 1024
+// threads, 1024 / dv groups; group j adds the partials i = j mod groups in
+// increasing i (many loads in flight per thread), then the group sums are
+// added in group order.
+constexpr int kWsumThreads = 1024;
+__global__ void __launch_bounds__(kWsumThreads)
+    sub_weight_sum_kernel(const float* __restrict__ wpart, int parts, int dv,
+                          float* dw) {
+  __shared__ float gs[kWsumThreads];
+  const int ng = kWsumThreads / dv, c = threadIdx.x % dv, j = threadIdx.x / dv;
   float s = 0.f;
-  for (int i = 0; i < parts; ++i) s += wpart[(size_t)i * dv + c];
-  dw[c] = s;
+  if (j < ng) {
+    int i = j;
+    for (; i + 3 * ng < parts; i += 4 * ng) {
+      const float x0 = wpart[(size_t)i * dv + c];
+      const float x1 = wpart[(size_t)(i + ng) * dv + c];
+      const float x2 = wpart[(size_t)(i + 2 * ng) * dv + c];
+      const float x3 = wpart[(size_t)(i + 3 * ng) * dv + c];
+      s += x0; s += x1; s += x2; s += x3;
+    }
+    for (; i < parts; i += ng) s += wpart[(size_t)i * dv + c];
+  }
+  gs[threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.x < dv) {
+    float t = 0.f;
+    for (int g = 0; g < ng; ++g) t += gs[g * dv + threadIdx.x];
+    dw[threadIdx.x] = t;
+  }
 }
 
 // dq_raw, dk_raw from the normalised vectors' gradients; da, db.
@@ -230,7 +253,7 @@ cudaError_t launch_sub_epilogue_bwd(const FusedBwdBufs& f, const void* dout,
   if (dv == 64) go(sub_epilogue_bwd_kernel<64>); else go(sub_epilogue_bwd_kernel<128>);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !dweight) return e;
-  sub_weight_sum_kernel<<<1, 128, 0, stream>>>(f.wpart, grid, dv, dweight);
+  sub_weight_sum_kernel<<<1, kWsumThreads, 0, stream>>>(f.wpart, grid, dv, dweight);
   return cudaGetLastError();
 }
 

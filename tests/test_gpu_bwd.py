@@ -219,3 +219,30 @@ def test_fused_bwd_packed(lib, cuda_device):
                                   eps=1e-6)
     for n in ("dq", "dk", "dv", "da", "db", "dh0", "dweight", "dgate"):
         assert rel_err(got[n], ref[n]) <= TOL, n
+
+
+def test_fused_bwd_bench_size_sampled(lib, cuda_device):
+    """The fused-sublayer backward at B=4, H=16, T=2048 (the bench workload:
+    RMSNorm weight and output gate, no h0, no dhT) in the bench's launch
+    configuration; two (sequence, head) pairs against the fused gradient
+    oracle on their slices (the norm and gate act within a (token, head), so
+    every gradient but dweight, a sum over all of them, depends on the slice
+    alone; dweight is checked at the small sizes above)."""
+    d = inputs.fused_inputs(4, 16, 2048, 128, 128, seed=75)
+    dout, _ = inputs.grad_inputs(d, seed=12, dhT=False)
+    x = lambda t: None if t is None else t.to(cuda_device)
+    got = lib.gdn_chunk_bwd_fused(x(d["q"]), x(d["k"]), x(d["v"]), x(d["a"]),
+                                  x(d["b"]), None, x(dout), None,
+                                  norm_weight=x(d["norm_weight"]),
+                                  gate=x(d["gate"]), want_dh0=True)
+    torch.cuda.synchronize(cuda_device)
+    assert lib.gdn_device_status() == 0
+    for n, h in ((1, 2), (2, 15)):
+        sl = lambda t: t[n:n + 1, :, h:h + 1]
+        ref = backward.fused_backward(sl(d["q"]), sl(d["k"]), sl(d["v"]),
+                                      sl(d["a"]), sl(d["b"]), None, sl(dout),
+                                      weight=d["norm_weight"],
+                                      gate=sl(d["gate"]))
+        for name in ("dq", "dk", "dv", "da", "db", "dgate"):
+            assert rel_err(sl(got[name]), ref[name]) <= TOL, (name, n, h)
+        assert rel_err(got["dh0"][n:n + 1, h:h + 1], ref["dh0"]) <= TOL

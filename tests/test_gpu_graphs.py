@@ -119,3 +119,28 @@ def test_decode_step_replays_advance_the_state(lib, cuda_device):
     torch.cuda.synchronize()
     assert torch.equal(replayed, static["state"])
     assert lib.gdn_device_status() == 0
+
+
+def test_fused_backward_replays(lib, cuda_device):
+    """The fused-sublayer backward (five kernels and the backward kernel's two
+    sweeps) replays bit for bit."""
+    dev = cuda_device
+    first = inputs.fused_inputs(1, 2, 150, 128, 128, seed=89, h0=True)
+    first["dout"], first["dhT"] = inputs.grad_inputs(first, seed=89)
+    static = {k: (None if v is None else v.to(dev)) for k, v in first.items()}
+    call = lambda: lib.gdn_chunk_bwd_fused(
+        static["q"], static["k"], static["v"], static["a"], static["b"],
+        static["h0"], static["dout"], static["dhT"],
+        norm_weight=static["norm_weight"], gate=static["gate"])
+    g, res = capture(call)
+    d = inputs.fused_inputs(1, 2, 150, 128, 128, seed=90, h0=True)
+    d["dout"], d["dhT"] = inputs.grad_inputs(d, seed=90)
+    fill(static, d)
+    g.replay()
+    torch.cuda.synchronize()
+    got = {k: v.clone() for k, v in res.items() if v is not None}
+    eager = call()
+    torch.cuda.synchronize()
+    for k in got:
+        assert torch.equal(got[k], eager[k]), k
+    assert lib.gdn_device_status() == 0
