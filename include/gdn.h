@@ -265,8 +265,10 @@ int gdn_kda_fwd_ex(const void* q, const void* k, const void* v, const float* g,
  * The forward state is recomputed on the GPU in fp32: a forward sweep keeps
  * the state every 16 tokens, then each 16-token block is recomputed from its
  * checkpoint and swept backwards. Scratch (cudaMallocAsync on `stream`):
- * about 1 KB per token and 32 value rows for the checkpoints, plus 3 dk + 1
- * floats per token, head and 32 value rows of partial sums. Asynchronous on
+ * about 1 KB per token and 32 value rows for the checkpoints (dk = 128; half
+ * for dk = 64), 3 dk + 1 floats per token, head and 32 value rows of partial
+ * sums, and a window of the recomputed 16-token block (256 KB per sequence,
+ * head and 32 value rows at dk = 128). Asynchronous on
  * `stream`; an invalid packing is recorded in the status word. Returns GDN_OK,
  * GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED (head dims other than 64 / 128,
  * more than 65535 sequences), GDN_ERR_MISALIGNED or GDN_ERR_CUDA.
@@ -310,10 +312,12 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g,
  * h0, dhT fp32; eps >= 0); outputs fp32: dq, dk [B, T, H, dk], dv
  * [B, T, H, dv], da, db [B, T, H], dh0 [N, H, dk, dv] or NULL, dweight
  * [dv] (only with norm_weight) or NULL, dgate like v (only with gate) or
- * NULL. The recurrence's output is recomputed in fp32 (gdn_chunk_fwd_f32's
- * path) and its backward runs on the fp32 normalised inputs, so these are the
- * gradients of the exact map. dk, dv in {64, 128}. Scratch: about 4 (4 dk +
- * 3 dv) bytes per token and head (cudaMallocAsync on `stream`). Returns as
+ * NULL. The recurrence runs on the fp32 normalised inputs: the backward
+ * kernel's forward sweep (a launch of its own) forms o in fp32 with its
+ * checkpoints, the epilogue's adjoint turns dout into do, and the reverse
+ * sweep follows; so these are the gradients of the exact (unrounded) map.
+ * dk, dv in {64, 128}. Scratch (cudaMallocAsync on `stream`): about 4 (4 dk
+ * + 3 dv + 6) bytes per token and head, plus gdn_chunk_bwd's. Returns as
  * gdn_chunk_bwd.
  */
 int gdn_chunk_bwd_fused(const void* q, const void* k, const void* v,
