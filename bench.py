@@ -123,10 +123,10 @@ MEASURED_TRAFFIC = {
     "kda1:21af4a2a3fb88473": 134819328 + 84282112,
     # bwd_kernel, bwd1, one launch (the per-CTA windows of S_bar do not all
     # stay in L2: most of the writes)
-    "bwd1:79feb7513035267b": 760394496 + 5006012672,
+    "bwd1:e6e8ce911b3198e0": 761174272 + 5027586560,
     # bwd_kernel, bwd1f: its two launches of one step (the forward sweep,
     # then the reverse sweep), summed: the backward roofline is per step
-    "bwd1f:3ec4992c980e6c1e": (202552832 + 547896064) + (854766336 + 4750786816),
+    "bwd1f:ed3ac2f1f4038bda": (202519808 + 547909632) + (860115968 + 4726744064),
 }
 
 

@@ -477,41 +477,59 @@ __global__ void __launch_bounds__(kBwThreads, 2) bwd_kernel(const BwdArgs a) {
 }
 
 // dq, dk, dg (per channel, or summed over channels for the scalar gate) and
-// dbeta: the sums of the row blocks' partials, one CTA of DK threads per
-// (token, head) row.
+// dbeta: the sums of the row blocks' partials in row-block order, one warp
+// per (token, head) row (each lane DK / 32 consecutive channels, loaded as
+// one vector: all 3 x RB loads of a row in flight at once).
+constexpr int kFinThreads = 256;
 template <int DK>
-__global__ void __launch_bounds__(DK)
+__global__ void __launch_bounds__(kFinThreads)
     bwd_finalize_kernel(const float* __restrict__ part,
                         const float* __restrict__ part_b, int RB,
                         long long rows, float* dq, float* dk, float* dg,
                         float* dbeta, int g_chan) {
-  __shared__ float red[DK / 32];
-  const int c = threadIdx.x, lane = c & 31, wv = c >> 5;
-  for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
-    float sq = 0.f, sk = 0.f, sg = 0.f;
+  constexpr int CPL = DK / 32;
+  using V = typename std::conditional<CPL == 4, float4, float2>::type;
+  const int lane = threadIdx.x & 31;
+  const long long w0 = ((long long)blockIdx.x * kFinThreads + threadIdx.x) >> 5;
+  const long long nw = ((long long)gridDim.x * kFinThreads) >> 5;
+  auto add = [](float (&acc)[CPL], const V& x) {
+    const float* f = reinterpret_cast<const float*>(&x);
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) acc[j] += f[j];
+  };
+  auto put = [](float* dst, const float (&x)[CPL]) {
+    V v;
+    float* f = reinterpret_cast<float*>(&v);
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) f[j] = x[j];
+    *reinterpret_cast<V*>(dst) = v;
+  };
+  for (long long row = w0; row < rows; row += nw) {
+    float sq[CPL], sk[CPL], sg[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) sq[j] = sk[j] = sg[j] = 0.f;
+    const size_t c0 = (size_t)row * DK + CPL * lane;
     for (int rb = 0; rb < RB; ++rb) {
-      sq += part[(((size_t)0 * RB + rb) * rows + row) * DK + c];
-      sk += part[(((size_t)1 * RB + rb) * rows + row) * DK + c];
-      sg += part[(((size_t)2 * RB + rb) * rows + row) * DK + c];
+      const V xq = *reinterpret_cast<const V*>(part + ((size_t)0 * RB + rb) * rows * DK + c0);
+      const V xk = *reinterpret_cast<const V*>(part + ((size_t)1 * RB + rb) * rows * DK + c0);
+      const V xg = *reinterpret_cast<const V*>(part + ((size_t)2 * RB + rb) * rows * DK + c0);
+      add(sq, xq);
+      add(sk, xk);
+      add(sg, xg);
     }
-    dq[(size_t)row * DK + c] = sq;
-    dk[(size_t)row * DK + c] = sk;
+    put(dq + c0, sq);
+    put(dk + c0, sk);
     if (g_chan != 1) {
-      dg[(size_t)row * DK + c] = sg;
+      put(dg + c0, sg);
     } else {
+      float t = 0.f;
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) sg += __shfl_xor_sync(0xffffffffu, sg, off);
-      if (lane == 0) red[wv] = sg;
-      __syncthreads();
-      if (c == 0) {
-        float s = 0.f;
+      for (int j = 0; j < CPL; ++j) t += sg[j];
 #pragma unroll
-        for (int i = 0; i < DK / 32; ++i) s += red[i];
-        dg[row] = s;
-      }
-      __syncthreads();
+      for (int off = 16; off >= 1; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+      if (lane == 0) dg[row] = t;
     }
-    if (c == 0) {
+    if (lane == 0) {
       float sb = 0.f;
       for (int rb = 0; rb < RB; ++rb) sb += part_b[(size_t)rb * rows + row];
       dbeta[row] = sb;
@@ -625,10 +643,10 @@ int run_bwd(const void* q, const void* k, const void* v, const float* g,
       ++launches;
     }
     if (rows == 0) return cudaSuccess;
-    const long long grid = std::min<long long>((long long)rows, 152ll * 32);
+    const long long grid = std::min<long long>(((long long)rows + 7) / 8, 152ll * 8);
     t = timing_start(GDN_KERNEL_BWD_FINALIZE, stream);
-    fin<<<(int)grid, DKv, 0, stream>>>(a.part, a.part_b, RB, (long long)rows, dq, dk, dg,
-                                       dbeta, a.g_chan);
+    fin<<<(int)grid, kFinThreads, 0, stream>>>(a.part, a.part_b, RB, (long long)rows, dq,
+                                               dk, dg, dbeta, a.g_chan);
     x = cudaGetLastError();
     timing_stop(t, stream, x);
     if (x == cudaSuccess) ++launches;

@@ -30,6 +30,36 @@ __device__ __forceinline__ float warp_sum(float x) {
 }
 __device__ __forceinline__ float sigm(float x) { return 1.f / (1.f + expf(-x)); }
 
+// A lane's N consecutive values of a row (N = d / 32), one vector access.
+template <int N>
+__device__ __forceinline__ void ldv(const float* p, float (&x)[N]) {
+  if constexpr (N == 4) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  } else {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    x[0] = v.x; x[1] = v.y;
+  }
+}
+template <int N>
+__device__ __forceinline__ void ldv(const __nv_bfloat16* p, float (&x)[N]) {
+  if constexpr (N == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    x[0] = __uint_as_float(v.x << 16); x[1] = __uint_as_float(v.x & 0xffff0000u);
+    x[2] = __uint_as_float(v.y << 16); x[3] = __uint_as_float(v.y & 0xffff0000u);
+  } else {
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+    x[0] = __uint_as_float(v << 16); x[1] = __uint_as_float(v & 0xffff0000u);
+  }
+}
+template <int N>
+__device__ __forceinline__ void stv(float* p, const float (&x)[N]) {
+  if constexpr (N == 4)
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+  else
+    *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
+}
+
 // q, k normalised (fp32), v widened to fp32, g = -softplus(a), beta =
 // sigmoid(b), and the inverse lengths of q and k (0 for a zero row).
 template <int DK, int DV>
@@ -40,15 +70,18 @@ __global__ void __launch_bounds__(kRowThreads)
                         const float* __restrict__ a, const float* __restrict__ b,
                         long long rows, float* qh, float* kh, float* vf,
                         float* g, float* beta, float* invq, float* invk) {
+  constexpr int NK = DK / 32, NV = DV / 32;
   const int lane = threadIdx.x & 31;
   const long long w0 = ((long long)blockIdx.x * kRowThreads + threadIdx.x) >> 5;
   const long long nw = ((long long)gridDim.x * kRowThreads) >> 5;
   for (long long row = w0; row < rows; row += nw) {
-    float xq[DK / 32], xk[DK / 32], sq = 0.f, sk = 0.f;
+    const long long ek = row * DK + NK * lane, ev = row * DV + NV * lane;
+    float xq[NK], xk[NK], xv[NV], sq = 0.f, sk = 0.f;
+    ldv<NK>(q + ek, xq);
+    ldv<NK>(k + ek, xk);
+    ldv<NV>(v + ev, xv);
 #pragma unroll
-    for (int j = 0; j < DK / 32; ++j) {
-      xq[j] = __bfloat162float(q[row * DK + lane + 32 * j]);
-      xk[j] = __bfloat162float(k[row * DK + lane + 32 * j]);
+    for (int j = 0; j < NK; ++j) {
       sq = fmaf(xq[j], xq[j], sq);
       sk = fmaf(xk[j], xk[j], sk);
     }
@@ -56,13 +89,13 @@ __global__ void __launch_bounds__(kRowThreads)
     sk = warp_sum(sk);
     const float iq = sq > 0.f ? rsqrtf(sq) : 0.f, ik = sk > 0.f ? rsqrtf(sk) : 0.f;
 #pragma unroll
-    for (int j = 0; j < DK / 32; ++j) {
-      qh[row * DK + lane + 32 * j] = xq[j] * iq;
-      kh[row * DK + lane + 32 * j] = xk[j] * ik;
+    for (int j = 0; j < NK; ++j) {
+      xq[j] *= iq;
+      xk[j] *= ik;
     }
-#pragma unroll
-    for (int j = 0; j < DV / 32; ++j)
-      vf[row * DV + lane + 32 * j] = __bfloat162float(v[row * DV + lane + 32 * j]);
+    stv<NK>(qh + ek, xq);
+    stv<NK>(kh + ek, xk);
+    stv<NV>(vf + ev, xv);
     if (lane == 0) {
       const float x = a[row];
       g[row] = -(fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))));
@@ -83,52 +116,54 @@ __global__ void __launch_bounds__(kRowThreads)
                             const __nv_bfloat16* __restrict__ z, float eps,
                             long long rows, float* dO, float* dgate,
                             float* wpart) {
+  constexpr int NV = DV / 32;
   __shared__ float red[kRowThreads / 32][DV];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long long w0 = ((long long)blockIdx.x * kRowThreads + threadIdx.x) >> 5;
   const long long nw = ((long long)gridDim.x * kRowThreads) >> 5;
-  float dwacc[DV / 32];
+  float dwacc[NV], wv[NV];
 #pragma unroll
-  for (int j = 0; j < DV / 32; ++j) dwacc[j] = 0.f;
+  for (int j = 0; j < NV; ++j) {
+    dwacc[j] = 0.f;
+    wv[j] = w ? w[NV * lane + j] : 1.f;
+  }
   for (long long row = w0; row < rows; row += nw) {
-    float x[DV / 32], dy[DV / 32], ss = 0.f;
+    const long long e = row * DV + NV * lane;
+    float x[NV], dy[NV], zz[NV], ss = 0.f;
+    ldv<NV>(o + e, x);
+    ldv<NV>(dout + e, dy);
+    if (z) ldv<NV>(z + e, zz);
 #pragma unroll
-    for (int j = 0; j < DV / 32; ++j) {
-      x[j] = o[row * DV + lane + 32 * j];
-      dy[j] = __bfloat162float(dout[row * DV + lane + 32 * j]);
-      ss = fmaf(x[j], x[j], ss);
-    }
+    for (int j = 0; j < NV; ++j) ss = fmaf(x[j], x[j], ss);
     const float r = w ? rsqrtf(warp_sum(ss) * (1.f / DV) + eps) : 1.f;
+    float dz[NV];
 #pragma unroll
-    for (int j = 0; j < DV / 32; ++j) {
-      const int c = lane + 32 * j;
-      const float n = x[j] * r, pre = w ? n * w[c] : x[j];
+    for (int j = 0; j < NV; ++j) {
+      const float n = x[j] * r, pre = w ? n * wv[j] : x[j];
       if (z) {
-        const float s = sigm(__bfloat162float(z[row * DV + c]));
-        if (dgate) dgate[row * DV + c] = dy[j] * pre * s * (1.f - s);
-        dy[j] *= s;
+        const float sg = sigm(zz[j]);
+        dz[j] = dy[j] * pre * sg * (1.f - sg);
+        dy[j] *= sg;
       }
       if (w) {
         dwacc[j] = fmaf(dy[j], n, dwacc[j]);
-        dy[j] *= w[c];  // now dn
+        dy[j] *= wv[j];  // now dn
       }
     }
+    if (z && dgate) stv<NV>(dgate + e, dz);
     if (w) {
       float t = 0.f;
 #pragma unroll
-      for (int j = 0; j < DV / 32; ++j) t = fmaf(dy[j], x[j] * r, t);
+      for (int j = 0; j < NV; ++j) t = fmaf(dy[j], x[j] * r, t);
       const float m = warp_sum(t) * (1.f / DV);
 #pragma unroll
-      for (int j = 0; j < DV / 32; ++j)
-        dO[row * DV + lane + 32 * j] = r * (dy[j] - x[j] * r * m);
-    } else {
-#pragma unroll
-      for (int j = 0; j < DV / 32; ++j) dO[row * DV + lane + 32 * j] = dy[j];
+      for (int j = 0; j < NV; ++j) dy[j] = r * (dy[j] - x[j] * r * m);
     }
+    stv<NV>(dO + e, dy);
   }
   if (!w) return;
 #pragma unroll
-  for (int j = 0; j < DV / 32; ++j) red[warp][lane + 32 * j] = dwacc[j];
+  for (int j = 0; j < NV; ++j) red[warp][NV * lane + j] = dwacc[j];
   __syncthreads();
   for (int c = threadIdx.x; c < DV; c += kRowThreads) {
     float s = 0.f;
@@ -183,26 +218,32 @@ __global__ void __launch_bounds__(kRowThreads)
                             const float* __restrict__ dg,
                             const float* __restrict__ dbeta, long long rows,
                             float* dq, float* dk, float* da, float* db) {
+  constexpr int NK = DK / 32;
   const int lane = threadIdx.x & 31;
   const long long w0 = ((long long)blockIdx.x * kRowThreads + threadIdx.x) >> 5;
   const long long nw = ((long long)gridDim.x * kRowThreads) >> 5;
   for (long long row = w0; row < rows; row += nw) {
-    float tq = 0.f, tk = 0.f;
+    const long long e = row * DK + NK * lane;
+    float xq[NK], xk[NK], gq[NK], gk[NK], tq = 0.f, tk = 0.f;
+    ldv<NK>(qh + e, xq);
+    ldv<NK>(kh + e, xk);
+    ldv<NK>(dqh + e, gq);
+    ldv<NK>(dkh + e, gk);
 #pragma unroll
-    for (int j = 0; j < DK / 32; ++j) {
-      const long long e = row * DK + lane + 32 * j;
-      tq = fmaf(qh[e], dqh[e], tq);
-      tk = fmaf(kh[e], dkh[e], tk);
+    for (int j = 0; j < NK; ++j) {
+      tq = fmaf(xq[j], gq[j], tq);
+      tk = fmaf(xk[j], gk[j], tk);
     }
     tq = warp_sum(tq);
     tk = warp_sum(tk);
     const float iq = invq[row], ik = invk[row];
 #pragma unroll
-    for (int j = 0; j < DK / 32; ++j) {
-      const long long e = row * DK + lane + 32 * j;
-      dq[e] = (dqh[e] - qh[e] * tq) * iq;
-      dk[e] = (dkh[e] - kh[e] * tk) * ik;
+    for (int j = 0; j < NK; ++j) {
+      gq[j] = (gq[j] - xq[j] * tq) * iq;
+      gk[j] = (gk[j] - xk[j] * tk) * ik;
     }
+    stv<NK>(dq + e, gq);
+    stv<NK>(dk + e, gk);
     if (lane == 0) {
       da[row] = -dg[row] * sigm(a[row]);
       const float bt = beta[row];
