@@ -7,7 +7,7 @@ One step = one call of the whole forward path (every kernel the library
 launches for it). Prints ONE JSON line on rank 0.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload w1|w2|w3|w4]
+                    [--workload w1|w1f|w2|w3|w4|kda1|bwd1|bwd1k|bwd1f]
 
 Timing: inputs resident in HBM, the L2 (129 MB) is flushed before every
 timed step by a 256 MiB memset followed by a read of another 256 MiB buffer
@@ -46,6 +46,8 @@ def _metric(w):
         return "KDA (per-channel decay) forward tokens/s + % of GB300 roofline, 1 GPU"
     if w["kind"] in ("bwd", "bwdf"):
         return "GDN backward tokens/s + % of GB300 fp32 ALU peak, 1 GPU"
+    if w["kind"] == "bwdk":
+        return "KDA (per-channel decay) backward tokens/s + % of GB300 fp32 ALU peak, 1 GPU"
     return METRIC
 
 # Algorithmic work per token-head of the chunked forward pass:
@@ -99,6 +101,10 @@ WORKLOADS = {
                  desc="gdn_chunk_bwd B=4 H=16 T=2048 dk=dv=128 bf16 inputs, "
                       "fp32 gradients of out (dout ~ N(0,1) bf16), h0=0, "
                       "no dhT"),
+    "bwd1k": dict(kind="bwdk", B=4, H=16, T=2048, dk=128, dv=128, h0=False,
+                  desc="gdn_kda_bwd B=4 H=16 T=2048 dk=dv=128 bf16 inputs, "
+                       "per-channel log-decays, fp32 gradients of out "
+                       "(dout ~ N(0,1) bf16), h0=0, no dhT"),
     "bwd1f": dict(kind="bwdf", B=4, H=16, T=2048, dk=128, dv=128, h0=False,
                   desc="gdn_chunk_bwd_fused B=4 H=16 T=2048 dk=dv=128: raw "
                        "q/k, gate and step logits, RMSNorm weight and output "
@@ -124,6 +130,8 @@ MEASURED_TRAFFIC = {
     # bwd_kernel, bwd1, one launch (the per-CTA windows of S_bar do not all
     # stay in L2: most of the writes)
     "bwd1:e6e8ce911b3198e0": 761174272 + 5027586560,
+    # bwd_kernel, bwd1k (per-channel decay), one launch
+    "bwd1k:e6e8ce911b3198e0": 917715968 + 5183326720,
     # bwd_kernel, bwd1f: its two launches of one step (the forward sweep,
     # then the reverse sweep), summed: the backward roofline is per step
     "bwd1f:ed3ac2f1f4038bda": (202519808 + 547909632) + (860115968 + 4726744064),
@@ -133,7 +141,7 @@ MEASURED_TRAFFIC = {
 def _kernel_source_hash(kind):
     csrc = ROOT / "gated_deltanet_chunkwise_gb300" / "csrc"
     files = (["decode.cu"] if kind == "decode"
-             else ["bwd.cu"] if kind == "bwd"
+             else ["bwd.cu"] if kind in ("bwd", "bwdk")
              else ["bwd.cu", "fused_bwd.cu"] if kind == "bwdf"
              else ["kda.cu", "kda_chunk.cu", "chunk_tc.cu"] if kind == "kda"
              else sorted(p.name for p in csrc.glob("chunk_*.cu")))
@@ -278,6 +286,11 @@ def _make_inputs(w, seed=0):
                                 seed=seed, h0=w["h0"])
         d["dout"], _ = inputs.grad_inputs(d, seed=seed, dhT=False)
         return d
+    if w["kind"] == "bwdk":
+        d = inputs.kda_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
+                              seed=seed, h0=w["h0"])
+        d["dout"], _ = inputs.grad_inputs(d, seed=seed, dhT=False)
+        return d
     return inputs.chunk_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
                                dtype="bf16", seed=seed, h0=w["h0"],
                                length_range=w.get("lengths"))
@@ -329,6 +342,11 @@ def run_ours(args, w, device, dist, rank, ws):
         def step():
             if w["kind"] == "bwd":
                 last["grads"] = gdn.gdn_chunk_bwd(
+                    d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"],
+                    d["dout"], None, want_dh0=False)
+                return
+            if w["kind"] == "bwdk":
+                last["grads"] = gdn.gdn_kda_bwd(
                     d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"],
                     d["dout"], None, want_dh0=False)
                 return
@@ -425,7 +443,7 @@ def run_ours(args, w, device, dist, rank, ws):
               if v is not None)
     d2h = out_host.numel() * out_host.element_size()
     grads_host = {}
-    if w["kind"] in ("bwd", "bwdf"):
+    if w["kind"] in ("bwd", "bwdf", "bwdk"):
         # the step's results are the gradients (no out)
         grads_host = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
                       for n, t in last["grads"].items() if t is not None}
@@ -479,7 +497,7 @@ def run_ours(args, w, device, dist, rank, ws):
         value = units_all / (ms * 1e-3) * (tok_heads / tokens)  # heads/s
         unit = "token-heads/s"
         e2e_val = units_all / (e2e_ms * 1e-3) * (tok_heads / tokens)
-    elif w["kind"] in ("bwd", "bwdf"):
+    elif w["kind"] in ("bwd", "bwdf", "bwdk"):
         # fp32 CUDA-core arithmetic per token-head: the forward states (decay
         # d_k d_v, prediction and update 2 d_k d_v each) and the adjoint
         # (S_t, dq, dS += do q^T, du, dS_bar, dg at 2 d_k d_v each, dk at 4,
@@ -586,10 +604,10 @@ def run_ours(args, w, device, dist, rank, ws):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if ((w["kind"] == "kda" and args.kda_path == "serial")
-                           or w["kind"] in ("bwd", "bwdf")) else "bf16",
+                           or w["kind"] in ("bwd", "bwdf", "bwdk")) else "bf16",
         "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), "
                 + ("per-channel g=max(-softplus(N(0,1)),-5)"
-                   if w["kind"] == "kda" else "g=-softplus(N(0,1))")
+                   if w["kind"] in ("kda", "bwdk") else "g=-softplus(N(0,1))")
                 + ", beta=sigmoid(N(0,1)))",
         "config": {"workload": w["desc"] + (
                        f" [sub-sequences: {args.sp_combine}"
@@ -659,6 +677,20 @@ def cpu_baseline(w, d_host, budget_s=20.0):
                 "sample": f"1 sequence x 1 of {w['H']} heads x {Tsub} tokens "
                           f"(fused forward and reverse sweep, numpy), scaled to "
                           f"all heads",
+                "seconds": round(dt, 3)}
+    if w["kind"] == "bwdk":
+        from oracle import backward
+        Tsub = 256
+        sl = lambda x: x[:1, :Tsub, :1]
+        t0 = time.perf_counter()
+        backward.kda_backward(sl(d_host["q"]), sl(d_host["k"]), sl(d_host["v"]),
+                              sl(d_host["g"]), sl(d_host["beta"]), None,
+                              sl(d_host["dout"]))
+        dt = time.perf_counter() - t0
+        return {"value": Tsub / w["H"] / dt, "unit": "tokens/s", "cores": 1,
+                "kind": "oracle",
+                "sample": f"1 sequence x 1 of {w['H']} heads x {Tsub} tokens "
+                          f"(reverse sweep, numpy), scaled to all heads",
                 "seconds": round(dt, 3)}
     if w["kind"] == "bwd":
         from oracle import backward
@@ -740,6 +772,17 @@ def run_reference(args, w):
                                     dout, weight=d["norm_weight"], gate=d["gate"])
         units, unit, sample = T, "tokens/s", \
             f"one sequence of {T} tokens x all {w['H']} heads (fused reverse sweep)"
+    elif w["kind"] == "bwdk":
+        from oracle import backward
+        T = 256
+        d = inputs.kda_inputs(1, w["H"], T, w["dk"], w["dv"], seed=0)
+        dout, _ = inputs.grad_inputs(d, seed=0, dhT=False)
+
+        def step():
+            backward.kda_backward(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                  None, dout)
+        units, unit, sample = T, "tokens/s", \
+            f"one sequence of {T} tokens x all {w['H']} heads (reverse sweep)"
     elif w["kind"] == "bwd":
         from oracle import backward
         T = 256

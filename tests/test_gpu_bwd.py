@@ -246,3 +246,23 @@ def test_fused_bwd_bench_size_sampled(lib, cuda_device):
         for name in ("dq", "dk", "dv", "da", "db", "dgate"):
             assert rel_err(sl(got[name]), ref[name]) <= TOL, (name, n, h)
         assert rel_err(got["dh0"][n:n + 1, h:h + 1], ref["dh0"]) <= TOL
+
+
+def test_kda_bwd_bench_size_sampled(lib, cuda_device):
+    """gdn_kda_bwd at B=4, H=16, T=2048 (the per-channel backward bench
+    workload) in the bench's launch configuration; two (sequence, head)
+    pairs against the oracle on their slices."""
+    d = inputs.kda_inputs(4, 16, 2048, 128, 128, seed=68)
+    dout, _ = inputs.grad_inputs(d, seed=7, dhT=False)
+    x = lambda t: None if t is None else t.to(cuda_device)
+    got = lib.gdn_kda_bwd(x(d["q"]), x(d["k"]), x(d["v"]), x(d["g"]),
+                          x(d["beta"]), None, x(dout), None)
+    torch.cuda.synchronize(cuda_device)
+    assert lib.gdn_device_status() == 0
+    for n, h in ((0, 5), (3, 11)):
+        sl = lambda t: t[n:n + 1, :, h:h + 1]
+        ref = backward.kda_backward(sl(d["q"]), sl(d["k"]), sl(d["v"]),
+                                    sl(d["g"]), sl(d["beta"]), None, sl(dout))
+        for name in GRADS:
+            assert rel_err(sl(got[name]), ref[name]) <= TOL, (name, n, h)
+        assert rel_err(got["dh0"][n:n + 1, h:h + 1], ref["dh0"]) <= TOL
