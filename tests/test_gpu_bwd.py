@@ -176,12 +176,12 @@ def test_bwd_bench_size_sampled(lib, cuda_device):
 
 @pytest.mark.parametrize("weight,gate", [(True, True), (True, False),
                                          (False, True), (False, False)])
-@pytest.mark.parametrize("dv", [64, 128])
-def test_fused_bwd_matches_oracle(lib, cuda_device, weight, gate, dv):
+@pytest.mark.parametrize("dk,dv", [(128, 64), (128, 128), (64, 64), (64, 128)])
+def test_fused_bwd_matches_oracle(lib, cuda_device, weight, gate, dk, dv):
     """gdn_chunk_bwd_fused against the fused-sublayer gradient oracle (raw q,
     k with lengths in [0.25, 4), gate and step logits, RMSNorm weight and
     output gate when present)."""
-    d = inputs.fused_inputs(2, 2, 77, 128, dv, seed=73, h0=True, weight=weight,
+    d = inputs.fused_inputs(2, 2, 77, dk, dv, seed=73, h0=True, weight=weight,
                             gate=gate)
     dout, dh = inputs.grad_inputs(d, seed=10)
     x = lambda t: None if t is None else t.to(cuda_device)
