@@ -591,7 +591,9 @@ def run_ours(args, w, device, dist, rank, ws):
         value = units_all / (ms * 1e-3)
         unit = "tokens/s"
         e2e_val = units_all / (e2e_ms * 1e-3)
-    key = f"{args.workload}:{_kernel_source_hash(w['kind'])}"
+    # the traffic entry belongs to the dominant kernel of the path timed
+    path_tag = "-serial" if (w["kind"] == "kda" and args.kda_path == "serial") else ""
+    key = f"{args.workload}{path_tag}:{_kernel_source_hash(w['kind'])}"
     roof["traffic"] = MEASURED_TRAFFIC.get(key)
     roof["kernel_ms_per_step"] = {k: round(v[1] / steps, 5)
                                   for k, v in kern.items()}
