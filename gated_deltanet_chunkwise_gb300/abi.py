@@ -165,6 +165,14 @@ def _need(t, name, dtype, device):
     return t
 
 
+def _shape(t, name, shape):
+    """The kernels index by the sizes passed: a tensor of another shape would
+    be read or written out of bounds, so it is refused here."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be {list(shape)}, got {list(t.shape)}")
+    return t
+
+
 def _chunk_call(fn_name, q, k, v, g, beta, h0, cu_seqlens, out, hT,
                 output_final_state, C, stream, io_dtype, extra=()):
     fn = getattr(library(), fn_name)
@@ -183,6 +191,8 @@ def _chunk_call_fn(fn, fn_name, q, k, v, g, beta, h0, cu_seqlens, out, hT,
     _need(v, "v", io_dtype, dev)
     _need(g, "g", torch.float32, dev)
     _need(beta, "beta", torch.float32, dev)
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q/k must be [B, T, H, dk] and v [B, T, H, dv]")
     Bt, T, H, dk = q.shape
     dv = v.shape[-1]
     if k.shape != q.shape or v.shape[:3] != (Bt, T, H):
@@ -203,11 +213,11 @@ def _chunk_call_fn(fn, fn_name, q, k, v, g, beta, h0, cu_seqlens, out, hT,
     if out is None:
         out = torch.empty_like(v)
     else:
-        _need(out, "out", io_dtype, dev)
+        _shape(_need(out, "out", io_dtype, dev), "out", v.shape)
     if hT is None and output_final_state:
         hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
     elif hT is not None:
-        _need(hT, "hT", torch.float32, dev)
+        _shape(_need(hT, "hT", torch.float32, dev), "hT", (N, H, dk, dv))
     with torch.cuda.device(dev):
         rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
                 _ptr(out), _ptr(hT), _ptr(cu_seqlens), N, H, T, dk, dv, C,
@@ -306,20 +316,30 @@ def gdn_chunk_bwd_fused(q, k, v, a, b, h0, dout, dhT=None, cu_seqlens=None, *,
         _need(t, name, torch.bfloat16, dev)
     _need(a, "a", torch.float32, dev)
     _need(b, "b", torch.float32, dev)
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q/k must be [B, T, H, dk] and v/dout [B, T, H, dv]")
     Bt, T, H, dk = q.shape
     dv = v.shape[-1]
+    _shape(k, "k", q.shape)
+    _shape(v, "v", (Bt, T, H, dv))
+    _shape(dout, "dout", v.shape)
+    _shape(a, "a", (Bt, T, H))
+    _shape(b, "b", (Bt, T, H))
     if cu_seqlens is not None:
         _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+        if Bt != 1:
+            raise ValueError("packed sequences are passed as [1, T, H, ...]")
         N = cu_seqlens.numel() - 1
     else:
         N = Bt
     if norm_weight is not None:
-        _need(norm_weight, "norm_weight", torch.float32, dev)
+        _shape(_need(norm_weight, "norm_weight", torch.float32, dev),
+               "norm_weight", (dv,))
     if gate is not None:
-        _need(gate, "gate", torch.bfloat16, dev)
+        _shape(_need(gate, "gate", torch.bfloat16, dev), "gate", v.shape)
     for name, st in (("h0", h0), ("dhT", dhT)):
         if st is not None:
-            _need(st, name, torch.float32, dev)
+            _shape(_need(st, name, torch.float32, dev), name, (N, H, dk, dv))
     f32 = dict(dtype=torch.float32, device=dev)
     res = {"dq": torch.empty(q.shape, **f32), "dk": torch.empty(q.shape, **f32),
            "dv": torch.empty(v.shape, **f32), "da": torch.empty(a.shape, **f32),
@@ -348,6 +368,8 @@ def _bwd(fn, q, k, v, g, beta, h0, dout, dhT, cu_seqlens, want_dh0, stream,
         _need(t, name, in_dtype, dev)
     _need(g, "g", torch.float32, dev)
     _need(beta, "beta", torch.float32, dev)
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q/k must be [B, T, H, dk] and v/dout [B, T, H, dv]")
     Bt, T, H, dk = q.shape
     dv = v.shape[-1]
     gshape = q.shape if per_channel else q.shape[:3]
@@ -392,6 +414,8 @@ def _kda(fn, q, k, v, g, beta, h0, cu_seqlens, out, hT, output_final_state,
     _need(v, "v", torch.bfloat16, dev)
     _need(g, "g", torch.float32, dev)
     _need(beta, "beta", torch.float32, dev)
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q/k/g must be [B, T, H, dk] and v [B, T, H, dv]")
     Bt, T, H, dk = q.shape
     dv = v.shape[-1]
     if k.shape != q.shape or v.shape[:3] != (Bt, T, H) or g.shape != q.shape:
@@ -413,7 +437,7 @@ def _kda(fn, q, k, v, g, beta, h0, cu_seqlens, out, hT, output_final_state,
     if out is None:
         out = torch.empty_like(v)
     else:
-        _need(out, "out", torch.bfloat16, dev)
+        _shape(_need(out, "out", torch.bfloat16, dev), "out", v.shape)
     if hT is None and output_final_state:
         hT = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
@@ -473,14 +497,20 @@ def gdn_recurrent_step(q, k, v, g, beta, state, *, out=None, stream=None):
     _need(g, "g", torch.float32, dev)
     _need(beta, "beta", torch.float32, dev)
     _need(state, "state", torch.float32, dev)
+    if q.dim() != 3 or v.dim() != 3:
+        raise ValueError("q/k must be [N, H, dk] and v [N, H, dv]")
     N, H, dk = q.shape
     dv = v.shape[-1]
+    _shape(k, "k", q.shape)
+    _shape(v, "v", (N, H, dv))
+    _shape(g, "g", (N, H))
+    _shape(beta, "beta", (N, H))
     if state.shape != (N, H, dk, dv):
         raise ValueError("state must be [N, H, dk, dv]")
     if out is None:
         out = torch.empty_like(v)
     else:
-        _need(out, "out", torch.bfloat16, dev)
+        _shape(_need(out, "out", torch.bfloat16, dev), "out", v.shape)
     with torch.cuda.device(dev):
         rc = library().gdn_recurrent_step(
             _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
