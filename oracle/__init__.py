@@ -26,6 +26,10 @@ Two parts:
   fp64; pinned in ``tests/test_oracle_backward_pins.py`` (finite differences
   through the forward oracles, closed forms, automatic differentiation of an
   independent PyTorch forward).
+* ``oracle.chunked_backward`` -- the same gradients chunk by chunk: the
+  adjoint of each step of the chunk form (the algebra a chunked backward
+  evaluates), pinned to ``oracle.backward`` at chunk sizes 1 to T in
+  ``tests/test_oracle_chunk_backward_pins.py``.
 
 Pins (all in ``tests/test_oracle_pins.py``): worked numbers of the illustrated
 DeltaNet page (delta-rule 1.5/2.25/2.625, the 2-D example, prediction/error,
