@@ -158,3 +158,17 @@ def test_kda_chunk_bench_size_sampled(lib, cuda_device):
                                    sl(d["g"]), sl(d["beta"]))
         assert rel_err(o[n:n + 1, :, h:h + 1], o_ref) <= TOL
         assert rel_err(hT[n:n + 1, h:h + 1], h_ref) <= TOL
+
+
+def test_kda_token_path_bench_size_sampled(lib, cuda_device):
+    """The same workload through the token-by-token kernel (path
+    GDN_PATH_SIMT, the bench's --kda-path serial line); two (sequence, head)
+    pairs against the oracle on their slices."""
+    d = inputs.kda_inputs(4, 16, 2048, 128, 128, seed=52, h0=False)
+    o, hT = run(lib, cuda_device, d, path=1)
+    for n, h in ((1, 4), (2, 15)):
+        sl = lambda x: x[n:n + 1, :, h:h + 1]
+        o_ref, h_ref = kda.forward(sl(d["q"]), sl(d["k"]), sl(d["v"]),
+                                   sl(d["g"]), sl(d["beta"]))
+        assert rel_err(o[n:n + 1, :, h:h + 1], o_ref) <= TOL
+        assert rel_err(hT[n:n + 1, h:h + 1], h_ref) <= TOL
