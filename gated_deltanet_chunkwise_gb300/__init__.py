@@ -13,6 +13,7 @@ _ABI_NAMES = (
     "gdn_chunk_fwd", "gdn_chunk_fwd_f32", "gdn_chunk_fwd_ex",
     "gdn_recurrent_step", "gdn_chunk_fwd_fused", "gdn_kda_fwd",
     "gdn_kda_fwd_ex", "gdn_kda_bwd", "gdn_chunk_bwd", "gdn_chunk_bwd_f32",
+    "gdn_chunk_bwd_chunked",
     "gdn_chunk_bwd_fused",
     "GDN_GATE_BEFORE_PREDICT", "GDN_GATE_AFTER_PREDICT",
     "gdn_status_string",
@@ -22,6 +23,7 @@ _ABI_NAMES = (
     "GDN_KERNEL_CHUNK_PREP", "GDN_KERNEL_CHUNK_CHAIN", "GDN_KERNEL_CHUNK_SIMT",
     "GDN_KERNEL_SP_CHAIN", "GDN_KERNEL_DECODE", "GDN_KERNEL_CHUNK_OFFSETS",
     "GDN_KERNEL_CHUNK_CHAIN_WHOLE", "GDN_KERNEL_KDA", "GDN_KERNEL_KDA_PREP", "GDN_KERNEL_BWD", "GDN_KERNEL_BWD_FINALIZE",
+    "GDN_KERNEL_CBWD_PREP", "GDN_KERNEL_CBWD_FWD", "GDN_KERNEL_CBWD_REV", "GDN_KERNEL_CBWD_GRAD",
     "GDN_KERNEL_COUNT",
     "KERNEL_NAMES",
     "GDN_PATH_AUTO", "GDN_PATH_SIMT", "GDN_PATH_TCGEN05",

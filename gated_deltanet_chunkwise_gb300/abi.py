@@ -41,7 +41,11 @@ GDN_KERNEL_KDA = 7
 GDN_KERNEL_KDA_PREP = 8
 GDN_KERNEL_BWD = 9
 GDN_KERNEL_BWD_FINALIZE = 10
-GDN_KERNEL_COUNT = 11
+GDN_KERNEL_CBWD_PREP = 11
+GDN_KERNEL_CBWD_FWD = 12
+GDN_KERNEL_CBWD_REV = 13
+GDN_KERNEL_CBWD_GRAD = 14
+GDN_KERNEL_COUNT = 15
 KERNEL_NAMES = {
     GDN_KERNEL_CHUNK_PREP: "ut_prep_kernel",
     GDN_KERNEL_CHUNK_CHAIN: "chunk_tc_kernel",
@@ -54,6 +58,10 @@ KERNEL_NAMES = {
     GDN_KERNEL_KDA_PREP: "kda_prep_kernel",
     GDN_KERNEL_BWD: "bwd_kernel",
     GDN_KERNEL_BWD_FINALIZE: "bwd_finalize_kernel",
+    GDN_KERNEL_CBWD_PREP: "cbwd_prep_kernel",
+    GDN_KERNEL_CBWD_FWD: "cbwd_fwd_kernel",
+    GDN_KERNEL_CBWD_REV: "cbwd_rev_kernel",
+    GDN_KERNEL_CBWD_GRAD: "cbwd_grad_kernel",
 }
 
 _lib = None
@@ -107,6 +115,8 @@ def library():
     lib.gdn_chunk_bwd.restype = i
     lib.gdn_chunk_bwd_f32.argtypes = bwd_args + [i, vp]
     lib.gdn_chunk_bwd_f32.restype = i
+    lib.gdn_chunk_bwd_chunked.argtypes = bwd_args + [vp]
+    lib.gdn_chunk_bwd_chunked.restype = i
     lib.gdn_chunk_bwd_fused.argtypes = [vp, vp, vp, fp, fp, fp, ip, fp, vp,
                                         ctypes.c_float, vp, fp, fp, fp, fp, fp,
                                         fp, fp, fp, fp, i, i, i, i, i, vp]
@@ -293,6 +303,16 @@ def gdn_chunk_bwd(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None, *,
     gate placement): as gdn_kda_bwd with g and dg [B, T, H]."""
     return _bwd("gdn_chunk_bwd", q, k, v, g, beta, h0, dout, dhT, cu_seqlens,
                 want_dh0, stream, per_channel=False, extra=(int(variant),))
+
+
+def gdn_chunk_bwd_chunked(q, k, v, g, beta, h0, dout, dhT=None, *,
+                          want_dh0=True, stream=None):
+    """gdn_chunk_bwd (decay before the prediction) through the chunk form:
+    per-chunk UT/WY quantities, the chunks' entry states and exit gradients by
+    two chains, then every chunk's gradients in parallel; dense batches only.
+    Returns the dict of gdn_chunk_bwd."""
+    return _bwd("gdn_chunk_bwd_chunked", q, k, v, g, beta, h0, dout, dhT,
+                None, want_dh0, stream, per_channel=False)
 
 
 def gdn_chunk_bwd_f32(q, k, v, g, beta, h0, dout, dhT=None, cu_seqlens=None,

@@ -1,0 +1,439 @@
+// Chunk-form backward of the scalar-gate recurrence (decay before the
+// prediction), fp32 arithmetic: the adjoint of the UT/WY chunk form (the
+// illustrated DeltaNet walk-through: UT transform, WY representation,
+// chunkwise state passing; its cost table and memory paragraphs and the
+// chunk form of "GPU parallelisation of Gated DeltaNet", m.lqnn.cn: keep the
+// state at chunk boundaries, recompute inside). Per chunk of L <= 64 tokens
+// with entry state S (d_v x d_k), G the chunk-local cumulative gate,
+// E = e^G, D_rs = e^{G_r - G_s}:
+//   A = strict_lower(diag(beta) K K^T (.) D),  T = (I + A)^{-1}
+//   W = T diag(beta E) K,  U0 = T diag(beta) V,  U = U0 - W S^T
+//   P = (Q K^T) (.) D (.) M_incl,  K_bar = diag(e^{G_L - G}) K
+//   O = diag(E) Q S^T + P U,  S' = e^{G_L} S + U^T K_bar
+// and, for the gradient dS' arriving at the exit state,
+//   dU = P^T dO + K_bar dS'^T,  dS = e^{G_L} dS' + dO^T diag(E) Q - dU^T W
+// (a reverse chain of the forward chain's shape) and, in parallel over
+// chunks, dQ, dK, dV, dbeta, dG from S, dS', U, dU, T, P (the terms are
+// written out in grad_body). Four bodies: prep (per chunk and head), the
+// forward chain and the reverse chain (per 32 value rows, head, sequence),
+// grad (per chunk and head). They are written over an execution context X
+// (x.tid, x.nt, x.smem, x.sync()) so that the kernels instantiate them with
+// one CUDA thread per tid; every loop bound is uniform across a CTA, so
+// every thread reaches every x.sync().
+#pragma once
+#include <cstring>
+#ifdef __CUDACC__
+#define GDN_HD __host__ __device__
+#else
+#define GDN_HD
+#include <cmath>
+#endif
+
+namespace gdn {
+namespace cbwd {
+
+constexpr int C = 64;
+
+// q, k, v, dout: bf16 (BF = true) or fp32 rows, read through ldin
+struct Args {
+  const void *q, *k, *v, *dout;
+  const float *g, *beta, *h0, *dhT;
+  int N, H, T, nch;  // nch = ceil(T / C)
+  // workspace per chunk-head z = (n * nch + c) * H + h
+  float *G, *Tm, *W, *U0, *P, *U, *S, *dSx, *dU;
+  // per-chunk-head scratch of the gradient body
+  float *dOS, *dKbar, *dW, *dKb, *dVb, *dP, *dT, *X, *dA, *KK, *dKs;
+  // outputs
+  float *dq, *dk, *dv, *dg, *dbeta, *dh0;
+};
+
+template <bool BF>
+GDN_HD inline float ldin(const void* p, size_t i) {
+  if (BF) {
+    const unsigned int w = (unsigned int)static_cast<const unsigned short*>(p)[i] << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return f;
+  }
+  return static_cast<const float*>(p)[i];
+}
+
+// C[M][N] via epi(i, j, sum_k A(i,k) B(k,j)), A(i,k) = A[i*ars + k*acs],
+// B(k,j) = B[k*brs + j*bcs]; each thread a 4 x 4 tile.
+template <class X, class F>
+GDN_HD void gemm(X& x, int M, int N, int K, const float* A, int ars, int acs,
+             const float* B, int brs, int bcs, F epi) {
+  const int nt_j = N / 4, ntiles = (M / 4) * nt_j;
+  for (int tile = x.tid; tile < ntiles; tile += x.nt) {
+    const int i0 = (tile / nt_j) * 4, j0 = (tile % nt_j) * 4;
+    float acc[4][4];
+    for (int i = 0; i < 4; ++i)
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int kk = 0; kk < K; ++kk) {
+      float a[4], b[4];
+      for (int i = 0; i < 4; ++i) a[i] = A[(i0 + i) * ars + kk * acs];
+      for (int j = 0; j < 4; ++j) b[j] = B[kk * brs + (j0 + j) * bcs];
+      for (int i = 0; i < 4; ++i)
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    for (int i = 0; i < 4; ++i)
+      for (int j = 0; j < 4; ++j) epi(i0 + i, j0 + j, acc[i][j]);
+  }
+}
+
+GDN_HD inline int chunk_len(const Args& a, int c) {
+  const int L = a.T - c * C;
+  return L < C ? L : C;
+}
+
+// ---- 1. per (chunk, head): G, T = (I + A)^{-1}, W, U0, P -----------------
+// smem floats: K, Q [C][DK], V [C][DV], A [C][C], T [C][C], G, beta [C]
+template <int DK, int DV>
+constexpr int prep_smem() { return 2 * C * DK + C * DV + 2 * C * C + 2 * C; }
+
+template <int DK, int DV, bool BF, class X>
+GDN_HD void prep_body(X& x, const Args& a, int z) {
+  const int h = z % a.H, nc = z / a.H, c = nc % a.nch, n = nc / a.nch;
+  const int L = chunk_len(a, c);
+  const long long t0 = (long long)n * a.T + (long long)c * C;
+  float* sK = x.smem;
+  float* sQ = sK + C * DK;
+  float* sV = sQ + C * DK;
+  float* sA = sV + C * DV;
+  float* sT = sA + C * C;
+  float* sG = sT + C * C;
+  float* sB = sG + C;
+  for (int i = x.tid; i < C * DK; i += x.nt) {
+    const int t = i / DK, cc = i % DK;
+    const bool in = t < L;
+    const size_t r = ((size_t)(t0 + t) * a.H + h) * DK + cc;
+    sK[i] = in ? ldin<BF>(a.k, r) : 0.f;
+    sQ[i] = in ? ldin<BF>(a.q, r) : 0.f;
+  }
+  for (int i = x.tid; i < C * DV; i += x.nt) {
+    const int t = i / DV, cc = i % DV;
+    sV[i] = t < L ? ldin<BF>(a.v, ((size_t)(t0 + t) * a.H + h) * DV + cc) : 0.f;
+  }
+  for (int t = x.tid; t < C; t += x.nt) {
+    sB[t] = t < L ? a.beta[(size_t)(t0 + t) * a.H + h] : 0.f;
+    sG[t] = t < L ? a.g[(size_t)(t0 + t) * a.H + h] : 0.f;
+  }
+  x.sync();
+  if (x.tid == 0)
+    for (int t = 1; t < C; ++t) sG[t] += sG[t - 1];  // padded g = 0
+  x.sync();
+  float* G = a.G + (size_t)z * C;
+  for (int t = x.tid; t < C; t += x.nt) G[t] = sG[t];
+  // A and P
+  float* P = a.P + (size_t)z * C * C;
+  gemm(x, C, C, DK, sK, DK, 1, sK, 1, DK, [&](int r, int s, float kk) {
+    sA[r * C + s] = r > s ? sB[r] * kk * expf(sG[r] - sG[s]) : 0.f;
+  });
+  gemm(x, C, C, DK, sQ, DK, 1, sK, 1, DK, [&](int r, int s, float qk) {
+    P[r * C + s] = r >= s ? qk * expf(sG[r] - sG[s]) : 0.f;
+  });
+  x.sync();
+  // T = (I + A)^{-1}, row by row (T is unit lower triangular)
+  for (int r = 0; r < C; ++r) {
+    for (int j = x.tid; j < C; j += x.nt) {
+      float t = r == j ? 1.f : 0.f;
+      for (int s = j; s < r; ++s) t = fmaf(-sA[r * C + s], sT[s * C + j], t);
+      sT[r * C + j] = j <= r ? t : 0.f;
+    }
+    x.sync();
+  }
+  float* Tg = a.Tm + (size_t)z * C * C;
+  for (int i = x.tid; i < C * C; i += x.nt) Tg[i] = sT[i];
+  // W = T diag(beta e^G) K, U0 = T diag(beta) V: scale the rows in place
+  x.sync();
+  for (int i = x.tid; i < C * DK; i += x.nt) {
+    const int t = i / DK;
+    sK[i] *= sB[t] * expf(sG[t]);
+  }
+  for (int i = x.tid; i < C * DV; i += x.nt) sV[i] *= sB[i / DV];
+  x.sync();
+  float* W = a.W + (size_t)z * C * DK;
+  float* U0 = a.U0 + (size_t)z * C * DV;
+  gemm(x, C, DK, C, sT, C, 1, sK, DK, 1, [&](int t, int cc, float s) { W[t * DK + cc] = s; });
+  gemm(x, C, DV, C, sT, C, 1, sV, DV, 1, [&](int t, int cc, float s) { U0[t * DV + cc] = s; });
+}
+
+// ---- 2. forward chain: entry state S and U of every chunk ----------------
+// one CTA per (RB value rows, head, sequence); smem: W, Kbar [C][DK],
+// U0 [C][RB], S [RB][DK], U [C][RB], Snew [RB][DK]
+template <int DK, int RB>
+constexpr int fwd_smem() { return 2 * C * DK + 2 * C * RB + 2 * RB * DK; }
+
+template <int DK, int DV, int RB, bool BF, class X>
+GDN_HD void fwd_body(X& x, const Args& a, int rb, int h, int n) {
+  float* sW = x.smem;
+  float* sKb = sW + C * DK;
+  float* sU0 = sKb + C * DK;
+  float* sS = sU0 + C * RB;
+  float* sU = sS + RB * DK;
+  float* sSn = sU + C * RB;
+  const int row0 = rb * RB;
+  for (int i = x.tid; i < RB * DK; i += x.nt) {
+    const int j = i / DK, cc = i % DK;
+    sS[i] = a.h0 ? a.h0[(((size_t)n * a.H + h) * DK + cc) * DV + row0 + j] : 0.f;
+  }
+  for (int c = 0; c < a.nch; ++c) {
+    const int z = (n * a.nch + c) * a.H + h, L = chunk_len(a, c);
+    const long long t0 = (long long)n * a.T + (long long)c * C;
+    const float* G = a.G + (size_t)z * C;
+    const float GL = G[L - 1];
+    x.sync();  // the previous chunk is done with the buffers
+    for (int i = x.tid; i < C * DK; i += x.nt) {
+      const int t = i / DK, cc = i % DK;
+      sW[i] = a.W[(size_t)z * C * DK + i];
+      sKb[i] = t < L ? expf(GL - G[t]) * ldin<BF>(a.k, ((size_t)(t0 + t) * a.H + h) * DK + cc) : 0.f;
+    }
+    for (int i = x.tid; i < C * RB; i += x.nt) {
+      const int t = i / RB, j = i % RB;
+      sU0[i] = a.U0[(size_t)z * C * DV + t * DV + row0 + j];
+    }
+    float* Sg = a.S + (size_t)z * DV * DK;
+    for (int i = x.tid; i < RB * DK; i += x.nt) Sg[(size_t)row0 * DK + i] = sS[i];
+    x.sync();
+    // U = U0 - W S^T (C x RB)
+    float* Ug = a.U + (size_t)z * C * DV;
+    gemm(x, C, RB, DK, sW, DK, 1, sS, 1, DK, [&](int t, int j, float ws) {
+      const float u = sU0[t * RB + j] - ws;
+      sU[t * RB + j] = u;
+      Ug[t * DV + row0 + j] = u;
+    });
+    x.sync();
+    // S <- gamma S + U^T Kbar (RB x DK)
+    const float gam = expf(GL);
+    gemm(x, RB, DK, C, sU, 1, RB, sKb, DK, 1, [&](int j, int cc, float s) {
+      sSn[j * DK + cc] = fmaf(gam, sS[j * DK + cc], s);
+    });
+    x.sync();
+    for (int i = x.tid; i < RB * DK; i += x.nt) sS[i] = sSn[i];
+  }
+}
+
+// ---- 3. reverse chain: exit gradient dS' and dU of every chunk -----------
+// smem: P [C][C], dO [C][RB], Kbar, Qg, W [C][DK], dS, dSn [RB][DK], dU [C][RB]
+template <int DK, int RB>
+constexpr int rev_smem() { return C * C + 2 * C * RB + 3 * C * DK + 2 * RB * DK; }
+
+template <int DK, int DV, int RB, bool BF, class X>
+GDN_HD void rev_body(X& x, const Args& a, int rb, int h, int n) {
+  float* sP = x.smem;
+  float* sO = sP + C * C;
+  float* sKb = sO + C * RB;
+  float* sQg = sKb + C * DK;
+  float* sW = sQg + C * DK;
+  float* sD = sW + C * DK;
+  float* sDn = sD + RB * DK;
+  float* sdU = sDn + RB * DK;
+  const int row0 = rb * RB;
+  for (int i = x.tid; i < RB * DK; i += x.nt) {
+    const int j = i / DK, cc = i % DK;
+    sD[i] = a.dhT ? a.dhT[(((size_t)n * a.H + h) * DK + cc) * DV + row0 + j] : 0.f;
+  }
+  for (int c = a.nch - 1; c >= 0; --c) {
+    const int z = (n * a.nch + c) * a.H + h, L = chunk_len(a, c);
+    const long long t0 = (long long)n * a.T + (long long)c * C;
+    const float* G = a.G + (size_t)z * C;
+    const float GL = G[L - 1];
+    x.sync();
+    for (int i = x.tid; i < C * C; i += x.nt) sP[i] = a.P[(size_t)z * C * C + i];
+    for (int i = x.tid; i < C * RB; i += x.nt) {
+      const int t = i / RB, j = i % RB;
+      sO[i] = t < L ? ldin<BF>(a.dout, ((size_t)(t0 + t) * a.H + h) * DV + row0 + j) : 0.f;
+    }
+    for (int i = x.tid; i < C * DK; i += x.nt) {
+      const int t = i / DK, cc = i % DK;
+      const bool in = t < L;
+      const size_t r = ((size_t)(t0 + t) * a.H + h) * DK + cc;
+      sKb[i] = in ? expf(GL - G[t]) * ldin<BF>(a.k, r) : 0.f;
+      sQg[i] = in ? expf(G[t]) * ldin<BF>(a.q, r) : 0.f;
+      sW[i] = a.W[(size_t)z * C * DK + i];
+    }
+    float* dSg = a.dSx + (size_t)z * DV * DK;
+    for (int i = x.tid; i < RB * DK; i += x.nt) dSg[(size_t)row0 * DK + i] = sD[i];
+    x.sync();
+    // dU = P^T dO + Kbar dS'^T (C x RB)
+    float* dUg = a.dU + (size_t)z * C * DV;
+    gemm(x, C, RB, DK, sKb, DK, 1, sD, 1, DK, [&](int t, int j, float s) {
+      sdU[t * RB + j] = s;
+    });
+    x.sync();
+    gemm(x, C, RB, C, sP, 1, C, sO, RB, 1, [&](int t, int j, float s) {
+      const float u = sdU[t * RB + j] + s;
+      sdU[t * RB + j] = u;
+      dUg[t * DV + row0 + j] = u;
+    });
+    x.sync();
+    // dS = gamma dS' + dO^T Qg - dU^T W (RB x DK)
+    const float gam = expf(GL);
+    gemm(x, RB, DK, C, sO, 1, RB, sQg, DK, 1, [&](int j, int cc, float s) {
+      sDn[j * DK + cc] = fmaf(gam, sD[j * DK + cc], s);
+    });
+    x.sync();
+    gemm(x, RB, DK, C, sdU, 1, RB, sW, DK, 1, [&](int j, int cc, float s) {
+      sDn[j * DK + cc] -= s;
+    });
+    x.sync();
+    for (int i = x.tid; i < RB * DK; i += x.nt) sD[i] = sDn[i];
+  }
+  x.sync();
+  if (a.dh0)
+    for (int i = x.tid; i < RB * DK; i += x.nt) {
+      const int j = i / DK, cc = i % DK;
+      a.dh0[(((size_t)n * a.H + h) * DK + cc) * DV + row0 + j] = sD[i];
+    }
+}
+
+// ---- 4. per (chunk, head): dq, dk, dv, dbeta, dg -------------------------
+// smem: K, Q [C][DK], V, dO [C][DV], G, beta, E, ebar, dG [C], red [nt + 1]
+template <int DK, int DV>
+constexpr int grad_smem(int nt) { return 2 * C * DK + 2 * C * DV + 5 * C + nt + 1; }
+
+template <int DK, int DV, bool BF, class X>
+GDN_HD void grad_body(X& x, const Args& a, int z) {
+  const int h = z % a.H, nc = z / a.H, c = nc % a.nch, n = nc / a.nch;
+  const int L = chunk_len(a, c);
+  const long long t0 = (long long)n * a.T + (long long)c * C;
+  float* sK = x.smem;
+  float* sQ = sK + C * DK;
+  float* sV = sQ + C * DK;
+  float* sO = sV + C * DV;
+  float* sG = sO + C * DV;
+  float* sB = sG + C;
+  float* sE = sB + C;
+  float* sEb = sE + C;
+  float* sdG = sEb + C;
+  float* red = sdG + C;
+  for (int i = x.tid; i < C * DK; i += x.nt) {
+    const int t = i / DK, cc = i % DK;
+    const bool in = t < L;
+    const size_t r = ((size_t)(t0 + t) * a.H + h) * DK + cc;
+    sK[i] = in ? ldin<BF>(a.k, r) : 0.f;
+    sQ[i] = in ? ldin<BF>(a.q, r) : 0.f;
+  }
+  for (int i = x.tid; i < C * DV; i += x.nt) {
+    const int t = i / DV, cc = i % DV;
+    const bool in = t < L;
+    const size_t r = ((size_t)(t0 + t) * a.H + h) * DV + cc;
+    sV[i] = in ? ldin<BF>(a.v, r) : 0.f;
+    sO[i] = in ? ldin<BF>(a.dout, r) : 0.f;
+  }
+  const float* G = a.G + (size_t)z * C;
+  const float GL = G[L - 1];
+  for (int t = x.tid; t < C; t += x.nt) {
+    sG[t] = G[t];
+    sB[t] = t < L ? a.beta[(size_t)(t0 + t) * a.H + h] : 0.f;
+    sE[t] = t < L ? expf(G[t]) : 0.f;
+    sEb[t] = t < L ? expf(GL - G[t]) : 0.f;
+  }
+  x.sync();
+  const size_t zCK = (size_t)z * C * DK, zCV = (size_t)z * C * DV, zCC = (size_t)z * C * C;
+  const float* S = a.S + (size_t)z * DV * DK;
+  const float* dSx = a.dSx + (size_t)z * DV * DK;
+  const float* U = a.U + zCV;
+  const float* dU = a.dU + zCV;
+  const float* Tm = a.Tm + zCC;
+  const float* P = a.P + zCC;
+  float *dOS = a.dOS + zCK, *dKbar = a.dKbar + zCK, *dW = a.dW + zCK;
+  float *dKb = a.dKb + zCK, *dKs = a.dKs + zCK, *dVb = a.dVb + zCV;
+  float *dP = a.dP + zCC, *dT = a.dT + zCC, *Xm = a.X + zCC, *dA = a.dA + zCC;
+  float* KK = a.KK + zCC;
+  // contractions over the value rows; K K^T
+  gemm(x, C, DK, DV, sO, DV, 1, S, DK, 1, [&](int t, int cc, float s) { dOS[t * DK + cc] = s; });
+  gemm(x, C, DK, DV, U, DV, 1, dSx, DK, 1, [&](int t, int cc, float s) { dKbar[t * DK + cc] = s; });
+  gemm(x, C, DK, DV, dU, DV, 1, S, DK, 1, [&](int t, int cc, float s) { dW[t * DK + cc] = -s; });
+  gemm(x, C, C, DV, sO, DV, 1, U, 1, DV, [&](int t, int s, float d) { dP[t * C + s] = t >= s ? d : 0.f; });
+  gemm(x, C, C, DK, sK, DK, 1, sK, 1, DK, [&](int r, int s, float d) { KK[r * C + s] = d; });
+  float part = 0.f;  // sum(dS' (.) S)
+  for (int i = x.tid; i < DV * DK; i += x.nt) part = fmaf(dSx[i], S[i], part);
+  red[x.tid] = part;
+  x.sync();
+  if (x.tid == 0) {
+    float sd = 0.f;
+    for (int i = 0; i < x.nt; ++i) sd += red[i];
+    red[x.nt] = sd;
+  }
+  // dKb = T^T dW, dVb = T^T dU
+  gemm(x, C, DK, C, Tm, 1, C, dW, DK, 1, [&](int t, int cc, float s) { dKb[t * DK + cc] = s; });
+  gemm(x, C, DV, C, Tm, 1, C, dU, DV, 1, [&](int t, int cc, float s) { dVb[t * DV + cc] = s; });
+  // dT = dW Kb^T + dU Vb^T, Kb = diag(beta E) K, Vb = diag(beta) V
+  gemm(x, C, C, DK, dW, DK, 1, sK, 1, DK, [&](int r, int s, float d) { dT[r * C + s] = d * sB[s] * sE[s]; });
+  x.sync();
+  gemm(x, C, C, DV, dU, DV, 1, sV, 1, DV, [&](int r, int s, float d) { dT[r * C + s] += d * sB[s]; });
+  x.sync();
+  // X = T^T dT; dA = strict_lower(-X T^T)
+  gemm(x, C, C, C, Tm, 1, C, dT, C, 1, [&](int r, int s, float d) { Xm[r * C + s] = d; });
+  x.sync();
+  gemm(x, C, C, C, Xm, C, 1, Tm, 1, C, [&](int r, int s, float d) { dA[r * C + s] = r > s ? -d : 0.f; });
+  x.sync();
+  // dbeta and dG, one thread per token t
+  for (int t = x.tid; t < C; t += x.nt) {
+    float kdkb = 0.f, vdvb = 0.f, qdos = 0.f, kdkbar = 0.f;
+    for (int cc = 0; cc < DK; ++cc) {
+      kdkb = fmaf(sK[t * DK + cc], dKb[t * DK + cc], kdkb);
+      qdos = fmaf(sQ[t * DK + cc], dOS[t * DK + cc], qdos);
+      kdkbar = fmaf(sK[t * DK + cc], dKbar[t * DK + cc], kdkbar);
+    }
+    for (int cc = 0; cc < DV; ++cc) vdvb = fmaf(sV[t * DV + cc], dVb[t * DV + cc], vdvb);
+    float db = sE[t] * kdkb + vdvb;
+    float dG = sB[t] * sE[t] * kdkb + sE[t] * qdos - sEb[t] * kdkbar;
+    for (int s = 0; s < C; ++s) {
+      const float kk = KK[t * C + s];
+      if (s < t) {
+        const float D = expf(sG[t] - sG[s]);
+        db = fmaf(dA[t * C + s] * D, kk, db);
+        dG = fmaf(dA[t * C + s], sB[t] * kk * D, dG);
+      }
+      if (s > t) dG -= dA[s * C + t] * sB[s] * kk * expf(sG[s] - sG[t]);
+      if (s <= t) dG = fmaf(dP[t * C + s], P[t * C + s], dG);
+      if (s >= t) dG -= dP[s * C + t] * P[s * C + t];
+    }
+    if (t < L) a.dbeta[(size_t)(t0 + t) * a.H + h] = db;
+    sdG[t] = dG;
+    red[t] = sEb[t] * kdkbar;  // the partials above were summed into red[nt]
+  }
+  x.sync();
+  if (x.tid == 0) {
+    float kb = 0.f;
+    for (int t = 0; t < L; ++t) kb += red[t];
+    sdG[L - 1] += kb + expf(GL) * red[x.nt];
+    float acc = 0.f;
+    for (int t = L - 1; t >= 0; --t) {
+      acc += sdG[t];
+      a.dg[(size_t)(t0 + t) * a.H + h] = acc;
+    }
+  }
+  // dP (.) D into X, B = diag(beta) (dA (.) D) into dT
+  for (int i = x.tid; i < C * C; i += x.nt) {
+    const int r = i / C, s = i % C;
+    const float D = r >= s ? expf(sG[r] - sG[s]) : 0.f;
+    Xm[i] = dP[i] * D;
+    dT[i] = sB[r] * dA[i] * D;
+  }
+  x.sync();
+  // dQ = diag(E) dOS + (dP (.) D) K
+  gemm(x, C, DK, C, Xm, C, 1, sK, DK, 1, [&](int t, int cc, float s) {
+    if (t < L) a.dq[((size_t)(t0 + t) * a.H + h) * DK + cc] = fmaf(sE[t], dOS[t * DK + cc], s);
+  });
+  // dK = (dP (.) D)^T Q + B K + B^T K + diag(ebar) dKbar + diag(beta E) dKb
+  gemm(x, C, DK, C, Xm, 1, C, sQ, DK, 1, [&](int s, int cc, float v) { dKs[s * DK + cc] = v; });
+  x.sync();
+  gemm(x, C, DK, C, dT, C, 1, sK, DK, 1, [&](int s, int cc, float v) { dKs[s * DK + cc] += v; });
+  x.sync();
+  gemm(x, C, DK, C, dT, 1, C, sK, DK, 1, [&](int s, int cc, float v) {
+    const float r = dKs[s * DK + cc] + v + sEb[s] * dKbar[s * DK + cc] +
+                    sB[s] * sE[s] * dKb[s * DK + cc];
+    if (s < L) a.dk[((size_t)(t0 + s) * a.H + h) * DK + cc] = r;
+  });
+  // dV = diag(beta) dVb
+  for (int i = x.tid; i < C * DV; i += x.nt) {
+    const int t = i / DV, cc = i % DV;
+    if (t < L) a.dv[((size_t)(t0 + t) * a.H + h) * DV + cc] = sB[t] * dVb[i];
+  }
+}
+
+}  // namespace cbwd
+}  // namespace gdn

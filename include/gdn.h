@@ -329,6 +329,27 @@ int gdn_chunk_bwd_fused(const void* q, const void* k, const void* v,
                         float* dgate, int B, int H, int T, int dk_dim,
                         int dv_dim, gdn_stream_t stream);
 
+/*
+ * gdn_chunk_bwd_chunked -- gdn_chunk_bwd (decay before the prediction) through
+ * the chunk form instead of the token-by-token reverse sweep (the
+ * walk-through's chunkwise form and memory paragraphs: the state is kept at
+ * chunk boundaries and everything inside a chunk is recomputed in parallel).
+ * Per chunk of 64 tokens: the UT/WY quantities, the chunks' entry states by a
+ * forward chain, their exit gradients by a reverse chain
+ *   dU = P^T dO + K_bar dS'^T,  dS = e^{G_L} dS' + dO^T diag(e^G) Q - dU^T W,
+ * then dq, dk, dv, dbeta, dg of every chunk in parallel (the adjoint of each
+ * step of the chunk form; all fp32). Arguments, layouts, outputs and error
+ * codes as gdn_chunk_bwd; cu_seqlens must be NULL (dense batches; otherwise
+ * GDN_ERR_UNSUPPORTED). Scratch: about 650 KB per 64-token chunk and head at
+ * d_k = d_v = 128 (cudaMallocAsync on `stream`).
+ */
+int gdn_chunk_bwd_chunked(const void* q, const void* k, const void* v,
+                          const float* g, const float* beta, const float* h0,
+                          const void* dout, const float* dhT, float* dq,
+                          float* dk, float* dv, float* dg, float* dbeta,
+                          float* dh0, const int32_t* cu_seqlens, int B, int H,
+                          int T, int dk_dim, int dv_dim, gdn_stream_t stream);
+
 /* gdn_chunk_bwd_f32 -- gdn_chunk_bwd for fp32 q, k, v and dout (the inputs
  * of gdn_chunk_fwd_f32 / gdn_chunk_fwd_ex with GDN_DTYPE_F32); everything
  * else, outputs included, as gdn_chunk_bwd. */
@@ -413,7 +434,11 @@ typedef enum {
   GDN_KERNEL_BWD = 9,           /* backward pass: checkpoints, recomputation
                                    and the reverse sweep */
   GDN_KERNEL_BWD_FINALIZE = 10, /* backward pass: sums over row blocks */
-  GDN_KERNEL_COUNT = 11
+  GDN_KERNEL_CBWD_PREP = 11,    /* chunk-form backward: per-chunk T, W, U0, P */
+  GDN_KERNEL_CBWD_FWD = 12,     /* chunk-form backward: entry states, U */
+  GDN_KERNEL_CBWD_REV = 13,     /* chunk-form backward: exit gradients, dU */
+  GDN_KERNEL_CBWD_GRAD = 14,    /* chunk-form backward: per-chunk gradients */
+  GDN_KERNEL_COUNT = 15
 } gdn_kernel_t;
 
 /* gdn_timing_enable -- per-kernel device timing on (nonzero) or off (0).

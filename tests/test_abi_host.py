@@ -240,14 +240,16 @@ def bwd(so, fn="gdn_chunk_bwd", **kw):
              dv=A + 0x8000, dg=A + 0x9000, db=A + 0xa000, dh0=None, cu=None,
              B=1, H=1, T=16, dk_=128, dv_=128)
     a.update(kw)
-    extra = (a.get("variant", 0),) if fn != "gdn_kda_bwd" else ()
+    extra = ((a.get("variant", 0),) if fn in ("gdn_chunk_bwd", "gdn_chunk_bwd_f32")
+             else ())
     return getattr(so, fn)(a["q"], a["k"], a["v"], a["g"], a["b"], a["h0"],
                            a["do"], a["dhT"], a["dq"], a["dk"], a["dv"],
                            a["dg"], a["db"], a["dh0"], a["cu"], a["B"], a["H"],
                            a["T"], a["dk_"], a["dv_"], *extra, None)
 
 
-@pytest.mark.parametrize("fn", ["gdn_chunk_bwd", "gdn_kda_bwd", "gdn_chunk_bwd_f32"])
+@pytest.mark.parametrize("fn", ["gdn_chunk_bwd", "gdn_kda_bwd", "gdn_chunk_bwd_f32",
+                                "gdn_chunk_bwd_chunked"])
 @pytest.mark.parametrize("kw,expect", [
     (dict(B=-1), INVALID), (dict(H=0), INVALID), (dict(T=-1), INVALID),
     (dict(q=None), INVALID), (dict(do=None), INVALID), (dict(dg=None), INVALID),
@@ -266,9 +268,14 @@ def test_chunk_bwd_rejects_unknown_gate_placement(lib, fn, variant):
     assert bwd(lib.library(), fn, variant=variant) == INVALID
 
 
-@pytest.mark.parametrize("fn", ["gdn_chunk_bwd", "gdn_kda_bwd", "gdn_chunk_bwd_f32"])
+@pytest.mark.parametrize("fn", ["gdn_chunk_bwd", "gdn_kda_bwd", "gdn_chunk_bwd_f32",
+                                "gdn_chunk_bwd_chunked"])
 def test_bwd_empty_batch_is_a_no_op(lib, fn):
     assert bwd(lib.library(), fn, B=0) == OK
+
+
+def test_chunked_bwd_takes_dense_batches_only(lib):
+    assert bwd(lib.library(), "gdn_chunk_bwd_chunked", cu=A + 0xb000) == UNSUPPORTED
 
 
 def bwd_fused(so, **kw):
