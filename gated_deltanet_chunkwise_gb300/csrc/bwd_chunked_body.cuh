@@ -62,7 +62,7 @@ GDN_HD inline float ldin(const void* p, size_t i) {
 // B(k,j) = B[k*brs + j*bcs]; each thread a 4 x 4 tile.
 template <class X, class F>
 GDN_HD void gemm(X& x, int M, int N, int K, const float* A, int ars, int acs,
-             const float* B, int brs, int bcs, F epi) {
+                 const float* B, int brs, int bcs, F epi) {
   const int nt_j = N / 4, ntiles = (M / 4) * nt_j;
   for (int tile = x.tid; tile < ntiles; tile += x.nt) {
     const int i0 = (tile / nt_j) * 4, j0 = (tile % nt_j) * 4;
