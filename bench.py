@@ -7,7 +7,7 @@ One step = one call of the whole forward path (every kernel the library
 launches for it). Prints ONE JSON line on rank 0.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload w1|w1f|w2|w3|w4|kda1|bwd1|bwd1k|bwd1f]
+                    [--workload w1|w1f|w2|w3|w4|kda1|bwd1|bwd1c|bwd1k|bwd1f]
 
 Timing: inputs resident in HBM, the L2 (129 MB) is flushed before every
 timed step by a 256 MiB memset followed by a read of another 256 MiB buffer
@@ -44,7 +44,7 @@ def _metric(w):
         return "GDN decode-step token-heads/s + % of GB300 HBM roofline, 1 GPU"
     if w["kind"] == "kda":
         return "KDA (per-channel decay) forward tokens/s + % of GB300 roofline, 1 GPU"
-    if w["kind"] in ("bwd", "bwdf"):
+    if w["kind"] in ("bwd", "bwdf", "bwdc"):
         return "GDN backward tokens/s + % of GB300 fp32 ALU peak, 1 GPU"
     if w["kind"] == "bwdk":
         return "KDA (per-channel decay) backward tokens/s + % of GB300 fp32 ALU peak, 1 GPU"
@@ -101,6 +101,10 @@ WORKLOADS = {
                  desc="gdn_chunk_bwd B=4 H=16 T=2048 dk=dv=128 bf16 inputs, "
                       "fp32 gradients of out (dout ~ N(0,1) bf16), h0=0, "
                       "no dhT"),
+    "bwd1c": dict(kind="bwdc", B=4, H=16, T=2048, dk=128, dv=128, h0=False,
+                  desc="gdn_chunk_bwd_chunked B=4 H=16 T=2048 dk=dv=128 bf16 "
+                       "inputs (chunk form of the backward), fp32 gradients of "
+                       "out (dout ~ N(0,1) bf16), h0=0, no dhT"),
     "bwd1k": dict(kind="bwdk", B=4, H=16, T=2048, dk=128, dv=128, h0=False,
                   desc="gdn_kda_bwd B=4 H=16 T=2048 dk=dv=128 bf16 inputs, "
                        "per-channel log-decays, fp32 gradients of out "
@@ -142,6 +146,7 @@ def _kernel_source_hash(kind):
     csrc = ROOT / "gated_deltanet_chunkwise_gb300" / "csrc"
     files = (["decode.cu"] if kind == "decode"
              else ["bwd.cu"] if kind in ("bwd", "bwdk")
+             else ["bwd_chunked.cu", "bwd_chunked_body.cuh"] if kind == "bwdc"
              else ["bwd.cu", "fused_bwd.cu"] if kind == "bwdf"
              else ["kda.cu", "kda_chunk.cu", "chunk_tc.cu"] if kind == "kda"
              else sorted(p.name for p in csrc.glob("chunk_*.cu")))
@@ -276,7 +281,7 @@ def _make_inputs(w, seed=0):
     if w["kind"] == "kda":
         return inputs.kda_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
                                  seed=seed, h0=w["h0"])
-    if w["kind"] == "bwd":
+    if w["kind"] in ("bwd", "bwdc"):
         d = inputs.chunk_inputs(w["B"], w["H"], w["T"], w["dk"], w["dv"],
                                 dtype="bf16", seed=seed, h0=w["h0"])
         d["dout"], _ = inputs.grad_inputs(d, seed=seed, dhT=False)
@@ -342,6 +347,11 @@ def run_ours(args, w, device, dist, rank, ws):
         def step():
             if w["kind"] == "bwd":
                 last["grads"] = gdn.gdn_chunk_bwd(
+                    d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"],
+                    d["dout"], None, want_dh0=False)
+                return
+            if w["kind"] == "bwdc":
+                last["grads"] = gdn.gdn_chunk_bwd_chunked(
                     d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"],
                     d["dout"], None, want_dh0=False)
                 return
@@ -443,7 +453,7 @@ def run_ours(args, w, device, dist, rank, ws):
               if v is not None)
     d2h = out_host.numel() * out_host.element_size()
     grads_host = {}
-    if w["kind"] in ("bwd", "bwdf", "bwdk"):
+    if w["kind"] in ("bwd", "bwdf", "bwdk", "bwdc"):
         # the step's results are the gradients (no out)
         grads_host = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
                       for n, t in last["grads"].items() if t is not None}
@@ -497,6 +507,32 @@ def run_ours(args, w, device, dist, rank, ws):
         value = units_all / (ms * 1e-3) * (tok_heads / tokens)  # heads/s
         unit = "token-heads/s"
         e2e_val = units_all / (e2e_ms * 1e-3) * (tok_heads / tokens)
+    elif w["kind"] == "bwdc":
+        # the chunk form's gradient kernel (fp32 CUDA cores): per chunk and
+        # head the products over the value rows (dO S, U dS', dU S: 3 C d_k
+        # d_v multiply-adds), the C x C products (dP, K K^T, T^T dW, T^T dU,
+        # dT, the dq and three dk products: C^2 (7 d_k + 3 d_v)) and
+        # dA = -T^T dT T^T (2 C^3)
+        C = 64
+        n_k, ms_k = kern.get("cbwd_grad_kernel", (0, 0.0))
+        k_ms = ms_k / steps if n_k else ms
+        chunk_heads = math.ceil(w["T"] / C) * w["B"] * w["H"]
+        flops = 2 * chunk_heads * (3 * C * dk * dv + C * C * (7 * dk + 3 * dv)
+                                   + 2 * C ** 3)
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        mhz = _sm_max_mhz()
+        alu_tflops = sms * 128 * 2 * mhz * 1e6 / 1e12
+        achieved = flops / (k_ms * 1e-3) / 1e12
+        roof = {"bound": "alu", "kernel": "cbwd_grad_kernel",
+                "achieved": round(achieved, 2), "peak": round(alu_tflops, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / alu_tflops, 4),
+                "peak_source": f"derived: {sms} SMs x 128 fp32 FMA/cycle x 2 "
+                               f"x {mhz:.0f} MHz (max SM clock)",
+                "algorithmic_flops_per_step": flops,
+                "launches_per_step": n_k / steps, "ms_per_step": k_ms}
+        value = units_all / (ms * 1e-3)
+        unit = "tokens/s"
+        e2e_val = units_all / (e2e_ms * 1e-3)
     elif w["kind"] in ("bwd", "bwdf", "bwdk"):
         # fp32 CUDA-core arithmetic per token-head: the forward states (decay
         # d_k d_v, prediction and update 2 d_k d_v each) and the adjoint
@@ -606,7 +642,7 @@ def run_ours(args, w, device, dist, rank, ws):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if ((w["kind"] == "kda" and args.kda_path == "serial")
-                           or w["kind"] in ("bwd", "bwdf", "bwdk")) else "bf16",
+                           or w["kind"] in ("bwd", "bwdf", "bwdk", "bwdc")) else "bf16",
         "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), "
                 + ("per-channel g=max(-softplus(N(0,1)),-5)"
                    if w["kind"] in ("kda", "bwdk") else "g=-softplus(N(0,1))")
@@ -694,7 +730,7 @@ def cpu_baseline(w, d_host, budget_s=20.0):
                 "sample": f"1 sequence x 1 of {w['H']} heads x {Tsub} tokens "
                           f"(reverse sweep, numpy), scaled to all heads",
                 "seconds": round(dt, 3)}
-    if w["kind"] == "bwd":
+    if w["kind"] in ("bwd", "bwdc"):
         from oracle import backward
         Tsub = 512
         sl = lambda x: x[:1, :Tsub, :1]
@@ -785,7 +821,7 @@ def run_reference(args, w):
                                   None, dout)
         units, unit, sample = T, "tokens/s", \
             f"one sequence of {T} tokens x all {w['H']} heads (reverse sweep)"
-    elif w["kind"] == "bwd":
+    elif w["kind"] in ("bwd", "bwdc"):
         from oracle import backward
         T = 256
         d = inputs.chunk_inputs(1, w["H"], T, w["dk"], w["dv"], dtype="bf16",
