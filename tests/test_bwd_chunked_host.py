@@ -33,7 +33,7 @@ def emu(tmp_path_factory):
     return exe
 
 
-def run_case(emu, tmp_path, N, H, T, DK, DV, h0, dhT, seed):
+def run_case(emu, tmp_path, N, H, T, DK, DV, h0, dhT, seed, bf16=False):
     rng = np.random.default_rng(seed)
     unit = lambda x: x / np.linalg.norm(x, axis=-1, keepdims=True)
     f32 = lambda x: np.ascontiguousarray(x, dtype=np.float32)
@@ -45,12 +45,25 @@ def run_case(emu, tmp_path, N, H, T, DK, DV, h0, dhT, seed):
     dout = f32(rng.standard_normal((N, T, H, DV)))
     H0 = f32(0.1 * rng.standard_normal((N, H, DK, DV))) if h0 else None
     DH = f32(0.1 * rng.standard_normal((N, H, DK, DV))) if dhT else None
-    for name, x in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta),
-                    ("dout", dout), ("h0", H0), ("dhT", DH)):
+    if bf16:
+        # round to bf16 (nearest even); the file holds the bit patterns and
+        # the oracle reads the rounded values
+        import torch
+        def to_bf16(x):
+            t = torch.from_numpy(x).to(torch.bfloat16)
+            return t.view(torch.int16).numpy().view(np.uint16), t.float().numpy()
+        (qb, q), (kb, k), (vb, v), (ob, dout) = map(to_bf16, (q, k, v, dout))
+        for name, x in (("q", qb), ("k", kb), ("v", vb), ("dout", ob)):
+            x.tofile(tmp_path / f"{name}.bin")
+    else:
+        for name, x in (("q", q), ("k", k), ("v", v), ("dout", dout)):
+            x.tofile(tmp_path / f"{name}.bin")
+    for name, x in (("g", g), ("beta", beta), ("h0", H0), ("dhT", DH)):
         if x is not None:
             x.tofile(tmp_path / f"{name}.bin")
     r = subprocess.run([str(emu), str(tmp_path), str(N), str(H), str(T),
-                        str(DK), str(DV), str(int(h0)), str(int(dhT))],
+                        str(DK), str(DV), str(int(h0)), str(int(dhT)),
+                        str(int(bf16))],
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     ref = backward.backward(q, k, v, g, beta, H0, dout, DH, variant=1)
@@ -73,3 +86,8 @@ def run_case(emu, tmp_path, N, H, T, DK, DV, h0, dhT, seed):
 ])
 def test_chunked_bwd_bodies_on_the_host(emu, tmp_path, N, H, T, DK, DV, h0, dhT):
     run_case(emu, tmp_path, N, H, T, DK, DV, h0, dhT, seed=T + DK + DV)
+
+
+def test_chunked_bwd_bodies_read_bf16_inputs(emu, tmp_path):
+    # the GPU entry point's input type: bf16 bit patterns widened in the loads
+    run_case(emu, tmp_path, 2, 2, 100, 128, 64, True, True, seed=7, bf16=True)
