@@ -897,6 +897,9 @@ def main(argv=None):
     ap.add_argument("--sequences", type=int, default=0,
                     help="override the number of sequences of the workload "
                          "(smaller cases for profiler captures)")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="headline run only: skip the decode-step record "
+                         "that the default workload carries as a second key")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     w = dict(WORKLOADS[args.workload])
@@ -919,9 +922,28 @@ def main(argv=None):
     torch.cuda.set_device(device)
     dist = _init_dist(ws, True)
     line, d_host = run_ours(args, w, device, dist, rank, ws)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, d_host)
+    del d_host
+    if args.workload == "w1" and args.sequences == 0 and not args.no_decode:
+        # The decode step (N=512, H=32, d=128, fp32 state) is the path's
+        # other measured kernel: its own timed region, roofline, clocks,
+        # end-to-end figure and CPU baseline, as a second record of the
+        # headline line (the metric, value and unit above stay the
+        # chunked forward's).
+        wd = dict(WORKLOADS["w4"])
+        dargs = argparse.Namespace(**vars(args))
+        dargs.workload = "w4"
+        dline, dd_host = run_ours(dargs, wd, device, dist, rank, ws)
+        if rank == 0:
+            rec = {k: dline[k] for k in ("metric", "value", "unit", "steps",
+                                         "ms_per_step", "config", "roofline",
+                                         "e2e", "gpu_launches", "clocks")}
+            if not args.no_cpu_baseline:
+                rec["cpu_baseline"] = cpu_baseline(wd, dd_host)
+            line["decode"] = rec
+        del dd_host
     if rank == 0:
-        if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(w, d_host)
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -15,6 +15,8 @@
 // entry a call reads is written earlier in the same call, so nothing needs
 // clearing. Calls whose work overlaps on the GPU (two streams, or two host
 // threads) race on the array: the caller must order them.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "gdn_internal.cuh"
@@ -26,23 +28,65 @@ static __device__ __align__(256) unsigned char
     g_noalloc_scratch[GDN_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
+// Per device: the array's address and the driver context it belongs to.
 void* g_scratch_addr[kMaxDevices];
+unsigned long long g_scratch_ctx[kMaxDevices];
 std::mutex g_scratch_mutex;
 
-// Device address of the array on the current device. In host code the
-// symbol itself is only a host-side stand-in, so the address is looked up
-// once per device (on that device's first call) and cached.
+// Unique id of the calling thread's current driver context (0 when there is
+// none yet), through driver entry points so that the library needs no link
+// against the driver library. A device reset, or another context made
+// current on the same device, gives a different id: the module holding the
+// array has been loaded again there and its address must be looked up anew.
+typedef CUresult (*ctx_current_fn)(CUcontext*);
+typedef CUresult (*ctx_id_fn)(CUcontext, unsigned long long*);
+ctx_current_fn g_ctx_current;
+ctx_id_fn g_ctx_id;
+std::once_flag g_ctx_once;
+
+bool current_context_id(unsigned long long* id) {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000,
+                                         cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<ctx_current_fn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000,
+                                         cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<ctx_id_fn>(fn);
+  });
+  if (!g_ctx_current || !g_ctx_id) return false;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return false;
+  *id = 0;
+  return ctx == nullptr || g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the array in the current device's current context. In
+// host code the symbol itself is only a host-side stand-in, so the address
+// is looked up with the device current (the first call on a device, and the
+// first call after its context changed) and cached.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return GDN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_addr[dev]) {
+  unsigned long long ctx = 0;
+  if (!current_context_id(&ctx)) return GDN_ERR_CUDA;
+  if (!g_scratch_addr[dev] || ctx == 0 || g_scratch_ctx[dev] != ctx) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess ||
         ptr == nullptr)
       return GDN_ERR_CUDA;
+    // the lookup made the runtime's context current if none was
+    if (!current_context_id(&ctx) || ctx == 0) return GDN_ERR_CUDA;
     g_scratch_addr[dev] = ptr;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_addr[dev];
   return GDN_OK;
@@ -54,9 +98,15 @@ int scratch_address(void** out) {
 extern "C" unsigned long long gdn_noalloc_scratch_bytes(int B, int H, int dk,
                                                         int dv,
                                                         int sp_parts) {
-  if (B <= 0 || H <= 0 || dk <= 0 || dv <= 0 || sp_parts < 2) return 0;
-  const unsigned long long nhp = (unsigned long long)B * H * sp_parts;
-  return nhp * (unsigned long long)(2 * dv + dk) * dk * sizeof(float);
+  // only the head dimensions the entry point serves (64, 128); all
+  // products in 64 bits
+  const bool dims_ok = (dk == 64 || dk == 128) && (dv == 64 || dv == 128);
+  if (B <= 0 || H <= 0 || !dims_ok || sp_parts < 2) return 0;
+  const unsigned long long nhp = (unsigned long long)B *
+                                 (unsigned long long)H *
+                                 (unsigned long long)sp_parts;
+  return nhp * (2ull * (unsigned long long)dv + (unsigned long long)dk) *
+         (unsigned long long)dk * sizeof(float);
 }
 
 extern "C" int gdn_chunk_fwd_sp_noalloc(

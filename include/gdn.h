@@ -374,7 +374,10 @@ int gdn_chunk_bwd_f32(const float* q, const float* k, const float* v,
  * cudaMalloc, cudaFree or other allocating routine.
  *   - Set-up: the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current and caches it; make
- *     that first call before any stream capture on that device.
+ *     that first call before any stream capture on that device. The cache
+ *     is keyed on the current driver context: after a device reset (or
+ *     with another context current on the device) the next call looks the
+ *     address up again, so that call too should precede any capture.
  *   - Size limit: the request needs gdn_noalloc_scratch_bytes(B, H, dk, dv,
  *     sp_parts) bytes; a request above GDN_NOALLOC_SCRATCH_BYTES returns
  *     GDN_ERR_UNSUPPORTED and enqueues nothing. sp_parts < 2 returns
@@ -395,7 +398,7 @@ int gdn_chunk_fwd_sp_noalloc(const void* q, const void* k, const void* v,
                              int sp_parts, gdn_stream_t stream);
 
 /* Scratch bytes gdn_chunk_fwd_sp_noalloc needs for these sizes (0 when
- * sp_parts < 2 or a size is not positive). */
+ * sp_parts < 2, B or H is not positive, or dk / dv is not 64 or 128). */
 unsigned long long gdn_noalloc_scratch_bytes(int B, int H, int dk, int dv,
                                              int sp_parts);
 
