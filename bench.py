@@ -583,11 +583,15 @@ def run_ours(args, w, device, dist, rank, ws):
         # roofline of the dominant kernel (the chain), from the library's own
         # CUDA events around each of its launches in the timed region
         # (whichever chain kernel the library chose for this shape)
-        chain_name = max(("chunk_tc_kernel", "chain_tx_kernel"),
+        chain_name = max(("chunk_tc_kernel", "chain_tx_kernel",
+                          "fused_chunk_kernel"),
                          key=lambda k: kern.get(k, (0, 0.0))[1])
         n_chain, ms_chain = kern.get(chain_name, (0, 0.0))
         chain_step_ms = ms_chain / steps if n_chain else ms
-        flops = chain_flops(tok_heads, dk, dv)
+        # the single-launch kernel does the whole path (preparation too)
+        flops = (chunk_flops(tok_heads, dk, dv)
+                 if chain_name == "fused_chunk_kernel"
+                 else chain_flops(tok_heads, dk, dv))
         achieved = flops / (chain_step_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": chain_name,
                 "achieved": round(achieved, 2),

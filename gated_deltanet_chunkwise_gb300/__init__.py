@@ -24,10 +24,12 @@ _ABI_NAMES = (
     "GDN_KERNEL_SP_CHAIN", "GDN_KERNEL_DECODE", "GDN_KERNEL_CHUNK_OFFSETS",
     "GDN_KERNEL_CHUNK_CHAIN_WHOLE", "GDN_KERNEL_KDA", "GDN_KERNEL_KDA_PREP", "GDN_KERNEL_BWD", "GDN_KERNEL_BWD_FINALIZE",
     "GDN_KERNEL_CBWD_PREP", "GDN_KERNEL_CBWD_FWD", "GDN_KERNEL_CBWD_REV", "GDN_KERNEL_CBWD_GRAD",
+    "GDN_KERNEL_CHUNK_FUSED",
     "GDN_KERNEL_COUNT",
     "KERNEL_NAMES",
     "GDN_PATH_AUTO", "GDN_PATH_SIMT", "GDN_PATH_TCGEN05",
-    "GDN_PATH_TCGEN05_SPLIT", "GDN_PATH_TCGEN05_WHOLE", "GDN_SP_CHAIN",
+    "GDN_PATH_TCGEN05_SPLIT", "GDN_PATH_TCGEN05_WHOLE",
+    "GDN_PATH_TCGEN05_FUSED", "GDN_SP_CHAIN",
     "GDN_SP_SCAN",
 )
 

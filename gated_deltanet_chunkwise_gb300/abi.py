@@ -27,6 +27,7 @@ GDN_PATH_SIMT = 1
 GDN_PATH_TCGEN05 = 2
 GDN_PATH_TCGEN05_SPLIT = 3
 GDN_PATH_TCGEN05_WHOLE = 4
+GDN_PATH_TCGEN05_FUSED = 5
 GDN_SP_CHAIN = 0x100
 GDN_SP_SCAN = 0x200
 # kernel families for per-kernel timing (gdn_kernel_t)
@@ -45,7 +46,8 @@ GDN_KERNEL_CBWD_PREP = 11
 GDN_KERNEL_CBWD_FWD = 12
 GDN_KERNEL_CBWD_REV = 13
 GDN_KERNEL_CBWD_GRAD = 14
-GDN_KERNEL_COUNT = 15
+GDN_KERNEL_CHUNK_FUSED = 15
+GDN_KERNEL_COUNT = 16
 KERNEL_NAMES = {
     GDN_KERNEL_CHUNK_PREP: "ut_prep_kernel",
     GDN_KERNEL_CHUNK_CHAIN: "chunk_tc_kernel",
@@ -62,6 +64,7 @@ KERNEL_NAMES = {
     GDN_KERNEL_CBWD_FWD: "cbwd_fwd_kernel",
     GDN_KERNEL_CBWD_REV: "cbwd_rev_kernel",
     GDN_KERNEL_CBWD_GRAD: "cbwd_grad_kernel",
+    GDN_KERNEL_CHUNK_FUSED: "fused_chunk_kernel",
 }
 
 _lib = None

@@ -59,14 +59,21 @@ __device__ __forceinline__ float sigmoid_f(float b) {
 }
 
 // Gate vectors of the chunk whose first token row (token * H + head) is
-// rbase; tokens at or past len get g = 0 and beta = 0. One whole warp. With
-// `logits` the inputs are a and b of log alpha = -softplus(a), beta =
-// sigmoid(b).
+// rbase; tokens at or past len get g = 0 and beta = 0. One whole warp, lane
+// l taking tokens l and l + 32. With `logits` the inputs are a and b of
+// log alpha = -softplus(a), beta = sigmoid(b). Computed into registers
+// (gate_lanes) and written out separately (put), so that a caller can form
+// them before the buffer is free.
+struct GateLanes {
+  float G[2], alpha[2], egpb[2], beta[2], eg[2], dec[2], ieg[2];
+  float gam, safe;
+};
+
 template <int VARIANT>
-__device__ __forceinline__ void gate_vectors(const float* g, const float* beta,
-                                             size_t rbase, int H, int len,
-                                             float* vec, bool logits,
-                                             int lane) {
+__device__ __forceinline__ GateLanes gate_lanes(const float* g,
+                                                const float* beta,
+                                                size_t rbase, int H, int len,
+                                                bool logits, int lane) {
   const unsigned fm = 0xffffffffu;
   float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
   if (lane < len) {
@@ -101,27 +108,44 @@ __device__ __forceinline__ void gate_vectors(const float* g, const float* beta,
   const float p1 = VARIANT == GDN_GATE_BEFORE_PREDICT ? s1 : s1 - g1;
   const bool in_range =
       __all_sync(fm, s0 >= -87.f && s0 <= 87.f && s1 >= -87.f && s1 <= 87.f);
-  vec[VEC_G + lane] = s0;
-  vec[VEC_G + 32 + lane] = s1;
-  vec[VEC_ALPHA + lane] = expf(g0);
-  vec[VEC_ALPHA + 32 + lane] = expf(g1);
-  vec[VEC_EGPB + lane] = expf(p0) * b0;
-  vec[VEC_EGPB + 32 + lane] = expf(p1) * b1;
-  vec[VEC_BETA + lane] = b0;
-  vec[VEC_BETA + 32 + lane] = b1;
-  const float e0 = expf(s0), e1 = expf(s1);
-  const float d0 = expf(Gl - s0), d1 = expf(Gl - s1);
-  const float gam = expf(Gl);
-  vec[VEC_EG + lane] = e0;
-  vec[VEC_EG + 32 + lane] = e1;
-  vec[VEC_DEC + lane] = d0;
-  vec[VEC_DEC + 32 + lane] = d1;
-  vec[VEC_IEG + lane] = expf(-s0);
-  vec[VEC_IEG + 32 + lane] = expf(-s1);
-  if (lane == 0) {
-    vec[VEC_GAMMA] = gam;
-    vec[VEC_SAFE] = in_range ? 1.f : 0.f;
+  GateLanes v;
+  v.G[0] = s0; v.G[1] = s1;
+  v.alpha[0] = expf(g0); v.alpha[1] = expf(g1);
+  v.egpb[0] = expf(p0) * b0; v.egpb[1] = expf(p1) * b1;
+  v.beta[0] = b0; v.beta[1] = b1;
+  v.eg[0] = expf(s0); v.eg[1] = expf(s1);
+  v.dec[0] = expf(Gl - s0); v.dec[1] = expf(Gl - s1);
+  v.ieg[0] = expf(-s0); v.ieg[1] = expf(-s1);
+  v.gam = expf(Gl);
+  v.safe = in_range ? 1.f : 0.f;
+  return v;
+}
+
+__device__ __forceinline__ void put_gate_lanes(const GateLanes& v, float* vec,
+                                               int lane) {
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    vec[VEC_G + 32 * k + lane] = v.G[k];
+    vec[VEC_ALPHA + 32 * k + lane] = v.alpha[k];
+    vec[VEC_EGPB + 32 * k + lane] = v.egpb[k];
+    vec[VEC_BETA + 32 * k + lane] = v.beta[k];
+    vec[VEC_EG + 32 * k + lane] = v.eg[k];
+    vec[VEC_DEC + 32 * k + lane] = v.dec[k];
+    vec[VEC_IEG + 32 * k + lane] = v.ieg[k];
   }
+  if (lane == 0) {
+    vec[VEC_GAMMA] = v.gam;
+    vec[VEC_SAFE] = v.safe;
+  }
+}
+
+template <int VARIANT>
+__device__ __forceinline__ void gate_vectors(const float* g, const float* beta,
+                                             size_t rbase, int H, int len,
+                                             float* vec, bool logits,
+                                             int lane) {
+  put_gate_lanes(gate_lanes<VARIANT>(g, beta, rbase, H, len, logits, lane),
+                 vec, lane);
 }
 
 
@@ -1197,6 +1221,18 @@ enum {
 };
 constexpr uint32_t TXO_MISC = TXO_BAR + TB_COUNT * 8;
 constexpr uint32_t TX_SMEM = TXO_MISC + 16 + 1024;
+// The fused kernel's chain CTA keeps P and the decay vectors in a ring of
+// three slots of their own (P tile | decay vectors), so that the
+// preparation CTA can deliver them a chunk earlier than the two-deep stage
+// allows; then full / empty barriers of the ring.
+constexpr uint32_t TXO_PC = ((TXO_MISC + 16 + 1023) / 1024) * 1024;
+constexpr uint32_t PC_SLOT = 9216, PC_CV = 8192;
+constexpr uint32_t TXO_PCBAR = TXO_PC + 3 * PC_SLOT;
+// READY barriers of the hand-off ring's four slots (the preparation CTA
+// arrives once a slot holds the chunk)
+constexpr uint32_t TXO_RDYBAR = TXO_PCBAR + 6 * 8;
+constexpr uint32_t TX_FUSED_SMEM = TXO_RDYBAR + 4 * 8 + 1024;
+static_assert(TX_FUSED_SMEM <= 232448, "shared memory budget");
 static_assert(TX_CV + KCV_BYTES <= TX_STAGE && TX_STAGE % 1024 == 0,
               "transposed stage layout");
 static_assert(TX_SMEM <= 232448, "shared memory budget");
@@ -1208,13 +1244,16 @@ constexpr uint32_t ID_TX_N128 = idesc_bf16(128, 128, false, false);
 constexpr uint32_t ID_TX_D = idesc_bf16(128, 128, false, true);
 constexpr uint32_t ID_TX_N64 = idesc_bf16(128, 64, false, false);
 
-__device__ __forceinline__ uint32_t tx_bar_count(int b) {
+__device__ __forceinline__ uint32_t tx_bar_count(int b, bool fused) {
   switch (b) {
     case TB_D1FREE0: case TB_D1FREE1: return kTxOutThreads / 32;
     // both issuers' commits (Delta^T reads K_d, P U reads P), one per chain
-    // warp (gamma, K_d) and one per output warp (e^G)
+    // warp (gamma, K_d) and one per output warp (e^G); in the fused kernel
+    // P and e^G live in a ring of their own, so K alone: the Delta^T
+    // issuer's commit and the chain warps
     case TB_EMPTYC0: case TB_EMPTYC1:
-      return 2 + (kTxChainThreads + kTxOutThreads) / 32;
+      return fused ? 1 + kTxChainThreads / 32
+                   : 2 + (kTxChainThreads + kTxOutThreads) / 32;
     case TB_SREADY: case TB_UREADY: return kTxChainThreads / 32;
     default: return 1;
   }
@@ -1254,16 +1293,449 @@ __device__ __forceinline__ void tx_scale_rows(uint8_t* tile, uint32_t blk,
   }
 }
 
-// KDA: per-channel decays (the Q_g / K_d images from the workspace, the
-// state decayed column by column); otherwise the scalar gate.
-template <bool KDA>
-__global__ void __launch_bounds__(kTxThreads, 1)
-    chain_tx_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tmq,
-                    const __grid_constant__ CUtensorMap tmk,
-                    const __grid_constant__ CUtensorMap tmv,
-                    const __grid_constant__ CUtensorMap tmo,
-                    const __grid_constant__ CUtensorMap tmg, int nch_dense,
-                    int tiles) {
+// ---------------------------------------------------------------------------
+// The preparation CTA of the fused kernel (fused_chunk_kernel below): the
+// state-independent part of every chunk of one (sequence, head), handed to
+// the chain CTA of its cluster through distributed shared memory instead of
+// a workspace in global memory. Three groups of four compute warps take the
+// chunks in turn (chunk i: group i % 3), each with a loader warp (gate
+// vectors, K and Q by TMA into the group's one stage). P is built over Q's
+// first 64-column block and T_U over the second once the [K;Q] K^T product
+// has read them. When a chunk is done its results (-W, P, T_U, the chain's
+// decay vectors) are gathered into outbox i % 2, so that the stage is free
+// for the group's next chunk at once; a copier warp stores the outboxes in
+// chunk order, by one bulk copy each, into slot i % 4 of the (sequence,
+// head)'s hand-off ring in global memory (small enough to stay in L2; a
+// copy between the two CTAs' shared memories measured at about 8 bytes per
+// cycle, too slow for 33 KB a chunk), then tells the chain CTA (READY
+// barrier i % 4 there), whose producer loads the slot into its stage with
+// the chunk's own tiles. A ring slot is refilled once the chain CTA reports
+// that the chunk four before has landed (LANDED barrier i % 4 here; the
+// chain warps arrive on it when they start on the chunk).
+constexpr int kFpGroups = 3;
+constexpr uint32_t FP_KQ = 0;        // K0 | Q0 | K1 | Q1 (8 KB each)
+constexpr uint32_t FP_AT = 32768;    // fp32 solve buffer, then [T_W; T_W]
+constexpr uint32_t FP_VEC = FP_AT + 64 * AP * 4;      // gate vectors
+constexpr uint32_t FP_CVS = FP_VEC + VEC_FLOATS * 4;  // the chain's decay
+                                                      // vectors, staged
+constexpr uint32_t FP_GROUP = 53248;                  // bytes per group
+// outboxes, each the image of a ring slot: -W (two 64-column blocks) | P |
+// T_U | decay vectors
+constexpr uint32_t FP_OB = kFpGroups * FP_GROUP;
+constexpr uint32_t OB_W = 0, OB_P = 16384, OB_TU = 24576, OB_CV = 32768;
+constexpr uint32_t FP_OB_BYTES = 33792;
+constexpr uint32_t RING_COPY = OB_CV + CV_BYTES;  // bytes stored per chunk
+constexpr int kRingSlots = 4;
+constexpr uint32_t FP_BAR = FP_OB + 2 * FP_OB_BYTES;
+enum {
+  FB_FULL = 0, FB_MMA = FB_FULL + kFpGroups, FB_MMAW = FB_MMA + kFpGroups,
+  FB_DRAIN = FB_MMAW + kFpGroups, FB_SFREE = FB_DRAIN + kFpGroups,
+  FB_OBREADY = FB_SFREE + kFpGroups, FB_STORED = FB_OBREADY + 2,
+  FB_LANDED = FB_STORED + 6, FB_N = FB_LANDED + kRingSlots
+};
+constexpr uint32_t FP_MISC = FP_BAR + FB_N * 8;
+constexpr uint32_t FP_SMEM = FP_MISC + 16 + 1024;
+static_assert(FP_CVS + CV_BYTES <= FP_GROUP && FP_AT % 1024 == 0 &&
+                  FP_GROUP % 1024 == 0 && FP_OB_BYTES % 1024 == 0 &&
+                  OB_CV + CV_BYTES <= FP_OB_BYTES,
+              "preparation CTA layout");
+static_assert(FP_SMEM <= 232448, "shared memory budget");
+static_assert(kFpGroups * 5 * 32 + 32 == 16 * 32,
+              "three groups of four compute warps and a loader, one copier");
+// the fused kernel's shared memory serves both roles
+constexpr uint32_t FUSED_SMEM =
+    FP_SMEM > TX_FUSED_SMEM ? FP_SMEM : TX_FUSED_SMEM;
+
+template <int VARIANT>
+__device__ __forceinline__ void prep_role(const ChunkParams& p,
+                                          const CUtensorMap& tmk,
+                                          const CUtensorMap& tmq, int n,
+                                          int h, uint32_t chain) {
+  const long long u_index = (long long)n * p.H + h;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + FP_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + FP_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + FP_MISC + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // warps 0-11: compute (group warp / 4); 12-14: the groups' loaders; 15:
+  // the outbox copier
+  constexpr int kWarpCopier = 4 * kFpGroups + kFpGroups;
+  const bool loader = warp >= 4 * kFpGroups && warp < kWarpCopier;
+  const int grp = warp < 4 * kFpGroups ? warp >> 2
+                                       : (loader ? warp - 4 * kFpGroups : 0);
+  const int H = p.H;
+  long long bos = 0, eos = 0;
+  if (!sequence_range(p, n, bos, eos)) bos = eos = 0;
+  const int nch = (int)((eos - bos + C - 1) / C);
+
+  if (tid == 0) {
+    for (int b = 0; b < FB_N; ++b) mbar_init(&bars[b], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (loader && lane == 0) {
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmq);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // both CTAs' barriers are initialised before either side uses the other's
+  cluster_sync();
+  const uint32_t tmem = *tmem_slot + 128u * grp;
+  uint8_t* gs = sm + grp * FP_GROUP;
+  const uint32_t gsb = base + grp * FP_GROUP;
+  float* vec = reinterpret_cast<float*>(gs + FP_VEC);
+  uint64_t* full = &bars[FB_FULL + grp];
+  const int bid = 1 + grp;  // the group's named barrier
+
+  if (warp == kWarpCopier) {
+    // ============ copier: outbox i % 2 into ring slot i % 4 ============
+    if (lane == 0) {
+      uint8_t* ring = static_cast<uint8_t*>(p.ring) +
+                      (size_t)u_index * kRingSlots * FP_OB_BYTES;
+      for (int i = 0; i < nch; ++i) {
+        const int s = i & 1;
+        // the outbox is filled; the slot's previous chunk (i - 4) has
+        // landed in the chain CTA
+        if (!mbar_wait(&bars[FB_OBREADY + s], (i >> 1) & 1, abort_flag) ||
+            (i >= kRingSlots &&
+             !mbar_spin_remote(&bars[FB_LANDED + i % kRingSlots],
+                               ((i / kRingSlots) - 1) & 1, abort_flag)))
+          break;
+        bulk_store(ring + (size_t)(i % kRingSlots) * FP_OB_BYTES,
+                   sm + FP_OB + s * FP_OB_BYTES, RING_COPY);
+        bulk_commit();
+        bulk_wait_read();
+        // outbox s may take chunk i + 2 (STORED barrier i % 6: its waiter,
+        // the group of chunk i + 2, waits every phase of it in order)
+        mbar_arrive(&bars[FB_STORED + i % 6]);
+        bulk_wait_all();
+        // the slot's bytes are in global memory: tell the chain CTA
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        mbar_arrive_cluster(
+            map_to_cta(sm + TXO_RDYBAR + 8 * (i % kRingSlots), chain));
+      }
+    }
+  } else if (loader) {
+    // ============ loader: gate vectors, K and Q by TMA ============
+    int li = 0;
+    bool ok = true;
+    for (int i = grp; i < nch; i += kFpGroups, ++li) {
+      const long long t0 = bos + (long long)i * C;
+      const int len = (int)min((long long)C, eos - t0);
+      // the gate vectors are formed while the group still works on its
+      // previous chunk; they and the stage are written once the compute
+      // warps have finished it
+      const GateLanes gl = gate_lanes<VARIANT>(p.g, p.beta, (size_t)t0 * H + h,
+                                               H, len, p.prologue != 0, lane);
+      if (lane == 0 && li >= 1)
+        ok = mbar_wait(&bars[FB_SFREE + grp], (li - 1) & 1, abort_flag);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      put_gate_lanes(gl, vec, lane);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full, 32768);
+        tma_load_3d(gs + FP_KQ, &tmk, full, 0, h, (int)t0);
+        tma_load_3d(gs + FP_KQ + 8192, &tmq, full, 0, h, (int)t0);
+        tma_load_3d(gs + FP_KQ + 16384, &tmk, full, 64, h, (int)t0);
+        tma_load_3d(gs + FP_KQ + 24576, &tmq, full, 64, h, (int)t0);
+        if (i + kFpGroups < nch) {
+          const int t2 = (int)(t0 + kFpGroups * C);
+          prefetch_l2_3d(&tmk, 0, h, t2);
+          prefetch_l2_3d(&tmk, 64, h, t2);
+          prefetch_l2_3d(&tmq, 0, h, t2);
+          prefetch_l2_3d(&tmq, 64, h, t2);
+        }
+      }
+    }
+    // never leave with a TMA copy still landing in shared memory
+    if (lane == 0 && li > 0) wait_ignoring_abort(full, (li - 1) & 1);
+  } else if (warp < 4 * kFpGroups) {
+    // ================= compute warps of the group =================
+    // A warp reaches the TMEM lanes of its quarter warp % 4 only; the four
+    // compute warps of a group cover the four quarters: thread ct owns row
+    // ct of the group's 128-lane accumulator.
+    const int q = warp & 3;
+    const int ct = 32 * q + lane;  // 0..127
+    float* AT = reinterpret_cast<float*>(gs + FP_AT);
+    uint8_t* st = gs + FP_KQ;
+    const uint32_t stb = gsb + FP_KQ;
+    int li = 0;
+    for (int i = grp; i < nch; i += kFpGroups, ++li) {
+      bool ok = mbar_wait(full, li & 1, abort_flag);
+      if (!bar_and(bid, 128, ok)) break;
+      if (ct == 0) {
+        // [K;Q] K^T: rows 0-63 K K^T, rows 64-127 Q K^T
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t a = sdesc(stb + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+          mma_bf16(tmem, a, a, ID_PREP, k > 0);
+        }
+        mma_commit(&bars[FB_MMA + grp]);
+      }
+      {
+        // inverse lengths of raw k / q rows (prologue), folded into the
+        // factors the rows and columns are scaled with (as in
+        // ut_prep_kernel)
+        const int r = ct & 63;
+        float inv = 1.f;
+        if (p.prologue) {
+          const uint8_t* tl = st + (ct < 64 ? 0 : 8192);
+          float ss = 0.f;
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              float f[8];
+              unpack_bf16x8(*reinterpret_cast<const uint4*>(tl + cb * 16384 + sw128(r, c)), f);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+            }
+          }
+          inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+        }
+        vec[(ct < 64 ? VEC_SK : VEC_SQ) + r] = inv;
+        if (p.prologue) {
+          if (ct < 64) {
+            vec[VEC_EGPB + r] *= inv;
+            vec[VEC_IEG + r] *= inv;
+            vec[VEC_DEC + r] *= inv;
+          } else {
+            vec[VEC_EG + r] *= inv;
+          }
+        }
+        named_bar(bid, 128);
+        // the chain's decay vectors (after the fold), staged for the outbox
+        float* cv = reinterpret_cast<float*>(gs + FP_CVS);
+        if (ct < 64) {
+          cv[CV_EG + ct] = vec[VEC_EG + ct];
+          cv[CV_DEC + ct] = vec[VEC_DEC + ct];
+        } else if (ct < 68) {
+          cv[CV_GAMMA + ct - 64] = ct == 64 ? vec[VEC_GAMMA] : 0.f;
+        }
+      }
+      ok = mbar_wait(&bars[FB_MMA + grp], li & 1, abort_flag);
+      if (!bar_and(bid, 128, ok)) break;
+      tc_fence_after();
+      const uint32_t lanes = (uint32_t)(32 * q) << 16;
+      if (ct < 64) {
+        // row r of A (as in ut_prep_kernel)
+        const int r = ct;
+        const bool safe = vec[VEC_SAFE] != 0.f;
+        const float er = vec[VEC_EGPB + r];
+        const float br = vec[VEC_BETA + r] * vec[VEC_SK + r];
+        const float* alpha = vec + VEC_ALPHA;
+        const float* sk = vec + VEC_SK;
+        float d = 1.f;
+#pragma unroll
+        for (int hf = 1; hf >= 0; --hf) {
+          float x[32];
+          tmem_ld32(tmem + lanes + 32 * hf, x);
+          tmem_ld_wait();
+          if (safe) {
+            const float4* w4 = reinterpret_cast<const float4*>(vec + VEC_IEG + 32 * hf);
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 w = w4[c4];
+              const int j = 32 * hf + 4 * c4;
+              x[4 * c4] = j < r ? er * w.x * x[4 * c4] : 0.f;
+              x[4 * c4 + 1] = j + 1 < r ? er * w.y * x[4 * c4 + 1] : 0.f;
+              x[4 * c4 + 2] = j + 2 < r ? er * w.z * x[4 * c4 + 2] : 0.f;
+              x[4 * c4 + 3] = j + 3 < r ? er * w.w * x[4 * c4 + 3] : 0.f;
+            }
+          } else {
+#pragma unroll
+            for (int e = 31; e >= 0; --e) {
+              const int jj = 32 * hf + e;
+              float a = 0.f;
+              if (jj < r) {
+                if (VARIANT == GDN_GATE_BEFORE_PREDICT) {
+                  d *= alpha[jj + 1];
+                  a = br * d * sk[jj] * x[e];
+                } else {
+                  a = br * d * sk[jj] * x[e];
+                  d *= alpha[jj];
+                }
+              }
+              x[e] = a;
+            }
+          }
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4)
+            *reinterpret_cast<float4*>(AT + r * AP + 32 * hf + 4 * c4) =
+                make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
+        }
+      } else {
+        // row r of P, over Q's first block (read by the K K^T product only)
+        const int r = ct - 64;
+        const bool safe = vec[VEC_SAFE] != 0.f;
+        const float er = vec[VEC_EG + r];
+        const float* alpha = vec + VEC_ALPHA;
+        uint8_t* ptile = st + 8192;
+        float d = 1.f;
+#pragma unroll
+        for (int hf = 1; hf >= 0; --hf) {
+          float x[32];
+          tmem_ld32(tmem + lanes + 32 * hf, x);
+          tmem_ld_wait();
+          if (safe) {
+            const float4* w4 = reinterpret_cast<const float4*>(vec + VEC_IEG + 32 * hf);
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 w = w4[c4];
+              const int j = 32 * hf + 4 * c4;
+              x[4 * c4] = j <= r ? w.x * x[4 * c4] : 0.f;
+              x[4 * c4 + 1] = j + 1 <= r ? w.y * x[4 * c4 + 1] : 0.f;
+              x[4 * c4 + 2] = j + 2 <= r ? w.z * x[4 * c4 + 2] : 0.f;
+              x[4 * c4 + 3] = j + 3 <= r ? w.w * x[4 * c4 + 3] : 0.f;
+            }
+            store_half_bf16_scaled(ptile, r, hf, x, er);
+          } else {
+            const float* sk = vec + VEC_SK;
+#pragma unroll
+            for (int e = 31; e >= 0; --e) {
+              const int jj = 32 * hf + e;
+              float pv = 0.f;
+              if (jj <= r) {
+                pv = d * sk[jj] * x[e];
+                d *= alpha[jj];
+              }
+              x[e] = pv;
+            }
+            store_half_bf16_scaled(ptile, r, hf, x, vec[VEC_SQ + r]);
+          }
+        }
+      }
+      tc_fence_before();
+      named_bar(bid, 128);
+      solve_unit_lower(AT, ct, bid);
+      {
+        // T_W rows into [T_W; T_W] over the solve buffer, T_U rows over Q's
+        // second block (thread (r, hh): columns 32 hh .. 32 hh + 31)
+        const int r = ct & 63, hh = ct >> 6;
+        float t[32];
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 v = *reinterpret_cast<const float4*>(AT + r * AP + 32 * hh + 4 * c4);
+          t[4 * c4] = v.x; t[4 * c4 + 1] = v.y; t[4 * c4 + 2] = v.z; t[4 * c4 + 3] = v.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = 32 * hh + e;
+          t[e] = col < r ? t[e] : (col == r ? 1.f : 0.f);
+        }
+        named_bar(bid, 128);  // T fully read before the tile overwrites it
+        float tw[32], tu[32];
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 w4 = *reinterpret_cast<const float4*>(vec + VEC_EGPB + 32 * hh + 4 * c4);
+          const float4 u4 = *reinterpret_cast<const float4*>(vec + VEC_BETA + 32 * hh + 4 * c4);
+          tw[4 * c4] = t[4 * c4] * w4.x; tw[4 * c4 + 1] = t[4 * c4 + 1] * w4.y;
+          tw[4 * c4 + 2] = t[4 * c4 + 2] * w4.z; tw[4 * c4 + 3] = t[4 * c4 + 3] * w4.w;
+          tu[4 * c4] = t[4 * c4] * u4.x; tu[4 * c4 + 1] = t[4 * c4 + 1] * u4.y;
+          tu[4 * c4 + 2] = t[4 * c4 + 2] * u4.z; tu[4 * c4 + 3] = t[4 * c4 + 3] * u4.w;
+        }
+        uint8_t* tile_tw = gs + FP_AT;
+        store_half_bf16(tile_tw, r, hh, tw);
+        store_half_bf16(tile_tw, 64 + r, hh, tw);
+        store_half_bf16(st + 24576, r, hh, tu);
+        fence_proxy_async();
+      }
+      named_bar(bid, 128);
+      if (ct == 0) {
+        // [T_W; T_W] K: both halves of the accumulator hold W
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_bf16(tmem, sdesc(gsb + FP_AT + k * 32, 16, 1024),
+                   sdesc(stb + k * 2048, 16384, 1024), ID_PREP_W, k > 0);
+        mma_commit(&bars[FB_MMAW + grp]);
+      }
+      // Outbox i % 2 is free once the copier has stored chunk i - 2 from it
+      // (STORED barrier (i - 2) % 6, whose phases this group alone waits, in
+      // order; a barrier per outbox would be waited by the groups in turn,
+      // and a group running ahead could take a phase two back for its own).
+      ok = mbar_wait(&bars[FB_MMAW + grp], li & 1, abort_flag) &&
+           (ct != 0 || i < 2 ||
+            mbar_wait(&bars[FB_STORED + (i - 2) % 6], ((i - 2) / 6) & 1,
+                      abort_flag));
+      if (!bar_and(bid, 128, ok)) break;
+      tc_fence_after();
+      {
+        uint8_t* ob = sm + FP_OB + (i & 1) * FP_OB_BYTES;
+        // -W: warps of lane quarters 0-1 columns 0-63, 2-3 columns 64-127
+        // (the copy of W in lanes 64-127)
+        const int r = ct & 63, cb = q >> 1;
+        uint8_t* wtile = ob + OB_W + cb * TILE_BYTES;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float x[32];
+          tmem_ld32(tmem + lanes + 64 * cb + 32 * hf, x);
+          tmem_ld_wait();
+          store_half_bf16_scaled(wtile, r, hf, x, -1.f);
+        }
+        // P, T_U and the decay vectors: byte images, 16 bytes a piece
+        uint4 pv[4], uv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          pv[e] = reinterpret_cast<const uint4*>(st + 8192)[ct + 128 * e];
+          uv[e] = reinterpret_cast<const uint4*>(st + 24576)[ct + 128 * e];
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          reinterpret_cast<uint4*>(ob + OB_P)[ct + 128 * e] = pv[e];
+          reinterpret_cast<uint4*>(ob + OB_TU)[ct + 128 * e] = uv[e];
+        }
+        if (ct < (int)(CV_BYTES / 16))
+          reinterpret_cast<uint4*>(ob + OB_CV)[ct] =
+              reinterpret_cast<const uint4*>(gs + FP_CVS)[ct];
+        fence_proxy_async();  // the bulk copies read the outbox
+      }
+      tc_fence_before();
+      named_bar(bid, 128);
+      if (ct == 0) {
+        mbar_arrive(&bars[FB_SFREE + grp]);        // the stage may load again
+        mbar_arrive(&bars[FB_OBREADY + (i & 1)]);  // the outbox may be copied
+      }
+    }
+    if (ct == 0) {
+      mma_commit(&bars[FB_DRAIN + grp]);
+      wait_ignoring_abort(&bars[FB_DRAIN + grp], 0);
+    }
+  }
+  // Neither CTA leaves while the other may still write into it: every copy
+  // from this CTA into the chain CTA has landed once the chain CTA arrives
+  // here (it consumed every chunk, or gave up after its bounded waits), and
+  // the chain CTA's remote arrivals were issued before it arrives.
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(*tmem_slot, 512);
+  }
+  if (tid == 0 && *abort_flag) record_status(p.status, GDN_ERR_TIMEOUT);
+}
+
+// The whole-state chain. KDA: per-channel decays (the Q_g / K_d images from
+// the workspace, the state decayed column by column); otherwise the scalar
+// gate. FUSED: the chain CTA of fused_chunk_kernel, fed by the preparation
+// CTA of its cluster (rank 0) instead of the workspace; `xblock` is the
+// 128-row block (blockIdx.x of chain_tx_kernel, 0 in the fused kernel).
+template <bool KDA, bool FUSED>
+__device__ __forceinline__ void chain_tx_body(
+    const ChunkParams& p, const CUtensorMap& tmq, const CUtensorMap& tmk,
+    const CUtensorMap& tmv, const CUtensorMap& tmo, const CUtensorMap& tmg,
+    int nch_dense, int tiles, int xblock, int h, int zblock, uint32_t prep) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1274,10 +1746,9 @@ __global__ void __launch_bounds__(kTxThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = p.H, dv = p.dv;
-  const int h = blockIdx.y;
-  const int n = blockIdx.z / p.part_count;
-  const int part = p.part_begin + blockIdx.z % p.part_count;
-  const int row0 = blockIdx.x * TXR;
+  const int n = zblock / p.part_count;
+  const int part = p.part_begin + zblock % p.part_count;
+  const int row0 = xblock * TXR;
   const bool value_rows = row0 < dv;
   const bool split_tail = (p.mode == kModeSplit) && part > 0;
   if (!value_rows && !(split_tail && row0 < dv + DK)) return;
@@ -1285,8 +1756,10 @@ __global__ void __launch_bounds__(kTxThreads, 1)
   const bool emit = value_rows && ((p.mode == kModeOutput) || part == 0);
   const bool epi = p.epilogue && emit;
   const bool has_gate = epi && p.gate_z != nullptr;
-  long long bos, eos;
-  if (!sequence_range(p, n, bos, eos)) return;
+  long long bos = 0, eos = 0;
+  // (the fused kernel's chain CTA carries on with no chunks: it meets its
+  // preparation CTA at the cluster barriers)
+  if (!sequence_range(p, n, bos, eos) && !FUSED) return;
   const int nch = (int)((eos - bos + C - 1) / C);
   int c_begin, c_end;
   part_range(nch, p.parts, part, c_begin, c_end);
@@ -1294,8 +1767,19 @@ __global__ void __launch_bounds__(kTxThreads, 1)
   const size_t nh = (size_t)n * H + h;
 
   // ---- set-up ----
+  // fused: P and decay-vector ring (full: the producer's arm; empty: the
+  // side issuer's P U commit, the chain warps and the output warps)
+  uint64_t* pcbars = reinterpret_cast<uint64_t*>(sm + TXO_PCBAR);
   if (tid == 0) {
-    for (int b = 0; b < TB_COUNT; ++b) mbar_init(&bars[b], tx_bar_count(b));
+    for (int b = 0; b < TB_COUNT; ++b)
+      mbar_init(&bars[b], tx_bar_count(b, FUSED));
+    if (FUSED) {
+      for (int r = 0; r < 3; ++r) {
+        mbar_init(&pcbars[r], 1);
+        mbar_init(&pcbars[3 + r], 1 + (kTxChainThreads + kTxOutThreads) / 32);
+      }
+      for (int r = 0; r < 4; ++r) mbar_init(&pcbars[6 + r], 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1323,13 +1807,90 @@ __global__ void __launch_bounds__(kTxThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // fused: both CTAs' barriers initialised before either side uses the
+  // other's
+  if (FUSED) cluster_sync();
   const uint32_t tmem = *tmem_slot;
   auto stage = [&](int i) { return base + (i & 1) * TX_STAGE; };
   // set-up above overlaps the tail of the preceding kernel
   griddep_wait();
-  const int cbase = nloc > 0 ? chunk_base(p, n, nch_dense) + c_begin : 0;
+  const int cbase = (nloc > 0 && !FUSED) ? chunk_base(p, n, nch_dense) + c_begin : 0;
 
-  if (warp == kTxWarpProducer) {
+  if (FUSED && warp == kTxWarpProducer) {
+    // ================= producer of the fused kernel =================
+    // Q, K, V by tensor map; -W, P, T_U and the decay vectors are stored
+    // into the stage by the preparation CTA (rank `prep`). Each group's
+    // barrier is armed for all of its bytes, then the preparation CTA is
+    // told (SLOT barrier i % 6) that stage i % 2 may take chunk i.
+    if (lane == 0) {
+      auto prefetch_v = [&](int i) {
+        const int tok = (int)(bos + (long long)(c_begin + i) * C);
+        prefetch_l2_3d(&tmv, 0, h, tok);
+        if (dv > 64) prefetch_l2_3d(&tmv, 64, h, tok);
+      };
+      if (nloc > 0) prefetch_v(0);
+      if (nloc > 1) prefetch_v(1);
+      int armed = 0;  // chunks whose places are all armed
+      const uint8_t* ring = static_cast<const uint8_t*>(p.ring) +
+                            ((size_t)n * H + h) * kRingSlots * FP_OB_BYTES;
+      uint64_t* ready = pcbars + 6;
+      for (int i = 0; i < nloc; ++i) {
+        const int s = i & 1, r = i % 3;
+        const uint32_t ph = ((i >> 1) - 1) & 1;  // release of chunk i - 2
+        const int tok = (int)(bos + (long long)(c_begin + i) * C);
+        uint8_t* st = sm + s * TX_STAGE;
+        const uint8_t* slot = ring + (size_t)(i % kRingSlots) * FP_OB_BYTES;
+        // the preparation CTA has stored chunk i in its ring slot
+        if (!mbar_wait(&ready[i % kRingSlots], (i / kRingSlots) & 1, abort_flag))
+          break;
+        asm volatile("fence.acq_rel.cluster;\n\tfence.proxy.async.global;" :::
+                         "memory");
+        // ring slot r (released by chunk i - 3): P and the decay vectors
+        if (i >= 3 && !mbar_wait(&pcbars[3 + r], ((i / 3) - 1) & 1, abort_flag))
+          break;
+        mbar_arrive_expect_tx(&pcbars[r], TILE_BYTES + CV_BYTES);
+        bulk_load(sm + TXO_PC + r * PC_SLOT, slot + OB_P, TILE_BYTES, &pcbars[r]);
+        bulk_load(sm + TXO_PC + r * PC_SLOT + PC_CV, slot + OB_CV, CV_BYTES,
+                  &pcbars[r]);
+        // group A: V and T_U
+        if (i >= 2 && !mbar_wait(&bars[TB_EMPTYA0 + s], ph, abort_flag)) break;
+        uint64_t* fa = &bars[TB_FULLA0 + s];
+        mbar_arrive_expect_tx(fa, TX_A_BYTES - 128u * (128 - dv));
+        tma_load_3d(st + TX_V, &tmv, fa, 0, h, tok);
+        if (dv > 64) tma_load_3d(st + TX_V + 8192, &tmv, fa, 64, h, tok);
+        bulk_load(st + TX_TU, slot + OB_TU, TILE_BYTES, fa);
+        // group B: Q and -W
+        if (i >= 2 && !mbar_wait(&bars[TB_EMPTYB0 + s], ph, abort_flag)) break;
+        uint64_t* fb = &bars[TB_FULLB0 + s];
+        mbar_arrive_expect_tx(fb, TX_B_BYTES);
+        tma_load_3d(st + TX_Q, &tmq, fb, 0, h, tok);
+        tma_load_3d(st + TX_Q + TX_WQ_CB, &tmq, fb, 64, h, tok);
+        bulk_load(st + TX_W, slot + OB_W, TILE_BYTES, fb);
+        bulk_load(st + TX_W + TX_WQ_CB, slot + OB_W + TILE_BYTES, TILE_BYTES, fb);
+        // group C: K alone
+        if (i >= 2 && !mbar_wait(&bars[TB_EMPTYC0 + s], ph, abort_flag)) break;
+        uint64_t* fc = &bars[TB_FULLC0 + s];
+        mbar_arrive_expect_tx(fc, 16384);
+        tma_load_3d(st + TX_K, &tmk, fc, 0, h, tok);
+        tma_load_3d(st + TX_K + 8192, &tmk, fc, 64, h, tok);
+        armed = i + 1;
+        if (i + 2 < nloc) prefetch_v(i + 2);
+      }
+      // never leave with a copy still landing in shared memory: the latest
+      // use of every place (a chunk cut short by an abort may have some of
+      // its places armed but never filled: those waits give up after the
+      // bounded wait)
+      const int last = min(armed + 1, nloc);  // chunks that may be in flight
+      for (int i = max(0, last - 3); i < last; ++i)
+        wait_ignoring_abort(&pcbars[i % 3], (i / 3) & 1);
+      for (int i = max(0, last - 2); i < last; ++i) {
+        const uint32_t pf = (i >> 1) & 1;
+        wait_ignoring_abort(&bars[TB_FULLA0 + (i & 1)], pf);
+        wait_ignoring_abort(&bars[TB_FULLB0 + (i & 1)], pf);
+        wait_ignoring_abort(&bars[TB_FULLC0 + (i & 1)], pf);
+      }
+    }
+  } else if (warp == kTxWarpProducer) {
     // ================= TMA producer =================
     // Q, K, V by tensor map; -W, P, T_U and the decay vectors are images in
     // the workspace (bulk copies; the tile index is clamped because those
@@ -1489,7 +2050,50 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         return true;
       };
       bool ok = u0(0);
-      for (int i = 0; ok && i < nloc; ++i) {
+      if (FUSED) {
+        // The preparation CTA's T_U of chunk i + 1 may land after chunk i's
+        // Delta^T: issue U0^T of chunk i + 1 and U^T P^T of chunk i in
+        // whichever order their operands arrive.
+        for (int i = 0; ok && i < nloc; ++i) {
+          const int b = i & 1, nb = b ^ 1;
+          bool need_u0 = i + 1 < nloc, need_pu = true;
+          const uint64_t t0 = globaltimer_ns();
+          for (uint32_t it = 0; need_u0 || need_pu; ++it) {
+            if (need_u0 && mbar_test(&bars[TB_D1FULL0 + b], (i >> 1) & 1) &&
+                mbar_test(&bars[TB_FULLA0 + nb], ((i + 1) >> 1) & 1) &&
+                mbar_test(&bars[TB_D1FREE0 + nb], ((i + 1) >> 1) & 1)) {
+              tc_fence_after();
+              const uint32_t st = stage(i + 1);
+              mma_bf16_run<4>(tmem + TX_D1 + 128 * nb, sdesc(st + TX_V, 8192, 1024),
+                              2048, sdesc(st + TX_TU, 16, 1024), 32, ID_TX_U0,
+                              false);
+              mma_commit(&bars[TB_U0DONE0 + nb]);
+              mma_commit(&bars[TB_EMPTYA0 + nb]);
+              need_u0 = false;
+            }
+            if (need_pu && mbar_test(&bars[TB_D2FULL], i & 1) &&
+                mbar_test(&pcbars[i % 3], (i / 3) & 1)) {
+              tc_fence_after();
+              // U^T P^T over U^T (P in ring slot i % 3)
+              mma_bf16_ta_run<4>(tmem + TX_D1 + 128 * b, tmem + TX_UB,
+                                 sdesc(base + TXO_PC + (i % 3) * PC_SLOT, 16, 1024),
+                                 32, ID_TX_N64, false);
+              mma_commit(&bars[TB_OFULL0 + b]);
+              mma_commit(&pcbars[3 + i % 3]);
+              need_pu = false;
+            }
+            if ((it & 255) == 255) {
+              if (*abort_flag) { ok = false; break; }
+              if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                ok = false;
+                break;
+              }
+            }
+          }
+        }
+      }
+      for (int i = 0; !FUSED && ok && i < nloc; ++i) {
         const int b = i & 1;
         if (i + 1 < nloc) {
           ok = mbar_wait(&bars[TB_D1FULL0 + b], (i >> 1) & 1, abort_flag) &&
@@ -1563,10 +2167,16 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     put_s();
     for (int i = 0; ok && i < nloc; ++i) {
       const int b = i & 1;
-      const float* cvs = reinterpret_cast<const float*>(sm + b * TX_STAGE + TX_CV);
+      // (fused: the decay vectors in ring slot i % 3)
+      const float* cvs = reinterpret_cast<const float*>(
+          FUSED ? sm + TXO_PC + (i % 3) * PC_SLOT + PC_CV
+                : sm + b * TX_STAGE + TX_CV);
       ok = __all_sync(0xffffffffu,
-                      ok && mbar_wait(&bars[TB_FULLC0 + b], (i >> 1) & 1, abort_flag));
+                      ok && mbar_wait(&bars[TB_FULLC0 + b], (i >> 1) & 1, abort_flag) &&
+                          (!FUSED || mbar_wait(&pcbars[i % 3], (i / 3) & 1, abort_flag)));
       if (!ok) break;
+
+
       if (kda) {
         // this warp's half of gamma (per key channel) out of the stage
         // before it is released; read back in the state update below
@@ -1581,7 +2191,10 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       if (!kda) tx_scale_rows(sm + b * TX_STAGE + TX_K, 8192, cvs + CV_DEC, tid);
       fence_proxy_async();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[TB_EMPTYC0 + b]);
+      if (lane == 0) {
+        mbar_arrive(&bars[TB_EMPTYC0 + b]);
+        if (FUSED) mbar_arrive(&pcbars[3 + i % 3]);
+      }
       // U^T (fp32, accumulator columns 32 ch ..: tokens) -> bf16 pairs, over
       // chunk i - 1's, which P U has read
       ok = __all_sync(0xffffffffu,
@@ -1590,6 +2203,14 @@ __global__ void __launch_bounds__(kTxThreads, 1)
                            mbar_wait(&bars[TB_OFULL0 + (b ^ 1)], ((i - 1) >> 1) & 1,
                                      abort_flag)));
       if (!ok) break;
+      // Fused: the [-W;Q] product of chunk i has completed, so every part of
+      // the chunk has landed (T_U and -W included): the preparation CTA may
+      // refill its ring slot (LANDED barrier i % 4). (Waiting on the
+      // chunk's own full barriers here instead could see them two phases
+      // on.)
+      if (FUSED && tid == 0)
+        mbar_arrive_cluster(map_to_cta(
+            sm + FP_BAR + 8 * (FB_LANDED + (c_begin + i) % kRingSlots), prep));
       tc_fence_after();
       {
         float u[32];
@@ -1653,7 +2274,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         for (int c = 0; c < 64; ++c) dst[(size_t)c * dv] = S[c];
       }
     }
-  } else {
+  } else if (warp < kTxThreads / 32) {
     // ================= output =================
     // Thread o of 128 (warp 8 + (warp & 3), TMEM lane quarter warp & 3) owns
     // row r of O^T, i.e. output column r of the chunk's 64 tokens.
@@ -1707,13 +2328,16 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       const int len = (int)min((long long)C, eos - t0);
       // (all output threads decide alike: they meet at named barriers)
       ok = bar_and(5, kTxOutThreads,
-                   mbar_wait(&bars[TB_FULLC0 + b], (i >> 1) & 1, abort_flag) &&
+                   (FUSED ? mbar_wait(&pcbars[i % 3], (i / 3) & 1, abort_flag)
+                          : mbar_wait(&bars[TB_FULLC0 + b], (i >> 1) & 1, abort_flag)) &&
                        mbar_wait(&bars[TB_OFULL0 + b], (i >> 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      // O^T = H^T diag(e^G) + U^T P^T, 32 tokens at a time
-      const float* eg =
-          reinterpret_cast<const float*>(sm + b * TX_STAGE + TX_CV) + CV_EG;
+      // O^T = H^T diag(e^G) + U^T P^T, 32 tokens at a time (fused: the
+      // decay vectors in ring slot i % 3)
+      const float* eg = reinterpret_cast<const float*>(
+                            FUSED ? sm + TXO_PC + (i % 3) * PC_SLOT + PC_CV
+                                  : sm + b * TX_STAGE + TX_CV) + CV_EG;
       float y[64];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -1745,7 +2369,8 @@ __global__ void __launch_bounds__(kTxThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&bars[TB_D1FREE0 + b]);
-        mbar_arrive(&bars[TB_EMPTYC0 + b]);  // e^G has been read
+        // e^G has been read (fused: from ring slot i % 3)
+        mbar_arrive(FUSED ? &pcbars[3 + i % 3] : &bars[TB_EMPTYC0 + b]);
       }
       if (epi && p.norm_w) {
         // sum over the 128 rows of O^T (a token's d_v values) of y^2: a
@@ -1820,11 +2445,65 @@ __global__ void __launch_bounds__(kTxThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // fused: the preparation CTA's pushes into this CTA have all landed (or
+  // this CTA gave up on them), and neither CTA leaves before the other's
+  // last remote write
+  if (FUSED) cluster_sync();
   if (warp == kTxWarpMMA) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
   if (tid == 0 && *abort_flag) record_status(p.status, GDN_ERR_TIMEOUT);
+}
+
+template <bool KDA>
+__global__ void __launch_bounds__(kTxThreads, 1)
+    chain_tx_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tmq,
+                    const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv,
+                    const __grid_constant__ CUtensorMap tmo,
+                    const __grid_constant__ CUtensorMap tmg, int nch_dense,
+                    int tiles) {
+  chain_tx_body<KDA, false>(p, tmq, tmk, tmv, tmo, tmg, nch_dense, tiles,
+                            blockIdx.x, blockIdx.y, blockIdx.z, 0);
+}
+
+// The fused kernel's block: the chain CTA's fifteen warps and one more,
+// idle there; in the preparation CTA twelve compute warps (three groups of
+// four), a loader warp per group and one warp that copies the outboxes.
+constexpr int kFusedThreads = 16 * 32;
+
+// fused_chunk_kernel: the whole forward pass with no workspace. A cluster
+// of four CTAs serves two (sequence, head) pairs u = 2c and 2c + 1: ranks 0
+// and 1 prepare every chunk of pair 2c + rank (prep_role) and push -W, P,
+// T_U and the decay vectors into the stages of ranks 2 and 3, which run the
+// whole-state chains and write the outputs (chain_tx_body). The two
+// preparation CTAs share a TPC and so do the two chains: a chain whose TPC
+// neighbour runs a preparation measured about twice as slow per chunk (and
+// the preparation too) as one beside another chain. Grid (4 ceil(N H / 2)),
+// cluster (4, 1, 1); one sub-sequence (no split). A rank with no pair (odd
+// N H) only meets the others at the cluster barriers.
+template <int VARIANT>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    fused_chunk_kernel(const ChunkParams p,
+                       const __grid_constant__ CUtensorMap tmq,
+                       const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv,
+                       const __grid_constant__ CUtensorMap tmo,
+                       const __grid_constant__ CUtensorMap tmg) {
+  const uint32_t rank = cluster_ctarank();
+  const long long u = 2ll * (blockIdx.x >> 2) + (rank & 1);
+  if (u >= (long long)p.N * p.H) {
+    cluster_sync();
+    cluster_sync();
+    return;
+  }
+  const int n = (int)(u / p.H), h = (int)(u - (long long)n * p.H);
+  if (rank < 2)
+    prep_role<VARIANT>(p, tmk, tmq, n, h, rank + 2);
+  else
+    chain_tx_body<false, true>(p, tmq, tmk, tmv, tmo, tmg, 1, 1, 0, h, n,
+                               rank - 2);
 }
 
 
@@ -2096,6 +2775,51 @@ cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
                       : launch(ut_prep_kernel<GDN_GATE_BEFORE_PREDICT>);
   if (e == cudaSuccess) ++*launches;
   return e;
+}
+
+size_t fused_ring_bytes(const ChunkParams& p) {
+  return (size_t)p.N * p.H * kRingSlots * FP_OB_BYTES;
+}
+
+// The fused single-kernel path: per two (sequence, head) pairs a cluster of
+// two preparation and two chain CTAs, handing chunks over through a ring in
+// global memory (p.ring, fused_ring_bytes; one sub-sequence; dense or
+// packed).
+cudaError_t launch_chunk_fused(const ChunkParams& p, cudaStream_t stream) {
+  const long long tokens = call_tokens(p);
+  CUtensorMap mq, mk, mv, mo, mg;
+  if (!make_map(&mq, p.q, p.dk, p.H, tokens, 1, 64) ||
+      !make_map(&mk, p.k, p.dk, p.H, tokens, 1, 64) ||
+      !make_map(&mv, p.v, p.dv, p.H, tokens, 1, 64) ||
+      !make_map(&mo, p.out, p.dv, p.H, tokens, 1, 64) ||
+      !make_map(&mg, p.gate_z ? p.gate_z : p.out, p.dv, p.H, tokens, 1, 64))
+    return cudaErrorInvalidValue;
+  auto launch = [&](auto kern) {
+    cudaError_t e = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)FUSED_SMEM);
+    if (e != cudaSuccess) return e;
+    const int t = timing_start(GDN_KERNEL_CHUNK_FUSED, stream);
+    cudaLaunchConfig_t cfg{};
+    const long long pairs = ((long long)p.N * p.H + 1) / 2;
+    cfg.gridDim = dim3((unsigned)(4 * pairs), 1, 1);
+    cfg.blockDim = dim3(kFusedThreads);
+    cfg.dynamicSmemBytes = FUSED_SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 4;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p, mq, mk, mv, mo, mg);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    timing_stop(t, stream, e);
+    return e;
+  };
+  return p.variant == GDN_GATE_AFTER_PREDICT
+             ? launch(fused_chunk_kernel<GDN_GATE_AFTER_PREDICT>)
+             : launch(fused_chunk_kernel<GDN_GATE_BEFORE_PREDICT>);
 }
 
 // One pass of the chain kernel (after launch_ut_prep on the same stream).

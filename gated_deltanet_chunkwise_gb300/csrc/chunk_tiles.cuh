@@ -158,8 +158,10 @@ __device__ __forceinline__ void mm16x16(float* D, int dr, int dc, const float* X
 // blocks are zero except the upper-right 32 x 32 block, which is scratch.
 // Blocked in powers of two: the four 16 x 16 diagonal blocks by substitution,
 // then T_10 = -T_11 A_10 T_00 at 16 and at 32 with the products on the tensor
-// cores (tf32). All 128 prep threads take part.
-__device__ __forceinline__ void solve_unit_lower(float* AT, int tid) {
+// cores (tf32). All 128 prep threads take part (tid 0..127); they meet at
+// named barrier `bar`.
+__device__ __forceinline__ void solve_unit_lower(float* AT, int tid,
+                                                 int bar = 1) {
   const int warp = tid >> 5, lane = tid & 31;
   // 1. diagonal 16 x 16 blocks: one per warp, lane l < 16 owns column l,
   //    x_m = delta_ml - sum_{j<m} A_mj x_j
@@ -170,16 +172,19 @@ __device__ __forceinline__ void solve_unit_lower(float* AT, int tid) {
 #pragma unroll
       for (int m = 0; m < 16; ++m) {
         const float4* arow = reinterpret_cast<const float4*>(AT + (b + m) * AP + b);
-        float acc = (m == lane) ? 1.f : 0.f;
+        // four partial sums, so that the dependent chain of a row is m / 4
+        // multiply-adds long rather than m
+        float acc0 = (m == lane) ? 1.f : 0.f, acc1 = 0.f, acc2 = 0.f,
+              acc3 = 0.f;
 #pragma unroll
         for (int q = 0; q < (m + 3) / 4; ++q) {
           const float4 a = arow[q];  // one broadcast load for four terms
-          if (4 * q < m) acc = fmaf(-a.x, xs[4 * q], acc);
-          if (4 * q + 1 < m) acc = fmaf(-a.y, xs[4 * q + 1], acc);
-          if (4 * q + 2 < m) acc = fmaf(-a.z, xs[4 * q + 2], acc);
-          if (4 * q + 3 < m) acc = fmaf(-a.w, xs[4 * q + 3], acc);
+          if (4 * q < m) acc0 = fmaf(-a.x, xs[4 * q], acc0);
+          if (4 * q + 1 < m) acc1 = fmaf(-a.y, xs[4 * q + 1], acc1);
+          if (4 * q + 2 < m) acc2 = fmaf(-a.z, xs[4 * q + 2], acc2);
+          if (4 * q + 3 < m) acc3 = fmaf(-a.w, xs[4 * q + 3], acc3);
         }
-        xs[m] = acc;
+        xs[m] = (acc0 + acc1) + (acc2 + acc3);
       }
     }
     __syncwarp();  // the whole block is read before it is overwritten
@@ -188,7 +193,7 @@ __device__ __forceinline__ void solve_unit_lower(float* AT, int tid) {
       for (int m = 0; m < 16; ++m) AT[(b + m) * AP + b + lane] = xs[m];
     }
   }
-  named_bar(1, 128);
+  named_bar(bar, 128);
   // 2. 16 -> 32: warp p in {0, 1} merges diagonal blocks (2p, 2p+1); the
   //    product X = A_10 T_00 goes to rows 16p.., columns 32+16p.. (scratch)
   if (warp < 2) {
@@ -198,16 +203,16 @@ __device__ __forceinline__ void solve_unit_lower(float* AT, int tid) {
     mm16x16<16>(AT, kb + 16, kb, AT, kb + 16, kb + 16, AT, xr, xc, -1.f,
                 lane);
   }
-  named_bar(1, 128);
+  named_bar(bar, 128);
   // 3. 32 -> 64: X = A_21 T_11 into rows 0-31, columns 32-63, then
   //    T_21 = -T_22 X; warp w owns rows 16 (w >> 1), columns 16 (w & 1)
   {
     const int mr = 16 * (warp >> 1), nc = 16 * (warp & 1);
     mm16x16<32>(AT, mr, 32 + nc, AT, 32 + mr, 0, AT, 0, nc, 1.f, lane);
-    named_bar(1, 128);
+    named_bar(bar, 128);
     mm16x16<32>(AT, 32 + mr, nc, AT, 32 + mr, 32, AT, 0, 32 + nc, -1.f, lane);
   }
-  named_bar(1, 128);
+  named_bar(bar, 128);
 }
 
 

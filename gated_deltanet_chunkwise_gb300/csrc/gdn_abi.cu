@@ -56,9 +56,11 @@ int check_chunk_args(const void* q, const void* k, const void* v,
     return GDN_ERR_INVALID_ARG;
   if (variant != GDN_GATE_BEFORE_PREDICT && variant != GDN_GATE_AFTER_PREDICT)
     return GDN_ERR_INVALID_ARG;
-  if (path < GDN_PATH_AUTO || path > GDN_PATH_TCGEN05_WHOLE)
+  if (path < GDN_PATH_AUTO || path > GDN_PATH_TCGEN05_FUSED)
     return GDN_ERR_INVALID_ARG;
   if (sp_parts < 0 || sp_parts > 4096) return GDN_ERR_INVALID_ARG;
+  // the fused single-kernel path has no sequence-parallel split
+  if (path == GDN_PATH_TCGEN05_FUSED && sp_parts > 1) return GDN_ERR_UNSUPPORTED;
   if (cu_seqlens && B == 0) return GDN_ERR_INVALID_ARG;
   const long long tokens = cu_seqlens ? (long long)T : (long long)B * T;
   if (tokens > 0 || (cu_seqlens && B > 0)) {
@@ -144,8 +146,13 @@ long long parts_cost_tc(int requested, int N, int H, int T, int dv, int C,
 
 // rows per chain CTA and the split for the tensor-core path (`path` may fix
 // the chain kernel)
+// `path` may fix the chain kernel; GDN_PATH_TCGEN05_FUSED asks for the
+// single-launch form (`*fused`, one sub-sequence). The automatic choice
+// keeps the two-kernel form: measured on GB300, the single launch moves
+// far fewer DRAM bytes (the hand-off stays in L2) but is not faster (W1
+// 0.095 vs 0.091 ms, the packed workload 1.41 vs 1.05 ms).
 void choose_chain_tc(int path, int requested, int N, int H, int T, int dv,
-                     int C, bool packed, int* rows, int* parts) {
+                     int C, bool packed, int* rows, int* parts, bool* fused) {
   int sms = 148, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) {
     int v = 0;
@@ -162,6 +169,11 @@ void choose_chain_tc(int path, int requested, int N, int H, int T, int dv,
                      (path != GDN_PATH_TCGEN05_SPLIT && c128 < c64);
   *rows = whole ? 128 : 64;
   *parts = whole ? p128 : p64;
+  *fused = path == GDN_PATH_TCGEN05_FUSED;
+  if (*fused) {
+    *rows = 128;
+    *parts = 1;
+  }
 }
 
 // The steps either side of the recurrence (gdn_chunk_fwd_fused).
@@ -229,12 +241,25 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
                   : launch_chunk_simt(q, bf16, stream);
   };
   int parts = 1;
+  bool fused = false;
   if (use_tc)
     choose_chain_tc(kda ? GDN_PATH_TCGEN05_WHOLE : path, sp_parts, B, H, T,
-                    dv, C, cu_seqlens != nullptr, &p.chain_rows, &parts);
+                    dv, C, cu_seqlens != nullptr, &p.chain_rows, &parts,
+                    &fused);
   else
     parts = choose_parts(sp_parts, B, H, T, dv, C, cu_seqlens != nullptr);
   p.parts = parts;
+  if (fused) {
+    // one launch; the hand-off ring (a few slots per (sequence, head))
+    p.part_begin = 0; p.part_count = 1; p.mode = kModeOutput;
+    void* ring = nullptr;
+    if (cudaMallocAsync(&ring, fused_ring_bytes(p), stream) != cudaSuccess)
+      return GDN_ERR_CUDA;
+    p.ring = ring;
+    const cudaError_t e = counted(launch_chunk_fused(p, stream), 1);
+    const cudaError_t f = cudaFreeAsync(ring, stream);
+    return (e == cudaSuccess && f == cudaSuccess) ? GDN_OK : GDN_ERR_CUDA;
+  }
   // Combination of the sub-sequences: the scan when forced, or when its
   // rounds of parallel work (64-row CTAs, two per SM, each worth four of the
   // chain's 16-row steps) take less time than the chain's P - 2 dependent
@@ -437,7 +462,7 @@ int gdn_chunk_fwd_fused(const void* q, const void* k, const void* v,
                         const float* norm_weight, const void* gate, float eps,
                         int B, int H, int T, int dk, int dv, int C, int path,
                         gdn_stream_t stream) {
-  if (path < GDN_PATH_AUTO || path > GDN_PATH_TCGEN05_WHOLE)
+  if (path < GDN_PATH_AUTO || path > GDN_PATH_TCGEN05_FUSED)
     return GDN_ERR_INVALID_ARG;
   if (path == GDN_PATH_SIMT) return GDN_ERR_UNSUPPORTED;
   gdn::Sublayer sub;
@@ -578,9 +603,12 @@ int gdn_kda_fwd_ex(const void* q, const void* k, const void* v,
                    gdn_stream_t stream) {
   const int sp_mode = path & (GDN_SP_CHAIN | GDN_SP_SCAN);
   const int kernels = path & ~(GDN_SP_CHAIN | GDN_SP_SCAN);
-  if (kernels < GDN_PATH_AUTO || kernels > GDN_PATH_TCGEN05_WHOLE)
+  if (kernels < GDN_PATH_AUTO || kernels > GDN_PATH_TCGEN05_FUSED)
     return GDN_ERR_INVALID_ARG;
-  if (kernels == GDN_PATH_TCGEN05_SPLIT) return GDN_ERR_UNSUPPORTED;
+  // the chunk form of KDA runs on the whole-state chain with its own
+  // preparation kernel only
+  if (kernels == GDN_PATH_TCGEN05_SPLIT || kernels == GDN_PATH_TCGEN05_FUSED)
+    return GDN_ERR_UNSUPPORTED;
   const long long tokens = cu_seqlens ? (long long)T : (long long)B * T;
   // nothing to compute but the state copy: the token-by-token kernel
   if (kernels == GDN_PATH_SIMT || B <= 0 || H <= 0 || T <= 0 || tokens <= 0 ||

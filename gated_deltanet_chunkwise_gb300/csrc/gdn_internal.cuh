@@ -74,6 +74,9 @@ struct ChunkParams {
   const float* norm_w;       // [dv] fp32 or null
   const void* gate_z;        // like out (bf16) or null
   float eps;
+  // fused single-launch path: per (sequence, head) a ring of hand-off
+  // slots in global memory (launch_chunk_fused, fused_ring_bytes)
+  void* ring;
 };
 
 struct DecodeParams {
@@ -134,6 +137,12 @@ cudaError_t launch_block_offsets(const int32_t* cu_seqlens, int N, int T,
                                  cudaStream_t stream);
 int chunk_tc_nch_dense(const ChunkParams& p);
 cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream);
+// The same path in one launch with no workspace (one sub-sequence): a
+// cluster per (sequence, head) of a preparation CTA and a whole-state chain
+// CTA (bf16, dk = 128, dv in {64, 128}; not KDA).
+cudaError_t launch_chunk_fused(const ChunkParams& p, cudaStream_t stream);
+// Bytes of the hand-off ring the fused path needs (p.ring).
+size_t fused_ring_bytes(const ChunkParams& p);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_kda(const KdaParams& p, cudaStream_t stream);
 

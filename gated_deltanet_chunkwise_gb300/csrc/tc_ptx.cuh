@@ -187,6 +187,26 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar,
     }
   }
 }
+// Waits for a phase completed by another CTA's remote arrivals: polls with
+// the CTA-scope non-blocking test (one thread that must react at once),
+// then one cluster-scope fence orders what follows after the remote side's
+// release.
+__device__ __forceinline__ bool mbar_spin_remote(uint64_t* bar, uint32_t parity,
+                                                 volatile int* abort_flag) {
+  const bool ok = mbar_spin(bar, parity, abort_flag);
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+  return ok;
+}
+// Asynchronous 16-byte store into another CTA of the cluster that counts its
+// bytes on that CTA's mbarrier (both addresses from map_to_cta).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint4 v,
+                                            uint32_t bar_addr) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], "
+      "{%1, %2, %3, %4}, [%5];" ::"r"(addr),
+      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar_addr)
+      : "memory");
+}
 // All threads of every CTA of the cluster (release / acquire).
 __device__ __forceinline__ void cluster_sync() {
   asm volatile(

@@ -80,6 +80,13 @@ typedef enum {
                                     (sequence, head) when dv = 128) */
 #define GDN_PATH_TCGEN05_WHOLE 4 /* 128 state rows per CTA, state in TMEM
                                     lanes (zero-padded when dv = 64) */
+#define GDN_PATH_TCGEN05_FUSED 5 /* one launch: clusters of two preparation
+                                    and two whole-state chain CTAs, the
+                                    chunks handed over through a small ring
+                                    in global memory that stays in L2 (a few
+                                    chunks per (sequence, head)); no
+                                    sequence-parallel split (sp_parts must be
+                                    0 or 1); never chosen by GDN_PATH_AUTO */
 /* How the sub-sequences of a sequence-parallel split are combined, OR-ed into
  * `path` of gdn_chunk_fwd_ex (default: the library's choice by a cost model,
  * in practice the serial chain): */
@@ -441,7 +448,10 @@ typedef enum {
   GDN_KERNEL_CBWD_FWD = 12,     /* chunk-form backward: entry states, U */
   GDN_KERNEL_CBWD_REV = 13,     /* chunk-form backward: exit gradients, dU */
   GDN_KERNEL_CBWD_GRAD = 14,    /* chunk-form backward: per-chunk gradients */
-  GDN_KERNEL_COUNT = 15
+  GDN_KERNEL_CHUNK_FUSED = 15,  /* tensor-core path in one launch: the
+                                   preparation and the chain of each
+                                   (sequence, head) in one cluster */
+  GDN_KERNEL_COUNT = 16
 } gdn_kernel_t;
 
 /* gdn_timing_enable -- per-kernel device timing on (nonzero) or off (0).

@@ -95,7 +95,10 @@ def chunk(so, q=A, k=A + 0x1000, v=A + 0x2000, g=A + 0x3000, beta=A + 0x4000,
     (dict(dtype=1, path=2), UNSUPPORTED),  # tensor-core path is bf16 only
     (dict(dtype=1, path=3), UNSUPPORTED),
     (dict(dtype=1, path=4), UNSUPPORTED),
-    (dict(path=5), INVALID),
+    (dict(dtype=1, path=5), UNSUPPORTED),
+    (dict(path=5), UNSUPPORTED),           # tensor-core shapes only (dk=64)
+    (dict(path=5, dk=128, dv=128, sp_parts=3), UNSUPPORTED),  # no split
+    (dict(path=6), INVALID),
 ])
 def test_chunk_fwd_rejects_on_host(lib, kw, expect):
     assert chunk(lib.library(), **kw) == expect
@@ -173,7 +176,7 @@ def fused(so, q=A, k=A + 0x1000, v=A + 0x2000, a=A + 0x3000, b=A + 0x4000,
     (dict(gate=A + 0x5000), INVALID),    # gate aliases out
     (dict(C=32), UNSUPPORTED),
     (dict(path=1), UNSUPPORTED),         # no fp32 CUDA-core fused path
-    (dict(path=5), INVALID),
+    (dict(path=6), INVALID),
     (dict(path=-1), INVALID),
 ])
 def test_fused_rejects_on_host(lib, kw, expect):
@@ -216,7 +219,8 @@ def kda_ex(so, path=0, sp=0, **kw):
 
 
 @pytest.mark.parametrize("kw,expect", [
-    (dict(path=-1), INVALID), (dict(path=5), INVALID),
+    (dict(path=-1), INVALID), (dict(path=6), INVALID),
+    (dict(path=5), UNSUPPORTED),                 # single-launch form: GDN only
     (dict(path=0x300), INVALID), (dict(path=0x400), INVALID),
     (dict(path=3), UNSUPPORTED),                 # split chain: scalar gate only
     (dict(path=2, dk=64), UNSUPPORTED),          # chunk form: dk = 128 only

@@ -18,6 +18,8 @@ TOL = 2e-2
 # CTAs per head when dv = 128, a cluster pair for the fused epilogue) and
 # 128 rows per CTA (the whole state in TMEM lanes)
 CHAINS = [3, 4]
+# and the single-launch form (preparation and chain in one cluster)
+FUSED = 5
 
 
 def rel_err(x, ref):
@@ -47,7 +49,7 @@ def check(lib, dev, d, eps=1e-6, path=0):
     assert rel_err(hT, h_ref) <= TOL, rel_err(hT, h_ref)
 
 
-@pytest.mark.parametrize("path", CHAINS)
+@pytest.mark.parametrize("path", CHAINS + [FUSED])
 @pytest.mark.parametrize("dv", [64, 128])
 @pytest.mark.parametrize("weight,gate", [(True, True), (True, False),
                                          (False, True), (False, False)])
@@ -57,14 +59,14 @@ def test_fused_matches_oracle(lib, cuda_device, dv, weight, gate, path):
     check(lib, cuda_device, d, path=path)
 
 
-@pytest.mark.parametrize("path", CHAINS)
+@pytest.mark.parametrize("path", CHAINS + [FUSED])
 @pytest.mark.parametrize("T", [1, 63, 65, 130])
 def test_fused_short_and_ragged(lib, cuda_device, T, path):
     d = inputs.fused_inputs(1, 2, T, 128, 128, seed=12)
     check(lib, cuda_device, d, path=path)
 
 
-@pytest.mark.parametrize("path", CHAINS)
+@pytest.mark.parametrize("path", CHAINS + [FUSED])
 def test_fused_packed(lib, cuda_device, path):
     d = inputs.fused_inputs(0, 4, 0, 128, 128, seed=13, h0=True,
                             lengths=[70, 1, 0, 300, 64, 129])

@@ -215,9 +215,12 @@ def test_recurrent_step_matches_chunk_path_single_token(lib, cuda_device):
 TC = 2
 # its two chain kernels, forced: 64 state rows per CTA, 128 rows per CTA
 CHAINS = [3, 4]
+# the single-launch form (preparation and chain of a (sequence, head) in one
+# cluster, no workspace), forced; it takes no sequence-parallel split
+FUSED = 5
 
 
-@pytest.mark.parametrize("path", [TC] + CHAINS)
+@pytest.mark.parametrize("path", [TC] + CHAINS + [FUSED])
 @pytest.mark.parametrize("dv", [64, 128])
 @pytest.mark.parametrize("variant", [0, 1])
 def test_tensor_core_path(lib, cuda_device, dv, variant, path):
@@ -226,15 +229,15 @@ def test_tensor_core_path(lib, cuda_device, dv, variant, path):
     check(lib, cuda_device, d, "bf16", variant=variant, path=path)
 
 
-@pytest.mark.parametrize("path", CHAINS)
+@pytest.mark.parametrize("path", CHAINS + [FUSED])
 def test_tensor_core_alpha_one_single_chunk(lib, cuda_device, path):
     d = inputs.chunk_inputs(1, 2, 64, 128, 128, dtype="bf16", seed=13,
                             gated=False)
     check(lib, cuda_device, d, "bf16", path=path)
 
 
-@pytest.mark.parametrize("path", CHAINS)
-@pytest.mark.parametrize("T", [1, 17, 63, 65, 128])
+@pytest.mark.parametrize("path", CHAINS + [FUSED])
+@pytest.mark.parametrize("T", [1, 17, 63, 65, 128, 64 * 7 + 5])
 def test_tensor_core_short_lengths(lib, cuda_device, T, path):
     d = inputs.chunk_inputs(2, 2, T, 128, 128, dtype="bf16", seed=14, h0=True)
     check(lib, cuda_device, d, "bf16", path=path)
@@ -249,7 +252,7 @@ def test_tensor_core_sequence_parallel(lib, cuda_device, parts, dv, path):
     check(lib, cuda_device, d, "bf16", path=path, sp_parts=parts)
 
 
-@pytest.mark.parametrize("path", CHAINS)
+@pytest.mark.parametrize("path", CHAINS + [FUSED])
 def test_tensor_core_packed(lib, cuda_device, path):
     lengths = [70, 0, 1, 64, 200, 3, 129]
     d = inputs.chunk_inputs(len(lengths), 2, 0, 128, 128, dtype="bf16",
@@ -257,7 +260,7 @@ def test_tensor_core_packed(lib, cuda_device, path):
     check(lib, cuda_device, d, "bf16", path=path)
 
 
-@pytest.mark.parametrize("path", [1] + CHAINS)
+@pytest.mark.parametrize("path", [1] + CHAINS + [FUSED])
 def test_strong_gates_chunk_decay_beyond_fp32_range(lib, cuda_device, path):
     """Log-gates ~6x stronger than the workload's, so a chunk's total decay
     exceeds e^-87: the tensor-core kernel must switch from factored decays
@@ -274,7 +277,7 @@ def test_mixed_gate_strength_across_chunks(lib, cuda_device):
                             h0=True)
     d["g"][:, 64:128] *= 8.0
     d["g"][:, 192:] *= 5.0
-    for path in CHAINS:
+    for path in CHAINS + [FUSED]:
         check(lib, cuda_device, d, "bf16", path=path)
 
 
@@ -287,6 +290,7 @@ def test_kernel_timing_counts_the_launches(lib, cuda_device):
         run_gpu(lib, d, cuda_device, "bf16", path=3, sp_parts=1)
         run_gpu(lib, d, cuda_device, "bf16", path=4, sp_parts=1)
         run_gpu(lib, d, cuda_device, "bf16", path=1, sp_parts=1)
+        run_gpu(lib, d, cuda_device, "bf16", path=FUSED, sp_parts=1)
         t = lib.kernel_timings()
     finally:
         lib.gdn_timing_enable(False)
@@ -294,4 +298,23 @@ def test_kernel_timing_counts_the_launches(lib, cuda_device):
     assert t["chunk_tc_kernel"][0] == 1
     assert t["chain_tx_kernel"][0] == 1
     assert t["chunk_simt_kernel"][0] == 1
+    assert t["fused_chunk_kernel"][0] == 1
     assert all(ms > 0 for _, ms in t.values())
+
+
+def test_fused_path_rejects_a_split(lib, cuda_device):
+    d = to_dev(inputs.chunk_inputs(1, 2, 300, 128, 128, dtype="bf16", seed=6),
+               cuda_device)
+    with pytest.raises(lib.GdnError) as e:
+        lib.gdn_chunk_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                             path=FUSED, sp_parts=3)
+    assert e.value.status == -2
+
+
+@pytest.mark.parametrize("dv", [64, 128])
+def test_fused_path_many_chunks_and_heads(lib, cuda_device, dv):
+    # more (sequence, head) clusters than SMs hold at once, long enough that
+    # every preparation group cycles its stage many times
+    d = inputs.chunk_inputs(3, 40, 64 * 21 + 33, 128, dv, dtype="bf16",
+                            seed=19, h0=True)
+    check(lib, cuda_device, d, "bf16", path=FUSED)
