@@ -693,7 +693,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int row0 = blockIdx.x * DVT;
   const bool value_rows = row0 < dv;
   const bool split_tail = (p.mode == kModeSplit) && part > 0;
-  if (!value_rows && !(split_tail && row0 < dv + DK)) return;
+  // d_k = 64 runs on the d_k = 128 layout: the second 64-column block of
+  // K and Q loads as zeros (its tensor-map box lies outside the tensor), so
+  // the state's rows d_k..127 stay zero; only rows < d_k are read and
+  // written
+  const int dkr = p.dk;
+  if (!value_rows && !(split_tail && row0 < dv + dkr)) return;
   const bool scale_rows = !value_rows;
   const bool emit = (p.mode == kModeOutput) || part == 0;
   // fused epilogue on this CTA's outputs; with d_v = 128 the two CTAs of a
@@ -903,14 +908,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (split_tail) {
 #pragma unroll
       for (int c = 0; c < kCW; ++c) S[c] = 0.f;
+    } else if (ct >= dkr) {
+#pragma unroll
+      for (int c = 0; c < kCW; ++c) S[c] = 0.f;
     } else if (part > 0) {
       const float* src =
-          p.ws_start + ((nh * p.parts + part) * dv + row0 + cols) * DK + ct;
+          p.ws_start + ((nh * p.parts + part) * dv + row0 + cols) * dkr + ct;
 #pragma unroll
-      for (int c = 0; c < kCW; ++c) S[c] = src[(size_t)c * DK];
+      for (int c = 0; c < kCW; ++c) S[c] = src[(size_t)c * dkr];
     } else if (p.h0) {
       const float4* src = reinterpret_cast<const float4*>(
-          p.h0 + (nh * DK + ct) * dv + row0 + cols);
+          p.h0 + (nh * dkr + ct) * dv + row0 + cols);
 #pragma unroll
       for (int c = 0; c < kCW / 4; ++c) {
         const float4 v4 = src[c];
@@ -1120,23 +1128,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ok = bar_and(2, kChainThreads, ok);
     if (tid == 0) bulk_wait_all();
-    if (ok && !*abort_flag) {
+    if (ok && !*abort_flag && ct < dkr) {
       if (p.mode == kModeSplit) {
         if (part == 0) {
           if (p.parts > 1) {
             float* dst =
-                p.ws_start + ((nh * p.parts + 1) * dv + row0 + cols) * DK + ct;
+                p.ws_start + ((nh * p.parts + 1) * dv + row0 + cols) * dkr + ct;
 #pragma unroll
-            for (int c = 0; c < kCW; ++c) dst[(size_t)c * DK] = S[c];
+            for (int c = 0; c < kCW; ++c) dst[(size_t)c * dkr] = S[c];
           }
         } else {
           float* dst = p.ws_end +
-                       ((nh * p.parts + part) * (dv + DK) + row0 + cols) * DK + ct;
+                       ((nh * p.parts + part) * (dv + dkr) + row0 + cols) * dkr + ct;
 #pragma unroll
-          for (int c = 0; c < kCW; ++c) dst[(size_t)c * DK] = S[c];
+          for (int c = 0; c < kCW; ++c) dst[(size_t)c * dkr] = S[c];
         }
       } else if (p.hT && part == p.parts - 1) {
-        float4* dst = reinterpret_cast<float4*>(p.hT + (nh * DK + ct) * dv + row0 + cols);
+        float4* dst = reinterpret_cast<float4*>(p.hT + (nh * dkr + ct) * dv + row0 + cols);
 #pragma unroll
         for (int c = 0; c < kCW / 4; ++c)
           dst[c] = make_float4(S[4 * c], S[4 * c + 1], S[4 * c + 2], S[4 * c + 3]);
@@ -1751,7 +1759,11 @@ __device__ __forceinline__ void chain_tx_body(
   const int row0 = xblock * TXR;
   const bool value_rows = row0 < dv;
   const bool split_tail = (p.mode == kModeSplit) && part > 0;
-  if (!value_rows && !(split_tail && row0 < dv + DK)) return;
+  // d_k = 64 runs on the d_k = 128 layout (K and Q's second 64-column block
+  // loads as zeros): the state's columns (and the scaling matrix's rows)
+  // d_k..127 stay zero; only those < d_k are read and written
+  const int dkr = p.dk;
+  if (!value_rows && !(split_tail && row0 < dv + dkr)) return;
   const bool scale_rows = !value_rows;
   const bool emit = value_rows && ((p.mode == kModeOutput) || part == 0);
   const bool epi = p.epilogue && emit;
@@ -2126,24 +2138,26 @@ __device__ __forceinline__ void chain_tx_body(
     const int r = 32 * (warp & 3) + lane;
     const uint32_t lanes = (uint32_t)(32 * (warp & 3)) << 16;
     float S[64];
-    // value rows r >= d_v (d_v = 64) stay zero: no input, no output
-    const bool live = scale_rows || r < dv;
+    // value rows r >= d_v (d_v = 64) and scaling-matrix rows r >= d_k stay
+    // zero: no input, no output; so do the columns 64 ch >= d_k
+    const bool live = scale_rows ? r < dkr : r < dv;
+    const bool live_cols = 64 * ch < dkr;
     if (scale_rows) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) S[c] = (r == 64 * ch + c) ? 1.f : 0.f;
-    } else if (split_tail || !live) {
+      for (int c = 0; c < 64; ++c) S[c] = (live && r == 64 * ch + c) ? 1.f : 0.f;
+    } else if (split_tail || !live || !live_cols) {
 #pragma unroll
       for (int c = 0; c < 64; ++c) S[c] = 0.f;
     } else if (part > 0) {
       const float4* src = reinterpret_cast<const float4*>(
-          p.ws_start + ((nh * p.parts + part) * dv + r) * DK + 64 * ch);
+          p.ws_start + ((nh * p.parts + part) * dv + r) * dkr + 64 * ch);
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const float4 v4 = src[c];
         S[4 * c] = v4.x; S[4 * c + 1] = v4.y; S[4 * c + 2] = v4.z; S[4 * c + 3] = v4.w;
       }
     } else if (p.h0) {
-      const float* src = p.h0 + (nh * DK + 64 * ch) * dv + r;
+      const float* src = p.h0 + (nh * dkr + 64 * ch) * dv + r;
 #pragma unroll
       for (int c = 0; c < 64; ++c) S[c] = src[(size_t)c * dv];
     } else {
@@ -2253,14 +2267,14 @@ __device__ __forceinline__ void chain_tx_body(
       }
       put_s();
     }
-    if (ok && live && !*abort_flag) {
+    if (ok && live && live_cols && !*abort_flag) {
       if (p.mode == kModeSplit) {
         float* dst = nullptr;
         if (part == 0) {
-          if (p.parts > 1) dst = p.ws_start + ((nh * p.parts + 1) * dv + r) * DK;
+          if (p.parts > 1) dst = p.ws_start + ((nh * p.parts + 1) * dv + r) * dkr;
         } else {
           dst = p.ws_end +
-                ((nh * p.parts + part) * (dv + DK) + (scale_rows ? dv : 0) + r) * DK;
+                ((nh * p.parts + part) * (dv + dkr) + (scale_rows ? dv : 0) + r) * dkr;
         }
         if (dst) {
           float4* d4 = reinterpret_cast<float4*>(dst + 64 * ch);
@@ -2269,7 +2283,7 @@ __device__ __forceinline__ void chain_tx_body(
             d4[c] = make_float4(S[4 * c], S[4 * c + 1], S[4 * c + 2], S[4 * c + 3]);
         }
       } else if (p.hT && part == p.parts - 1) {
-        float* dst = p.hT + (nh * DK + 64 * ch) * dv + r;
+        float* dst = p.hT + (nh * dkr + 64 * ch) * dv + r;
 #pragma unroll
         for (int c = 0; c < 64; ++c) dst[(size_t)c * dv] = S[c];
       }
@@ -2679,7 +2693,8 @@ bool make_rows_map(CUtensorMap* map, const void* ptr, bool fp32, long long d0,
 
 bool chunk_tc_supported(int dk, int dv, long long tokens, int N, int H) {
   // chunk-tile indices (chunk * H + head) and token rows stay in int
-  return dk == DK && (dv == 64 || dv == 128) && tokens > 0 &&
+  // d_k = 64: the d_k = 128 kernels with K and Q zero-filled to 128
+  return (dk == DK || dk == 64) && (dv == 64 || dv == 128) && tokens > 0 &&
          tokens < (1ll << 31) - 64 &&
          (tokens / C + N + 1) * (long long)H < (1ll << 31);
 }
@@ -2866,7 +2881,7 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    const int rows = p.mode == kModeSplit ? p.dv + DK : p.dv;
+    const int rows = p.mode == kModeSplit ? p.dv + p.dk : p.dv;
     dim3 grid(rows / DVT, p.H, p.N * p.part_count);
     const int t = timing_start(GDN_KERNEL_CHUNK_CHAIN, stream);
     // programmatic stream serialisation: the launch may begin while the

@@ -112,11 +112,12 @@ int choose_parts(int requested, int N, int H, int T, int dv, int C,
 // a split pass ceil(dk / rows) more for the scaling matrix. Picks the split
 // count P that minimises split pass + corrected output pass and returns
 // that cost.
-long long parts_cost_tc(int requested, int N, int H, int T, int dv, int C,
-                        bool packed, int rows, int sms, int* parts_out) {
+long long parts_cost_tc(int requested, int N, int H, int T, int dk, int dv,
+                        int C, bool packed, int rows, int sms,
+                        int* parts_out) {
   const long long nch = (T + C - 1) / C;
   const long long nh = (long long)N * H, tv = (dv + rows - 1) / rows,
-                  tk = (128 + rows - 1) / rows;
+                  tk = (dk + rows - 1) / rows;
   auto waves = [&](long long ctas) { return (ctas + sms - 1) / sms; };
   // packed calls: passes over the longest possible sequence
   const long long len = packed ? (long long)T / C + 1 : nch;
@@ -151,8 +152,9 @@ long long parts_cost_tc(int requested, int N, int H, int T, int dv, int C,
 // keeps the two-kernel form: measured on GB300, the single launch moves
 // far fewer DRAM bytes (the hand-off stays in L2) but is not faster (W1
 // 0.095 vs 0.091 ms, the packed workload 1.41 vs 1.05 ms).
-void choose_chain_tc(int path, int requested, int N, int H, int T, int dv,
-                     int C, bool packed, int* rows, int* parts, bool* fused) {
+void choose_chain_tc(int path, int requested, int N, int H, int T, int dk,
+                     int dv, int C, bool packed, int* rows, int* parts,
+                     bool* fused) {
   int sms = 148, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) {
     int v = 0;
@@ -161,10 +163,10 @@ void choose_chain_tc(int path, int requested, int N, int H, int T, int dv,
       sms = v;
   }
   int p64 = 1, p128 = 1;
-  const long long c64 = parts_cost_tc(requested, N, H, T, dv, C, packed, 64,
-                                      sms, &p64);
-  const long long c128 = parts_cost_tc(requested, N, H, T, dv, C, packed, 128,
-                                       sms, &p128);
+  const long long c64 = parts_cost_tc(requested, N, H, T, dk, dv, C, packed,
+                                      64, sms, &p64);
+  const long long c128 = parts_cost_tc(requested, N, H, T, dk, dv, C, packed,
+                                       128, sms, &p128);
   const bool whole = path == GDN_PATH_TCGEN05_WHOLE ||
                      (path != GDN_PATH_TCGEN05_SPLIT && c128 < c64);
   *rows = whole ? 128 : 64;
@@ -215,8 +217,10 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
   const bool tc_ok = bf16 && chunk_tc_supported(dk, dv, tokens, B, H);
   if ((path >= GDN_PATH_TCGEN05 || sub.on || kda) && !tc_ok)
     return GDN_ERR_UNSUPPORTED;
-  // KDA runs on the whole-state chain only (its column-wise state decay)
-  if (kda && (path == GDN_PATH_SIMT || path == GDN_PATH_TCGEN05_SPLIT))
+  // KDA runs on the whole-state chain only (its column-wise state decay),
+  // with its own preparation kernel for d_k = 128
+  if (kda && (path == GDN_PATH_SIMT || path == GDN_PATH_TCGEN05_SPLIT ||
+              dk != 128))
     return GDN_ERR_UNSUPPORTED;
   int* status = nullptr;
   if ((rc = current_status_ptr(&status)) != GDN_OK) return rc;
@@ -244,7 +248,7 @@ int run_chunk(const void* q, const void* k, const void* v, const float* g,
   bool fused = false;
   if (use_tc)
     choose_chain_tc(kda ? GDN_PATH_TCGEN05_WHOLE : path, sp_parts, B, H, T,
-                    dv, C, cu_seqlens != nullptr, &p.chain_rows, &parts,
+                    dk, dv, C, cu_seqlens != nullptr, &p.chain_rows, &parts,
                     &fused);
   else
     parts = choose_parts(sp_parts, B, H, T, dv, C, cu_seqlens != nullptr);
@@ -613,7 +617,7 @@ int gdn_kda_fwd_ex(const void* q, const void* k, const void* v,
   // nothing to compute but the state copy: the token-by-token kernel
   if (kernels == GDN_PATH_SIMT || B <= 0 || H <= 0 || T <= 0 || tokens <= 0 ||
       (kernels == GDN_PATH_AUTO &&
-       !gdn::chunk_tc_supported(dk, dv, tokens, B, H)))
+       (dk != 128 || !gdn::chunk_tc_supported(dk, dv, tokens, B, H))))
     return gdn_kda_fwd(q, k, v, g, beta, h0, out, hT, cu_seqlens, B, H, T, dk,
                        dv, stream);
   return gdn::run_chunk(q, k, v, g, beta, h0, out, hT, cu_seqlens, B, H, T, dk,

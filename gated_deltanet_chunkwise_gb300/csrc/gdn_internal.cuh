@@ -114,7 +114,9 @@ cudaError_t launch_sp_chain(const ChunkParams& p, cudaStream_t stream);
 // `buf` holds as many bytes as ws_end.
 cudaError_t launch_sp_scan(const ChunkParams& p, float* buf,
                            cudaStream_t stream, int* launches);
-// Tensor-core (tcgen05) path: bf16, dk = 128, dv in {64, 128}. A call takes
+// Tensor-core (tcgen05) path: bf16, dk in {64, 128} (64 on the 128 layout,
+// the keys' and queries' second block read as zeros), dv in {64, 128}
+// (KDA: dk = 128). A call takes
 // chunk_tc_workspace_bytes of workspace (bound with chunk_tc_bind_workspace),
 // runs launch_ut_prep once, then launch_chunk_tc for each pass.
 bool chunk_tc_supported(int dk, int dv, long long tokens, int N, int H);
@@ -139,7 +141,7 @@ int chunk_tc_nch_dense(const ChunkParams& p);
 cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream);
 // The same path in one launch with no workspace (one sub-sequence): a
 // cluster per (sequence, head) of a preparation CTA and a whole-state chain
-// CTA (bf16, dk = 128, dv in {64, 128}; not KDA).
+// CTA (bf16, dk in {64, 128}, dv in {64, 128}; not KDA).
 cudaError_t launch_chunk_fused(const ChunkParams& p, cudaStream_t stream);
 // Bytes of the hand-off ring the fused path needs (p.ring).
 size_t fused_ring_bytes(const ChunkParams& p);

@@ -135,7 +135,9 @@ int gdn_chunk_fwd_f32(const float* q, const float* k, const float* v,
  * gdn_chunk_fwd_ex -- gdn_chunk_fwd with explicit options.
  *   dtype      GDN_DTYPE_BF16 or GDN_DTYPE_F32 (q, k, v, out)
  *   variant    GDN_GATE_BEFORE_PREDICT or GDN_GATE_AFTER_PREDICT
- *   path       GDN_PATH_* (the GDN_PATH_TCGEN05* paths require bf16),
+ *   path       GDN_PATH_* (the GDN_PATH_TCGEN05* paths require bf16;
+ *              they serve dk = 64 on the dk = 128 kernels with the keys'
+ *              and queries' second 64 columns read as zeros),
  *              optionally OR GDN_SP_CHAIN or GDN_SP_SCAN (not both)
  *   sp_parts   sequence-parallel split: 0 = automatic, 1 = never split,
  *              P >= 2 = split every sequence into P sub-sequences of whole
@@ -167,7 +169,8 @@ int gdn_chunk_fwd_ex(const void* q, const void* k, const void* v,
  *   gate        bf16 [B, T, H, dv] (device) or NULL: no output gate
  *   eps         >= 0, added to the mean of squares
  *   path        GDN_PATH_AUTO or GDN_PATH_TCGEN05 (the same here),
- *               GDN_PATH_TCGEN05_SPLIT or GDN_PATH_TCGEN05_WHOLE
+ *               GDN_PATH_TCGEN05_SPLIT, GDN_PATH_TCGEN05_WHOLE or
+ *               GDN_PATH_TCGEN05_FUSED
  * Other arguments as gdn_chunk_fwd (decay before the prediction, automatic
  * sequence-parallel split). Served by the bf16 tensor-core path only:
  * dk = 128 and dv in {64, 128}; other shapes (and GDN_PATH_SIMT) return

@@ -96,7 +96,7 @@ def chunk(so, q=A, k=A + 0x1000, v=A + 0x2000, g=A + 0x3000, beta=A + 0x4000,
     (dict(dtype=1, path=3), UNSUPPORTED),
     (dict(dtype=1, path=4), UNSUPPORTED),
     (dict(dtype=1, path=5), UNSUPPORTED),
-    (dict(path=5), UNSUPPORTED),           # tensor-core shapes only (dk=64)
+    (dict(path=5, dv=32), UNSUPPORTED),    # tensor-core shapes only
     (dict(path=5, dk=128, dv=128, sp_parts=3), UNSUPPORTED),  # no split
     (dict(path=6), INVALID),
 ])

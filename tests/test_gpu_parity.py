@@ -302,6 +302,34 @@ def test_kernel_timing_counts_the_launches(lib, cuda_device):
     assert all(ms > 0 for _, ms in t.values())
 
 
+@pytest.mark.parametrize("path", [TC] + CHAINS + [FUSED])
+@pytest.mark.parametrize("dv", [64, 128])
+def test_tensor_core_dk64(lib, cuda_device, dv, path):
+    # d_k = 64 runs on the d_k = 128 kernels with the keys' and queries'
+    # second 64 columns read as zeros: every state row and column beyond
+    # d_k must stay out of h0 / hT and the split's workspace
+    d = inputs.chunk_inputs(2, 3, 64 * 4 + 29, 64, dv, dtype="bf16", seed=20,
+                            h0=True)
+    check(lib, cuda_device, d, "bf16", variant=1 if path == 4 else 0,
+          path=path)
+
+
+@pytest.mark.parametrize("path", CHAINS)
+@pytest.mark.parametrize("parts", [2, 5])
+def test_tensor_core_dk64_sequence_parallel(lib, cuda_device, parts, path):
+    d = inputs.chunk_inputs(1, 2, 64 * 9 + 40, 64, 128, dtype="bf16", seed=21,
+                            h0=True)
+    check(lib, cuda_device, d, "bf16", path=path, sp_parts=parts)
+
+
+@pytest.mark.parametrize("path", CHAINS + [FUSED])
+def test_tensor_core_dk64_packed(lib, cuda_device, path):
+    lengths = [70, 0, 1, 64, 200, 3, 129]
+    d = inputs.chunk_inputs(len(lengths), 2, 0, 64, 64, dtype="bf16",
+                            seed=22, h0=True, lengths=lengths)
+    check(lib, cuda_device, d, "bf16", path=path)
+
+
 def test_fused_path_rejects_a_split(lib, cuda_device):
     d = to_dev(inputs.chunk_inputs(1, 2, 300, 128, 128, dtype="bf16", seed=6),
                cuda_device)
