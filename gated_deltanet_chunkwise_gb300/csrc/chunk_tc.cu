@@ -669,7 +669,9 @@ __device__ __forceinline__ uint32_t bar_count(int b) {
   }
 }
 
-template <int VARIANT>
+// EPI: the fused sublayer's epilogue (RMS normalisation over d_v, output
+// gate) compiled in; the plain forward pass is instantiated without it.
+template <int VARIANT, bool EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     chunk_tc_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tmq,
                     const __grid_constant__ CUtensorMap tmk,
@@ -704,8 +706,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // fused epilogue on this CTA's outputs; with d_v = 128 the two CTAs of a
   // (sequence, head, part) form a cluster and exchange the per-row sums of
   // squares of their halves of each output row
-  const bool epi = p.epilogue && emit;
-  const bool clustered = p.epilogue && dv == 128;
+  const bool epi = EPI && p.epilogue && emit;
+  const bool clustered = EPI && p.epilogue && dv == 128;
   const bool has_gate = epi && p.gate_z != nullptr;
   long long bos, eos;
   if (!sequence_range(p, n, bos, eos)) return;
@@ -2906,8 +2908,10 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream) {
     return e;
   };
   return p.variant == GDN_GATE_AFTER_PREDICT
-             ? launch(chunk_tc_kernel<GDN_GATE_AFTER_PREDICT>)
-             : launch(chunk_tc_kernel<GDN_GATE_BEFORE_PREDICT>);
+             ? (p.epilogue ? launch(chunk_tc_kernel<GDN_GATE_AFTER_PREDICT, true>)
+                           : launch(chunk_tc_kernel<GDN_GATE_AFTER_PREDICT, false>))
+             : (p.epilogue ? launch(chunk_tc_kernel<GDN_GATE_BEFORE_PREDICT, true>)
+                           : launch(chunk_tc_kernel<GDN_GATE_BEFORE_PREDICT, false>));
 }
 
 }  // namespace gdn
