@@ -29,10 +29,14 @@
 //
 // Warp roles of chunk_tc_kernel (kChainWarps + 3 warps; with 8 chain warps
 // 352 threads): the chain warps hold the state rows (those with lane quarter
-// 2-3 also U rows, 0-1 output rows; each takes 32 of the 64 columns; one
-// U-row thread issues the Delta product right after the barrier that
-// completes its operand), then the TMA producer, the P U warp and the U0 /
-// [Q;-W] S^T warp (woken when the state is in shared memory). Operand tiles
+// 2-3 also U rows, 0-1 output rows; each takes 32 of the 64 columns), then
+// the TMA producer, the P U warp and the U0 / [Q;-W] S^T / Delta warp.
+// Only warps 4k and 4k + 1 reach TMEM lanes 0-63 (the output rows), so the
+// U-row warps take the elementwise work of the fused output gate (the
+// logits of the next chunk turned into sigmoids in shared memory) to keep
+// the output-row warps within a chunk's period. The MMA warp is woken by
+// barriers: the state in shared memory for [Q;-W] S^T, diag(e^{G_L-G}) U
+// for the Delta product. Operand tiles
 // are bf16 with the 128-byte swizzle and arrive in a two-stage ring, each
 // stage in two parts; whole output tiles leave by TMA store. Every wait is
 // bounded; a CTA that gives up records GDN_ERR_TIMEOUT, drains its MMAs,
@@ -606,9 +610,6 @@ constexpr int kCW = 64 / (kChainWarps / 4);
 constexpr int kWarpProducer = kChainWarps, kWarpPU = kChainWarps + 1,
               kWarpMMA = kChainWarps + 2;
 constexpr int kThreads = 32 * (kChainWarps + 3);
-// The chain thread that issues the Delta product right after the barrier
-// that completes diag(e^{G_L-G}) U (a U-row thread: it waits there anyway).
-constexpr int kIssuerU = 64;
 // Stage: per 64-column block of d_k, three 64-row groups K | Q | -W: [Q;-W]
 // is a 128-row K-major tile and K alone the M-major operand of the Delta
 // product. Then V, a zero block and T_U ([0;T_U] is a 128-row tile), P
@@ -642,7 +643,7 @@ enum {
   B_FULLA0, B_FULLA1, B_FULLB0, B_FULLB1, B_EMPTY0, B_EMPTY1, B_SREADY,
   B_D1FULL0, B_D1FULL1,
   B_UREADY, B_D2FULL, B_D3FULL0, B_D3FULL1, B_D3FREE0, B_D3FREE1, B_DRAIN_C,
-  B_DRAIN_S, B_XS0, B_XS1, NBARS
+  B_DRAIN_S, B_XS0, B_XS1, B_UDREADY, B_GREADY0, B_GREADY1, NBARS
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -657,13 +658,15 @@ constexpr uint32_t ID_MNMN = idesc_bf16(128, 64, true, true);
 
 __device__ __forceinline__ uint32_t bar_count(int b) {
   switch (b) {
-    // the U issuer's and the P U warp's MMA commits (the state issuer's
-    // products have completed before the U issuer's), one per chain warp
-    // (each chain warp arrives once, after its lanes' writes and fences)
+    // the MMA warp's commit after the Delta product and the P U warp's
+    // commit, one per chain warp (each chain warp arrives once, after its
+    // lanes' reads)
     case B_EMPTY0: case B_EMPTY1: return 2 + kChainThreads / 32;
     case B_SREADY: return kChainThreads / 32;
-    case B_UREADY: case B_D3FREE0: case B_D3FREE1: return kChainThreads / 64;
-    case B_DRAIN_C: return 2;  // the state issuer warp and the U issuer
+    // the U-row warps (UREADY, UDREADY, GREADY) or the output-row warps
+    case B_UREADY: case B_D3FREE0: case B_D3FREE1: case B_UDREADY:
+    case B_GREADY0: case B_GREADY1:
+      return kChainThreads / 64;
     // the partner's 64 row sums, counted in bytes (armed once per use)
     default: return 1;
   }
@@ -703,11 +706,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!value_rows && !(split_tail && row0 < dv + dkr)) return;
   const bool scale_rows = !value_rows;
   const bool emit = (p.mode == kModeOutput) || part == 0;
-  // fused epilogue on this CTA's outputs; with d_v = 128 the two CTAs of a
-  // (sequence, head, part) form a cluster and exchange the per-row sums of
-  // squares of their halves of each output row
+  // fused epilogue on this CTA's outputs; for the RMS normalisation with
+  // d_v = 128 the two CTAs of a (sequence, head, part) form a cluster and
+  // exchange the per-row sums of squares of their halves of each output row
   const bool epi = EPI && p.epilogue && emit;
-  const bool clustered = EPI && p.epilogue && dv == 128;
+  const bool clustered = EPI && p.epilogue && p.norm_w && dv == 128;
   const bool has_gate = epi && p.gate_z != nullptr;
   long long bos, eos;
   if (!sequence_range(p, n, bos, eos)) return;
@@ -830,12 +833,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= U0 and [Q;-W] S^T =================
     if (lane == 0 && nloc > 0) {
       // All from one thread so that they execute in issue order: U0 =
-      // [0;T_U] V starts a chunk's accumulator and [Q;-W] S^T is added once
-      // the state is in shared memory. The next chunk's U0 goes in as soon
-      // as this chunk's Delta product has completed, so that it runs while
-      // the chain warps update the state. The accumulator of chunk i + 1 was
-      // last read (H and U of chunk i - 1) before the chain warps signalled
-      // the state of chunk i - 1, which this thread has waited for.
+      // [0;T_U] V starts a chunk's accumulator, [Q;-W] S^T is added once
+      // the state is in shared memory and the Delta product K^T diag(e^{G_L-
+      // G}) U goes in once the U rows have written its operand. The next
+      // chunk's U0 goes in right behind this chunk's [Q;-W] S^T if its
+      // operands have landed (it then runs while U is read out), else behind
+      // the Delta product. The accumulator of chunk i + 1 was last read (H
+      // and U of chunk i - 1) before the chain warps signalled the state of
+      // chunk i, which this thread has waited for. Barriers on the chain are
+      // polled rather than waited with suspension.
       auto issue_u0 = [&](int j) {
         const int s = j & 1;
         if (!mbar_wait(&bars[B_FULLA0 + s], (j >> 1) & 1, abort_flag)) return false;
@@ -848,8 +854,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = issue_u0(0);
       for (int i = 0; ok && i < nloc; ++i) {
         const int b = i & 1;
-        if (!mbar_wait(&bars[B_SREADY], i & 1, abort_flag) ||
-            !mbar_wait(&bars[B_FULLB0 + b], (i >> 1) & 1, abort_flag))
+        // the stage (landed long before) first, then the state barrier
+        if (!mbar_wait(&bars[B_FULLB0 + b], (i >> 1) & 1, abort_flag) ||
+            !mbar_spin(&bars[B_SREADY], i & 1, abort_flag))
           break;
         tc_fence_after();
         const uint32_t st = stage(i);
@@ -859,8 +866,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_bf16_run<4>(tmem + TM_D1 + 64 * b, sdesc(st + ST_Q + ST_CB, 16, 1024),
                         32, sb + (8192 >> 4), 2048, ID_KMN, true);
         mma_commit(&bars[B_D1FULL0 + b]);
-        if (i + 1 < nloc)
-          ok = mbar_wait(&bars[B_D2FULL], i & 1, abort_flag) && issue_u0(i + 1);
+        const bool u0_now =
+            i + 1 < nloc &&
+            mbar_test(&bars[B_FULLA0 + (b ^ 1)], ((i + 1) >> 1) & 1);
+        if (u0_now && !issue_u0(i + 1)) break;
+        if (!mbar_spin(&bars[B_UDREADY], i & 1, abort_flag)) break;
+        tc_fence_after();
+        mma_bf16_run<4>(tmem + TM_D2, sdesc(st + ST_K, ST_CB, 1024), 2048,
+                        sdesc(base + OFF_UD, 8192, 1024), 2048, ID_MNMN, false);
+        mma_commit(&bars[B_D2FULL]);
+        mma_commit(&bars[B_EMPTY0 + b]);
+        if (i + 1 < nloc && !u0_now) ok = issue_u0(i + 1);
       }
       mma_commit(&bars[B_DRAIN_C]);
       wait_ignoring_abort(&bars[B_DRAIN_C], 0);
@@ -868,9 +884,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpPU) {
     // ================= P U, off the chain =================
     if (lane == 0 && nloc > 0) {
+      // P U of chunk j goes in once the chunk's Delta product has
+      // completed, so that the two never share the tensor pipe (the Delta
+      // product is on the chain). No phase of D2FULL can pass unseen: the
+      // Delta product of chunk j + 1 waits for the U rows of chunk j + 1,
+      // and they wait for this P U first.
       for (int j = 0; j < nloc; ++j) {
         const int b = j & 1;
         if (!mbar_wait(&bars[B_UREADY], j & 1, abort_flag) ||
+            !mbar_wait(&bars[B_D2FULL], j & 1, abort_flag) ||
             !mbar_wait(&bars[B_FULLB0 + b], (j >> 1) & 1, abort_flag))
           break;
         // P U of chunk j - 2 has been read out of this accumulator
@@ -891,16 +913,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= chain warps =================
     // lane quarter qw = warp & 3 (TMEM lanes 32 qw ..), column group cg:
     // state rows ct = 32 qw + lane (d_k index), columns cols .. cols + kCW - 1;
-    // qw >= 2 also U rows ct - 64, qw < 2 output rows ct. Thread kIssuerU
-    // issues the Delta product right after the barrier that completes its
-    // operand.
+    // qw >= 2 also U rows ct - 64, qw < 2 output rows ct.
     const int qw = warp & 3, cg = warp >> 2;
     const int ct = 32 * qw + lane;
     const uint32_t lanes = (uint32_t)(32 * qw) << 16;
     const uint32_t cols = kCW * cg;
     const int chunk0 = cols / 8;  // first 16-byte chunk of the columns
     const bool u_rows = qw >= 2;
-    const bool issuer_u = tid == kIssuerU;
     uint8_t* s_tile = sm + OFF_S;
     float S[kCW];
     if (scale_rows) {
@@ -934,11 +953,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars[B_SREADY]);
+    // Output gate: a U-row thread turns the gate logits of chunk j (row
+    // ct - 64 of its stage tile, the thread's kCW columns, the same slice its
+    // output-row twin reads) into sigmoid(z) in place and its warp arrives on
+    // GREADY of the stage. The tile of chunk j + 2 reuses the stage only
+    // after the output rows have read chunk j's and released the stage, so
+    // one barrier per stage sees its phases in order.
+    auto gate_to_sigmoid = [&](int j, bool okj) {
+      const int sj = j & 1;
+      okj = okj && mbar_wait(&bars[B_FULLB0 + sj], (j >> 1) & 1, abort_flag);
+      if (okj) {
+        uint8_t* gt = sm + OFF_STAGE + sj * STAGE_BYTES + ST_G;
+#pragma unroll
+        for (int c = 0; c < kCW / 8; ++c) {
+          uint4* q = reinterpret_cast<uint4*>(gt + sw128(ct - 64, chunk0 + c));
+          float f[8];
+          unpack_bf16x8(*q, f);
+          uint4 w;
+          w.x = pack_bf16x2(sigmoid_approx(f[0]), sigmoid_approx(f[1]));
+          w.y = pack_bf16x2(sigmoid_approx(f[2]), sigmoid_approx(f[3]));
+          w.z = pack_bf16x2(sigmoid_approx(f[4]), sigmoid_approx(f[5]));
+          w.w = pack_bf16x2(sigmoid_approx(f[6]), sigmoid_approx(f[7]));
+          *q = w;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_GREADY0 + sj]);
+    };
+    if (has_gate && u_rows && nloc > 0) gate_to_sigmoid(0, true);
     // [Q;-W] S^T accumulated onto U0: H = Q S^T (rows 0-63), U (64-127)
     // Fused epilogue on one chunk's output rows (o: this thread's kCW
-    // columns of row r): o <- o / sqrt(mean(o^2) + eps) * w, then *
-    // sigmoid(gate). Returns false, the same on every output thread, when a
-    // wait for the partner CTA gave up.
+    // columns of row r; gzv: sigmoid of the gate logits, bf16): o <- o /
+    // sqrt(mean(o^2) + eps) * w, then * sigmoid(gate). Returns false, the
+    // same on every output thread, when a wait for the partner CTA gave up.
     const float* ep_w = reinterpret_cast<const float*>(sm + OFF_EPW);
     float* ep_red = reinterpret_cast<float*>(sm + OFF_EPRED);
     float* ep_x = reinterpret_cast<float*>(sm + OFF_EPX);
@@ -981,11 +1028,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           float f[8];
           unpack_bf16x8(gzv[c8], f);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[8 * c8 + e] *= sigmoid_approx(f[e]);
+          for (int e = 0; e < 8; ++e) o[8 * c8 + e] *= f[e];
         }
       }
       return okp;
     };
+    // The loop has no early exit: a failed wait only clears `ok` (made
+    // warp-uniform before every warp-collective TMEM read), so every warp
+    // passes every named barrier of every chunk and no group can be left
+    // waiting at one; the work of a failed chunk is skipped.
     bool ok = true;
     for (int i = 0; i < nloc; ++i) {
       const int b = i & 1;
@@ -998,40 +1049,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           reinterpret_cast<const float*>(sm + OFF_STAGE + b * STAGE_BYTES + ST_CV);
       const float gam = cv[CV_GAMMA];
       const float rowf = cv[(u_rows ? CV_DEC : CV_EG) + (ct & 63)];
-      // the output row's gate logits, copied out before the stage is freed
-      uint4 gz[kCW / 8];
-      if (has_gate && !u_rows) {
-        ok = ok && mbar_wait(&bars[B_FULLB0 + b], (i >> 1) & 1, abort_flag);
-        const uint8_t* gt = sm + OFF_STAGE + b * STAGE_BYTES + ST_G;
-#pragma unroll
-        for (int c = 0; c < kCW / 8; ++c)
-          gz[c] = *reinterpret_cast<const uint4*>(gt + sw128(ct, chunk0 + c));
-      }
+      // with an output gate the output rows read its logits at read-out and
+      // release the stage only then (nothing is held in registers across
+      // the chunk)
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_EMPTY0 + b]);
+      if (lane == 0 && !(has_gate && !u_rows)) mbar_arrive(&bars[B_EMPTY0 + b]);
       float hq[kCW];  // H = Q S^T of this chunk (output rows)
       if (!u_rows) {
         // read H as soon as it is complete: the accumulator is reused by the
         // U0 product of the chunk after next, issued after this chunk's state
         // barrier
-        bool okh = ok && mbar_wait(&bars[B_D1FULL0 + b], (i >> 1) & 1, abort_flag);
-        okh = bar_and(4, kChainThreads / 2, okh);
-        if (okh) {
+        ok = __all_sync(0xffffffffu,
+                        ok && mbar_wait(&bars[B_D1FULL0 + b], (i >> 1) & 1,
+                                        abort_flag));
+        if (ok) {
           tc_fence_after();
           tmem_ldn<kCW>(tmem + TM_D1 + 64 * b + lanes + cols, hq);
           tmem_ld_wait();
           tc_fence_before();
         }
-        ok = okh;
       }
       if (u_rows) {
         // U = U0 - W S^T (rows 64-127 of the accumulator)
         const int r = ct - 64;
-        bool ok1 = ok && mbar_wait(&bars[B_D1FULL0 + b], (i >> 1) & 1, abort_flag);
         // the U tile is free once the previous chunk's P U has completed
-        ok1 = ok1 && (i == 0 || mbar_wait(&bars[B_D3FULL0 + (b ^ 1)],
-                                          ((i - 1) >> 1) & 1, abort_flag));
-        ok1 = bar_and(3, kChainThreads / 2, ok1);
+        // (long before U itself: waited first, off the chain)
+        bool ok1 = ok && (i == 0 || mbar_wait(&bars[B_D3FULL0 + (b ^ 1)],
+                                              ((i - 1) >> 1) & 1, abort_flag));
+        ok1 = ok1 && mbar_wait(&bars[B_D1FULL0 + b], (i >> 1) & 1, abort_flag);
+        ok1 = __all_sync(0xffffffffu, ok1);
         float u[kCW];
         if (ok1) {
           tc_fence_after();
@@ -1043,17 +1089,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           store_cols_bf16<kCW>(sm + OFF_UD, r, chunk0, ud);
           fence_proxy_async();
         }
-        ok1 = bar_and(3, kChainThreads / 2, ok1);  // diag(e^{G_L-G}) U complete
-        if (ok1 && issuer_u &&
-            mbar_wait(&bars[B_FULLB0 + b], (i >> 1) & 1, abort_flag)) {
-          // Delta = K^T diag(e^{G_L-G}) U
-          tc_fence_after();
-          const uint32_t st = stage(i);
-          mma_bf16_run<4>(tmem + TM_D2, sdesc(st + ST_K, ST_CB, 1024), 2048,
-                          sdesc(base + OFF_UD, 8192, 1024), 2048, ID_MNMN, false);
-          mma_commit(&bars[B_D2FULL]);
-          mma_commit(&bars[B_EMPTY0 + b]);
-        }
+        // diag(e^{G_L-G}) U complete in this warp: the MMA warp issues the
+        // Delta product once all U-row warps have arrived
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_UDREADY]);
         if (ok1) {
           // U itself only feeds P U, off the chain
           store_cols_bf16<kCW>(sm + OFF_U, r, chunk0, u);
@@ -1064,28 +1103,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ok = ok1;
       }
-      bool ok3 = ok && mbar_wait(&bars[B_D2FULL], i & 1, abort_flag);
-      if (!bar_and(2, kChainThreads, ok3)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      {
+      const bool ok3 = __all_sync(
+          0xffffffffu, ok && mbar_wait(&bars[B_D2FULL], i & 1, abort_flag));
+      ok = ok3;
+      if (ok3) {
+        tc_fence_after();
         float dl[kCW];
         tmem_ldn<kCW>(tmem + TM_D2 + lanes + cols, dl);
         tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < kCW; ++c) S[c] = fmaf(gam, S[c], dl[c]);
+        store_cols_bf16<kCW>(s_tile, ct, chunk0, S);
+        fence_proxy_async();
+        tc_fence_before();
       }
-      store_cols_bf16<kCW>(s_tile, ct, chunk0, S);
-      fence_proxy_async();
-      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_SREADY]);
+      if (has_gate && u_rows && i + 1 < nloc) gate_to_sigmoid(i + 1, ok);
       if (!u_rows) {
         // O = e^{G_r} H + P U, through a shared-memory tile and a TMA store
         // for a whole chunk, direct stores for a partial one
         const int r = ct;
+        uint4 gz[kCW / 8];  // sigmoid of the output row's gate logits
+        if (has_gate) {
+          ok = ok && mbar_wait(&bars[B_GREADY0 + b], (i >> 1) & 1, abort_flag);
+          const uint8_t* gt = sm + OFF_STAGE + b * STAGE_BYTES + ST_G;
+#pragma unroll
+          for (int c = 0; c < kCW / 8; ++c)
+            gz[c] = ok ? *reinterpret_cast<const uint4*>(gt + sw128(ct, chunk0 + c))
+                       : make_uint4(0, 0, 0, 0);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[B_EMPTY0 + b]);
+        }
         bool ok4 = ok && mbar_wait(&bars[B_D3FULL0 + b], (i >> 1) & 1, abort_flag);
         if (tid == 0) bulk_wait_read();  // previous output tile read out
         ok4 = bar_and(4, kChainThreads / 2, ok4);
@@ -1151,10 +1200,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kCW / 4; ++c)
           dst[c] = make_float4(S[4 * c], S[4 * c + 1], S[4 * c + 2], S[4 * c + 3]);
       }
-    }
-    if (issuer_u) {
-      mma_commit(&bars[B_DRAIN_C]);
-      wait_ignoring_abort(&bars[B_DRAIN_C], 0);
     }
   }
 
@@ -2876,9 +2921,10 @@ cudaError_t launch_chunk_tc(const ChunkParams& p, cudaStream_t stream) {
     timing_stop(t, stream, e);
     return e;
   }
-  // the fused epilogue pairs the two CTAs of each (sequence, head, part)
-  // when d_v = 128 (grid.x is then 2 or 4)
-  const bool clustered = p.epilogue && p.dv == 128;
+  // the fused epilogue's RMS normalisation pairs the two CTAs of each
+  // (sequence, head, part) when d_v = 128 (grid.x is then 2 or 4); the
+  // output gate alone needs no partner
+  const bool clustered = p.epilogue && p.norm_w && p.dv == 128;
   auto launch = [&](auto kern) {
     cudaError_t e = cudaFuncSetAttribute(
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
