@@ -63,21 +63,24 @@ GDN_HD inline float ldin(const void* p, size_t i) {
 template <class X, class F>
 GDN_HD void gemm(X& x, int M, int N, int K, const float* A, int ars, int acs,
                  const float* B, int brs, int bcs, F epi) {
-  const int nt_j = N / 4, ntiles = (M / 4) * nt_j;
+  // thread (ti, tj) owns rows ti + m*M/4 and columns tj + n*N/4: neighbouring
+  // threads read neighbouring columns of B (coalesced, and conflict-free in
+  // shared memory when B's column stride is 1 or an odd number of floats)
+  const int tm = M / 4, tn = N / 4, ntiles = tm * tn;
   for (int tile = x.tid; tile < ntiles; tile += x.nt) {
-    const int i0 = (tile / nt_j) * 4, j0 = (tile % nt_j) * 4;
+    const int ti = tile / tn, tj = tile % tn;
     float acc[4][4];
     for (int i = 0; i < 4; ++i)
       for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
     for (int kk = 0; kk < K; ++kk) {
       float a[4], b[4];
-      for (int i = 0; i < 4; ++i) a[i] = A[(i0 + i) * ars + kk * acs];
-      for (int j = 0; j < 4; ++j) b[j] = B[kk * brs + (j0 + j) * bcs];
+      for (int i = 0; i < 4; ++i) a[i] = A[(ti + i * tm) * ars + kk * acs];
+      for (int j = 0; j < 4; ++j) b[j] = B[kk * brs + (tj + j * tn) * bcs];
       for (int i = 0; i < 4; ++i)
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
     for (int i = 0; i < 4; ++i)
-      for (int j = 0; j < 4; ++j) epi(i0 + i, j0 + j, acc[i][j]);
+      for (int j = 0; j < 4; ++j) epi(ti + i * tm, tj + j * tn, acc[i][j]);
   }
 }
 
@@ -89,15 +92,16 @@ GDN_HD inline int chunk_len(const Args& a, int c) {
 // ---- 1. per (chunk, head): G, T = (I + A)^{-1}, W, U0, P -----------------
 // smem floats: K, Q [C][DK], V [C][DV], A [C][C], T [C][C], G, beta [C]
 template <int DK, int DV>
-constexpr int prep_smem() { return 2 * C * DK + C * DV + 2 * C * C + 2 * C; }
+constexpr int prep_smem() { return C * (DK + 1) + C * DK + C * DV + 2 * C * C + 2 * C; }
 
 template <int DK, int DV, bool BF, class X>
 GDN_HD void prep_body(X& x, const Args& a, int z) {
   const int h = z % a.H, nc = z / a.H, c = nc % a.nch, n = nc / a.nch;
   const int L = chunk_len(a, c);
   const long long t0 = (long long)n * a.T + (long long)c * C;
+  constexpr int LK = DK + 1;  // padded: K is read transposed
   float* sK = x.smem;
-  float* sQ = sK + C * DK;
+  float* sQ = sK + C * LK;
   float* sV = sQ + C * DK;
   float* sA = sV + C * DV;
   float* sT = sA + C * C;
@@ -107,7 +111,7 @@ GDN_HD void prep_body(X& x, const Args& a, int z) {
     const int t = i / DK, cc = i % DK;
     const bool in = t < L;
     const size_t r = ((size_t)(t0 + t) * a.H + h) * DK + cc;
-    sK[i] = in ? ldin<BF>(a.k, r) : 0.f;
+    sK[t * LK + cc] = in ? ldin<BF>(a.k, r) : 0.f;
     sQ[i] = in ? ldin<BF>(a.q, r) : 0.f;
   }
   for (int i = x.tid; i < C * DV; i += x.nt) {
@@ -126,19 +130,51 @@ GDN_HD void prep_body(X& x, const Args& a, int z) {
   for (int t = x.tid; t < C; t += x.nt) G[t] = sG[t];
   // A and P
   float* P = a.P + (size_t)z * C * C;
-  gemm(x, C, C, DK, sK, DK, 1, sK, 1, DK, [&](int r, int s, float kk) {
+  gemm(x, C, C, DK, sK, LK, 1, sK, 1, LK, [&](int r, int s, float kk) {
     sA[r * C + s] = r > s ? sB[r] * kk * expf(sG[r] - sG[s]) : 0.f;
   });
-  gemm(x, C, C, DK, sQ, DK, 1, sK, 1, DK, [&](int r, int s, float qk) {
+  gemm(x, C, C, DK, sQ, DK, 1, sK, 1, LK, [&](int r, int s, float qk) {
     P[r * C + s] = r >= s ? qk * expf(sG[r] - sG[s]) : 0.f;
   });
   x.sync();
-  // T = (I + A)^{-1}, row by row (T is unit lower triangular)
-  for (int r = 0; r < C; ++r) {
-    for (int j = x.tid; j < C; j += x.nt) {
+  // T = (I + A)^{-1} (unit lower triangular) by 16 x 16 blocks: the four
+  // diagonal blocks by substitution side by side (16 steps), then the
+  // blocks below the diagonal one sub-diagonal at a time:
+  //   T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj   (i > j)
+  for (int i = x.tid; i < C * C; i += x.nt) {
+    const int r = i / C, c2 = i % C;
+    if (r / 16 != c2 / 16) sT[i] = 0.f;
+  }
+  for (int r = 0; r < 16; ++r) {
+    for (int e = x.tid; e < 64; e += x.nt) {
+      const int b = e / 16, j = e % 16, R = 16 * b + r, J = 16 * b + j;
       float t = r == j ? 1.f : 0.f;
-      for (int s = j; s < r; ++s) t = fmaf(-sA[r * C + s], sT[s * C + j], t);
-      sT[r * C + j] = j <= r ? t : 0.f;
+      for (int s = j; s < r; ++s) t = fmaf(-sA[R * C + 16 * b + s], sT[(16 * b + s) * C + J], t);
+      sT[R * C + J] = j <= r ? t : 0.f;
+    }
+    x.sync();
+  }
+  float* sM = sA;  // scratch rows: A's blocks on and above the diagonal are
+                   // not read again (A_ik with k < i only)
+  for (int dd = 1; dd < 4; ++dd) {
+    // M_ij = sum_k A_ik T_kj for the blocks (i, j = i - dd), into the
+    // (j, i) block of the scratch (above the diagonal)
+    for (int e = x.tid; e < (4 - dd) * 256; e += x.nt) {
+      const int bi = dd + e / 256, bj = bi - dd, r = (e % 256) / 16, c2 = e % 16;
+      const int R = 16 * bi + r, J = 16 * bj + c2;
+      float m = 0.f;
+      for (int k = 16 * bj; k < 16 * bi; ++k) m = fmaf(sA[R * C + k], sT[k * C + J], m);
+      sM[(16 * bj + r) * C + 16 * bi + c2] = m;
+    }
+    x.sync();
+    // T_ij = -T_ii M_ij
+    for (int e = x.tid; e < (4 - dd) * 256; e += x.nt) {
+      const int bi = dd + e / 256, bj = bi - dd, r = (e % 256) / 16, c2 = e % 16;
+      const int R = 16 * bi + r;
+      float t = 0.f;
+      for (int k = 0; k <= r; ++k)
+        t = fmaf(sT[R * C + 16 * bi + k], sM[(16 * bj + k) * C + 16 * bi + c2], t);
+      sT[R * C + 16 * bj + c2] = -t;
     }
     x.sync();
   }
@@ -147,14 +183,14 @@ GDN_HD void prep_body(X& x, const Args& a, int z) {
   // W = T diag(beta e^G) K, U0 = T diag(beta) V: scale the rows in place
   x.sync();
   for (int i = x.tid; i < C * DK; i += x.nt) {
-    const int t = i / DK;
-    sK[i] *= sB[t] * expf(sG[t]);
+    const int t = i / DK, cc = i % DK;
+    sK[t * LK + cc] *= sB[t] * expf(sG[t]);
   }
   for (int i = x.tid; i < C * DV; i += x.nt) sV[i] *= sB[i / DV];
   x.sync();
   float* W = a.W + (size_t)z * C * DK;
   float* U0 = a.U0 + (size_t)z * C * DV;
-  gemm(x, C, DK, C, sT, C, 1, sK, DK, 1, [&](int t, int cc, float s) { W[t * DK + cc] = s; });
+  gemm(x, C, DK, C, sT, C, 1, sK, LK, 1, [&](int t, int cc, float s) { W[t * DK + cc] = s; });
   gemm(x, C, DV, C, sT, C, 1, sV, DV, 1, [&](int t, int cc, float s) { U0[t * DV + cc] = s; });
 }
 
@@ -162,20 +198,21 @@ GDN_HD void prep_body(X& x, const Args& a, int z) {
 // one CTA per (RB value rows, head, sequence); smem: W, Kbar [C][DK],
 // U0 [C][RB], S [RB][DK], U [C][RB], Snew [RB][DK]
 template <int DK, int RB>
-constexpr int fwd_smem() { return 2 * C * DK + 2 * C * RB + 2 * RB * DK; }
+constexpr int fwd_smem() { return 2 * C * DK + 2 * C * RB + 2 * RB * (DK + 1); }
 
 template <int DK, int DV, int RB, bool BF, class X>
 GDN_HD void fwd_body(X& x, const Args& a, int rb, int h, int n) {
+  constexpr int LS = DK + 1;  // padded: S is read transposed
   float* sW = x.smem;
   float* sKb = sW + C * DK;
   float* sU0 = sKb + C * DK;
   float* sS = sU0 + C * RB;
-  float* sU = sS + RB * DK;
+  float* sU = sS + RB * LS;
   float* sSn = sU + C * RB;
   const int row0 = rb * RB;
   for (int i = x.tid; i < RB * DK; i += x.nt) {
     const int j = i / DK, cc = i % DK;
-    sS[i] = a.h0 ? a.h0[(((size_t)n * a.H + h) * DK + cc) * DV + row0 + j] : 0.f;
+    sS[j * LS + cc] = a.h0 ? a.h0[(((size_t)n * a.H + h) * DK + cc) * DV + row0 + j] : 0.f;
   }
   for (int c = 0; c < a.nch; ++c) {
     const int z = (n * a.nch + c) * a.H + h, L = chunk_len(a, c);
@@ -193,11 +230,12 @@ GDN_HD void fwd_body(X& x, const Args& a, int rb, int h, int n) {
       sU0[i] = a.U0[(size_t)z * C * DV + t * DV + row0 + j];
     }
     float* Sg = a.S + (size_t)z * DV * DK;
-    for (int i = x.tid; i < RB * DK; i += x.nt) Sg[(size_t)row0 * DK + i] = sS[i];
+    for (int i = x.tid; i < RB * DK; i += x.nt)
+      Sg[(size_t)row0 * DK + i] = sS[(i / DK) * LS + i % DK];
     x.sync();
     // U = U0 - W S^T (C x RB)
     float* Ug = a.U + (size_t)z * C * DV;
-    gemm(x, C, RB, DK, sW, DK, 1, sS, 1, DK, [&](int t, int j, float ws) {
+    gemm(x, C, RB, DK, sW, DK, 1, sS, 1, LS, [&](int t, int j, float ws) {
       const float u = sU0[t * RB + j] - ws;
       sU[t * RB + j] = u;
       Ug[t * DV + row0 + j] = u;
@@ -206,32 +244,33 @@ GDN_HD void fwd_body(X& x, const Args& a, int rb, int h, int n) {
     // S <- gamma S + U^T Kbar (RB x DK)
     const float gam = expf(GL);
     gemm(x, RB, DK, C, sU, 1, RB, sKb, DK, 1, [&](int j, int cc, float s) {
-      sSn[j * DK + cc] = fmaf(gam, sS[j * DK + cc], s);
+      sSn[j * LS + cc] = fmaf(gam, sS[j * LS + cc], s);
     });
     x.sync();
-    for (int i = x.tid; i < RB * DK; i += x.nt) sS[i] = sSn[i];
+    for (int i = x.tid; i < RB * LS; i += x.nt) sS[i] = sSn[i];
   }
 }
 
 // ---- 3. reverse chain: exit gradient dS' and dU of every chunk -----------
 // smem: P [C][C], dO [C][RB], Kbar, Qg, W [C][DK], dS, dSn [RB][DK], dU [C][RB]
 template <int DK, int RB>
-constexpr int rev_smem() { return C * C + 2 * C * RB + 3 * C * DK + 2 * RB * DK; }
+constexpr int rev_smem() { return C * C + 2 * C * RB + 3 * C * DK + 2 * RB * (DK + 1); }
 
 template <int DK, int DV, int RB, bool BF, class X>
 GDN_HD void rev_body(X& x, const Args& a, int rb, int h, int n) {
+  constexpr int LD = DK + 1;  // padded: dS is read transposed
   float* sP = x.smem;
   float* sO = sP + C * C;
   float* sKb = sO + C * RB;
   float* sQg = sKb + C * DK;
   float* sW = sQg + C * DK;
   float* sD = sW + C * DK;
-  float* sDn = sD + RB * DK;
-  float* sdU = sDn + RB * DK;
+  float* sDn = sD + RB * LD;
+  float* sdU = sDn + RB * LD;
   const int row0 = rb * RB;
   for (int i = x.tid; i < RB * DK; i += x.nt) {
     const int j = i / DK, cc = i % DK;
-    sD[i] = a.dhT ? a.dhT[(((size_t)n * a.H + h) * DK + cc) * DV + row0 + j] : 0.f;
+    sD[j * LD + cc] = a.dhT ? a.dhT[(((size_t)n * a.H + h) * DK + cc) * DV + row0 + j] : 0.f;
   }
   for (int c = a.nch - 1; c >= 0; --c) {
     const int z = (n * a.nch + c) * a.H + h, L = chunk_len(a, c);
@@ -253,11 +292,12 @@ GDN_HD void rev_body(X& x, const Args& a, int rb, int h, int n) {
       sW[i] = a.W[(size_t)z * C * DK + i];
     }
     float* dSg = a.dSx + (size_t)z * DV * DK;
-    for (int i = x.tid; i < RB * DK; i += x.nt) dSg[(size_t)row0 * DK + i] = sD[i];
+    for (int i = x.tid; i < RB * DK; i += x.nt)
+      dSg[(size_t)row0 * DK + i] = sD[(i / DK) * LD + i % DK];
     x.sync();
     // dU = P^T dO + Kbar dS'^T (C x RB)
     float* dUg = a.dU + (size_t)z * C * DV;
-    gemm(x, C, RB, DK, sKb, DK, 1, sD, 1, DK, [&](int t, int j, float s) {
+    gemm(x, C, RB, DK, sKb, DK, 1, sD, 1, LD, [&](int t, int j, float s) {
       sdU[t * RB + j] = s;
     });
     x.sync();
@@ -270,37 +310,38 @@ GDN_HD void rev_body(X& x, const Args& a, int rb, int h, int n) {
     // dS = gamma dS' + dO^T Qg - dU^T W (RB x DK)
     const float gam = expf(GL);
     gemm(x, RB, DK, C, sO, 1, RB, sQg, DK, 1, [&](int j, int cc, float s) {
-      sDn[j * DK + cc] = fmaf(gam, sD[j * DK + cc], s);
+      sDn[j * LD + cc] = fmaf(gam, sD[j * LD + cc], s);
     });
     x.sync();
     gemm(x, RB, DK, C, sdU, 1, RB, sW, DK, 1, [&](int j, int cc, float s) {
-      sDn[j * DK + cc] -= s;
+      sDn[j * LD + cc] -= s;
     });
     x.sync();
-    for (int i = x.tid; i < RB * DK; i += x.nt) sD[i] = sDn[i];
+    for (int i = x.tid; i < RB * LD; i += x.nt) sD[i] = sDn[i];
   }
   x.sync();
   if (a.dh0)
     for (int i = x.tid; i < RB * DK; i += x.nt) {
       const int j = i / DK, cc = i % DK;
-      a.dh0[(((size_t)n * a.H + h) * DK + cc) * DV + row0 + j] = sD[i];
+      a.dh0[(((size_t)n * a.H + h) * DK + cc) * DV + row0 + j] = sD[j * LD + cc];
     }
 }
 
 // ---- 4. per (chunk, head): dq, dk, dv, dbeta, dg -------------------------
 // smem: K, Q [C][DK], V, dO [C][DV], G, beta, E, ebar, dG [C], red [nt + 1]
 template <int DK, int DV>
-constexpr int grad_smem(int nt) { return 2 * C * DK + 2 * C * DV + 5 * C + nt + 1; }
+constexpr int grad_smem(int nt) { return C * (DK + 1) + C * DK + C * (DV + 1) + C * DV + 5 * C + nt + 1; }
 
 template <int DK, int DV, bool BF, class X>
 GDN_HD void grad_body(X& x, const Args& a, int z) {
   const int h = z % a.H, nc = z / a.H, c = nc % a.nch, n = nc / a.nch;
   const int L = chunk_len(a, c);
   const long long t0 = (long long)n * a.T + (long long)c * C;
+  constexpr int LK = DK + 1, LV = DV + 1;  // padded: K and V are read transposed
   float* sK = x.smem;
-  float* sQ = sK + C * DK;
+  float* sQ = sK + C * LK;
   float* sV = sQ + C * DK;
-  float* sO = sV + C * DV;
+  float* sO = sV + C * LV;
   float* sG = sO + C * DV;
   float* sB = sG + C;
   float* sE = sB + C;
@@ -311,14 +352,14 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
     const int t = i / DK, cc = i % DK;
     const bool in = t < L;
     const size_t r = ((size_t)(t0 + t) * a.H + h) * DK + cc;
-    sK[i] = in ? ldin<BF>(a.k, r) : 0.f;
+    sK[t * LK + cc] = in ? ldin<BF>(a.k, r) : 0.f;
     sQ[i] = in ? ldin<BF>(a.q, r) : 0.f;
   }
   for (int i = x.tid; i < C * DV; i += x.nt) {
     const int t = i / DV, cc = i % DV;
     const bool in = t < L;
     const size_t r = ((size_t)(t0 + t) * a.H + h) * DV + cc;
-    sV[i] = in ? ldin<BF>(a.v, r) : 0.f;
+    sV[t * LV + cc] = in ? ldin<BF>(a.v, r) : 0.f;
     sO[i] = in ? ldin<BF>(a.dout, r) : 0.f;
   }
   const float* G = a.G + (size_t)z * C;
@@ -346,7 +387,7 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
   gemm(x, C, DK, DV, U, DV, 1, dSx, DK, 1, [&](int t, int cc, float s) { dKbar[t * DK + cc] = s; });
   gemm(x, C, DK, DV, dU, DV, 1, S, DK, 1, [&](int t, int cc, float s) { dW[t * DK + cc] = -s; });
   gemm(x, C, C, DV, sO, DV, 1, U, 1, DV, [&](int t, int s, float d) { dP[t * C + s] = t >= s ? d : 0.f; });
-  gemm(x, C, C, DK, sK, DK, 1, sK, 1, DK, [&](int r, int s, float d) { KK[r * C + s] = d; });
+  gemm(x, C, C, DK, sK, LK, 1, sK, 1, LK, [&](int r, int s, float d) { KK[r * C + s] = d; });
   float part = 0.f;  // sum(dS' (.) S)
   for (int i = x.tid; i < DV * DK; i += x.nt) part = fmaf(dSx[i], S[i], part);
   red[x.tid] = part;
@@ -360,9 +401,9 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
   gemm(x, C, DK, C, Tm, 1, C, dW, DK, 1, [&](int t, int cc, float s) { dKb[t * DK + cc] = s; });
   gemm(x, C, DV, C, Tm, 1, C, dU, DV, 1, [&](int t, int cc, float s) { dVb[t * DV + cc] = s; });
   // dT = dW Kb^T + dU Vb^T, Kb = diag(beta E) K, Vb = diag(beta) V
-  gemm(x, C, C, DK, dW, DK, 1, sK, 1, DK, [&](int r, int s, float d) { dT[r * C + s] = d * sB[s] * sE[s]; });
+  gemm(x, C, C, DK, dW, DK, 1, sK, 1, LK, [&](int r, int s, float d) { dT[r * C + s] = d * sB[s] * sE[s]; });
   x.sync();
-  gemm(x, C, C, DV, dU, DV, 1, sV, 1, DV, [&](int r, int s, float d) { dT[r * C + s] += d * sB[s]; });
+  gemm(x, C, C, DV, dU, DV, 1, sV, 1, LV, [&](int r, int s, float d) { dT[r * C + s] += d * sB[s]; });
   x.sync();
   // X = T^T dT; dA = strict_lower(-X T^T)
   gemm(x, C, C, C, Tm, 1, C, dT, C, 1, [&](int r, int s, float d) { Xm[r * C + s] = d; });
@@ -373,11 +414,11 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
   for (int t = x.tid; t < C; t += x.nt) {
     float kdkb = 0.f, vdvb = 0.f, qdos = 0.f, kdkbar = 0.f;
     for (int cc = 0; cc < DK; ++cc) {
-      kdkb = fmaf(sK[t * DK + cc], dKb[t * DK + cc], kdkb);
+      kdkb = fmaf(sK[t * LK + cc], dKb[t * DK + cc], kdkb);
       qdos = fmaf(sQ[t * DK + cc], dOS[t * DK + cc], qdos);
-      kdkbar = fmaf(sK[t * DK + cc], dKbar[t * DK + cc], kdkbar);
+      kdkbar = fmaf(sK[t * LK + cc], dKbar[t * DK + cc], kdkbar);
     }
-    for (int cc = 0; cc < DV; ++cc) vdvb = fmaf(sV[t * DV + cc], dVb[t * DV + cc], vdvb);
+    for (int cc = 0; cc < DV; ++cc) vdvb = fmaf(sV[t * LV + cc], dVb[t * DV + cc], vdvb);
     float db = sE[t] * kdkb + vdvb;
     float dG = sB[t] * sE[t] * kdkb + sE[t] * qdos - sEb[t] * kdkbar;
     for (int s = 0; s < C; ++s) {
@@ -415,15 +456,15 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
   }
   x.sync();
   // dQ = diag(E) dOS + (dP (.) D) K
-  gemm(x, C, DK, C, Xm, C, 1, sK, DK, 1, [&](int t, int cc, float s) {
+  gemm(x, C, DK, C, Xm, C, 1, sK, LK, 1, [&](int t, int cc, float s) {
     if (t < L) a.dq[((size_t)(t0 + t) * a.H + h) * DK + cc] = fmaf(sE[t], dOS[t * DK + cc], s);
   });
   // dK = (dP (.) D)^T Q + B K + B^T K + diag(ebar) dKbar + diag(beta E) dKb
   gemm(x, C, DK, C, Xm, 1, C, sQ, DK, 1, [&](int s, int cc, float v) { dKs[s * DK + cc] = v; });
   x.sync();
-  gemm(x, C, DK, C, dT, C, 1, sK, DK, 1, [&](int s, int cc, float v) { dKs[s * DK + cc] += v; });
+  gemm(x, C, DK, C, dT, C, 1, sK, LK, 1, [&](int s, int cc, float v) { dKs[s * DK + cc] += v; });
   x.sync();
-  gemm(x, C, DK, C, dT, 1, C, sK, DK, 1, [&](int s, int cc, float v) {
+  gemm(x, C, DK, C, dT, 1, C, sK, LK, 1, [&](int s, int cc, float v) {
     const float r = dKs[s * DK + cc] + v + sEb[s] * dKbar[s * DK + cc] +
                     sB[s] * sE[s] * dKb[s * DK + cc];
     if (s < L) a.dk[((size_t)(t0 + s) * a.H + h) * DK + cc] = r;
