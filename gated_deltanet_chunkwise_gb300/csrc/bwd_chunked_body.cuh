@@ -58,11 +58,77 @@ GDN_HD inline float ldin(const void* p, size_t i) {
   return static_cast<const float*>(p)[i];
 }
 
+#ifdef __CUDA_ARCH__
+// fp32 x as a tf32 pair hi + lo (hi rounded to nearest, lo the rounded
+// remainder): products of the pairs keep about fp32 accuracy.
+__device__ __forceinline__ void tf32_split(float v, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(v));
+  const float rest = v - __uint_as_float(hi);
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(rest));
+}
+// d += a b for one m16n8k8 tile (tf32 operands, fp32 accumulate).
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+#endif
+
 // C[M][N] via epi(i, j, sum_k A(i,k) B(k,j)), A(i,k) = A[i*ars + k*acs],
-// B(k,j) = B[k*brs + j*bcs]; each thread a 4 x 4 tile.
+// B(k,j) = B[k*brs + j*bcs]. Every output element is passed to epi exactly
+// once, by one thread.
 template <class X, class F>
 GDN_HD void gemm(X& x, int M, int N, int K, const float* A, int ars, int acs,
                  const float* B, int brs, int bcs, F epi) {
+#ifdef __CUDA_ARCH__
+  if (M % 16 == 0 && N % 32 == 0 && K % 8 == 0 && x.nt % 32 == 0) {
+    // Tensor cores: each warp a 16 x 32 tile of C (four m16n8k8 tiles
+    // sharing the A fragment), operands split into tf32 pairs and
+    // multiplied as hi*hi + hi*lo + lo*hi, accumulated in fp32.
+    // Fragment layout (m16n8k8, tf32): lane = 4 g + t; A rows g, g + 8 and
+    // columns t, t + 4; B rows t, t + 4 and column g; C rows g, g + 8 and
+    // columns 2t, 2t + 1.
+    const int warp = x.tid >> 5, lane = x.tid & 31, nw = x.nt >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int tn = N / 32, ntiles = (M / 16) * tn;
+    for (int tile = warp; tile < ntiles; tile += nw) {
+      const int m0 = (tile / tn) * 16, n0 = (tile % tn) * 32;
+      float acc[4][4];
+      for (int q = 0; q < 4; ++q)
+        for (int e = 0; e < 4; ++e) acc[q][e] = 0.f;
+#pragma unroll 4
+      for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t ah[4], al[4];
+        tf32_split(A[(m0 + g) * ars + (k0 + t) * acs], ah[0], al[0]);
+        tf32_split(A[(m0 + g + 8) * ars + (k0 + t) * acs], ah[1], al[1]);
+        tf32_split(A[(m0 + g) * ars + (k0 + t + 4) * acs], ah[2], al[2]);
+        tf32_split(A[(m0 + g + 8) * ars + (k0 + t + 4) * acs], ah[3], al[3]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int n = n0 + 8 * q + g;
+          uint32_t bh0, bl0, bh1, bl1;
+          tf32_split(B[(k0 + t) * brs + n * bcs], bh0, bl0);
+          tf32_split(B[(k0 + t + 4) * brs + n * bcs], bh1, bl1);
+          mma_tf32(acc[q], al, bh0, bh1);
+          mma_tf32(acc[q], ah, bl0, bl1);
+          mma_tf32(acc[q], ah, bh0, bh1);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c = n0 + 8 * q + 2 * t;
+        epi(m0 + g, c, acc[q][0]);
+        epi(m0 + g, c + 1, acc[q][1]);
+        epi(m0 + g + 8, c, acc[q][2]);
+        epi(m0 + g + 8, c + 1, acc[q][3]);
+      }
+    }
+    return;
+  }
+#endif
   // thread (ti, tj) owns rows ti + m*M/4 and columns tj + n*N/4: neighbouring
   // threads read neighbouring columns of B (coalesced, and conflict-free in
   // shared memory when B's column stride is 1 or an odd number of floats)
@@ -220,10 +286,13 @@ GDN_HD void fwd_body(X& x, const Args& a, int rb, int h, int n) {
     const float* G = a.G + (size_t)z * C;
     const float GL = G[L - 1];
     x.sync();  // the previous chunk is done with the buffers
+    // e^{G_L - G_t} once per token, in sU until U overwrites it
+    for (int t = x.tid; t < C; t += x.nt) sU[t] = t < L ? expf(GL - G[t]) : 0.f;
+    x.sync();
     for (int i = x.tid; i < C * DK; i += x.nt) {
       const int t = i / DK, cc = i % DK;
       sW[i] = a.W[(size_t)z * C * DK + i];
-      sKb[i] = t < L ? expf(GL - G[t]) * ldin<BF>(a.k, ((size_t)(t0 + t) * a.H + h) * DK + cc) : 0.f;
+      sKb[i] = t < L ? sU[t] * ldin<BF>(a.k, ((size_t)(t0 + t) * a.H + h) * DK + cc) : 0.f;
     }
     for (int i = x.tid; i < C * RB; i += x.nt) {
       const int t = i / RB, j = i % RB;
@@ -278,6 +347,12 @@ GDN_HD void rev_body(X& x, const Args& a, int rb, int h, int n) {
     const float* G = a.G + (size_t)z * C;
     const float GL = G[L - 1];
     x.sync();
+    // e^{G_L - G_t} and e^{G_t} once per token, in sdU until dU overwrites it
+    for (int t = x.tid; t < C; t += x.nt) {
+      sdU[t] = t < L ? expf(GL - G[t]) : 0.f;
+      sdU[C + t] = t < L ? expf(G[t]) : 0.f;
+    }
+    x.sync();
     for (int i = x.tid; i < C * C; i += x.nt) sP[i] = a.P[(size_t)z * C * C + i];
     for (int i = x.tid; i < C * RB; i += x.nt) {
       const int t = i / RB, j = i % RB;
@@ -287,8 +362,8 @@ GDN_HD void rev_body(X& x, const Args& a, int rb, int h, int n) {
       const int t = i / DK, cc = i % DK;
       const bool in = t < L;
       const size_t r = ((size_t)(t0 + t) * a.H + h) * DK + cc;
-      sKb[i] = in ? expf(GL - G[t]) * ldin<BF>(a.k, r) : 0.f;
-      sQg[i] = in ? expf(G[t]) * ldin<BF>(a.q, r) : 0.f;
+      sKb[i] = in ? sdU[t] * ldin<BF>(a.k, r) : 0.f;
+      sQg[i] = in ? sdU[C + t] * ldin<BF>(a.q, r) : 0.f;
       sW[i] = a.W[(size_t)z * C * DK + i];
     }
     float* dSg = a.dSx + (size_t)z * DV * DK;
