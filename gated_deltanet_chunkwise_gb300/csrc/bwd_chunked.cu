@@ -17,7 +17,10 @@ namespace gdn {
 namespace {
 
 constexpr int kCbThreads = 256;
-constexpr int kCbRows = 32;  // value rows per chain CTA
+// value rows per chain CTA: with 64 the chain grids (d_v / 64 per head and
+// sequence) of a 4-sequence, 16-head problem run in one wave at one CTA per
+// SM (32 rows took two)
+constexpr int kCbRows = 64;
 
 struct DevX {
   int tid, nt;

@@ -485,7 +485,49 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
   x.sync();
   gemm(x, C, C, C, Xm, C, 1, Tm, 1, C, [&](int r, int s, float d) { dA[r * C + s] = r > s ? -d : 0.f; });
   x.sync();
-  // dbeta and dG, one thread per token t
+  // dbeta and dG per token t: on the device four lanes per token, each a
+  // quarter of every sum, combined by shuffles; on the host one thread per
+  // token
+#ifdef __CUDA_ARCH__
+  if (x.nt == 4 * C) {
+    const int t = x.tid >> 2, q = x.tid & 3;
+    float kdkb = 0.f, vdvb = 0.f, qdos = 0.f, kdkbar = 0.f, dbp = 0.f, dGp = 0.f;
+    for (int cc = q; cc < DK; cc += 4) {
+      kdkb = fmaf(sK[t * LK + cc], dKb[t * DK + cc], kdkb);
+      qdos = fmaf(sQ[t * DK + cc], dOS[t * DK + cc], qdos);
+      kdkbar = fmaf(sK[t * LK + cc], dKbar[t * DK + cc], kdkbar);
+    }
+    for (int cc = q; cc < DV; cc += 4) vdvb = fmaf(sV[t * LV + cc], dVb[t * DV + cc], vdvb);
+    for (int s = q; s < C; s += 4) {
+      const float kk = KK[t * C + s];
+      if (s < t) {
+        const float D = expf(sG[t] - sG[s]);
+        dbp = fmaf(dA[t * C + s] * D, kk, dbp);
+        dGp = fmaf(dA[t * C + s], sB[t] * kk * D, dGp);
+      }
+      if (s > t) dGp -= dA[s * C + t] * sB[s] * kk * expf(sG[s] - sG[t]);
+      if (s <= t) dGp = fmaf(dP[t * C + s], P[t * C + s], dGp);
+      if (s >= t) dGp -= dP[s * C + t] * P[s * C + t];
+    }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+      kdkb += __shfl_xor_sync(0xffffffffu, kdkb, o);
+      vdvb += __shfl_xor_sync(0xffffffffu, vdvb, o);
+      qdos += __shfl_xor_sync(0xffffffffu, qdos, o);
+      kdkbar += __shfl_xor_sync(0xffffffffu, kdkbar, o);
+      dbp += __shfl_xor_sync(0xffffffffu, dbp, o);
+      dGp += __shfl_xor_sync(0xffffffffu, dGp, o);
+    }
+    if (q == 0) {
+      const float db = sE[t] * kdkb + vdvb + dbp;
+      const float dG = sB[t] * sE[t] * kdkb + sE[t] * qdos - sEb[t] * kdkbar + dGp;
+      if (t < L) a.dbeta[(size_t)(t0 + t) * a.H + h] = db;
+      sdG[t] = dG;
+      red[t] = sEb[t] * kdkbar;  // the partials above were summed into red[nt]
+    }
+  } else
+#endif
+  {
   for (int t = x.tid; t < C; t += x.nt) {
     float kdkb = 0.f, vdvb = 0.f, qdos = 0.f, kdkbar = 0.f;
     for (int cc = 0; cc < DK; ++cc) {
@@ -510,6 +552,7 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
     if (t < L) a.dbeta[(size_t)(t0 + t) * a.H + h] = db;
     sdG[t] = dG;
     red[t] = sEb[t] * kdkbar;  // the partials above were summed into red[nt]
+  }
   }
   x.sync();
   if (x.tid == 0) {
