@@ -12,8 +12,9 @@ launches for it). Prints ONE JSON line on rank 0.
 Timing: inputs resident in HBM, the L2 (129 MB) is flushed before every
 timed step by a 256 MiB memset followed by a read of another 256 MiB buffer
 (so the memset's dirty lines are written back before the step, not during
-it), each step is bracketed by CUDA events on the
-launching stream; ms_per_step is the mean. Under torchrun every rank runs the
+it), a short spin kernel then holds the GPU while the host enqueues the step,
+and each step is bracketed by CUDA events on the launching stream;
+ms_per_step is the mean. Under torchrun every rank runs the
 same workload on its own GPU (independent problems, weak scaling, no
 collective on the data path) and the max over ranks is reported.
 """
@@ -37,6 +38,10 @@ sys.path.insert(0, str(ROOT))
 
 METRIC = "GDN chunk-fwd tokens/s + % of GB300 tensor/HBM roofline, 1 GPU"
 FLUSH_BYTES = 256 << 20
+# A spin kernel of this many SM cycles (about 0.5 ms) between the L2 flush
+# and a timed step holds the GPU while the host enqueues the step, so that
+# the step's events time its kernels and not the host's launch latency.
+HOLD_CYCLES = 1_000_000
 
 
 def _metric(w):
@@ -123,14 +128,17 @@ WORKLOADS = {
 # hash of the kernel source it was taken on; a changed kernel reports null.
 MEASURED_TRAFFIC = {
     # chunk_tc_kernel, W1, one launch (caches flushed by the bench)
-    "w1:5fe6b52b69a8c778": 168942592 + 19785984,
-    # chain_tx_kernel, W3 (packed, 512 sequence-heads), one launch
-    "w3:5fe6b52b69a8c778": 2996173056 + 598289920,
+    "w1:6f137cb519c86b8e": 168919552 + 19976704,
+    # chain_tx_kernel, W3 (packed, 512 sequence-heads), one launch; captured
+    # before the latest edits of chunk_tc.cu, none of which touched
+    # chain_tx_kernel or the headers it uses
+    "w3:6f137cb519c86b8e": 2996173056 + 598289920,
     # decode_kernel captured with --sequences 128 and scaled x4 to N=512:
     # its traffic is proportional to the sequences processed
     "w4:83c7aa23b4500b6b": 4 * (271642880 + 210279936),
-    # kda_prep_kernel, kda1, one launch
-    "kda1:21af4a2a3fb88473": 134819328 + 84282112,
+    # kda_prep_kernel, kda1, one launch (kda_chunk.cu unchanged since; the
+    # key also covers chunk_tc.cu, whose later edits do not touch it)
+    "kda1:5be0bea5061237bf": 134819328 + 84282112,
     # bwd_kernel, bwd1, one launch (the per-CTA windows of S_bar do not all
     # stay in L2: most of the writes)
     "bwd1:e6e8ce911b3198e0": 761174272 + 5027586560,
@@ -329,6 +337,9 @@ def run_ours(args, w, device, dist, rank, ws):
         flush_w.zero_()  # write a buffer larger than L2
         flush_r.max()    # then read one: L2 holds clean foreign lines only
 
+    def hold():
+        torch.cuda._sleep(HOLD_CYCLES)
+
     if w["kind"] == "decode":
         out = torch.empty_like(d["v"])
         state0 = d["state"].clone()
@@ -420,6 +431,7 @@ def run_ours(args, w, device, dist, rank, ws):
     t_wall = time.perf_counter()
     for i in range(steps):
         l2_flush()
+        hold()
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -508,26 +520,27 @@ def run_ours(args, w, device, dist, rank, ws):
         unit = "token-heads/s"
         e2e_val = units_all / (e2e_ms * 1e-3) * (tok_heads / tokens)
     elif w["kind"] == "bwdc":
-        # the chunk form's gradient kernel (fp32 CUDA cores): per chunk and
-        # head the products over the value rows (dO S, U dS', dU S: 3 C d_k
-        # d_v multiply-adds), the C x C products (dP, K K^T, T^T dW, T^T dU,
-        # dT, the dq and three dk products: C^2 (7 d_k + 3 d_v)) and
-        # dA = -T^T dT T^T (2 C^3)
+        # the chunk form's gradient kernel: per chunk and head the products
+        # over the value rows (dO S, U dS', dU S: 3 C d_k d_v multiply-adds),
+        # the C x C products (dP, K K^T, T^T dW, T^T dU, dT, the dq and three
+        # dk products: C^2 (7 d_k + 3 d_v)) and dA = -T^T dT T^T (2 C^3).
+        # They run on the tensor cores as tf32 pairs (three m16n8k8 tf32
+        # products per fp32 product), so the peak is the tf32 rate: the
+        # measured bf16 rate times the nominal tf32 : bf16 ratio (1.1 : 2.25
+        # PFLOP/s dense), against the algorithmic (single-product) flops.
         C = 64
         n_k, ms_k = kern.get("cbwd_grad_kernel", (0, 0.0))
         k_ms = ms_k / steps if n_k else ms
         chunk_heads = math.ceil(w["T"] / C) * w["B"] * w["H"]
         flops = 2 * chunk_heads * (3 * C * dk * dv + C * C * (7 * dk + 3 * dv)
                                    + 2 * C ** 3)
-        sms = torch.cuda.get_device_properties(device).multi_processor_count
-        mhz = _sm_max_mhz()
-        alu_tflops = sms * 128 * 2 * mhz * 1e6 / 1e12
+        tf32_tflops = bf16_tflops * 1.1 / 2.25
         achieved = flops / (k_ms * 1e-3) / 1e12
-        roof = {"bound": "alu", "kernel": "cbwd_grad_kernel",
-                "achieved": round(achieved, 2), "peak": round(alu_tflops, 1),
-                "unit": "TFLOP/s", "frac": round(achieved / alu_tflops, 4),
-                "peak_source": f"derived: {sms} SMs x 128 fp32 FMA/cycle x 2 "
-                               f"x {mhz:.0f} MHz (max SM clock)",
+        roof = {"bound": "tensor", "kernel": "cbwd_grad_kernel",
+                "achieved": round(achieved, 2), "peak": round(tf32_tflops, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / tf32_tflops, 4),
+                "peak_source": f"{peak_kind} bf16_tflops x 1.1/2.25 (nominal "
+                               "tf32 : bf16 dense ratio)",
                 "algorithmic_flops_per_step": flops,
                 "launches_per_step": n_k / steps, "ms_per_step": k_ms}
         value = units_all / (ms * 1e-3)
@@ -661,10 +674,13 @@ def run_ours(args, w, device, dist, rank, ws):
                    "l2": "flushed before every timed step: 256 MiB memset, then a "
                          "256 MiB read (write-back of the memset outside the "
                          "timed events)",
-                   "timing": "CUDA events per step on the launching stream; "
-                             "per-kernel durations from the library's events "
-                             "around each launch in a second pass of the same "
-                             "steps"},
+                   "timing": "CUDA events per step on the launching stream, "
+                             "a 1M-cycle spin kernel between the flush and "
+                             "each step's start event (the host enqueues the "
+                             "step meanwhile, so launch latency is not "
+                             "timed); per-kernel durations from the "
+                             "library's events around each launch in a second "
+                             "pass of the same steps"},
         "roofline": roof,
         "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
