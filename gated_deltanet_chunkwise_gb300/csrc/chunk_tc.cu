@@ -956,9 +956,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Output gate: a U-row thread turns the gate logits of chunk j (row
     // ct - 64 of its stage tile, the thread's kCW columns, the same slice its
     // output-row twin reads) into sigmoid(z) in place and its warp arrives on
-    // GREADY of the stage. The tile of chunk j + 2 reuses the stage only
-    // after the output rows have read chunk j's and released the stage, so
-    // one barrier per stage sees its phases in order.
+    // GREADY of the stage. It does so in chunk j itself, between storing U
+    // and the state update, when the stage has landed (the chunk's MMAs have
+    // read it): waiting for a later stage there would hold up the U rows.
+    // The tile of chunk j + 2 reuses the stage only after the output rows
+    // have read chunk j's and released the stage, so one barrier per stage
+    // sees its phases in order.
     auto gate_to_sigmoid = [&](int j, bool okj) {
       const int sj = j & 1;
       okj = okj && mbar_wait(&bars[B_FULLB0 + sj], (j >> 1) & 1, abort_flag);
@@ -967,20 +970,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kCW / 8; ++c) {
           uint4* q = reinterpret_cast<uint4*>(gt + sw128(ct - 64, chunk0 + c));
-          float f[8];
-          unpack_bf16x8(*q, f);
-          uint4 w;
-          w.x = pack_bf16x2(sigmoid_approx(f[0]), sigmoid_approx(f[1]));
-          w.y = pack_bf16x2(sigmoid_approx(f[2]), sigmoid_approx(f[3]));
-          w.z = pack_bf16x2(sigmoid_approx(f[4]), sigmoid_approx(f[5]));
-          w.w = pack_bf16x2(sigmoid_approx(f[6]), sigmoid_approx(f[7]));
+          uint4 w = *q;
+          w.x = sigmoid2_bf16(w.x);
+          w.y = sigmoid2_bf16(w.y);
+          w.z = sigmoid2_bf16(w.z);
+          w.w = sigmoid2_bf16(w.w);
           *q = w;
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_GREADY0 + sj]);
     };
-    if (has_gate && u_rows && nloc > 0) gate_to_sigmoid(0, true);
     // [Q;-W] S^T accumulated onto U0: H = Q S^T (rows 0-63), U (64-127)
     // Fused epilogue on one chunk's output rows (o: this thread's kCW
     // columns of row r; gzv: sigmoid of the gate logits, bf16): o <- o /
@@ -1101,6 +1101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[B_UREADY]);
         }
+        if (has_gate) gate_to_sigmoid(i, ok1);
         ok = ok1;
       }
       const bool ok3 = __all_sync(
@@ -1119,7 +1120,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_SREADY]);
-      if (has_gate && u_rows && i + 1 < nloc) gate_to_sigmoid(i + 1, ok);
       if (!u_rows) {
         // O = e^{G_r} H + P U, through a shared-memory tile and a TMA store
         // for a whole chunk, direct stores for a partial one

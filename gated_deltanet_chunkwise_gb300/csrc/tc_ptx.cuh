@@ -121,6 +121,19 @@ __device__ __forceinline__ float sigmoid_approx(float z) {
   return fmaf(0.5f, t, 0.5f);
 }
 
+// Two sigmoids of a packed bf16 pair, in bf16 arithmetic: (1 + tanh(z / 2))
+// / 2 with the halving exact, one tanh instruction per pair and the result
+// rounded to bf16 (absolute error about 2^-9, the size of bf16 rounding of a
+// value in (0, 1)).
+__device__ __forceinline__ uint32_t sigmoid2_bf16(uint32_t z2) {
+  const uint32_t half2 = 0x3F003F00u;  // (0.5, 0.5) in bf16
+  uint32_t h, t, r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(h) : "r"(z2), "r"(half2));
+  asm("tanh.approx.bf16x2 %0, %1;" : "=r"(t) : "r"(h));
+  asm("fma.rn.bf16x2 %0, %1, %2, %2;" : "=r"(r) : "r"(t), "r"(half2));
+  return r;
+}
+
 // ---- thread-block clusters ---------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
