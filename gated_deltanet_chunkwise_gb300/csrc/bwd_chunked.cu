@@ -61,8 +61,8 @@ bool al16c(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; 
 template <int DK, int DV>
 cudaError_t launch_all(const cbwd::Args& a, long long zc, cudaStream_t st, int* launches) {
   using namespace cbwd;
-  const int s_prep = prep_smem<DK, DV>() * 4, s_fwd = fwd_smem<DK, kCbRows>() * 4,
-            s_rev = rev_smem<DK, kCbRows>() * 4, s_grad = grad_smem<DK, DV>(kCbThreads) * 4;
+  const int s_prep = prep_smem<DK, DV, true>() * 4, s_fwd = fwd_smem<DK, kCbRows>() * 4,
+            s_rev = rev_smem<DK, kCbRows>() * 4, s_grad = grad_smem<DK, DV, true>(kCbThreads) * 4;
   auto kp = cbwd_prep_kernel<DK, DV, true>;
   auto kf = cbwd_fwd_kernel<DK, DV, true>;
   auto kr = cbwd_rev_kernel<DK, DV, true>;

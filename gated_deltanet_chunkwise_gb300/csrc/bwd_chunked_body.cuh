@@ -22,6 +22,7 @@
 // every thread reaches every x.sync().
 #pragma once
 #include <cstring>
+#include <type_traits>
 #ifdef __CUDACC__
 #define GDN_HD __host__ __device__
 #else
@@ -58,6 +59,23 @@ GDN_HD inline float ldin(const void* p, size_t i) {
   return static_cast<const float*>(p)[i];
 }
 
+// Shared-memory copies of the inputs: bf16 inputs stay bf16 bit patterns
+// (exact, half the bytes), fp32 inputs stay fp32. tv reads either as fp32.
+template <bool BF>
+using tile_t = typename std::conditional<BF, unsigned short, float>::type;
+GDN_HD inline float tv(float v) { return v; }
+GDN_HD inline float tv(unsigned short u) {
+  const unsigned int w = (unsigned int)u << 16;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return f;
+}
+template <bool BF>
+GDN_HD inline tile_t<BF> ldtile(const void* p, size_t i) {
+  if constexpr (BF) return static_cast<const unsigned short*>(p)[i];
+  else return static_cast<const float*>(p)[i];
+}
+
 #ifdef __CUDA_ARCH__
 // fp32 x as a tf32 pair hi + lo (hi rounded to nearest, lo the rounded
 // remainder): products of the pairs keep about fp32 accuracy.
@@ -80,10 +98,14 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
 // C[M][N] via epi(i, j, sum_k A(i,k) B(k,j)), A(i,k) = A[i*ars + k*acs],
 // B(k,j) = B[k*brs + j*bcs]. Every output element is passed to epi exactly
 // once, by one thread.
-template <class X, class F>
-GDN_HD void gemm(X& x, int M, int N, int K, const float* A, int ars, int acs,
-                 const float* B, int brs, int bcs, F epi) {
+template <class X, class TA, class TB, class F>
+GDN_HD void gemm(X& x, int M, int N, int K, const TA* A, int ars, int acs,
+                 const TB* B, int brs, int bcs, F epi) {
 #ifdef __CUDA_ARCH__
+  // a bf16 operand is exact in tf32: its low part is zero and its two
+  // products with it are skipped
+  constexpr bool a_exact = std::is_same<TA, unsigned short>::value;
+  constexpr bool b_exact = std::is_same<TB, unsigned short>::value;
   if (M % 16 == 0 && N % 32 == 0 && K % 8 == 0 && x.nt % 32 == 0) {
     // Tensor cores: each warp a 16 x 32 tile of C (four m16n8k8 tiles
     // sharing the A fragment), operands split into tf32 pairs and
@@ -102,18 +124,18 @@ GDN_HD void gemm(X& x, int M, int N, int K, const float* A, int ars, int acs,
 #pragma unroll 4
       for (int k0 = 0; k0 < K; k0 += 8) {
         uint32_t ah[4], al[4];
-        tf32_split(A[(m0 + g) * ars + (k0 + t) * acs], ah[0], al[0]);
-        tf32_split(A[(m0 + g + 8) * ars + (k0 + t) * acs], ah[1], al[1]);
-        tf32_split(A[(m0 + g) * ars + (k0 + t + 4) * acs], ah[2], al[2]);
-        tf32_split(A[(m0 + g + 8) * ars + (k0 + t + 4) * acs], ah[3], al[3]);
+        tf32_split(tv(A[(m0 + g) * ars + (k0 + t) * acs]), ah[0], al[0]);
+        tf32_split(tv(A[(m0 + g + 8) * ars + (k0 + t) * acs]), ah[1], al[1]);
+        tf32_split(tv(A[(m0 + g) * ars + (k0 + t + 4) * acs]), ah[2], al[2]);
+        tf32_split(tv(A[(m0 + g + 8) * ars + (k0 + t + 4) * acs]), ah[3], al[3]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int n = n0 + 8 * q + g;
           uint32_t bh0, bl0, bh1, bl1;
-          tf32_split(B[(k0 + t) * brs + n * bcs], bh0, bl0);
-          tf32_split(B[(k0 + t + 4) * brs + n * bcs], bh1, bl1);
-          mma_tf32(acc[q], al, bh0, bh1);
-          mma_tf32(acc[q], ah, bl0, bl1);
+          tf32_split(tv(B[(k0 + t) * brs + n * bcs]), bh0, bl0);
+          tf32_split(tv(B[(k0 + t + 4) * brs + n * bcs]), bh1, bl1);
+          if (!a_exact) mma_tf32(acc[q], al, bh0, bh1);
+          if (!b_exact) mma_tf32(acc[q], ah, bl0, bl1);
           mma_tf32(acc[q], ah, bh0, bh1);
         }
       }
@@ -140,8 +162,8 @@ GDN_HD void gemm(X& x, int M, int N, int K, const float* A, int ars, int acs,
       for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
     for (int kk = 0; kk < K; ++kk) {
       float a[4], b[4];
-      for (int i = 0; i < 4; ++i) a[i] = A[(ti + i * tm) * ars + kk * acs];
-      for (int j = 0; j < 4; ++j) b[j] = B[kk * brs + (tj + j * tn) * bcs];
+      for (int i = 0; i < 4; ++i) a[i] = tv(A[(ti + i * tm) * ars + kk * acs]);
+      for (int j = 0; j < 4; ++j) b[j] = tv(B[kk * brs + (tj + j * tn) * bcs]);
       for (int i = 0; i < 4; ++i)
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
@@ -157,8 +179,10 @@ GDN_HD inline int chunk_len(const Args& a, int c) {
 
 // ---- 1. per (chunk, head): G, T = (I + A)^{-1}, W, U0, P -----------------
 // smem floats: K, Q [C][DK], V [C][DV], A [C][C], T [C][C], G, beta [C]
-template <int DK, int DV>
-constexpr int prep_smem() { return C * (DK + 1) + C * DK + C * DV + 2 * C * C + 2 * C; }
+template <int DK, int DV, bool BF>
+constexpr int prep_smem() {
+  return (C * (DK + 1) + C * DK + C * DV) * (int)sizeof(tile_t<BF>) / 4 + 2 * C * C + 2 * C;
+}
 
 template <int DK, int DV, bool BF, class X>
 GDN_HD void prep_body(X& x, const Args& a, int z) {
@@ -166,10 +190,11 @@ GDN_HD void prep_body(X& x, const Args& a, int z) {
   const int L = chunk_len(a, c);
   const long long t0 = (long long)n * a.T + (long long)c * C;
   constexpr int LK = DK + 1;  // padded: K is read transposed
-  float* sK = x.smem;
-  float* sQ = sK + C * LK;
-  float* sV = sQ + C * DK;
-  float* sA = sV + C * DV;
+  using TT = tile_t<BF>;
+  TT* sK = reinterpret_cast<TT*>(x.smem);
+  TT* sQ = sK + C * LK;
+  TT* sV = sQ + C * DK;
+  float* sA = reinterpret_cast<float*>(sV + C * DV);
   float* sT = sA + C * C;
   float* sG = sT + C * C;
   float* sB = sG + C;
@@ -177,12 +202,12 @@ GDN_HD void prep_body(X& x, const Args& a, int z) {
     const int t = i / DK, cc = i % DK;
     const bool in = t < L;
     const size_t r = ((size_t)(t0 + t) * a.H + h) * DK + cc;
-    sK[t * LK + cc] = in ? ldin<BF>(a.k, r) : 0.f;
-    sQ[i] = in ? ldin<BF>(a.q, r) : 0.f;
+    sK[t * LK + cc] = in ? ldtile<BF>(a.k, r) : TT(0);
+    sQ[i] = in ? ldtile<BF>(a.q, r) : TT(0);
   }
   for (int i = x.tid; i < C * DV; i += x.nt) {
     const int t = i / DV, cc = i % DV;
-    sV[i] = t < L ? ldin<BF>(a.v, ((size_t)(t0 + t) * a.H + h) * DV + cc) : 0.f;
+    sV[i] = t < L ? ldtile<BF>(a.v, ((size_t)(t0 + t) * a.H + h) * DV + cc) : TT(0);
   }
   for (int t = x.tid; t < C; t += x.nt) {
     sB[t] = t < L ? a.beta[(size_t)(t0 + t) * a.H + h] : 0.f;
@@ -246,17 +271,21 @@ GDN_HD void prep_body(X& x, const Args& a, int z) {
   }
   float* Tg = a.Tm + (size_t)z * C * C;
   for (int i = x.tid; i < C * C; i += x.nt) Tg[i] = sT[i];
-  // W = T diag(beta e^G) K, U0 = T diag(beta) V: scale the rows in place
+  // W = (T diag(beta e^G)) K, U0 = (T diag(beta)) V: the factors scale the
+  // columns of copies of T (T itself is stored above), so that K and V keep
+  // their exact input values
   x.sync();
-  for (int i = x.tid; i < C * DK; i += x.nt) {
-    const int t = i / DK, cc = i % DK;
-    sK[t * LK + cc] *= sB[t] * expf(sG[t]);
+  float* sTW = sA;  // A and the merge scratch are not read again
+  for (int i = x.tid; i < C * C; i += x.nt) {
+    const int s2 = i % C;
+    const float tt = sT[i];
+    sTW[i] = tt * (sB[s2] * expf(sG[s2]));
+    sT[i] = tt * sB[s2];
   }
-  for (int i = x.tid; i < C * DV; i += x.nt) sV[i] *= sB[i / DV];
   x.sync();
   float* W = a.W + (size_t)z * C * DK;
   float* U0 = a.U0 + (size_t)z * C * DV;
-  gemm(x, C, DK, C, sT, C, 1, sK, LK, 1, [&](int t, int cc, float s) { W[t * DK + cc] = s; });
+  gemm(x, C, DK, C, sTW, C, 1, sK, LK, 1, [&](int t, int cc, float s) { W[t * DK + cc] = s; });
   gemm(x, C, DV, C, sT, C, 1, sV, DV, 1, [&](int t, int cc, float s) { U0[t * DV + cc] = s; });
 }
 
@@ -404,8 +433,11 @@ GDN_HD void rev_body(X& x, const Args& a, int rb, int h, int n) {
 
 // ---- 4. per (chunk, head): dq, dk, dv, dbeta, dg -------------------------
 // smem: K, Q [C][DK], V, dO [C][DV], G, beta, E, ebar, dG [C], red [nt + 1]
-template <int DK, int DV>
-constexpr int grad_smem(int nt) { return C * (DK + 1) + C * DK + C * (DV + 1) + C * DV + 5 * C + nt + 1; }
+template <int DK, int DV, bool BF>
+constexpr int grad_smem(int nt) {
+  return (C * (DK + 1) + C * DK + C * (DV + 1) + C * DV) * (int)sizeof(tile_t<BF>) / 4 +
+         5 * C + nt + 1;
+}
 
 template <int DK, int DV, bool BF, class X>
 GDN_HD void grad_body(X& x, const Args& a, int z) {
@@ -413,11 +445,12 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
   const int L = chunk_len(a, c);
   const long long t0 = (long long)n * a.T + (long long)c * C;
   constexpr int LK = DK + 1, LV = DV + 1;  // padded: K and V are read transposed
-  float* sK = x.smem;
-  float* sQ = sK + C * LK;
-  float* sV = sQ + C * DK;
-  float* sO = sV + C * LV;
-  float* sG = sO + C * DV;
+  using TT = tile_t<BF>;
+  TT* sK = reinterpret_cast<TT*>(x.smem);
+  TT* sQ = sK + C * LK;
+  TT* sV = sQ + C * DK;
+  TT* sO = sV + C * LV;
+  float* sG = reinterpret_cast<float*>(sO + C * DV);
   float* sB = sG + C;
   float* sE = sB + C;
   float* sEb = sE + C;
@@ -427,15 +460,15 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
     const int t = i / DK, cc = i % DK;
     const bool in = t < L;
     const size_t r = ((size_t)(t0 + t) * a.H + h) * DK + cc;
-    sK[t * LK + cc] = in ? ldin<BF>(a.k, r) : 0.f;
-    sQ[i] = in ? ldin<BF>(a.q, r) : 0.f;
+    sK[t * LK + cc] = in ? ldtile<BF>(a.k, r) : TT(0);
+    sQ[i] = in ? ldtile<BF>(a.q, r) : TT(0);
   }
   for (int i = x.tid; i < C * DV; i += x.nt) {
     const int t = i / DV, cc = i % DV;
     const bool in = t < L;
     const size_t r = ((size_t)(t0 + t) * a.H + h) * DV + cc;
-    sV[t * LV + cc] = in ? ldin<BF>(a.v, r) : 0.f;
-    sO[i] = in ? ldin<BF>(a.dout, r) : 0.f;
+    sV[t * LV + cc] = in ? ldtile<BF>(a.v, r) : TT(0);
+    sO[i] = in ? ldtile<BF>(a.dout, r) : TT(0);
   }
   const float* G = a.G + (size_t)z * C;
   const float GL = G[L - 1];
@@ -493,11 +526,11 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
     const int t = x.tid >> 2, q = x.tid & 3;
     float kdkb = 0.f, vdvb = 0.f, qdos = 0.f, kdkbar = 0.f, dbp = 0.f, dGp = 0.f;
     for (int cc = q; cc < DK; cc += 4) {
-      kdkb = fmaf(sK[t * LK + cc], dKb[t * DK + cc], kdkb);
-      qdos = fmaf(sQ[t * DK + cc], dOS[t * DK + cc], qdos);
-      kdkbar = fmaf(sK[t * LK + cc], dKbar[t * DK + cc], kdkbar);
+      kdkb = fmaf(tv(sK[t * LK + cc]), dKb[t * DK + cc], kdkb);
+      qdos = fmaf(tv(sQ[t * DK + cc]), dOS[t * DK + cc], qdos);
+      kdkbar = fmaf(tv(sK[t * LK + cc]), dKbar[t * DK + cc], kdkbar);
     }
-    for (int cc = q; cc < DV; cc += 4) vdvb = fmaf(sV[t * LV + cc], dVb[t * DV + cc], vdvb);
+    for (int cc = q; cc < DV; cc += 4) vdvb = fmaf(tv(sV[t * LV + cc]), dVb[t * DV + cc], vdvb);
     for (int s = q; s < C; s += 4) {
       const float kk = KK[t * C + s];
       if (s < t) {
@@ -531,11 +564,11 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
   for (int t = x.tid; t < C; t += x.nt) {
     float kdkb = 0.f, vdvb = 0.f, qdos = 0.f, kdkbar = 0.f;
     for (int cc = 0; cc < DK; ++cc) {
-      kdkb = fmaf(sK[t * LK + cc], dKb[t * DK + cc], kdkb);
-      qdos = fmaf(sQ[t * DK + cc], dOS[t * DK + cc], qdos);
-      kdkbar = fmaf(sK[t * LK + cc], dKbar[t * DK + cc], kdkbar);
+      kdkb = fmaf(tv(sK[t * LK + cc]), dKb[t * DK + cc], kdkb);
+      qdos = fmaf(tv(sQ[t * DK + cc]), dOS[t * DK + cc], qdos);
+      kdkbar = fmaf(tv(sK[t * LK + cc]), dKbar[t * DK + cc], kdkbar);
     }
-    for (int cc = 0; cc < DV; ++cc) vdvb = fmaf(sV[t * LV + cc], dVb[t * DV + cc], vdvb);
+    for (int cc = 0; cc < DV; ++cc) vdvb = fmaf(tv(sV[t * LV + cc]), dVb[t * DV + cc], vdvb);
     float db = sE[t] * kdkb + vdvb;
     float dG = sB[t] * sE[t] * kdkb + sE[t] * qdos - sEb[t] * kdkbar;
     for (int s = 0; s < C; ++s) {

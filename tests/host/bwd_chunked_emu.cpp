@@ -90,7 +90,7 @@ int run(const char* dir, int N, int H, int T, int has_h0, int has_dhT) {
          dA.data(), KK.data(), dKs.data(),
          dq.data(), dk.data(), dv.data(), dg.data(), dbeta.data(), dh0.data()};
   for (size_t z = 0; z < zc; ++z)
-    run_cta(NT, prep_smem<DK, DV>(), [&](HostX& x) { prep_body<DK, DV, BF>(x, a, (int)z); });
+    run_cta(NT, prep_smem<DK, DV, BF>(), [&](HostX& x) { prep_body<DK, DV, BF>(x, a, (int)z); });
   for (int n = 0; n < N; ++n)
     for (int h = 0; h < H; ++h)
       for (int rb = 0; rb < DV / RB; ++rb)
@@ -100,7 +100,7 @@ int run(const char* dir, int N, int H, int T, int has_h0, int has_dhT) {
       for (int rb = 0; rb < DV / RB; ++rb)
         run_cta(NT, rev_smem<DK, RB>(), [&](HostX& x) { rev_body<DK, DV, RB, BF>(x, a, rb, h, n); });
   for (size_t z = 0; z < zc; ++z)
-    run_cta(NT, grad_smem<DK, DV>(NT), [&](HostX& x) { grad_body<DK, DV, BF>(x, a, (int)z); });
+    run_cta(NT, grad_smem<DK, DV, BF>(NT), [&](HostX& x) { grad_body<DK, DV, BF>(x, a, (int)z); });
   writef(dir, "dq", dq); writef(dir, "dk", dk); writef(dir, "dv", dv);
   writef(dir, "dg", dg); writef(dir, "dbeta", dbeta); writef(dir, "dh0", dh0);
   return 0;
