@@ -70,6 +70,29 @@ GDN_HD inline float tv(unsigned short u) {
   memcpy(&f, &w, sizeof f);
   return f;
 }
+#ifdef __CUDA_ARCH__
+// Eight consecutive bf16 values at element i of p (16-byte aligned), times s,
+// into dst[0..7] (16-byte aligned); zeros without a read when !in.
+__device__ __forceinline__ void ld8_bf16_scaled(float* dst, const void* p, size_t i,
+                                                float s, bool in = true) {
+  if (!in) {
+    reinterpret_cast<float4*>(dst)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const unsigned short*>(p) + i);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  float f[8];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    f[2 * e] = __uint_as_float(w[e] << 16) * s;
+    f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u) * s;
+  }
+  reinterpret_cast<float4*>(dst)[0] = make_float4(f[0], f[1], f[2], f[3]);
+  reinterpret_cast<float4*>(dst)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+#endif
+
 template <bool BF>
 GDN_HD inline tile_t<BF> ldtile(const void* p, size_t i) {
   if constexpr (BF) return static_cast<const unsigned short*>(p)[i];
@@ -318,14 +341,33 @@ GDN_HD void fwd_body(X& x, const Args& a, int rb, int h, int n) {
     // e^{G_L - G_t} once per token, in sU until U overwrites it
     for (int t = x.tid; t < C; t += x.nt) sU[t] = t < L ? expf(GL - G[t]) : 0.f;
     x.sync();
-    for (int i = x.tid; i < C * DK; i += x.nt) {
-      const int t = i / DK, cc = i % DK;
-      sW[i] = a.W[(size_t)z * C * DK + i];
-      sKb[i] = t < L ? sU[t] * ldin<BF>(a.k, ((size_t)(t0 + t) * a.H + h) * DK + cc) : 0.f;
-    }
-    for (int i = x.tid; i < C * RB; i += x.nt) {
-      const int t = i / RB, j = i % RB;
-      sU0[i] = a.U0[(size_t)z * C * DV + t * DV + row0 + j];
+#ifdef __CUDA_ARCH__
+    if constexpr (BF) {
+      // 16-byte loads: W and U0 as float4, K eight bf16 at a time
+      const float4* W4 = reinterpret_cast<const float4*>(a.W + (size_t)z * C * DK);
+      for (int i = x.tid; i < C * DK / 4; i += x.nt) reinterpret_cast<float4*>(sW)[i] = W4[i];
+      for (int i = x.tid; i < C * DK / 8; i += x.nt) {
+        const int t = 8 * i / DK, cc = 8 * i % DK;
+        ld8_bf16_scaled(sKb + 8 * i, a.k, ((size_t)(t0 + t) * a.H + h) * DK + cc,
+                        sU[t], t < L);
+      }
+      for (int i = x.tid; i < C * RB / 4; i += x.nt) {
+        const int t = 4 * i / RB, j = 4 * i % RB;
+        reinterpret_cast<float4*>(sU0)[i] =
+            *reinterpret_cast<const float4*>(a.U0 + (size_t)z * C * DV + t * DV + row0 + j);
+      }
+    } else
+#endif
+    {
+      for (int i = x.tid; i < C * DK; i += x.nt) {
+        const int t = i / DK, cc = i % DK;
+        sW[i] = a.W[(size_t)z * C * DK + i];
+        sKb[i] = t < L ? sU[t] * ldin<BF>(a.k, ((size_t)(t0 + t) * a.H + h) * DK + cc) : 0.f;
+      }
+      for (int i = x.tid; i < C * RB; i += x.nt) {
+        const int t = i / RB, j = i % RB;
+        sU0[i] = a.U0[(size_t)z * C * DV + t * DV + row0 + j];
+      }
     }
     float* Sg = a.S + (size_t)z * DV * DK;
     for (int i = x.tid; i < RB * DK; i += x.nt)
@@ -382,18 +424,41 @@ GDN_HD void rev_body(X& x, const Args& a, int rb, int h, int n) {
       sdU[C + t] = t < L ? expf(G[t]) : 0.f;
     }
     x.sync();
-    for (int i = x.tid; i < C * C; i += x.nt) sP[i] = a.P[(size_t)z * C * C + i];
-    for (int i = x.tid; i < C * RB; i += x.nt) {
-      const int t = i / RB, j = i % RB;
-      sO[i] = t < L ? ldin<BF>(a.dout, ((size_t)(t0 + t) * a.H + h) * DV + row0 + j) : 0.f;
-    }
-    for (int i = x.tid; i < C * DK; i += x.nt) {
-      const int t = i / DK, cc = i % DK;
-      const bool in = t < L;
-      const size_t r = ((size_t)(t0 + t) * a.H + h) * DK + cc;
-      sKb[i] = in ? sdU[t] * ldin<BF>(a.k, r) : 0.f;
-      sQg[i] = in ? sdU[C + t] * ldin<BF>(a.q, r) : 0.f;
-      sW[i] = a.W[(size_t)z * C * DK + i];
+#ifdef __CUDA_ARCH__
+    if constexpr (BF) {
+      // 16-byte loads: P and W as float4, dO, K and Q eight bf16 at a time
+      const float4* P4 = reinterpret_cast<const float4*>(a.P + (size_t)z * C * C);
+      for (int i = x.tid; i < C * C / 4; i += x.nt) reinterpret_cast<float4*>(sP)[i] = P4[i];
+      for (int i = x.tid; i < C * RB / 8; i += x.nt) {
+        const int t = 8 * i / RB, j = 8 * i % RB;
+        ld8_bf16_scaled(sO + 8 * i, a.dout, ((size_t)(t0 + t) * a.H + h) * DV + row0 + j,
+                        1.f, t < L);
+      }
+      for (int i = x.tid; i < C * DK / 8; i += x.nt) {
+        const int t = 8 * i / DK, cc = 8 * i % DK;
+        const bool in = t < L;
+        const size_t r = ((size_t)(t0 + t) * a.H + h) * DK + cc;
+        ld8_bf16_scaled(sKb + 8 * i, a.k, r, sdU[t], in);
+        ld8_bf16_scaled(sQg + 8 * i, a.q, r, sdU[C + t], in);
+      }
+      const float4* W4 = reinterpret_cast<const float4*>(a.W + (size_t)z * C * DK);
+      for (int i = x.tid; i < C * DK / 4; i += x.nt) reinterpret_cast<float4*>(sW)[i] = W4[i];
+    } else
+#endif
+    {
+      for (int i = x.tid; i < C * C; i += x.nt) sP[i] = a.P[(size_t)z * C * C + i];
+      for (int i = x.tid; i < C * RB; i += x.nt) {
+        const int t = i / RB, j = i % RB;
+        sO[i] = t < L ? ldin<BF>(a.dout, ((size_t)(t0 + t) * a.H + h) * DV + row0 + j) : 0.f;
+      }
+      for (int i = x.tid; i < C * DK; i += x.nt) {
+        const int t = i / DK, cc = i % DK;
+        const bool in = t < L;
+        const size_t r = ((size_t)(t0 + t) * a.H + h) * DK + cc;
+        sKb[i] = in ? sdU[t] * ldin<BF>(a.k, r) : 0.f;
+        sQg[i] = in ? sdU[C + t] * ldin<BF>(a.q, r) : 0.f;
+        sW[i] = a.W[(size_t)z * C * DK + i];
+      }
     }
     float* dSg = a.dSx + (size_t)z * DV * DK;
     for (int i = x.tid; i < RB * DK; i += x.nt)
