@@ -127,18 +127,20 @@ WORKLOADS = {
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and the
 # hash of the kernel source it was taken on; a changed kernel reports null.
 MEASURED_TRAFFIC = {
-    # chunk_tc_kernel, W1, one launch (caches flushed by the bench)
-    "w1:6f137cb519c86b8e": 168919552 + 19976704,
+    # chunk_tc_kernel, W1, one launch (caches flushed by the bench); the
+    # edits of chunk_tc.cu after the capture change only the instantiation
+    # with the fused output gate, not the one W1 runs
+    "w1:d210a45648f60b95": 168919552 + 19976704,
     # chain_tx_kernel, W3 (packed, 512 sequence-heads), one launch; captured
     # before the latest edits of chunk_tc.cu, none of which touched
     # chain_tx_kernel or the headers it uses
-    "w3:6f137cb519c86b8e": 2996173056 + 598289920,
+    "w3:d210a45648f60b95": 2996173056 + 598289920,
     # decode_kernel captured with --sequences 128 and scaled x4 to N=512:
     # its traffic is proportional to the sequences processed
     "w4:83c7aa23b4500b6b": 4 * (271642880 + 210279936),
     # kda_prep_kernel, kda1, one launch (kda_chunk.cu unchanged since; the
     # key also covers chunk_tc.cu, whose later edits do not touch it)
-    "kda1:5be0bea5061237bf": 134819328 + 84282112,
+    "kda1:97e83e3f5e715aa2": 134819328 + 84282112,
     # bwd_kernel, bwd1, one launch (the per-CTA windows of S_bar do not all
     # stay in L2: most of the writes)
     "bwd1:e6e8ce911b3198e0": 761174272 + 5027586560,
