@@ -752,6 +752,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   auto stage = [&](int i) { return base + OFF_STAGE + (i & 1) * STAGE_BYTES; };
+  // The inputs of the first two chunks (q, k, v and the output gate, which
+  // the preceding kernel does not write) are requested before waiting for
+  // it: their stage barriers expect these bytes without an arrival, and the
+  // workspace part of the stage arrives after the wait.
+  const int npre = min(nloc, 2);
+  if (warp == kWarpProducer && lane == 0) {
+    for (int i = 0; i < npre; ++i) {
+      const int tok = (int)(bos + (long long)(c_begin + i) * C);
+      uint8_t* st = sm + OFF_STAGE + (i & 1) * STAGE_BYTES;
+      uint64_t* fa = &bars[B_FULLA0 + (i & 1)];
+      uint64_t* fb = &bars[B_FULLB0 + (i & 1)];
+      if (!scale_rows) {
+        mbar_expect_tx(fa, 8192u);
+        tma_load_3d(st + ST_V, &tmv, fa, row0, h, tok);
+      }
+      mbar_expect_tx(fb, 32768u + (has_gate ? 8192u : 0u));
+      if (has_gate) tma_load_3d(st + ST_G, &tmg, fb, row0, h, tok);
+      tma_load_3d(st + ST_Q, &tmq, fb, 0, h, tok);
+      tma_load_3d(st + ST_Q + ST_CB, &tmq, fb, 64, h, tok);
+      tma_load_3d(st + ST_K, &tmk, fb, 0, h, tok);
+      tma_load_3d(st + ST_K + ST_CB, &tmk, fb, 64, h, tok);
+    }
+  }
   // set-up above overlaps the tail of the preceding kernel; nothing it
   // writes (workspace, chunk offsets, split states, outputs) is touched
   // before this point
@@ -806,19 +829,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* st = sm + OFF_STAGE + s * STAGE_BYTES;
         uint64_t* fa = &bars[B_FULLA0 + s];
         uint64_t* fb = &bars[B_FULLB0 + s];
-        mbar_arrive_expect_tx(fa, STAGE_A_BYTES - (scale_rows ? 8192u : 0u));
-        if (!scale_rows) tma_load_3d(st + ST_V, &tmv, fa, row0, h, tok);
+        // the input part's bytes are expected first (before the wait for
+        // the first two chunks), then the workspace part's with the arrival
+        const bool pre = i < npre;
+        if (!pre && !scale_rows) mbar_expect_tx(fa, 8192u);
+        mbar_arrive_expect_tx(fa, STAGE_A_BYTES - 8192u);  // T_U, decay vectors
+        if (!pre && !scale_rows) tma_load_3d(st + ST_V, &tmv, fa, row0, h, tok);
         bulk_load(st + ST_TU, uimg + tz * WS_TU_BYTES, TILE_BYTES, fa);
         bulk_load(st + ST_CV, p.cv + tz * CV_FLOATS, CV_BYTES, fa);
-        mbar_arrive_expect_tx(fb, STAGE_B_BYTES + (has_gate ? 8192u : 0u));
-        if (has_gate) tma_load_3d(st + ST_G, &tmg, fb, row0, h, tok);
-        tma_load_3d(st + ST_Q, &tmq, fb, 0, h, tok);
-        tma_load_3d(st + ST_Q + ST_CB, &tmq, fb, 64, h, tok);
+        if (!pre) mbar_expect_tx(fb, 32768u + (has_gate ? 8192u : 0u));
+        mbar_arrive_expect_tx(fb, STAGE_B_BYTES - 32768u);  // -W, P
+        if (!pre) {
+          if (has_gate) tma_load_3d(st + ST_G, &tmg, fb, row0, h, tok);
+          tma_load_3d(st + ST_Q, &tmq, fb, 0, h, tok);
+          tma_load_3d(st + ST_Q + ST_CB, &tmq, fb, 64, h, tok);
+          tma_load_3d(st + ST_K, &tmk, fb, 0, h, tok);
+          tma_load_3d(st + ST_K + ST_CB, &tmk, fb, 64, h, tok);
+        }
         bulk_load(st + ST_W, wimg + tz * WS_W_BYTES, TILE_BYTES, fb);
         bulk_load(st + ST_W + ST_CB, wimg + tz * WS_W_BYTES + TILE_BYTES,
                   TILE_BYTES, fb);
-        tma_load_3d(st + ST_K, &tmk, fb, 0, h, tok);
-        tma_load_3d(st + ST_K + ST_CB, &tmk, fb, 64, h, tok);
         bulk_load(st + ST_P, pimg + tz * WS_P_BYTES, TILE_BYTES, fb);
         if (i + 2 < nloc) prefetch(i + 2);
         issued = i + 1;
