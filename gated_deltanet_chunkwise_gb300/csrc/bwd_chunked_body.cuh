@@ -93,6 +93,13 @@ __device__ __forceinline__ void ld8_bf16_scaled(float* dst, const void* p, size_
 }
 #endif
 
+// Row padding of the shared-memory tiles, in elements: the products' fragment
+// loads read 8 rows x 4 elements or 4 rows x 8 elements at a time, and a pad
+// of 16 bytes (bf16) or 4 floats puts those rows in distinct banks.
+template <bool BF>
+constexpr int kPad = BF ? 8 : 4;
+constexpr int kPadF = 4;  // fp32 state tiles
+
 template <bool BF>
 GDN_HD inline tile_t<BF> ldtile(const void* p, size_t i) {
   if constexpr (BF) return static_cast<const unsigned short*>(p)[i];
@@ -204,7 +211,8 @@ GDN_HD inline int chunk_len(const Args& a, int c) {
 // smem floats: K, Q [C][DK], V [C][DV], A [C][C], T [C][C], G, beta [C]
 template <int DK, int DV, bool BF>
 constexpr int prep_smem() {
-  return (C * (DK + 1) + C * DK + C * DV) * (int)sizeof(tile_t<BF>) / 4 + 2 * C * C + 2 * C;
+  return (2 * C * (DK + kPad<BF>) + C * (DV + kPad<BF>)) * (int)sizeof(tile_t<BF>) / 4 +
+         2 * C * C + 2 * C;
 }
 
 template <int DK, int DV, bool BF, class X>
@@ -212,12 +220,12 @@ GDN_HD void prep_body(X& x, const Args& a, int z) {
   const int h = z % a.H, nc = z / a.H, c = nc % a.nch, n = nc / a.nch;
   const int L = chunk_len(a, c);
   const long long t0 = (long long)n * a.T + (long long)c * C;
-  constexpr int LK = DK + 1;  // padded: K is read transposed
+  constexpr int LK = DK + kPad<BF>, LQ = DK + kPad<BF>, LV = DV + kPad<BF>;
   using TT = tile_t<BF>;
   TT* sK = reinterpret_cast<TT*>(x.smem);
   TT* sQ = sK + C * LK;
-  TT* sV = sQ + C * DK;
-  float* sA = reinterpret_cast<float*>(sV + C * DV);
+  TT* sV = sQ + C * LQ;
+  float* sA = reinterpret_cast<float*>(sV + C * LV);
   float* sT = sA + C * C;
   float* sG = sT + C * C;
   float* sB = sG + C;
@@ -226,11 +234,11 @@ GDN_HD void prep_body(X& x, const Args& a, int z) {
     const bool in = t < L;
     const size_t r = ((size_t)(t0 + t) * a.H + h) * DK + cc;
     sK[t * LK + cc] = in ? ldtile<BF>(a.k, r) : TT(0);
-    sQ[i] = in ? ldtile<BF>(a.q, r) : TT(0);
+    sQ[t * LQ + cc] = in ? ldtile<BF>(a.q, r) : TT(0);
   }
   for (int i = x.tid; i < C * DV; i += x.nt) {
     const int t = i / DV, cc = i % DV;
-    sV[i] = t < L ? ldtile<BF>(a.v, ((size_t)(t0 + t) * a.H + h) * DV + cc) : TT(0);
+    sV[t * LV + cc] = t < L ? ldtile<BF>(a.v, ((size_t)(t0 + t) * a.H + h) * DV + cc) : TT(0);
   }
   for (int t = x.tid; t < C; t += x.nt) {
     sB[t] = t < L ? a.beta[(size_t)(t0 + t) * a.H + h] : 0.f;
@@ -247,7 +255,7 @@ GDN_HD void prep_body(X& x, const Args& a, int z) {
   gemm(x, C, C, DK, sK, LK, 1, sK, 1, LK, [&](int r, int s, float kk) {
     sA[r * C + s] = r > s ? sB[r] * kk * expf(sG[r] - sG[s]) : 0.f;
   });
-  gemm(x, C, C, DK, sQ, DK, 1, sK, 1, LK, [&](int r, int s, float qk) {
+  gemm(x, C, C, DK, sQ, LQ, 1, sK, 1, LK, [&](int r, int s, float qk) {
     P[r * C + s] = r >= s ? qk * expf(sG[r] - sG[s]) : 0.f;
   });
   x.sync();
@@ -309,18 +317,18 @@ GDN_HD void prep_body(X& x, const Args& a, int z) {
   float* W = a.W + (size_t)z * C * DK;
   float* U0 = a.U0 + (size_t)z * C * DV;
   gemm(x, C, DK, C, sTW, C, 1, sK, LK, 1, [&](int t, int cc, float s) { W[t * DK + cc] = s; });
-  gemm(x, C, DV, C, sT, C, 1, sV, DV, 1, [&](int t, int cc, float s) { U0[t * DV + cc] = s; });
+  gemm(x, C, DV, C, sT, C, 1, sV, LV, 1, [&](int t, int cc, float s) { U0[t * DV + cc] = s; });
 }
 
 // ---- 2. forward chain: entry state S and U of every chunk ----------------
 // one CTA per (RB value rows, head, sequence); smem: W, Kbar [C][DK],
 // U0 [C][RB], S [RB][DK], U [C][RB], Snew [RB][DK]
 template <int DK, int RB>
-constexpr int fwd_smem() { return 2 * C * DK + 2 * C * RB + 2 * RB * (DK + 1); }
+constexpr int fwd_smem() { return 2 * C * DK + 2 * C * RB + 2 * RB * (DK + kPadF); }
 
 template <int DK, int DV, int RB, bool BF, class X>
 GDN_HD void fwd_body(X& x, const Args& a, int rb, int h, int n) {
-  constexpr int LS = DK + 1;  // padded: S is read transposed
+  constexpr int LS = DK + kPadF;  // padded rows (fragment loads)
   float* sW = x.smem;
   float* sKb = sW + C * DK;
   float* sU0 = sKb + C * DK;
@@ -394,11 +402,11 @@ GDN_HD void fwd_body(X& x, const Args& a, int rb, int h, int n) {
 // ---- 3. reverse chain: exit gradient dS' and dU of every chunk -----------
 // smem: P [C][C], dO [C][RB], Kbar, Qg, W [C][DK], dS, dSn [RB][DK], dU [C][RB]
 template <int DK, int RB>
-constexpr int rev_smem() { return C * C + 2 * C * RB + 3 * C * DK + 2 * RB * (DK + 1); }
+constexpr int rev_smem() { return C * C + 2 * C * RB + 3 * C * DK + 2 * RB * (DK + kPadF); }
 
 template <int DK, int DV, int RB, bool BF, class X>
 GDN_HD void rev_body(X& x, const Args& a, int rb, int h, int n) {
-  constexpr int LD = DK + 1;  // padded: dS is read transposed
+  constexpr int LD = DK + kPadF;  // padded rows (fragment loads)
   float* sP = x.smem;
   float* sO = sP + C * C;
   float* sKb = sO + C * RB;
@@ -500,7 +508,7 @@ GDN_HD void rev_body(X& x, const Args& a, int rb, int h, int n) {
 // smem: K, Q [C][DK], V, dO [C][DV], G, beta, E, ebar, dG [C], red [nt + 1]
 template <int DK, int DV, bool BF>
 constexpr int grad_smem(int nt) {
-  return (C * (DK + 1) + C * DK + C * (DV + 1) + C * DV) * (int)sizeof(tile_t<BF>) / 4 +
+  return (2 * C * (DK + kPad<BF>) + 2 * C * (DV + kPad<BF>)) * (int)sizeof(tile_t<BF>) / 4 +
          5 * C + nt + 1;
 }
 
@@ -509,13 +517,14 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
   const int h = z % a.H, nc = z / a.H, c = nc % a.nch, n = nc / a.nch;
   const int L = chunk_len(a, c);
   const long long t0 = (long long)n * a.T + (long long)c * C;
-  constexpr int LK = DK + 1, LV = DV + 1;  // padded: K and V are read transposed
+  constexpr int LK = DK + kPad<BF>, LQ = DK + kPad<BF>, LV = DV + kPad<BF>,
+                LO = DV + kPad<BF>;  // padded rows (fragment loads)
   using TT = tile_t<BF>;
   TT* sK = reinterpret_cast<TT*>(x.smem);
   TT* sQ = sK + C * LK;
-  TT* sV = sQ + C * DK;
+  TT* sV = sQ + C * LQ;
   TT* sO = sV + C * LV;
-  float* sG = reinterpret_cast<float*>(sO + C * DV);
+  float* sG = reinterpret_cast<float*>(sO + C * LO);
   float* sB = sG + C;
   float* sE = sB + C;
   float* sEb = sE + C;
@@ -526,14 +535,14 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
     const bool in = t < L;
     const size_t r = ((size_t)(t0 + t) * a.H + h) * DK + cc;
     sK[t * LK + cc] = in ? ldtile<BF>(a.k, r) : TT(0);
-    sQ[i] = in ? ldtile<BF>(a.q, r) : TT(0);
+    sQ[t * LQ + cc] = in ? ldtile<BF>(a.q, r) : TT(0);
   }
   for (int i = x.tid; i < C * DV; i += x.nt) {
     const int t = i / DV, cc = i % DV;
     const bool in = t < L;
     const size_t r = ((size_t)(t0 + t) * a.H + h) * DV + cc;
     sV[t * LV + cc] = in ? ldtile<BF>(a.v, r) : TT(0);
-    sO[i] = in ? ldtile<BF>(a.dout, r) : TT(0);
+    sO[t * LO + cc] = in ? ldtile<BF>(a.dout, r) : TT(0);
   }
   const float* G = a.G + (size_t)z * C;
   const float GL = G[L - 1];
@@ -556,10 +565,10 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
   float *dP = a.dP + zCC, *dT = a.dT + zCC, *Xm = a.X + zCC, *dA = a.dA + zCC;
   float* KK = a.KK + zCC;
   // contractions over the value rows; K K^T
-  gemm(x, C, DK, DV, sO, DV, 1, S, DK, 1, [&](int t, int cc, float s) { dOS[t * DK + cc] = s; });
+  gemm(x, C, DK, DV, sO, LO, 1, S, DK, 1, [&](int t, int cc, float s) { dOS[t * DK + cc] = s; });
   gemm(x, C, DK, DV, U, DV, 1, dSx, DK, 1, [&](int t, int cc, float s) { dKbar[t * DK + cc] = s; });
   gemm(x, C, DK, DV, dU, DV, 1, S, DK, 1, [&](int t, int cc, float s) { dW[t * DK + cc] = -s; });
-  gemm(x, C, C, DV, sO, DV, 1, U, 1, DV, [&](int t, int s, float d) { dP[t * C + s] = t >= s ? d : 0.f; });
+  gemm(x, C, C, DV, sO, LO, 1, U, 1, DV, [&](int t, int s, float d) { dP[t * C + s] = t >= s ? d : 0.f; });
   gemm(x, C, C, DK, sK, LK, 1, sK, 1, LK, [&](int r, int s, float d) { KK[r * C + s] = d; });
   float part = 0.f;  // sum(dS' (.) S)
   for (int i = x.tid; i < DV * DK; i += x.nt) part = fmaf(dSx[i], S[i], part);
@@ -592,7 +601,7 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
     float kdkb = 0.f, vdvb = 0.f, qdos = 0.f, kdkbar = 0.f, dbp = 0.f, dGp = 0.f;
     for (int cc = q; cc < DK; cc += 4) {
       kdkb = fmaf(tv(sK[t * LK + cc]), dKb[t * DK + cc], kdkb);
-      qdos = fmaf(tv(sQ[t * DK + cc]), dOS[t * DK + cc], qdos);
+      qdos = fmaf(tv(sQ[t * LQ + cc]), dOS[t * DK + cc], qdos);
       kdkbar = fmaf(tv(sK[t * LK + cc]), dKbar[t * DK + cc], kdkbar);
     }
     for (int cc = q; cc < DV; cc += 4) vdvb = fmaf(tv(sV[t * LV + cc]), dVb[t * DV + cc], vdvb);
@@ -630,7 +639,7 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
     float kdkb = 0.f, vdvb = 0.f, qdos = 0.f, kdkbar = 0.f;
     for (int cc = 0; cc < DK; ++cc) {
       kdkb = fmaf(tv(sK[t * LK + cc]), dKb[t * DK + cc], kdkb);
-      qdos = fmaf(tv(sQ[t * DK + cc]), dOS[t * DK + cc], qdos);
+      qdos = fmaf(tv(sQ[t * LQ + cc]), dOS[t * DK + cc], qdos);
       kdkbar = fmaf(tv(sK[t * LK + cc]), dKbar[t * DK + cc], kdkbar);
     }
     for (int cc = 0; cc < DV; ++cc) vdvb = fmaf(tv(sV[t * LV + cc]), dVb[t * DV + cc], vdvb);
@@ -676,7 +685,7 @@ GDN_HD void grad_body(X& x, const Args& a, int z) {
     if (t < L) a.dq[((size_t)(t0 + t) * a.H + h) * DK + cc] = fmaf(sE[t], dOS[t * DK + cc], s);
   });
   // dK = (dP (.) D)^T Q + B K + B^T K + diag(ebar) dKbar + diag(beta E) dKb
-  gemm(x, C, DK, C, Xm, 1, C, sQ, DK, 1, [&](int s, int cc, float v) { dKs[s * DK + cc] = v; });
+  gemm(x, C, DK, C, Xm, 1, C, sQ, LQ, 1, [&](int s, int cc, float v) { dKs[s * DK + cc] = v; });
   x.sync();
   gemm(x, C, DK, C, dT, C, 1, sK, LK, 1, [&](int s, int cc, float v) { dKs[s * DK + cc] += v; });
   x.sync();
