@@ -148,7 +148,7 @@ MEASURED_TRAFFIC = {
     # cbwd_grad_kernel, bwd1c (chunk-form backward), one launch (ncu reports
     # the bytes to 4 significant digits); captured before the shared-memory
     # rows were padded, which changes no global access
-    "bwd1c:84dad394db6bbb63": 1351398000 + 749125376,
+    "bwd1c:bbea4bbb6dbed5a7": 1351398000 + 749125376,
     # bwd_kernel, bwd1k (per-channel decay), one launch
     "bwd1k:e6e8ce911b3198e0": 917715968 + 5183326720,
     # bwd_kernel, bwd1f: its two launches of one step (the forward sweep,

@@ -324,17 +324,21 @@ GDN_HD void prep_body(X& x, const Args& a, int z) {
 // one CTA per (RB value rows, head, sequence); smem: W, Kbar [C][DK],
 // U0 [C][RB], S [RB][DK], U [C][RB], Snew [RB][DK]
 template <int DK, int RB>
-constexpr int fwd_smem() { return 2 * C * DK + 2 * C * RB + 2 * RB * (DK + kPadF); }
+constexpr int fwd_smem() {
+  return C * (DK + 4) + C * (DK + 8) + C * RB + 2 * RB * (DK + kPadF) + C * (RB + 8);
+}
 
 template <int DK, int DV, int RB, bool BF, class X>
 GDN_HD void fwd_body(X& x, const Args& a, int rb, int h, int n) {
-  constexpr int LS = DK + kPadF;  // padded rows (fragment loads)
+  // padded rows: a tile read as 8 rows x 4 elements by the products' fragment
+  // loads gets 4 floats, one read as 4 rows x 8 elements 8 floats
+  constexpr int LS = DK + kPadF, LW = DK + 4, LKb = DK + 8, LU = RB + 8;
   float* sW = x.smem;
-  float* sKb = sW + C * DK;
-  float* sU0 = sKb + C * DK;
+  float* sKb = sW + C * LW;
+  float* sU0 = sKb + C * LKb;
   float* sS = sU0 + C * RB;
   float* sU = sS + RB * LS;
-  float* sSn = sU + C * RB;
+  float* sSn = sU + C * LU;
   const int row0 = rb * RB;
   for (int i = x.tid; i < RB * DK; i += x.nt) {
     const int j = i / DK, cc = i % DK;
@@ -353,10 +357,11 @@ GDN_HD void fwd_body(X& x, const Args& a, int rb, int h, int n) {
     if constexpr (BF) {
       // 16-byte loads: W and U0 as float4, K eight bf16 at a time
       const float4* W4 = reinterpret_cast<const float4*>(a.W + (size_t)z * C * DK);
-      for (int i = x.tid; i < C * DK / 4; i += x.nt) reinterpret_cast<float4*>(sW)[i] = W4[i];
+      for (int i = x.tid; i < C * DK / 4; i += x.nt)
+        *reinterpret_cast<float4*>(sW + (4 * i / DK) * LW + 4 * i % DK) = W4[i];
       for (int i = x.tid; i < C * DK / 8; i += x.nt) {
         const int t = 8 * i / DK, cc = 8 * i % DK;
-        ld8_bf16_scaled(sKb + 8 * i, a.k, ((size_t)(t0 + t) * a.H + h) * DK + cc,
+        ld8_bf16_scaled(sKb + t * LKb + cc, a.k, ((size_t)(t0 + t) * a.H + h) * DK + cc,
                         sU[t], t < L);
       }
       for (int i = x.tid; i < C * RB / 4; i += x.nt) {
@@ -369,8 +374,9 @@ GDN_HD void fwd_body(X& x, const Args& a, int rb, int h, int n) {
     {
       for (int i = x.tid; i < C * DK; i += x.nt) {
         const int t = i / DK, cc = i % DK;
-        sW[i] = a.W[(size_t)z * C * DK + i];
-        sKb[i] = t < L ? sU[t] * ldin<BF>(a.k, ((size_t)(t0 + t) * a.H + h) * DK + cc) : 0.f;
+        sW[t * LW + cc] = a.W[(size_t)z * C * DK + i];
+        sKb[t * LKb + cc] =
+            t < L ? sU[t] * ldin<BF>(a.k, ((size_t)(t0 + t) * a.H + h) * DK + cc) : 0.f;
       }
       for (int i = x.tid; i < C * RB; i += x.nt) {
         const int t = i / RB, j = i % RB;
@@ -383,15 +389,15 @@ GDN_HD void fwd_body(X& x, const Args& a, int rb, int h, int n) {
     x.sync();
     // U = U0 - W S^T (C x RB)
     float* Ug = a.U + (size_t)z * C * DV;
-    gemm(x, C, RB, DK, sW, DK, 1, sS, 1, LS, [&](int t, int j, float ws) {
+    gemm(x, C, RB, DK, sW, LW, 1, sS, 1, LS, [&](int t, int j, float ws) {
       const float u = sU0[t * RB + j] - ws;
-      sU[t * RB + j] = u;
+      sU[t * LU + j] = u;
       Ug[t * DV + row0 + j] = u;
     });
     x.sync();
     // S <- gamma S + U^T Kbar (RB x DK)
     const float gam = expf(GL);
-    gemm(x, RB, DK, C, sU, 1, RB, sKb, DK, 1, [&](int j, int cc, float s) {
+    gemm(x, RB, DK, C, sU, 1, LU, sKb, LKb, 1, [&](int j, int cc, float s) {
       sSn[j * LS + cc] = fmaf(gam, sS[j * LS + cc], s);
     });
     x.sync();
@@ -402,17 +408,23 @@ GDN_HD void fwd_body(X& x, const Args& a, int rb, int h, int n) {
 // ---- 3. reverse chain: exit gradient dS' and dU of every chunk -----------
 // smem: P [C][C], dO [C][RB], Kbar, Qg, W [C][DK], dS, dSn [RB][DK], dU [C][RB]
 template <int DK, int RB>
-constexpr int rev_smem() { return C * C + 2 * C * RB + 3 * C * DK + 2 * RB * (DK + kPadF); }
+constexpr int rev_smem() {
+  return C * (C + 8) + C * (RB + 8) + C * (DK + 4) + 2 * C * (DK + 8) + 2 * RB * (DK + kPadF) +
+         C * (RB + 8);
+}
 
 template <int DK, int DV, int RB, bool BF, class X>
 GDN_HD void rev_body(X& x, const Args& a, int rb, int h, int n) {
-  constexpr int LD = DK + kPadF;  // padded rows (fragment loads)
+  // padded rows: a tile read as 8 rows x 4 elements by the products' fragment
+  // loads gets 4 floats, one read as 4 rows x 8 elements 8 floats
+  constexpr int LD = DK + kPadF, LP = C + 8, LO = RB + 8, LKb = DK + 4, LQg = DK + 8,
+                LW = DK + 8, LdU = RB + 8;
   float* sP = x.smem;
-  float* sO = sP + C * C;
-  float* sKb = sO + C * RB;
-  float* sQg = sKb + C * DK;
-  float* sW = sQg + C * DK;
-  float* sD = sW + C * DK;
+  float* sO = sP + C * LP;
+  float* sKb = sO + C * LO;
+  float* sQg = sKb + C * LKb;
+  float* sW = sQg + C * LQg;
+  float* sD = sW + C * LW;
   float* sDn = sD + RB * LD;
   float* sdU = sDn + RB * LD;
   const int row0 = rb * RB;
@@ -436,36 +448,39 @@ GDN_HD void rev_body(X& x, const Args& a, int rb, int h, int n) {
     if constexpr (BF) {
       // 16-byte loads: P and W as float4, dO, K and Q eight bf16 at a time
       const float4* P4 = reinterpret_cast<const float4*>(a.P + (size_t)z * C * C);
-      for (int i = x.tid; i < C * C / 4; i += x.nt) reinterpret_cast<float4*>(sP)[i] = P4[i];
+      for (int i = x.tid; i < C * C / 4; i += x.nt)
+        *reinterpret_cast<float4*>(sP + (4 * i / C) * LP + 4 * i % C) = P4[i];
       for (int i = x.tid; i < C * RB / 8; i += x.nt) {
         const int t = 8 * i / RB, j = 8 * i % RB;
-        ld8_bf16_scaled(sO + 8 * i, a.dout, ((size_t)(t0 + t) * a.H + h) * DV + row0 + j,
+        ld8_bf16_scaled(sO + t * LO + j, a.dout, ((size_t)(t0 + t) * a.H + h) * DV + row0 + j,
                         1.f, t < L);
       }
       for (int i = x.tid; i < C * DK / 8; i += x.nt) {
         const int t = 8 * i / DK, cc = 8 * i % DK;
         const bool in = t < L;
         const size_t r = ((size_t)(t0 + t) * a.H + h) * DK + cc;
-        ld8_bf16_scaled(sKb + 8 * i, a.k, r, sdU[t], in);
-        ld8_bf16_scaled(sQg + 8 * i, a.q, r, sdU[C + t], in);
+        ld8_bf16_scaled(sKb + t * LKb + cc, a.k, r, sdU[t], in);
+        ld8_bf16_scaled(sQg + t * LQg + cc, a.q, r, sdU[C + t], in);
       }
       const float4* W4 = reinterpret_cast<const float4*>(a.W + (size_t)z * C * DK);
-      for (int i = x.tid; i < C * DK / 4; i += x.nt) reinterpret_cast<float4*>(sW)[i] = W4[i];
+      for (int i = x.tid; i < C * DK / 4; i += x.nt)
+        *reinterpret_cast<float4*>(sW + (4 * i / DK) * LW + 4 * i % DK) = W4[i];
     } else
 #endif
     {
-      for (int i = x.tid; i < C * C; i += x.nt) sP[i] = a.P[(size_t)z * C * C + i];
+      for (int i = x.tid; i < C * C; i += x.nt) sP[(i / C) * LP + i % C] = a.P[(size_t)z * C * C + i];
       for (int i = x.tid; i < C * RB; i += x.nt) {
         const int t = i / RB, j = i % RB;
-        sO[i] = t < L ? ldin<BF>(a.dout, ((size_t)(t0 + t) * a.H + h) * DV + row0 + j) : 0.f;
+        sO[t * LO + j] =
+            t < L ? ldin<BF>(a.dout, ((size_t)(t0 + t) * a.H + h) * DV + row0 + j) : 0.f;
       }
       for (int i = x.tid; i < C * DK; i += x.nt) {
         const int t = i / DK, cc = i % DK;
         const bool in = t < L;
         const size_t r = ((size_t)(t0 + t) * a.H + h) * DK + cc;
-        sKb[i] = in ? sdU[t] * ldin<BF>(a.k, r) : 0.f;
-        sQg[i] = in ? sdU[C + t] * ldin<BF>(a.q, r) : 0.f;
-        sW[i] = a.W[(size_t)z * C * DK + i];
+        sKb[t * LKb + cc] = in ? sdU[t] * ldin<BF>(a.k, r) : 0.f;
+        sQg[t * LQg + cc] = in ? sdU[C + t] * ldin<BF>(a.q, r) : 0.f;
+        sW[t * LW + cc] = a.W[(size_t)z * C * DK + i];
       }
     }
     float* dSg = a.dSx + (size_t)z * DV * DK;
@@ -474,23 +489,23 @@ GDN_HD void rev_body(X& x, const Args& a, int rb, int h, int n) {
     x.sync();
     // dU = P^T dO + Kbar dS'^T (C x RB)
     float* dUg = a.dU + (size_t)z * C * DV;
-    gemm(x, C, RB, DK, sKb, DK, 1, sD, 1, LD, [&](int t, int j, float s) {
-      sdU[t * RB + j] = s;
+    gemm(x, C, RB, DK, sKb, LKb, 1, sD, 1, LD, [&](int t, int j, float s) {
+      sdU[t * LdU + j] = s;
     });
     x.sync();
-    gemm(x, C, RB, C, sP, 1, C, sO, RB, 1, [&](int t, int j, float s) {
-      const float u = sdU[t * RB + j] + s;
-      sdU[t * RB + j] = u;
+    gemm(x, C, RB, C, sP, 1, LP, sO, LO, 1, [&](int t, int j, float s) {
+      const float u = sdU[t * LdU + j] + s;
+      sdU[t * LdU + j] = u;
       dUg[t * DV + row0 + j] = u;
     });
     x.sync();
     // dS = gamma dS' + dO^T Qg - dU^T W (RB x DK)
     const float gam = expf(GL);
-    gemm(x, RB, DK, C, sO, 1, RB, sQg, DK, 1, [&](int j, int cc, float s) {
+    gemm(x, RB, DK, C, sO, 1, LO, sQg, LQg, 1, [&](int j, int cc, float s) {
       sDn[j * LD + cc] = fmaf(gam, sD[j * LD + cc], s);
     });
     x.sync();
-    gemm(x, RB, DK, C, sdU, 1, RB, sW, DK, 1, [&](int j, int cc, float s) {
+    gemm(x, RB, DK, C, sdU, 1, LdU, sW, LW, 1, [&](int j, int cc, float s) {
       sDn[j * LD + cc] -= s;
     });
     x.sync();
