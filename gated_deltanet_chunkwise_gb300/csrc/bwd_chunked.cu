@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(kCbThreads) cbwd_rev_kernel(const cbwd::Args a
 }
 
 template <int DK, int DV, bool BF>
-__global__ void __launch_bounds__(kCbThreads) cbwd_grad_kernel(const cbwd::Args a) {
+__global__ void __launch_bounds__(kCbThreads, 3) cbwd_grad_kernel(const cbwd::Args a) {
   extern __shared__ float4 sm4[];
   DevX x{(int)threadIdx.x, kCbThreads, reinterpret_cast<float*>(sm4)};
   cbwd::grad_body<DK, DV, BF>(x, a, (int)blockIdx.x);

@@ -93,6 +93,37 @@ __device__ __forceinline__ void ld8_bf16_scaled(float* dst, const void* p, size_
 }
 #endif
 
+#ifdef __CUDA_ARCH__
+// p[0], p[s], p[2s], p[3s] (four consecutive k) as fp32: one 16-byte (fp32)
+// or 8-byte (bf16) load when s == 1 and the address allows it.
+template <class T>
+__device__ __forceinline__ void ld4k(const T* p, int s, float (&v)[4]) {
+  if constexpr (std::is_same<T, unsigned short>::value) {
+    if (s == 1 && (reinterpret_cast<uintptr_t>(p) & 7u) == 0) {
+      const uint2 u = *reinterpret_cast<const uint2*>(p);
+      v[0] = __uint_as_float(u.x << 16);
+      v[1] = __uint_as_float(u.x & 0xffff0000u);
+      v[2] = __uint_as_float(u.y << 16);
+      v[3] = __uint_as_float(u.y & 0xffff0000u);
+      return;
+    }
+  } else {
+    if (s == 1 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+      const float4 f = *reinterpret_cast<const float4*>(p);
+      v[0] = f.x;
+      v[1] = f.y;
+      v[2] = f.z;
+      v[3] = f.w;
+      return;
+    }
+  }
+  v[0] = tv(p[0]);
+  v[1] = tv(p[s]);
+  v[2] = tv(p[2 * s]);
+  v[3] = tv(p[3 * s]);
+}
+#endif
+
 // Row padding of the shared-memory tiles, in elements: the products' fragment
 // loads read 8 rows x 4 elements or 4 rows x 8 elements at a time, and a pad
 // of 16 bytes (bf16) or 4 floats puts those rows in distinct banks.
@@ -151,6 +182,43 @@ GDN_HD void gemm(X& x, int M, int N, int K, const TA* A, int ars, int acs,
       float acc[4][4];
       for (int q = 0; q < 4; ++q)
         for (int e = 0; e < 4; ++e) acc[q][e] = 0.f;
+      if (K % 16 == 0) {
+        // Sixteen k per step, two products: thread t takes k0 + 4t .. k0 +
+        // 4t + 3, the first product 4t and 4t + 1 (fragment columns / rows
+        // t and t + 4), the second 4t + 2 and 4t + 3. A and B take the same
+        // k in the same slot, so the sums are those of the plain order, and
+        // an operand contiguous in k is read with one vector load per row.
+#pragma unroll 1
+        for (int k0 = 0; k0 < K; k0 += 16) {
+          float ar0[4], ar1[4];
+          ld4k(A + (m0 + g) * ars + (k0 + 4 * t) * acs, acs, ar0);
+          ld4k(A + (m0 + g + 8) * ars + (k0 + 4 * t) * acs, acs, ar1);
+          uint32_t ah1[4], al1[4], ah2[4], al2[4];
+          tf32_split(ar0[0], ah1[0], al1[0]);
+          tf32_split(ar1[0], ah1[1], al1[1]);
+          tf32_split(ar0[1], ah1[2], al1[2]);
+          tf32_split(ar1[1], ah1[3], al1[3]);
+          tf32_split(ar0[2], ah2[0], al2[0]);
+          tf32_split(ar1[2], ah2[1], al2[1]);
+          tf32_split(ar0[3], ah2[2], al2[2]);
+          tf32_split(ar1[3], ah2[3], al2[3]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int n = n0 + 8 * q + g;
+            float br[4];
+            ld4k(B + (k0 + 4 * t) * brs + n * bcs, brs, br);
+            uint32_t bh[4], bl[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) tf32_split(br[e], bh[e], bl[e]);
+            if (!a_exact) mma_tf32(acc[q], al1, bh[0], bh[1]);
+            if (!b_exact) mma_tf32(acc[q], ah1, bl[0], bl[1]);
+            mma_tf32(acc[q], ah1, bh[0], bh[1]);
+            if (!a_exact) mma_tf32(acc[q], al2, bh[2], bh[3]);
+            if (!b_exact) mma_tf32(acc[q], ah2, bl[2], bl[3]);
+            mma_tf32(acc[q], ah2, bh[2], bh[3]);
+          }
+        }
+      } else
 #pragma unroll 4
       for (int k0 = 0; k0 < K; k0 += 8) {
         uint32_t ah[4], al[4];
