@@ -32,14 +32,15 @@
 // 2-3 also U rows, 0-1 output rows; each takes 32 of the 64 columns), then
 // the TMA producer, the P U warp and the U0 / [Q;-W] S^T / Delta warp.
 // Only warps 4k and 4k + 1 reach TMEM lanes 0-63 (the output rows), so the
-// U-row warps take the elementwise work of the fused output gate (the
-// logits of the next chunk turned into sigmoids in shared memory) to keep
-// the output-row warps within a chunk's period. The MMA warp is woken by
-// barriers: the state in shared memory for [Q;-W] S^T, diag(e^{G_L-G}) U
-// for the Delta product. Operand tiles
-// are bf16 with the 128-byte swizzle and arrive in a two-stage ring, each
-// stage in two parts; whole output tiles leave by TMA store. Every wait is
-// bounded; a CTA that gives up records GDN_ERR_TIMEOUT, drains its MMAs,
+// U-row warps take the elementwise work of the fused output gate (each
+// chunk's gate logits turned into sigmoids in shared memory while the U rows
+// wait for the Delta product) to keep the output-row warps within a chunk's
+// period. The MMA warp is woken by barriers: the state in shared memory for
+// [Q;-W] S^T, diag(e^{G_L-G}) U for the Delta product. Operand tiles are
+// bf16 with the 128-byte swizzle and arrive in a two-stage ring, each stage
+// in two parts (the first two chunks' q, k, v requested before the wait for
+// the preparation kernel); whole output tiles leave by TMA store. Every wait
+// is bounded; a CTA that gives up records GDN_ERR_TIMEOUT, drains its MMAs,
 // frees its TMEM and exits.
 #include <cudaTypedefs.h>
 
