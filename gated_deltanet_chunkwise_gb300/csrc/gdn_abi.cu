@@ -151,7 +151,7 @@ long long parts_cost_tc(int requested, int N, int H, int T, int dk, int dv,
 // single-launch form (`*fused`, one sub-sequence). The automatic choice
 // keeps the two-kernel form: measured on GB300, the single launch moves
 // far fewer DRAM bytes (the hand-off stays in L2) but is not faster (W1
-// 0.095 vs 0.091 ms, the packed workload 1.41 vs 1.05 ms).
+// 0.095 vs 0.086 ms, the packed workload 1.41 vs 1.08 ms).
 void choose_chain_tc(int path, int requested, int N, int H, int T, int dk,
                      int dv, int C, bool packed, int* rows, int* parts,
                      bool* fused) {
