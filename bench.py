@@ -130,16 +130,23 @@ WORKLOADS = {
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and the
 # hash of the kernel source it was taken on; a changed kernel reports null.
 MEASURED_TRAFFIC = {
-    # chunk_tc_kernel, W1, one launch (caches flushed by the bench)
-    "w1:978ba12454337261": 168910080 + 19627264,
-    # chain_tx_kernel, W3 (packed, 512 sequence-heads), one launch
-    "w3:978ba12454337261": 2982083584 + 598519296,
+    # chunk_tc_kernel, W1, one launch captured with the L2 as the
+    # preparation kernel leaves it (ncu --cache-control none), as in a bench
+    # step: reads 150.4 MB (part of the workspace, written with an
+    # evict-last hint, comes from L2), writes 70.8 MB, of which about 51 MB
+    # is the preparation's workspace written back from L2 meanwhile (with
+    # the caches flushed first: 168.9 + 19.6 MB)
+    "w1:fb29c6dd3a75ea27": 150369536 + 70773504,
+    # chain_tx_kernel, W3 (packed, 512 sequence-heads), one launch; the
+    # later edit of chunk_tc.cu (the preparation's evict-last hint) is off
+    # for this workload's 1.1 GB workspace and leaves chain_tx_kernel as it was
+    "w3:fb29c6dd3a75ea27": 2982083584 + 598519296,
     # decode_kernel captured with --sequences 128 and scaled x4 to N=512:
     # its traffic is proportional to the sequences processed
     "w4:83c7aa23b4500b6b": 4 * (271642880 + 210279936),
     # kda_prep_kernel, kda1, one launch (kda_chunk.cu unchanged since; the
     # key also covers chunk_tc.cu, whose later edits do not touch it)
-    "kda1:7cf69db86f1e1c67": 134819328 + 84282112,
+    "kda1:82cb1c560f09c62a": 134819328 + 84282112,
     # bwd_kernel, bwd1, one launch (the per-CTA windows of S_bar do not all
     # stay in L2: most of the writes)
     "bwd1:e6e8ce911b3198e0": 761174272 + 5027586560,

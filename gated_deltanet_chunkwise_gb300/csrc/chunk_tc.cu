@@ -180,6 +180,8 @@ enum {
 constexpr uint32_t PR_OFF_MISC = PR_OFF_BAR + PB_N * 8;
 constexpr uint32_t PR_SMEM_BYTES = PR_OFF_MISC + 16 + 1024;
 constexpr uint32_t PR_TMEM_COLS = 128;
+// Largest workspace (-W, P, T_U images) written with an evict-last L2 hint.
+constexpr long long kKeepWsBytes = 96ll << 20;
 constexpr uint32_t ID_PREP = idesc_bf16(128, 64, false, false);
 constexpr uint32_t ID_PREP_W = idesc_bf16(128, 128, false, true);
 static_assert(64 * AP * 4 >= 16384, "[T_W; T_W] must fit the solve buffer");
@@ -189,7 +191,7 @@ template <int VARIANT>
 __global__ void __launch_bounds__(kPrepThreads, kPrepCtas)
     ut_prep_kernel(const ChunkParams p, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmq, int nch_dense,
-                   int total_chunks_bound) {
+                   int total_chunks_bound, int keep_ws) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -490,10 +492,18 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtas)
       }
       named_bar(1, 128);
       if (tid == 0) {
-        bulk_store(static_cast<uint8_t*>(p.pm) + tile * WS_P_BYTES, st + 8192,
-                   TILE_BYTES);
-        bulk_store(static_cast<uint8_t*>(p.tu) + tile * WS_TU_BYTES, st + 24576,
-                   TILE_BYTES);
+        if (keep_ws) {
+          const uint64_t pol = l2_policy_evict_last();
+          bulk_store_hint(static_cast<uint8_t*>(p.pm) + tile * WS_P_BYTES,
+                          st + 8192, TILE_BYTES, pol);
+          bulk_store_hint(static_cast<uint8_t*>(p.tu) + tile * WS_TU_BYTES,
+                          st + 24576, TILE_BYTES, pol);
+        } else {
+          bulk_store(static_cast<uint8_t*>(p.pm) + tile * WS_P_BYTES, st + 8192,
+                     TILE_BYTES);
+          bulk_store(static_cast<uint8_t*>(p.tu) + tile * WS_TU_BYTES,
+                     st + 24576, TILE_BYTES);
+        }
         bulk_commit();
         // [T_W; T_W] K: both halves of the accumulator hold W
         tc_fence_after();
@@ -530,8 +540,12 @@ __global__ void __launch_bounds__(kPrepThreads, kPrepCtas)
       tc_fence_before();
       named_bar(1, 128);  // vec and TMEM free again; -W complete
       if (tid == 0) {
-        bulk_store(static_cast<uint8_t*>(p.wneg) + tile * WS_W_BYTES,
-                   sm + PR_OFF_AT, WS_W_BYTES);
+        if (keep_ws)
+          bulk_store_hint(static_cast<uint8_t*>(p.wneg) + tile * WS_W_BYTES,
+                          sm + PR_OFF_AT, WS_W_BYTES, l2_policy_evict_last());
+        else
+          bulk_store(static_cast<uint8_t*>(p.wneg) + tile * WS_W_BYTES,
+                     sm + PR_OFF_AT, WS_W_BYTES);
         bulk_commit();
       }
     }
@@ -2859,13 +2873,19 @@ cudaError_t launch_ut_prep(const ChunkParams& p, cudaStream_t stream,
   const long long items = bound * p.H;
   const int grid = (int)std::min<long long>(items, (long long)kPrepCtas * sm_count());
   const int nchd = chunk_tc_nch_dense(p);
+  // A workspace that fits the L2 well is written with an evict-last hint,
+  // so that the chain kernel right behind finds its first chunks' -W, P and
+  // T_U there rather than in HBM (on a larger one the hint would only push
+  // out lines still to be read).
+  const int keep_ws =
+      items * (long long)(WS_W_BYTES + WS_P_BYTES + WS_TU_BYTES) <= kKeepWsBytes;
   auto launch = [&](auto kern) {
     cudaError_t e = cudaFuncSetAttribute(
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PR_SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int t = timing_start(GDN_KERNEL_CHUNK_PREP, stream);
     kern<<<grid, kPrepThreads, PR_SMEM_BYTES, stream>>>(p, mk, mq, nchd,
-                                                         (int)bound);
+                                                         (int)bound, keep_ws);
     e = cudaGetLastError();
     timing_stop(t, stream, e);
     return e;

@@ -300,6 +300,20 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src,
       "r"(smem_u32(src)), "r"(bytes)
       : "memory");
 }
+// The same, with an L2 cache policy for the written lines.
+__device__ __forceinline__ void bulk_store_hint(void* dst, const void* src,
+                                                uint32_t bytes, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+      "r"(smem_u32(src)), "r"(bytes), "l"(policy)
+      : "memory");
+}
+// An L2 policy under which the lines it tags are evicted after untagged ones.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
+  return policy;
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
